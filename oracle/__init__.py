@@ -1,0 +1,249 @@
+"""CPU oracle for the paged decode path -- TEST INFRASTRUCTURE ONLY.
+
+A plain, slow, single-threaded C implementation (``oracle.c``) of what the
+path computes, loaded with ctypes. It is the checker the CUDA library is
+compared against and shares no code with it. Only the test suite,
+``__graft_entry__.smoke()`` and the benchmark's CPU-baseline leg (and its
+``--impl reference`` arm) may import this package; the product path never does.
+
+Every function takes and returns host numpy arrays; bf16 data is carried as
+``uint16`` bit patterns. Attention outputs are float64.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+from typing import Optional
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_BUILD_DIR = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD_DIR, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+CFLAGS = ["-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math", "-fPIC", "-shared"]
+
+
+def build(force: bool = False) -> str:
+    """Compile oracle.c into oracle/_build/liboracle.so (gcc, no FMA contraction)."""
+    os.makedirs(_BUILD_DIR, exist_ok=True)
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".{os.getpid()}.tmp"
+    subprocess.check_call(["gcc", *CFLAGS, _SRC, "-o", tmp, "-lm"])
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _p(a: Optional[np.ndarray]):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def lib():
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = build()
+            L = ctypes.CDLL(path)
+            vp, i32, i64, f64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_double
+            L.oracle_reshape_and_cache.argtypes = [vp, vp, vp, vp, vp, i64, i32, i32, i32, i64]
+            L.oracle_reshape_and_cache.restype = i64
+            L.oracle_quest_update_meta.argtypes = [vp, vp, vp, vp, i64, i32, i32, i32, i64]
+            L.oracle_quest_update_meta.restype = i64
+            L.oracle_quest_rebuild_meta.argtypes = [vp, vp, vp, vp, i32, vp, i32, i32, i32, i32, i64]
+            L.oracle_quest_rebuild_meta.restype = i32
+            att = [vp, vp, vp, vp, vp, i32, vp, i32, i32, i32, i32, i32, i64, f64]
+            L.oracle_paged_attention.argtypes = att + [vp, i64]
+            L.oracle_paged_attention.restype = i32
+            L.oracle_paged_attention_online.argtypes = att + [i64]
+            L.oracle_paged_attention_online.restype = i32
+            L.oracle_paged_attention_split.argtypes = att + [i32]
+            L.oracle_paged_attention_split.restype = i32
+            L.oracle_sparse_attention.argtypes = [vp, vp, vp, vp, vp, i32, vp, vp, i32,
+                                                  i32, i32, i32, i32, i32, i64, f64, vp, i64]
+            L.oracle_sparse_attention.restype = i32
+            L.oracle_quest_scores.argtypes = [vp, vp, vp, vp, vp, i32, vp, i32, i32, i32, i32, i32, i64]
+            L.oracle_quest_scores.restype = i32
+            L.oracle_quest_topk.argtypes = [vp, vp, i32, vp, i32, i32, i32, i32]
+            L.oracle_quest_topk.restype = i32
+            _lib = L
+    return _lib
+
+
+def _c(a, dtype):
+    a = np.ascontiguousarray(a, dtype=dtype)
+    return a
+
+
+def _check(rc: int, what: str):
+    if rc == -1:
+        raise ValueError(f"oracle {what}: block table entry outside the pool")
+    if rc == -2:
+        raise ValueError(f"oracle {what}: invalid sizes")
+    if rc != 0:
+        raise RuntimeError(f"oracle {what}: status {rc}")
+
+
+# ----------------------------------------------------------------- cache
+
+
+def reshape_and_cache(key, value, key_cache, value_cache, slot_mapping) -> int:
+    """Scatter new K/V rows into the caches IN PLACE; returns #out-of-pool slots."""
+    assert key_cache.dtype == np.uint16 and key_cache.flags.c_contiguous
+    assert value_cache.dtype == np.uint16 and value_cache.flags.c_contiguous
+    NB, BS, Hkv, D = key_cache.shape
+    key = _c(key, np.uint16)
+    value = _c(value, np.uint16)
+    slots = _c(slot_mapping, np.int64)
+    return int(lib().oracle_reshape_and_cache(_p(key), _p(value), _p(key_cache), _p(value_cache),
+                                              _p(slots), slots.shape[0], Hkv, D, BS, NB))
+
+
+def quest_update_meta(kmin, kmax, key, slot_mapping, BS: int) -> int:
+    """Incremental Quest metadata update IN PLACE; returns #out-of-pool slots."""
+    assert kmin.dtype == np.uint16 and kmin.flags.c_contiguous
+    assert kmax.dtype == np.uint16 and kmax.flags.c_contiguous
+    NB, Hkv, D = kmin.shape
+    key = _c(key, np.uint16)
+    slots = _c(slot_mapping, np.int64)
+    return int(lib().oracle_quest_update_meta(_p(kmin), _p(kmax), _p(key), _p(slots),
+                                              slots.shape[0], Hkv, D, BS, NB))
+
+
+def quest_rebuild_meta(key_cache, block_tables, context_lens, kmin=None, kmax=None):
+    """Metadata of every block a sequence uses, from the cache. Returns (kmin, kmax).
+
+    Blocks no sequence uses keep the values passed in (zeros by default)."""
+    NB, BS, Hkv, D = key_cache.shape
+    if kmin is None:
+        kmin = np.zeros((NB, Hkv, D), dtype=np.uint16)
+    if kmax is None:
+        kmax = np.zeros((NB, Hkv, D), dtype=np.uint16)
+    kc = _c(key_cache, np.uint16)
+    bt = _c(block_tables, np.int32)
+    ctx = _c(context_lens, np.int32)
+    rc = lib().oracle_quest_rebuild_meta(_p(kmin), _p(kmax), _p(kc), _p(bt), bt.shape[1], _p(ctx),
+                                         bt.shape[0], Hkv, D, BS, NB)
+    _check(rc, "quest_rebuild_meta")
+    return kmin, kmax
+
+
+# ------------------------------------------------------------- attention
+
+
+def _att_args(q, key_cache, value_cache, block_tables, context_lens):
+    q = _c(q, np.uint16)
+    kc = _c(key_cache, np.uint16)
+    vc = _c(value_cache, np.uint16)
+    bt = _c(block_tables, np.int32)
+    ctx = _c(context_lens, np.int32)
+    B, Hq, D = q.shape
+    NB, BS, Hkv, D2 = kc.shape
+    assert D == D2 and vc.shape == kc.shape and bt.shape[0] == B and ctx.shape == (B,)
+    return q, kc, vc, bt, ctx, B, Hq, Hkv, D, BS, NB
+
+
+def _rows_arg(rows):
+    if rows is None:
+        return None, 0
+    r = np.ascontiguousarray(np.asarray(rows, dtype=np.int32).reshape(-1, 2))
+    return r, r.shape[0]
+
+
+def paged_attention(q, key_cache, value_cache, block_tables, context_lens, scale, rows=None):
+    """Dense GQA paged decode attention, two-pass softmax in fp64.
+
+    Returns [B, Hq, D] float64, or [len(rows), D] for the listed (b, h) pairs."""
+    q, kc, vc, bt, ctx, B, Hq, Hkv, D, BS, NB = _att_args(q, key_cache, value_cache,
+                                                          block_tables, context_lens)
+    r, nr = _rows_arg(rows)
+    out = np.zeros((nr, D) if r is not None else (B, Hq, D), dtype=np.float64)
+    rc = lib().oracle_paged_attention(_p(out), _p(q), _p(kc), _p(vc), _p(bt), bt.shape[1], _p(ctx),
+                                      B, Hq, Hkv, D, BS, NB, float(scale), _p(r), nr)
+    _check(rc, "paged_attention")
+    return out
+
+
+def paged_attention_online(q, key_cache, value_cache, block_tables, context_lens, scale, chunk):
+    """Dense attention via the online-softmax recurrence (``chunk`` tokens per update)."""
+    q, kc, vc, bt, ctx, B, Hq, Hkv, D, BS, NB = _att_args(q, key_cache, value_cache,
+                                                          block_tables, context_lens)
+    out = np.zeros((B, Hq, D), dtype=np.float64)
+    rc = lib().oracle_paged_attention_online(_p(out), _p(q), _p(kc), _p(vc), _p(bt), bt.shape[1],
+                                             _p(ctx), B, Hq, Hkv, D, BS, NB, float(scale), int(chunk))
+    _check(rc, "paged_attention_online")
+    return out
+
+
+def paged_attention_split(q, key_cache, value_cache, block_tables, context_lens, scale, num_splits):
+    """Dense attention via split-KV partials and their log-sum-exp combine."""
+    q, kc, vc, bt, ctx, B, Hq, Hkv, D, BS, NB = _att_args(q, key_cache, value_cache,
+                                                          block_tables, context_lens)
+    out = np.zeros((B, Hq, D), dtype=np.float64)
+    rc = lib().oracle_paged_attention_split(_p(out), _p(q), _p(kc), _p(vc), _p(bt), bt.shape[1],
+                                            _p(ctx), B, Hq, Hkv, D, BS, NB, float(scale),
+                                            int(num_splits))
+    _check(rc, "paged_attention_split")
+    return out
+
+
+def sparse_attention(q, key_cache, value_cache, block_tables, context_lens, selected, scale,
+                     rows=None):
+    """Quest sparse attention over the selected logical blocks (fp64)."""
+    q, kc, vc, bt, ctx, B, Hq, Hkv, D, BS, NB = _att_args(q, key_cache, value_cache,
+                                                          block_tables, context_lens)
+    sel = _c(selected, np.int32)
+    assert sel.shape[:2] == (B, Hkv)
+    topk = sel.shape[2]
+    r, nr = _rows_arg(rows)
+    out = np.zeros((nr, D) if r is not None else (B, Hq, D), dtype=np.float64)
+    rc = lib().oracle_sparse_attention(_p(out), _p(q), _p(kc), _p(vc), _p(bt), bt.shape[1], _p(ctx),
+                                       _p(sel), topk, B, Hq, Hkv, D, BS, NB, float(scale),
+                                       _p(r), nr)
+    _check(rc, "sparse_attention")
+    return out
+
+
+# ----------------------------------------------------------------- Quest
+
+
+def quest_scores(q, kmin, kmax, block_tables, context_lens, BS: int):
+    """Quest block scores [B, Hkv, MBS] float32 (-inf past each sequence's blocks)."""
+    q = _c(q, np.uint16)
+    kmin = _c(kmin, np.uint16)
+    kmax = _c(kmax, np.uint16)
+    bt = _c(block_tables, np.int32)
+    ctx = _c(context_lens, np.int32)
+    B, Hq, D = q.shape
+    NB, Hkv, D2 = kmin.shape
+    assert D == D2
+    MBS = bt.shape[1]
+    out = np.empty((B, Hkv, MBS), dtype=np.float32)
+    rc = lib().oracle_quest_scores(_p(out), _p(q), _p(kmin), _p(kmax), _p(bt), MBS, _p(ctx),
+                                   B, Hq, Hkv, D, BS, NB)
+    _check(rc, "quest_scores")
+    return out
+
+
+def quest_topk(scores, context_lens, BS: int, topk: int):
+    """Top-K logical blocks per (b, kvh): [B, Hkv, topk] int32, ascending, -1 padded."""
+    s = _c(scores, np.float32)
+    ctx = _c(context_lens, np.int32)
+    B, Hkv, MBS = s.shape
+    out = np.empty((B, Hkv, topk), dtype=np.int32)
+    rc = lib().oracle_quest_topk(_p(out), _p(s), MBS, _p(ctx), B, Hkv, BS, int(topk))
+    _check(rc, "quest_topk")
+    return out
+
+
+def quest_select(q, kmin, kmax, block_tables, context_lens, BS: int, topk: int):
+    """Scores then top-K: the selection the Quest path attends over."""
+    return quest_topk(quest_scores(q, kmin, kmax, block_tables, context_lens, BS),
+                      context_lens, BS, topk)

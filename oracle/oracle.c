@@ -1,0 +1,654 @@
+/*
+ * oracle.c -- plain, slow, single-threaded CPU reference for the paged decode
+ * path: ReshapeAndCache, GQA paged decode attention, Quest metadata, Quest
+ * block scoring and top-K selection, Quest sparse attention.
+ *
+ * TEST INFRASTRUCTURE ONLY. This file is the checker the CUDA kernels are
+ * compared against. It shares no code, header, table or helper with the CUDA
+ * library. Only the test suite, the smoke check and the benchmark's CPU
+ * baseline may build, load or call it; the product path never does.
+ *
+ * Sources (web pages, by title and section):
+ *   [P1] "Ascend Kernel-to-Serving Pipeline": sections "ReshapeAndCache",
+ *        "GQA Paged Attention", "Quest Sparse Attention", "Sparse precision".
+ *   [P2] "18 e2e inference serving" (TileLang tutorial): section 2.6 (paged KV
+ *        layout and block table), section 4.1 (split-KV partial outputs and
+ *        their weighted combine).
+ *   Quest scoring rule (not printed on the pages; fixed by the project's
+ *   statement of the method): per physical block and KV head, elementwise
+ *   min/max of K; block score = sum over the GQA group of
+ *   sum_d max(q_d*min_d, q_d*max_d); top-K blocks, ties to the lower index.
+ *
+ * Conventions:
+ *   bf16 values are passed as uint16 bit patterns.
+ *   Cache layout [NB][BS][Hkv][D] per layer ([P2] 2.6).
+ *   block_tables [B][MBS] int32, context_lens [B] int32, slot_mapping [T] int64.
+ *   Query head h uses KV head h / G, G = Hq / Hkv (contiguous groups; [P1]
+ *   "GQA Paged Attention" says only that several query heads share one KV head).
+ *   Attention arithmetic is fp64 (at least the fp32 the method asks for).
+ *
+ * Build: gcc -O2 -std=c11 -ffp-contract=off -fPIC -shared oracle.c -lm
+ * (no fused multiply-add contraction: the Quest score below is defined as a
+ * sequence of individually rounded fp32 operations).
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+/* ---------------------------------------------------------------- helpers */
+
+static double bf16_val(uint16_t h)
+{
+    uint32_t u = (uint32_t)h << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+static float bf16_f32(uint16_t h)
+{
+    uint32_t u = (uint32_t)h << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return f;
+}
+
+/* IEEE-754 totalOrder key of a bf16 bit pattern: numeric order for non-NaN
+ * values, with -0 ranked below +0 (so min/max are unique bit patterns). */
+static uint16_t bf16_order_key(uint16_t h)
+{
+    return (h & 0x8000u) ? (uint16_t)(~h & 0xFFFFu) : (uint16_t)(h | 0x8000u);
+}
+
+/* totalOrder key of an fp32 value (same idea, 32 bits). */
+static uint32_t f32_order_key(float f)
+{
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+/* ------------------------------------------------------ ReshapeAndCache */
+
+/* [P1] "ReshapeAndCache": for every new token t with slot = slot_mapping[t]:
+ *   block_idx = slot // block_size, block_offset = slot % block_size,
+ *   and the token's K and V rows (all KV heads) go to that block and offset;
+ *   slot < 0 means the token is skipped.
+ * Tokens are applied in order. A slot past the pool (block_idx >= NB) is not
+ * written; the return value counts such slots. */
+int64_t oracle_reshape_and_cache(const uint16_t *key, const uint16_t *value,
+                                 uint16_t *key_cache, uint16_t *value_cache,
+                                 const int64_t *slot_mapping, int64_t T,
+                                 int Hkv, int D, int BS, int64_t NB)
+{
+    const int64_t row = (int64_t)Hkv * D;
+    int64_t out_of_range = 0;
+    for (int64_t t = 0; t < T; ++t) {
+        const int64_t slot = slot_mapping[t];
+        if (slot < 0)
+            continue;
+        const int64_t block_idx = slot / BS;
+        const int64_t block_offset = slot % BS;
+        if (block_idx >= NB) {
+            ++out_of_range;
+            continue;
+        }
+        const int64_t dst = (block_idx * BS + block_offset) * row;
+        for (int64_t e = 0; e < row; ++e) {
+            key_cache[dst + e] = key[t * row + e];
+            value_cache[dst + e] = value[t * row + e];
+        }
+    }
+    return out_of_range;
+}
+
+/* ---------------------------------------------------- Quest metadata */
+
+/* Incremental metadata update for the tokens of one ReshapeAndCache call.
+ * Metadata is per physical block p and KV head h: kmin[p][h][d], kmax[p][h][d]
+ * = elementwise min / max of K over the block's tokens.
+ * For each physical block touched by a valid slot in this call:
+ *   - if some token of the call lands at offset 0 of the block (the block
+ *     starts fresh), the new metadata is the min/max over this call's tokens
+ *     in that block only;
+ *   - otherwise it is min/max of the old metadata and this call's tokens.
+ * min/max follow IEEE totalOrder (so -0 < +0) and the result does not depend
+ * on token order. Returns the number of out-of-pool slots ignored. */
+int64_t oracle_quest_update_meta(uint16_t *kmin, uint16_t *kmax,
+                                 const uint16_t *key, const int64_t *slot_mapping,
+                                 int64_t T, int Hkv, int D, int BS, int64_t NB)
+{
+    const int64_t row = (int64_t)Hkv * D;
+    int64_t out_of_range = 0;
+    unsigned char *done = (unsigned char *)calloc((size_t)T, 1);
+    uint16_t *lo = (uint16_t *)malloc((size_t)row * sizeof(uint16_t));
+    uint16_t *hi = (uint16_t *)malloc((size_t)row * sizeof(uint16_t));
+    for (int64_t t = 0; t < T; ++t) {
+        const int64_t s = slot_mapping[t];
+        if (s < 0 || done[t])
+            continue;
+        const int64_t p = s / BS;
+        if (p >= NB) {
+            ++out_of_range;
+            done[t] = 1;
+            continue;
+        }
+        /* every token of this call that lands in block p */
+        int reset = 0;
+        for (int64_t u = t; u < T; ++u) {
+            const int64_t su = slot_mapping[u];
+            if (su >= 0 && su / BS == p && su % BS == 0)
+                reset = 1;
+        }
+        int have = 0;
+        if (!reset) {
+            memcpy(lo, kmin + p * row, (size_t)row * sizeof(uint16_t));
+            memcpy(hi, kmax + p * row, (size_t)row * sizeof(uint16_t));
+            have = 1;
+        }
+        for (int64_t u = t; u < T; ++u) {
+            const int64_t su = slot_mapping[u];
+            if (su < 0 || su / BS != p)
+                continue;
+            done[u] = 1;
+            const uint16_t *k = key + u * row;
+            for (int64_t e = 0; e < row; ++e) {
+                if (!have) {
+                    lo[e] = k[e];
+                    hi[e] = k[e];
+                } else {
+                    if (bf16_order_key(k[e]) < bf16_order_key(lo[e]))
+                        lo[e] = k[e];
+                    if (bf16_order_key(k[e]) > bf16_order_key(hi[e]))
+                        hi[e] = k[e];
+                }
+            }
+            have = 1;
+        }
+        memcpy(kmin + p * row, lo, (size_t)row * sizeof(uint16_t));
+        memcpy(kmax + p * row, hi, (size_t)row * sizeof(uint16_t));
+    }
+    free(done);
+    free(lo);
+    free(hi);
+    return out_of_range;
+}
+
+/* Metadata from scratch: for each sequence b and logical block j < ceil(ctx/BS),
+ * p = block_tables[b][j], min/max over the block's valid tokens
+ * (positions j*BS .. min(ctx, (j+1)*BS) - 1). Returns -1 on a table entry
+ * outside the pool, else 0. */
+int oracle_quest_rebuild_meta(uint16_t *kmin, uint16_t *kmax,
+                              const uint16_t *key_cache,
+                              const int32_t *block_tables, int MBS,
+                              const int32_t *context_lens, int B,
+                              int Hkv, int D, int BS, int64_t NB)
+{
+    const int64_t row = (int64_t)Hkv * D;
+    for (int b = 0; b < B; ++b) {
+        const int64_t ctx = context_lens[b] > 0 ? context_lens[b] : 0;
+        const int64_t nblk = (ctx + BS - 1) / BS;
+        for (int64_t j = 0; j < nblk && j < MBS; ++j) {
+            const int64_t p = block_tables[(int64_t)b * MBS + j];
+            if (p < 0 || p >= NB)
+                return -1;
+            const int64_t t_end = (j + 1) * BS < ctx ? (j + 1) * BS : ctx;
+            for (int64_t e = 0; e < row; ++e) {
+                uint16_t lo = 0, hi = 0;
+                for (int64_t t = j * BS; t < t_end; ++t) {
+                    const uint16_t v = key_cache[(p * BS + (t % BS)) * row + e];
+                    if (t == j * BS || bf16_order_key(v) < bf16_order_key(lo))
+                        lo = v;
+                    if (t == j * BS || bf16_order_key(v) > bf16_order_key(hi))
+                        hi = v;
+                }
+                kmin[p * row + e] = lo;
+                kmax[p * row + e] = hi;
+            }
+        }
+    }
+    return 0;
+}
+
+/* ------------------------------------------------------------ attention */
+
+/* The tokens one (sequence, KV head) attends to, in order.
+ * Dense ([P1] "GQA Paged Attention"): positions 0 .. ctx-1.
+ * Sparse ([P1] "Quest Sparse Attention"): for each selected logical block j
+ * (in the order given, negative entries skipped), the positions
+ * j*BS .. min(ctx, (j+1)*BS) - 1; blocks and tokens past ctx are skipped.
+ * Writes positions into pos[] and returns their count. */
+static int64_t token_list(int64_t *pos, int64_t ctx, int BS,
+                          const int32_t *sel_row, int topk)
+{
+    int64_t n = 0;
+    if (ctx < 0)
+        ctx = 0;
+    if (!sel_row) {
+        for (int64_t t = 0; t < ctx; ++t)
+            pos[n++] = t;
+        return n;
+    }
+    for (int i = 0; i < topk; ++i) {
+        const int64_t j = sel_row[i];
+        if (j < 0)
+            continue;
+        for (int64_t t = j * BS; t < (j + 1) * BS && t < ctx; ++t)
+            pos[n++] = t;
+    }
+    return n;
+}
+
+/* Address of K (or V) of sequence position t for one KV head through the
+ * block table ([P2] 2.6: K_cache[physical_block][block_size][kv_head][head_dim],
+ * block_table[seq][logical_block] = physical_block). NULL if the table entry
+ * is outside the pool. */
+static const uint16_t *kv_row(const uint16_t *cache, const int32_t *bt_row,
+                              int64_t t, int kvh, int Hkv, int D, int BS, int64_t NB)
+{
+    const int64_t p = bt_row[t / BS];
+    if (p < 0 || p >= NB)
+        return NULL;
+    return cache + ((p * BS + t % BS) * Hkv + kvh) * (int64_t)D;
+}
+
+/* scores s_i = scale * q . K[pos_i] for every listed position (fp64). */
+static int compute_scores(double *s, const uint16_t *qrow, const uint16_t *key_cache,
+                          const int32_t *bt_row, const int64_t *pos, int64_t n,
+                          int kvh, int Hkv, int D, int BS, int64_t NB, double scale)
+{
+    for (int64_t i = 0; i < n; ++i) {
+        const uint16_t *k = kv_row(key_cache, bt_row, pos[i], kvh, Hkv, D, BS, NB);
+        if (!k)
+            return -1;
+        double dot = 0.0;
+        for (int d = 0; d < D; ++d)
+            dot += bf16_val(qrow[d]) * bf16_val(k[d]);
+        s[i] = scale * dot;
+    }
+    return 0;
+}
+
+/* Reference form: explicit two-pass softmax over the listed tokens,
+ *   m = max_i s_i, p_i = exp(s_i - m), l = sum p_i, out = sum p_i V_i / l.
+ * An empty token list gives a zero output. */
+static int attend_two_pass(double *out, const uint16_t *qrow,
+                           const uint16_t *key_cache, const uint16_t *value_cache,
+                           const int32_t *bt_row, const int64_t *pos, int64_t n,
+                           int kvh, int Hkv, int D, int BS, int64_t NB,
+                           double scale, double *s)
+{
+    for (int d = 0; d < D; ++d)
+        out[d] = 0.0;
+    if (n == 0)
+        return 0;
+    if (compute_scores(s, qrow, key_cache, bt_row, pos, n, kvh, Hkv, D, BS, NB, scale))
+        return -1;
+    double m = -INFINITY;
+    for (int64_t i = 0; i < n; ++i)
+        if (s[i] > m)
+            m = s[i];
+    double l = 0.0;
+    for (int64_t i = 0; i < n; ++i) {
+        const double p = exp(s[i] - m);
+        l += p;
+        const uint16_t *v = kv_row(value_cache, bt_row, pos[i], kvh, Hkv, D, BS, NB);
+        for (int d = 0; d < D; ++d)
+            out[d] += p * bf16_val(v[d]);
+    }
+    for (int d = 0; d < D; ++d)
+        out[d] /= l;
+    return 0;
+}
+
+/* Online softmax ([P1] "GQA Paged Attention"): one pass over the tokens in
+ * chunks of `chunk`, keeping a running max m, normaliser l and accumulator acc;
+ * when a chunk raises the max, the old l and acc are rescaled by
+ * exp(m_old - m_new). The full score vector is not needed by the method (the
+ * scores buffer here is only a convenience). */
+static int attend_online(double *out, const uint16_t *qrow,
+                         const uint16_t *key_cache, const uint16_t *value_cache,
+                         const int32_t *bt_row, const int64_t *pos, int64_t n,
+                         int kvh, int Hkv, int D, int BS, int64_t NB,
+                         double scale, int64_t chunk, double *s, double *acc)
+{
+    for (int d = 0; d < D; ++d) {
+        out[d] = 0.0;
+        acc[d] = 0.0;
+    }
+    if (n == 0)
+        return 0;
+    if (compute_scores(s, qrow, key_cache, bt_row, pos, n, kvh, Hkv, D, BS, NB, scale))
+        return -1;
+    double m = -INFINITY, l = 0.0;
+    for (int64_t c0 = 0; c0 < n; c0 += chunk) {
+        const int64_t c1 = c0 + chunk < n ? c0 + chunk : n;
+        double m_chunk = -INFINITY;
+        for (int64_t i = c0; i < c1; ++i)
+            if (s[i] > m_chunk)
+                m_chunk = s[i];
+        const double m_new = m_chunk > m ? m_chunk : m;
+        const double alpha = exp(m - m_new);  /* exp(-inf) = 0 on the first chunk */
+        l *= alpha;
+        for (int d = 0; d < D; ++d)
+            acc[d] *= alpha;
+        for (int64_t i = c0; i < c1; ++i) {
+            const double p = exp(s[i] - m_new);
+            l += p;
+            const uint16_t *v = kv_row(value_cache, bt_row, pos[i], kvh, Hkv, D, BS, NB);
+            for (int d = 0; d < D; ++d)
+                acc[d] += p * bf16_val(v[d]);
+        }
+        m = m_new;
+    }
+    for (int d = 0; d < D; ++d)
+        out[d] = acc[d] / l;
+    return 0;
+}
+
+/* Split-KV ([P2] 4.1): the token list is cut into num_splits ranges with the
+ * proportional boundaries n*s/num_splits; each range writes its normalised
+ * output O_s and its log-sum-exp lse_s = m_s + log(l_s); the combine weights
+ * each O_s by l_s relative to a common max:
+ *   m* = max_s lse_s, w_s = exp(lse_s - m*), out = sum_s w_s O_s / sum_s w_s.
+ * (The page prints out = sum l_s O_s / sum l_s, which is this formula when all
+ * ranges share one max; rebasing to m* makes it hold for any maxima.) Empty
+ * ranges carry no weight. */
+static int attend_split(double *out, const uint16_t *qrow,
+                        const uint16_t *key_cache, const uint16_t *value_cache,
+                        const int32_t *bt_row, const int64_t *pos, int64_t n,
+                        int kvh, int Hkv, int D, int BS, int64_t NB,
+                        double scale, int num_splits, double *s, double *part)
+{
+    for (int d = 0; d < D; ++d)
+        out[d] = 0.0;
+    if (n == 0)
+        return 0;
+    double *lse = (double *)malloc(sizeof(double) * (size_t)num_splits);
+    for (int sp = 0; sp < num_splits; ++sp) {
+        const int64_t a = n * sp / num_splits, b = n * (sp + 1) / num_splits;
+        lse[sp] = -INFINITY;
+        if (b <= a)
+            continue;
+        if (attend_two_pass(part + (int64_t)sp * D, qrow, key_cache, value_cache, bt_row,
+                            pos + a, b - a, kvh, Hkv, D, BS, NB, scale, s)) {
+            free(lse);
+            return -1;
+        }
+        double m = -INFINITY, l = 0.0;
+        for (int64_t i = 0; i < b - a; ++i)
+            if (s[i] > m)
+                m = s[i];
+        for (int64_t i = 0; i < b - a; ++i)
+            l += exp(s[i] - m);
+        lse[sp] = m + log(l);
+    }
+    double mstar = -INFINITY;
+    for (int sp = 0; sp < num_splits; ++sp)
+        if (lse[sp] > mstar)
+            mstar = lse[sp];
+    double wsum = 0.0;
+    for (int sp = 0; sp < num_splits; ++sp) {
+        if (lse[sp] == -INFINITY)
+            continue;
+        const double w = exp(lse[sp] - mstar);
+        wsum += w;
+        for (int d = 0; d < D; ++d)
+            out[d] += w * part[(int64_t)sp * D + d];
+    }
+    for (int d = 0; d < D; ++d)
+        out[d] /= wsum;
+    free(lse);
+    return 0;
+}
+
+/* mode: 0 = two-pass, 1 = online (chunk = param), 2 = split (num_splits = param) */
+static int attention_rows(double *out, const uint16_t *q,
+                          const uint16_t *key_cache, const uint16_t *value_cache,
+                          const int32_t *block_tables, int MBS,
+                          const int32_t *context_lens, const int32_t *selected, int topk,
+                          int B, int Hq, int Hkv, int D, int BS, int64_t NB, double scale,
+                          const int32_t *rows, int64_t nrows, int mode, int64_t param)
+{
+    if (B <= 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || D <= 0 || BS <= 0)
+        return -2;
+    const int G = Hq / Hkv;
+    int64_t max_tokens = (int64_t)MBS * BS;
+    int64_t *pos = (int64_t *)malloc(sizeof(int64_t) * (size_t)(max_tokens + 1));
+    double *s = (double *)malloc(sizeof(double) * (size_t)(max_tokens + 1));
+    double *acc = (double *)malloc(sizeof(double) * (size_t)D * (size_t)(mode == 2 ? param + 1 : 1));
+    int rc = 0;
+    const int64_t total = rows ? nrows : (int64_t)B * Hq;
+    for (int64_t r = 0; r < total && rc == 0; ++r) {
+        const int64_t b = rows ? rows[2 * r] : r / Hq;
+        const int64_t h = rows ? rows[2 * r + 1] : r % Hq;
+        const int kvh = (int)(h / G);
+        int64_t ctx = context_lens[b];
+        if (ctx > max_tokens)
+            ctx = max_tokens;
+        const int32_t *sel_row = selected ? selected + (b * Hkv + kvh) * (int64_t)topk : NULL;
+        const int64_t n = token_list(pos, ctx, BS, sel_row, topk);
+        const uint16_t *qrow = q + (b * Hq + h) * (int64_t)D;
+        const int32_t *bt_row = block_tables + b * (int64_t)MBS;
+        double *o = out + r * (int64_t)D;
+        if (mode == 0)
+            rc = attend_two_pass(o, qrow, key_cache, value_cache, bt_row, pos, n, kvh,
+                                 Hkv, D, BS, NB, scale, s);
+        else if (mode == 1)
+            rc = attend_online(o, qrow, key_cache, value_cache, bt_row, pos, n, kvh,
+                               Hkv, D, BS, NB, scale, param, s, acc);
+        else
+            rc = attend_split(o, qrow, key_cache, value_cache, bt_row, pos, n, kvh,
+                              Hkv, D, BS, NB, scale, (int)param, s, acc);
+    }
+    free(pos);
+    free(s);
+    free(acc);
+    return rc;
+}
+
+/* Dense GQA paged decode attention ([P1] "GQA Paged Attention"): one query
+ * token per sequence; out [B][Hq][D] (fp64), or only the (b, h) pairs listed
+ * in rows[2*nrows] (out then [nrows][D]) when rows is not NULL.
+ * Returns 0, -1 on a table entry outside the pool, -2 on bad sizes. */
+int oracle_paged_attention(double *out, const uint16_t *q,
+                           const uint16_t *key_cache, const uint16_t *value_cache,
+                           const int32_t *block_tables, int MBS,
+                           const int32_t *context_lens, int B, int Hq, int Hkv,
+                           int D, int BS, int64_t NB, double scale,
+                           const int32_t *rows, int64_t nrows)
+{
+    return attention_rows(out, q, key_cache, value_cache, block_tables, MBS, context_lens,
+                          NULL, 0, B, Hq, Hkv, D, BS, NB, scale, rows, nrows, 0, 0);
+}
+
+/* Same attention through the online-softmax recurrence, tokens taken `chunk`
+ * at a time. */
+int oracle_paged_attention_online(double *out, const uint16_t *q,
+                                  const uint16_t *key_cache, const uint16_t *value_cache,
+                                  const int32_t *block_tables, int MBS,
+                                  const int32_t *context_lens, int B, int Hq, int Hkv,
+                                  int D, int BS, int64_t NB, double scale, int64_t chunk)
+{
+    if (chunk <= 0)
+        return -2;
+    return attention_rows(out, q, key_cache, value_cache, block_tables, MBS, context_lens,
+                          NULL, 0, B, Hq, Hkv, D, BS, NB, scale, NULL, 0, 1, chunk);
+}
+
+/* Same attention through split-KV partials and their combine. */
+int oracle_paged_attention_split(double *out, const uint16_t *q,
+                                 const uint16_t *key_cache, const uint16_t *value_cache,
+                                 const int32_t *block_tables, int MBS,
+                                 const int32_t *context_lens, int B, int Hq, int Hkv,
+                                 int D, int BS, int64_t NB, double scale, int num_splits)
+{
+    if (num_splits <= 0)
+        return -2;
+    return attention_rows(out, q, key_cache, value_cache, block_tables, MBS, context_lens,
+                          NULL, 0, B, Hq, Hkv, D, BS, NB, scale, NULL, 0, 2, num_splits);
+}
+
+/* Quest sparse paged attention ([P1] "Quest Sparse Attention", "Sparse
+ * precision"): exact attention over only the tokens of the selected logical
+ * blocks, selected[B][Hkv][topk] (shared by the GQA group of each KV head,
+ * negative entries are padding), tokens past ctx skipped. */
+int oracle_sparse_attention(double *out, const uint16_t *q,
+                            const uint16_t *key_cache, const uint16_t *value_cache,
+                            const int32_t *block_tables, int MBS,
+                            const int32_t *context_lens, const int32_t *selected, int topk,
+                            int B, int Hq, int Hkv, int D, int BS, int64_t NB, double scale,
+                            const int32_t *rows, int64_t nrows)
+{
+    if (topk <= 0)
+        return -2;
+    return attention_rows(out, q, key_cache, value_cache, block_tables, MBS, context_lens,
+                          selected, topk, B, Hq, Hkv, D, BS, NB, scale, rows, nrows, 0, 0);
+}
+
+/* ------------------------------------------------------------ Quest score */
+
+/* Quest block score, evaluated in fp32 in one fixed order that the GPU
+ * kernel reproduces bit for bit (the score decides an integer, the top-K
+ * set, so both sides take that decision in the same precision and order).
+ *
+ * Definition: score(b, kvh, j) = sum_{h in group(kvh)} sum_d
+ *                                max(q[b,h,d]*min_d, q[b,h,d]*max_d)
+ * with min/max the metadata of physical block p = block_tables[b][j].
+ * Since max >= min, max(q*min, q*max) = q+ * max + q- * min with
+ * q+ = max(q, 0) and q- = min(q, 0); summing over the group first:
+ *     score = sum_d ( P_d * max_d + N_d * min_d ),
+ *     P_d = sum_h q+[h,d],  N_d = sum_h q-[h,d].
+ * fp32 evaluation order:
+ *   1. P_d, N_d: start at +0, add h = 0, 1, ..., G-1 in turn;
+ *   2. t_d = fl(fl(P_d * max_d) + fl(N_d * min_d));
+ *   3. D is cut into 32 equal chunks of C = D/32 consecutive d; chunk sum
+ *      c_l = (((t_{lC} + t_{lC+1}) + ...) + t_{lC+C-1}), left to right;
+ *   4. the 32 chunk sums are combined pairwise: for off = 16, 8, 4, 2, 1:
+ *      c_l <- c_l + c_{l xor off}; the score is c_0.
+ * Logical blocks j >= ceil(ctx/BS) are excluded (score -inf). A table entry
+ * outside the pool also scores -inf.
+ * scores: [B][Hkv][MBS] fp32. Requires D % 32 == 0. */
+int oracle_quest_scores(float *scores, const uint16_t *q,
+                        const uint16_t *kmin, const uint16_t *kmax,
+                        const int32_t *block_tables, int MBS,
+                        const int32_t *context_lens, int B, int Hq, int Hkv,
+                        int D, int BS, int64_t NB)
+{
+    if (Hq % Hkv != 0 || D % 32 != 0)
+        return -2;
+    const int G = Hq / Hkv, C = D / 32;
+    float *P = (float *)malloc(sizeof(float) * (size_t)D);
+    float *N = (float *)malloc(sizeof(float) * (size_t)D);
+    float c[32];
+    for (int b = 0; b < B; ++b) {
+        const int64_t ctx = context_lens[b] > 0 ? context_lens[b] : 0;
+        const int64_t nblk = (ctx + BS - 1) / BS;
+        for (int kvh = 0; kvh < Hkv; ++kvh) {
+            for (int d = 0; d < D; ++d) {
+                float pp = 0.0f, nn = 0.0f;
+                for (int g = 0; g < G; ++g) {
+                    const float v = bf16_f32(q[((int64_t)b * Hq + (int64_t)kvh * G + g) * D + d]);
+                    pp = pp + (v > 0.0f ? v : 0.0f);
+                    nn = nn + (v < 0.0f ? v : 0.0f);
+                }
+                P[d] = pp;
+                N[d] = nn;
+            }
+            float *srow = scores + ((int64_t)b * Hkv + kvh) * MBS;
+            for (int64_t j = 0; j < MBS; ++j) {
+                if (j >= nblk) {
+                    srow[j] = -INFINITY;
+                    continue;
+                }
+                const int64_t p = block_tables[(int64_t)b * MBS + j];
+                if (p < 0 || p >= NB) {
+                    srow[j] = -INFINITY;
+                    continue;
+                }
+                const uint16_t *mn = kmin + (p * Hkv + kvh) * (int64_t)D;
+                const uint16_t *mx = kmax + (p * Hkv + kvh) * (int64_t)D;
+                for (int l = 0; l < 32; ++l) {
+                    float acc = 0.0f;
+                    for (int i = 0; i < C; ++i) {
+                        const int d = l * C + i;
+                        const float a = P[d] * bf16_f32(mx[d]);
+                        const float bb = N[d] * bf16_f32(mn[d]);
+                        const float t = a + bb;
+                        acc = (i == 0) ? t : acc + t;
+                    }
+                    c[l] = acc;
+                }
+                for (int off = 16; off >= 1; off >>= 1) {
+                    float nc[32];
+                    for (int l = 0; l < 32; ++l)
+                        nc[l] = c[l] + c[l ^ off];
+                    memcpy(c, nc, sizeof c);
+                }
+                srow[j] = c[0];
+            }
+        }
+    }
+    free(P);
+    free(N);
+    return 0;
+}
+
+/* ------------------------------------------------------------ Quest top-K */
+
+typedef struct {
+    uint32_t key;
+    int32_t j;
+} ranked_block;
+
+static int rank_cmp(const void *a, const void *b)
+{
+    const ranked_block *x = (const ranked_block *)a, *y = (const ranked_block *)b;
+    if (x->key != y->key)
+        return x->key > y->key ? -1 : 1; /* higher score first */
+    return x->j < y->j ? -1 : (x->j > y->j); /* tie: lower block index first */
+}
+
+static int index_cmp(const void *a, const void *b)
+{
+    const int32_t x = *(const int32_t *)a, y = *(const int32_t *)b;
+    return x < y ? -1 : (x > y);
+}
+
+/* Top-K per (sequence, KV head) ([P1] "Quest Sparse Attention": pick the
+ * top-K logical blocks; ties go to the lower block index). Candidates are the
+ * logical blocks j < ceil(ctx/BS); they are fully sorted by (score desc,
+ * j asc) with scores ranked by IEEE totalOrder; the first min(topk, nblk) are
+ * returned in ascending block order and the row is padded with -1.
+ * selected: [B][Hkv][topk] int32. */
+int oracle_quest_topk(int32_t *selected, const float *scores, int MBS,
+                      const int32_t *context_lens, int B, int Hkv, int BS, int topk)
+{
+    if (topk <= 0)
+        return -2;
+    ranked_block *items = (ranked_block *)malloc(sizeof(ranked_block) * (size_t)(MBS + 1));
+    for (int b = 0; b < B; ++b) {
+        const int64_t ctx = context_lens[b] > 0 ? context_lens[b] : 0;
+        int64_t nblk = (ctx + BS - 1) / BS;
+        if (nblk > MBS)
+            nblk = MBS;
+        for (int kvh = 0; kvh < Hkv; ++kvh) {
+            const float *srow = scores + ((int64_t)b * Hkv + kvh) * MBS;
+            for (int64_t j = 0; j < nblk; ++j) {
+                items[j].key = f32_order_key(srow[j]);
+                items[j].j = (int32_t)j;
+            }
+            qsort(items, (size_t)nblk, sizeof(ranked_block), rank_cmp);
+            const int64_t k = nblk < topk ? nblk : topk;
+            int32_t *out = selected + ((int64_t)b * Hkv + kvh) * topk;
+            for (int64_t i = 0; i < k; ++i)
+                out[i] = items[i].j;
+            qsort(out, (size_t)k, sizeof(int32_t), index_cmp);
+            for (int64_t i = k; i < topk; ++i)
+                out[i] = -1;
+        }
+    }
+    free(items);
+    return 0;
+}

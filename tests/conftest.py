@@ -1,0 +1,24 @@
+"""Shared test configuration.
+
+Tests marked ``gpu`` call the CUDA library's kernels and need a GPU; the rest
+(oracle pins, host logic, library loading) run on any machine.
+"""
+import os
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+
+def pytest_configure(config):
+    config.addinivalue_line("markers", "gpu: needs a CUDA GPU (runs the CUDA library's kernels)")
+
+
+@pytest.fixture(scope="session")
+def oracle_lib():
+    import oracle
+    oracle.build()
+    return oracle
