@@ -1,0 +1,202 @@
+/*
+ * paged_decode.h -- C ABI of the GB300 (sm_103a) paged GQA decode library:
+ * ReshapeAndCache, dense GQA paged decode attention with split-KV, and Quest
+ * sparse paged attention (per-block min/max key metadata, block scoring,
+ * top-K selection, attention over the selected blocks).
+ *
+ * Sources (web pages, by title and section):
+ *   [P1] "Ascend Kernel-to-Serving Pipeline": sections "ReshapeAndCache",
+ *        "GQA Paged Attention", "Quest Sparse Attention", "Sparse precision".
+ *   [P2] "18 e2e inference serving" (TileLang tutorial): 2.4 (decode
+ *        attention is memory-bound), 2.6 (paged KV layout, block table),
+ *        4.1 (split-KV partial outputs combined with l_s weights), 6.1 (run on
+ *        the framework's current stream).
+ *   The Quest scoring rule (per-block elementwise min/max of K; score =
+ *   sum over the GQA group of sum_d max(q_d*min_d, q_d*max_d); top-K with ties
+ *   to the lower block index) is part of the method's statement; the pages
+ *   only say "score logical blocks cheaply, keep the top-K" ([P1] "Quest").
+ *
+ * Conventions shared by every entry point
+ *   - Pointers are DEVICE pointers owned by the caller; the library never
+ *     allocates device memory. Scratch space comes from a caller-provided
+ *     workspace whose size a *_workspace_size() function returns.
+ *   - bf16 tensors are passed as pa_bf16 (the raw 16-bit pattern).
+ *   - Layouts are contiguous, row-major:
+ *       query / out      [B][Hq][D]
+ *       key / value      [T][Hkv][D]         (this step's new tokens)
+ *       key_cache,
+ *       value_cache      [NB][BS][Hkv][D]    (one layer, [P2] 2.6)
+ *       kmin / kmax      [NB][Hkv][D]        (Quest metadata per physical block)
+ *       block_tables     [B][MBS] int32      (logical -> physical block)
+ *       context_lens     [B] int32           (valid tokens, including this step's)
+ *       slot_mapping     [T] int64           (flat slot = block * BS + offset)
+ *       selected         [B][Hkv][topk] int32 (logical blocks, ascending, -1 padded)
+ *   - Query head h reads KV head h / (Hq / Hkv) ([P1] "GQA Paged Attention":
+ *     Hq is an integer multiple of Hkv).
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream). Every call
+ *     is asynchronous on that stream and returns a pa_status. Argument errors
+ *     are detected on the host before anything is launched.
+ *   - Supported shapes: head_dim D in {64, 128}; block_size BS = 16;
+ *     group size Hq / Hkv in 1..8; B <= 4096.
+ *   - Device data is never trusted to the point of a fault: negative or
+ *     out-of-pool slots are skipped, context_lens are clamped to
+ *     [0, MBS * BS], block-table entries outside [0, NB) make that block read
+ *     as empty (no tokens). pa_check_metadata() reports such entries.
+ *   - The library keeps no state between calls except per-device launch
+ *     parameters computed on first use.
+ */
+#ifndef PAGED_DECODE_H
+#define PAGED_DECODE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Entry points are the only symbols the shared library exports. */
+#if defined(__GNUC__)
+#define PA_API __attribute__((visibility("default")))
+#else
+#define PA_API
+#endif
+
+typedef uint16_t pa_bf16; /* bfloat16 bit pattern */
+
+typedef enum {
+    PA_OK = 0,
+    PA_ERR_INVALID_ARG = -1, /* null pointer, non-positive size, Hq % Hkv != 0 ... */
+    PA_ERR_UNSUPPORTED = -2, /* shape outside the supported set listed above */
+    PA_ERR_WORKSPACE = -3,   /* workspace missing or smaller than required */
+    PA_ERR_CUDA = -4,        /* a CUDA runtime/driver call or launch failed */
+    PA_ERR_DEVICE = -5       /* a kernel recorded a device-side failure (timeout) */
+} pa_status;
+
+/* Human-readable name of a pa_status value (static storage). */
+PA_API const char *pa_status_string(int status);
+
+/* The CUDA error code of the last PA_ERR_CUDA returned on this thread. */
+PA_API int pa_last_cuda_error(void);
+
+/* ReshapeAndCache ([P1] "ReshapeAndCache"): for every token t < num_tokens
+ * with slot = slot_mapping[t] >= 0, copies key[t] and value[t] (all KV heads)
+ * to key_cache / value_cache at block slot / block_size, offset
+ * slot % block_size. Negative slots are skipped; slots >= num_blocks *
+ * block_size are skipped as well. Slots must be distinct (two tokens writing
+ * one slot race). num_tokens == 0 is a no-op. */
+PA_API int pa_reshape_and_cache(const pa_bf16 *key, const pa_bf16 *value,
+                         pa_bf16 *key_cache, pa_bf16 *value_cache,
+                         const int64_t *slot_mapping, int64_t num_tokens,
+                         int num_kv_heads, int head_dim, int block_size,
+                         int64_t num_blocks, void *stream);
+
+/* Bytes of workspace pa_decode / quest_sparse_decode need on the CURRENT
+ * device for this batch and head shape (0 on invalid arguments). The
+ * workspace holds split-KV partial outputs, their log-sum-exp, per-sequence
+ * arrival counters and a status word. It must be ZERO-FILLED before its first
+ * use; every successful call leaves it zeroed again, so one buffer can serve
+ * any number of sequential calls on one stream. Calls that overlap in time
+ * must use different workspaces. */
+PA_API size_t pa_decode_workspace_size(int batch, int num_q_heads, int num_kv_heads, int head_dim);
+
+/* Dense GQA paged decode attention ([P1] "GQA Paged Attention"; split-KV and
+ * combine per [P2] 4.1). One query token per sequence:
+ *   out[b][h] = softmax_t(scale * query[b][h] . K[b][t]) . V[b][t]
+ * over t < context_lens[b], with K/V[b][t] at key/value_cache
+ * [block_tables[b][t / BS]][t % BS][h / G]. The score vector is never
+ * materialised (online softmax, fp32 accumulation); the KV range of the batch
+ * is split evenly over the GPU's warps and partial results are merged with
+ * log-sum-exp weights. out is bf16 (round to nearest even); a sequence with
+ * context_lens[b] == 0 gets a zero output. */
+PA_API int pa_decode(pa_bf16 *out, const pa_bf16 *query,
+              const pa_bf16 *key_cache, const pa_bf16 *value_cache,
+              const int32_t *block_tables, int max_blocks_per_seq,
+              const int32_t *context_lens, int batch, int num_q_heads,
+              int num_kv_heads, int head_dim, int block_size, int64_t num_blocks,
+              float scale, void *workspace, size_t workspace_bytes, void *stream);
+
+/* Quest metadata update for the tokens of one ReshapeAndCache call. For each
+ * physical block touched by a valid slot: if one of the call's tokens lands
+ * at offset 0 (the block starts fresh) the block's kmin/kmax become the
+ * elementwise min/max over the call's tokens in that block; otherwise they
+ * become min/max of the old values and those tokens. min/max follow IEEE
+ * totalOrder (-0 < +0), so the result is independent of token order.
+ * Slots must be the ones passed to pa_reshape_and_cache (same skip rules). */
+PA_API int quest_update_meta(pa_bf16 *kmin, pa_bf16 *kmax, const pa_bf16 *key,
+                      const int64_t *slot_mapping, int64_t num_tokens,
+                      int num_kv_heads, int head_dim, int block_size,
+                      int64_t num_blocks, void *stream);
+
+/* Quest metadata from scratch: for every sequence b and logical block
+ * j < ceil(context_lens[b] / BS), kmin/kmax of physical block
+ * block_tables[b][j] = elementwise min/max of K over the block's valid tokens
+ * (positions < context_lens[b]). Blocks no sequence uses are left as they are. */
+PA_API int quest_rebuild_meta(pa_bf16 *kmin, pa_bf16 *kmax, const pa_bf16 *key_cache,
+                       const int32_t *block_tables, int max_blocks_per_seq,
+                       const int32_t *context_lens, int batch, int num_kv_heads,
+                       int head_dim, int block_size, int64_t num_blocks, void *stream);
+
+/* Bytes of workspace quest_select_topk needs (0 on invalid arguments). The
+ * first batch * num_kv_heads * max_blocks_per_seq floats of the workspace hold
+ * the block scores [B][Hkv][MBS] after the call (entries for blocks past a
+ * sequence's context are not written). No zero-fill needed. */
+PA_API size_t quest_select_workspace_size(int batch, int num_kv_heads, int max_blocks_per_seq);
+
+/* Quest block selection ([P1] "Quest Sparse Attention"). For each sequence b
+ * and KV head g, every logical block j < ceil(context_lens[b] / BS) gets the
+ * score  sum_{h in group g} sum_d max(q[b,h,d]*kmin[p,g,d], q[b,h,d]*kmax[p,g,d])
+ * with p = block_tables[b][j] (an upper bound of the group's summed logits on
+ * that block). The score is computed in fp32 in one fixed order:
+ *   P_d = sum_h max(q,0), N_d = sum_h min(q,0) (h ascending, from +0);
+ *   t_d = fl(fl(P_d*kmax_d) + fl(N_d*kmin_d));
+ *   D split into 32 chunks of D/32 consecutive d, each summed left to right;
+ *   the 32 chunk sums combined by a xor-butterfly (offsets 16, 8, 4, 2, 1).
+ * The topk highest-scoring blocks are selected (ties: the lower block index;
+ * scores compared in IEEE totalOrder) and written ascending to
+ * selected[b][g][0..), the rest of the row padded with -1. If a sequence has
+ * no more than topk blocks, all of them are selected. */
+PA_API int quest_select_topk(int32_t *selected, const pa_bf16 *query,
+                      const pa_bf16 *kmin, const pa_bf16 *kmax,
+                      const int32_t *block_tables, int max_blocks_per_seq,
+                      const int32_t *context_lens, int batch, int num_q_heads,
+                      int num_kv_heads, int head_dim, int block_size, int64_t num_blocks,
+                      int topk, void *workspace, size_t workspace_bytes, void *stream);
+
+/* Quest sparse paged attention ([P1] "Quest Sparse Attention", "Sparse
+ * precision"): exact attention, as pa_decode, over only the tokens of the
+ * logical blocks listed in selected[b][h / G][0..topk) (entries < 0 or past
+ * the sequence's blocks are ignored; entries must be distinct), tokens at
+ * positions >= context_lens[b] masked. Uses the same workspace as pa_decode
+ * (size from pa_decode_workspace_size, same zero-fill rule). */
+PA_API int quest_sparse_decode(pa_bf16 *out, const pa_bf16 *query,
+                        const pa_bf16 *key_cache, const pa_bf16 *value_cache,
+                        const int32_t *block_tables, int max_blocks_per_seq,
+                        const int32_t *context_lens, const int32_t *selected, int topk,
+                        int batch, int num_q_heads, int num_kv_heads, int head_dim,
+                        int block_size, int64_t num_blocks, float scale,
+                        void *workspace, size_t workspace_bytes, void *stream);
+
+/* Reads the status word a pa_decode / quest_sparse_decode workspace carries
+ * (synchronises `stream`): PA_OK, or PA_ERR_DEVICE if a kernel gave up on a
+ * wait (its output is then undefined and the workspace must be zero-filled
+ * again before reuse). */
+PA_API int pa_workspace_status(const void *workspace, void *stream);
+
+/* Input checker (not on the hot path). Counts, on the device, into
+ * counts[0..3] (device int32, overwritten):
+ *   [0] slots >= num_blocks * block_size,
+ *   [1] context_lens outside [0, max_blocks_per_seq * block_size],
+ *   [2] block-table entries j < ceil(ctx/BS) outside [0, num_blocks),
+ *   [3] valid slots that repeat an earlier token's slot.
+ * Any pointer may be NULL (with its count 0) to skip that check. */
+PA_API int pa_check_metadata(int32_t *counts, const int64_t *slot_mapping, int64_t num_tokens,
+                      const int32_t *block_tables, int max_blocks_per_seq,
+                      const int32_t *context_lens, int batch, int block_size,
+                      int64_t num_blocks, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PAGED_DECODE_H */

@@ -1,0 +1,291 @@
+// api.cu -- the C ABI (include/paged_decode.h): argument checks on the host,
+// TMA descriptors, workspace carving, and the kernel launches. Nothing here
+// allocates device memory.
+#include <cstring>
+
+#include "../../include/paged_decode.h"
+#include "kernels.h"
+
+using namespace pa;
+
+namespace {
+
+thread_local int g_last_cuda_error = 0;
+
+int cuda_fail(cudaError_t e) {
+    g_last_cuda_error = int(e);
+    return PA_ERR_CUDA;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool shape_supported(int head_dim, int block_size) {
+    return (head_dim == 64 || head_dim == 128) && block_size == kBlockSize;
+}
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no link
+// against libcuda needed).
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static bool tried = false;
+    if (!tried) {
+        tried = true;
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    }
+    return fn;
+}
+
+// Tensor map over one layer's paged cache [NB][BS][Hkv][D] (bf16), boxes of
+// [1 block][BS tokens][1 head][64 dims] with 128-byte swizzle.
+int make_cache_map(CUtensorMap *map, const void *cache, int Hkv, int D, int BS, int64_t NB) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return cuda_fail(cudaErrorNotSupported);
+    const cuuint64_t dims[4] = {cuuint64_t(D), cuuint64_t(Hkv), cuuint64_t(BS), cuuint64_t(NB)};
+    const cuuint64_t strides[3] = {cuuint64_t(D) * 2, cuuint64_t(Hkv) * D * 2,
+                                   cuuint64_t(BS) * Hkv * D * 2};
+    const cuuint32_t box[4] = {64u, 1u, cuuint32_t(BS), 1u};
+    const cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
+    const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(cache), dims,
+                          strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return cuda_fail(cudaErrorInvalidValue);
+    return PA_OK;
+}
+
+struct DecodeWorkspace {
+    int32_t *status;
+    int32_t *counters;
+    float *part;
+};
+
+DecodeWorkspace carve_decode_ws(void *ws, int B, int Hkv) {
+    uint8_t *p = static_cast<uint8_t *>(ws);
+    const size_t segs = size_t(B) * Hkv;
+    const size_t counters = (segs * 4 + 255) / 256 * 256;
+    DecodeWorkspace d;
+    d.status = reinterpret_cast<int32_t *>(p);
+    d.counters = reinterpret_cast<int32_t *>(p + 256);
+    d.part = reinterpret_cast<float *>(p + 256 + counters);
+    return d;
+}
+
+int check_attention_args(const void *out, const void *q, const void *kc, const void *vc,
+                         const int32_t *bt, int MBS, const int32_t *ctx, int B, int Hq, int Hkv,
+                         int D, int BS, int64_t NB, float scale, const void *ws) {
+    if (!out || !q || !kc || !vc || !bt || !ctx || !ws) return PA_ERR_INVALID_ARG;
+    if (B <= 0 || Hq <= 0 || Hkv <= 0 || D <= 0 || BS <= 0 || NB <= 0 || MBS <= 0)
+        return PA_ERR_INVALID_ARG;
+    if (Hq % Hkv != 0) return PA_ERR_INVALID_ARG;
+    if (!(scale > 0.f) || scale != scale) return PA_ERR_INVALID_ARG;
+    if (!shape_supported(D, BS) || Hq / Hkv > kMaxGroup || B > kMaxBatch) return PA_ERR_UNSUPPORTED;
+    if (int64_t(MBS) * BS > int64_t(1) << 30) return PA_ERR_UNSUPPORTED;
+    if (NB > (int64_t(1) << 31) - 1) return PA_ERR_UNSUPPORTED;
+    if (!aligned16(out) || !aligned16(q) || !aligned16(kc) || !aligned16(vc) || !aligned16(ws))
+        return PA_ERR_INVALID_ARG;
+    return PA_OK;
+}
+
+int run_decode(pa_bf16 *out, const pa_bf16 *query, const pa_bf16 *key_cache,
+               const pa_bf16 *value_cache, const int32_t *block_tables, int MBS,
+               const int32_t *context_lens, const int32_t *selected, int topk, int B, int Hq,
+               int Hkv, int D, int BS, int64_t NB, float scale, void *workspace,
+               size_t workspace_bytes, void *stream, bool sparse) {
+    int rc = check_attention_args(out, query, key_cache, value_cache, block_tables, MBS,
+                                  context_lens, B, Hq, Hkv, D, BS, NB, scale, workspace);
+    if (rc != PA_OK) return rc;
+    if (sparse && (!selected || topk <= 0)) return PA_ERR_INVALID_ARG;
+    DecodeGeometry geo;
+    cudaError_t e = decode_geometry(D, &geo);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (workspace_bytes < decode_workspace_bytes(B, Hkv, D, geo.workers)) return PA_ERR_WORKSPACE;
+    CUtensorMap tk, tv;
+    if ((rc = make_cache_map(&tk, key_cache, Hkv, D, BS, NB)) != PA_OK) return rc;
+    if ((rc = make_cache_map(&tv, value_cache, Hkv, D, BS, NB)) != PA_OK) return rc;
+    const DecodeWorkspace w = carve_decode_ws(workspace, B, Hkv);
+    DecodeArgs a;
+    a.q = query;
+    a.bt = block_tables;
+    a.ctx = context_lens;
+    a.sel = selected;
+    a.out = out;
+    a.part = w.part;
+    a.counters = w.counters;
+    a.status = w.status;
+    a.NB = NB;
+    a.MBS = MBS;
+    a.topk = sparse ? topk : 0;
+    a.B = B;
+    a.Hq = Hq;
+    a.Hkv = Hkv;
+    a.G = Hq / Hkv;
+    a.scale_log2 = scale * 1.4426950408889634f;
+    e = launch_decode(tk, tv, a, D, sparse, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e);
+    return PA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *pa_status_string(int status) {
+    switch (status) {
+        case PA_OK: return "PA_OK";
+        case PA_ERR_INVALID_ARG: return "PA_ERR_INVALID_ARG";
+        case PA_ERR_UNSUPPORTED: return "PA_ERR_UNSUPPORTED";
+        case PA_ERR_WORKSPACE: return "PA_ERR_WORKSPACE";
+        case PA_ERR_CUDA: return "PA_ERR_CUDA";
+        case PA_ERR_DEVICE: return "PA_ERR_DEVICE";
+        default: return "PA_ERR_UNKNOWN";
+    }
+}
+
+int pa_last_cuda_error(void) { return g_last_cuda_error; }
+
+int pa_reshape_and_cache(const pa_bf16 *key, const pa_bf16 *value, pa_bf16 *key_cache,
+                         pa_bf16 *value_cache, const int64_t *slot_mapping, int64_t num_tokens,
+                         int num_kv_heads, int head_dim, int block_size, int64_t num_blocks,
+                         void *stream) {
+    if (num_tokens < 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 || num_blocks <= 0)
+        return PA_ERR_INVALID_ARG;
+    if (num_tokens == 0) return PA_OK;
+    if (!key || !value || !key_cache || !value_cache || !slot_mapping) return PA_ERR_INVALID_ARG;
+    if (!shape_supported(head_dim, block_size)) return PA_ERR_UNSUPPORTED;
+    if (num_tokens > (int64_t(1) << 31) - 1) return PA_ERR_UNSUPPORTED;
+    if (!aligned16(key) || !aligned16(value) || !aligned16(key_cache) || !aligned16(value_cache))
+        return PA_ERR_INVALID_ARG;
+    const cudaError_t e = launch_reshape_and_cache(key, value, key_cache, value_cache, slot_mapping,
+                                                   num_tokens, num_kv_heads, head_dim, block_size,
+                                                   num_blocks, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? PA_OK : cuda_fail(e);
+}
+
+size_t pa_decode_workspace_size(int batch, int num_q_heads, int num_kv_heads, int head_dim) {
+    if (batch <= 0 || num_q_heads <= 0 || num_kv_heads <= 0 || num_q_heads % num_kv_heads != 0)
+        return 0;
+    if (!shape_supported(head_dim, kBlockSize) || batch > kMaxBatch) return 0;
+    DecodeGeometry geo;
+    if (decode_geometry(head_dim, &geo) != cudaSuccess) return 0;
+    return decode_workspace_bytes(batch, num_kv_heads, head_dim, geo.workers);
+}
+
+int pa_decode(pa_bf16 *out, const pa_bf16 *query, const pa_bf16 *key_cache,
+              const pa_bf16 *value_cache, const int32_t *block_tables, int max_blocks_per_seq,
+              const int32_t *context_lens, int batch, int num_q_heads, int num_kv_heads,
+              int head_dim, int block_size, int64_t num_blocks, float scale, void *workspace,
+              size_t workspace_bytes, void *stream) {
+    return run_decode(out, query, key_cache, value_cache, block_tables, max_blocks_per_seq,
+                      context_lens, nullptr, 0, batch, num_q_heads, num_kv_heads, head_dim,
+                      block_size, num_blocks, scale, workspace, workspace_bytes, stream, false);
+}
+
+int quest_sparse_decode(pa_bf16 *out, const pa_bf16 *query, const pa_bf16 *key_cache,
+                        const pa_bf16 *value_cache, const int32_t *block_tables,
+                        int max_blocks_per_seq, const int32_t *context_lens,
+                        const int32_t *selected, int topk, int batch, int num_q_heads,
+                        int num_kv_heads, int head_dim, int block_size, int64_t num_blocks,
+                        float scale, void *workspace, size_t workspace_bytes, void *stream) {
+    return run_decode(out, query, key_cache, value_cache, block_tables, max_blocks_per_seq,
+                      context_lens, selected, topk, batch, num_q_heads, num_kv_heads, head_dim,
+                      block_size, num_blocks, scale, workspace, workspace_bytes, stream, true);
+}
+
+int quest_update_meta(pa_bf16 *kmin, pa_bf16 *kmax, const pa_bf16 *key,
+                      const int64_t *slot_mapping, int64_t num_tokens, int num_kv_heads,
+                      int head_dim, int block_size, int64_t num_blocks, void *stream) {
+    if (num_tokens < 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 || num_blocks <= 0)
+        return PA_ERR_INVALID_ARG;
+    if (num_tokens == 0) return PA_OK;
+    if (!kmin || !kmax || !key || !slot_mapping) return PA_ERR_INVALID_ARG;
+    if (!shape_supported(head_dim, block_size)) return PA_ERR_UNSUPPORTED;
+    if (num_tokens > (int64_t(1) << 31) - 1) return PA_ERR_UNSUPPORTED;
+    if (!aligned16(kmin) || !aligned16(kmax) || !aligned16(key)) return PA_ERR_INVALID_ARG;
+    const cudaError_t e = launch_update_meta(kmin, kmax, key, slot_mapping, num_tokens, num_kv_heads,
+                                             head_dim, block_size, num_blocks,
+                                             static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? PA_OK : cuda_fail(e);
+}
+
+int quest_rebuild_meta(pa_bf16 *kmin, pa_bf16 *kmax, const pa_bf16 *key_cache,
+                       const int32_t *block_tables, int max_blocks_per_seq,
+                       const int32_t *context_lens, int batch, int num_kv_heads, int head_dim,
+                       int block_size, int64_t num_blocks, void *stream) {
+    if (!kmin || !kmax || !key_cache || !block_tables || !context_lens) return PA_ERR_INVALID_ARG;
+    if (batch <= 0 || max_blocks_per_seq <= 0 || num_kv_heads <= 0 || num_blocks <= 0)
+        return PA_ERR_INVALID_ARG;
+    if (!shape_supported(head_dim, block_size) || batch > 65535) return PA_ERR_UNSUPPORTED;
+    if (!aligned16(kmin) || !aligned16(kmax) || !aligned16(key_cache)) return PA_ERR_INVALID_ARG;
+    const cudaError_t e = launch_rebuild_meta(kmin, kmax, key_cache, block_tables,
+                                              max_blocks_per_seq, context_lens, batch, num_kv_heads,
+                                              head_dim, block_size, num_blocks,
+                                              static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? PA_OK : cuda_fail(e);
+}
+
+size_t quest_select_workspace_size(int batch, int num_kv_heads, int max_blocks_per_seq) {
+    if (batch <= 0 || num_kv_heads <= 0 || max_blocks_per_seq <= 0) return 0;
+    const size_t bytes = size_t(batch) * num_kv_heads * max_blocks_per_seq * sizeof(float);
+    return (bytes + 255) / 256 * 256;
+}
+
+int quest_select_topk(int32_t *selected, const pa_bf16 *query, const pa_bf16 *kmin,
+                      const pa_bf16 *kmax, const int32_t *block_tables, int max_blocks_per_seq,
+                      const int32_t *context_lens, int batch, int num_q_heads, int num_kv_heads,
+                      int head_dim, int block_size, int64_t num_blocks, int topk, void *workspace,
+                      size_t workspace_bytes, void *stream) {
+    if (!selected || !query || !kmin || !kmax || !block_tables || !context_lens || !workspace)
+        return PA_ERR_INVALID_ARG;
+    if (batch <= 0 || num_q_heads <= 0 || num_kv_heads <= 0 || max_blocks_per_seq <= 0 ||
+        num_blocks <= 0 || topk <= 0 || head_dim <= 0 || block_size <= 0)
+        return PA_ERR_INVALID_ARG;
+    if (num_q_heads % num_kv_heads != 0) return PA_ERR_INVALID_ARG;
+    if (!shape_supported(head_dim, block_size) || batch > kMaxBatch) return PA_ERR_UNSUPPORTED;
+    if (int64_t(max_blocks_per_seq) * block_size > int64_t(1) << 30) return PA_ERR_UNSUPPORTED;
+    if (!aligned16(query) || !aligned16(kmin) || !aligned16(kmax) || !aligned16(workspace))
+        return PA_ERR_INVALID_ARG;
+    if (workspace_bytes < quest_select_workspace_size(batch, num_kv_heads, max_blocks_per_seq))
+        return PA_ERR_WORKSPACE;
+    const cudaError_t e = launch_quest_select(
+        selected, static_cast<float *>(workspace), query, kmin, kmax, block_tables,
+        max_blocks_per_seq, context_lens, batch, num_q_heads, num_kv_heads, head_dim, block_size,
+        num_blocks, topk, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? PA_OK : cuda_fail(e);
+}
+
+int pa_workspace_status(const void *workspace, void *stream) {
+    if (!workspace) return PA_ERR_INVALID_ARG;
+    int32_t st = 0;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaMemcpyAsync(&st, workspace, sizeof st, cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return cuda_fail(e);
+    return st == 0 ? PA_OK : PA_ERR_DEVICE;
+}
+
+int pa_check_metadata(int32_t *counts, const int64_t *slot_mapping, int64_t num_tokens,
+                      const int32_t *block_tables, int max_blocks_per_seq,
+                      const int32_t *context_lens, int batch, int block_size, int64_t num_blocks,
+                      void *stream) {
+    if (!counts || num_tokens < 0 || batch < 0 || block_size <= 0 || num_blocks <= 0)
+        return PA_ERR_INVALID_ARG;
+    if (num_tokens > 0 && !slot_mapping) return PA_ERR_INVALID_ARG;
+    if (block_tables && (!context_lens || max_blocks_per_seq <= 0)) return PA_ERR_INVALID_ARG;
+    if (num_tokens > (int64_t(1) << 31) - 1) return PA_ERR_UNSUPPORTED;
+    const cudaError_t e = launch_check_metadata(counts, slot_mapping, num_tokens, block_tables,
+                                                max_blocks_per_seq, context_lens, batch, block_size,
+                                                num_blocks, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? PA_OK : cuda_fail(e);
+}
+
+}  // extern "C"

@@ -1,0 +1,208 @@
+// cache_ops.cu -- KV-cache write path (sm_103a): ReshapeAndCache, Quest
+// metadata update / rebuild, and the input checker.
+//
+// ReshapeAndCache ("Ascend Kernel-to-Serving Pipeline", section
+// "ReshapeAndCache"): token t's K and V rows go to block slot / BS, offset
+// slot % BS; negative slots are skipped. In the [NB][BS][Hkv][D] layout the
+// destination of one token is one contiguous Hkv*D row, so the kernel is a
+// 16-byte vectorised row copy, one CTA per token.
+//
+// Quest metadata: per physical block and KV head, elementwise min/max of K
+// over the block's tokens, compared in IEEE totalOrder (-0 < +0) so the result
+// is a unique bit pattern whatever the order of the tokens.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace pa {
+
+namespace {
+
+// ------------------------------------------------------------ ReshapeAndCache
+
+__global__ void __launch_bounds__(128) reshape_and_cache_kernel(
+    const uint4 *__restrict__ key, const uint4 *__restrict__ value, uint4 *__restrict__ kc,
+    uint4 *__restrict__ vc, const int64_t *__restrict__ slots, int row_vecs, int BS, int64_t NB) {
+    const int64_t t = blockIdx.x;
+    const int64_t slot = __ldg(slots + t);
+    if (slot < 0 || slot >= NB * BS) return;  // padding token, or outside the pool
+    const int64_t block_idx = slot / BS, block_offset = slot % BS;
+    const int64_t dst = (block_idx * BS + block_offset) * row_vecs;
+    const int64_t src = t * row_vecs;
+    for (int e = threadIdx.x; e < row_vecs; e += blockDim.x) {
+        kc[dst + e] = __ldg(key + src + e);
+        vc[dst + e] = __ldg(value + src + e);
+    }
+}
+
+// ---------------------------------------------------------- metadata update
+
+__device__ __forceinline__ uint32_t min_key(uint32_t a, uint32_t b) {
+    return bf16_order_key(b) < bf16_order_key(a) ? b : a;
+}
+__device__ __forceinline__ uint32_t max_key(uint32_t a, uint32_t b) {
+    return bf16_order_key(b) > bf16_order_key(a) ? b : a;
+}
+
+// Elementwise min/max of 8 packed bf16 values (uint4) in totalOrder.
+__device__ __forceinline__ void minmax8(uint4 &lo, uint4 &hi, const uint4 &v) {
+    uint32_t *l = reinterpret_cast<uint32_t *>(&lo);
+    uint32_t *h = reinterpret_cast<uint32_t *>(&hi);
+    const uint32_t *x = reinterpret_cast<const uint32_t *>(&v);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const uint32_t xl = x[i] & 0xffffu, xh = x[i] >> 16;
+        const uint32_t ll = min_key(l[i] & 0xffffu, xl), lh = min_key(l[i] >> 16, xh);
+        const uint32_t hl = max_key(h[i] & 0xffffu, xl), hh = max_key(h[i] >> 16, xh);
+        l[i] = ll | (lh << 16);
+        h[i] = hl | (hh << 16);
+    }
+}
+
+// One warp per token. The warp of the lowest-index token landing in a
+// physical block (its "leader") gathers every token of the call in that block
+// and writes the block's new metadata; the other warps exit. So each block is
+// written by exactly one warp and no atomics are needed.
+__global__ void __launch_bounds__(256) update_meta_kernel(
+    uint4 *__restrict__ kmin, uint4 *__restrict__ kmax, const uint4 *__restrict__ key,
+    const int64_t *__restrict__ slots, int64_t T, int row_vecs, int BS, int64_t NB) {
+    const int64_t t = int64_t(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (t >= T) return;
+    const int64_t s = __ldg(slots + t);
+    if (s < 0 || s >= NB * BS) return;
+    const int64_t p = s / BS;
+    bool reset = false;
+    for (int64_t u0 = 0; u0 < T; u0 += 32) {
+        const int64_t u = u0 + lane;
+        const int64_t su = u < T ? __ldg(slots + u) : -1;
+        const bool in_blk = su >= 0 && su < NB * BS && su / BS == p;
+        if (__any_sync(0xffffffffu, in_blk && u < t)) return;  // not the leader
+        reset |= __any_sync(0xffffffffu, in_blk && (su % BS) == 0);
+    }
+    // leader: start from the old metadata or, if the block starts fresh, from
+    // this token; then merge every later token of the call in the block
+    for (int e = lane; e < row_vecs; e += 32) {
+        uint4 lo, hi;
+        const uint4 kt = __ldg(key + t * row_vecs + e);
+        if (reset) {
+            lo = kt;
+            hi = kt;
+        } else {
+            lo = kmin[p * row_vecs + e];
+            hi = kmax[p * row_vecs + e];
+            minmax8(lo, hi, kt);
+        }
+        for (int64_t u = t + 1; u < T; ++u) {
+            const int64_t su = __ldg(slots + u);
+            if (su >= 0 && su < NB * BS && su / BS == p) minmax8(lo, hi, __ldg(key + u * row_vecs + e));
+        }
+        kmin[p * row_vecs + e] = lo;
+        kmax[p * row_vecs + e] = hi;
+    }
+}
+
+// ---------------------------------------------------------- metadata rebuild
+
+// One CTA per (logical block j, sequence b): min/max over the block's valid
+// tokens, read straight from the cache.
+__global__ void __launch_bounds__(64) rebuild_meta_kernel(
+    uint4 *__restrict__ kmin, uint4 *__restrict__ kmax, const uint4 *__restrict__ kc,
+    const int32_t *__restrict__ bt, int MBS, const int32_t *__restrict__ ctx, int row_vecs,
+    int BS, int64_t NB) {
+    const int j = blockIdx.x, b = blockIdx.y;
+    const int c = min(max(__ldg(ctx + b), 0), MBS * BS);
+    if (j * BS >= c) return;
+    const int p = __ldg(bt + int64_t(b) * MBS + j);
+    if (p < 0 || int64_t(p) >= NB) return;
+    const int nv = min(BS, c - j * BS);
+    for (int e = threadIdx.x; e < row_vecs; e += blockDim.x) {
+        uint4 lo = __ldg(kc + (int64_t(p) * BS) * row_vecs + e), hi = lo;
+        for (int o = 1; o < nv; ++o) minmax8(lo, hi, __ldg(kc + (int64_t(p) * BS + o) * row_vecs + e));
+        kmin[int64_t(p) * row_vecs + e] = lo;
+        kmax[int64_t(p) * row_vecs + e] = hi;
+    }
+}
+
+// ------------------------------------------------------------- input checker
+
+__global__ void __launch_bounds__(256) check_metadata_kernel(
+    int32_t *counts, const int64_t *__restrict__ slots, int64_t T, const int32_t *__restrict__ bt,
+    int MBS, const int32_t *__restrict__ ctx, int B, int BS, int64_t NB) {
+    const int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (slots && i < T) {
+        const int64_t s = slots[i];
+        if (s >= NB * BS) atomicAdd(counts + 0, 1);
+        if (s >= 0) {
+            for (int64_t u = 0; u < i; ++u)
+                if (slots[u] == s) {
+                    atomicAdd(counts + 3, 1);
+                    break;
+                }
+        }
+    }
+    if (ctx && i < B) {
+        const int c = ctx[i];
+        if (c < 0 || int64_t(c) > int64_t(MBS) * BS) atomicAdd(counts + 1, 1);
+        if (bt) {
+            const int cc = min(max(c, 0), MBS * BS);
+            const int nblk = (cc + BS - 1) / BS;
+            int bad = 0;
+            for (int j = 0; j < nblk; ++j) {
+                const int p = bt[i * MBS + j];
+                bad += (p < 0 || int64_t(p) >= NB);
+            }
+            if (bad) atomicAdd(counts + 2, bad);
+        }
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_reshape_and_cache(const uint16_t *key, const uint16_t *value, uint16_t *kc,
+                                     uint16_t *vc, const int64_t *slots, int64_t T, int Hkv, int D,
+                                     int BS, int64_t NB, cudaStream_t stream) {
+    if (T == 0) return cudaSuccess;
+    const int row_vecs = Hkv * D / 8;
+    reshape_and_cache_kernel<<<unsigned(T), 128, 0, stream>>>(
+        reinterpret_cast<const uint4 *>(key), reinterpret_cast<const uint4 *>(value),
+        reinterpret_cast<uint4 *>(kc), reinterpret_cast<uint4 *>(vc), slots, row_vecs, BS, NB);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_update_meta(uint16_t *kmin, uint16_t *kmax, const uint16_t *key,
+                               const int64_t *slots, int64_t T, int Hkv, int D, int BS, int64_t NB,
+                               cudaStream_t stream) {
+    if (T == 0) return cudaSuccess;
+    const int row_vecs = Hkv * D / 8;
+    const int warps = 8;
+    const unsigned grid = unsigned((T + warps - 1) / warps);
+    update_meta_kernel<<<grid, warps * 32, 0, stream>>>(
+        reinterpret_cast<uint4 *>(kmin), reinterpret_cast<uint4 *>(kmax),
+        reinterpret_cast<const uint4 *>(key), slots, T, row_vecs, BS, NB);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_rebuild_meta(uint16_t *kmin, uint16_t *kmax, const uint16_t *kc,
+                                const int32_t *bt, int MBS, const int32_t *ctx, int B, int Hkv,
+                                int D, int BS, int64_t NB, cudaStream_t stream) {
+    const int row_vecs = Hkv * D / 8;
+    const dim3 grid{unsigned(MBS), unsigned(B), 1u};
+    rebuild_meta_kernel<<<grid, 64, 0, stream>>>(
+        reinterpret_cast<uint4 *>(kmin), reinterpret_cast<uint4 *>(kmax),
+        reinterpret_cast<const uint4 *>(kc), bt, MBS, ctx, row_vecs, BS, NB);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_check_metadata(int32_t *counts, const int64_t *slots, int64_t T,
+                                  const int32_t *bt, int MBS, const int32_t *ctx, int B, int BS,
+                                  int64_t NB, cudaStream_t stream) {
+    cudaError_t e = cudaMemsetAsync(counts, 0, 4 * sizeof(int32_t), stream);
+    if (e != cudaSuccess) return e;
+    const int64_t n = T > B ? T : B;
+    if (n == 0) return cudaSuccess;
+    check_metadata_kernel<<<unsigned((n + 255) / 256), 256, 0, stream>>>(counts, slots, T, bt, MBS,
+                                                                          ctx, B, BS, NB);
+    return cudaGetLastError();
+}
+
+}  // namespace pa

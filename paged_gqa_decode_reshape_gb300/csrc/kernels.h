@@ -1,0 +1,60 @@
+// kernels.h -- internal interface between the C-ABI layer and the kernels.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace pa {
+
+constexpr int kBlockSize = 16;       // tokens per KV block
+constexpr int kMaxBatch = 4096;      // sequences per call
+constexpr int kMaxGroup = 8;         // query heads per KV head (one mma n-tile)
+
+// Arguments of the split-KV decode kernel (dense and Quest-sparse).
+struct DecodeArgs {
+    const uint16_t *q;          // [B][Hq][D] bf16
+    const int32_t *bt;          // [B][MBS]
+    const int32_t *ctx;         // [B]
+    const int32_t *sel;         // [B][Hkv][topk] (sparse only)
+    uint16_t *out;              // [B][Hq][D] bf16
+    float *part;                // [B*Hkv + W][D*8 + 8] partial outputs and lse (log2 domain)
+    int32_t *counters;          // [B*Hkv] arrival counters (zero between calls)
+    int32_t *status;            // workspace status word
+    int64_t NB;
+    int MBS, topk, B, Hq, Hkv, G;
+    float scale_log2;           // softmax scale * log2(e)
+};
+
+// Per-device launch geometry of the decode kernel for one head_dim.
+struct DecodeGeometry {
+    int grid;          // CTAs (persistent)
+    int warps;         // warps per CTA
+    int workers;       // grid * warps
+    size_t smem;       // dynamic shared memory bytes for B = kMaxBatch
+};
+
+cudaError_t decode_geometry(int head_dim, DecodeGeometry *g);
+size_t decode_workspace_bytes(int B, int Hkv, int head_dim, int workers);
+cudaError_t launch_decode(const CUtensorMap &tm_k, const CUtensorMap &tm_v, const DecodeArgs &a,
+                          int head_dim, bool sparse, cudaStream_t stream);
+
+cudaError_t launch_reshape_and_cache(const uint16_t *key, const uint16_t *value, uint16_t *kc,
+                                     uint16_t *vc, const int64_t *slots, int64_t T, int Hkv, int D,
+                                     int BS, int64_t NB, cudaStream_t stream);
+cudaError_t launch_update_meta(uint16_t *kmin, uint16_t *kmax, const uint16_t *key,
+                               const int64_t *slots, int64_t T, int Hkv, int D, int BS, int64_t NB,
+                               cudaStream_t stream);
+cudaError_t launch_rebuild_meta(uint16_t *kmin, uint16_t *kmax, const uint16_t *kc,
+                                const int32_t *bt, int MBS, const int32_t *ctx, int B, int Hkv,
+                                int D, int BS, int64_t NB, cudaStream_t stream);
+cudaError_t launch_check_metadata(int32_t *counts, const int64_t *slots, int64_t T,
+                                  const int32_t *bt, int MBS, const int32_t *ctx, int B, int BS,
+                                  int64_t NB, cudaStream_t stream);
+
+cudaError_t launch_quest_select(int32_t *sel, float *scores, const uint16_t *q,
+                                const uint16_t *kmin, const uint16_t *kmax, const int32_t *bt,
+                                int MBS, const int32_t *ctx, int B, int Hq, int Hkv, int D, int BS,
+                                int64_t NB, int topk, cudaStream_t stream);
+
+}  // namespace pa

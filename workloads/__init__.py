@@ -42,7 +42,9 @@ Recipe (all draws from ``numpy.random.default_rng`` streams spawned from one
 
 from __future__ import annotations
 
+import concurrent.futures
 import math
+import os
 from dataclasses import dataclass, field
 from typing import Dict, Optional
 
@@ -52,14 +54,43 @@ BF16_NAN = np.uint16(0x7FC0)
 
 # Draw K/V in chunks of this many physical blocks so that the byte stream of a
 # seed does not depend on the machine's memory.
-_CHUNK_BLOCKS = 4096
+_CHUNK_BLOCKS = 1024
 
 
 def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
     """Round float32 values to bf16 (round to nearest, ties to even); finite inputs."""
-    u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32)
-    bias = ((u >> np.uint32(16)) & np.uint32(1)) + np.uint32(0x7FFF)
-    return ((u + bias) >> np.uint32(16)).astype(np.uint16)
+    u = np.array(x, dtype=np.float32, copy=True, order="C").view(np.uint32)
+    b = np.right_shift(u, 16)
+    np.bitwise_and(b, 1, out=b)
+    b += np.uint32(0x7FFF)
+    u += b
+    return np.right_shift(u, 16).astype(np.uint16)
+
+
+def _draw_pool(seed_seq: np.random.SeedSequence, n: int, inner: tuple) -> np.ndarray:
+    """n x inner bf16 values ~ N(0, 1).
+
+    The leading dimension is cut into chunks of _CHUNK_BLOCKS; chunk c draws
+    from its own stream spawned from `seed_seq`, so the result depends only
+    on the seed (not on how many threads fill the chunks)."""
+    out = np.empty((n,) + tuple(inner), dtype=np.uint16)
+    starts = list(range(0, n, _CHUNK_BLOCKS))
+    seeds = seed_seq.spawn(len(starts))
+
+    def fill(i):
+        c0 = starts[i]
+        c1 = min(n, c0 + _CHUNK_BLOCKS)
+        rng = np.random.default_rng(seeds[i])
+        out[c0:c1] = f32_to_bf16_bits(rng.standard_normal((c1 - c0,) + tuple(inner), dtype=np.float32))
+
+    workers = max(1, min(len(starts), os.cpu_count() or 1))
+    if workers == 1:
+        for i in range(len(starts)):
+            fill(i)
+    else:
+        with concurrent.futures.ThreadPoolExecutor(max_workers=workers) as ex:
+            list(ex.map(fill, range(len(starts))))
+    return out
 
 
 def bf16_bits_to_f32(h: np.ndarray) -> np.ndarray:
@@ -159,16 +190,8 @@ def build_workload(name: str, *, B: int, Hq: int, Hkv: int, D: int, BS: int,
     q = f32_to_bf16_bits(np.random.default_rng(s_q).standard_normal((B, Hq, D), dtype=np.float32))
 
     # cache pools (N(0,1) everywhere, then poison and planting)
-    def draw_pool(seed):
-        rng = np.random.default_rng(seed)
-        out = np.empty((NB, BS, Hkv, D), dtype=np.uint16)
-        for c0 in range(0, NB, _CHUNK_BLOCKS):
-            c1 = min(NB, c0 + _CHUNK_BLOCKS)
-            out[c0:c1] = f32_to_bf16_bits(rng.standard_normal((c1 - c0, BS, Hkv, D), dtype=np.float32))
-        return out
-
-    kc = draw_pool(s_k)
-    vc = draw_pool(s_v)
+    kc = _draw_pool(s_k, NB, (BS, Hkv, D))
+    vc = _draw_pool(s_v, NB, (BS, Hkv, D))
 
     # the step's new tokens: one per sequence, at position ctx-1
     T = B
@@ -247,13 +270,22 @@ WORKLOADS = ("tiny", "dense_b32", "quest_8k", "long_40k", "mixed_b128")
 
 
 def make(name: str, *, poison: bool = True, seed: Optional[int] = None,
-         batch: Optional[int] = None, ctx_scale: float = 1.0) -> Workload:
+         batch: Optional[int] = None, ctx_scale: float = 1.0,
+         topk: Optional[int] = None) -> Workload:
     """Build one of the named workloads.
 
     ``batch`` and ``ctx_scale`` shrink a workload for fast elementwise parity
-    (same recipe, fewer and shorter sequences); leave them at their defaults
-    for the full sizes.
+    (same recipe, fewer and shorter sequences) and ``topk`` overrides the
+    selection size; leave them at their defaults for the full sizes.
     """
+    w = _make(name, poison=poison, seed=seed, batch=batch, ctx_scale=ctx_scale)
+    if topk is not None:
+        w.topk = int(topk)
+    return w
+
+
+def _make(name: str, *, poison: bool, seed: Optional[int], batch: Optional[int],
+          ctx_scale: float) -> Workload:
     if name == "tiny":
         # batch 2, Hq 4, Hkv 1, D 64, ctx {37, 100}, pool of 16 blocks, topk 3,
         # the second sequence's new-token slot is -1
