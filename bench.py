@@ -1,0 +1,463 @@
+"""Benchmark of the paged decode hot path on GB300.
+
+One step = one pass of the whole path over one batch of synthetic input:
+ReshapeAndCache -> Quest metadata update -> dense GQA paged decode (split-KV +
+combine) -> Quest scoring + top-K -> Quest sparse decode, every call through
+the C ABI. Inputs are resident in HBM before timing; the L2 is flushed (a
+512 MiB write) before every step, outside the timed events. Each call is
+bracketed by CUDA events on the launching stream, so per-kernel times and
+the roofline of the dominant kernel (the dense decode) come from the same run.
+
+Prints ONE JSON line (rank 0). With --impl reference it times the CPU oracle
+instead (a bounded sample of the same workload per step).
+
+Multi-GPU: the path shards by sequence with no exchange, so N ranks run N
+independent replicas (weak scaling); the ranks only meet for the timing
+barrier and the max-over-ranks reduction.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+if HERE not in sys.path:
+    sys.path.insert(0, HERE)
+
+METRIC = "decode-attn KV GB/s & % HBM roofline; µs/step dense vs Quest at 8K/40K ctx"
+UNIT = "GB/s"
+L2_FLUSH_BYTES = 512 << 20
+
+
+def parse():
+    p = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=50)
+    p.add_argument("--warmup", type=int, default=10)
+    p.add_argument("--impl", choices=["native", "reference"], default="native")
+    p.add_argument("--workload", default="quest_8k",
+                   choices=["tiny", "dense_b32", "quest_8k", "long_40k", "mixed_b128"])
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--cpu-budget", type=float, default=12.0,
+                   help="seconds of oracle work for the CPU baseline sample")
+    return p.parse_args()
+
+
+# ----------------------------------------------------------------- helpers
+
+
+def measured_peaks():
+    path = os.path.join(HERE, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def recorded_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from an ncu capture, if it was taken on the
+    current source of the kernel (else None)."""
+    import hashlib
+    path = os.path.join(HERE, "profiles", "dram_traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        rec = json.load(f)
+    ent = rec.get(kernel, {}).get(workload)
+    if not ent:
+        return None
+    src = os.path.join(HERE, "paged_gqa_decode_reshape_gb300", "csrc", ent["source"])
+    if not os.path.exists(src):
+        return None
+    sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    if sha != ent.get("source_sha"):
+        return None
+    return int(ent["dram_bytes_per_launch"])
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.gpu_id = gpu_id
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self.gpu_id, f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        rows = [r.split(",") for r in out.strip().splitlines() if r.strip()]
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            r = [x.strip() for x in r]
+            if len(r) < 8:
+                continue
+            try:
+                sm.append(float(r[0]))
+                mx = float(r[1])
+            except ValueError:
+                continue
+            for n, v in zip(names, r[4:8]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def gpu_id_for(torch, dev) -> str:
+    try:
+        uuid = str(torch.cuda.get_device_properties(dev).uuid)
+        return uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+    except Exception:
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+        parts = [p for p in vis.split(",") if p.strip()]
+        idx = dev.index or 0
+        return parts[idx] if idx < len(parts) else str(idx)
+
+
+# --------------------------------------------------------------- the step
+
+
+class Step:
+    """Device buffers of one workload and the five C-ABI calls of a step."""
+
+    def __init__(self, w, dev):
+        import torch
+        import paged_gqa_decode_reshape_gb300 as pg
+        self.pg, self.torch, self.w, self.dev = pg, torch, w, dev
+
+        def d16(a):
+            return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)
+
+        self.q = d16(w.q)
+        self.kc = d16(w.key_cache)
+        self.vc = d16(w.value_cache)
+        self.key = d16(w.key)
+        self.value = d16(w.value)
+        self.slots = torch.from_numpy(w.slot_mapping).to(dev)
+        self.bt = torch.from_numpy(w.block_tables).to(dev)
+        self.ctx = torch.from_numpy(w.context_lens).to(dev)
+        self.out = torch.empty((w.B, w.Hq, w.D), dtype=torch.bfloat16, device=dev)
+        self.out_sparse = torch.empty_like(self.out)
+        self.kmin = torch.zeros((w.NB, w.Hkv, w.D), dtype=torch.bfloat16, device=dev)
+        self.kmax = torch.zeros_like(self.kmin)
+        self.sel = torch.empty((w.B, w.Hkv, w.topk), dtype=torch.int32, device=dev)
+        self.ws = torch.zeros(pg.pa_decode_workspace_size(w.B, w.Hq, w.Hkv, w.D), dtype=torch.uint8,
+                              device=dev)
+        self.sel_ws = torch.zeros(pg.quest_select_workspace_size(w.B, w.Hkv, w.MBS),
+                                  dtype=torch.uint8, device=dev)
+        # Quest metadata of the cache as it stands (setup, not timed)
+        pg.pa_reshape_and_cache(self.key, self.value, self.kc, self.vc, self.slots)
+        pg.quest_rebuild_meta(self.kmin, self.kmax, self.kc, self.bt, self.ctx)
+        torch.cuda.synchronize(dev)
+
+    def calls(self):
+        pg, w = self.pg, self.w
+        return [
+            lambda: pg.pa_reshape_and_cache(self.key, self.value, self.kc, self.vc, self.slots),
+            lambda: pg.quest_update_meta(self.kmin, self.kmax, self.key, self.slots, w.BS),
+            lambda: pg.pa_decode(self.out, self.q, self.kc, self.vc, self.bt, self.ctx, w.scale,
+                                 workspace=self.ws),
+            lambda: pg.quest_select_topk(self.sel, self.q, self.kmin, self.kmax, self.bt, self.ctx,
+                                         w.BS, workspace=self.sel_ws),
+            lambda: pg.quest_sparse_decode(self.out_sparse, self.q, self.kc, self.vc, self.bt,
+                                           self.ctx, self.sel, w.scale, workspace=self.ws),
+        ]
+
+
+CALL_NAMES = ["reshape", "meta", "dense", "select", "sparse"]
+LAUNCHES_PER_CALL = [1, 1, 1, 2, 1]
+
+
+# -------------------------------------------------------------- CPU oracle
+
+
+def oracle_sample(w, budget_s: float):
+    """The oracle on a bounded sample of the step: the write path for every
+    token, then whole sequences (dense attention for all heads, Quest scores
+    and top-K for all KV heads, sparse attention for all heads) until the
+    time budget is spent. Returns (algorithmic bytes, seconds, sequences)."""
+    import oracle
+    from paged_gqa_decode_reshape_gb300 import ledger
+    kc, vc = w.key_cache, w.value_cache       # the oracle writes in place: state after the step
+    t0 = time.perf_counter()
+    oracle.reshape_and_cache(w.key, w.value, kc, vc, w.slot_mapping)
+    kmin = np.zeros((w.NB, w.Hkv, w.D), dtype=np.uint16)
+    kmax = np.zeros_like(kmin)
+    # the metadata of the pre-existing cache is setup on both sides (not timed)
+    t_setup0 = time.perf_counter()
+    oracle.quest_rebuild_meta(kc, w.block_tables, w.context_lens, kmin, kmax)
+    t_setup = time.perf_counter() - t_setup0
+    oracle.quest_update_meta(kmin, kmax, w.key, w.slot_mapping, w.BS)
+    nbytes = ledger.step_bytes(w.context_lens, w.slot_mapping, w.Hq, w.Hkv, w.D, w.BS, w.topk)
+    done_bytes = nbytes.reshape + nbytes.meta
+    seqs = 0
+    for b in range(w.B):
+        if time.perf_counter() - t0 - t_setup > budget_s and seqs > 0:
+            break
+        rows = np.array([(b, h) for h in range(w.Hq)], dtype=np.int32)
+        oracle.paged_attention(w.q, kc, vc, w.block_tables, w.context_lens, w.scale, rows=rows)
+        sc = oracle.quest_scores(w.q[b:b + 1], kmin, kmax, w.block_tables[b:b + 1],
+                                 w.context_lens[b:b + 1], w.BS)
+        sel = oracle.quest_topk(sc, w.context_lens[b:b + 1], w.BS, w.topk)
+        full_sel = np.full((w.B, w.Hkv, w.topk), -1, dtype=np.int32)
+        full_sel[b] = sel[0]
+        oracle.sparse_attention(w.q, kc, vc, w.block_tables, w.context_lens, full_sel, w.scale,
+                                rows=rows)
+        one = ledger.step_bytes(w.context_lens[b:b + 1], np.zeros(0, np.int64), w.Hq, w.Hkv, w.D,
+                                w.BS, w.topk, selected=sel)
+        done_bytes += one.dense + one.select + one.sparse
+        seqs += 1
+    elapsed = time.perf_counter() - t0 - t_setup
+    return done_bytes, elapsed, seqs
+
+
+# -------------------------------------------------------------------- main
+
+
+def max_over_ranks(values, pgroup):
+    """Element-wise max of per-rank timings (the slowest replica sets the
+    job's time); identity on one rank."""
+    if pgroup is None:
+        return [float(v) for v in values]
+    import torch
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64)
+    pgroup.all_reduce(t, op=pgroup.ReduceOp.MAX)
+    pgroup.barrier()
+    return [float(v) for v in t]
+
+
+def job_throughput(world: int, bytes_per_replica_step: int, ms_per_step: float) -> float:
+    """Whole-job GB/s: every replica moves its step's bytes in the max-over-ranks time."""
+    return world * bytes_per_replica_step / (ms_per_step * 1e-3) / 1e9
+
+
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    pgroup = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("gloo")
+        pgroup = dist
+    return world, rank, local, pgroup
+
+
+def run_reference(args, world, rank, pgroup):
+    import workloads
+    if rank != 0:
+        return 0
+    w0 = workloads.make(args.workload, poison=False)
+    cores = 1
+    times, nbytes = [], []
+    for i in range(args.warmup + args.steps):
+        # the oracle's writes are idempotent, so every step reuses the same inputs
+        b, s, seqs = oracle_sample(w0, args.cpu_budget / max(1, args.steps + args.warmup))
+        if i >= args.warmup:
+            times.append(s)
+            nbytes.append(b)
+    value = sum(nbytes) / sum(times) / 1e9
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": 1e3 * sum(times) / len(times),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "impl": "reference",
+        "config": {"workload": args.workload, "sample": "per step: the write path for every token, "
+                   "then whole sequences in order until the step's time share is spent"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": f"{args.steps} steps of a bounded sample of {args.workload}"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+    return 0
+
+
+def main():
+    args = parse()
+    world, rank, local, pgroup = dist_setup(args)
+    if args.impl == "reference":
+        return run_reference(args, world, rank, pgroup)
+
+    import torch
+    import paged_gqa_decode_reshape_gb300 as pg
+    import paged_gqa_decode_reshape_gb300.build as pgb
+    import workloads
+    from paged_gqa_decode_reshape_gb300 import ledger
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU (the native path has no CPU fallback)")
+    pgb.build()
+    pg.load_library()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    w = workloads.make(args.workload, poison=False)
+    step = Step(w, dev)
+    calls = step.calls()
+    stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    # warm-up (untimed)
+    for _ in range(max(3, args.warmup)):
+        for c in calls:
+            c()
+    torch.cuda.synchronize(dev)
+    sel_host = step.sel.cpu().numpy()
+    nb = ledger.step_bytes(w.context_lens, w.slot_mapping, w.Hq, w.Hkv, w.D, w.BS, w.topk,
+                           selected=sel_host)
+
+    # timed device steps: flush L2, then events around every call
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(calls) + 1)] for _ in range(K)]
+    sampler = ClockSampler(gpu_id_for(torch, dev))
+    if pgroup:
+        pgroup.barrier()
+    torch.cuda.synchronize(dev)
+    sampler.start()
+    time.sleep(0.3)
+    wall0 = time.perf_counter()
+    for i in range(K):
+        flush.fill_(i & 0xFF)
+        ev[i][0].record(stream)
+        for j, c in enumerate(calls):
+            c()
+            ev[i][j + 1].record(stream)
+    torch.cuda.synchronize(dev)
+    wall = time.perf_counter() - wall0
+    clocks = sampler.stop()
+    per_call = np.array([[ev[i][j].elapsed_time(ev[i][j + 1]) for j in range(len(calls))]
+                         for i in range(K)])              # ms
+    step_ms = per_call.sum(axis=1)
+    local_ms = float(step_ms.mean())
+
+    # end to end through the C ABI with host buffers: H2D of the step's inputs
+    # from pinned memory, the five calls, D2H of the outputs, every step
+    h_in = {n: t.cpu().pin_memory() for n, t in
+            dict(q=step.q, key=step.key, value=step.value, slots=step.slots, bt=step.bt,
+                 ctx=step.ctx).items()}
+    h_out = {n: torch.empty_like(t, device="cpu").pin_memory() for n, t in
+             dict(out=step.out, out_sparse=step.out_sparse, sel=step.sel).items()}
+    h2d = sum(t.numel() * t.element_size() for t in h_in.values())
+    d2h = sum(t.numel() * t.element_size() for t in h_out.values())
+    e2e_ms = []
+    for i in range(K):
+        flush.fill_(i & 0xFF)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        step.q.copy_(h_in["q"], non_blocking=True)
+        step.key.copy_(h_in["key"], non_blocking=True)
+        step.value.copy_(h_in["value"], non_blocking=True)
+        step.slots.copy_(h_in["slots"], non_blocking=True)
+        step.bt.copy_(h_in["bt"], non_blocking=True)
+        step.ctx.copy_(h_in["ctx"], non_blocking=True)
+        for c in calls:
+            c()
+        h_out["out"].copy_(step.out, non_blocking=True)
+        h_out["out_sparse"].copy_(step.out_sparse, non_blocking=True)
+        h_out["sel"].copy_(step.sel, non_blocking=True)
+        e1.record(stream)
+        e1.synchronize()
+        e2e_ms.append(e0.elapsed_time(e1))
+    e2e_local = float(np.mean(e2e_ms))
+
+    ms, e2e_ms_max = max_over_ranks([local_ms, e2e_local], pgroup)
+
+    if rank != 0:
+        return 0
+
+    call_ms = per_call.mean(axis=0)
+    call_bytes = [nb.reshape, nb.meta, nb.dense, nb.select, nb.sparse]
+    value = job_throughput(world, nb.total, ms)
+    peak, peak_kind = measured_peaks()
+    dense_gbs = nb.dense / (call_ms[2] * 1e-3) / 1e9
+    breakdown = {n: {"us": round(float(m) * 1e3, 2), "GBps": round(b / (m * 1e-3) / 1e9, 1),
+                     "frac_of_peak": round(b / (m * 1e-3) / 1e9 / peak, 3), "bytes": int(b)}
+                 for n, m, b in zip(CALL_NAMES, call_ms, call_bytes)}
+    dense_us = float(call_ms[0] + call_ms[2]) * 1e3
+    quest_us = float(call_ms[0] + call_ms[1] + call_ms[3] + call_ms[4]) * 1e3
+    line = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": UNIT,
+        "n_gpus": world,
+        "steps": K,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic",
+        "config": {
+            "workload": args.workload, "batch": w.B, "num_q_heads": w.Hq, "num_kv_heads": w.Hkv,
+            "head_dim": w.D, "block_size": w.BS, "topk_blocks": w.topk,
+            "context_lens_mean": round(float(w.context_lens.mean()), 1),
+            "context_lens_max": int(w.context_lens.max()), "pool_blocks": w.NB,
+            "kv_pool_bytes": int(2 * w.key_cache.nbytes),
+            "step": "reshape_and_cache + quest_update_meta + pa_decode + quest_select_topk + "
+                    "quest_sparse_decode",
+            "l2": f"flushed before every step ({L2_FLUSH_BYTES >> 20} MiB write), outside the timed events",
+            "parallelism": f"replicas x{world}",
+        },
+        "roofline": {
+            "bound": "hbm", "kernel": "pa_decode (split-KV decode + fused combine, 1 launch)",
+            "achieved": round(dense_gbs, 1), "peak": peak, "unit": "GB/s",
+            "frac": round(dense_gbs / peak, 4), "peak_kind": peak_kind,
+            "traffic": recorded_traffic("pa_decode", args.workload),
+            "algorithmic_bytes_per_launch": int(nb.dense),
+        },
+        "breakdown": breakdown,
+        "dense_us_per_step": round(dense_us, 2),
+        "quest_us_per_step": round(quest_us, 2),
+        "tokens_per_s": {"dense": round(world * w.B / (dense_us * 1e-6), 1),
+                         "quest": round(world * w.B / (quest_us * 1e-6), 1)},
+        "e2e": {"value": round(job_throughput(world, nb.total, e2e_ms_max), 2), "unit": UNIT,
+                "ms_per_step": round(e2e_ms_max, 5), "h2d_bytes_per_step": int(h2d),
+                "d2h_bytes_per_step": int(d2h)},
+        "gpu_launches": int(K * sum(LAUNCHES_PER_CALL)),
+        "wall_s_timed_region": round(wall, 4),
+        "clocks": clocks,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        wc = workloads.make(args.workload, poison=False)
+        b, s, seqs = oracle_sample(wc, args.cpu_budget)
+        line["cpu_baseline"] = {
+            "value": round(b / s / 1e9, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"write path for all {w.T} tokens + {seqs} of {w.B} sequences "
+                      f"(dense, Quest select, sparse; all heads), {s:.1f} s of CPU time"}
+    print(json.dumps(line))
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

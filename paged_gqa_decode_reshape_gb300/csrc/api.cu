@@ -122,6 +122,12 @@ int run_decode(pa_bf16 *out, const pa_bf16 *query, const pa_bf16 *key_cache,
     a.part = w.part;
     a.counters = w.counters;
     a.status = w.status;
+#ifdef PA_DECODE_TRACE
+    a.trace = reinterpret_cast<uint64_t *>(static_cast<uint8_t *>(workspace) +
+                                           decode_trace_offset(B, Hkv, D, geo.workers));
+#else
+    a.trace = nullptr;
+#endif
     a.NB = NB;
     a.MBS = MBS;
     a.topk = sparse ? topk : 0;

@@ -61,7 +61,9 @@ __device__ __forceinline__ void minmax8(uint4 &lo, uint4 &hi, const uint4 &v) {
 // One warp per token. The warp of the lowest-index token landing in a
 // physical block (its "leader") gathers every token of the call in that block
 // and writes the block's new metadata; the other warps exit. So each block is
-// written by exactly one warp and no atomics are needed.
+// written by exactly one warp and no atomics are needed. The slot scan is one
+// coalesced pass (ballots over 32 tokens at a time); in a decode step a block
+// receives one token, so the leader has no further members to visit.
 __global__ void __launch_bounds__(256) update_meta_kernel(
     uint4 *__restrict__ kmin, uint4 *__restrict__ kmax, const uint4 *__restrict__ key,
     const int64_t *__restrict__ slots, int64_t T, int row_vecs, int BS, int64_t NB) {
@@ -71,33 +73,51 @@ __global__ void __launch_bounds__(256) update_meta_kernel(
     const int64_t s = __ldg(slots + t);
     if (s < 0 || s >= NB * BS) return;
     const int64_t p = s / BS;
-    bool reset = false;
+    bool reset = (s % BS) == 0;
+    int64_t first_member_chunk = -1;   // first 32-token chunk holding a later token of block p
     for (int64_t u0 = 0; u0 < T; u0 += 32) {
         const int64_t u = u0 + lane;
         const int64_t su = u < T ? __ldg(slots + u) : -1;
         const bool in_blk = su >= 0 && su < NB * BS && su / BS == p;
         if (__any_sync(0xffffffffu, in_blk && u < t)) return;  // not the leader
-        reset |= __any_sync(0xffffffffu, in_blk && (su % BS) == 0);
+        const unsigned later = __ballot_sync(0xffffffffu, in_blk && u > t);
+        reset |= __any_sync(0xffffffffu, in_blk && u > t && (su % BS) == 0);
+        if (later && first_member_chunk < 0) first_member_chunk = u0;
     }
     // leader: start from the old metadata or, if the block starts fresh, from
     // this token; then merge every later token of the call in the block
-    for (int e = lane; e < row_vecs; e += 32) {
-        uint4 lo, hi;
+    const int per_lane = (row_vecs + 31) / 32;
+    for (int r = 0; r < per_lane; ++r) {
+        const int e = lane + 32 * r;
+        if (e >= row_vecs) break;
         const uint4 kt = __ldg(key + t * row_vecs + e);
-        if (reset) {
-            lo = kt;
-            hi = kt;
-        } else {
+        uint4 lo = kt, hi = kt;
+        if (!reset) {
             lo = kmin[p * row_vecs + e];
             hi = kmax[p * row_vecs + e];
             minmax8(lo, hi, kt);
         }
-        for (int64_t u = t + 1; u < T; ++u) {
-            const int64_t su = __ldg(slots + u);
-            if (su >= 0 && su < NB * BS && su / BS == p) minmax8(lo, hi, __ldg(key + u * row_vecs + e));
-        }
         kmin[p * row_vecs + e] = lo;
         kmax[p * row_vecs + e] = hi;
+    }
+    if (first_member_chunk < 0) return;
+    for (int64_t u0 = first_member_chunk; u0 < T; u0 += 32) {
+        const int64_t u = u0 + lane;
+        const int64_t su = u < T ? __ldg(slots + u) : -1;
+        unsigned m = __ballot_sync(0xffffffffu, su >= 0 && su < NB * BS && su / BS == p && u > t);
+        while (m) {
+            const int bit = __ffs(m) - 1;
+            m &= m - 1;
+            const int64_t tu = u0 + bit;
+            for (int r = 0; r < per_lane; ++r) {
+                const int e = lane + 32 * r;
+                if (e >= row_vecs) break;
+                uint4 lo = kmin[p * row_vecs + e], hi = kmax[p * row_vecs + e];
+                minmax8(lo, hi, __ldg(key + tu * row_vecs + e));
+                kmin[p * row_vecs + e] = lo;
+                kmax[p * row_vecs + e] = hi;
+            }
+        }
     }
 }
 

@@ -10,28 +10,37 @@
 //
 // How (GB300 design):
 //  * Work list. Each (sequence, KV head) is a segment of items, one item per
-//    KV block (dense: logical blocks 0..ceil(ctx/16)-1; sparse: the topk
-//    selection entries). Segments are concatenated and the list is cut into
-//    equal contiguous ranges, one per warp of a persistent grid (one or two
-//    CTAs per SM). Every warp moves the same number of KV bytes whatever the
-//    length mix; a warp's range touches at most a few segments.
-//  * Data movement. Each warp owns an S-stage ring of shared-memory stages.
-//    One lane issues two TMA tile loads per K and V block ([16 tokens x 64
-//    dims] boxes of a 4-D tensor map over the whole pool, 128-byte swizzle)
-//    with an L2 evict-first hint; the physical block number is a runtime TMA
-//    coordinate. Stage completion is an mbarrier transaction count.
-//  * Math. The GQA group's queries stay in registers as mma B fragments.
-//    S^T = K Q^T and O^T += V^T P^T run on bf16 mma.sync (m16n8k16) with the
-//    16 tokens of a block as the M dimension and the (up to 8) heads of the
-//    group as N, so every K/V byte serves the whole group. Online softmax in
-//    the log2 domain (running max, normaliser, rescaled accumulator), P
-//    rounded to bf16 and transposed in registers with movmatrix.
+//    16-token KV block (dense: logical blocks 0..ceil(ctx/16)-1; sparse: the
+//    topk selection entries). The segments are concatenated and cut into
+//    equal contiguous ranges, one per CTA of a persistent grid (one CTA per
+//    SM), so every SM streams the same number of KV bytes whatever the
+//    length mix.
+//  * Data movement. A producer warp walks the CTA's range, resolves each
+//    item's physical block (block table, and selection for sparse) a window
+//    of 32 items ahead, and issues two TMA tile loads per K and per V block
+//    ([16 tokens x 64 dims] boxes of a 4-D tensor map over the whole pool,
+//    128-byte swizzle, L2 evict-first) into an S-stage shared-memory ring with
+//    full/empty mbarriers. The physical block number is a runtime TMA
+//    coordinate.
+//    The producer's lanes work on 8 items at a time (one lane per tile copy),
+//    so one warp instruction issues up to 32 TMA copies.
+//  * Math. Consumer warps take the ring's items in pairs, round-robin; the
+//    ring has 2 * consumers * pairs-in-flight stages so that every stage
+//    belongs to one consumer.
+//    The GQA group's queries stay in registers as mma B fragments; S^T = K Q^T
+//    and O^T += V^T P^T run on bf16 mma.sync (m16n8k16) with the tokens as M
+//    and the (up to 8) heads of the group as N, so every K/V byte serves the
+//    whole group. Online softmax in the log2 domain over 32 tokens per step
+//    (running max, normaliser, accumulator rescaled only when the max grows);
+//    P is rounded to bf16 and transposed in registers with movmatrix.
 //  * Masking. Tokens past ctx get score -inf and their V fragment lanes are
 //    zeroed, so NaN/Inf garbage in unused slots never reaches the output.
-//  * Combine. A warp that covers a whole segment writes bf16 output directly.
-//    Otherwise each piece writes a normalised partial and its log2-sum-exp;
-//    the last piece to arrive (atomic counter per segment) merges the pieces
-//    with weights exp2(lse_s - max lse) and resets the counter to zero.
+//  * Combine. At the end of each segment the consumer warps merge their
+//    states through shared memory. A CTA holding a whole segment writes bf16
+//    output; otherwise it writes a normalised partial and its log2-sum-exp,
+//    and the last CTA to arrive (atomic counter per segment, reset to zero
+//    afterwards) merges the pieces with weights exp2(lse_s - max lse), one
+//    float4 of the output per thread and step.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -41,6 +50,32 @@ namespace {
 
 constexpr uint64_t kWaitLimitNs = 500ull * 1000ull * 1000ull;  // 0.5 s per mbarrier wait
 
+// Launch geometry (tuning knobs): consumer warps, and block pairs each
+// consumer has in flight. The ring has S = 2 * consumers * pairs stages, so
+// stage s always belongs to consumer (s / 2) % consumers: every consumer waits
+// on its own stages in order and an mbarrier parity wait can never be
+// answered by an older phase.
+#ifndef PA_DECODE_CONSUMERS
+#define PA_DECODE_CONSUMERS 4
+#endif
+#ifndef PA_DECODE_PAIRS
+#define PA_DECODE_PAIRS 3
+#endif
+
+// Optional CTA timeline (%globaltimer) for tuning builds: compile with
+// -DPA_DECODE_TRACE and the kernel writes 8 timestamps per CTA after the
+// partials in the workspace.
+#ifdef PA_DECODE_TRACE
+#define PA_TRACE(k)                                                                      \
+    do {                                                                                 \
+        if (tid == 0 && a.trace) a.trace[int64_t(blockIdx.x) * 8 + (k)] = global_timer_ns(); \
+    } while (0)
+#else
+#define PA_TRACE(k) \
+    do {            \
+    } while (0)
+#endif
+
 template <int D>
 struct DecodeCfg {
     static constexpr int BS = kBlockSize;
@@ -48,52 +83,65 @@ struct DecodeCfg {
     static constexpr int STAGE = 2 * KT;        // K + V
     static constexpr int NKK = D / 16;          // QK k-steps == PV m-tiles
     static constexpr int HALF = BS * 128;       // bytes of one 64-dim half tile
-    static constexpr int PART = D * 8 + 8;      // floats per partial slot
-    static constexpr int DPL = D / 32;          // dims per lane in the combine
-    static constexpr int NW = 4;                // warps per CTA
-    static constexpr int S = (D == 128) ? 6 : 8; // stages per warp
-    static constexpr size_t smem_bytes(int B) {
-        return 1024 + size_t(NW) * S * STAGE + size_t(NW) * S * 8 + size_t(B + 1) * 4;
-    }
+    static constexpr int PART = D * 8 + 8;      // floats per partial slot: O[D][8], lse[8]
+    static constexpr int NC = PA_DECODE_CONSUMERS;
+    static constexpr int THREADS = (NC + 1) * 32;
+    static constexpr int R = (D == 128) ? PA_DECODE_PAIRS : 2 * PA_DECODE_PAIRS;
+    static constexpr int S = 2 * NC * R;        // ring stages
+    static constexpr int SCR = D * 8 + 16;      // floats per consumer merge slot: acc[D][8], m[8], l[8]
+    static constexpr size_t off_bars = size_t(S) * STAGE;
+    static constexpr size_t off_info = off_bars + size_t(S) * 16;
+    static constexpr size_t off_scr = off_info + size_t(S) * 8;
+    static constexpr size_t off_flags = off_scr + size_t(NC) * SCR * 4;
+    static constexpr size_t off_pre = off_flags + 64;
+    static constexpr size_t smem_bytes(int B) { return 1024 + off_pre + size_t(B + 1) * 4; }
 };
 
-struct ItemInfo {
-    int seg;   // b * Hkv + kvh, -1 past the range
-    int phys;  // physical block, -1 if the block has no tokens to read
-    int nv;    // valid tokens in the block (0..16)
-};
+__device__ __forceinline__ void consumer_sync(int nthreads) {
+    asm volatile("bar.sync 1, %0;" ::"r"(nthreads) : "memory");
+}
 
 template <int D, bool SPARSE>
-__global__ void __launch_bounds__(DecodeCfg<D>::NW * 32, 1)
+__global__ void __launch_bounds__(DecodeCfg<D>::THREADS, 1)
     decode_kernel(const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const DecodeArgs a) {
     using C = DecodeCfg<D>;
-    constexpr int BS = C::BS, NW = C::NW, S = C::S, NKK = C::NKK;
+    constexpr int BS = C::BS, NC = C::NC, S = C::S, NKK = C::NKK;
 
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
-    uint8_t *base_ptr = smem_raw + (base - raw);
-    const uint32_t bars = base + NW * S * C::STAGE;
-    int32_t *pre = reinterpret_cast<int32_t *>(base_ptr + NW * S * C::STAGE + NW * S * 8);
+    uint8_t *bp = smem_raw + (base - raw);
+    const uint32_t full_bar = base + uint32_t(C::off_bars);
+    const uint32_t empty_bar = full_bar + S * 8;
+    int2 *info = reinterpret_cast<int2 *>(bp + C::off_info);
+    float *scr = reinterpret_cast<float *>(bp + C::off_scr);
+    volatile int *flags = reinterpret_cast<volatile int *>(bp + C::off_flags);  // [0] abort, [1] last
+    int32_t *pre = reinterpret_cast<int32_t *>(bp + C::off_pre);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int B = a.B, Hkv = a.Hkv, G = a.G;
     const int max_tok = a.MBS * BS;
+    PA_TRACE(0);
 
+    // ---- prologue: items per KV head of every sequence and their prefix sum
     if (tid == 0) {
         prefetch_tensormap(&tm_k);
         prefetch_tensormap(&tm_v);
     }
-    // items per KV head of every sequence, then their prefix sum
-    for (int b = tid; b < B; b += NW * 32) {
+    for (int b = tid; b < B; b += C::THREADS) {
         const int c = min(max(__ldg(a.ctx + b), 0), max_tok);
         const int nblk = (c + BS - 1) / BS;
         pre[b + 1] = SPARSE ? (nblk > 0 ? a.topk : 0) : nblk;
     }
-    if (tid == 0) pre[0] = 0;
-    if (lane == 0) {
-        for (int s = 0; s < S; ++s) mbar_init(bars + (warp * S + s) * 8, 1);
+    if (tid == 0) {
+        pre[0] = 0;
+        flags[0] = 0;
+        flags[1] = 0;
+        for (int s = 0; s < S; ++s) {
+            mbar_init(full_bar + s * 8, 1);
+            mbar_init(empty_bar + s * 8, 1);
+        }
         fence_barrier_init();
     }
     __syncthreads();
@@ -114,7 +162,7 @@ __global__ void __launch_bounds__(DecodeCfg<D>::NW * 32, 1)
     __syncthreads();
 
     // sequences with nothing to attend to get a zero output
-    for (int idx = blockIdx.x * NW * 32 + tid; idx < B * a.Hq; idx += gridDim.x * NW * 32) {
+    for (int idx = blockIdx.x * C::THREADS + tid; idx < B * a.Hq; idx += gridDim.x * C::THREADS) {
         const int b = idx / a.Hq;
         if (pre[b + 1] == pre[b]) {
             uint4 *o = reinterpret_cast<uint4 *>(a.out + int64_t(idx) * D);
@@ -124,89 +172,141 @@ __global__ void __launch_bounds__(DecodeCfg<D>::NW * 32, 1)
     }
 
     const int64_t total = int64_t(Hkv) * pre[B];
-    const int W = gridDim.x * NW;
-    const int w = blockIdx.x * NW + warp;
-    const int64_t L = (total + W - 1) / W;
-    const int64_t pos0 = int64_t(w) * L;
+    const int64_t L = (total + gridDim.x - 1) / gridDim.x;
+    const int64_t pos0 = int64_t(blockIdx.x) * L;
     const int64_t pos1 = min(total, pos0 + L);
-    if (pos0 >= pos1) return;  // no __syncthreads below this point
+    if (pos0 >= pos1) return;  // whole CTA: nothing to do
     const int n_items = int(pos1 - pos0);
+    PA_TRACE(1);
 
-    // where item k of this warp's range lives
-    auto locate = [&](int k) -> ItemInfo {
-        ItemInfo it{-1, -1, 0};
-        if (k >= n_items) return it;
-        const int64_t pos = pos0 + k;
+    // sequence holding global item position p
+    auto find_seq = [&](int64_t p) -> int {
         int lo = 0, hi = B;
         while (hi - lo > 1) {
             const int mid = (lo + hi) >> 1;
-            if (int64_t(Hkv) * pre[mid] <= pos) lo = mid; else hi = mid;
+            if (int64_t(Hkv) * pre[mid] <= p) lo = mid; else hi = mid;
         }
-        const int b = lo;
-        const int n = pre[b + 1] - pre[b];
-        const int64_t r = pos - int64_t(Hkv) * pre[b];
-        const int kvh = int(r / n);
-        const int i = int(r - int64_t(kvh) * n);
-        const int c = min(max(__ldg(a.ctx + b), 0), max_tok);
-        const int nblk = (c + BS - 1) / BS;
-        const int j = SPARSE ? __ldg(a.sel + (int64_t(b) * Hkv + kvh) * a.topk + i) : i;
-        it.seg = b * Hkv + kvh;
-        if (j >= 0 && j < nblk) {
-            const int ph = __ldg(a.bt + int64_t(b) * a.MBS + j);
-            if (ph >= 0 && int64_t(ph) < a.NB) {
-                it.phys = ph;
-                it.nv = min(BS, c - j * BS);
+        return lo;
+    };
+
+    if (warp == NC) {
+        // ================================================================ producer
+        // Item windows of 32 (one item per lane), refilled in three steps so no
+        // load is waited on before its value is needed: stage C locates the
+        // item and starts loading ctx (and the selection entry for sparse);
+        // one window later stage B starts loading the block-table entry; one
+        // window after that the items are issued.
+        struct Win {
+            int seg, j, phys, ctxv;
+        };
+        auto stage_c = [&](int k0) -> Win {
+            Win it{-1, -1, -1, 0};
+            const int k = k0 + lane;
+            if (k >= n_items) return it;
+            const int64_t p = pos0 + k;
+            const int b = find_seq(p);
+            const int n = pre[b + 1] - pre[b];
+            const int64_t r = p - int64_t(Hkv) * pre[b];
+            const int kvh = int(r / n);
+            const int i = int(r - int64_t(kvh) * n);
+            it.seg = b * Hkv + kvh;
+            it.ctxv = __ldg(a.ctx + b);
+            it.j = SPARSE ? __ldg(a.sel + (int64_t(b) * Hkv + kvh) * a.topk + i) : i;
+            return it;
+        };
+        auto stage_b = [&](Win &it) {
+            if (it.seg < 0) return;
+            const int b = it.seg / Hkv;
+            it.phys = (it.j >= 0 && it.j < a.MBS) ? __ldg(a.bt + int64_t(b) * a.MBS + it.j) : -1;
+        };
+        const uint64_t policy = l2_policy_evict_first();
+        Win wa = stage_c(0), wb = stage_c(32);
+        stage_b(wa);
+        stage_b(wb);
+        Win wc = stage_c(64);
+        int wbase = 0;
+        int issued = 0;  // items [0, issued) have been armed
+        int fail_step = 0;
+        unsigned fail_armed = 0;  // after a failure: leader lanes whose item was armed
+        // 8 items per step: lane = 4 * item + part, part = which tile copy
+        const int it = lane >> 2, part = lane & 3;
+        constexpr int PARTS = 2 * (D / 64);  // K and V, 64-dim halves
+        for (int k0 = 0; k0 < n_items; k0 += 8) {
+            if (k0 >= wbase + 32) {
+                wa = wb;
+                wb = wc;
+                stage_b(wb);
+                wbase += 32;
+                wc = stage_c(wbase + 64);
             }
-        }
-        return it;
-    };
-
-    const uint32_t my_stages = base + warp * S * C::STAGE;
-    const uint32_t my_bars = bars + warp * S * 8;
-    const uint64_t policy = l2_policy_evict_first();
-
-    // two 32-item windows of per-lane item info
-    ItemInfo wa = locate(lane), wb = locate(32 + lane);
-    int wbase = 0;
-    auto item = [&](int k) -> ItemInfo {
-        const bool first = k < wbase + 32;
-        ItemInfo src = first ? wa : wb;
-        ItemInfo r;
-        r.seg = __shfl_sync(0xffffffffu, src.seg, k & 31);
-        r.phys = __shfl_sync(0xffffffffu, src.phys, k & 31);
-        r.nv = __shfl_sync(0xffffffffu, src.nv, k & 31);
-        return r;
-    };
-    auto issue = [&](int k, const ItemInfo &it) {
-        const int st = k % S;
-        const uint32_t bar = my_bars + st * 8;
-        if (it.phys >= 0) {
-            const uint32_t dst = my_stages + st * C::STAGE;
-            const int kvh = it.seg % Hkv;
-            mbar_arrive_expect_tx(bar, C::STAGE);
-#pragma unroll
-            for (int hf = 0; hf < D / 64; ++hf) {
-                tma_load_4d(dst + hf * C::HALF, &tm_k, bar, hf * 64, kvh, 0, it.phys, policy);
-                tma_load_4d(dst + C::KT + hf * C::HALF, &tm_v, bar, hf * 64, kvh, 0, it.phys,
-                            policy);
+            const int k = k0 + it;
+            const int seg = __shfl_sync(0xffffffffu, wa.seg, k & 31);
+            const int j = __shfl_sync(0xffffffffu, wa.j, k & 31);
+            const int ph = __shfl_sync(0xffffffffu, wa.phys, k & 31);
+            const int cv = __shfl_sync(0xffffffffu, wa.ctxv, k & 31);
+            const bool live = k < n_items;
+            const int c = min(max(cv, 0), max_tok);
+            const int nblk = (c + BS - 1) / BS;
+            const bool valid = live && j >= 0 && j < nblk && ph >= 0 && int64_t(ph) < a.NB;
+            const int nv = valid ? min(BS, c - j * BS) : 0;
+            const int st = k % S;
+            const uint32_t fb = full_bar + st * 8;
+            // the item's leader lane waits for its stage to be released, then arms it
+            int ok = 1;
+            if (live && part == 0) {
+                if (k >= S && !mbar_wait_bounded(empty_bar + st * 8, ((k / S) & 1) ^ 1, kWaitLimitNs)) {
+                    ok = 0;
+                } else {
+                    info[st] = make_int2(seg, nv);
+                    if (nv > 0) mbar_arrive_expect_tx(fb, C::STAGE);
+                    else mbar_arrive(fb);
+                }
             }
-        } else {
-            mbar_arrive(bar);
+            ok = __shfl_sync(0xffffffffu, ok, lane & ~3);
+            __syncwarp();
+            if (live && ok && nv > 0 && part < PARTS) {
+                constexpr int HV = D / 64;             // 64-dim halves per tile
+                const int tsel = part / HV, hf = part % HV;  // 0: K, 1: V
+                const uint32_t dst = base + st * C::STAGE + tsel * C::KT + hf * C::HALF;
+                tma_load_4d(dst, tsel ? &tm_v : &tm_k, fb, hf * 64, seg % Hkv, 0, ph, policy);
+            }
+            if (!__all_sync(0xffffffffu, ok)) {
+                // a stage was never released: give up (consumers skip their
+                // waits from now on), remembering which items of this step
+                // were armed so their copies can land before the CTA exits
+                if (lane == 0) {
+                    flags[0] = 1;
+                    atomicOr(a.status, kStatusTimeout);
+                }
+                fail_step = k0;
+                fail_armed = __ballot_sync(0xffffffffu, live && part == 0 && ok);
+                break;
+            }
+            issued = min(n_items, k0 + 8);
         }
-    };
-
-    const int nprolog = min(S, n_items);
-    for (int k = 0; k < nprolog; ++k) {
-        const ItemInfo it = item(k);
-        if (lane == 0) issue(k, it);
+        // keep the CTA alive until every copy issued has landed (consumers that
+        // gave up do not wait for them)
+        if (lane == 0) {
+            for (int k = max(0, issued - S); k < issued; ++k)
+                mbar_wait_bounded(full_bar + (k % S) * 8, (k / S) & 1, kWaitLimitNs);
+            for (int i = 0; i < 8; ++i)
+                if (fail_armed & (1u << (4 * i))) {
+                    const int k = fail_step + i;
+                    mbar_wait_bounded(full_bar + (k % S) * 8, (k / S) & 1, kWaitLimitNs);
+                }
+        }
+        return;
     }
 
+    // ==================================================================== consumers
+    const int c_id = warp;  // 0 .. NC-1
+    const int ctid = tid;   // 0 .. NC*32-1
     const int g = lane >> 2, q4 = lane & 3;
+    const float scale_log2 = a.scale_log2;
     uint32_t qb[NKK][2];
     float acc[NKK][4];
-    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
-    int cur_seg = -1;
-    int64_t piece_begin = pos0;
+    float m0, m1, l0, l1;
+    bool traced_first = false;
 
     auto load_q = [&](int seg) {
         const int b = seg / Hkv, kvh = seg % Hkv;
@@ -225,182 +325,90 @@ __global__ void __launch_bounds__(DecodeCfg<D>::NW * 32, 1)
         m0 = m1 = -INFINITY;
         l0 = l1 = 0.f;
     };
-
-    // merge the pieces of segment `seg` (called by the last piece to arrive)
-    auto combine = [&](int seg, int64_t s0, int64_t e0) {
-        constexpr int DPL = C::DPL;
-        const int b = seg / Hkv, kvh = seg % Hkv;
-        const int w0 = int(s0 / L), w1 = int((e0 - 1) / L);
-        float M[8];
+    // S^T = K Q^T for the 16 tokens of one staged block (two mma chains)
+    auto qk = [&](uint32_t kb, float (&sc)[4]) {
+        float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
+        const int rk = (lane & 7) + (((lane >> 3) & 1) << 3);
 #pragma unroll
-        for (int h = 0; h < 8; ++h) M[h] = -INFINITY;
-        for (int ww = w0; ww <= w1; ++ww) {
-            const float *ps = a.part + int64_t(seg + ww) * C::PART + D * 8;
-#pragma unroll
-            for (int h = 0; h < 8; ++h) M[h] = fmaxf(M[h], __ldcg(ps + h));
-        }
-        float o[DPL][8], ws[8];
-#pragma unroll
-        for (int h = 0; h < 8; ++h) {
-            ws[h] = 0.f;
-#pragma unroll
-            for (int dd = 0; dd < DPL; ++dd) o[dd][h] = 0.f;
-        }
-        for (int ww = w0; ww <= w1; ++ww) {
-            const float *ps = a.part + int64_t(seg + ww) * C::PART;
-            float wt[8];
-#pragma unroll
-            for (int h = 0; h < 8; ++h) {
-                const float lse = __ldcg(ps + D * 8 + h);
-                wt[h] = (lse == -INFINITY) ? 0.f : fast_exp2(lse - M[h]);
-                ws[h] += wt[h];
-            }
-#pragma unroll
-            for (int dd = 0; dd < DPL; ++dd) {
-                const float4 x0 = __ldcg(reinterpret_cast<const float4 *>(ps + (lane * DPL + dd) * 8));
-                const float4 x1 = __ldcg(reinterpret_cast<const float4 *>(ps + (lane * DPL + dd) * 8 + 4));
-                o[dd][0] += wt[0] * x0.x; o[dd][1] += wt[1] * x0.y;
-                o[dd][2] += wt[2] * x0.z; o[dd][3] += wt[3] * x0.w;
-                o[dd][4] += wt[4] * x1.x; o[dd][5] += wt[5] * x1.y;
-                o[dd][6] += wt[6] * x1.z; o[dd][7] += wt[7] * x1.w;
-            }
+        for (int kk = 0; kk < NKK; ++kk) {
+            const int ch = ((kk & 3) << 1) + (lane >> 4);
+            const uint32_t addr = kb + (kk >> 2) * C::HALF + rk * 128 + ((ch ^ (lane & 7)) << 4);
+            uint32_t a0, a1, a2, a3;
+            ldsm_x4(addr, a0, a1, a2, a3);
+            if (kk & 1) mma_bf16(sb, a0, a1, a2, a3, qb[kk][0], qb[kk][1]);
+            else mma_bf16(sa, a0, a1, a2, a3, qb[kk][0], qb[kk][1]);
         }
 #pragma unroll
-        for (int h = 0; h < 8; ++h) {
-            if (h >= G) break;
-            const float inv = ws[h] > 0.f ? 1.f / ws[h] : 0.f;
-            uint16_t *dst = a.out + (int64_t(b) * a.Hq + kvh * G + h) * D + lane * DPL;
-            if (DPL == 4) {
-                uint2 v;
-                v.x = pack_bf16x2(o[0][h] * inv, o[1][h] * inv);
-                v.y = pack_bf16x2(o[2 % DPL][h] * inv, o[3 % DPL][h] * inv);
-                *reinterpret_cast<uint2 *>(dst) = v;
-            } else {
-                *reinterpret_cast<uint32_t *>(dst) = pack_bf16x2(o[0][h] * inv, o[1 % DPL][h] * inv);
-            }
-        }
+        for (int e = 0; e < 4; ++e) sc[e] = sa[e] + sb[e];
     };
-
-    auto finalize = [&](int seg, int64_t pb, int64_t pe) {
-        l0 += __shfl_xor_sync(0xffffffffu, l0, 4);
-        l0 += __shfl_xor_sync(0xffffffffu, l0, 8);
-        l0 += __shfl_xor_sync(0xffffffffu, l0, 16);
-        l1 += __shfl_xor_sync(0xffffffffu, l1, 4);
-        l1 += __shfl_xor_sync(0xffffffffu, l1, 8);
-        l1 += __shfl_xor_sync(0xffffffffu, l1, 16);
-        const int b = seg / Hkv, kvh = seg % Hkv;
-        const int n = pre[b + 1] - pre[b];
-        const int64_t s0 = int64_t(Hkv) * pre[b] + int64_t(kvh) * n;
-        const int64_t e0 = s0 + n;
-        const float inv0 = l0 > 0.f ? 1.f / l0 : 0.f;
-        const float inv1 = l1 > 0.f ? 1.f / l1 : 0.f;
-        const int h0 = 2 * q4, h1 = 2 * q4 + 1;
-        if (pb == s0 && pe == e0) {
-            // the whole segment is in this piece: final bf16 output
-            uint16_t *ob = a.out + (int64_t(b) * a.Hq + kvh * G) * D;
-#pragma unroll
-            for (int mt = 0; mt < NKK; ++mt) {
-                const int d = 16 * mt + g;
-                if (h0 < G) {
-                    ob[h0 * D + d] = __bfloat16_as_ushort(__float2bfloat16_rn(acc[mt][0] * inv0));
-                    ob[h0 * D + d + 8] = __bfloat16_as_ushort(__float2bfloat16_rn(acc[mt][2] * inv0));
-                }
-                if (h1 < G) {
-                    ob[h1 * D + d] = __bfloat16_as_ushort(__float2bfloat16_rn(acc[mt][1] * inv1));
-                    ob[h1 * D + d + 8] = __bfloat16_as_ushort(__float2bfloat16_rn(acc[mt][3] * inv1));
-                }
-            }
-            return;
+    // O^T += V^T P^T for one staged block; V lanes of tokens >= nv zeroed
+    auto pv = [&](uint32_t vb, uint32_t p01, uint32_t p23, int nv) {
+        const uint32_t pb0 = movmatrix_trans(p01), pb1 = movmatrix_trans(p23);
+        uint32_t mlo = 0xffffffffu, mhi = 0xffffffffu;
+        if (nv < BS) {
+            const int t0 = 2 * q4;
+            mlo = (t0 < nv ? 0x0000ffffu : 0u) | (t0 + 1 < nv ? 0xffff0000u : 0u);
+            mhi = (t0 + 8 < nv ? 0x0000ffffu : 0u) | (t0 + 9 < nv ? 0xffff0000u : 0u);
         }
-        float *ps = a.part + int64_t(seg + w) * C::PART;
+        const int rv = (lane & 7) + ((lane >> 4) << 3);
 #pragma unroll
         for (int mt = 0; mt < NKK; ++mt) {
-            const int d = 16 * mt + g;
-            __stcg(reinterpret_cast<float2 *>(ps + d * 8 + h0),
-                   make_float2(acc[mt][0] * inv0, acc[mt][1] * inv1));
-            __stcg(reinterpret_cast<float2 *>(ps + (d + 8) * 8 + h0),
-                   make_float2(acc[mt][2] * inv0, acc[mt][3] * inv1));
-        }
-        if (g == 0) {
-            const float lse0 = l0 > 0.f ? m0 + log2f(l0) : -INFINITY;
-            const float lse1 = l1 > 0.f ? m1 + log2f(l1) : -INFINITY;
-            __stcg(reinterpret_cast<float2 *>(ps + D * 8 + h0), make_float2(lse0, lse1));
-        }
-        __threadfence();
-        __syncwarp();
-        int last = 0;
-        if (lane == 0) {
-            const int npieces = int((e0 - 1) / L - s0 / L) + 1;
-            const int old = atomicAdd(a.counters + seg, 1);
-            last = (old == npieces - 1);
-        }
-        last = __shfl_sync(0xffffffffu, last, 0);
-        if (last) {
-            __threadfence();
-            combine(seg, s0, e0);
-            if (lane == 0) a.counters[seg] = 0;
+            const int ch = ((mt & 3) << 1) + ((lane >> 3) & 1);
+            const uint32_t addr = vb + (mt >> 2) * C::HALF + rv * 128 + ((ch ^ (lane & 7)) << 4);
+            uint32_t a0, a1, a2, a3;
+            ldsm_x4_trans(addr, a0, a1, a2, a3);
+            mma_bf16(acc[mt], a0 & mlo, a1 & mlo, a2 & mhi, a3 & mhi, pb0, pb1);
         }
     };
-
-    const float scale_log2 = a.scale_log2;
-    for (int i = 0; i < n_items; ++i) {
-        if (i == wbase + 32) {
-            wa = wb;
-            wbase += 32;
-            wb = locate(wbase + 32 + lane);
-        }
-        const ItemInfo it = item(i);
-        if (it.seg != cur_seg) {
-            if (cur_seg >= 0) finalize(cur_seg, piece_begin, pos0 + i);
-            cur_seg = it.seg;
-            piece_begin = pos0 + i;
-            load_q(it.seg);
-        }
-        const int st = i % S;
-        if (!mbar_wait_bounded(my_bars + st * 8, (i / S) & 1, kWaitLimitNs)) {
-            // give up: record it, let the copies already issued land, leave
-            if (lane == 0) atomicOr(a.status, kStatusTimeout);
-            for (int k = i + 1; k < min(n_items, i + S); ++k)
-                mbar_wait_bounded(my_bars + (k % S) * 8, (k / S) & 1, kWaitLimitNs);
-            return;
-        }
-        const int nv = it.nv;
-        if (nv > 0) {
-            const uint32_t kb = my_stages + st * C::STAGE;
-            const uint32_t vb = kb + C::KT;
-            // ---- S^T = K Q^T (16 tokens x 8 heads)
-            float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
-            const int rk = (lane & 7) + (((lane >> 3) & 1) << 3);
-#pragma unroll
-            for (int kk = 0; kk < NKK; ++kk) {
-                const int ch = ((kk & 3) << 1) + (lane >> 4);
-                const uint32_t addr = kb + (kk >> 2) * C::HALF + rk * 128 + ((ch ^ (lane & 7)) << 4);
-                uint32_t a0, a1, a2, a3;
-                ldsm_x4(addr, a0, a1, a2, a3);
-                if (kk & 1) mma_bf16(sb, a0, a1, a2, a3, qb[kk][0], qb[kk][1]);
-                else mma_bf16(sa, a0, a1, a2, a3, qb[kk][0], qb[kk][1]);
+    // wait for an item's stage (skipped once the CTA has given up); returns
+    // the item's valid token count
+    auto wait_full = [&](int k) -> int {
+        if (flags[0]) return 0;
+        if (!mbar_wait_bounded(full_bar + (k % S) * 8, (k / S) & 1, kWaitLimitNs)) {
+            if (lane == 0) {
+                flags[0] = 1;
+                atomicOr(a.status, kStatusTimeout);
             }
-            // ---- online softmax (log2 domain); rows g and g+8, heads h0 and h1
-            const float x0 = (g < nv) ? (sa[0] + sb[0]) * scale_log2 : -INFINITY;
-            const float x1 = (g < nv) ? (sa[1] + sb[1]) * scale_log2 : -INFINITY;
-            const float x2 = (g + 8 < nv) ? (sa[2] + sb[2]) * scale_log2 : -INFINITY;
-            const float x3 = (g + 8 < nv) ? (sa[3] + sb[3]) * scale_log2 : -INFINITY;
-            float bm0 = fmaxf(x0, x2), bm1 = fmaxf(x1, x3);
+            return 0;
+        }
+        return info[k % S].y;
+    };
+    // one online-softmax step over up to two staged blocks (nv == 0: no block)
+    auto step = [&](int ka, int nva, int kb_, int nvb) {
+        const uint32_t s0a = base + (ka % S) * C::STAGE;
+        const uint32_t s1a = base + (kb_ % S) * C::STAGE;
+        float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
+        if (nva > 0) qk(s0a, s0);
+        if (nvb > 0) qk(s1a, s1);
+        const float x0 = (g < nva) ? s0[0] * scale_log2 : -INFINITY;
+        const float x1 = (g < nva) ? s0[1] * scale_log2 : -INFINITY;
+        const float x2 = (g + 8 < nva) ? s0[2] * scale_log2 : -INFINITY;
+        const float x3 = (g + 8 < nva) ? s0[3] * scale_log2 : -INFINITY;
+        const float y0 = (g < nvb) ? s1[0] * scale_log2 : -INFINITY;
+        const float y1 = (g < nvb) ? s1[1] * scale_log2 : -INFINITY;
+        const float y2 = (g + 8 < nvb) ? s1[2] * scale_log2 : -INFINITY;
+        const float y3 = (g + 8 < nvb) ? s1[3] * scale_log2 : -INFINITY;
+        float bm0 = fmaxf(fmaxf(x0, x2), fmaxf(y0, y2));
+        float bm1 = fmaxf(fmaxf(x1, x3), fmaxf(y1, y3));
 #pragma unroll
-            for (int o = 4; o < 32; o <<= 1) {
-                bm0 = fmaxf(bm0, __shfl_xor_sync(0xffffffffu, bm0, o));
-                bm1 = fmaxf(bm1, __shfl_xor_sync(0xffffffffu, bm1, o));
-            }
-            const float mn0 = fmaxf(m0, bm0), mn1 = fmaxf(m1, bm1);
-            const float r0 = (mn0 == -INFINITY) ? 0.f : mn0;
-            const float r1 = (mn1 == -INFINITY) ? 0.f : mn1;
-            const float al0 = fast_exp2(m0 - r0), al1 = fast_exp2(m1 - r1);
-            const uint32_t p01 = pack_bf16x2(fast_exp2(x0 - r0), fast_exp2(x1 - r1));
-            const uint32_t p23 = pack_bf16x2(fast_exp2(x2 - r0), fast_exp2(x3 - r1));
-            l0 = l0 * al0 + (bf16_lo(p01) + bf16_lo(p23));
-            l1 = l1 * al1 + (bf16_hi(p01) + bf16_hi(p23));
-            m0 = mn0;
-            m1 = mn1;
+        for (int o = 4; o < 32; o <<= 1) {
+            bm0 = fmaxf(bm0, __shfl_xor_sync(0xffffffffu, bm0, o));
+            bm1 = fmaxf(bm1, __shfl_xor_sync(0xffffffffu, bm1, o));
+        }
+        const float mn0 = fmaxf(m0, bm0), mn1 = fmaxf(m1, bm1);
+        const float r0 = (mn0 == -INFINITY) ? 0.f : mn0;
+        const float r1 = (mn1 == -INFINITY) ? 0.f : mn1;
+        const bool grow = (mn0 != m0) || (mn1 != m1);
+        const float al0 = fast_exp2(m0 - r0), al1 = fast_exp2(m1 - r1);
+        const uint32_t p01 = pack_bf16x2(fast_exp2(x0 - r0), fast_exp2(x1 - r1));
+        const uint32_t p23 = pack_bf16x2(fast_exp2(x2 - r0), fast_exp2(x3 - r1));
+        const uint32_t q01 = pack_bf16x2(fast_exp2(y0 - r0), fast_exp2(y1 - r1));
+        const uint32_t q23 = pack_bf16x2(fast_exp2(y2 - r0), fast_exp2(y3 - r1));
+        l0 = l0 * al0 + ((bf16_lo(p01) + bf16_lo(p23)) + (bf16_lo(q01) + bf16_lo(q23)));
+        l1 = l1 * al1 + ((bf16_hi(p01) + bf16_hi(p23)) + (bf16_hi(q01) + bf16_hi(q23)));
+        m0 = mn0;
+        m1 = mn1;
+        if (__any_sync(0xffffffffu, grow)) {
 #pragma unroll
             for (int mt = 0; mt < NKK; ++mt) {
                 acc[mt][0] *= al0;
@@ -408,32 +416,216 @@ __global__ void __launch_bounds__(DecodeCfg<D>::NW * 32, 1)
                 acc[mt][2] *= al0;
                 acc[mt][3] *= al1;
             }
-            const uint32_t pb0 = movmatrix_trans(p01), pb1 = movmatrix_trans(p23);
-            // ---- O^T += V^T P^T; V lanes of tokens >= nv zeroed
-            uint32_t mlo = 0xffffffffu, mhi = 0xffffffffu;
-            if (nv < BS) {
-                const int t0 = 2 * q4;
-                mlo = (t0 < nv ? 0x0000ffffu : 0u) | (t0 + 1 < nv ? 0xffff0000u : 0u);
-                mhi = (t0 + 8 < nv ? 0x0000ffffu : 0u) | (t0 + 9 < nv ? 0xffff0000u : 0u);
-            }
-            const int rv = (lane & 7) + ((lane >> 4) << 3);
+        }
+        if (nva > 0) pv(s0a + C::KT, p01, p23, nva);
+        if (nvb > 0) pv(s1a + C::KT, q01, q23, nvb);
+    };
+
+    // merge the CTA pieces of segment `seg` (run by every consumer thread of
+    // the last CTA to arrive); one float4 of the [D][8] output per thread,
+    // pieces merged in order with a running max
+    auto combine = [&](int seg, int64_t s0, int64_t e0) {
+        const int w0 = int(s0 / L), np = int((e0 - 1) / L) - w0 + 1;
+        const float *pb = a.part + int64_t(seg + w0) * C::PART;
+        for (int slot = ctid; slot < 2 * D; slot += NC * 32) {
+        const int d = slot >> 1, h4 = (slot & 1) * 4;
+        float M[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+        float W[4] = {0.f, 0.f, 0.f, 0.f}, O[4] = {0.f, 0.f, 0.f, 0.f};
+        constexpr int U = 4;
+        for (int i0 = 0; i0 < np; i0 += U) {
+            float4 lx[U], xv[U];
 #pragma unroll
-            for (int mt = 0; mt < NKK; ++mt) {
-                const int ch = ((mt & 3) << 1) + ((lane >> 3) & 1);
-                const uint32_t addr = vb + (mt >> 2) * C::HALF + rv * 128 + ((ch ^ (lane & 7)) << 4);
-                uint32_t a0, a1, a2, a3;
-                ldsm_x4_trans(addr, a0, a1, a2, a3);
-                mma_bf16(acc[mt], a0 & mlo, a1 & mlo, a2 & mhi, a3 & mhi, pb0, pb1);
+            for (int u = 0; u < U; ++u) {
+                const float *ps = pb + int64_t(min(i0 + u, np - 1)) * C::PART;
+                lx[u] = __ldcg(reinterpret_cast<const float4 *>(ps + D * 8 + h4));
+                xv[u] = __ldcg(reinterpret_cast<const float4 *>(ps + d * 8 + h4));
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                if (i0 + u >= np) break;
+                const float l4[4] = {lx[u].x, lx[u].y, lx[u].z, lx[u].w};
+                const float x4[4] = {xv[u].x, xv[u].y, xv[u].z, xv[u].w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    if (l4[e] == -INFINITY) continue;
+                    if (l4[e] > M[e]) {
+                        const float sc = fast_exp2(M[e] - l4[e]);  // 0 when M was -inf
+                        W[e] *= sc;
+                        O[e] *= sc;
+                        M[e] = l4[e];
+                    }
+                    const float wt = fast_exp2(l4[e] - M[e]);
+                    W[e] += wt;
+                    O[e] += wt * x4[e];
+                }
             }
         }
-        __syncwarp();
-        const int k = i + S;
-        if (k < n_items) {
-            const ItemInfo nx = item(k);
-            if (lane == 0) issue(k, nx);
+        const int b = seg / Hkv, kvh = seg % Hkv;
+        uint16_t *ob = a.out + (int64_t(b) * a.Hq + kvh * G) * D + d;
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+            if (h4 + e < G)
+                ob[(h4 + e) * D] = __bfloat16_as_ushort(__float2bfloat16_rn(W[e] > 0.f ? O[e] / W[e] : 0.f));
+        }
+    };
+
+    // merge the consumer warps' states of one segment, then write the CTA's
+    // piece (final output, or partial + arrival)
+    auto merge = [&](int seg, int64_t s0, int64_t e0, bool whole) {
+        l0 += __shfl_xor_sync(0xffffffffu, l0, 4);
+        l0 += __shfl_xor_sync(0xffffffffu, l0, 8);
+        l0 += __shfl_xor_sync(0xffffffffu, l0, 16);
+        l1 += __shfl_xor_sync(0xffffffffu, l1, 4);
+        l1 += __shfl_xor_sync(0xffffffffu, l1, 8);
+        l1 += __shfl_xor_sync(0xffffffffu, l1, 16);
+        float *my = scr + c_id * C::SCR;
+        const int h0 = 2 * q4;
+#pragma unroll
+        for (int mt = 0; mt < NKK; ++mt) {
+            const int d = 16 * mt + g;
+            *reinterpret_cast<float2 *>(my + d * 8 + h0) = make_float2(acc[mt][0], acc[mt][1]);
+            *reinterpret_cast<float2 *>(my + (d + 8) * 8 + h0) = make_float2(acc[mt][2], acc[mt][3]);
+        }
+        if (g == 0) {
+            *reinterpret_cast<float2 *>(my + D * 8 + h0) = make_float2(m0, m1);
+            *reinterpret_cast<float2 *>(my + D * 8 + 8 + h0) = make_float2(l0, l1);
+        }
+        consumer_sync(NC * 32);
+        const int b = seg / Hkv, kvh = seg % Hkv;
+        for (int slot = ctid; slot < 2 * D; slot += NC * 32) {
+            const int d = slot >> 1, h4 = (slot & 1) * 4;
+            float M[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+            for (int cc = 0; cc < NC; ++cc) {
+                const float4 mm = *reinterpret_cast<const float4 *>(scr + cc * C::SCR + D * 8 + h4);
+                M[0] = fmaxf(M[0], mm.x); M[1] = fmaxf(M[1], mm.y);
+                M[2] = fmaxf(M[2], mm.z); M[3] = fmaxf(M[3], mm.w);
+            }
+            float Ls[4] = {0.f, 0.f, 0.f, 0.f}, O[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int cc = 0; cc < NC; ++cc) {
+                const float *sc = scr + cc * C::SCR;
+                const float4 mm = *reinterpret_cast<const float4 *>(sc + D * 8 + h4);
+                const float4 ll = *reinterpret_cast<const float4 *>(sc + D * 8 + 8 + h4);
+                const float4 xx = *reinterpret_cast<const float4 *>(sc + d * 8 + h4);
+                const float m4[4] = {mm.x, mm.y, mm.z, mm.w}, l4[4] = {ll.x, ll.y, ll.z, ll.w};
+                const float x4[4] = {xx.x, xx.y, xx.z, xx.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float wt = (m4[e] == -INFINITY) ? 0.f : fast_exp2(m4[e] - M[e]);
+                    Ls[e] += wt * l4[e];
+                    O[e] += wt * x4[e];
+                }
+            }
+            if (whole) {
+                uint16_t *ob = a.out + (int64_t(b) * a.Hq + kvh * G) * D + d;
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    if (h4 + e < G)
+                        ob[(h4 + e) * D] =
+                            __bfloat16_as_ushort(__float2bfloat16_rn(Ls[e] > 0.f ? O[e] / Ls[e] : 0.f));
+            } else {
+                float *ps = a.part + int64_t(seg + blockIdx.x) * C::PART;
+                float r[4], lse[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    r[e] = Ls[e] > 0.f ? O[e] / Ls[e] : 0.f;
+                    lse[e] = Ls[e] > 0.f ? M[e] + log2f(Ls[e]) : -INFINITY;
+                }
+                __stcg(reinterpret_cast<float4 *>(ps + d * 8 + h4), make_float4(r[0], r[1], r[2], r[3]));
+                if (d == 0)
+                    __stcg(reinterpret_cast<float4 *>(ps + D * 8 + h4),
+                           make_float4(lse[0], lse[1], lse[2], lse[3]));
+            }
+        }
+        consumer_sync(NC * 32);  // partial written by every thread; scratch free again
+        if (whole) return;
+        if (ctid == 0) {
+            // release the CTA's partial (ordered after the barrier) and count it
+            __threadfence();
+            const int npieces = int((e0 - 1) / L - s0 / L) + 1;
+            const int old = atomicAdd(a.counters + seg, 1);
+            const int last = (old == npieces - 1);
+            if (last) __threadfence();  // acquire the other pieces before the merge
+            flags[1] = last;
+        }
+        consumer_sync(NC * 32);
+        if (flags[1]) {
+            combine(seg, s0, e0);
+            if (ctid == 0) a.counters[seg] = 0;
+        }
+    };
+
+    // walk the segments of this CTA's range in order; every consumer warp
+    // takes part in every segment's merge
+    int64_t p = pos0;
+    int b = find_seq(p);
+    int kvh = int((p - int64_t(Hkv) * pre[b]) / (pre[b + 1] - pre[b]));
+    while (p < pos1) {
+        const int n = pre[b + 1] - pre[b];
+        const int seg = b * Hkv + kvh;
+        const int64_t s0 = int64_t(Hkv) * pre[b] + int64_t(kvh) * n;
+        const int64_t e0 = s0 + n;
+        const int ks0 = int(p - pos0), ks1 = int(min(e0, pos1) - pos0);
+        load_q(seg);
+        // item pairs (2q, 2q+1) of this segment owned by this warp: q % NC == c_id
+        int q = ks0 >> 1;
+        q += (c_id - q % NC + NC) % NC;
+        for (; 2 * q < ks1; q += NC) {
+            const int ka = max(2 * q, ks0);
+            const int kb = min(2 * q + 1, ks1 - 1);
+            const int nva = wait_full(ka);
+            const int nvb = (kb > ka) ? wait_full(kb) : 0;
+            if (!traced_first) {
+                traced_first = true;
+                if (c_id == 0) PA_TRACE(2);
+            }
+            if (nva > 0 || nvb > 0) step(ka, nva, kb, nvb);
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(empty_bar + (ka % S) * 8);
+                if (kb > ka) mbar_arrive(empty_bar + (kb % S) * 8);
+            }
+        }
+        const bool whole = (s0 >= pos0) && (e0 <= pos1);
+        if (e0 >= pos1) PA_TRACE(3);
+        merge(seg, s0, e0, whole);
+        p = min(e0, pos1);
+        if (++kvh == Hkv) {
+            kvh = 0;
+            do {
+                ++b;
+            } while (b < B && pre[b + 1] == pre[b]);
         }
     }
-    finalize(cur_seg, piece_begin, pos1);
+    PA_TRACE(4);
+}
+
+template <int D>
+cudaError_t geometry_t(DecodeGeometry *g) {
+    using C = DecodeCfg<D>;
+    cudaError_t e;
+    int dev = 0, sms = 0, per_sm = 0, optin = 0;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+    if ((e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev)) != cudaSuccess)
+        return e;
+    // shared memory for the largest batch that fits (the ring is fixed; the
+    // per-sequence prefix grows with the batch)
+    const size_t smem = C::smem_bytes(kMaxBatch) < size_t(optin) ? C::smem_bytes(kMaxBatch) : size_t(optin);
+    if (smem < C::smem_bytes(1)) return cudaErrorInvalidConfiguration;
+    e = cudaFuncSetAttribute(decode_kernel<D, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(decode_kernel<D, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+    if (e != cudaSuccess) return e;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_kernel<D, false>, C::THREADS, smem);
+    if (e != cudaSuccess) return e;
+    if (per_sm < 1) return cudaErrorInvalidConfiguration;
+    g->grid = sms * per_sm;
+    g->warps = C::NC + 1;
+    g->workers = g->grid;
+    g->smem = smem;
+    return cudaSuccess;
 }
 
 template <int D, bool SPARSE>
@@ -443,31 +635,9 @@ cudaError_t launch_t(const CUtensorMap &tm_k, const CUtensorMap &tm_v, const Dec
     DecodeGeometry geo;
     cudaError_t e = decode_geometry(D, &geo);
     if (e != cudaSuccess) return e;
-    const size_t smem = C::smem_bytes(a.B);
-    decode_kernel<D, SPARSE><<<geo.grid, C::NW * 32, smem, stream>>>(tm_k, tm_v, a);
+    if (C::smem_bytes(a.B) > geo.smem) return cudaErrorInvalidConfiguration;  // batch too large
+    decode_kernel<D, SPARSE><<<geo.grid, C::THREADS, C::smem_bytes(a.B), stream>>>(tm_k, tm_v, a);
     return cudaGetLastError();
-}
-
-template <int D>
-cudaError_t geometry_t(DecodeGeometry *g) {
-    using C = DecodeCfg<D>;
-    const size_t smem = C::smem_bytes(kMaxBatch);
-    cudaError_t e;
-    e = cudaFuncSetAttribute(decode_kernel<D, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(decode_kernel<D, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
-    if (e != cudaSuccess) return e;
-    int dev = 0, sms = 0, per_sm = 0;
-    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
-    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_kernel<D, false>, C::NW * 32, smem);
-    if (e != cudaSuccess) return e;
-    if (per_sm < 1) return cudaErrorInvalidConfiguration;
-    g->grid = sms * per_sm;
-    g->warps = C::NW;
-    g->workers = g->grid * C::NW;
-    g->smem = smem;
-    return cudaSuccess;
 }
 
 constexpr int kMaxDevices = 64;
@@ -493,12 +663,20 @@ cudaError_t decode_geometry(int head_dim, DecodeGeometry *g) {
     return cudaSuccess;
 }
 
-size_t decode_workspace_bytes(int B, int Hkv, int head_dim, int workers) {
+size_t decode_trace_offset(int B, int Hkv, int head_dim, int workers) {
     const size_t segs = size_t(B) * Hkv;
     const size_t head = 256;                                        // status word + padding
     const size_t counters = (segs * 4 + 255) / 256 * 256;
     const size_t part = (segs + size_t(workers)) * size_t(head_dim * 8 + 8) * 4;
     return head + counters + part;
+}
+
+size_t decode_workspace_bytes(int B, int Hkv, int head_dim, int workers) {
+    size_t bytes = decode_trace_offset(B, Hkv, head_dim, workers);
+#ifdef PA_DECODE_TRACE
+    bytes += size_t(workers) * 8 * sizeof(uint64_t);
+#endif
+    return bytes;
 }
 
 cudaError_t launch_decode(const CUtensorMap &tm_k, const CUtensorMap &tm_v, const DecodeArgs &a,

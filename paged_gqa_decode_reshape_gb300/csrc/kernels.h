@@ -21,6 +21,7 @@ struct DecodeArgs {
     float *part;                // [B*Hkv + W][D*8 + 8] partial outputs and lse (log2 domain)
     int32_t *counters;          // [B*Hkv] arrival counters (zero between calls)
     int32_t *status;            // workspace status word
+    uint64_t *trace;            // per-warp timeline (tuning builds only), or null
     int64_t NB;
     int MBS, topk, B, Hq, Hkv, G;
     float scale_log2;           // softmax scale * log2(e)
@@ -31,11 +32,12 @@ struct DecodeGeometry {
     int grid;          // CTAs (persistent)
     int warps;         // warps per CTA
     int workers;       // grid * warps
-    size_t smem;       // dynamic shared memory bytes for B = kMaxBatch
+    size_t smem;       // dynamic shared memory limit set on the kernel
 };
 
 cudaError_t decode_geometry(int head_dim, DecodeGeometry *g);
 size_t decode_workspace_bytes(int B, int Hkv, int head_dim, int workers);
+size_t decode_trace_offset(int B, int Hkv, int head_dim, int workers);
 cudaError_t launch_decode(const CUtensorMap &tm_k, const CUtensorMap &tm_v, const DecodeArgs &a,
                           int head_dim, bool sparse, cudaStream_t stream);
 

@@ -87,6 +87,11 @@ __global__ void __launch_bounds__(kScoreWarps * 32) quest_score_kernel(
     int j = int(r - int64_t(kvh) * n);
 
     while (pos < pos1) {
+        const int j_end = int(min(int64_t(n), int64_t(j) + (pos1 - pos)));
+        const int32_t *bt_row = bt + int64_t(b) * MBS;
+        float *srow = scores + (int64_t(b) * Hkv + kvh) * MBS;
+        // first chunk's block-table entries, in flight while P/N are formed
+        int ph_next = (j + lane < j_end) ? __ldg(bt_row + j + lane) : -1;
         // P_d, N_d of this (b, kvh) for this lane's dims
         float P[C], N[C];
 #pragma unroll
@@ -96,20 +101,25 @@ __global__ void __launch_bounds__(kScoreWarps * 32) quest_score_kernel(
         }
         for (int gg = 0; gg < G; ++gg) {
             const uint16_t *qr = q + (int64_t(b) * Hq + int64_t(kvh) * G + gg) * D + lane * C;
+            uint32_t qw[C / 2];
+            if (C == 4) {
+                const uint2 v2 = __ldg(reinterpret_cast<const uint2 *>(qr));
+                qw[0] = v2.x;
+                qw[C / 2 - 1] = v2.y;
+            } else {
+                qw[0] = __ldg(reinterpret_cast<const uint32_t *>(qr));
+            }
 #pragma unroll
             for (int c = 0; c < C; ++c) {
-                const float v = __uint_as_float(uint32_t(__ldg(qr + c)) << 16);
+                const float v = (c & 1) ? bf16_hi(qw[c >> 1]) : bf16_lo(qw[c >> 1]);
                 P[c] = __fadd_rn(P[c], v > 0.f ? v : 0.f);
                 N[c] = __fadd_rn(N[c], v < 0.f ? v : 0.f);
             }
         }
-        const int j_end = int(min(int64_t(n), int64_t(j) + (pos1 - pos)));
-        const int32_t *bt_row = bt + int64_t(b) * MBS;
-        float *srow = scores + (int64_t(b) * Hkv + kvh) * MBS;
         for (int j0 = j; j0 < j_end; j0 += 32) {
             // physical blocks of up to 32 items, one per lane
-            const int jl = j0 + lane;
-            const int ph_l = jl < j_end ? __ldg(bt_row + jl) : -1;
+            const int ph_l = ph_next;
+            if (j0 + 32 < j_end) ph_next = (j0 + 32 + lane < j_end) ? __ldg(bt_row + j0 + 32 + lane) : -1;
             const int cnt = min(32, j_end - j0);
             for (int i0 = 0; i0 < cnt; i0 += 4) {
                 float sc[4];
@@ -187,12 +197,15 @@ __device__ __forceinline__ int block_rank(bool flag, int *warp_cnt, int &total) 
     return before + in_warp;
 }
 
+constexpr int kTopkSmemKeys = 8192;  // keys cached in shared memory (32 KiB)
+
 __global__ void __launch_bounds__(kTopkThreads) quest_topk_kernel(
     int32_t *__restrict__ sel, const float *__restrict__ scores, int MBS,
     const int32_t *__restrict__ ctx, int Hkv, int BS, int topk) {
     __shared__ int hist[256];
     __shared__ int warp_cnt[kTopkThreads / 32];
     __shared__ int sh_digit, sh_above;
+    __shared__ uint32_t keys[kTopkSmemKeys];
     const int seg = blockIdx.x;
     const int b = seg / Hkv;
     const int tid = threadIdx.x, lane = tid & 31;
@@ -204,13 +217,18 @@ __global__ void __launch_bounds__(kTopkThreads) quest_topk_kernel(
         for (int i = tid; i < topk; i += kTopkThreads) out[i] = i < n ? i : -1;
         return;
     }
+    // totalOrder keys of the segment's scores: in shared memory when they fit
+    const bool cached = n <= kTopkSmemKeys;
+    if (cached)
+        for (int j = tid; j < n; j += kTopkThreads) keys[j] = f32_order_key(__ldcg(srow + j));
+    auto key_of = [&](int j) -> uint32_t { return cached ? keys[j] : f32_order_key(__ldcg(srow + j)); };
     uint32_t prefix = 0, mask = 0;
     int k = topk;
     for (int shift = 24; shift >= 0; shift -= 8) {
         hist[tid] = 0;  // kTopkThreads == 256 bins
         __syncthreads();
         for (int j = tid; j < n; j += kTopkThreads) {
-            const uint32_t u = f32_order_key(srow[j]);
+            const uint32_t u = key_of(j);
             if ((u & mask) == prefix) atomicAdd(&hist[(u >> shift) & 255u], 1);
         }
         __syncthreads();
@@ -252,7 +270,7 @@ __global__ void __launch_bounds__(kTopkThreads) quest_topk_kernel(
     int carry_eq = 0, carry_pos = 0;
     for (int j0 = 0; j0 < n; j0 += kTopkThreads) {
         const int j = j0 + tid;
-        const uint32_t u = j < n ? f32_order_key(srow[j]) : 0u;
+        const uint32_t u = j < n ? key_of(j) : 0u;
         const bool gt = j < n && u > prefix;
         const bool eq = j < n && u == prefix;
         int tot_eq;

@@ -208,7 +208,8 @@ def test_out_of_range_metadata_never_faults():
     """Bad slots and block-table entries are skipped, not followed; the
     checker counts them."""
     import paged_gqa_decode_reshape_gb300 as pg
-    w = workloads.make("tiny")
+    # no poison: the token whose slot is invalid stays unwritten inside ctx
+    w = workloads.make("tiny", poison=False)
     w.slot_mapping[0] = w.NB * w.BS + 3            # past the pool
     w.block_tables[1, 2] = w.NB + 100               # past the pool
     w.block_tables[1, 4] = -5
