@@ -116,6 +116,31 @@ PA_API int pa_decode(pa_bf16 *out, const pa_bf16 *query,
               int num_kv_heads, int head_dim, int block_size, int64_t num_blocks,
               float scale, void *workspace, size_t workspace_bytes, void *stream);
 
+/* Size of the fixed scratch buffer behind pa_decode_no_alloc (8 MiB). */
+#define PA_NO_ALLOC_SCRATCH_BYTES (8u << 20)
+
+/* pa_decode for callers that may not allocate device memory at all (no
+ * counterpart on the pages; an addition of this library). Examples: a plugin
+ * inside a serving engine that is handed only its input and output tensors
+ * while the engine keeps the rest of HBM for its KV-cache pool, or a
+ * latency-critical loop where cudaMalloc/cudaFree are not allowed because
+ * they can synchronise the device. Same arguments and result as pa_decode,
+ * without a workspace: the scratch is a PA_NO_ALLOC_SCRATCH_BYTES buffer
+ * compiled into the library, present on every GPU that loads it until the
+ * process exits. The call allocates nothing. Its first call on a device
+ * looks up that buffer's device address (make that first call before any
+ * stream capture). Every call clears the buffer's status word and counters on
+ * `stream` and then runs pa_decode's kernel; all calls share the one buffer,
+ * so calls that overlap on the GPU race. Returns PA_ERR_WORKSPACE when the
+ * batch and head shape need more scratch than the buffer holds (about
+ * B * Hkv + number_of_SMs partial slots of (8 * head_dim + 8) floats). */
+PA_API int pa_decode_no_alloc(pa_bf16 *out, const pa_bf16 *query,
+                              const pa_bf16 *key_cache, const pa_bf16 *value_cache,
+                              const int32_t *block_tables, int max_blocks_per_seq,
+                              const int32_t *context_lens, int batch, int num_q_heads,
+                              int num_kv_heads, int head_dim, int block_size, int64_t num_blocks,
+                              float scale, void *stream);
+
 /* Quest metadata update for the tokens of one ReshapeAndCache call. For each
  * physical block touched by a valid slot: if one of the call's tokens lands
  * at offset 0 (the block starts fresh) the block's kmin/kmax become the
