@@ -153,6 +153,18 @@ PA_API int quest_update_meta(pa_bf16 *kmin, pa_bf16 *kmax, const pa_bf16 *key,
                       int num_kv_heads, int head_dim, int block_size,
                       int64_t num_blocks, void *stream);
 
+/* The write path in one launch: pa_reshape_and_cache followed by
+ * quest_update_meta on the same tokens, with identical results (the fused
+ * KV-update step of "Day-0 porting of a sparse-attention model", section on
+ * the prefill/decode pipeline, where the cache update is folded into one
+ * kernel launch). Same argument rules as the two calls it replaces. */
+PA_API int quest_reshape_and_cache(const pa_bf16 *key, const pa_bf16 *value,
+                                   pa_bf16 *key_cache, pa_bf16 *value_cache,
+                                   pa_bf16 *kmin, pa_bf16 *kmax,
+                                   const int64_t *slot_mapping, int64_t num_tokens,
+                                   int num_kv_heads, int head_dim, int block_size,
+                                   int64_t num_blocks, void *stream);
+
 /* Quest metadata from scratch: for every sequence b and logical block
  * j < ceil(context_lens[b] / BS), kmin/kmax of physical block
  * block_tables[b][j] = elementwise min/max of K over the block's valid tokens

@@ -30,7 +30,8 @@ _lock = threading.Lock()
 
 __all__ = [
     "PagedDecodeError", "load_library", "pa_status_string", "pa_reshape_and_cache",
-    "pa_decode_workspace_size", "pa_decode", "quest_update_meta", "quest_rebuild_meta",
+    "pa_decode_workspace_size", "pa_decode", "quest_update_meta", "quest_reshape_and_cache",
+    "quest_rebuild_meta",
     "quest_select_workspace_size", "quest_select_topk", "quest_sparse_decode",
     "pa_workspace_status", "pa_check_metadata", "Workspace",
 ]
@@ -71,6 +72,8 @@ def load_library(path: Optional[str] = None):
         L.pa_decode.restype = i32
         L.quest_update_meta.argtypes = [vp, vp, vp, vp, i64, i32, i32, i32, i64, vp]
         L.quest_update_meta.restype = i32
+        L.quest_reshape_and_cache.argtypes = [vp, vp, vp, vp, vp, vp, vp, i64, i32, i32, i32, i64, vp]
+        L.quest_reshape_and_cache.restype = i32
         L.quest_rebuild_meta.argtypes = [vp, vp, vp, vp, i32, vp, i32, i32, i32, i32, i64, vp]
         L.quest_rebuild_meta.restype = i32
         L.quest_select_workspace_size.argtypes = [i32, i32, i32]
@@ -248,6 +251,30 @@ def quest_update_meta(kmin: torch.Tensor, kmax: torch.Tensor, key: torch.Tensor,
     _check("quest_update_meta",
            L.quest_update_meta(_ptr(kmin), _ptr(kmax), _ptr(key), _ptr(slot_mapping), T, Hkv, D,
                                int(block_size), NB, _stream(dev)))
+
+
+def quest_reshape_and_cache(key: torch.Tensor, value: torch.Tensor, key_cache: torch.Tensor,
+                            value_cache: torch.Tensor, kmin: torch.Tensor, kmax: torch.Tensor,
+                            slot_mapping: torch.Tensor) -> None:
+    """The write path in one launch: pa_reshape_and_cache then quest_update_meta."""
+    L = load_library()
+    _need(key_cache, "key_cache", torch.bfloat16, 4)
+    dev = key_cache.device
+    _need(value_cache, "value_cache", torch.bfloat16, 4, dev)
+    _need(kmin, "kmin", torch.bfloat16, 3, dev)
+    _need(kmax, "kmax", torch.bfloat16, 3, dev)
+    _need(key, "key", torch.bfloat16, 3, dev)
+    _need(value, "value", torch.bfloat16, 3, dev)
+    _need(slot_mapping, "slot_mapping", torch.int64, 1, dev)
+    NB, BS, Hkv, D = key_cache.shape
+    T = slot_mapping.shape[0]
+    if (value_cache.shape != key_cache.shape or key.shape != (T, Hkv, D) or value.shape != key.shape
+            or kmin.shape != (NB, Hkv, D) or kmax.shape != kmin.shape):
+        raise ValueError("shape mismatch between key/value, the caches and the metadata")
+    _check("quest_reshape_and_cache",
+           L.quest_reshape_and_cache(_ptr(key), _ptr(value), _ptr(key_cache), _ptr(value_cache),
+                                     _ptr(kmin), _ptr(kmax), _ptr(slot_mapping), T, Hkv, D, BS, NB,
+                                     _stream(dev)))
 
 
 def quest_rebuild_meta(kmin: torch.Tensor, kmax: torch.Tensor, key_cache: torch.Tensor,

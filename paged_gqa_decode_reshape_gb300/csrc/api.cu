@@ -223,6 +223,26 @@ int quest_update_meta(pa_bf16 *kmin, pa_bf16 *kmax, const pa_bf16 *key,
     return e == cudaSuccess ? PA_OK : cuda_fail(e);
 }
 
+int quest_reshape_and_cache(const pa_bf16 *key, const pa_bf16 *value, pa_bf16 *key_cache,
+                            pa_bf16 *value_cache, pa_bf16 *kmin, pa_bf16 *kmax,
+                            const int64_t *slot_mapping, int64_t num_tokens, int num_kv_heads,
+                            int head_dim, int block_size, int64_t num_blocks, void *stream) {
+    if (num_tokens < 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 || num_blocks <= 0)
+        return PA_ERR_INVALID_ARG;
+    if (num_tokens == 0) return PA_OK;
+    if (!key || !value || !key_cache || !value_cache || !kmin || !kmax || !slot_mapping)
+        return PA_ERR_INVALID_ARG;
+    if (!shape_supported(head_dim, block_size)) return PA_ERR_UNSUPPORTED;
+    if (num_tokens > (int64_t(1) << 31) - 1) return PA_ERR_UNSUPPORTED;
+    if (!aligned16(key) || !aligned16(value) || !aligned16(key_cache) || !aligned16(value_cache) ||
+        !aligned16(kmin) || !aligned16(kmax))
+        return PA_ERR_INVALID_ARG;
+    const cudaError_t e = launch_write_quest(key_cache, value_cache, kmin, kmax, key, value,
+                                             slot_mapping, num_tokens, num_kv_heads, head_dim,
+                                             block_size, num_blocks, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? PA_OK : cuda_fail(e);
+}
+
 int quest_rebuild_meta(pa_bf16 *kmin, pa_bf16 *kmax, const pa_bf16 *key_cache,
                        const int32_t *block_tables, int max_blocks_per_seq,
                        const int32_t *context_lens, int batch, int num_kv_heads, int head_dim,

@@ -9,7 +9,8 @@
 //
 // Quest metadata: per physical block and KV head, elementwise min/max of K
 // over the block's tokens, compared in IEEE totalOrder (-0 < +0) so the result
-// is a unique bit pattern whatever the order of the tokens.
+// is a unique bit pattern whatever the order of the tokens. The fused write
+// path does both in one launch.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -22,6 +23,8 @@ namespace {
 __global__ void __launch_bounds__(128) reshape_and_cache_kernel(
     const uint4 *__restrict__ key, const uint4 *__restrict__ value, uint4 *__restrict__ kc,
     uint4 *__restrict__ vc, const int64_t *__restrict__ slots, int row_vecs, int BS, int64_t NB) {
+    pdl_trigger();
+    pdl_wait();
     const int64_t t = blockIdx.x;
     const int64_t slot = __ldg(slots + t);
     if (slot < 0 || slot >= NB * BS) return;  // padding token, or outside the pool
@@ -58,20 +61,18 @@ __device__ __forceinline__ void minmax8(uint4 &lo, uint4 &hi, const uint4 &v) {
     }
 }
 
-// One warp per token. The warp of the lowest-index token landing in a
-// physical block (its "leader") gathers every token of the call in that block
-// and writes the block's new metadata; the other warps exit. So each block is
-// written by exactly one warp and no atomics are needed. The slot scan is one
-// coalesced pass (ballots over 32 tokens at a time); in a decode step a block
-// receives one token, so the leader has no further members to visit.
-__global__ void __launch_bounds__(256) update_meta_kernel(
-    uint4 *__restrict__ kmin, uint4 *__restrict__ kmax, const uint4 *__restrict__ key,
-    const int64_t *__restrict__ slots, int64_t T, int row_vecs, int BS, int64_t NB) {
-    const int64_t t = int64_t(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
-    const int lane = threadIdx.x & 31;
-    if (t >= T) return;
-    const int64_t s = __ldg(slots + t);
-    if (s < 0 || s >= NB * BS) return;
+// Metadata update for token t, run by one warp. The warp of the
+// lowest-index token landing in a physical block (its "leader") gathers every
+// token of the call in that block and writes the block's new metadata; the
+// other warps do nothing. So each block is written by exactly one warp and no
+// atomics are needed. The slot scan is one coalesced pass (ballots over 32
+// tokens at a time); in a decode step a block receives one token, so the
+// leader has no further members to visit.
+__device__ __forceinline__ void meta_update_warp(uint4 *__restrict__ kmin, uint4 *__restrict__ kmax,
+                                                 const uint4 *__restrict__ key,
+                                                 const int64_t *__restrict__ slots, int64_t T,
+                                                 int64_t t, int64_t s, int row_vecs, int BS,
+                                                 int64_t NB, int lane) {
     const int64_t p = s / BS;
     bool reset = (s % BS) == 0;
     int64_t first_member_chunk = -1;   // first 32-token chunk holding a later token of block p
@@ -86,10 +87,7 @@ __global__ void __launch_bounds__(256) update_meta_kernel(
     }
     // leader: start from the old metadata or, if the block starts fresh, from
     // this token; then merge every later token of the call in the block
-    const int per_lane = (row_vecs + 31) / 32;
-    for (int r = 0; r < per_lane; ++r) {
-        const int e = lane + 32 * r;
-        if (e >= row_vecs) break;
+    for (int e = lane; e < row_vecs; e += 32) {
         const uint4 kt = __ldg(key + t * row_vecs + e);
         uint4 lo = kt, hi = kt;
         if (!reset) {
@@ -109,9 +107,7 @@ __global__ void __launch_bounds__(256) update_meta_kernel(
             const int bit = __ffs(m) - 1;
             m &= m - 1;
             const int64_t tu = u0 + bit;
-            for (int r = 0; r < per_lane; ++r) {
-                const int e = lane + 32 * r;
-                if (e >= row_vecs) break;
+            for (int e = lane; e < row_vecs; e += 32) {
                 uint4 lo = kmin[p * row_vecs + e], hi = kmax[p * row_vecs + e];
                 minmax8(lo, hi, __ldg(key + tu * row_vecs + e));
                 kmin[p * row_vecs + e] = lo;
@@ -119,6 +115,42 @@ __global__ void __launch_bounds__(256) update_meta_kernel(
             }
         }
     }
+}
+
+// quest_update_meta: one warp per token.
+__global__ void __launch_bounds__(256) update_meta_kernel(
+    uint4 *__restrict__ kmin, uint4 *__restrict__ kmax, const uint4 *__restrict__ key,
+    const int64_t *__restrict__ slots, int64_t T, int row_vecs, int BS, int64_t NB) {
+    pdl_trigger();
+    pdl_wait();
+    const int64_t t = int64_t(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (t >= T) return;
+    const int64_t s = __ldg(slots + t);
+    if (s < 0 || s >= NB * BS) return;
+    meta_update_warp(kmin, kmax, key, slots, T, t, s, row_vecs, BS, NB, lane);
+}
+
+// The write path in one pass (ReshapeAndCache followed by the metadata
+// update): one warp per token copies its K and V rows into the cache, then
+// takes part in the metadata update of its block.
+__global__ void __launch_bounds__(256) write_quest_kernel(
+    uint4 *__restrict__ kc, uint4 *__restrict__ vc, uint4 *__restrict__ kmin,
+    uint4 *__restrict__ kmax, const uint4 *__restrict__ key, const uint4 *__restrict__ value,
+    const int64_t *__restrict__ slots, int64_t T, int row_vecs, int BS, int64_t NB) {
+    pdl_trigger();
+    pdl_wait();
+    const int64_t t = int64_t(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (t >= T) return;
+    const int64_t s = __ldg(slots + t);
+    if (s < 0 || s >= NB * BS) return;  // padding token, or outside the pool
+    const int64_t dst = s * row_vecs;   // (block * BS + offset) rows of Hkv*D
+    for (int e = lane; e < row_vecs; e += 32) {
+        kc[dst + e] = __ldg(key + t * row_vecs + e);
+        vc[dst + e] = __ldg(value + t * row_vecs + e);
+    }
+    meta_update_warp(kmin, kmax, key, slots, T, t, s, row_vecs, BS, NB, lane);
 }
 
 // ---------------------------------------------------------- metadata rebuild
@@ -129,6 +161,8 @@ __global__ void __launch_bounds__(64) rebuild_meta_kernel(
     uint4 *__restrict__ kmin, uint4 *__restrict__ kmax, const uint4 *__restrict__ kc,
     const int32_t *__restrict__ bt, int MBS, const int32_t *__restrict__ ctx, int row_vecs,
     int BS, int64_t NB) {
+    pdl_trigger();
+    pdl_wait();
     const int j = blockIdx.x, b = blockIdx.y;
     const int c = min(max(__ldg(ctx + b), 0), MBS * BS);
     if (j * BS >= c) return;
@@ -183,10 +217,10 @@ cudaError_t launch_reshape_and_cache(const uint16_t *key, const uint16_t *value,
                                      int BS, int64_t NB, cudaStream_t stream) {
     if (T == 0) return cudaSuccess;
     const int row_vecs = Hkv * D / 8;
-    reshape_and_cache_kernel<<<unsigned(T), 128, 0, stream>>>(
-        reinterpret_cast<const uint4 *>(key), reinterpret_cast<const uint4 *>(value),
-        reinterpret_cast<uint4 *>(kc), reinterpret_cast<uint4 *>(vc), slots, row_vecs, BS, NB);
-    return cudaGetLastError();
+    return launch_pdl(reshape_and_cache_kernel, dim3(unsigned(T)), dim3(128), 0, stream,
+                      reinterpret_cast<const uint4 *>(key), reinterpret_cast<const uint4 *>(value),
+                      reinterpret_cast<uint4 *>(kc), reinterpret_cast<uint4 *>(vc), slots, row_vecs,
+                      BS, NB);
 }
 
 cudaError_t launch_update_meta(uint16_t *kmin, uint16_t *kmax, const uint16_t *key,
@@ -196,10 +230,23 @@ cudaError_t launch_update_meta(uint16_t *kmin, uint16_t *kmax, const uint16_t *k
     const int row_vecs = Hkv * D / 8;
     const int warps = 8;
     const unsigned grid = unsigned((T + warps - 1) / warps);
-    update_meta_kernel<<<grid, warps * 32, 0, stream>>>(
-        reinterpret_cast<uint4 *>(kmin), reinterpret_cast<uint4 *>(kmax),
-        reinterpret_cast<const uint4 *>(key), slots, T, row_vecs, BS, NB);
-    return cudaGetLastError();
+    return launch_pdl(update_meta_kernel, dim3(grid), dim3(warps * 32), 0, stream,
+                      reinterpret_cast<uint4 *>(kmin), reinterpret_cast<uint4 *>(kmax),
+                      reinterpret_cast<const uint4 *>(key), slots, T, row_vecs, BS, NB);
+}
+
+cudaError_t launch_write_quest(uint16_t *kc, uint16_t *vc, uint16_t *kmin, uint16_t *kmax,
+                               const uint16_t *key, const uint16_t *value, const int64_t *slots,
+                               int64_t T, int Hkv, int D, int BS, int64_t NB, cudaStream_t stream) {
+    if (T == 0) return cudaSuccess;
+    const int row_vecs = Hkv * D / 8;
+    const int warps = 8;
+    const unsigned grid = unsigned((T + warps - 1) / warps);
+    return launch_pdl(write_quest_kernel, dim3(grid), dim3(warps * 32), 0, stream,
+                      reinterpret_cast<uint4 *>(kc), reinterpret_cast<uint4 *>(vc),
+                      reinterpret_cast<uint4 *>(kmin), reinterpret_cast<uint4 *>(kmax),
+                      reinterpret_cast<const uint4 *>(key), reinterpret_cast<const uint4 *>(value),
+                      slots, T, row_vecs, BS, NB);
 }
 
 cudaError_t launch_rebuild_meta(uint16_t *kmin, uint16_t *kmax, const uint16_t *kc,
@@ -207,10 +254,9 @@ cudaError_t launch_rebuild_meta(uint16_t *kmin, uint16_t *kmax, const uint16_t *
                                 int D, int BS, int64_t NB, cudaStream_t stream) {
     const int row_vecs = Hkv * D / 8;
     const dim3 grid{unsigned(MBS), unsigned(B), 1u};
-    rebuild_meta_kernel<<<grid, 64, 0, stream>>>(
-        reinterpret_cast<uint4 *>(kmin), reinterpret_cast<uint4 *>(kmax),
-        reinterpret_cast<const uint4 *>(kc), bt, MBS, ctx, row_vecs, BS, NB);
-    return cudaGetLastError();
+    return launch_pdl(rebuild_meta_kernel, grid, dim3(64), 0, stream,
+                      reinterpret_cast<uint4 *>(kmin), reinterpret_cast<uint4 *>(kmax),
+                      reinterpret_cast<const uint4 *>(kc), bt, MBS, ctx, row_vecs, BS, NB);
 }
 
 cudaError_t launch_check_metadata(int32_t *counts, const int64_t *slots, int64_t T,

@@ -35,12 +35,12 @@
 //    P is rounded to bf16 and transposed in registers with movmatrix.
 //  * Masking. Tokens past ctx get score -inf and their V fragment lanes are
 //    zeroed, so NaN/Inf garbage in unused slots never reaches the output.
-//  * Combine. At the end of each segment the consumer warps merge their
-//    states through shared memory. A CTA holding a whole segment writes bf16
-//    output; otherwise it writes a normalised partial and its log2-sum-exp,
-//    and the last CTA to arrive (atomic counter per segment, reset to zero
-//    afterwards) merges the pieces with weights exp2(lse_s - max lse), one
-//    float4 of the output per thread and step.
+//  * Combine. At the end of each segment every consumer warp deposits its
+//    state in shared memory and moves on; the last one to arrive merges the
+//    states. A CTA holding a whole segment writes bf16 output; otherwise the
+//    merging warp writes a normalised partial and its log2-sum-exp, and in
+//    the last CTA to arrive (atomic counter per segment, reset to zero
+//    afterwards) merges the pieces with weights exp2(lse_s - max lse).
 #include "common.cuh"
 #include "kernels.h"
 
@@ -70,9 +70,16 @@ constexpr uint64_t kWaitLimitNs = 500ull * 1000ull * 1000ull;  // 0.5 s per mbar
     do {                                                                                 \
         if (tid == 0 && a.trace) a.trace[int64_t(blockIdx.x) * 8 + (k)] = global_timer_ns(); \
     } while (0)
+#define PA_TRACE_LANE(k)                                                                  \
+    do {                                                                                  \
+        if (lane == 0 && a.trace) a.trace[int64_t(blockIdx.x) * 8 + (k)] = global_timer_ns(); \
+    } while (0)
 #else
 #define PA_TRACE(k) \
     do {            \
+    } while (0)
+#define PA_TRACE_LANE(k) \
+    do {                 \
     } while (0)
 #endif
 
@@ -97,10 +104,6 @@ struct DecodeCfg {
     static constexpr size_t smem_bytes(int B) { return 1024 + off_pre + size_t(B + 1) * 4; }
 };
 
-__device__ __forceinline__ void consumer_sync(int nthreads) {
-    asm volatile("bar.sync 1, %0;" ::"r"(nthreads) : "memory");
-}
-
 template <int D, bool SPARSE>
 __global__ void __launch_bounds__(DecodeCfg<D>::THREADS, 1)
     decode_kernel(const __grid_constant__ CUtensorMap tm_k,
@@ -116,7 +119,7 @@ __global__ void __launch_bounds__(DecodeCfg<D>::THREADS, 1)
     const uint32_t empty_bar = full_bar + S * 8;
     int2 *info = reinterpret_cast<int2 *>(bp + C::off_info);
     float *scr = reinterpret_cast<float *>(bp + C::off_scr);
-    volatile int *flags = reinterpret_cast<volatile int *>(bp + C::off_flags);  // [0] abort, [1] last
+    volatile int *flags = reinterpret_cast<volatile int *>(bp + C::off_flags);
     int32_t *pre = reinterpret_cast<int32_t *>(bp + C::off_pre);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -125,10 +128,12 @@ __global__ void __launch_bounds__(DecodeCfg<D>::THREADS, 1)
     PA_TRACE(0);
 
     // ---- prologue: items per KV head of every sequence and their prefix sum
+    pdl_trigger();
     if (tid == 0) {
         prefetch_tensormap(&tm_k);
         prefetch_tensormap(&tm_v);
     }
+    pdl_wait();  // inputs may come from the previous kernel in the stream
     for (int b = tid; b < B; b += C::THREADS) {
         const int c = min(max(__ldg(a.ctx + b), 0), max_tok);
         const int nblk = (c + BS - 1) / BS;
@@ -136,8 +141,9 @@ __global__ void __launch_bounds__(DecodeCfg<D>::THREADS, 1)
     }
     if (tid == 0) {
         pre[0] = 0;
-        flags[0] = 0;
-        flags[1] = 0;
+        flags[0] = 0;  // abort
+        flags[1] = 0;  // consumers arrived at the current segment end
+        flags[2] = 0;  // segment ends whose states have been merged
         for (int s = 0; s < S; ++s) {
             mbar_init(full_bar + s * 8, 1);
             mbar_init(empty_bar + s * 8, 1);
@@ -421,144 +427,219 @@ __global__ void __launch_bounds__(DecodeCfg<D>::THREADS, 1)
         if (nvb > 0) pv(s1a + C::KT, q01, q23, nvb);
     };
 
-    // merge the CTA pieces of segment `seg` (run by every consumer thread of
-    // the last CTA to arrive); one float4 of the [D][8] output per thread,
-    // pieces merged in order with a running max
+    // Lane layout of the merge and the combine: the [D][8] output is 2*D
+    // float4 slots (a dim and 4 heads each); lane handles slots lane + 32 r,
+    // i.e. dims (lane >> 1) + 16 r for the heads h4 .. h4 + 3.
+    constexpr int NSL = 2 * D / 32;  // slots per lane
+    const int h4 = (lane & 1) * 4;
+
+    // merge the CTA pieces of segment `seg` (run by one warp of the last CTA
+    // to arrive), pieces in order with a running max per head
     auto combine = [&](int seg, int64_t s0, int64_t e0) {
         const int w0 = int(s0 / L), np = int((e0 - 1) / L) - w0 + 1;
         const float *pb = a.part + int64_t(seg + w0) * C::PART;
-        for (int slot = ctid; slot < 2 * D; slot += NC * 32) {
-        const int d = slot >> 1, h4 = (slot & 1) * 4;
         float M[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-        float W[4] = {0.f, 0.f, 0.f, 0.f}, O[4] = {0.f, 0.f, 0.f, 0.f};
-        constexpr int U = 4;
+        float W[4] = {0.f, 0.f, 0.f, 0.f};
+        float O[NSL][4];
+#pragma unroll
+        for (int r = 0; r < NSL; ++r)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) O[r][e] = 0.f;
+        constexpr int U = 4;  // pieces in flight per round
         for (int i0 = 0; i0 < np; i0 += U) {
-            float4 lx[U], xv[U];
+            float4 lx[U], xv[U][NSL];
 #pragma unroll
             for (int u = 0; u < U; ++u) {
                 const float *ps = pb + int64_t(min(i0 + u, np - 1)) * C::PART;
                 lx[u] = __ldcg(reinterpret_cast<const float4 *>(ps + D * 8 + h4));
-                xv[u] = __ldcg(reinterpret_cast<const float4 *>(ps + d * 8 + h4));
+#pragma unroll
+                for (int r = 0; r < NSL; ++r)
+                    xv[u][r] = __ldcg(reinterpret_cast<const float4 *>(ps + ((lane >> 1) + 16 * r) * 8 + h4));
             }
 #pragma unroll
             for (int u = 0; u < U; ++u) {
                 if (i0 + u >= np) break;
                 const float l4[4] = {lx[u].x, lx[u].y, lx[u].z, lx[u].w};
-                const float x4[4] = {xv[u].x, xv[u].y, xv[u].z, xv[u].w};
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     if (l4[e] == -INFINITY) continue;
                     if (l4[e] > M[e]) {
                         const float sc = fast_exp2(M[e] - l4[e]);  // 0 when M was -inf
                         W[e] *= sc;
-                        O[e] *= sc;
+#pragma unroll
+                        for (int r = 0; r < NSL; ++r) O[r][e] *= sc;
                         M[e] = l4[e];
                     }
                     const float wt = fast_exp2(l4[e] - M[e]);
                     W[e] += wt;
-                    O[e] += wt * x4[e];
+#pragma unroll
+                    for (int r = 0; r < NSL; ++r) {
+                        const float x = e == 0 ? xv[u][r].x : e == 1 ? xv[u][r].y : e == 2 ? xv[u][r].z : xv[u][r].w;
+                        O[r][e] += wt * x;
+                    }
                 }
             }
         }
         const int b = seg / Hkv, kvh = seg % Hkv;
-        uint16_t *ob = a.out + (int64_t(b) * a.Hq + kvh * G) * D + d;
+        uint16_t *ob = a.out + (int64_t(b) * a.Hq + kvh * G) * D;
 #pragma unroll
-        for (int e = 0; e < 4; ++e)
-            if (h4 + e < G)
-                ob[(h4 + e) * D] = __bfloat16_as_ushort(__float2bfloat16_rn(W[e] > 0.f ? O[e] / W[e] : 0.f));
+        for (int r = 0; r < NSL; ++r) {
+            const int d = (lane >> 1) + 16 * r;
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                if (h4 + e < G)
+                    ob[(h4 + e) * D + d] =
+                        __bfloat16_as_ushort(__float2bfloat16_rn(W[e] > 0.f ? O[r][e] / W[e] : 0.f));
         }
     };
 
-    // merge the consumer warps' states of one segment, then write the CTA's
-    // piece (final output, or partial + arrival)
-    auto merge = [&](int seg, int64_t s0, int64_t e0, bool whole) {
+    // End of a segment for this warp. Every consumer deposits its state in
+    // its shared-memory slot and counts itself in; the last warp to arrive
+    // merges the NC states and writes the CTA's piece (final output, or a
+    // partial followed by the cross-CTA arrival and, for the last CTA, the
+    // combine); the other warps go straight on to the next segment.
+    volatile int *arrive_cnt = flags + 1;  // warps that deposited the current instance
+    volatile int *read_done = flags + 2;   // instances whose states the merger has read
+    auto merge = [&](int seg, int64_t s0, int64_t e0, bool whole, int inst, bool last_seg) {
         l0 += __shfl_xor_sync(0xffffffffu, l0, 4);
         l0 += __shfl_xor_sync(0xffffffffu, l0, 8);
         l0 += __shfl_xor_sync(0xffffffffu, l0, 16);
         l1 += __shfl_xor_sync(0xffffffffu, l1, 4);
         l1 += __shfl_xor_sync(0xffffffffu, l1, 8);
         l1 += __shfl_xor_sync(0xffffffffu, l1, 16);
+        // the slot is free once the previous instance's merger has read it
+        if (lane == 0 && *read_done < inst) {
+            const uint64_t t0 = global_timer_ns();
+            while (*read_done < inst) {
+                if (global_timer_ns() - t0 > kWaitLimitNs) {
+                    flags[0] = 1;
+                    atomicOr(a.status, kStatusTimeout);
+                    break;
+                }
+            }
+        }
+        __syncwarp();
         float *my = scr + c_id * C::SCR;
-        const int h0 = 2 * q4;
+        const int hh = 2 * q4;
 #pragma unroll
         for (int mt = 0; mt < NKK; ++mt) {
             const int d = 16 * mt + g;
-            *reinterpret_cast<float2 *>(my + d * 8 + h0) = make_float2(acc[mt][0], acc[mt][1]);
-            *reinterpret_cast<float2 *>(my + (d + 8) * 8 + h0) = make_float2(acc[mt][2], acc[mt][3]);
+            *reinterpret_cast<float2 *>(my + d * 8 + hh) = make_float2(acc[mt][0], acc[mt][1]);
+            *reinterpret_cast<float2 *>(my + (d + 8) * 8 + hh) = make_float2(acc[mt][2], acc[mt][3]);
         }
         if (g == 0) {
-            *reinterpret_cast<float2 *>(my + D * 8 + h0) = make_float2(m0, m1);
-            *reinterpret_cast<float2 *>(my + D * 8 + 8 + h0) = make_float2(l0, l1);
+            *reinterpret_cast<float2 *>(my + D * 8 + hh) = make_float2(m0, m1);
+            *reinterpret_cast<float2 *>(my + D * 8 + 8 + hh) = make_float2(l0, l1);
         }
-        consumer_sync(NC * 32);
+        __syncwarp();
+        int merger = 0;
+        if (lane == 0) {
+            __threadfence_block();
+            merger = (atomicAdd(const_cast<int *>(arrive_cnt), 1) == NC - 1);
+            if (merger) {
+                *arrive_cnt = 0;
+                __threadfence_block();
+            }
+        }
+        merger = __shfl_sync(0xffffffffu, merger, 0);
+        if (!merger) return;
+
+        // ---- this warp merges the NC states
+        if (last_seg) PA_TRACE_LANE(5);
+        float M[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+        float mc[NC][4], lc[NC][4];
+#pragma unroll
+        for (int cc = 0; cc < NC; ++cc) {
+            const float4 mm = *reinterpret_cast<const float4 *>(scr + cc * C::SCR + D * 8 + h4);
+            const float4 ll = *reinterpret_cast<const float4 *>(scr + cc * C::SCR + D * 8 + 8 + h4);
+            mc[cc][0] = mm.x; mc[cc][1] = mm.y; mc[cc][2] = mm.z; mc[cc][3] = mm.w;
+            lc[cc][0] = ll.x; lc[cc][1] = ll.y; lc[cc][2] = ll.z; lc[cc][3] = ll.w;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) M[e] = fmaxf(M[e], mc[cc][e]);
+        }
+        float Ls[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int cc = 0; cc < NC; ++cc)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                mc[cc][e] = (mc[cc][e] == -INFINITY) ? 0.f : fast_exp2(mc[cc][e] - M[e]);  // weight
+                Ls[e] += mc[cc][e] * lc[cc][e];
+            }
+        float O[NSL][4];
+#pragma unroll
+        for (int r = 0; r < NSL; ++r) {
+            const int d = (lane >> 1) + 16 * r;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) O[r][e] = 0.f;
+#pragma unroll
+            for (int cc = 0; cc < NC; ++cc) {
+                const float4 xx = *reinterpret_cast<const float4 *>(scr + cc * C::SCR + d * 8 + h4);
+                O[r][0] += mc[cc][0] * xx.x;
+                O[r][1] += mc[cc][1] * xx.y;
+                O[r][2] += mc[cc][2] * xx.z;
+                O[r][3] += mc[cc][3] * xx.w;
+            }
+        }
+        __syncwarp();
+        if (lane == 0) {
+            __threadfence_block();
+            *read_done = inst + 1;  // the slots may be written again
+        }
         const int b = seg / Hkv, kvh = seg % Hkv;
-        for (int slot = ctid; slot < 2 * D; slot += NC * 32) {
-            const int d = slot >> 1, h4 = (slot & 1) * 4;
-            float M[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+        if (whole) {
+            uint16_t *ob = a.out + (int64_t(b) * a.Hq + kvh * G) * D;
 #pragma unroll
-            for (int cc = 0; cc < NC; ++cc) {
-                const float4 mm = *reinterpret_cast<const float4 *>(scr + cc * C::SCR + D * 8 + h4);
-                M[0] = fmaxf(M[0], mm.x); M[1] = fmaxf(M[1], mm.y);
-                M[2] = fmaxf(M[2], mm.z); M[3] = fmaxf(M[3], mm.w);
-            }
-            float Ls[4] = {0.f, 0.f, 0.f, 0.f}, O[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-            for (int cc = 0; cc < NC; ++cc) {
-                const float *sc = scr + cc * C::SCR;
-                const float4 mm = *reinterpret_cast<const float4 *>(sc + D * 8 + h4);
-                const float4 ll = *reinterpret_cast<const float4 *>(sc + D * 8 + 8 + h4);
-                const float4 xx = *reinterpret_cast<const float4 *>(sc + d * 8 + h4);
-                const float m4[4] = {mm.x, mm.y, mm.z, mm.w}, l4[4] = {ll.x, ll.y, ll.z, ll.w};
-                const float x4[4] = {xx.x, xx.y, xx.z, xx.w};
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float wt = (m4[e] == -INFINITY) ? 0.f : fast_exp2(m4[e] - M[e]);
-                    Ls[e] += wt * l4[e];
-                    O[e] += wt * x4[e];
-                }
-            }
-            if (whole) {
-                uint16_t *ob = a.out + (int64_t(b) * a.Hq + kvh * G) * D + d;
+            for (int r = 0; r < NSL; ++r) {
+                const int d = (lane >> 1) + 16 * r;
 #pragma unroll
                 for (int e = 0; e < 4; ++e)
                     if (h4 + e < G)
-                        ob[(h4 + e) * D] =
-                            __bfloat16_as_ushort(__float2bfloat16_rn(Ls[e] > 0.f ? O[e] / Ls[e] : 0.f));
-            } else {
-                float *ps = a.part + int64_t(seg + blockIdx.x) * C::PART;
-                float r[4], lse[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    r[e] = Ls[e] > 0.f ? O[e] / Ls[e] : 0.f;
-                    lse[e] = Ls[e] > 0.f ? M[e] + log2f(Ls[e]) : -INFINITY;
-                }
-                __stcg(reinterpret_cast<float4 *>(ps + d * 8 + h4), make_float4(r[0], r[1], r[2], r[3]));
-                if (d == 0)
-                    __stcg(reinterpret_cast<float4 *>(ps + D * 8 + h4),
-                           make_float4(lse[0], lse[1], lse[2], lse[3]));
+                        ob[(h4 + e) * D + d] =
+                            __bfloat16_as_ushort(__float2bfloat16_rn(Ls[e] > 0.f ? O[r][e] / Ls[e] : 0.f));
             }
+            if (last_seg) PA_TRACE_LANE(4);
+            return;
         }
-        consumer_sync(NC * 32);  // partial written by every thread; scratch free again
-        if (whole) return;
-        if (ctid == 0) {
-            // release the CTA's partial (ordered after the barrier) and count it
-            __threadfence();
+        float *ps = a.part + int64_t(seg + blockIdx.x) * C::PART;
+        float inv[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) inv[e] = Ls[e] > 0.f ? 1.f / Ls[e] : 0.f;
+#pragma unroll
+        for (int r = 0; r < NSL; ++r) {
+            const int d = (lane >> 1) + 16 * r;
+            __stcg(reinterpret_cast<float4 *>(ps + d * 8 + h4),
+                   make_float4(O[r][0] * inv[0], O[r][1] * inv[1], O[r][2] * inv[2], O[r][3] * inv[3]));
+        }
+        if (lane < 2) {
+            float lse[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) lse[e] = Ls[e] > 0.f ? M[e] + log2f(Ls[e]) : -INFINITY;
+            __stcg(reinterpret_cast<float4 *>(ps + D * 8 + h4), make_float4(lse[0], lse[1], lse[2], lse[3]));
+        }
+        __syncwarp();
+        int last = 0;
+        if (lane == 0) {
+            // release this CTA's partial (written by the warp, ordered by the
+            // warp barrier) and acquire the pieces counted before it
+            __threadfence_block();
             const int npieces = int((e0 - 1) / L - s0 / L) + 1;
-            const int old = atomicAdd(a.counters + seg, 1);
-            const int last = (old == npieces - 1);
-            if (last) __threadfence();  // acquire the other pieces before the merge
-            flags[1] = last;
+            last = (atomic_add_acq_rel_gpu(a.counters + seg, 1) == npieces - 1);
         }
-        consumer_sync(NC * 32);
-        if (flags[1]) {
+        last = __shfl_sync(0xffffffffu, last, 0);
+        __syncwarp();  // every lane's reads of the pieces follow lane 0's acquire
+        if (last_seg) PA_TRACE_LANE(6);
+        if (last) {
             combine(seg, s0, e0);
-            if (ctid == 0) a.counters[seg] = 0;
+            if (lane == 0) a.counters[seg] = 0;
+            if (last_seg) PA_TRACE_LANE(7);
         }
+        if (last_seg) PA_TRACE_LANE(4);
     };
 
     // walk the segments of this CTA's range in order; every consumer warp
     // takes part in every segment's merge
     int64_t p = pos0;
+    int inst = 0;  // segments finished so far (the same count in every consumer)
     int b = find_seq(p);
     int kvh = int((p - int64_t(Hkv) * pre[b]) / (pre[b + 1] - pre[b]));
     while (p < pos1) {
@@ -589,7 +670,7 @@ __global__ void __launch_bounds__(DecodeCfg<D>::THREADS, 1)
         }
         const bool whole = (s0 >= pos0) && (e0 <= pos1);
         if (e0 >= pos1) PA_TRACE(3);
-        merge(seg, s0, e0, whole);
+        merge(seg, s0, e0, whole, inst++, e0 >= pos1);
         p = min(e0, pos1);
         if (++kvh == Hkv) {
             kvh = 0;
@@ -598,7 +679,6 @@ __global__ void __launch_bounds__(DecodeCfg<D>::THREADS, 1)
             } while (b < B && pre[b + 1] == pre[b]);
         }
     }
-    PA_TRACE(4);
 }
 
 template <int D>
@@ -636,8 +716,8 @@ cudaError_t launch_t(const CUtensorMap &tm_k, const CUtensorMap &tm_v, const Dec
     cudaError_t e = decode_geometry(D, &geo);
     if (e != cudaSuccess) return e;
     if (C::smem_bytes(a.B) > geo.smem) return cudaErrorInvalidConfiguration;  // batch too large
-    decode_kernel<D, SPARSE><<<geo.grid, C::THREADS, C::smem_bytes(a.B), stream>>>(tm_k, tm_v, a);
-    return cudaGetLastError();
+    return launch_pdl(decode_kernel<D, SPARSE>, dim3(geo.grid), dim3(C::THREADS), C::smem_bytes(a.B),
+                      stream, tm_k, tm_v, a);
 }
 
 constexpr int kMaxDevices = 64;

@@ -47,6 +47,9 @@ cudaError_t launch_reshape_and_cache(const uint16_t *key, const uint16_t *value,
 cudaError_t launch_update_meta(uint16_t *kmin, uint16_t *kmax, const uint16_t *key,
                                const int64_t *slots, int64_t T, int Hkv, int D, int BS, int64_t NB,
                                cudaStream_t stream);
+cudaError_t launch_write_quest(uint16_t *kc, uint16_t *vc, uint16_t *kmin, uint16_t *kmax,
+                               const uint16_t *key, const uint16_t *value, const int64_t *slots,
+                               int64_t T, int Hkv, int D, int BS, int64_t NB, cudaStream_t stream);
 cudaError_t launch_rebuild_meta(uint16_t *kmin, uint16_t *kmax, const uint16_t *kc,
                                 const int32_t *bt, int MBS, const int32_t *ctx, int B, int Hkv,
                                 int D, int BS, int64_t NB, cudaStream_t stream);

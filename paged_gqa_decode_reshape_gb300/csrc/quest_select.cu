@@ -15,10 +15,9 @@
 // combined by a xor butterfly (16, 8, 4, 2, 1). No FMA contraction (the
 // products and sums are explicit __fmul_rn / __fadd_rn).
 //
-// Work split: the (sequence, KV head, block) list is cut into equal contiguous
-// ranges, one per warp of a persistent grid; a warp reads each block's two
-// metadata rows with one 8-byte (D=128) load per lane, i.e. 256 contiguous
-// bytes per row per warp, four blocks in flight per step.
+// Work split: one warp per chunk of 16 logical blocks of a (sequence, KV head);
+// a warp reads each block's two metadata rows with one 8-byte (D=128) load per
+// lane, i.e. 256 contiguous bytes per row per warp, all 16 blocks in flight.
 //
 // Top-K: one CTA per (sequence, KV head): a 4-pass, 8-bit radix select over
 // the totalOrder keys of the scores finds the K-th largest key; blocks above
@@ -31,8 +30,15 @@ namespace pa {
 
 namespace {
 
-constexpr int kScoreWarps = 8;
+constexpr int kScoreWarps = 4;
 constexpr int kTopkThreads = 256;
+
+// One warp scores a chunk of up to kChunk consecutive logical blocks of one
+// (sequence, KV head): grid (ceil(MBS / (kChunk * kScoreWarps)), Hkv, B).
+// Every load is issued before any result is needed: the context length, the
+// chunk's block-table entries (one per lane) and the query group in one round
+// trip, then the metadata rows of all the chunk's blocks in a second.
+constexpr int kChunk = 16;
 
 template <int D>
 __global__ void __launch_bounds__(kScoreWarps * 32) quest_score_kernel(
@@ -40,142 +46,90 @@ __global__ void __launch_bounds__(kScoreWarps * 32) quest_score_kernel(
     const uint16_t *__restrict__ kmax, const int32_t *__restrict__ bt, int MBS,
     const int32_t *__restrict__ ctx, int B, int Hq, int Hkv, int BS, int64_t NB) {
     constexpr int C = D / 32;  // dims per lane
-    extern __shared__ int32_t pre[];
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    constexpr int CW = C / 2;  // 32-bit words per lane per row
+    pdl_trigger();
+    pdl_wait();
+    const int lane = threadIdx.x & 31;
+    const int b = blockIdx.z, kvh = blockIdx.y;
+    const int j0 = (blockIdx.x * kScoreWarps + (threadIdx.x >> 5)) * kChunk;
+    if (j0 >= MBS) return;
     const int G = Hq / Hkv;
-    const int max_tok = MBS * BS;
-    for (int b = tid; b < B; b += blockDim.x) {
-        const int c = min(max(__ldg(ctx + b), 0), max_tok);
-        pre[b + 1] = (c + BS - 1) / BS;
-    }
-    if (tid == 0) pre[0] = 0;
-    __syncthreads();
-    if (warp == 0) {
-        int carry = 0;
-        for (int b0 = 0; b0 < B; b0 += 32) {
-            const int b = b0 + lane;
-            int v = (b < B) ? pre[b + 1] : 0;
+    // round trip 1: ctx, block-table entries, query group
+    const int craw = __ldg(ctx + b);
+    const int ph_l = (lane < kChunk && j0 + lane < MBS) ? __ldg(bt + int64_t(b) * MBS + j0 + lane) : -1;
+    uint32_t qw[kMaxGroup][CW];
 #pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const int u = __shfl_up_sync(0xffffffffu, v, o);
-                if (lane >= o) v += u;
-            }
-            if (b < B) pre[b + 1] = carry + v;
-            carry += __shfl_sync(0xffffffffu, v, 31);
-        }
-    }
-    __syncthreads();
-
-    const int64_t total = int64_t(Hkv) * pre[B];
-    const int W = gridDim.x * kScoreWarps;
-    const int w = blockIdx.x * kScoreWarps + warp;
-    const int64_t L = (total + W - 1) / W;
-    int64_t pos = int64_t(w) * L;
-    const int64_t pos1 = min(total, pos + L);
-    if (pos >= pos1) return;
-
-    // locate the first item
-    int lo = 0, hi = B;
-    while (hi - lo > 1) {
-        const int mid = (lo + hi) >> 1;
-        if (int64_t(Hkv) * pre[mid] <= pos) lo = mid; else hi = mid;
-    }
-    int b = lo;
-    int n = pre[b + 1] - pre[b];
-    int64_t r = pos - int64_t(Hkv) * pre[b];
-    int kvh = int(r / n);
-    int j = int(r - int64_t(kvh) * n);
-
-    while (pos < pos1) {
-        const int j_end = int(min(int64_t(n), int64_t(j) + (pos1 - pos)));
-        const int32_t *bt_row = bt + int64_t(b) * MBS;
-        float *srow = scores + (int64_t(b) * Hkv + kvh) * MBS;
-        // first chunk's block-table entries, in flight while P/N are formed
-        int ph_next = (j + lane < j_end) ? __ldg(bt_row + j + lane) : -1;
-        // P_d, N_d of this (b, kvh) for this lane's dims
-        float P[C], N[C];
-#pragma unroll
-        for (int c = 0; c < C; ++c) {
-            P[c] = 0.f;
-            N[c] = 0.f;
-        }
-        for (int gg = 0; gg < G; ++gg) {
+    for (int gg = 0; gg < kMaxGroup; ++gg) {
+        if (gg < G) {
             const uint16_t *qr = q + (int64_t(b) * Hq + int64_t(kvh) * G + gg) * D + lane * C;
-            uint32_t qw[C / 2];
             if (C == 4) {
                 const uint2 v2 = __ldg(reinterpret_cast<const uint2 *>(qr));
-                qw[0] = v2.x;
-                qw[C / 2 - 1] = v2.y;
+                qw[gg][0] = v2.x;
+                qw[gg][CW - 1] = v2.y;
             } else {
-                qw[0] = __ldg(reinterpret_cast<const uint32_t *>(qr));
+                qw[gg][0] = __ldg(reinterpret_cast<const uint32_t *>(qr));
             }
-#pragma unroll
-            for (int c = 0; c < C; ++c) {
-                const float v = (c & 1) ? bf16_hi(qw[c >> 1]) : bf16_lo(qw[c >> 1]);
-                P[c] = __fadd_rn(P[c], v > 0.f ? v : 0.f);
-                N[c] = __fadd_rn(N[c], v < 0.f ? v : 0.f);
-            }
-        }
-        for (int j0 = j; j0 < j_end; j0 += 32) {
-            // physical blocks of up to 32 items, one per lane
-            const int ph_l = ph_next;
-            if (j0 + 32 < j_end) ph_next = (j0 + 32 + lane < j_end) ? __ldg(bt_row + j0 + 32 + lane) : -1;
-            const int cnt = min(32, j_end - j0);
-            for (int i0 = 0; i0 < cnt; i0 += 4) {
-                float sc[4];
-                uint32_t mnv[4][C / 2 > 0 ? C / 2 : 1], mxv[4][C / 2 > 0 ? C / 2 : 1];
-                bool ok[4];
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const int ph = __shfl_sync(0xffffffffu, ph_l, (i0 + u) & 31);
-                    ok[u] = (i0 + u < cnt) && ph >= 0 && int64_t(ph) < NB;
-                    const int64_t off = (int64_t(ok[u] ? ph : 0) * Hkv + kvh) * D + lane * C;
-                    if (C == 4) {
-                        const uint2 a2 = __ldg(reinterpret_cast<const uint2 *>(kmin + off));
-                        const uint2 b2 = __ldg(reinterpret_cast<const uint2 *>(kmax + off));
-                        mnv[u][0] = a2.x; mnv[u][C / 2 - 1] = a2.y;
-                        mxv[u][0] = b2.x; mxv[u][C / 2 - 1] = b2.y;
-                    } else {
-                        mnv[u][0] = __ldg(reinterpret_cast<const uint32_t *>(kmin + off));
-                        mxv[u][0] = __ldg(reinterpret_cast<const uint32_t *>(kmax + off));
-                    }
-                }
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    float acc = 0.f;
-#pragma unroll
-                    for (int c = 0; c < C; ++c) {
-                        const uint32_t wmn = mnv[u][c >> 1], wmx = mxv[u][c >> 1];
-                        const float mn = (c & 1) ? bf16_hi(wmn) : bf16_lo(wmn);
-                        const float mx = (c & 1) ? bf16_hi(wmx) : bf16_lo(wmx);
-                        const float t = __fadd_rn(__fmul_rn(P[c], mx), __fmul_rn(N[c], mn));
-                        acc = (c == 0) ? t : __fadd_rn(acc, t);
-                    }
-#pragma unroll
-                    for (int o = 16; o >= 1; o >>= 1) acc = __fadd_rn(acc, __shfl_xor_sync(0xffffffffu, acc, o));
-                    sc[u] = ok[u] ? acc : -INFINITY;
-                }
-                if (lane < 4 && i0 + lane < cnt) {
-                    float v = sc[0];
-#pragma unroll
-                    for (int u = 1; u < 4; ++u)
-                        if (lane == u) v = sc[u];
-                    srow[j0 + i0 + lane] = v;
-                }
-            }
-        }
-        pos += j_end - j;
-        // next segment
-        j = 0;
-        if (++kvh == Hkv) {
-            kvh = 0;
-            do {
-                ++b;
-            } while (b < B && pre[b + 1] == pre[b]);
-            if (b >= B) break;
-            n = pre[b + 1] - pre[b];
         }
     }
+    const int c = min(max(craw, 0), MBS * BS);
+    const int nblk = (c + BS - 1) / BS;
+    if (j0 >= nblk) return;
+    const int cnt = min(kChunk, nblk - j0);
+    // round trip 2: both metadata rows of every block of the chunk
+    uint32_t mnv[kChunk][CW], mxv[kChunk][CW];
+    bool ok[kChunk];
+#pragma unroll
+    for (int u = 0; u < kChunk; ++u) {
+        const int ph = __shfl_sync(0xffffffffu, ph_l, u);
+        ok[u] = (u < cnt) && ph >= 0 && int64_t(ph) < NB;
+        const int64_t off = (int64_t(ok[u] ? ph : 0) * Hkv + kvh) * D + lane * C;
+        if (C == 4) {
+            const uint2 a2 = __ldg(reinterpret_cast<const uint2 *>(kmin + off));
+            const uint2 b2 = __ldg(reinterpret_cast<const uint2 *>(kmax + off));
+            mnv[u][0] = a2.x;
+            mnv[u][CW - 1] = a2.y;
+            mxv[u][0] = b2.x;
+            mxv[u][CW - 1] = b2.y;
+        } else {
+            mnv[u][0] = __ldg(reinterpret_cast<const uint32_t *>(kmin + off));
+            mxv[u][0] = __ldg(reinterpret_cast<const uint32_t *>(kmax + off));
+        }
+    }
+    // P_d = sum_h max(q, 0), N_d = sum_h min(q, 0), h ascending from +0
+    float P[C], N[C];
+#pragma unroll
+    for (int cc = 0; cc < C; ++cc) {
+        P[cc] = 0.f;
+        N[cc] = 0.f;
+    }
+#pragma unroll
+    for (int gg = 0; gg < kMaxGroup; ++gg) {
+        if (gg < G) {
+#pragma unroll
+            for (int cc = 0; cc < C; ++cc) {
+                const float v = (cc & 1) ? bf16_hi(qw[gg][cc >> 1]) : bf16_lo(qw[gg][cc >> 1]);
+                P[cc] = __fadd_rn(P[cc], v > 0.f ? v : 0.f);
+                N[cc] = __fadd_rn(N[cc], v < 0.f ? v : 0.f);
+            }
+        }
+    }
+    float mine = -INFINITY;  // lane u keeps block j0 + u's score
+#pragma unroll
+    for (int u = 0; u < kChunk; ++u) {
+        float acc = 0.f;
+#pragma unroll
+        for (int cc = 0; cc < C; ++cc) {
+            const uint32_t wmn = mnv[u][cc >> 1], wmx = mxv[u][cc >> 1];
+            const float mn = (cc & 1) ? bf16_hi(wmn) : bf16_lo(wmn);
+            const float mx = (cc & 1) ? bf16_hi(wmx) : bf16_lo(wmx);
+            const float t = __fadd_rn(__fmul_rn(P[cc], mx), __fmul_rn(N[cc], mn));
+            acc = (cc == 0) ? t : __fadd_rn(acc, t);
+        }
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) acc = __fadd_rn(acc, __shfl_xor_sync(0xffffffffu, acc, o));
+        if (lane == u) mine = ok[u] ? acc : -INFINITY;
+    }
+    if (lane < cnt) scores[(int64_t(b) * Hkv + kvh) * MBS + j0 + lane] = mine;
 }
 
 // block-wide exclusive scan of a 0/1 flag (kTopkThreads threads)
@@ -206,6 +160,8 @@ __global__ void __launch_bounds__(kTopkThreads) quest_topk_kernel(
     __shared__ int warp_cnt[kTopkThreads / 32];
     __shared__ int sh_digit, sh_above;
     __shared__ uint32_t keys[kTopkSmemKeys];
+    pdl_trigger();
+    pdl_wait();
     const int seg = blockIdx.x;
     const int b = seg / Hkv;
     const int tid = threadIdx.x, lane = tid & 31;
@@ -288,18 +244,10 @@ template <int D>
 cudaError_t launch_score(float *scores, const uint16_t *q, const uint16_t *kmin,
                          const uint16_t *kmax, const int32_t *bt, int MBS, const int32_t *ctx,
                          int B, int Hq, int Hkv, int BS, int64_t NB, cudaStream_t stream) {
-    const size_t smem = size_t(B + 1) * 4;
-    int dev = 0, sms = 0, per_sm = 0;
-    cudaError_t e;
-    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
-    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, quest_score_kernel<D>,
-                                                      kScoreWarps * 32, smem);
-    if (e != cudaSuccess) return e;
-    per_sm = per_sm < 1 ? 1 : per_sm;
-    quest_score_kernel<D><<<sms * per_sm, kScoreWarps * 32, smem, stream>>>(
-        scores, q, kmin, kmax, bt, MBS, ctx, B, Hq, Hkv, BS, NB);
-    return cudaGetLastError();
+    const dim3 grid{unsigned((MBS + kChunk * kScoreWarps - 1) / (kChunk * kScoreWarps)), unsigned(Hkv),
+                    unsigned(B)};
+    return launch_pdl(quest_score_kernel<D>, grid, dim3(kScoreWarps * 32), 0, stream, scores, q, kmin,
+                      kmax, bt, MBS, ctx, B, Hq, Hkv, BS, NB);
 }
 
 }  // namespace
@@ -312,9 +260,8 @@ cudaError_t launch_quest_select(int32_t *sel, float *scores, const uint16_t *q,
         ? launch_score<128>(scores, q, kmin, kmax, bt, MBS, ctx, B, Hq, Hkv, BS, NB, stream)
         : launch_score<64>(scores, q, kmin, kmax, bt, MBS, ctx, B, Hq, Hkv, BS, NB, stream);
     if (e != cudaSuccess) return e;
-    quest_topk_kernel<<<unsigned(B) * unsigned(Hkv), kTopkThreads, 0, stream>>>(sel, scores, MBS, ctx,
-                                                                               Hkv, BS, topk);
-    return cudaGetLastError();
+    return launch_pdl(quest_topk_kernel, dim3(unsigned(B) * unsigned(Hkv)), dim3(kTopkThreads), 0, stream,
+                      sel, static_cast<const float *>(scores), MBS, ctx, Hkv, BS, topk);
 }
 
 }  // namespace pa

@@ -238,3 +238,25 @@ def test_repeated_calls_reuse_workspace():
     s1 = dev.sparse(torch.from_numpy(sel).to(dev.dev)).clone()
     s2 = dev.sparse(torch.from_numpy(sel).to(dev.dev))
     assert torch.equal(s1, s2)
+
+
+@pytest.mark.parametrize("name,kw", [("mixed_b128", dict(batch=24, ctx_scale=0.03, topk=8)),
+                                     ("tiny", {})])
+def test_fused_write_path_equals_separate_calls(name, kw):
+    """quest_reshape_and_cache = pa_reshape_and_cache + quest_update_meta,
+    bit for bit, and equal to the oracle's two steps."""
+    import oracle
+    from paged_gqa_decode_reshape_gb300 import quest_rebuild_meta, quest_reshape_and_cache
+    w = workloads.make(name, **kw)
+    dev, ora = DeviceStep(w), OracleStep(w)
+    pre_ctx = torch.from_numpy((w.context_lens - 1).astype(np.int32)).to(dev.dev)
+    quest_rebuild_meta(dev.kmin, dev.kmax, dev.kc, dev.bt, pre_ctx)
+    kmin = to_host_u16(dev.kmin).copy()
+    kmax = to_host_u16(dev.kmax).copy()
+    quest_reshape_and_cache(dev.key, dev.value, dev.kc, dev.vc, dev.kmin, dev.kmax, dev.slots)
+    ora.reshape()
+    oracle.quest_update_meta(kmin, kmax, w.key, w.slot_mapping, w.BS)
+    np.testing.assert_array_equal(to_host_u16(dev.kc), ora.kc)
+    np.testing.assert_array_equal(to_host_u16(dev.vc), ora.vc)
+    np.testing.assert_array_equal(to_host_u16(dev.kmin), kmin)
+    np.testing.assert_array_equal(to_host_u16(dev.kmax), kmax)
