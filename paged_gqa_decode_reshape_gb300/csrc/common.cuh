@@ -95,6 +95,12 @@ __device__ __forceinline__ uint64_t l2_policy_evict_first() {
     return p;
 }
 
+// Hint: bring one 128-byte line into L2 (no value is returned, nothing is
+// cached closer to the SM, so a later write by another kernel is still seen).
+__device__ __forceinline__ void prefetch_l2(const void *p) {
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
@@ -172,9 +178,17 @@ __device__ __forceinline__ uint32_t f32_order_key(float f) {
 }
 
 // Host side: launch a kernel with programmatic stream serialization allowed.
+// The first launch of each kernel also asks for the largest shared-memory
+// carveout, the split the decode kernel needs, so consecutive kernels of the
+// library never make the SMs reconfigure between them.
 template <typename... KArgs, typename... Args>
 inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
                               cudaStream_t stream, Args... args) {
+    static const bool carveout_set = [kernel] {
+        cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+        return true;
+    }();
+    (void)carveout_set;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
     cfg.blockDim = block;

@@ -63,16 +63,16 @@ constexpr uint64_t kWaitLimitNs = 500ull * 1000ull * 1000ull;  // 0.5 s per mbar
 #endif
 
 // Optional CTA timeline (%globaltimer) for tuning builds: compile with
-// -DPA_DECODE_TRACE and the kernel writes 8 timestamps per CTA after the
-// partials in the workspace.
+// -DPA_DECODE_TRACE and the kernel writes 16 words per CTA (timestamps, SM id,
+// item count) after the partials in the workspace.
 #ifdef PA_DECODE_TRACE
 #define PA_TRACE(k)                                                                      \
     do {                                                                                 \
-        if (tid == 0 && a.trace) a.trace[int64_t(blockIdx.x) * 8 + (k)] = global_timer_ns(); \
+        if (tid == 0 && a.trace) a.trace[int64_t(blockIdx.x) * 16 + (k)] = global_timer_ns(); \
     } while (0)
 #define PA_TRACE_LANE(k)                                                                  \
     do {                                                                                  \
-        if (lane == 0 && a.trace) a.trace[int64_t(blockIdx.x) * 8 + (k)] = global_timer_ns(); \
+        if (lane == 0 && a.trace) a.trace[int64_t(blockIdx.x) * 16 + (k)] = global_timer_ns(); \
     } while (0)
 #else
 #define PA_TRACE(k) \
@@ -133,6 +133,19 @@ __global__ void __launch_bounds__(DecodeCfg<D>::THREADS, 1)
         prefetch_tensormap(&tm_k);
         prefetch_tensormap(&tm_v);
     }
+    {
+        // While the previous kernel finishes: pull this CTA's share of the
+        // context lengths, block table and selection into L2 (hints only).
+        const int64_t nthr = int64_t(gridDim.x) * C::THREADS;
+        const int64_t gt = int64_t(blockIdx.x) * C::THREADS + tid;
+        for (int64_t off = gt * 32; off < int64_t(B); off += nthr * 32) prefetch_l2(a.ctx + off);
+        const int64_t bt_n = int64_t(B) * a.MBS;
+        for (int64_t off = gt * 32; off < bt_n; off += nthr * 32) prefetch_l2(a.bt + off);
+        if (SPARSE) {
+            const int64_t sel_n = int64_t(B) * Hkv * a.topk;
+            for (int64_t off = gt * 32; off < sel_n; off += nthr * 32) prefetch_l2(a.sel + off);
+        }
+    }
     pdl_wait();  // inputs may come from the previous kernel in the stream
     for (int b = tid; b < B; b += C::THREADS) {
         const int c = min(max(__ldg(a.ctx + b), 0), max_tok);
@@ -184,6 +197,14 @@ __global__ void __launch_bounds__(DecodeCfg<D>::THREADS, 1)
     if (pos0 >= pos1) return;  // whole CTA: nothing to do
     const int n_items = int(pos1 - pos0);
     PA_TRACE(1);
+#ifdef PA_DECODE_TRACE
+    if (tid == 0 && a.trace) {
+        uint32_t smid;
+        asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
+        a.trace[int64_t(blockIdx.x) * 16 + 8] = smid;
+        a.trace[int64_t(blockIdx.x) * 16 + 9] = uint64_t(n_items);
+    }
+#endif
 
     // sequence holding global item position p
     auto find_seq = [&](int64_t p) -> int {
@@ -698,6 +719,9 @@ cudaError_t geometry_t(DecodeGeometry *g) {
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(decode_kernel<D, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
     if (e != cudaSuccess) return e;
+    // same L1/shared split as the library's other kernels: no reconfiguration between them
+    cudaFuncSetAttribute(decode_kernel<D, false>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+    cudaFuncSetAttribute(decode_kernel<D, true>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
     e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_kernel<D, false>, C::THREADS, smem);
     if (e != cudaSuccess) return e;
     if (per_sm < 1) return cudaErrorInvalidConfiguration;
@@ -754,7 +778,7 @@ size_t decode_trace_offset(int B, int Hkv, int head_dim, int workers) {
 size_t decode_workspace_bytes(int B, int Hkv, int head_dim, int workers) {
     size_t bytes = decode_trace_offset(B, Hkv, head_dim, workers);
 #ifdef PA_DECODE_TRACE
-    bytes += size_t(workers) * 8 * sizeof(uint64_t);
+    bytes += size_t(workers) * 16 * sizeof(uint64_t);
 #endif
     return bytes;
 }

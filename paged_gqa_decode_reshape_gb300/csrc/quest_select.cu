@@ -15,9 +15,10 @@
 // combined by a xor butterfly (16, 8, 4, 2, 1). No FMA contraction (the
 // products and sums are explicit __fmul_rn / __fadd_rn).
 //
-// Work split: one warp per chunk of 16 logical blocks of a (sequence, KV head);
-// a warp reads each block's two metadata rows with one 8-byte (D=128) load per
-// lane, i.e. 256 contiguous bytes per row per warp, all 16 blocks in flight.
+// Work split: a persistent grid; the (sequence, KV head, 8-block chunk) list
+// is cut into equal contiguous ranges, one per warp; a warp reads each
+// block's two metadata rows with one 8-byte (D=128) load per lane, i.e. 256
+// contiguous bytes per row per warp, a whole chunk in flight.
 //
 // Top-K: one CTA per (sequence, KV head): a 4-pass, 8-bit radix select over
 // the totalOrder keys of the scores finds the K-th largest key; blocks above
@@ -30,106 +31,150 @@ namespace pa {
 
 namespace {
 
-constexpr int kScoreWarps = 4;
 constexpr int kTopkThreads = 256;
 
-// One warp scores a chunk of up to kChunk consecutive logical blocks of one
-// (sequence, KV head): grid (ceil(MBS / (kChunk * kScoreWarps)), Hkv, B).
-// Every load is issued before any result is needed: the context length, the
-// chunk's block-table entries (one per lane) and the query group in one round
-// trip, then the metadata rows of all the chunk's blocks in a second.
-constexpr int kChunk = 16;
+// Persistent grid: the list of (sequence, KV head, chunk of kChunk logical
+// blocks) is cut into equal contiguous ranges, one per warp. A warp walks its
+// range: per chunk one round trip for the block-table entries (one per lane)
+// and one for both metadata rows of all the chunk's blocks; the query group's
+// P/N sums are formed once per (sequence, KV head).
+constexpr int kChunk = 8;
+constexpr int kScoreThreads = 256;
 
 template <int D>
-__global__ void __launch_bounds__(kScoreWarps * 32) quest_score_kernel(
+__global__ void __launch_bounds__(kScoreThreads, 4) quest_score_kernel(
     float *__restrict__ scores, const uint16_t *__restrict__ q, const uint16_t *__restrict__ kmin,
     const uint16_t *__restrict__ kmax, const int32_t *__restrict__ bt, int MBS,
     const int32_t *__restrict__ ctx, int B, int Hq, int Hkv, int BS, int64_t NB) {
     constexpr int C = D / 32;  // dims per lane
     constexpr int CW = C / 2;  // 32-bit words per lane per row
+    extern __shared__ int32_t pre[];  // [B+1] chunk prefix per KV head
     pdl_trigger();
     pdl_wait();
-    const int lane = threadIdx.x & 31;
-    const int b = blockIdx.z, kvh = blockIdx.y;
-    const int j0 = (blockIdx.x * kScoreWarps + (threadIdx.x >> 5)) * kChunk;
-    if (j0 >= MBS) return;
+    const int tid = threadIdx.x, lane = tid & 31;
     const int G = Hq / Hkv;
-    // round trip 1: ctx, block-table entries, query group
-    const int craw = __ldg(ctx + b);
-    const int ph_l = (lane < kChunk && j0 + lane < MBS) ? __ldg(bt + int64_t(b) * MBS + j0 + lane) : -1;
-    uint32_t qw[kMaxGroup][CW];
+    const int max_tok = MBS * BS;
+    for (int b = tid; b < B; b += kScoreThreads) {
+        const int c = min(max(__ldg(ctx + b), 0), max_tok);
+        pre[b + 1] = ((c + BS - 1) / BS + kChunk - 1) / kChunk;
+    }
+    if (tid == 0) pre[0] = 0;
+    __syncthreads();
+    if (tid < 32) {
+        int carry = 0;
+        for (int b0 = 0; b0 < B; b0 += 32) {
+            const int b = b0 + lane;
+            int v = (b < B) ? pre[b + 1] : 0;
 #pragma unroll
-    for (int gg = 0; gg < kMaxGroup; ++gg) {
-        if (gg < G) {
-            const uint16_t *qr = q + (int64_t(b) * Hq + int64_t(kvh) * G + gg) * D + lane * C;
-            if (C == 4) {
-                const uint2 v2 = __ldg(reinterpret_cast<const uint2 *>(qr));
-                qw[gg][0] = v2.x;
-                qw[gg][CW - 1] = v2.y;
-            } else {
-                qw[gg][0] = __ldg(reinterpret_cast<const uint32_t *>(qr));
+            for (int o = 1; o < 32; o <<= 1) {
+                const int u = __shfl_up_sync(0xffffffffu, v, o);
+                if (lane >= o) v += u;
             }
+            if (b < B) pre[b + 1] = carry + v;
+            carry += __shfl_sync(0xffffffffu, v, 31);
         }
     }
-    const int c = min(max(craw, 0), MBS * BS);
-    const int nblk = (c + BS - 1) / BS;
-    if (j0 >= nblk) return;
-    const int cnt = min(kChunk, nblk - j0);
-    // round trip 2: both metadata rows of every block of the chunk
-    uint32_t mnv[kChunk][CW], mxv[kChunk][CW];
-    bool ok[kChunk];
-#pragma unroll
-    for (int u = 0; u < kChunk; ++u) {
-        const int ph = __shfl_sync(0xffffffffu, ph_l, u);
-        ok[u] = (u < cnt) && ph >= 0 && int64_t(ph) < NB;
-        const int64_t off = (int64_t(ok[u] ? ph : 0) * Hkv + kvh) * D + lane * C;
-        if (C == 4) {
-            const uint2 a2 = __ldg(reinterpret_cast<const uint2 *>(kmin + off));
-            const uint2 b2 = __ldg(reinterpret_cast<const uint2 *>(kmax + off));
-            mnv[u][0] = a2.x;
-            mnv[u][CW - 1] = a2.y;
-            mxv[u][0] = b2.x;
-            mxv[u][CW - 1] = b2.y;
-        } else {
-            mnv[u][0] = __ldg(reinterpret_cast<const uint32_t *>(kmin + off));
-            mxv[u][0] = __ldg(reinterpret_cast<const uint32_t *>(kmax + off));
-        }
+    __syncthreads();
+    const int64_t total = int64_t(Hkv) * pre[B];
+    const int64_t W = int64_t(gridDim.x) * (kScoreThreads / 32);
+    const int64_t w = int64_t(blockIdx.x) * (kScoreThreads / 32) + (tid >> 5);
+    const int64_t R = (total + W - 1) / W;
+    int64_t id = w * R;
+    const int64_t id1 = min(total, id + R);
+    if (id >= id1) return;
+    // locate the first chunk
+    int lo = 0, hi = B;
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (int64_t(Hkv) * pre[mid] <= id) lo = mid; else hi = mid;
     }
-    // P_d = sum_h max(q, 0), N_d = sum_h min(q, 0), h ascending from +0
+    int b = lo;
+    int nch = pre[b + 1] - pre[b];
+    int kvh = int((id - int64_t(Hkv) * pre[b]) / nch);
+    int ch = int(id - int64_t(Hkv) * pre[b] - int64_t(kvh) * nch);
+    int pn_seg = -1;
     float P[C], N[C];
-#pragma unroll
-    for (int cc = 0; cc < C; ++cc) {
-        P[cc] = 0.f;
-        N[cc] = 0.f;
-    }
-#pragma unroll
-    for (int gg = 0; gg < kMaxGroup; ++gg) {
-        if (gg < G) {
+    for (; id < id1; ++id) {
+        const int c = min(max(__ldg(ctx + b), 0), max_tok);
+        const int nblk = (c + BS - 1) / BS;
+        const int j0 = ch * kChunk;
+        const int cnt = min(kChunk, nblk - j0);
+        const int ph_l = lane < cnt ? __ldg(bt + int64_t(b) * MBS + j0 + lane) : -1;
+        if (b * Hkv + kvh != pn_seg) {
+            // P_d = sum_h max(q, 0), N_d = sum_h min(q, 0), h ascending from +0
+            pn_seg = b * Hkv + kvh;
 #pragma unroll
             for (int cc = 0; cc < C; ++cc) {
-                const float v = (cc & 1) ? bf16_hi(qw[gg][cc >> 1]) : bf16_lo(qw[gg][cc >> 1]);
-                P[cc] = __fadd_rn(P[cc], v > 0.f ? v : 0.f);
-                N[cc] = __fadd_rn(N[cc], v < 0.f ? v : 0.f);
+                P[cc] = 0.f;
+                N[cc] = 0.f;
+            }
+            for (int gg = 0; gg < G; ++gg) {
+                const uint16_t *qr = q + (int64_t(b) * Hq + int64_t(kvh) * G + gg) * D + lane * C;
+                uint32_t qw[CW];
+                if (C == 4) {
+                    const uint2 v2 = __ldg(reinterpret_cast<const uint2 *>(qr));
+                    qw[0] = v2.x;
+                    qw[CW - 1] = v2.y;
+                } else {
+                    qw[0] = __ldg(reinterpret_cast<const uint32_t *>(qr));
+                }
+#pragma unroll
+                for (int cc = 0; cc < C; ++cc) {
+                    const float v = (cc & 1) ? bf16_hi(qw[cc >> 1]) : bf16_lo(qw[cc >> 1]);
+                    P[cc] = __fadd_rn(P[cc], v > 0.f ? v : 0.f);
+                    N[cc] = __fadd_rn(N[cc], v < 0.f ? v : 0.f);
+                }
+            }
+        }
+        uint32_t mnv[kChunk][CW], mxv[kChunk][CW];
+        bool ok[kChunk];
+#pragma unroll
+        for (int u = 0; u < kChunk; ++u) {
+            const int ph = __shfl_sync(0xffffffffu, ph_l, u);
+            ok[u] = (u < cnt) && ph >= 0 && int64_t(ph) < NB;
+            const int64_t off = (int64_t(ok[u] ? ph : 0) * Hkv + kvh) * D + lane * C;
+            if (C == 4) {
+                const uint2 a2 = __ldg(reinterpret_cast<const uint2 *>(kmin + off));
+                const uint2 b2 = __ldg(reinterpret_cast<const uint2 *>(kmax + off));
+                mnv[u][0] = a2.x;
+                mnv[u][CW - 1] = a2.y;
+                mxv[u][0] = b2.x;
+                mxv[u][CW - 1] = b2.y;
+            } else {
+                mnv[u][0] = __ldg(reinterpret_cast<const uint32_t *>(kmin + off));
+                mxv[u][0] = __ldg(reinterpret_cast<const uint32_t *>(kmax + off));
+            }
+        }
+        float mine = -INFINITY;  // lane u keeps block j0 + u's score
+#pragma unroll
+        for (int u = 0; u < kChunk; ++u) {
+            float acc = 0.f;
+#pragma unroll
+            for (int cc = 0; cc < C; ++cc) {
+                const uint32_t wmn = mnv[u][cc >> 1], wmx = mxv[u][cc >> 1];
+                const float mn = (cc & 1) ? bf16_hi(wmn) : bf16_lo(wmn);
+                const float mx = (cc & 1) ? bf16_hi(wmx) : bf16_lo(wmx);
+                const float t = __fadd_rn(__fmul_rn(P[cc], mx), __fmul_rn(N[cc], mn));
+                acc = (cc == 0) ? t : __fadd_rn(acc, t);
+            }
+#pragma unroll
+            for (int o = 16; o >= 1; o >>= 1) acc = __fadd_rn(acc, __shfl_xor_sync(0xffffffffu, acc, o));
+            if (lane == u) mine = ok[u] ? acc : -INFINITY;
+        }
+        if (lane < cnt) scores[(int64_t(b) * Hkv + kvh) * MBS + j0 + lane] = mine;
+        // next chunk
+        if (++ch == nch) {
+            ch = 0;
+            if (++kvh == Hkv) {
+                kvh = 0;
+                do {
+                    ++b;
+                } while (b < B && pre[b + 1] == pre[b]);
+                if (b >= B) break;
+                nch = pre[b + 1] - pre[b];
             }
         }
     }
-    float mine = -INFINITY;  // lane u keeps block j0 + u's score
-#pragma unroll
-    for (int u = 0; u < kChunk; ++u) {
-        float acc = 0.f;
-#pragma unroll
-        for (int cc = 0; cc < C; ++cc) {
-            const uint32_t wmn = mnv[u][cc >> 1], wmx = mxv[u][cc >> 1];
-            const float mn = (cc & 1) ? bf16_hi(wmn) : bf16_lo(wmn);
-            const float mx = (cc & 1) ? bf16_hi(wmx) : bf16_lo(wmx);
-            const float t = __fadd_rn(__fmul_rn(P[cc], mx), __fmul_rn(N[cc], mn));
-            acc = (cc == 0) ? t : __fadd_rn(acc, t);
-        }
-#pragma unroll
-        for (int o = 16; o >= 1; o >>= 1) acc = __fadd_rn(acc, __shfl_xor_sync(0xffffffffu, acc, o));
-        if (lane == u) mine = ok[u] ? acc : -INFINITY;
-    }
-    if (lane < cnt) scores[(int64_t(b) * Hkv + kvh) * MBS + j0 + lane] = mine;
 }
 
 // block-wide exclusive scan of a 0/1 flag (kTopkThreads threads)
@@ -244,10 +289,20 @@ template <int D>
 cudaError_t launch_score(float *scores, const uint16_t *q, const uint16_t *kmin,
                          const uint16_t *kmax, const int32_t *bt, int MBS, const int32_t *ctx,
                          int B, int Hq, int Hkv, int BS, int64_t NB, cudaStream_t stream) {
-    const dim3 grid{unsigned((MBS + kChunk * kScoreWarps - 1) / (kChunk * kScoreWarps)), unsigned(Hkv),
-                    unsigned(B)};
-    return launch_pdl(quest_score_kernel<D>, grid, dim3(kScoreWarps * 32), 0, stream, scores, q, kmin,
-                      kmax, bt, MBS, ctx, B, Hq, Hkv, BS, NB);
+    static int grid = 0;  // persistent grid: every SM full
+    const size_t smem = size_t(B + 1) * 4;
+    if (!grid) {
+        int dev = 0, sms = 0, per_sm = 0;
+        cudaError_t e;
+        if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+        if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, quest_score_kernel<D>, kScoreThreads,
+                                                          size_t(kMaxBatch + 1) * 4);
+        if (e != cudaSuccess) return e;
+        grid = sms * (per_sm < 1 ? 1 : per_sm);
+    }
+    return launch_pdl(quest_score_kernel<D>, dim3(grid), dim3(kScoreThreads), smem, stream, scores, q,
+                      kmin, kmax, bt, MBS, ctx, B, Hq, Hkv, BS, NB);
 }
 
 }  // namespace
