@@ -60,6 +60,13 @@ __device__ __forceinline__ int atomic_add_acq_rel_gpu(int *p, int v) {
     return old;
 }
 
+// Relaxed load at GPU scope (a counter other CTAs update atomically).
+__device__ __forceinline__ int ld_relaxed_s32(const int *p) {
+    int v;
+    asm volatile("ld.relaxed.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
 // Programmatic dependent launch: a kernel launched with programmatic stream
 // serialization may start while the previous kernel in the stream is still
 // running; pdl_wait() blocks until that kernel has completed and its memory

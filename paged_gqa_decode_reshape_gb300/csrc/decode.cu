@@ -327,7 +327,6 @@ __global__ void __launch_bounds__(DecodeCfg<D>::THREADS, 1)
 
     // ==================================================================== consumers
     const int c_id = warp;  // 0 .. NC-1
-    const int ctid = tid;   // 0 .. NC*32-1
     const int g = lane >> 2, q4 = lane & 3;
     const float scale_log2 = a.scale_log2;
     uint32_t qb[NKK][2];
@@ -455,8 +454,11 @@ __global__ void __launch_bounds__(DecodeCfg<D>::THREADS, 1)
     const int h4 = (lane & 1) * 4;
 
     // merge the CTA pieces of segment `seg` (run by one warp of the last CTA
-    // to arrive), pieces in order with a running max per head
-    auto combine = [&](int seg, int64_t s0, int64_t e0) {
+    // to arrive), pieces in order with a running max per head; piece `own`
+    // (or none: -1) comes from registers (log2-sum-exp ol, normalised ox)
+    // instead of the workspace
+    auto combine = [&](int seg, int64_t s0, int64_t e0, int own, const float (&ol)[4],
+                       const float4 (&ox)[NSL]) {
         const int w0 = int(s0 / L), np = int((e0 - 1) / L) - w0 + 1;
         const float *pb = a.part + int64_t(seg + w0) * C::PART;
         float M[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
@@ -471,6 +473,12 @@ __global__ void __launch_bounds__(DecodeCfg<D>::THREADS, 1)
             float4 lx[U], xv[U][NSL];
 #pragma unroll
             for (int u = 0; u < U; ++u) {
+                if (i0 + u == own) {
+                    lx[u] = make_float4(ol[0], ol[1], ol[2], ol[3]);
+#pragma unroll
+                    for (int r = 0; r < NSL; ++r) xv[u][r] = ox[r];
+                    continue;
+                }
                 const float *ps = pb + int64_t(min(i0 + u, np - 1)) * C::PART;
                 lx[u] = __ldcg(reinterpret_cast<const float4 *>(ps + D * 8 + h4));
 #pragma unroll
@@ -567,6 +575,9 @@ __global__ void __launch_bounds__(DecodeCfg<D>::THREADS, 1)
 
         // ---- this warp merges the NC states
         if (last_seg) PA_TRACE_LANE(5);
+        // pieces of a split segment already counted (read while merging)
+        int seen = 0;
+        if (!whole && lane == 0) seen = ld_relaxed_s32(a.counters + seg);
         float M[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
         float mc[NC][4], lc[NC][4];
 #pragma unroll
@@ -621,36 +632,56 @@ __global__ void __launch_bounds__(DecodeCfg<D>::THREADS, 1)
             if (last_seg) PA_TRACE_LANE(4);
             return;
         }
-        float *ps = a.part + int64_t(seg + blockIdx.x) * C::PART;
-        float inv[4];
+        // this CTA's piece, normalised, and its log2-sum-exp
+        float inv[4], lse[4];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) inv[e] = Ls[e] > 0.f ? 1.f / Ls[e] : 0.f;
+        for (int e = 0; e < 4; ++e) {
+            inv[e] = Ls[e] > 0.f ? 1.f / Ls[e] : 0.f;
+            lse[e] = Ls[e] > 0.f ? M[e] + log2f(Ls[e]) : -INFINITY;
+        }
+        float4 ox[NSL];
+#pragma unroll
+        for (int r = 0; r < NSL; ++r)
+            ox[r] = make_float4(O[r][0] * inv[0], O[r][1] * inv[1], O[r][2] * inv[2], O[r][3] * inv[3]);
+        const int w0 = int(s0 / L);
+        const int npieces = int((e0 - 1) / L) - w0 + 1;
+        seen = __shfl_sync(0xffffffffu, seen, 0);
+        if (seen == npieces - 1) {
+            // Every other piece has been counted, so this one completes the
+            // segment: combine from registers, without publishing it. The
+            // fence makes the counted pieces' partials visible to the loads.
+            __threadfence();
+            if (last_seg) PA_TRACE_LANE(6);
+            combine(seg, s0, e0, int(blockIdx.x) - w0, lse, ox);
+            if (lane == 0) a.counters[seg] = 0;
+            if (last_seg) {
+                PA_TRACE_LANE(7);
+                PA_TRACE_LANE(4);
+            }
+            return;
+        }
+        float *ps = a.part + int64_t(seg + blockIdx.x) * C::PART;
 #pragma unroll
         for (int r = 0; r < NSL; ++r) {
             const int d = (lane >> 1) + 16 * r;
-            __stcg(reinterpret_cast<float4 *>(ps + d * 8 + h4),
-                   make_float4(O[r][0] * inv[0], O[r][1] * inv[1], O[r][2] * inv[2], O[r][3] * inv[3]));
+            __stcg(reinterpret_cast<float4 *>(ps + d * 8 + h4), ox[r]);
         }
-        if (lane < 2) {
-            float lse[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) lse[e] = Ls[e] > 0.f ? M[e] + log2f(Ls[e]) : -INFINITY;
+        if (lane < 2)
             __stcg(reinterpret_cast<float4 *>(ps + D * 8 + h4), make_float4(lse[0], lse[1], lse[2], lse[3]));
-        }
         __syncwarp();
         int last = 0;
         if (lane == 0) {
             // release this CTA's partial (written by the warp, ordered by the
             // warp barrier) and acquire the pieces counted before it
             __threadfence_block();
-            const int npieces = int((e0 - 1) / L - s0 / L) + 1;
             last = (atomic_add_acq_rel_gpu(a.counters + seg, 1) == npieces - 1);
         }
         last = __shfl_sync(0xffffffffu, last, 0);
         __syncwarp();  // every lane's reads of the pieces follow lane 0's acquire
         if (last_seg) PA_TRACE_LANE(6);
         if (last) {
-            combine(seg, s0, e0);
+            const float nol[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+            combine(seg, s0, e0, -1, nol, ox);
             if (lane == 0) a.counters[seg] = 0;
             if (last_seg) PA_TRACE_LANE(7);
         }
