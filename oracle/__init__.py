@@ -73,6 +73,21 @@ def lib():
             L.oracle_quest_scores.restype = i32
             L.oracle_quest_topk.argtypes = [vp, vp, i32, vp, i32, i32, i32, i32]
             L.oracle_quest_topk.restype = i32
+            L.oracle_e4m3_encode_array.argtypes = [vp, vp, i64]
+            L.oracle_e4m3_encode_array.restype = None
+            L.oracle_e4m3_decode_array.argtypes = [vp, vp, i64]
+            L.oracle_e4m3_decode_array.restype = None
+            L.oracle_reshape_and_cache_fp8.argtypes = [vp, vp, vp, vp, vp, i64, vp, vp, i32, i32, i32, i64]
+            L.oracle_reshape_and_cache_fp8.restype = i64
+            L.oracle_quest_update_meta_fp8.argtypes = [vp, vp, vp, vp, i64, vp, i32, i32, i32, i64]
+            L.oracle_quest_update_meta_fp8.restype = i64
+            L.oracle_quest_rebuild_meta_fp8.argtypes = [vp, vp, vp, vp, i32, vp, i32, i32, i32, i32, i64]
+            L.oracle_quest_rebuild_meta_fp8.restype = i32
+            L.oracle_attention_fp8.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, vp, vp, i32,
+                                               i32, i32, i32, i32, i32, i64, f64, vp, i64]
+            L.oracle_attention_fp8.restype = i32
+            L.oracle_quest_scores_fp8.argtypes = [vp, vp, vp, vp, vp, i32, vp, i32, i32, i32, i32, i32, i64]
+            L.oracle_quest_scores_fp8.restype = i32
             _lib = L
     return _lib
 
@@ -246,4 +261,118 @@ def quest_topk(scores, context_lens, BS: int, topk: int):
 def quest_select(q, kmin, kmax, block_tables, context_lens, BS: int, topk: int):
     """Scores then top-K: the selection the Quest path attends over."""
     return quest_topk(quest_scores(q, kmin, kmax, block_tables, context_lens, BS),
+                      context_lens, BS, topk)
+
+
+# ------------------------------------------------------- fp8 (E4M3) cache
+
+
+def e4m3_encode(x) -> np.ndarray:
+    """Nearest E4M3 code of every fp32 value (ties to even, +-448 saturation, NaN -> 0x7F)."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    out = np.empty(x.shape, dtype=np.uint8)
+    lib().oracle_e4m3_encode_array(_p(x), _p(out), x.size)
+    return out
+
+
+def e4m3_decode(codes) -> np.ndarray:
+    """Value of every E4M3 code (float64, NaN for 0x7F / 0xFF)."""
+    c = np.ascontiguousarray(codes, dtype=np.uint8)
+    out = np.empty(c.shape, dtype=np.float64)
+    lib().oracle_e4m3_decode_array(_p(c), _p(out), c.size)
+    return out
+
+
+def reshape_and_cache_fp8(key, value, key_cache, value_cache, slot_mapping, k_scale, v_scale) -> int:
+    """Quantise and scatter new K/V rows into uint8 E4M3 caches IN PLACE; returns #out-of-pool slots."""
+    assert key_cache.dtype == np.uint8 and key_cache.flags.c_contiguous
+    assert value_cache.dtype == np.uint8 and value_cache.flags.c_contiguous
+    NB, BS, Hkv, D = key_cache.shape
+    key = _c(key, np.uint16)
+    value = _c(value, np.uint16)
+    slots = _c(slot_mapping, np.int64)
+    ks = _c(k_scale, np.float32)
+    vs = _c(v_scale, np.float32)
+    assert ks.shape == (Hkv,) and vs.shape == (Hkv,)
+    return int(lib().oracle_reshape_and_cache_fp8(_p(key), _p(value), _p(key_cache), _p(value_cache),
+                                                  _p(slots), slots.shape[0], _p(ks), _p(vs), Hkv, D, BS,
+                                                  NB))
+
+
+def quest_update_meta_fp8(kmin, kmax, key, slot_mapping, k_scale, BS: int) -> int:
+    """Incremental Quest metadata (E4M3 codes) update IN PLACE; returns #out-of-pool slots."""
+    assert kmin.dtype == np.uint8 and kmin.flags.c_contiguous
+    assert kmax.dtype == np.uint8 and kmax.flags.c_contiguous
+    NB, Hkv, D = kmin.shape
+    key = _c(key, np.uint16)
+    slots = _c(slot_mapping, np.int64)
+    ks = _c(k_scale, np.float32)
+    return int(lib().oracle_quest_update_meta_fp8(_p(kmin), _p(kmax), _p(key), _p(slots),
+                                                  slots.shape[0], _p(ks), Hkv, D, BS, NB))
+
+
+def quest_rebuild_meta_fp8(key_cache, block_tables, context_lens, kmin=None, kmax=None):
+    """E4M3 metadata of every block a sequence uses, from an E4M3 cache. Returns (kmin, kmax)."""
+    NB, BS, Hkv, D = key_cache.shape
+    if kmin is None:
+        kmin = np.zeros((NB, Hkv, D), dtype=np.uint8)
+    if kmax is None:
+        kmax = np.zeros((NB, Hkv, D), dtype=np.uint8)
+    kc = _c(key_cache, np.uint8)
+    bt = _c(block_tables, np.int32)
+    ctx = _c(context_lens, np.int32)
+    rc = lib().oracle_quest_rebuild_meta_fp8(_p(kmin), _p(kmax), _p(kc), _p(bt), bt.shape[1],
+                                             _p(ctx), bt.shape[0], Hkv, D, BS, NB)
+    _check(rc, "quest_rebuild_meta_fp8")
+    return kmin, kmax
+
+
+def attention_fp8(q, key_cache, value_cache, k_scale, v_scale, block_tables, context_lens, scale,
+                  selected=None, rows=None):
+    """Dense (selected None) or Quest sparse attention over E4M3 caches, fp64."""
+    q = _c(q, np.uint16)
+    kc = _c(key_cache, np.uint8)
+    vc = _c(value_cache, np.uint8)
+    ks = _c(k_scale, np.float32)
+    vs = _c(v_scale, np.float32)
+    bt = _c(block_tables, np.int32)
+    ctx = _c(context_lens, np.int32)
+    B, Hq, D = q.shape
+    NB, BS, Hkv, D2 = kc.shape
+    assert D == D2 and vc.shape == kc.shape and ks.shape == (Hkv,) and vs.shape == (Hkv,)
+    sel, topk = None, 0
+    if selected is not None:
+        sel = _c(selected, np.int32)
+        assert sel.shape[:2] == (B, Hkv)
+        topk = sel.shape[2]
+    r, nr = _rows_arg(rows)
+    out = np.zeros((nr, D) if r is not None else (B, Hq, D), dtype=np.float64)
+    rc = lib().oracle_attention_fp8(_p(out), _p(q), _p(kc), _p(vc), _p(ks), _p(vs), _p(bt),
+                                    bt.shape[1], _p(ctx), _p(sel), topk, B, Hq, Hkv, D, BS, NB,
+                                    float(scale), _p(r), nr)
+    _check(rc, "attention_fp8")
+    return out
+
+
+def quest_scores_fp8(q, kmin, kmax, block_tables, context_lens, BS: int):
+    """Quest block scores [B, Hkv, MBS] float32 on E4M3 metadata."""
+    q = _c(q, np.uint16)
+    kmin = _c(kmin, np.uint8)
+    kmax = _c(kmax, np.uint8)
+    bt = _c(block_tables, np.int32)
+    ctx = _c(context_lens, np.int32)
+    B, Hq, D = q.shape
+    NB, Hkv, D2 = kmin.shape
+    assert D == D2
+    MBS = bt.shape[1]
+    out = np.empty((B, Hkv, MBS), dtype=np.float32)
+    rc = lib().oracle_quest_scores_fp8(_p(out), _p(q), _p(kmin), _p(kmax), _p(bt), MBS, _p(ctx),
+                                       B, Hq, Hkv, D, BS, NB)
+    _check(rc, "quest_scores_fp8")
+    return out
+
+
+def quest_select_fp8(q, kmin, kmax, block_tables, context_lens, BS: int, topk: int):
+    """Scores on E4M3 metadata then top-K."""
+    return quest_topk(quest_scores_fp8(q, kmin, kmax, block_tables, context_lens, BS),
                       context_lens, BS, topk)

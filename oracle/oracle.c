@@ -69,6 +69,89 @@ static uint32_t f32_order_key(float f)
     return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
+/* ------------------------------------------------- 8-bit float (E4M3) */
+
+/* The E4M3 variant of the OCP 8-bit floating-point format (the "fn" variant:
+ * no infinities). Bit 7 is the sign, bits 6..3 the exponent field e (bias 7),
+ * bits 2..0 the mantissa m:
+ *   e = 0:          (-1)^s * (m / 8) * 2^-6          (zero and subnormals)
+ *   e = 1 .. 15:    (-1)^s * (1 + m / 8) * 2^(e - 7)
+ *   e = 15, m = 7:  NaN (0x7F and 0xFF).
+ * Largest finite magnitude 448 (0x7E), smallest nonzero 2^-9 (0x01). */
+double oracle_e4m3_decode(uint8_t c)
+{
+    const int sgn = (c >> 7) & 1, e = (c >> 3) & 15, m = c & 7;
+    if (e == 15 && m == 7)
+        return NAN;
+    const double mag = e == 0 ? ldexp((double)m / 8.0, -6) : ldexp(1.0 + (double)m / 8.0, e - 7);
+    return sgn ? -mag : mag;
+}
+
+/* Nearest E4M3 value to x, ties to the even mantissa; magnitudes beyond 448
+ * (infinities included) saturate to +-448; NaN gives 0x7F. The grid spacing
+ * is 2^(E-3) in the binade [2^E, 2^(E+1)) for E >= -6 and 2^-9 below 2^-6,
+ * so x / spacing is exact in double and is rounded to an integer. */
+uint8_t oracle_e4m3_encode(float x)
+{
+    if (isnan(x))
+        return 0x7F;
+    const uint8_t sgn = signbit(x) ? 0x80 : 0x00;
+    const double a = fabs((double)x);
+    if (a >= 448.0)
+        return sgn | 0x7E;
+    int E = 0;
+    if (a > 0.0) {
+        (void)frexp(a, &E); /* a = f * 2^E, f in [0.5, 1): binade exponent E - 1 */
+        E -= 1;
+    }
+    if (a == 0.0 || E < -6)
+        E = -6;
+    const double q = ldexp(1.0, E - 3);
+    const double n = a / q;
+    double r = floor(n);
+    const double frac = n - r;
+    if (frac > 0.5 || (frac == 0.5 && fmod(r, 2.0) == 1.0))
+        r += 1.0;
+    const double v = r * q; /* <= 448: 448 is on the grid and a < 448 */
+    if (v == 0.0)
+        return sgn;
+    if (v < ldexp(1.0, -6))
+        return sgn | (uint8_t)(v / ldexp(1.0, -9));
+    int ev = 0;
+    (void)frexp(v, &ev);
+    ev -= 1; /* v in [2^ev, 2^(ev+1)) */
+    const int mant = (int)((v / ldexp(1.0, ev) - 1.0) * 8.0);
+    return sgn | (uint8_t)(((ev + 7) << 3) | mant);
+}
+
+/* encode / decode whole arrays (for the tests) */
+void oracle_e4m3_encode_array(const float *x, uint8_t *c, int64_t n)
+{
+    for (int64_t i = 0; i < n; ++i)
+        c[i] = oracle_e4m3_encode(x[i]);
+}
+
+void oracle_e4m3_decode_array(const uint8_t *c, double *x, int64_t n)
+{
+    for (int64_t i = 0; i < n; ++i)
+        x[i] = oracle_e4m3_decode(c[i]);
+}
+
+/* Order key of an E4M3 code: numeric order for non-NaN codes, -0 below +0
+ * (the same totalOrder convention as the bf16 metadata). */
+static uint8_t e4m3_order_key(uint8_t c)
+{
+    return (c & 0x80u) ? (uint8_t)(~c & 0x7Fu) : (uint8_t)(c | 0x80u);
+}
+
+/* code of one bf16 element quantised with a per-KV-head scale:
+ * e4m3(fl32(x / scale)) */
+static uint8_t quantize(uint16_t x, float scale)
+{
+    const float y = bf16_f32(x) / scale;
+    return oracle_e4m3_encode(y);
+}
+
 /* ------------------------------------------------------ ReshapeAndCache */
 
 /* [P1] "ReshapeAndCache": for every new token t with slot = slot_mapping[t]:
@@ -211,6 +294,137 @@ int oracle_quest_rebuild_meta(uint16_t *kmin, uint16_t *kmax,
     return 0;
 }
 
+/* ------------------------------------------- fp8 KV cache: write path */
+
+/* ReshapeAndCache into an E4M3 cache: the same slot arithmetic as
+ * oracle_reshape_and_cache; element d of KV head h of the token's K row is
+ * stored as e4m3(fl32(k / k_scale[h])), likewise V with v_scale[h].
+ * Returns the number of out-of-pool slots skipped. */
+int64_t oracle_reshape_and_cache_fp8(const uint16_t *key, const uint16_t *value,
+                                     uint8_t *key_cache, uint8_t *value_cache,
+                                     const int64_t *slot_mapping, int64_t T,
+                                     const float *k_scale, const float *v_scale,
+                                     int Hkv, int D, int BS, int64_t NB)
+{
+    const int64_t row = (int64_t)Hkv * D;
+    int64_t out_of_range = 0;
+    for (int64_t t = 0; t < T; ++t) {
+        const int64_t slot = slot_mapping[t];
+        if (slot < 0)
+            continue;
+        const int64_t block_idx = slot / BS;
+        const int64_t block_offset = slot % BS;
+        if (block_idx >= NB) {
+            ++out_of_range;
+            continue;
+        }
+        const int64_t dst = (block_idx * BS + block_offset) * row;
+        for (int64_t e = 0; e < row; ++e) {
+            const int h = (int)(e / D);
+            key_cache[dst + e] = quantize(key[t * row + e], k_scale[h]);
+            value_cache[dst + e] = quantize(value[t * row + e], v_scale[h]);
+        }
+    }
+    return out_of_range;
+}
+
+/* Quest metadata of an E4M3 cache: per physical block and KV head, the
+ * elementwise min / max of the stored K codes (numeric order, -0 < +0), with
+ * the update rule of oracle_quest_update_meta (reset when a token of the call
+ * lands at offset 0 of the block, else merge). The new tokens' codes are
+ * e4m3(fl32(k / k_scale[h])), as in the cache. */
+int64_t oracle_quest_update_meta_fp8(uint8_t *kmin, uint8_t *kmax, const uint16_t *key,
+                                     const int64_t *slot_mapping, int64_t T,
+                                     const float *k_scale, int Hkv, int D, int BS, int64_t NB)
+{
+    const int64_t row = (int64_t)Hkv * D;
+    int64_t out_of_range = 0;
+    unsigned char *done = (unsigned char *)calloc((size_t)T, 1);
+    uint8_t *lo = (uint8_t *)malloc((size_t)row);
+    uint8_t *hi = (uint8_t *)malloc((size_t)row);
+    for (int64_t t = 0; t < T; ++t) {
+        const int64_t s = slot_mapping[t];
+        if (s < 0 || done[t])
+            continue;
+        const int64_t p = s / BS;
+        if (p >= NB) {
+            ++out_of_range;
+            done[t] = 1;
+            continue;
+        }
+        int reset = 0;
+        for (int64_t u = t; u < T; ++u) {
+            const int64_t su = slot_mapping[u];
+            if (su >= 0 && su / BS == p && su % BS == 0)
+                reset = 1;
+        }
+        int have = 0;
+        if (!reset) {
+            memcpy(lo, kmin + p * row, (size_t)row);
+            memcpy(hi, kmax + p * row, (size_t)row);
+            have = 1;
+        }
+        for (int64_t u = t; u < T; ++u) {
+            const int64_t su = slot_mapping[u];
+            if (su < 0 || su / BS != p)
+                continue;
+            done[u] = 1;
+            for (int64_t e = 0; e < row; ++e) {
+                const uint8_t c = quantize(key[u * row + e], k_scale[e / D]);
+                if (!have) {
+                    lo[e] = c;
+                    hi[e] = c;
+                } else {
+                    if (e4m3_order_key(c) < e4m3_order_key(lo[e]))
+                        lo[e] = c;
+                    if (e4m3_order_key(c) > e4m3_order_key(hi[e]))
+                        hi[e] = c;
+                }
+            }
+            have = 1;
+        }
+        memcpy(kmin + p * row, lo, (size_t)row);
+        memcpy(kmax + p * row, hi, (size_t)row);
+    }
+    free(done);
+    free(lo);
+    free(hi);
+    return out_of_range;
+}
+
+/* Metadata of an E4M3 cache from scratch (as oracle_quest_rebuild_meta, on
+ * the stored codes). */
+int oracle_quest_rebuild_meta_fp8(uint8_t *kmin, uint8_t *kmax, const uint8_t *key_cache,
+                                  const int32_t *block_tables, int MBS,
+                                  const int32_t *context_lens, int B,
+                                  int Hkv, int D, int BS, int64_t NB)
+{
+    const int64_t row = (int64_t)Hkv * D;
+    for (int b = 0; b < B; ++b) {
+        const int64_t ctx = context_lens[b] > 0 ? context_lens[b] : 0;
+        const int64_t nblk = (ctx + BS - 1) / BS;
+        for (int64_t j = 0; j < nblk && j < MBS; ++j) {
+            const int64_t p = block_tables[(int64_t)b * MBS + j];
+            if (p < 0 || p >= NB)
+                return -1;
+            const int64_t t_end = (j + 1) * BS < ctx ? (j + 1) * BS : ctx;
+            for (int64_t e = 0; e < row; ++e) {
+                uint8_t lo = 0, hi = 0;
+                for (int64_t t = j * BS; t < t_end; ++t) {
+                    const uint8_t v = key_cache[(p * BS + (t % BS)) * row + e];
+                    if (t == j * BS || e4m3_order_key(v) < e4m3_order_key(lo))
+                        lo = v;
+                    if (t == j * BS || e4m3_order_key(v) > e4m3_order_key(hi))
+                        hi = v;
+                }
+                kmin[p * row + e] = lo;
+                kmax[p * row + e] = hi;
+            }
+        }
+    }
+    return 0;
+}
+
 /* ------------------------------------------------------------ attention */
 
 /* The tokens one (sequence, KV head) attends to, in order.
@@ -240,31 +454,47 @@ static int64_t token_list(int64_t *pos, int64_t ctx, int BS,
     return n;
 }
 
-/* Address of K (or V) of sequence position t for one KV head through the
- * block table ([P2] 2.6: K_cache[physical_block][block_size][kv_head][head_dim],
- * block_table[seq][logical_block] = physical_block). NULL if the table entry
- * is outside the pool. */
-static const uint16_t *kv_row(const uint16_t *cache, const int32_t *bt_row,
-                              int64_t t, int kvh, int Hkv, int D, int BS, int64_t NB)
+/* A K or V cache as the attention reads it: bf16 elements, or E4M3 codes
+ * with one fp32 scale per KV head (element value = decode(code) * scale,
+ * exact in fp64). */
+typedef struct {
+    const uint16_t *bf16;
+    const uint8_t *e4m3;
+    const float *scale;
+} kvsrc;
+
+static double kv_val(const kvsrc *c, int64_t idx, int kvh)
+{
+    if (c->bf16)
+        return bf16_val(c->bf16[idx]);
+    return oracle_e4m3_decode(c->e4m3[idx]) * (double)c->scale[kvh];
+}
+
+/* Element index of K (or V) of sequence position t for one KV head through
+ * the block table ([P2] 2.6: K_cache[physical_block][block_size][kv_head]
+ * [head_dim], block_table[seq][logical_block] = physical_block); -1 if the
+ * table entry is outside the pool. */
+static int64_t kv_index(const int32_t *bt_row, int64_t t, int kvh, int Hkv, int D, int BS,
+                        int64_t NB)
 {
     const int64_t p = bt_row[t / BS];
     if (p < 0 || p >= NB)
-        return NULL;
-    return cache + ((p * BS + t % BS) * Hkv + kvh) * (int64_t)D;
+        return -1;
+    return ((p * BS + t % BS) * Hkv + kvh) * (int64_t)D;
 }
 
 /* scores s_i = scale * q . K[pos_i] for every listed position (fp64). */
-static int compute_scores(double *s, const uint16_t *qrow, const uint16_t *key_cache,
+static int compute_scores(double *s, const uint16_t *qrow, const kvsrc *K,
                           const int32_t *bt_row, const int64_t *pos, int64_t n,
                           int kvh, int Hkv, int D, int BS, int64_t NB, double scale)
 {
     for (int64_t i = 0; i < n; ++i) {
-        const uint16_t *k = kv_row(key_cache, bt_row, pos[i], kvh, Hkv, D, BS, NB);
-        if (!k)
+        const int64_t k = kv_index(bt_row, pos[i], kvh, Hkv, D, BS, NB);
+        if (k < 0)
             return -1;
         double dot = 0.0;
         for (int d = 0; d < D; ++d)
-            dot += bf16_val(qrow[d]) * bf16_val(k[d]);
+            dot += bf16_val(qrow[d]) * kv_val(K, k + d, kvh);
         s[i] = scale * dot;
     }
     return 0;
@@ -273,8 +503,7 @@ static int compute_scores(double *s, const uint16_t *qrow, const uint16_t *key_c
 /* Reference form: explicit two-pass softmax over the listed tokens,
  *   m = max_i s_i, p_i = exp(s_i - m), l = sum p_i, out = sum p_i V_i / l.
  * An empty token list gives a zero output. */
-static int attend_two_pass(double *out, const uint16_t *qrow,
-                           const uint16_t *key_cache, const uint16_t *value_cache,
+static int attend_two_pass(double *out, const uint16_t *qrow, const kvsrc *K, const kvsrc *V,
                            const int32_t *bt_row, const int64_t *pos, int64_t n,
                            int kvh, int Hkv, int D, int BS, int64_t NB,
                            double scale, double *s)
@@ -283,7 +512,7 @@ static int attend_two_pass(double *out, const uint16_t *qrow,
         out[d] = 0.0;
     if (n == 0)
         return 0;
-    if (compute_scores(s, qrow, key_cache, bt_row, pos, n, kvh, Hkv, D, BS, NB, scale))
+    if (compute_scores(s, qrow, K, bt_row, pos, n, kvh, Hkv, D, BS, NB, scale))
         return -1;
     double m = -INFINITY;
     for (int64_t i = 0; i < n; ++i)
@@ -293,9 +522,9 @@ static int attend_two_pass(double *out, const uint16_t *qrow,
     for (int64_t i = 0; i < n; ++i) {
         const double p = exp(s[i] - m);
         l += p;
-        const uint16_t *v = kv_row(value_cache, bt_row, pos[i], kvh, Hkv, D, BS, NB);
+        const int64_t v = kv_index(bt_row, pos[i], kvh, Hkv, D, BS, NB);
         for (int d = 0; d < D; ++d)
-            out[d] += p * bf16_val(v[d]);
+            out[d] += p * kv_val(V, v + d, kvh);
     }
     for (int d = 0; d < D; ++d)
         out[d] /= l;
@@ -307,8 +536,7 @@ static int attend_two_pass(double *out, const uint16_t *qrow,
  * when a chunk raises the max, the old l and acc are rescaled by
  * exp(m_old - m_new). The full score vector is not needed by the method (the
  * scores buffer here is only a convenience). */
-static int attend_online(double *out, const uint16_t *qrow,
-                         const uint16_t *key_cache, const uint16_t *value_cache,
+static int attend_online(double *out, const uint16_t *qrow, const kvsrc *K, const kvsrc *V,
                          const int32_t *bt_row, const int64_t *pos, int64_t n,
                          int kvh, int Hkv, int D, int BS, int64_t NB,
                          double scale, int64_t chunk, double *s, double *acc)
@@ -319,7 +547,7 @@ static int attend_online(double *out, const uint16_t *qrow,
     }
     if (n == 0)
         return 0;
-    if (compute_scores(s, qrow, key_cache, bt_row, pos, n, kvh, Hkv, D, BS, NB, scale))
+    if (compute_scores(s, qrow, K, bt_row, pos, n, kvh, Hkv, D, BS, NB, scale))
         return -1;
     double m = -INFINITY, l = 0.0;
     for (int64_t c0 = 0; c0 < n; c0 += chunk) {
@@ -336,9 +564,9 @@ static int attend_online(double *out, const uint16_t *qrow,
         for (int64_t i = c0; i < c1; ++i) {
             const double p = exp(s[i] - m_new);
             l += p;
-            const uint16_t *v = kv_row(value_cache, bt_row, pos[i], kvh, Hkv, D, BS, NB);
+            const int64_t v = kv_index(bt_row, pos[i], kvh, Hkv, D, BS, NB);
             for (int d = 0; d < D; ++d)
-                acc[d] += p * bf16_val(v[d]);
+                acc[d] += p * kv_val(V, v + d, kvh);
         }
         m = m_new;
     }
@@ -355,8 +583,7 @@ static int attend_online(double *out, const uint16_t *qrow,
  * (The page prints out = sum l_s O_s / sum l_s, which is this formula when all
  * ranges share one max; rebasing to m* makes it hold for any maxima.) Empty
  * ranges carry no weight. */
-static int attend_split(double *out, const uint16_t *qrow,
-                        const uint16_t *key_cache, const uint16_t *value_cache,
+static int attend_split(double *out, const uint16_t *qrow, const kvsrc *K, const kvsrc *V,
                         const int32_t *bt_row, const int64_t *pos, int64_t n,
                         int kvh, int Hkv, int D, int BS, int64_t NB,
                         double scale, int num_splits, double *s, double *part)
@@ -371,7 +598,7 @@ static int attend_split(double *out, const uint16_t *qrow,
         lse[sp] = -INFINITY;
         if (b <= a)
             continue;
-        if (attend_two_pass(part + (int64_t)sp * D, qrow, key_cache, value_cache, bt_row,
+        if (attend_two_pass(part + (int64_t)sp * D, qrow, K, V, bt_row,
                             pos + a, b - a, kvh, Hkv, D, BS, NB, scale, s)) {
             free(lse);
             return -1;
@@ -404,8 +631,7 @@ static int attend_split(double *out, const uint16_t *qrow,
 }
 
 /* mode: 0 = two-pass, 1 = online (chunk = param), 2 = split (num_splits = param) */
-static int attention_rows(double *out, const uint16_t *q,
-                          const uint16_t *key_cache, const uint16_t *value_cache,
+static int attention_rows(double *out, const uint16_t *q, const kvsrc *K, const kvsrc *V,
                           const int32_t *block_tables, int MBS,
                           const int32_t *context_lens, const int32_t *selected, int topk,
                           int B, int Hq, int Hkv, int D, int BS, int64_t NB, double scale,
@@ -433,14 +659,13 @@ static int attention_rows(double *out, const uint16_t *q,
         const int32_t *bt_row = block_tables + b * (int64_t)MBS;
         double *o = out + r * (int64_t)D;
         if (mode == 0)
-            rc = attend_two_pass(o, qrow, key_cache, value_cache, bt_row, pos, n, kvh,
-                                 Hkv, D, BS, NB, scale, s);
+            rc = attend_two_pass(o, qrow, K, V, bt_row, pos, n, kvh, Hkv, D, BS, NB, scale, s);
         else if (mode == 1)
-            rc = attend_online(o, qrow, key_cache, value_cache, bt_row, pos, n, kvh,
-                               Hkv, D, BS, NB, scale, param, s, acc);
+            rc = attend_online(o, qrow, K, V, bt_row, pos, n, kvh, Hkv, D, BS, NB, scale, param,
+                               s, acc);
         else
-            rc = attend_split(o, qrow, key_cache, value_cache, bt_row, pos, n, kvh,
-                              Hkv, D, BS, NB, scale, (int)param, s, acc);
+            rc = attend_split(o, qrow, K, V, bt_row, pos, n, kvh, Hkv, D, BS, NB, scale,
+                              (int)param, s, acc);
     }
     free(pos);
     free(s);
@@ -459,7 +684,8 @@ int oracle_paged_attention(double *out, const uint16_t *q,
                            int D, int BS, int64_t NB, double scale,
                            const int32_t *rows, int64_t nrows)
 {
-    return attention_rows(out, q, key_cache, value_cache, block_tables, MBS, context_lens,
+    const kvsrc K = {key_cache, NULL, NULL}, V = {value_cache, NULL, NULL};
+    return attention_rows(out, q, &K, &V, block_tables, MBS, context_lens,
                           NULL, 0, B, Hq, Hkv, D, BS, NB, scale, rows, nrows, 0, 0);
 }
 
@@ -473,7 +699,8 @@ int oracle_paged_attention_online(double *out, const uint16_t *q,
 {
     if (chunk <= 0)
         return -2;
-    return attention_rows(out, q, key_cache, value_cache, block_tables, MBS, context_lens,
+    const kvsrc K = {key_cache, NULL, NULL}, V = {value_cache, NULL, NULL};
+    return attention_rows(out, q, &K, &V, block_tables, MBS, context_lens,
                           NULL, 0, B, Hq, Hkv, D, BS, NB, scale, NULL, 0, 1, chunk);
 }
 
@@ -486,7 +713,8 @@ int oracle_paged_attention_split(double *out, const uint16_t *q,
 {
     if (num_splits <= 0)
         return -2;
-    return attention_rows(out, q, key_cache, value_cache, block_tables, MBS, context_lens,
+    const kvsrc K = {key_cache, NULL, NULL}, V = {value_cache, NULL, NULL};
+    return attention_rows(out, q, &K, &V, block_tables, MBS, context_lens,
                           NULL, 0, B, Hq, Hkv, D, BS, NB, scale, NULL, 0, 2, num_splits);
 }
 
@@ -503,8 +731,28 @@ int oracle_sparse_attention(double *out, const uint16_t *q,
 {
     if (topk <= 0)
         return -2;
-    return attention_rows(out, q, key_cache, value_cache, block_tables, MBS, context_lens,
+    const kvsrc K = {key_cache, NULL, NULL}, V = {value_cache, NULL, NULL};
+    return attention_rows(out, q, &K, &V, block_tables, MBS, context_lens,
                           selected, topk, B, Hq, Hkv, D, BS, NB, scale, rows, nrows, 0, 0);
+}
+
+/* Attention over an E4M3 cache (dense when selected is NULL, else Quest
+ * sparse): the same two-pass softmax in fp64 on the dequantised elements
+ * decode(code) * scale[kvh] of K and V. */
+int oracle_attention_fp8(double *out, const uint16_t *q,
+                         const uint8_t *key_cache, const uint8_t *value_cache,
+                         const float *k_scale, const float *v_scale,
+                         const int32_t *block_tables, int MBS,
+                         const int32_t *context_lens, const int32_t *selected, int topk,
+                         int B, int Hq, int Hkv, int D, int BS, int64_t NB, double scale,
+                         const int32_t *rows, int64_t nrows)
+{
+    if (selected && topk <= 0)
+        return -2;
+    const kvsrc K = {NULL, key_cache, k_scale}, V = {NULL, value_cache, v_scale};
+    return attention_rows(out, q, &K, &V, block_tables, MBS, context_lens,
+                          selected, selected ? topk : 0, B, Hq, Hkv, D, BS, NB, scale, rows,
+                          nrows, 0, 0);
 }
 
 /* ------------------------------------------------------------ Quest score */
@@ -530,11 +778,18 @@ int oracle_sparse_attention(double *out, const uint16_t *q,
  * Logical blocks j >= ceil(ctx/BS) are excluded (score -inf). A table entry
  * outside the pool also scores -inf.
  * scores: [B][Hkv][MBS] fp32. Requires D % 32 == 0. */
-int oracle_quest_scores(float *scores, const uint16_t *q,
-                        const uint16_t *kmin, const uint16_t *kmax,
-                        const int32_t *block_tables, int MBS,
-                        const int32_t *context_lens, int B, int Hq, int Hkv,
-                        int D, int BS, int64_t NB)
+/* metadata element as fp32: bf16, or an E4M3 code (decoded exactly) */
+static float meta_f32(const uint16_t *m16, const uint8_t *m8, int64_t idx)
+{
+    return m16 ? bf16_f32(m16[idx]) : (float)oracle_e4m3_decode(m8[idx]);
+}
+
+static int quest_scores_impl(float *scores, const uint16_t *q,
+                             const uint16_t *kmin, const uint16_t *kmax,
+                             const uint8_t *kmin8, const uint8_t *kmax8,
+                             const int32_t *block_tables, int MBS,
+                             const int32_t *context_lens, int B, int Hq, int Hkv,
+                             int D, int BS, int64_t NB)
 {
     if (Hq % Hkv != 0 || D % 32 != 0)
         return -2;
@@ -567,14 +822,13 @@ int oracle_quest_scores(float *scores, const uint16_t *q,
                     srow[j] = -INFINITY;
                     continue;
                 }
-                const uint16_t *mn = kmin + (p * Hkv + kvh) * (int64_t)D;
-                const uint16_t *mx = kmax + (p * Hkv + kvh) * (int64_t)D;
+                const int64_t base = (p * Hkv + kvh) * (int64_t)D;
                 for (int l = 0; l < 32; ++l) {
                     float acc = 0.0f;
                     for (int i = 0; i < C; ++i) {
                         const int d = l * C + i;
-                        const float a = P[d] * bf16_f32(mx[d]);
-                        const float bb = N[d] * bf16_f32(mn[d]);
+                        const float a = P[d] * meta_f32(kmax, kmax8, base + d);
+                        const float bb = N[d] * meta_f32(kmin, kmin8, base + d);
                         const float t = a + bb;
                         acc = (i == 0) ? t : acc + t;
                     }
@@ -593,6 +847,30 @@ int oracle_quest_scores(float *scores, const uint16_t *q,
     free(P);
     free(N);
     return 0;
+}
+
+int oracle_quest_scores(float *scores, const uint16_t *q,
+                        const uint16_t *kmin, const uint16_t *kmax,
+                        const int32_t *block_tables, int MBS,
+                        const int32_t *context_lens, int B, int Hq, int Hkv,
+                        int D, int BS, int64_t NB)
+{
+    return quest_scores_impl(scores, q, kmin, kmax, NULL, NULL, block_tables, MBS,
+                             context_lens, B, Hq, Hkv, D, BS, NB);
+}
+
+/* The same score on E4M3 metadata: min_d and max_d are the decoded codes
+ * (exact in fp32), every other step as above. The cache's per-KV-head scale
+ * is left out: it multiplies every score of a (sequence, KV head) row by the
+ * same positive factor and cannot change that row's top-K. */
+int oracle_quest_scores_fp8(float *scores, const uint16_t *q,
+                            const uint8_t *kmin, const uint8_t *kmax,
+                            const int32_t *block_tables, int MBS,
+                            const int32_t *context_lens, int B, int Hq, int Hkv,
+                            int D, int BS, int64_t NB)
+{
+    return quest_scores_impl(scores, q, NULL, NULL, kmin, kmax, block_tables, MBS,
+                             context_lens, B, Hq, Hkv, D, BS, NB);
 }
 
 /* ------------------------------------------------------------ Quest top-K */
