@@ -46,6 +46,8 @@ def parse():
     p.add_argument("--impl", choices=["native", "reference"], default="native")
     p.add_argument("--workload", default="quest_8k",
                    choices=["tiny", "dense_b32", "quest_8k", "long_40k", "mixed_b128"])
+    p.add_argument("--kv", choices=["bf16", "fp8"], default="bf16",
+                   help="KV-cache element type: bf16, or 8-bit E4M3 codes with per-KV-head scales")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-budget", type=float, default=12.0,
                    help="seconds of oracle work for the CPU baseline sample")
@@ -152,10 +154,11 @@ def gpu_id_for(torch, dev) -> str:
 class Step:
     """Device buffers of one workload and the five C-ABI calls of a step."""
 
-    def __init__(self, w, dev):
+    def __init__(self, w, dev, kv: str = "bf16"):
         import torch
         import paged_gqa_decode_reshape_gb300 as pg
-        self.pg, self.torch, self.w, self.dev = pg, torch, w, dev
+        import workloads
+        self.pg, self.torch, self.w, self.dev, self.kv = pg, torch, w, dev, kv
 
         def d16(a):
             return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)
@@ -177,6 +180,25 @@ class Step:
                               device=dev)
         self.sel_ws = torch.zeros(pg.quest_select_workspace_size(w.B, w.Hkv, w.MBS),
                                   dtype=torch.uint8, device=dev)
+        if kv == "fp8":
+            # the 8-bit pool: every slot of the bf16 pool quantised once (setup)
+            ks, vs = workloads.fp8_scales(w.Hkv)
+            self.k_scale, self.v_scale = torch.from_numpy(ks).to(dev), torch.from_numpy(vs).to(dev)
+            NB, BS = w.NB, w.BS
+            kc8 = torch.empty((NB, BS, w.Hkv, w.D), dtype=torch.uint8, device=dev)
+            vc8 = torch.empty((NB, w.Hkv, w.D, BS), dtype=torch.uint8, device=dev)
+            pg.pa_reshape_and_cache_fp8(self.kc.view(NB * BS, w.Hkv, w.D), self.vc.view(NB * BS, w.Hkv, w.D),
+                                        kc8, vc8, torch.arange(NB * BS, dtype=torch.int64, device=dev),
+                                        self.k_scale, self.v_scale)
+            torch.cuda.synchronize(dev)
+            self.kc, self.vc = kc8, vc8
+            self.kmin = torch.zeros((w.NB, w.Hkv, w.D), dtype=torch.uint8, device=dev)
+            self.kmax = torch.zeros_like(self.kmin)
+            pg.quest_reshape_and_cache_fp8(self.key, self.value, self.kc, self.vc, self.kmin, self.kmax,
+                                           self.slots, self.k_scale, self.v_scale)
+            pg.quest_rebuild_meta_fp8(self.kmin, self.kmax, self.kc, self.bt, self.ctx)
+            torch.cuda.synchronize(dev)
+            return
         # Quest metadata of the cache as it stands (setup, not timed)
         pg.pa_reshape_and_cache(self.key, self.value, self.kc, self.vc, self.slots)
         pg.quest_rebuild_meta(self.kmin, self.kmax, self.kc, self.bt, self.ctx)
@@ -187,6 +209,18 @@ class Step:
         the metadata update in one launch), dense decode, Quest selection
         (score + top-K launches), Quest sparse decode."""
         pg, w = self.pg, self.w
+        if self.kv == "fp8":
+            return [
+                lambda: pg.quest_reshape_and_cache_fp8(self.key, self.value, self.kc, self.vc, self.kmin,
+                                                       self.kmax, self.slots, self.k_scale, self.v_scale),
+                lambda: pg.pa_decode_fp8(self.out, self.q, self.kc, self.vc, self.k_scale, self.v_scale,
+                                         self.bt, self.ctx, w.scale, workspace=self.ws),
+                lambda: pg.quest_select_topk_fp8(self.sel, self.q, self.kmin, self.kmax, self.bt,
+                                                 self.ctx, w.BS, workspace=self.sel_ws),
+                lambda: pg.quest_sparse_decode_fp8(self.out_sparse, self.q, self.kc, self.vc,
+                                                   self.k_scale, self.v_scale, self.bt, self.ctx,
+                                                   self.sel, w.scale, workspace=self.ws),
+            ]
         return [
             lambda: pg.quest_reshape_and_cache(self.key, self.value, self.kc, self.vc, self.kmin,
                                                self.kmax, self.slots),
@@ -206,13 +240,15 @@ LAUNCHES_PER_CALL = [1, 1, 2, 1]
 # -------------------------------------------------------------- CPU oracle
 
 
-def oracle_sample(w, budget_s: float):
+def oracle_sample(w, budget_s: float, kv: str = "bf16"):
     """The oracle on a bounded sample of the step: the write path for every
     token, then whole sequences (dense attention for all heads, Quest scores
     and top-K for all KV heads, sparse attention for all heads) until the
     time budget is spent. Returns (algorithmic bytes, seconds, sequences)."""
     import oracle
     from paged_gqa_decode_reshape_gb300 import ledger
+    if kv == "fp8":
+        return oracle_sample_fp8(w, budget_s)
     kc, vc = w.key_cache, w.value_cache       # the oracle writes in place: state after the step
     t0 = time.perf_counter()
     oracle.reshape_and_cache(w.key, w.value, kc, vc, w.slot_mapping)
@@ -244,6 +280,50 @@ def oracle_sample(w, budget_s: float):
         seqs += 1
     elapsed = time.perf_counter() - t0 - t_setup
     return done_bytes, elapsed, seqs
+
+
+def oracle_sample_fp8(w, budget_s: float):
+    """oracle_sample over an 8-bit cache: the pool quantised once (setup, not
+    timed), then the 8-bit write path for every token and whole sequences of
+    8-bit dense attention, Quest selection and sparse attention."""
+    import oracle
+    import workloads
+    from paged_gqa_decode_reshape_gb300 import ledger
+    ks, vs = workloads.fp8_scales(w.Hkv)
+    NB, BS = w.NB, w.BS
+    t_setup0 = time.perf_counter()
+    kc = np.zeros((NB, BS, w.Hkv, w.D), dtype=np.uint8)
+    vc = np.zeros((NB, w.Hkv, w.D, BS), dtype=np.uint8)
+    oracle.reshape_and_cache_fp8(w.key_cache.reshape(NB * BS, w.Hkv, w.D),
+                                 w.value_cache.reshape(NB * BS, w.Hkv, w.D), kc, vc,
+                                 np.arange(NB * BS, dtype=np.int64), ks, vs)
+    kmin, kmax = oracle.quest_rebuild_meta_fp8(kc, w.block_tables, w.context_lens)
+    t_setup = time.perf_counter() - t_setup0
+    t0 = time.perf_counter()
+    oracle.reshape_and_cache_fp8(w.key, w.value, kc, vc, w.slot_mapping, ks, vs)
+    oracle.quest_update_meta_fp8(kmin, kmax, w.key, w.slot_mapping, ks, w.BS)
+    nbytes = ledger.step_bytes(w.context_lens, w.slot_mapping, w.Hq, w.Hkv, w.D, w.BS, w.topk,
+                               elem_bytes=1)
+    done_bytes = nbytes.reshape + nbytes.meta
+    seqs = 0
+    for b in range(w.B):
+        if time.perf_counter() - t0 > budget_s and seqs > 0:
+            break
+        rows = np.array([(b, h) for h in range(w.Hq)], dtype=np.int32)
+        oracle.attention_fp8(w.q, kc, vc, ks, vs, w.block_tables, w.context_lens, w.scale, rows=rows)
+        sc = oracle.quest_scores_fp8(w.q[b:b + 1], kmin, kmax, w.block_tables[b:b + 1],
+                                     w.context_lens[b:b + 1], w.BS)
+        sel = oracle.quest_topk(sc, w.context_lens[b:b + 1], w.BS, w.topk)
+        full_sel = np.full((w.B, w.Hkv, w.topk), -1, dtype=np.int32)
+        full_sel[b] = sel[0]
+        oracle.attention_fp8(w.q, kc, vc, ks, vs, w.block_tables, w.context_lens, w.scale,
+                             selected=full_sel, rows=rows)
+        one = ledger.step_bytes(w.context_lens[b:b + 1], np.zeros(0, np.int64), w.Hq, w.Hkv, w.D,
+                                w.BS, w.topk, selected=sel, elem_bytes=1)
+        done_bytes += one.dense + one.select + one.sparse
+        seqs += 1
+    del t_setup
+    return done_bytes, time.perf_counter() - t0, seqs
 
 
 # -------------------------------------------------------------------- main
@@ -287,7 +367,7 @@ def run_reference(args, world, rank, pgroup):
     times, nbytes = [], []
     for i in range(args.warmup + args.steps):
         # the oracle's writes are idempotent, so every step reuses the same inputs
-        b, s, seqs = oracle_sample(w0, args.cpu_budget / max(1, args.steps + args.warmup))
+        b, s, seqs = oracle_sample(w0, args.cpu_budget / max(1, args.steps + args.warmup), args.kv)
         if i >= args.warmup:
             times.append(s)
             nbytes.append(b)
@@ -297,7 +377,8 @@ def run_reference(args, world, rank, pgroup):
         "warmup": args.warmup, "ms_per_step": 1e3 * sum(times) / len(times),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "impl": "reference",
-        "config": {"workload": args.workload, "sample": "per step: the write path for every token, "
+        "config": {"workload": args.workload, "kv_cache": args.kv,
+                   "sample": "per step: the write path for every token, "
                    "then whole sequences in order until the step's time share is spent"},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
                          "sample": f"{args.steps} steps of a bounded sample of {args.workload}"},
@@ -326,7 +407,7 @@ def main():
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     w = workloads.make(args.workload, poison=False)
-    step = Step(w, dev)
+    step = Step(w, dev, args.kv)
     calls = step.calls()
     stream = torch.cuda.current_stream(dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
@@ -337,8 +418,9 @@ def main():
             c()
     torch.cuda.synchronize(dev)
     sel_host = step.sel.cpu().numpy()
+    fp8 = args.kv == "fp8"
     nb = ledger.step_bytes(w.context_lens, w.slot_mapping, w.Hq, w.Hkv, w.D, w.BS, w.topk,
-                           selected=sel_host)
+                           selected=sel_host, elem_bytes=1 if fp8 else 2)
 
     # Pass A (the timed region): whole steps, one event pair per step, L2
     # flushed before each step outside the events. Kernels launch with
@@ -454,26 +536,28 @@ def main():
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "bf16",
+        "dtype": "e4m3 KV cache, bf16 q/out" if fp8 else "bf16",
         "data": "synthetic",
         "config": {
             "workload": args.workload, "batch": w.B, "num_q_heads": w.Hq, "num_kv_heads": w.Hkv,
-            "head_dim": w.D, "block_size": w.BS, "topk_blocks": w.topk,
+            "head_dim": w.D, "block_size": w.BS, "topk_blocks": w.topk, "kv_cache": args.kv,
             "context_lens_mean": round(float(w.context_lens.mean()), 1),
             "context_lens_max": int(w.context_lens.max()), "pool_blocks": w.NB,
-            "kv_pool_bytes": int(2 * w.key_cache.nbytes),
-            "step": "quest_reshape_and_cache (ReshapeAndCache + metadata update, one launch) + "
-                    "pa_decode + quest_select_topk + quest_sparse_decode",
+            "kv_pool_bytes": int(2 * w.key_cache.nbytes // (2 if fp8 else 1)),
+            "step": ("quest_reshape_and_cache{0} (ReshapeAndCache + metadata update, one launch) + "
+                     "pa_decode{0} + quest_select_topk{0} + quest_sparse_decode{0}").format(
+                         "_fp8" if fp8 else ""),
             "timing": "value/ms_per_step: one event pair per step; breakdown/roofline: a second "
                       "pass of the same steps with an event between calls",
             "l2": f"flushed before every step ({L2_FLUSH_BYTES >> 20} MiB write), outside the timed events",
             "parallelism": f"replicas x{world}",
         },
         "roofline": {
-            "bound": "hbm", "kernel": "pa_decode (split-KV decode + fused combine, 1 launch)",
+            "bound": "hbm",
+            "kernel": ("pa_decode_fp8" if fp8 else "pa_decode") + " (split-KV decode + fused combine, 1 launch)",
             "achieved": round(dense_gbs, 1), "peak": peak, "unit": "GB/s",
             "frac": round(dense_gbs / peak, 4), "peak_kind": peak_kind,
-            "traffic": recorded_traffic("pa_decode", args.workload),
+            "traffic": recorded_traffic("pa_decode_fp8" if fp8 else "pa_decode", args.workload),
             "algorithmic_bytes_per_launch": int(nb.dense),
         },
         "breakdown": breakdown,
@@ -495,7 +579,7 @@ def main():
     }
     if world == 1 and not args.no_cpu_baseline:
         wc = workloads.make(args.workload, poison=False)
-        b, s, seqs = oracle_sample(wc, args.cpu_budget)
+        b, s, seqs = oracle_sample(wc, args.cpu_budget, args.kv)
         line["cpu_baseline"] = {
             "value": round(b / s / 1e9, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
             "sample": f"write path for all {w.T} tokens + {seqs} of {w.B} sequences "

@@ -63,6 +63,7 @@ extern "C" {
 #endif
 
 typedef uint16_t pa_bf16; /* bfloat16 bit pattern */
+typedef uint8_t pa_e4m3;  /* 8-bit float, E4M3 variant (see the 8-bit cache section) */
 
 typedef enum {
     PA_OK = 0,
@@ -231,6 +232,101 @@ PA_API int pa_check_metadata(int32_t *counts, const int64_t *slot_mapping, int64
                       const int32_t *block_tables, int max_blocks_per_seq,
                       const int32_t *context_lens, int batch, int block_size,
                       int64_t num_blocks, void *stream);
+
+/* ---------------------------------------------------- 8-bit KV cache ----
+ * The same path over a KV cache stored in 8 bits per element, which halves
+ * the bytes decode attention reads ([P2] 2.5 and 3.1: long-context serving is
+ * bound by KV bandwidth, and KV quantisation is the lever the tutorial names).
+ *
+ * Format: the E4M3 variant of the OCP 8-bit float ("fn": sign bit, 4 exponent
+ * bits with bias 7, 3 mantissa bits, no infinities, largest finite 448,
+ * 0x7F / 0xFF NaN). Element d of KV head h of a token is stored as
+ *     code = e4m3(fl32(x / scale[h])),
+ * rounded to nearest with ties to the even mantissa, magnitudes beyond 448
+ * (and infinities) saturated to +-448, NaN stored as 0x7F; it stands for
+ * decode(code) * scale[h]. k_scale and v_scale are [Hkv] fp32 device arrays,
+ * positive and finite, fixed by the caller for the cache's lifetime (a
+ * calibration outside this library). Quest metadata of an 8-bit cache are
+ * E4M3 codes too: the elementwise min / max of the stored K codes (numeric
+ * order, -0 < +0), [NB][Hkv][D] bytes.
+ *
+ * Layouts: key_cache [NB][BS][Hkv][D] bytes (as the bf16 cache) and kmin /
+ * kmax [NB][Hkv][D] bytes; value_cache [NB][Hkv][D][BS] bytes: per block and
+ * KV head a dim-by-token matrix whose 16-byte row of dim d holds the block's
+ * tokens in the order 0 1 8 9 2 3 10 11 4 5 12 13 6 7 14 15 (token o at byte
+ * 4*((o%8)/2) + 2*(o/8) + o%2), the order the attention kernel's fragment
+ * loads take it in. Supported: head_dim 128, block_size 16; 16-byte aligned
+ * pointers. Queries stay bf16; the
+ * attention converts them to f16 (values outside the f16 range, about
+ * 6.1e-5 .. 65504 in magnitude, are rounded or overflow there), multiplies
+ * exactly decoded K / V codes in f16 with fp32 accumulation, and applies the
+ * scales in fp32. The decode workspace is the one pa_decode uses. */
+
+/* ReshapeAndCache into an 8-bit cache: the slot arithmetic of
+ * pa_reshape_and_cache ([P1] "ReshapeAndCache"), each element quantised as
+ * above with its KV head's scale. */
+PA_API int pa_reshape_and_cache_fp8(const pa_bf16 *key, const pa_bf16 *value,
+                             pa_e4m3 *key_cache, pa_e4m3 *value_cache,
+                             const int64_t *slot_mapping, int64_t num_tokens,
+                             const float *k_scale, const float *v_scale, int num_kv_heads,
+                             int head_dim, int block_size, int64_t num_blocks, void *stream);
+
+/* Metadata update of an 8-bit cache for this call's tokens: the rule of
+ * quest_update_meta on the tokens' codes (the codes pa_reshape_and_cache_fp8
+ * stores). */
+PA_API int quest_update_meta_fp8(pa_e4m3 *kmin, pa_e4m3 *kmax, const pa_bf16 *key,
+                          const int64_t *slot_mapping, int64_t num_tokens,
+                          const float *k_scale, int num_kv_heads, int head_dim,
+                          int block_size, int64_t num_blocks, void *stream);
+
+/* pa_reshape_and_cache_fp8 followed by quest_update_meta_fp8, one launch. */
+PA_API int quest_reshape_and_cache_fp8(const pa_bf16 *key, const pa_bf16 *value,
+                                pa_e4m3 *key_cache, pa_e4m3 *value_cache,
+                                pa_e4m3 *kmin, pa_e4m3 *kmax,
+                                const int64_t *slot_mapping, int64_t num_tokens,
+                                const float *k_scale, const float *v_scale, int num_kv_heads,
+                                int head_dim, int block_size, int64_t num_blocks, void *stream);
+
+/* Metadata of every block the sequences use, recomputed from an 8-bit cache
+ * (as quest_rebuild_meta). */
+PA_API int quest_rebuild_meta_fp8(pa_e4m3 *kmin, pa_e4m3 *kmax, const pa_e4m3 *key_cache,
+                           const int32_t *block_tables, int max_blocks_per_seq,
+                           const int32_t *context_lens, int batch, int num_kv_heads,
+                           int head_dim, int block_size, int64_t num_blocks, void *stream);
+
+/* Quest selection on 8-bit metadata: the score of quest_select_topk with
+ * kmin_d / kmax_d the decoded codes (exact in fp32), same evaluation order,
+ * same top-K rule and workspace. The cache's K scale is left out: it
+ * multiplies every score of a (sequence, KV head) row by one positive factor
+ * and cannot change that row's selection. */
+PA_API int quest_select_topk_fp8(int32_t *selected, const pa_bf16 *query,
+                          const pa_e4m3 *kmin, const pa_e4m3 *kmax,
+                          const int32_t *block_tables, int max_blocks_per_seq,
+                          const int32_t *context_lens, int batch, int num_q_heads,
+                          int num_kv_heads, int head_dim, int block_size, int64_t num_blocks,
+                          int topk, void *workspace, size_t workspace_bytes, void *stream);
+
+/* Dense GQA paged decode attention ([P1] "GQA Paged Attention", split-KV per
+ * [P2] 4.1) over an 8-bit cache: pa_decode with K and V read as
+ * decode(code) * scale[kvh]. Same workspace and status rules as pa_decode. */
+PA_API int pa_decode_fp8(pa_bf16 *out, const pa_bf16 *query,
+                  const pa_e4m3 *key_cache, const pa_e4m3 *value_cache,
+                  const float *k_scale, const float *v_scale,
+                  const int32_t *block_tables, int max_blocks_per_seq,
+                  const int32_t *context_lens, int batch, int num_q_heads, int num_kv_heads,
+                  int head_dim, int block_size, int64_t num_blocks, float scale,
+                  void *workspace, size_t workspace_bytes, void *stream);
+
+/* Quest sparse attention ([P1] "Quest Sparse Attention") over an 8-bit
+ * cache: quest_sparse_decode with K and V decoded as in pa_decode_fp8. */
+PA_API int quest_sparse_decode_fp8(pa_bf16 *out, const pa_bf16 *query,
+                            const pa_e4m3 *key_cache, const pa_e4m3 *value_cache,
+                            const float *k_scale, const float *v_scale,
+                            const int32_t *block_tables, int max_blocks_per_seq,
+                            const int32_t *context_lens, const int32_t *selected, int topk,
+                            int batch, int num_q_heads, int num_kv_heads, int head_dim,
+                            int block_size, int64_t num_blocks, float scale,
+                            void *workspace, size_t workspace_bytes, void *stream);
 
 #ifdef __cplusplus
 }

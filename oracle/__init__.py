@@ -284,10 +284,14 @@ def e4m3_decode(codes) -> np.ndarray:
 
 
 def reshape_and_cache_fp8(key, value, key_cache, value_cache, slot_mapping, k_scale, v_scale) -> int:
-    """Quantise and scatter new K/V rows into uint8 E4M3 caches IN PLACE; returns #out-of-pool slots."""
+    """Quantise and scatter new K/V rows into uint8 E4M3 caches IN PLACE; returns #out-of-pool slots.
+
+    key_cache is [NB, BS, Hkv, D]; value_cache is [NB, Hkv, D, BS] with the
+    tokens of each 16-byte row in the order 0 1 8 9 2 3 10 11 ... (BS = 16)."""
     assert key_cache.dtype == np.uint8 and key_cache.flags.c_contiguous
     assert value_cache.dtype == np.uint8 and value_cache.flags.c_contiguous
     NB, BS, Hkv, D = key_cache.shape
+    assert value_cache.shape == (NB, Hkv, D, BS) and BS == 16
     key = _c(key, np.uint16)
     value = _c(value, np.uint16)
     slots = _c(slot_mapping, np.int64)
@@ -329,7 +333,8 @@ def quest_rebuild_meta_fp8(key_cache, block_tables, context_lens, kmin=None, kma
 
 def attention_fp8(q, key_cache, value_cache, k_scale, v_scale, block_tables, context_lens, scale,
                   selected=None, rows=None):
-    """Dense (selected None) or Quest sparse attention over E4M3 caches, fp64."""
+    """Dense (selected None) or Quest sparse attention over E4M3 caches, fp64
+    (value_cache in the [NB, Hkv, D, 16] layout of reshape_and_cache_fp8)."""
     q = _c(q, np.uint16)
     kc = _c(key_cache, np.uint8)
     vc = _c(value_cache, np.uint8)
@@ -339,7 +344,7 @@ def attention_fp8(q, key_cache, value_cache, k_scale, v_scale, block_tables, con
     ctx = _c(context_lens, np.int32)
     B, Hq, D = q.shape
     NB, BS, Hkv, D2 = kc.shape
-    assert D == D2 and vc.shape == kc.shape and ks.shape == (Hkv,) and vs.shape == (Hkv,)
+    assert D == D2 and vc.shape == (NB, Hkv, D, BS) and ks.shape == (Hkv,) and vs.shape == (Hkv,)
     sel, topk = None, 0
     if selected is not None:
         sel = _c(selected, np.int32)

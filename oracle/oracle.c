@@ -144,6 +144,23 @@ static uint8_t e4m3_order_key(uint8_t c)
     return (c & 0x80u) ? (uint8_t)(~c & 0x7Fu) : (uint8_t)(c | 0x80u);
 }
 
+/* Layout of an E4M3 V cache. K codes keep the bf16 layout [NB][BS][Hkv][D]
+ * (one token's row of all KV heads). V codes are stored per block and KV head
+ * as a [D][16] byte matrix: the 16 bytes of dim d hold the block's 16 tokens
+ * in the order 0 1 8 9 2 3 10 11 4 5 12 13 6 7 14 15, i.e. token o at byte
+ *     pos(o) = 4 * ((o mod 8) div 2) + 2 * (o div 8) + (o mod 2).
+ * (That order makes the GPU's 4-byte fragment loads hold two consecutive
+ * token pairs; for the method it is only an address function.) Block size 16. */
+static int64_t vt_token_pos(int64_t o)
+{
+    return 4 * ((o & 7) >> 1) + 2 * (o >> 3) + (o & 1);
+}
+
+static int64_t vt_index(int64_t p, int64_t o, int64_t h, int64_t d, int Hkv, int D)
+{
+    return ((p * Hkv + h) * D + d) * 16 + vt_token_pos(o);
+}
+
 /* code of one bf16 element quantised with a per-KV-head scale:
  * e4m3(fl32(x / scale)) */
 static uint8_t quantize(uint16_t x, float scale)
@@ -308,6 +325,8 @@ int64_t oracle_reshape_and_cache_fp8(const uint16_t *key, const uint16_t *value,
 {
     const int64_t row = (int64_t)Hkv * D;
     int64_t out_of_range = 0;
+    if (BS != 16)
+        return -2;
     for (int64_t t = 0; t < T; ++t) {
         const int64_t slot = slot_mapping[t];
         if (slot < 0)
@@ -322,7 +341,8 @@ int64_t oracle_reshape_and_cache_fp8(const uint16_t *key, const uint16_t *value,
         for (int64_t e = 0; e < row; ++e) {
             const int h = (int)(e / D);
             key_cache[dst + e] = quantize(key[t * row + e], k_scale[h]);
-            value_cache[dst + e] = quantize(value[t * row + e], v_scale[h]);
+            value_cache[vt_index(block_idx, block_offset, h, e % D, Hkv, D)] =
+                quantize(value[t * row + e], v_scale[h]);
         }
     }
     return out_of_range;
@@ -461,12 +481,19 @@ typedef struct {
     const uint16_t *bf16;
     const uint8_t *e4m3;
     const float *scale;
+    int vt, Hkv, D, BS; /* vt: E4M3 codes in the V layout (vt_index) */
 } kvsrc;
 
+/* element idx of the [NB][BS][Hkv][D] index space */
 static double kv_val(const kvsrc *c, int64_t idx, int kvh)
 {
     if (c->bf16)
         return bf16_val(c->bf16[idx]);
+    if (c->vt) {
+        const int64_t d = idx % c->D, o = (idx / ((int64_t)c->D * c->Hkv)) % c->BS;
+        const int64_t p = idx / ((int64_t)c->D * c->Hkv * c->BS);
+        idx = vt_index(p, o, kvh, d, c->Hkv, c->D);
+    }
     return oracle_e4m3_decode(c->e4m3[idx]) * (double)c->scale[kvh];
 }
 
@@ -684,7 +711,7 @@ int oracle_paged_attention(double *out, const uint16_t *q,
                            int D, int BS, int64_t NB, double scale,
                            const int32_t *rows, int64_t nrows)
 {
-    const kvsrc K = {key_cache, NULL, NULL}, V = {value_cache, NULL, NULL};
+    const kvsrc K = {key_cache, NULL, NULL, 0, 0, 0, 0}, V = {value_cache, NULL, NULL, 0, 0, 0, 0};
     return attention_rows(out, q, &K, &V, block_tables, MBS, context_lens,
                           NULL, 0, B, Hq, Hkv, D, BS, NB, scale, rows, nrows, 0, 0);
 }
@@ -699,7 +726,7 @@ int oracle_paged_attention_online(double *out, const uint16_t *q,
 {
     if (chunk <= 0)
         return -2;
-    const kvsrc K = {key_cache, NULL, NULL}, V = {value_cache, NULL, NULL};
+    const kvsrc K = {key_cache, NULL, NULL, 0, 0, 0, 0}, V = {value_cache, NULL, NULL, 0, 0, 0, 0};
     return attention_rows(out, q, &K, &V, block_tables, MBS, context_lens,
                           NULL, 0, B, Hq, Hkv, D, BS, NB, scale, NULL, 0, 1, chunk);
 }
@@ -713,7 +740,7 @@ int oracle_paged_attention_split(double *out, const uint16_t *q,
 {
     if (num_splits <= 0)
         return -2;
-    const kvsrc K = {key_cache, NULL, NULL}, V = {value_cache, NULL, NULL};
+    const kvsrc K = {key_cache, NULL, NULL, 0, 0, 0, 0}, V = {value_cache, NULL, NULL, 0, 0, 0, 0};
     return attention_rows(out, q, &K, &V, block_tables, MBS, context_lens,
                           NULL, 0, B, Hq, Hkv, D, BS, NB, scale, NULL, 0, 2, num_splits);
 }
@@ -731,14 +758,14 @@ int oracle_sparse_attention(double *out, const uint16_t *q,
 {
     if (topk <= 0)
         return -2;
-    const kvsrc K = {key_cache, NULL, NULL}, V = {value_cache, NULL, NULL};
+    const kvsrc K = {key_cache, NULL, NULL, 0, 0, 0, 0}, V = {value_cache, NULL, NULL, 0, 0, 0, 0};
     return attention_rows(out, q, &K, &V, block_tables, MBS, context_lens,
                           selected, topk, B, Hq, Hkv, D, BS, NB, scale, rows, nrows, 0, 0);
 }
 
 /* Attention over an E4M3 cache (dense when selected is NULL, else Quest
  * sparse): the same two-pass softmax in fp64 on the dequantised elements
- * decode(code) * scale[kvh] of K and V. */
+ * decode(code) * scale[kvh] of K and V (V codes in the V layout). */
 int oracle_attention_fp8(double *out, const uint16_t *q,
                          const uint8_t *key_cache, const uint8_t *value_cache,
                          const float *k_scale, const float *v_scale,
@@ -747,9 +774,10 @@ int oracle_attention_fp8(double *out, const uint16_t *q,
                          int B, int Hq, int Hkv, int D, int BS, int64_t NB, double scale,
                          const int32_t *rows, int64_t nrows)
 {
-    if (selected && topk <= 0)
+    if ((selected && topk <= 0) || BS != 16)
         return -2;
-    const kvsrc K = {NULL, key_cache, k_scale}, V = {NULL, value_cache, v_scale};
+    const kvsrc K = {NULL, key_cache, k_scale, 0, Hkv, D, BS};
+    const kvsrc V = {NULL, value_cache, v_scale, 1, Hkv, D, BS};
     return attention_rows(out, q, &K, &V, block_tables, MBS, context_lens,
                           selected, selected ? topk : 0, B, Hq, Hkv, D, BS, NB, scale, rows,
                           nrows, 0, 0);

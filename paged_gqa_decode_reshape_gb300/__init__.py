@@ -88,6 +88,24 @@ def load_library(path: Optional[str] = None):
         L.pa_workspace_status.restype = i32
         L.pa_check_metadata.argtypes = [vp, vp, i64, vp, i32, vp, i32, i32, i64, vp]
         L.pa_check_metadata.restype = i32
+        L.pa_reshape_and_cache_fp8.argtypes = [vp, vp, vp, vp, vp, i64, vp, vp, i32, i32, i32, i64, vp]
+        L.pa_reshape_and_cache_fp8.restype = i32
+        L.quest_update_meta_fp8.argtypes = [vp, vp, vp, vp, i64, vp, i32, i32, i32, i64, vp]
+        L.quest_update_meta_fp8.restype = i32
+        L.quest_reshape_and_cache_fp8.argtypes = [vp, vp, vp, vp, vp, vp, vp, i64, vp, vp, i32, i32,
+                                                  i32, i64, vp]
+        L.quest_reshape_and_cache_fp8.restype = i32
+        L.quest_rebuild_meta_fp8.argtypes = [vp, vp, vp, vp, i32, vp, i32, i32, i32, i32, i64, vp]
+        L.quest_rebuild_meta_fp8.restype = i32
+        L.quest_select_topk_fp8.argtypes = [vp, vp, vp, vp, vp, i32, vp, i32, i32, i32, i32, i32,
+                                            i64, i32, vp, sz, vp]
+        L.quest_select_topk_fp8.restype = i32
+        L.pa_decode_fp8.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, vp, i32, i32, i32, i32, i32,
+                                    i64, f32, vp, sz, vp]
+        L.pa_decode_fp8.restype = i32
+        L.quest_sparse_decode_fp8.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, vp, vp, i32, i32, i32,
+                                              i32, i32, i32, i64, f32, vp, sz, vp]
+        L.quest_sparse_decode_fp8.restype = i32
         _lib = L
         return _lib
 
@@ -350,3 +368,195 @@ def pa_check_metadata(slot_mapping: Optional[torch.Tensor], block_tables: Option
            L.pa_check_metadata(_ptr(counts), _ptr(slot_mapping), T, _ptr(block_tables), MBS,
                                _ptr(context_lens), B, int(block_size), int(num_blocks), _stream(dev)))
     return counts.cpu().tolist()
+
+
+# ------------------------------------------------- 8-bit (E4M3) KV cache
+#
+# Caches and metadata are uint8 tensors holding E4M3 codes; k_scale / v_scale
+# are float32 [Hkv] tensors on the same device (see include/paged_decode.h).
+# key_cache is [NB, BS, Hkv, D]; value_cache is [NB, Hkv, D, BS] (per block
+# and KV head a dim-by-token byte matrix, tokens of a row in the order
+# 0 1 8 9 2 3 10 11 ...), BS = 16.
+
+
+def _scales(k_scale, v_scale, Hkv, dev):
+    _need(k_scale, "k_scale", torch.float32, 1, dev)
+    if v_scale is not None:
+        _need(v_scale, "v_scale", torch.float32, 1, dev)
+    if k_scale.shape[0] != Hkv or (v_scale is not None and v_scale.shape[0] != Hkv):
+        raise ValueError("scales must be [num_kv_heads]")
+
+
+def pa_reshape_and_cache_fp8(key: torch.Tensor, value: torch.Tensor, key_cache: torch.Tensor,
+                             value_cache: torch.Tensor, slot_mapping: torch.Tensor,
+                             k_scale: torch.Tensor, v_scale: torch.Tensor) -> None:
+    """Quantise this step's K/V rows [T, Hkv, D] (bf16) into 8-bit caches [NB, BS, Hkv, D]."""
+    L = load_library()
+    _need(key_cache, "key_cache", torch.uint8, 4)
+    dev = key_cache.device
+    _need(value_cache, "value_cache", torch.uint8, 4, dev)
+    _need(key, "key", torch.bfloat16, 3, dev)
+    _need(value, "value", torch.bfloat16, 3, dev)
+    _need(slot_mapping, "slot_mapping", torch.int64, 1, dev)
+    NB, BS, Hkv, D = key_cache.shape
+    T = slot_mapping.shape[0]
+    if value_cache.shape != (NB, Hkv, D, BS) or key.shape != (T, Hkv, D) or value.shape != key.shape:
+        raise ValueError("shape mismatch between key/value and the caches")
+    _scales(k_scale, v_scale, Hkv, dev)
+    _check("pa_reshape_and_cache_fp8",
+           L.pa_reshape_and_cache_fp8(_ptr(key), _ptr(value), _ptr(key_cache), _ptr(value_cache),
+                                      _ptr(slot_mapping), T, _ptr(k_scale), _ptr(v_scale), Hkv, D, BS,
+                                      NB, _stream(dev)))
+
+
+def quest_update_meta_fp8(kmin: torch.Tensor, kmax: torch.Tensor, key: torch.Tensor,
+                          slot_mapping: torch.Tensor, k_scale: torch.Tensor, block_size: int) -> None:
+    """Fold this step's quantised keys into the 8-bit metadata [NB, Hkv, D]."""
+    L = load_library()
+    _need(kmin, "kmin", torch.uint8, 3)
+    dev = kmin.device
+    _need(kmax, "kmax", torch.uint8, 3, dev)
+    _need(key, "key", torch.bfloat16, 3, dev)
+    _need(slot_mapping, "slot_mapping", torch.int64, 1, dev)
+    NB, Hkv, D = kmin.shape
+    T = slot_mapping.shape[0]
+    if kmax.shape != kmin.shape or key.shape != (T, Hkv, D):
+        raise ValueError("shape mismatch between key and the metadata")
+    _scales(k_scale, None, Hkv, dev)
+    _check("quest_update_meta_fp8",
+           L.quest_update_meta_fp8(_ptr(kmin), _ptr(kmax), _ptr(key), _ptr(slot_mapping), T,
+                                   _ptr(k_scale), Hkv, D, int(block_size), NB, _stream(dev)))
+
+
+def quest_reshape_and_cache_fp8(key: torch.Tensor, value: torch.Tensor, key_cache: torch.Tensor,
+                                value_cache: torch.Tensor, kmin: torch.Tensor, kmax: torch.Tensor,
+                                slot_mapping: torch.Tensor, k_scale: torch.Tensor,
+                                v_scale: torch.Tensor) -> None:
+    """The 8-bit write path in one launch: pa_reshape_and_cache_fp8 then quest_update_meta_fp8."""
+    L = load_library()
+    _need(key_cache, "key_cache", torch.uint8, 4)
+    dev = key_cache.device
+    _need(value_cache, "value_cache", torch.uint8, 4, dev)
+    _need(kmin, "kmin", torch.uint8, 3, dev)
+    _need(kmax, "kmax", torch.uint8, 3, dev)
+    _need(key, "key", torch.bfloat16, 3, dev)
+    _need(value, "value", torch.bfloat16, 3, dev)
+    _need(slot_mapping, "slot_mapping", torch.int64, 1, dev)
+    NB, BS, Hkv, D = key_cache.shape
+    T = slot_mapping.shape[0]
+    if (value_cache.shape != (NB, Hkv, D, BS) or key.shape != (T, Hkv, D) or value.shape != key.shape
+            or kmin.shape != (NB, Hkv, D) or kmax.shape != kmin.shape):
+        raise ValueError("shape mismatch between key/value, the caches and the metadata")
+    _scales(k_scale, v_scale, Hkv, dev)
+    _check("quest_reshape_and_cache_fp8",
+           L.quest_reshape_and_cache_fp8(_ptr(key), _ptr(value), _ptr(key_cache), _ptr(value_cache),
+                                         _ptr(kmin), _ptr(kmax), _ptr(slot_mapping), T, _ptr(k_scale),
+                                         _ptr(v_scale), Hkv, D, BS, NB, _stream(dev)))
+
+
+def quest_rebuild_meta_fp8(kmin: torch.Tensor, kmax: torch.Tensor, key_cache: torch.Tensor,
+                           block_tables: torch.Tensor, context_lens: torch.Tensor) -> None:
+    """Recompute the 8-bit metadata of every block the sequences use from the 8-bit cache."""
+    L = load_library()
+    _need(key_cache, "key_cache", torch.uint8, 4)
+    dev = key_cache.device
+    _need(kmin, "kmin", torch.uint8, 3, dev)
+    _need(kmax, "kmax", torch.uint8, 3, dev)
+    _need(block_tables, "block_tables", torch.int32, 2, dev)
+    _need(context_lens, "context_lens", torch.int32, 1, dev)
+    NB, BS, Hkv, D = key_cache.shape
+    B, MBS = block_tables.shape
+    if kmin.shape != (NB, Hkv, D) or kmax.shape != kmin.shape:
+        raise ValueError("metadata must be [NB, Hkv, D]")
+    _check("quest_rebuild_meta_fp8",
+           L.quest_rebuild_meta_fp8(_ptr(kmin), _ptr(kmax), _ptr(key_cache), _ptr(block_tables), MBS,
+                                    _ptr(context_lens), B, Hkv, D, BS, NB, _stream(dev)))
+
+
+def quest_select_topk_fp8(selected: torch.Tensor, query: torch.Tensor, kmin: torch.Tensor,
+                          kmax: torch.Tensor, block_tables: torch.Tensor, context_lens: torch.Tensor,
+                          block_size: int, workspace: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """Quest selection on 8-bit metadata; writes selected [B, Hkv, topk]."""
+    L = load_library()
+    _need(kmin, "kmin", torch.uint8, 3)
+    dev = kmin.device
+    _need(kmax, "kmax", torch.uint8, 3, dev)
+    _need(query, "query", torch.bfloat16, 3, dev)
+    _need(selected, "selected", torch.int32, 3, dev)
+    _need(block_tables, "block_tables", torch.int32, 2, dev)
+    _need(context_lens, "context_lens", torch.int32, 1, dev)
+    B, Hq, D = query.shape
+    NB, Hkv, D2 = kmin.shape
+    MBS = block_tables.shape[1]
+    if D != D2 or selected.shape[:2] != (B, Hkv):
+        raise ValueError("shape mismatch in quest_select_topk_fp8")
+    topk = selected.shape[2]
+    need = quest_select_workspace_size(B, Hkv, MBS)
+    ws = workspace if workspace is not None else _default_sel_ws.get(dev, need)
+    _check("quest_select_topk_fp8",
+           L.quest_select_topk_fp8(_ptr(selected), _ptr(query), _ptr(kmin), _ptr(kmax),
+                                   _ptr(block_tables), MBS, _ptr(context_lens), B, Hq, Hkv, D,
+                                   int(block_size), NB, topk, _ptr(ws), ws.numel() * ws.element_size(),
+                                   _stream(dev)))
+    return selected
+
+
+def _attention_checks_fp8(out, query, key_cache, value_cache, block_tables, context_lens,
+                          k_scale, v_scale):
+    _need(key_cache, "key_cache", torch.uint8, 4)
+    dev = key_cache.device
+    _need(value_cache, "value_cache", torch.uint8, 4, dev)
+    _need(query, "query", torch.bfloat16, 3, dev)
+    _need(out, "out", torch.bfloat16, 3, dev)
+    _need(block_tables, "block_tables", torch.int32, 2, dev)
+    _need(context_lens, "context_lens", torch.int32, 1, dev)
+    B, Hq, D = query.shape
+    NB, BS, Hkv, D2 = key_cache.shape
+    if D != D2 or value_cache.shape != (NB, Hkv, D, BS) or out.shape != query.shape:
+        raise ValueError("shape mismatch between query/out and the caches")
+    if block_tables.shape[0] != B or context_lens.shape[0] != B:
+        raise ValueError("block_tables / context_lens batch mismatch")
+    _scales(k_scale, v_scale, Hkv, dev)
+    return dev, B, Hq, Hkv, D, BS, NB, block_tables.shape[1]
+
+
+def pa_decode_fp8(out: torch.Tensor, query: torch.Tensor, key_cache: torch.Tensor,
+                  value_cache: torch.Tensor, k_scale: torch.Tensor, v_scale: torch.Tensor,
+                  block_tables: torch.Tensor, context_lens: torch.Tensor, scale: float,
+                  workspace: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """Dense GQA paged decode attention over 8-bit caches; writes out [B, Hq, D] (bf16)."""
+    L = load_library()
+    dev, B, Hq, Hkv, D, BS, NB, MBS = _attention_checks_fp8(out, query, key_cache, value_cache,
+                                                            block_tables, context_lens, k_scale, v_scale)
+    need = pa_decode_workspace_size(B, Hq, Hkv, D)
+    ws = workspace if workspace is not None else _default_ws.get(dev, need)
+    _check("pa_decode_fp8",
+           L.pa_decode_fp8(_ptr(out), _ptr(query), _ptr(key_cache), _ptr(value_cache), _ptr(k_scale),
+                           _ptr(v_scale), _ptr(block_tables), MBS, _ptr(context_lens), B, Hq, Hkv, D,
+                           BS, NB, float(scale), _ptr(ws), ws.numel() * ws.element_size(),
+                           _stream(dev)))
+    return out
+
+
+def quest_sparse_decode_fp8(out: torch.Tensor, query: torch.Tensor, key_cache: torch.Tensor,
+                            value_cache: torch.Tensor, k_scale: torch.Tensor, v_scale: torch.Tensor,
+                            block_tables: torch.Tensor, context_lens: torch.Tensor,
+                            selected: torch.Tensor, scale: float,
+                            workspace: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """Quest sparse attention over 8-bit caches and the selected [B, Hkv, topk] blocks."""
+    L = load_library()
+    dev, B, Hq, Hkv, D, BS, NB, MBS = _attention_checks_fp8(out, query, key_cache, value_cache,
+                                                            block_tables, context_lens, k_scale, v_scale)
+    _need(selected, "selected", torch.int32, 3, dev)
+    if selected.shape[:2] != (B, Hkv):
+        raise ValueError("selected must be [B, Hkv, topk]")
+    topk = selected.shape[2]
+    need = pa_decode_workspace_size(B, Hq, Hkv, D)
+    ws = workspace if workspace is not None else _default_ws.get(dev, need)
+    _check("quest_sparse_decode_fp8",
+           L.quest_sparse_decode_fp8(_ptr(out), _ptr(query), _ptr(key_cache), _ptr(value_cache),
+                                     _ptr(k_scale), _ptr(v_scale), _ptr(block_tables), MBS,
+                                     _ptr(context_lens), _ptr(selected), topk, B, Hq, Hkv, D, BS, NB,
+                                     float(scale), _ptr(ws), ws.numel() * ws.element_size(),
+                                     _stream(dev)))
+    return out

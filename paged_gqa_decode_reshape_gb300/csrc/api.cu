@@ -45,19 +45,27 @@ EncodeTiledFn encode_fn() {
     return fn;
 }
 
-// Tensor map over one layer's paged cache [NB][BS][Hkv][D] (bf16), boxes of
-// [1 block][BS tokens][1 head][64 dims] with 128-byte swizzle.
-int make_cache_map(CUtensorMap *map, const void *cache, int Hkv, int D, int BS, int64_t NB) {
+// Tensor map over one layer's paged cache [NB][BS][Hkv][D], boxes of
+// [1 block][BS tokens][1 head][128 bytes of dims] with 128-byte swizzle:
+// 64 bf16 dims, or 128 E4M3 codes (fp8).
+int make_cache_map(CUtensorMap *map, const void *cache, int Hkv, int D, int BS, int64_t NB,
+                   bool fp8 = false) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return cuda_fail(cudaErrorNotSupported);
+    const cuuint64_t eb = fp8 ? 1 : 2;
     const cuuint64_t dims[4] = {cuuint64_t(D), cuuint64_t(Hkv), cuuint64_t(BS), cuuint64_t(NB)};
-    const cuuint64_t strides[3] = {cuuint64_t(D) * 2, cuuint64_t(Hkv) * D * 2,
-                                   cuuint64_t(BS) * Hkv * D * 2};
-    const cuuint32_t box[4] = {64u, 1u, cuuint32_t(BS), 1u};
+    const cuuint64_t strides[3] = {cuuint64_t(D) * eb, cuuint64_t(Hkv) * D * eb,
+                                   cuuint64_t(BS) * Hkv * D * eb};
+    const cuuint32_t box[4] = {fp8 ? 128u : 64u, 1u, cuuint32_t(BS), 1u};
     const cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
-    const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(cache), dims,
+    // bf16: the two 128-byte halves of a row belong to the same tile, so L2
+    // fills of 256 bytes waste nothing; an E4M3 row is 128 bytes and its
+    // neighbour belongs to another KV head, so fills stay at 128 bytes.
+    const CUresult r = fn(map, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4,
+                          const_cast<void *>(cache), dims,
                           strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_SWIZZLE_128B,
+                          fp8 ? CU_TENSOR_MAP_L2_PROMOTION_L2_128B : CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return cuda_fail(cudaErrorInvalidValue);
     return PA_OK;
@@ -96,28 +104,35 @@ int check_attention_args(const void *out, const void *q, const void *kc, const v
     return PA_OK;
 }
 
-int run_decode(pa_bf16 *out, const pa_bf16 *query, const pa_bf16 *key_cache,
-               const pa_bf16 *value_cache, const int32_t *block_tables, int MBS,
-               const int32_t *context_lens, const int32_t *selected, int topk, int B, int Hq,
-               int Hkv, int D, int BS, int64_t NB, float scale, void *workspace,
-               size_t workspace_bytes, void *stream, bool sparse) {
+int run_decode(pa_bf16 *out, const pa_bf16 *query, const void *key_cache, const void *value_cache,
+               const int32_t *block_tables, int MBS, const int32_t *context_lens,
+               const int32_t *selected, int topk, int B, int Hq, int Hkv, int D, int BS, int64_t NB,
+               float scale, void *workspace, size_t workspace_bytes, void *stream, bool sparse,
+               const float *k_scale = nullptr, const float *v_scale = nullptr, bool fp8 = false) {
     int rc = check_attention_args(out, query, key_cache, value_cache, block_tables, MBS,
                                   context_lens, B, Hq, Hkv, D, BS, NB, scale, workspace);
     if (rc != PA_OK) return rc;
     if (sparse && (!selected || topk <= 0)) return PA_ERR_INVALID_ARG;
+    if (fp8 && (!k_scale || !v_scale)) return PA_ERR_INVALID_ARG;
+    if (fp8 && D != 128) return PA_ERR_UNSUPPORTED;
     DecodeGeometry geo;
-    cudaError_t e = decode_geometry(D, &geo);
+    cudaError_t e = decode_geometry(D, &geo, fp8);
     if (e != cudaSuccess) return cuda_fail(e);
     if (workspace_bytes < decode_workspace_bytes(B, Hkv, D, geo.workers)) return PA_ERR_WORKSPACE;
     CUtensorMap tk, tv;
-    if ((rc = make_cache_map(&tk, key_cache, Hkv, D, BS, NB)) != PA_OK) return rc;
-    if ((rc = make_cache_map(&tv, value_cache, Hkv, D, BS, NB)) != PA_OK) return rc;
+    if ((rc = make_cache_map(&tk, key_cache, Hkv, D, BS, NB, fp8)) != PA_OK) return rc;
+    // an E4M3 V cache is read with plain bulk copies (its tiles are contiguous)
+    if (fp8) std::memset(&tv, 0, sizeof tv);
+    else if ((rc = make_cache_map(&tv, value_cache, Hkv, D, BS, NB)) != PA_OK) return rc;
     const DecodeWorkspace w = carve_decode_ws(workspace, B, Hkv);
     DecodeArgs a;
     a.q = query;
     a.bt = block_tables;
     a.ctx = context_lens;
     a.sel = selected;
+    a.k_scale = k_scale;
+    a.v_scale = v_scale;
+    a.v8 = fp8 ? static_cast<const uint8_t *>(value_cache) : nullptr;
     a.out = out;
     a.part = w.part;
     a.counters = w.counters;
@@ -136,7 +151,7 @@ int run_decode(pa_bf16 *out, const pa_bf16 *query, const pa_bf16 *key_cache,
     a.Hkv = Hkv;
     a.G = Hq / Hkv;
     a.scale_log2 = scale * 1.4426950408889634f;
-    e = launch_decode(tk, tv, a, D, sparse, static_cast<cudaStream_t>(stream));
+    e = launch_decode(tk, tv, a, D, sparse, static_cast<cudaStream_t>(stream), fp8);
     if (e != cudaSuccess) return cuda_fail(e);
     return PA_OK;
 }
@@ -312,6 +327,139 @@ int pa_check_metadata(int32_t *counts, const int64_t *slot_mapping, int64_t num_
                                                 max_blocks_per_seq, context_lens, batch, block_size,
                                                 num_blocks, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? PA_OK : cuda_fail(e);
+}
+
+}  // extern "C"
+
+/* ------------------------------------------------- 8-bit (E4M3) KV cache */
+
+namespace {
+// shared checks of the fp8 write / metadata entry points
+int check_fp8_write(int64_t num_tokens, int num_kv_heads, int head_dim, int block_size,
+                    int64_t num_blocks) {
+    if (num_tokens < 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 || num_blocks <= 0)
+        return PA_ERR_INVALID_ARG;
+    if (head_dim != 128 || block_size != kBlockSize) return PA_ERR_UNSUPPORTED;
+    if (num_tokens > (int64_t(1) << 31) - 1) return PA_ERR_UNSUPPORTED;
+    return PA_OK;
+}
+}  // namespace
+
+extern "C" {
+
+int pa_reshape_and_cache_fp8(const pa_bf16 *key, const pa_bf16 *value, pa_e4m3 *key_cache,
+                             pa_e4m3 *value_cache, const int64_t *slot_mapping, int64_t num_tokens,
+                             const float *k_scale, const float *v_scale, int num_kv_heads,
+                             int head_dim, int block_size, int64_t num_blocks, void *stream) {
+    int rc = check_fp8_write(num_tokens, num_kv_heads, head_dim, block_size, num_blocks);
+    if (rc != PA_OK) return rc;
+    if (num_tokens == 0) return PA_OK;
+    if (!key || !value || !key_cache || !value_cache || !slot_mapping || !k_scale || !v_scale)
+        return PA_ERR_INVALID_ARG;
+    if (!aligned16(key) || !aligned16(value) || !aligned16(key_cache) || !aligned16(value_cache))
+        return PA_ERR_INVALID_ARG;
+    const cudaError_t e = launch_write_fp8(key_cache, value_cache, nullptr, nullptr, key, value, k_scale,
+                                           v_scale, slot_mapping, num_tokens, num_kv_heads, head_dim,
+                                           block_size, num_blocks, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? PA_OK : cuda_fail(e);
+}
+
+int quest_reshape_and_cache_fp8(const pa_bf16 *key, const pa_bf16 *value, pa_e4m3 *key_cache,
+                                pa_e4m3 *value_cache, pa_e4m3 *kmin, pa_e4m3 *kmax,
+                                const int64_t *slot_mapping, int64_t num_tokens, const float *k_scale,
+                                const float *v_scale, int num_kv_heads, int head_dim, int block_size,
+                                int64_t num_blocks, void *stream) {
+    int rc = check_fp8_write(num_tokens, num_kv_heads, head_dim, block_size, num_blocks);
+    if (rc != PA_OK) return rc;
+    if (num_tokens == 0) return PA_OK;
+    if (!key || !value || !key_cache || !value_cache || !kmin || !kmax || !slot_mapping || !k_scale ||
+        !v_scale)
+        return PA_ERR_INVALID_ARG;
+    if (!aligned16(key) || !aligned16(value) || !aligned16(key_cache) || !aligned16(value_cache) ||
+        !aligned16(kmin) || !aligned16(kmax))
+        return PA_ERR_INVALID_ARG;
+    const cudaError_t e = launch_write_fp8(key_cache, value_cache, kmin, kmax, key, value, k_scale, v_scale,
+                                           slot_mapping, num_tokens, num_kv_heads, head_dim, block_size,
+                                           num_blocks, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? PA_OK : cuda_fail(e);
+}
+
+int quest_update_meta_fp8(pa_e4m3 *kmin, pa_e4m3 *kmax, const pa_bf16 *key, const int64_t *slot_mapping,
+                          int64_t num_tokens, const float *k_scale, int num_kv_heads, int head_dim,
+                          int block_size, int64_t num_blocks, void *stream) {
+    int rc = check_fp8_write(num_tokens, num_kv_heads, head_dim, block_size, num_blocks);
+    if (rc != PA_OK) return rc;
+    if (num_tokens == 0) return PA_OK;
+    if (!kmin || !kmax || !key || !slot_mapping || !k_scale) return PA_ERR_INVALID_ARG;
+    if (!aligned16(kmin) || !aligned16(kmax) || !aligned16(key)) return PA_ERR_INVALID_ARG;
+    const cudaError_t e = launch_update_meta_fp8(kmin, kmax, key, k_scale, slot_mapping, num_tokens,
+                                                 num_kv_heads, head_dim, block_size, num_blocks,
+                                                 static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? PA_OK : cuda_fail(e);
+}
+
+int quest_rebuild_meta_fp8(pa_e4m3 *kmin, pa_e4m3 *kmax, const pa_e4m3 *key_cache,
+                           const int32_t *block_tables, int max_blocks_per_seq,
+                           const int32_t *context_lens, int batch, int num_kv_heads, int head_dim,
+                           int block_size, int64_t num_blocks, void *stream) {
+    if (!kmin || !kmax || !key_cache || !block_tables || !context_lens) return PA_ERR_INVALID_ARG;
+    if (batch <= 0 || max_blocks_per_seq <= 0 || num_kv_heads <= 0 || num_blocks <= 0)
+        return PA_ERR_INVALID_ARG;
+    if (head_dim != 128 || block_size != kBlockSize || batch > 65535) return PA_ERR_UNSUPPORTED;
+    if (!aligned16(kmin) || !aligned16(kmax) || !aligned16(key_cache)) return PA_ERR_INVALID_ARG;
+    const cudaError_t e = launch_rebuild_meta_fp8(kmin, kmax, key_cache, block_tables, max_blocks_per_seq,
+                                                  context_lens, batch, num_kv_heads, head_dim, block_size,
+                                                  num_blocks, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? PA_OK : cuda_fail(e);
+}
+
+int quest_select_topk_fp8(int32_t *selected, const pa_bf16 *query, const pa_e4m3 *kmin,
+                          const pa_e4m3 *kmax, const int32_t *block_tables, int max_blocks_per_seq,
+                          const int32_t *context_lens, int batch, int num_q_heads, int num_kv_heads,
+                          int head_dim, int block_size, int64_t num_blocks, int topk, void *workspace,
+                          size_t workspace_bytes, void *stream) {
+    if (!selected || !query || !kmin || !kmax || !block_tables || !context_lens || !workspace)
+        return PA_ERR_INVALID_ARG;
+    if (batch <= 0 || num_q_heads <= 0 || num_kv_heads <= 0 || max_blocks_per_seq <= 0 ||
+        num_blocks <= 0 || topk <= 0 || head_dim <= 0 || block_size <= 0)
+        return PA_ERR_INVALID_ARG;
+    if (num_q_heads % num_kv_heads != 0) return PA_ERR_INVALID_ARG;
+    if (head_dim != 128 || block_size != kBlockSize || batch > kMaxBatch) return PA_ERR_UNSUPPORTED;
+    if (int64_t(max_blocks_per_seq) * block_size > int64_t(1) << 30) return PA_ERR_UNSUPPORTED;
+    if (!aligned16(query) || !aligned16(kmin) || !aligned16(kmax) || !aligned16(workspace))
+        return PA_ERR_INVALID_ARG;
+    if (workspace_bytes < quest_select_workspace_size(batch, num_kv_heads, max_blocks_per_seq))
+        return PA_ERR_WORKSPACE;
+    const cudaError_t e = launch_quest_select(
+        selected, static_cast<float *>(workspace), query, kmin, kmax, block_tables, max_blocks_per_seq,
+        context_lens, batch, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, topk,
+        static_cast<cudaStream_t>(stream), true);
+    return e == cudaSuccess ? PA_OK : cuda_fail(e);
+}
+
+int pa_decode_fp8(pa_bf16 *out, const pa_bf16 *query, const pa_e4m3 *key_cache,
+                  const pa_e4m3 *value_cache, const float *k_scale, const float *v_scale,
+                  const int32_t *block_tables, int max_blocks_per_seq, const int32_t *context_lens,
+                  int batch, int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                  int64_t num_blocks, float scale, void *workspace, size_t workspace_bytes,
+                  void *stream) {
+    return run_decode(out, query, key_cache, value_cache, block_tables, max_blocks_per_seq,
+                      context_lens, nullptr, 0, batch, num_q_heads, num_kv_heads, head_dim,
+                      block_size, num_blocks, scale, workspace, workspace_bytes, stream, false, k_scale,
+                      v_scale, true);
+}
+
+int quest_sparse_decode_fp8(pa_bf16 *out, const pa_bf16 *query, const pa_e4m3 *key_cache,
+                            const pa_e4m3 *value_cache, const float *k_scale, const float *v_scale,
+                            const int32_t *block_tables, int max_blocks_per_seq,
+                            const int32_t *context_lens, const int32_t *selected, int topk, int batch,
+                            int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                            int64_t num_blocks, float scale, void *workspace, size_t workspace_bytes,
+                            void *stream) {
+    return run_decode(out, query, key_cache, value_cache, block_tables, max_blocks_per_seq,
+                      context_lens, selected, topk, batch, num_q_heads, num_kv_heads, head_dim,
+                      block_size, num_blocks, scale, workspace, workspace_bytes, stream, true, k_scale,
+                      v_scale, true);
 }
 
 }  // extern "C"

@@ -61,6 +61,14 @@ constexpr uint64_t kWaitLimitNs = 500ull * 1000ull * 1000ull;  // 0.5 s per mbar
 #ifndef PA_DECODE_PAIRS
 #define PA_DECODE_PAIRS 3
 #endif
+// E4M3 cache: consumer warps and pairs in flight (its items are half the
+// bytes, so twice the consumers keep the same bytes in flight)
+#ifndef PA_DECODE_CONSUMERS_F8
+#define PA_DECODE_CONSUMERS_F8 7
+#endif
+#ifndef PA_DECODE_PAIRS_F8
+#define PA_DECODE_PAIRS_F8 3
+#endif
 
 // Optional CTA timeline (%globaltimer) for tuning builds: compile with
 // -DPA_DECODE_TRACE and the kernel writes 16 words per CTA (timestamps, SM id,
@@ -83,17 +91,18 @@ constexpr uint64_t kWaitLimitNs = 500ull * 1000ull * 1000ull;  // 0.5 s per mbar
     } while (0)
 #endif
 
-template <int D>
+template <int D, bool F8 = false>
 struct DecodeCfg {
+    static_assert(!F8 || D == 128, "the E4M3 cache path is for head_dim 128");
     static constexpr int BS = kBlockSize;
-    static constexpr int KT = BS * D * 2;       // bytes of one K (or V) tile
+    static constexpr int KT = BS * D * (F8 ? 1 : 2);  // bytes of one K (or V) tile
     static constexpr int STAGE = 2 * KT;        // K + V
     static constexpr int NKK = D / 16;          // QK k-steps == PV m-tiles
     static constexpr int HALF = BS * 128;       // bytes of one 64-dim half tile
     static constexpr int PART = D * 8 + 8;      // floats per partial slot: O[D][8], lse[8]
-    static constexpr int NC = PA_DECODE_CONSUMERS;
+    static constexpr int NC = F8 ? PA_DECODE_CONSUMERS_F8 : PA_DECODE_CONSUMERS;
     static constexpr int THREADS = (NC + 1) * 32;
-    static constexpr int R = (D == 128) ? PA_DECODE_PAIRS : 2 * PA_DECODE_PAIRS;
+    static constexpr int R = F8 ? PA_DECODE_PAIRS_F8 : (D == 128 ? PA_DECODE_PAIRS : 2 * PA_DECODE_PAIRS);
     static constexpr int S = 2 * NC * R;        // ring stages
     static constexpr int SCR = D * 8 + 16;      // floats per consumer merge slot: acc[D][8], m[8], l[8]
     static constexpr size_t off_bars = size_t(S) * STAGE;
@@ -104,11 +113,11 @@ struct DecodeCfg {
     static constexpr size_t smem_bytes(int B) { return 1024 + off_pre + size_t(B + 1) * 4; }
 };
 
-template <int D, bool SPARSE>
-__global__ void __launch_bounds__(DecodeCfg<D>::THREADS, 1)
+template <int D, bool SPARSE, bool F8>
+__global__ void __launch_bounds__(DecodeCfg<D, F8>::THREADS, 1)
     decode_kernel(const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const DecodeArgs a) {
-    using C = DecodeCfg<D>;
+    using C = DecodeCfg<D, F8>;
     constexpr int BS = C::BS, NC = C::NC, S = C::S, NKK = C::NKK;
 
     extern __shared__ uint8_t smem_raw[];
@@ -257,7 +266,7 @@ __global__ void __launch_bounds__(DecodeCfg<D>::THREADS, 1)
         unsigned fail_armed = 0;  // after a failure: leader lanes whose item was armed
         // 8 items per step: lane = 4 * item + part, part = which tile copy
         const int it = lane >> 2, part = lane & 3;
-        constexpr int PARTS = 2 * (D / 64);  // K and V, 64-dim halves
+        constexpr int PARTS = F8 ? 2 : 2 * (D / 64);  // K and V (bf16: 64-dim halves)
         for (int k0 = 0; k0 < n_items; k0 += 8) {
             if (k0 >= wbase + 32) {
                 wa = wb;
@@ -292,10 +301,22 @@ __global__ void __launch_bounds__(DecodeCfg<D>::THREADS, 1)
             ok = __shfl_sync(0xffffffffu, ok, lane & ~3);
             __syncwarp();
             if (live && ok && nv > 0 && part < PARTS) {
-                constexpr int HV = D / 64;             // 64-dim halves per tile
-                const int tsel = part / HV, hf = part % HV;  // 0: K, 1: V
-                const uint32_t dst = base + st * C::STAGE + tsel * C::KT + hf * C::HALF;
-                tma_load_4d(dst, tsel ? &tm_v : &tm_k, fb, hf * 64, seg % Hkv, 0, ph, policy);
+                if constexpr (F8) {
+                    // K: one [16 tokens x 128 dims] byte box (tensor map); V:
+                    // the block's [128 dims x 16 tokens] byte matrix of this KV head
+                    const uint32_t dst = base + st * C::STAGE + part * C::KT;
+                    if (part == 0) {
+                        tma_load_4d(dst, &tm_k, fb, 0, seg % Hkv, 0, ph, policy);
+                    } else {  // the V tile is 2 KB of contiguous bytes: one plain bulk copy
+                        const uint8_t *src = a.v8 + (int64_t(ph) * Hkv + seg % Hkv) * int64_t(C::KT);
+                        bulk_load_1d(dst, src, uint32_t(C::KT), fb, policy);
+                    }
+                } else {
+                    constexpr int HV = D / 64;             // 64-dim halves per tile
+                    const int tsel = part / HV, hf = part % HV;  // 0: K, 1: V
+                    const uint32_t dst = base + st * C::STAGE + tsel * C::KT + hf * C::HALF;
+                    tma_load_4d(dst, tsel ? &tm_v : &tm_k, fb, hf * 64, seg % Hkv, 0, ph, policy);
+                }
             }
             if (!__all_sync(0xffffffffu, ok)) {
                 // a stage was never released: give up (consumers skip their
@@ -328,7 +349,8 @@ __global__ void __launch_bounds__(DecodeCfg<D>::THREADS, 1)
     // ==================================================================== consumers
     const int c_id = warp;  // 0 .. NC-1
     const int g = lane >> 2, q4 = lane & 3;
-    const float scale_log2 = a.scale_log2;
+    float scale_log2 = a.scale_log2;  // E4M3 cache: times the segment's K scale
+    float v_scale = 1.f;               // E4M3 cache: the segment's V scale
     uint32_t qb[NKK][2];
     float acc[NKK][4];
     float m0, m1, l0, l1;
@@ -339,10 +361,24 @@ __global__ void __launch_bounds__(DecodeCfg<D>::THREADS, 1)
         const bool hv = g < G;
         const uint32_t *qrow = reinterpret_cast<const uint32_t *>(
             a.q + (int64_t(b) * a.Hq + kvh * G + (hv ? g : 0)) * D);
+        if constexpr (F8) {
+            // f16 B fragments in the k order the E4M3 K fragments come in:
+            // k-step kk covers dims 16kk + 4*q4 + {0, 1} (b0) and {2, 3} (b1)
 #pragma unroll
-        for (int kk = 0; kk < NKK; ++kk) {
-            qb[kk][0] = hv ? __ldg(qrow + 8 * kk + q4) : 0u;
-            qb[kk][1] = hv ? __ldg(qrow + 8 * kk + 4 + q4) : 0u;
+            for (int kk = 0; kk < NKK; ++kk) {
+                const uint2 v = hv ? __ldg(reinterpret_cast<const uint2 *>(qrow + 8 * kk + 2 * q4))
+                                   : make_uint2(0u, 0u);
+                qb[kk][0] = pack_f16x2(bf16_lo(v.x), bf16_hi(v.x));
+                qb[kk][1] = pack_f16x2(bf16_lo(v.y), bf16_hi(v.y));
+            }
+            scale_log2 = a.scale_log2 * __ldg(a.k_scale + kvh);
+            v_scale = __ldg(a.v_scale + kvh);
+        } else {
+#pragma unroll
+            for (int kk = 0; kk < NKK; ++kk) {
+                qb[kk][0] = hv ? __ldg(qrow + 8 * kk + q4) : 0u;
+                qb[kk][1] = hv ? __ldg(qrow + 8 * kk + 4 + q4) : 0u;
+            }
         }
 #pragma unroll
         for (int mt = 0; mt < NKK; ++mt)
@@ -386,6 +422,63 @@ __global__ void __launch_bounds__(DecodeCfg<D>::THREADS, 1)
             mma_bf16(acc[mt], a0 & mlo, a1 & mlo, a2 & mhi, a3 & mhi, pb0, pb1);
         }
     };
+    // E4M3 tiles: one [16 tokens x 128 dims] byte box, 128-byte swizzle. An
+    // ldmatrix.x4 of 16-bit pairs gives lane (g, q4) the 4 codes at dims
+    // 32c + 4q4 .. +3 (and 32c + 16 + 4q4 ..) of tokens g and g + 8. For
+    // S^T = K Q^T those are the A fragments of two k-steps with k = 2q4 + e
+    // standing for dim 4q4 + e and k = 2q4 + 8 + e for dim 4q4 + 2 + e (the
+    // query fragments use the same order); each code pair becomes an f16 pair.
+    auto qk8 = [&](uint32_t kb, float (&sc)[4]) {
+        float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
+        const int rk = (lane & 7) + (((lane >> 3) & 1) << 3);
+#pragma unroll
+        for (int c2 = 0; c2 < NKK / 2; ++c2) {
+            const int ch = 2 * c2 + (lane >> 4);
+            uint32_t r0, r1, r2, r3;
+            ldsm_x4(kb + rk * 128 + ((ch ^ (lane & 7)) << 4), r0, r1, r2, r3);
+            uint32_t h0l, h0h, h1l, h1h, h2l, h2h, h3l, h3h;
+            e4m3x4_to_f16x2x2(r0, h0l, h0h);
+            e4m3x4_to_f16x2x2(r1, h1l, h1h);
+            e4m3x4_to_f16x2x2(r2, h2l, h2h);
+            e4m3x4_to_f16x2x2(r3, h3l, h3h);
+            mma_f16(sa, h0l, h1l, h0h, h1h, qb[2 * c2][0], qb[2 * c2][1]);
+            mma_f16(sb, h2l, h3l, h2h, h3h, qb[2 * c2 + 1][0], qb[2 * c2 + 1][1]);
+        }
+#pragma unroll
+        for (int e = 0; e < 4; ++e) sc[e] = sa[e] + sb[e];
+    };
+    // O^T += V^T P^T from an E4M3 V tile, stored per block and KV head as a
+    // [128 dims x 16 tokens] byte matrix with the tokens of a row in the
+    // order 0 1 8 9 2 3 10 11 ...: an ldmatrix.x4 over 32 consecutive dim
+    // rows gives lane (g, q4) the codes of tokens 2q4, 2q4+1, 8+2q4, 9+2q4 of
+    // dims g, g+8, g+16, g+24 -- after conversion exactly the V^T A
+    // fragments of two m-tiles (rows = dims, k = tokens), no transpose.
+    auto pv8 = [&](uint32_t vb, uint32_t p01, uint32_t p23, int nv) {
+        const uint32_t pb0 = movmatrix_trans(p01), pb1 = movmatrix_trans(p23);
+        const bool part_blk = nv < BS;
+        uint32_t mlo = 0xffffffffu, mhi = 0xffffffffu;
+        if (part_blk) {
+            const int t0 = 2 * q4;
+            mlo = (t0 < nv ? 0x0000ffffu : 0u) | (t0 + 1 < nv ? 0xffff0000u : 0u);
+            mhi = (t0 + 8 < nv ? 0x0000ffffu : 0u) | (t0 + 9 < nv ? 0xffff0000u : 0u);
+        }
+#pragma unroll
+        for (int c2 = 0; c2 < NKK / 2; ++c2) {
+            uint32_t r0, r1, r2, r3;
+            ldsm_x4(vb + (32 * c2 + lane) * 16, r0, r1, r2, r3);
+            uint32_t a0, a2, a1, a3, b0, b2, b1, b3;
+            e4m3x4_to_f16x2x2(r0, a0, a2);
+            e4m3x4_to_f16x2x2(r1, a1, a3);
+            e4m3x4_to_f16x2x2(r2, b0, b2);
+            e4m3x4_to_f16x2x2(r3, b1, b3);
+            if (part_blk) {  // tokens past the context: zero V (garbage may be NaN)
+                a0 &= mlo; a1 &= mlo; a2 &= mhi; a3 &= mhi;
+                b0 &= mlo; b1 &= mlo; b2 &= mhi; b3 &= mhi;
+            }
+            mma_f16(acc[2 * c2], a0, a1, a2, a3, pb0, pb1);
+            mma_f16(acc[2 * c2 + 1], b0, b1, b2, b3, pb0, pb1);
+        }
+    };
     // wait for an item's stage (skipped once the CTA has given up); returns
     // the item's valid token count
     auto wait_full = [&](int k) -> int {
@@ -404,8 +497,13 @@ __global__ void __launch_bounds__(DecodeCfg<D>::THREADS, 1)
         const uint32_t s0a = base + (ka % S) * C::STAGE;
         const uint32_t s1a = base + (kb_ % S) * C::STAGE;
         float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
-        if (nva > 0) qk(s0a, s0);
-        if (nvb > 0) qk(s1a, s1);
+        if constexpr (F8) {
+            if (nva > 0) qk8(s0a, s0);
+            if (nvb > 0) qk8(s1a, s1);
+        } else {
+            if (nva > 0) qk(s0a, s0);
+            if (nvb > 0) qk(s1a, s1);
+        }
         const float x0 = (g < nva) ? s0[0] * scale_log2 : -INFINITY;
         const float x1 = (g < nva) ? s0[1] * scale_log2 : -INFINITY;
         const float x2 = (g + 8 < nva) ? s0[2] * scale_log2 : -INFINITY;
@@ -426,12 +524,17 @@ __global__ void __launch_bounds__(DecodeCfg<D>::THREADS, 1)
         const float r1 = (mn1 == -INFINITY) ? 0.f : mn1;
         const bool grow = (mn0 != m0) || (mn1 != m1);
         const float al0 = fast_exp2(m0 - r0), al1 = fast_exp2(m1 - r1);
-        const uint32_t p01 = pack_bf16x2(fast_exp2(x0 - r0), fast_exp2(x1 - r1));
-        const uint32_t p23 = pack_bf16x2(fast_exp2(x2 - r0), fast_exp2(x3 - r1));
-        const uint32_t q01 = pack_bf16x2(fast_exp2(y0 - r0), fast_exp2(y1 - r1));
-        const uint32_t q23 = pack_bf16x2(fast_exp2(y2 - r0), fast_exp2(y3 - r1));
-        l0 = l0 * al0 + ((bf16_lo(p01) + bf16_lo(p23)) + (bf16_lo(q01) + bf16_lo(q23)));
-        l1 = l1 * al1 + ((bf16_hi(p01) + bf16_hi(p23)) + (bf16_hi(q01) + bf16_hi(q23)));
+        // P rounded to the mma input type (bf16, or f16 for an E4M3 cache);
+        // the normaliser sums the rounded values
+        auto pk = [](float lo, float hi) { return F8 ? pack_f16x2(lo, hi) : pack_bf16x2(lo, hi); };
+        auto plo = [](uint32_t v) { return F8 ? f16_lo(v) : bf16_lo(v); };
+        auto phi = [](uint32_t v) { return F8 ? f16_hi(v) : bf16_hi(v); };
+        const uint32_t p01 = pk(fast_exp2(x0 - r0), fast_exp2(x1 - r1));
+        const uint32_t p23 = pk(fast_exp2(x2 - r0), fast_exp2(x3 - r1));
+        const uint32_t q01 = pk(fast_exp2(y0 - r0), fast_exp2(y1 - r1));
+        const uint32_t q23 = pk(fast_exp2(y2 - r0), fast_exp2(y3 - r1));
+        l0 = l0 * al0 + ((plo(p01) + plo(p23)) + (plo(q01) + plo(q23)));
+        l1 = l1 * al1 + ((phi(p01) + phi(p23)) + (phi(q01) + phi(q23)));
         m0 = mn0;
         m1 = mn1;
         if (__any_sync(0xffffffffu, grow)) {
@@ -443,8 +546,13 @@ __global__ void __launch_bounds__(DecodeCfg<D>::THREADS, 1)
                 acc[mt][3] *= al1;
             }
         }
-        if (nva > 0) pv(s0a + C::KT, p01, p23, nva);
-        if (nvb > 0) pv(s1a + C::KT, q01, q23, nvb);
+        if constexpr (F8) {
+            if (nva > 0) pv8(s0a + C::KT, p01, p23, nva);
+            if (nvb > 0) pv8(s1a + C::KT, q01, q23, nvb);
+        } else {
+            if (nva > 0) pv(s0a + C::KT, p01, p23, nva);
+            if (nvb > 0) pv(s1a + C::KT, q01, q23, nvb);
+        }
     };
 
     // Lane layout of the merge and the combine: the [D][8] output is 2*D
@@ -552,9 +660,17 @@ __global__ void __launch_bounds__(DecodeCfg<D>::THREADS, 1)
         const int hh = 2 * q4;
 #pragma unroll
         for (int mt = 0; mt < NKK; ++mt) {
-            const int d = 16 * mt + g;
-            *reinterpret_cast<float2 *>(my + d * 8 + hh) = make_float2(acc[mt][0], acc[mt][1]);
-            *reinterpret_cast<float2 *>(my + (d + 8) * 8 + hh) = make_float2(acc[mt][2], acc[mt][3]);
+            if constexpr (F8) {  // the V scale of the segment's KV head
+                const int d = 16 * mt + g;
+                *reinterpret_cast<float2 *>(my + d * 8 + hh) =
+                    make_float2(acc[mt][0] * v_scale, acc[mt][1] * v_scale);
+                *reinterpret_cast<float2 *>(my + (d + 8) * 8 + hh) =
+                    make_float2(acc[mt][2] * v_scale, acc[mt][3] * v_scale);
+            } else {
+                const int d = 16 * mt + g;
+                *reinterpret_cast<float2 *>(my + d * 8 + hh) = make_float2(acc[mt][0], acc[mt][1]);
+                *reinterpret_cast<float2 *>(my + (d + 8) * 8 + hh) = make_float2(acc[mt][2], acc[mt][3]);
+            }
         }
         if (g == 0) {
             *reinterpret_cast<float2 *>(my + D * 8 + hh) = make_float2(m0, m1);
@@ -733,9 +849,9 @@ __global__ void __launch_bounds__(DecodeCfg<D>::THREADS, 1)
     }
 }
 
-template <int D>
+template <int D, bool F8>
 cudaError_t geometry_t(DecodeGeometry *g) {
-    using C = DecodeCfg<D>;
+    using C = DecodeCfg<D, F8>;
     cudaError_t e;
     int dev = 0, sms = 0, per_sm = 0, optin = 0;
     if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
@@ -746,14 +862,16 @@ cudaError_t geometry_t(DecodeGeometry *g) {
     // per-sequence prefix grows with the batch)
     const size_t smem = C::smem_bytes(kMaxBatch) < size_t(optin) ? C::smem_bytes(kMaxBatch) : size_t(optin);
     if (smem < C::smem_bytes(1)) return cudaErrorInvalidConfiguration;
-    e = cudaFuncSetAttribute(decode_kernel<D, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+    e = cudaFuncSetAttribute(decode_kernel<D, false, F8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             int(smem));
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(decode_kernel<D, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+    e = cudaFuncSetAttribute(decode_kernel<D, true, F8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             int(smem));
     if (e != cudaSuccess) return e;
     // same L1/shared split as the library's other kernels: no reconfiguration between them
-    cudaFuncSetAttribute(decode_kernel<D, false>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
-    cudaFuncSetAttribute(decode_kernel<D, true>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_kernel<D, false>, C::THREADS, smem);
+    cudaFuncSetAttribute(decode_kernel<D, false, F8>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+    cudaFuncSetAttribute(decode_kernel<D, true, F8>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_kernel<D, false, F8>, C::THREADS, smem);
     if (e != cudaSuccess) return e;
     if (per_sm < 1) return cudaErrorInvalidConfiguration;
     g->grid = sms * per_sm;
@@ -763,33 +881,35 @@ cudaError_t geometry_t(DecodeGeometry *g) {
     return cudaSuccess;
 }
 
-template <int D, bool SPARSE>
+template <int D, bool SPARSE, bool F8>
 cudaError_t launch_t(const CUtensorMap &tm_k, const CUtensorMap &tm_v, const DecodeArgs &a,
                      cudaStream_t stream) {
-    using C = DecodeCfg<D>;
+    using C = DecodeCfg<D, F8>;
     DecodeGeometry geo;
-    cudaError_t e = decode_geometry(D, &geo);
+    cudaError_t e = decode_geometry(D, &geo, F8);
     if (e != cudaSuccess) return e;
     if (C::smem_bytes(a.B) > geo.smem) return cudaErrorInvalidConfiguration;  // batch too large
-    return launch_pdl(decode_kernel<D, SPARSE>, dim3(geo.grid), dim3(C::THREADS), C::smem_bytes(a.B),
-                      stream, tm_k, tm_v, a);
+    return launch_pdl(decode_kernel<D, SPARSE, F8>, dim3(geo.grid), dim3(C::THREADS),
+                      C::smem_bytes(a.B), stream, tm_k, tm_v, a);
 }
 
 constexpr int kMaxDevices = 64;
-DecodeGeometry g_geo[kMaxDevices][2];
-bool g_geo_ok[kMaxDevices][2];
+DecodeGeometry g_geo[kMaxDevices][3];  // head_dim 64, 128, 128 with an E4M3 cache
+bool g_geo_ok[kMaxDevices][3];
 
 }  // namespace
 
-cudaError_t decode_geometry(int head_dim, DecodeGeometry *g) {
+cudaError_t decode_geometry(int head_dim, DecodeGeometry *g, bool fp8) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-    const int idx = head_dim == 128 ? 1 : 0;
+    if (fp8 && head_dim != 128) return cudaErrorInvalidValue;
+    const int idx = fp8 ? 2 : (head_dim == 128 ? 1 : 0);
     if (!g_geo_ok[dev][idx]) {
         DecodeGeometry t{};
-        e = head_dim == 128 ? geometry_t<128>(&t) : geometry_t<64>(&t);
+        e = fp8 ? geometry_t<128, true>(&t)
+                : (head_dim == 128 ? geometry_t<128, false>(&t) : geometry_t<64, false>(&t));
         if (e != cudaSuccess) return e;
         g_geo[dev][idx] = t;
         g_geo_ok[dev][idx] = true;
@@ -815,12 +935,17 @@ size_t decode_workspace_bytes(int B, int Hkv, int head_dim, int workers) {
 }
 
 cudaError_t launch_decode(const CUtensorMap &tm_k, const CUtensorMap &tm_v, const DecodeArgs &a,
-                          int head_dim, bool sparse, cudaStream_t stream) {
+                          int head_dim, bool sparse, cudaStream_t stream, bool fp8) {
+    if (fp8) {
+        if (head_dim != 128) return cudaErrorInvalidValue;
+        return sparse ? launch_t<128, true, true>(tm_k, tm_v, a, stream)
+                      : launch_t<128, false, true>(tm_k, tm_v, a, stream);
+    }
     if (head_dim == 128)
-        return sparse ? launch_t<128, true>(tm_k, tm_v, a, stream)
-                      : launch_t<128, false>(tm_k, tm_v, a, stream);
-    return sparse ? launch_t<64, true>(tm_k, tm_v, a, stream)
-                  : launch_t<64, false>(tm_k, tm_v, a, stream);
+        return sparse ? launch_t<128, true, false>(tm_k, tm_v, a, stream)
+                      : launch_t<128, false, false>(tm_k, tm_v, a, stream);
+    return sparse ? launch_t<64, true, false>(tm_k, tm_v, a, stream)
+                  : launch_t<64, false, false>(tm_k, tm_v, a, stream);
 }
 
 }  // namespace pa

@@ -17,6 +17,9 @@ struct DecodeArgs {
     const int32_t *bt;          // [B][MBS]
     const int32_t *ctx;         // [B]
     const int32_t *sel;         // [B][Hkv][topk] (sparse only)
+    const float *k_scale;       // [Hkv] per-KV-head scales of an E4M3 cache (else null)
+    const float *v_scale;
+    const uint8_t *v8;          // E4M3 V cache [NB][Hkv][D][16] (else null): tiles are contiguous
     uint16_t *out;              // [B][Hq][D] bf16
     float *part;                // [B*Hkv + W][D*8 + 8] partial outputs and lse (log2 domain)
     int32_t *counters;          // [B*Hkv] arrival counters (zero between calls)
@@ -35,11 +38,11 @@ struct DecodeGeometry {
     size_t smem;       // dynamic shared memory limit set on the kernel
 };
 
-cudaError_t decode_geometry(int head_dim, DecodeGeometry *g);
+cudaError_t decode_geometry(int head_dim, DecodeGeometry *g, bool fp8 = false);
 size_t decode_workspace_bytes(int B, int Hkv, int head_dim, int workers);
 size_t decode_trace_offset(int B, int Hkv, int head_dim, int workers);
 cudaError_t launch_decode(const CUtensorMap &tm_k, const CUtensorMap &tm_v, const DecodeArgs &a,
-                          int head_dim, bool sparse, cudaStream_t stream);
+                          int head_dim, bool sparse, cudaStream_t stream, bool fp8 = false);
 
 cudaError_t launch_reshape_and_cache(const uint16_t *key, const uint16_t *value, uint16_t *kc,
                                      uint16_t *vc, const int64_t *slots, int64_t T, int Hkv, int D,
@@ -57,9 +60,21 @@ cudaError_t launch_check_metadata(int32_t *counts, const int64_t *slots, int64_t
                                   const int32_t *bt, int MBS, const int32_t *ctx, int B, int BS,
                                   int64_t NB, cudaStream_t stream);
 
-cudaError_t launch_quest_select(int32_t *sel, float *scores, const uint16_t *q,
-                                const uint16_t *kmin, const uint16_t *kmax, const int32_t *bt,
-                                int MBS, const int32_t *ctx, int B, int Hq, int Hkv, int D, int BS,
-                                int64_t NB, int topk, cudaStream_t stream);
+cudaError_t launch_write_fp8(uint8_t *kc, uint8_t *vc, uint8_t *kmin, uint8_t *kmax, const uint16_t *key,
+                             const uint16_t *value, const float *k_scale, const float *v_scale,
+                             const int64_t *slots, int64_t T, int Hkv, int D, int BS, int64_t NB,
+                             cudaStream_t stream);
+cudaError_t launch_update_meta_fp8(uint8_t *kmin, uint8_t *kmax, const uint16_t *key, const float *k_scale,
+                                   const int64_t *slots, int64_t T, int Hkv, int D, int BS, int64_t NB,
+                                   cudaStream_t stream);
+cudaError_t launch_rebuild_meta_fp8(uint8_t *kmin, uint8_t *kmax, const uint8_t *kc, const int32_t *bt,
+                                    int MBS, const int32_t *ctx, int B, int Hkv, int D, int BS, int64_t NB,
+                                    cudaStream_t stream);
+
+// kmin / kmax: bf16 metadata, or E4M3 codes when fp8 (head_dim 128)
+cudaError_t launch_quest_select(int32_t *sel, float *scores, const uint16_t *q, const void *kmin,
+                                const void *kmax, const int32_t *bt, int MBS, const int32_t *ctx,
+                                int B, int Hq, int Hkv, int D, int BS, int64_t NB, int topk,
+                                cudaStream_t stream, bool fp8 = false);
 
 }  // namespace pa

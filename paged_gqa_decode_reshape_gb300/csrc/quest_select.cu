@@ -41,11 +41,16 @@ constexpr int kTopkThreads = 256;
 constexpr int kChunk = 8;
 constexpr int kScoreThreads = 256;
 
-template <int D>
+// F8: the metadata are E4M3 codes (one byte per element, decoded exactly);
+// the score is the same fp32 expression of the decoded values.
+template <int D, bool F8>
 __global__ void __launch_bounds__(kScoreThreads, 4) quest_score_kernel(
-    float *__restrict__ scores, const uint16_t *__restrict__ q, const uint16_t *__restrict__ kmin,
-    const uint16_t *__restrict__ kmax, const int32_t *__restrict__ bt, int MBS,
+    float *__restrict__ scores, const uint16_t *__restrict__ q, const void *__restrict__ kmin_v,
+    const void *__restrict__ kmax_v, const int32_t *__restrict__ bt, int MBS,
     const int32_t *__restrict__ ctx, int B, int Hq, int Hkv, int BS, int64_t NB) {
+    static_assert(!F8 || D == 128, "E4M3 metadata: head_dim 128");
+    const uint16_t *__restrict__ kmin = static_cast<const uint16_t *>(kmin_v);
+    const uint16_t *__restrict__ kmax = static_cast<const uint16_t *>(kmax_v);
     constexpr int C = D / 32;  // dims per lane
     constexpr int CW = C / 2;  // 32-bit words per lane per row
     extern __shared__ int32_t pre[];  // [B+1] chunk prefix per KV head
@@ -133,7 +138,10 @@ __global__ void __launch_bounds__(kScoreThreads, 4) quest_score_kernel(
             const int ph = __shfl_sync(0xffffffffu, ph_l, u);
             ok[u] = (u < cnt) && ph >= 0 && int64_t(ph) < NB;
             const int64_t off = (int64_t(ok[u] ? ph : 0) * Hkv + kvh) * D + lane * C;
-            if (C == 4) {
+            if constexpr (F8) {  // C = 4 codes per lane per row
+                mnv[u][0] = __ldg(reinterpret_cast<const uint32_t *>(static_cast<const uint8_t *>(kmin_v) + off));
+                mxv[u][0] = __ldg(reinterpret_cast<const uint32_t *>(static_cast<const uint8_t *>(kmax_v) + off));
+            } else if (C == 4) {
                 const uint2 a2 = __ldg(reinterpret_cast<const uint2 *>(kmin + off));
                 const uint2 b2 = __ldg(reinterpret_cast<const uint2 *>(kmax + off));
                 mnv[u][0] = a2.x;
@@ -151,9 +159,17 @@ __global__ void __launch_bounds__(kScoreThreads, 4) quest_score_kernel(
             float acc = 0.f;
 #pragma unroll
             for (int cc = 0; cc < C; ++cc) {
-                const uint32_t wmn = mnv[u][cc >> 1], wmx = mxv[u][cc >> 1];
-                const float mn = (cc & 1) ? bf16_hi(wmn) : bf16_lo(wmn);
-                const float mx = (cc & 1) ? bf16_hi(wmx) : bf16_lo(wmx);
+                float mn, mx;
+                if constexpr (F8) {
+                    const uint32_t hmn = e4m3x2_to_f16x2(mnv[u][0] >> (16 * (cc >> 1)));
+                    const uint32_t hmx = e4m3x2_to_f16x2(mxv[u][0] >> (16 * (cc >> 1)));
+                    mn = (cc & 1) ? f16_hi(hmn) : f16_lo(hmn);
+                    mx = (cc & 1) ? f16_hi(hmx) : f16_lo(hmx);
+                } else {
+                    const uint32_t wmn = mnv[u][cc >> 1], wmx = mxv[u][cc >> 1];
+                    mn = (cc & 1) ? bf16_hi(wmn) : bf16_lo(wmn);
+                    mx = (cc & 1) ? bf16_hi(wmx) : bf16_lo(wmx);
+                }
                 const float t = __fadd_rn(__fmul_rn(P[cc], mx), __fmul_rn(N[cc], mn));
                 acc = (cc == 0) ? t : __fadd_rn(acc, t);
             }
@@ -285,10 +301,10 @@ __global__ void __launch_bounds__(kTopkThreads) quest_topk_kernel(
     }
 }
 
-template <int D>
-cudaError_t launch_score(float *scores, const uint16_t *q, const uint16_t *kmin,
-                         const uint16_t *kmax, const int32_t *bt, int MBS, const int32_t *ctx,
-                         int B, int Hq, int Hkv, int BS, int64_t NB, cudaStream_t stream) {
+template <int D, bool F8>
+cudaError_t launch_score(float *scores, const uint16_t *q, const void *kmin, const void *kmax,
+                         const int32_t *bt, int MBS, const int32_t *ctx, int B, int Hq, int Hkv,
+                         int BS, int64_t NB, cudaStream_t stream) {
     static int grid = 0;  // persistent grid: every SM full
     const size_t smem = size_t(B + 1) * 4;
     if (!grid) {
@@ -296,24 +312,29 @@ cudaError_t launch_score(float *scores, const uint16_t *q, const uint16_t *kmin,
         cudaError_t e;
         if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
         if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, quest_score_kernel<D>, kScoreThreads,
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, quest_score_kernel<D, F8>, kScoreThreads,
                                                           size_t(kMaxBatch + 1) * 4);
         if (e != cudaSuccess) return e;
         grid = sms * (per_sm < 1 ? 1 : per_sm);
     }
-    return launch_pdl(quest_score_kernel<D>, dim3(grid), dim3(kScoreThreads), smem, stream, scores, q,
+    return launch_pdl(quest_score_kernel<D, F8>, dim3(grid), dim3(kScoreThreads), smem, stream, scores, q,
                       kmin, kmax, bt, MBS, ctx, B, Hq, Hkv, BS, NB);
 }
 
 }  // namespace
 
-cudaError_t launch_quest_select(int32_t *sel, float *scores, const uint16_t *q,
-                                const uint16_t *kmin, const uint16_t *kmax, const int32_t *bt,
-                                int MBS, const int32_t *ctx, int B, int Hq, int Hkv, int D, int BS,
-                                int64_t NB, int topk, cudaStream_t stream) {
-    cudaError_t e = D == 128
-        ? launch_score<128>(scores, q, kmin, kmax, bt, MBS, ctx, B, Hq, Hkv, BS, NB, stream)
-        : launch_score<64>(scores, q, kmin, kmax, bt, MBS, ctx, B, Hq, Hkv, BS, NB, stream);
+cudaError_t launch_quest_select(int32_t *sel, float *scores, const uint16_t *q, const void *kmin,
+                                const void *kmax, const int32_t *bt, int MBS, const int32_t *ctx,
+                                int B, int Hq, int Hkv, int D, int BS, int64_t NB, int topk,
+                                cudaStream_t stream, bool fp8) {
+    cudaError_t e;
+    if (fp8) {
+        if (D != 128) return cudaErrorInvalidValue;
+        e = launch_score<128, true>(scores, q, kmin, kmax, bt, MBS, ctx, B, Hq, Hkv, BS, NB, stream);
+    } else {
+        e = D == 128 ? launch_score<128, false>(scores, q, kmin, kmax, bt, MBS, ctx, B, Hq, Hkv, BS, NB, stream)
+                     : launch_score<64, false>(scores, q, kmin, kmax, bt, MBS, ctx, B, Hq, Hkv, BS, NB, stream);
+    }
     if (e != cudaSuccess) return e;
     return launch_pdl(quest_topk_kernel, dim3(unsigned(B) * unsigned(Hkv)), dim3(kTopkThreads), 0, stream,
                       sel, static_cast<const float *>(scores), MBS, ctx, Hkv, BS, topk);

@@ -56,7 +56,7 @@ class StepBytes:
 
 def step_bytes(context_lens: np.ndarray, slot_mapping: np.ndarray, Hq: int, Hkv: int, D: int,
                BS: int, topk: int, selected: Optional[np.ndarray] = None,
-               elem_bytes: int = BF16) -> StepBytes:
+               elem_bytes: int = BF16, io_elem_bytes: int = BF16) -> StepBytes:
     """Algorithmic bytes of one step's five calls.
 
     reshape: new K and V rows read and written, plus the slots;
@@ -67,18 +67,23 @@ def step_bytes(context_lens: np.ndarray, slot_mapping: np.ndarray, Hq: int, Hkv:
              ctx, the selection written;
     sparse:  K and V of the valid tokens of the selected blocks, q, out, the
              selection and the block-table entries it dereferences, ctx.
+
+    elem_bytes is the size of one cache / metadata element (2 for bf16, 1
+    for an 8-bit cache); io_elem_bytes that of q, out and the new K/V rows
+    (bf16 in both cases).
     """
     ctx = np.clip(np.asarray(context_lens, dtype=np.int64), 0, None)
     slots = np.asarray(slot_mapping, dtype=np.int64)
     B = ctx.shape[0]
-    row = Hkv * D * elem_bytes
+    row = Hkv * D * elem_bytes          # one token's K (or V) row in the cache
+    row_io = Hkv * D * io_elem_bytes    # one new token's K (or V) row as passed in
     nb = (ctx + BS - 1) // BS
     valid = slots[slots >= 0]
     t_valid = int(valid.shape[0])
     touched = int(np.unique(valid // BS).shape[0])
-    q_bytes = B * Hq * D * elem_bytes
-    reshape = 2 * 2 * t_valid * row + 8 * slots.shape[0]
-    meta = t_valid * row + touched * row * 2 * 2 + 8 * slots.shape[0]
+    q_bytes = B * Hq * D * io_elem_bytes
+    reshape = 2 * t_valid * (row_io + row) + 8 * slots.shape[0]
+    meta = t_valid * row_io + touched * row * 2 * 2 + 8 * slots.shape[0]
     dense = int(ctx.sum()) * 2 * row + 2 * q_bytes + int(nb.sum()) * 4 + 4 * B
     select = int(nb.sum()) * 2 * row + q_bytes + int(nb.sum()) * 4 + 4 * B + B * Hkv * topk * 4
     if selected is None:

@@ -110,3 +110,28 @@ def test_product_package_does_not_touch_the_oracle():
                 src = open(os.path.join(dirpath, f)).read()
                 assert not re.search(r"^\s*(import|from)\s+oracle", src, flags=re.M), f
                 assert "liboracle" not in src, f
+
+
+def test_fp8_entry_points_check_arguments_on_host(lib):
+    """The 8-bit cache entry points take head_dim 128 only and need both
+    scale arrays; both are rejected before anything is launched."""
+    fake = ctypes.c_void_p(1 << 20)
+    dec = lambda D, ks: lib.pa_decode_fp8(fake, fake, fake, fake, ks, fake, fake, 4, fake, 2, 28, 4, D,
+                                          16, 64, 0.088, fake, 1 << 30, None)
+    assert dec(64, fake) == -2
+    assert dec(128, None) == -1
+    assert lib.quest_sparse_decode_fp8(fake, fake, fake, fake, fake, fake, fake, 4, fake, None, 4, 2,
+                                       28, 4, 128, 16, 64, 0.088, fake, 1 << 30, None) == -1
+    assert lib.pa_reshape_and_cache_fp8(fake, fake, fake, fake, fake, 3, fake, fake, 4, 64, 16, 10,
+                                        None) == -2
+    assert lib.pa_reshape_and_cache_fp8(fake, fake, fake, fake, fake, 3, None, fake, 4, 128, 16, 10,
+                                        None) == -1
+    assert lib.pa_reshape_and_cache_fp8(None, None, None, None, None, 0, None, None, 4, 128, 16, 10,
+                                        None) == 0
+    assert lib.quest_reshape_and_cache_fp8(fake, fake, fake, fake, None, fake, fake, 3, fake, fake, 4,
+                                           128, 16, 10, None) == -1
+    need = pg.quest_select_workspace_size(2, 4, 8)
+    assert lib.quest_select_topk_fp8(fake, fake, fake, fake, fake, 8, fake, 2, 28, 4, 64, 16, 64, 4,
+                                     fake, need, None) == -2
+    assert lib.quest_select_topk_fp8(fake, fake, fake, fake, fake, 8, fake, 2, 28, 4, 128, 16, 64, 4,
+                                     fake, need - 1, None) == -3

@@ -34,6 +34,16 @@ def torch_encode_sat(x) -> np.ndarray:
 
 
 ALL_CODES = np.arange(256, dtype=np.uint8)
+
+# token order inside a 16-byte row of the 8-bit V layout (the format's definition)
+V_ORDER = np.array([0, 1, 8, 9, 2, 3, 10, 11, 4, 5, 12, 13, 6, 7, 14, 15])
+
+
+def v_token_major(vc):
+    """[NB, Hkv, D, 16] V codes (rows in V_ORDER) as [NB, 16, Hkv, D]."""
+    nat = np.empty_like(vc)
+    nat[..., V_ORDER] = vc
+    return np.ascontiguousarray(nat.transpose(0, 3, 1, 2))
 FINITE = np.array([c for c in range(256) if (c & 0x7F) != 0x7F], dtype=np.uint8)
 
 
@@ -105,17 +115,18 @@ def test_fp8_write_quantises_each_element(oracle_lib):
     """Written rows are the library cast of fl32(x / scale[h]); negative
     slots are skipped and untouched rows keep their bytes."""
     rng = np.random.default_rng(3)
-    NB, BS, Hkv, D, T = 5, 4, 3, 16, 9
+    NB, BS, Hkv, D, T = 5, 16, 3, 16, 9
     kc = rng.integers(0, 256, (NB, BS, Hkv, D), dtype=np.uint8)
-    vc = rng.integers(0, 256, (NB, BS, Hkv, D), dtype=np.uint8)
+    vc = rng.integers(0, 256, (NB, Hkv, D, BS), dtype=np.uint8)
     kc0, vc0 = kc.copy(), vc.copy()
     key = bf16(rng.standard_normal((T, Hkv, D)) * 3)
     value = bf16(rng.standard_normal((T, Hkv, D)) * 3)
     ks = np.array([0.011, 0.0137, 0.02], dtype=np.float32)
     vs = np.array([0.009, 0.031, 0.0077], dtype=np.float32)
-    slots = np.array([0, 5, -1, 19, 7, -3, 10, 13, 2], dtype=np.int64)
+    slots = np.array([0, 21, -1, 79, 7, -3, 40, 53, 18], dtype=np.int64)
     assert oracle_lib.reshape_and_cache_fp8(key, value, kc, vc, slots, ks, vs) == 0
     written = np.zeros((NB * BS,), dtype=bool)
+    vnat, vnat0 = v_token_major(vc).reshape(NB * BS, -1), v_token_major(vc0).reshape(NB * BS, -1)
     for t, s in enumerate(slots):
         if s < 0:
             continue
@@ -123,9 +134,9 @@ def test_fp8_write_quantises_each_element(oracle_lib):
         kq = torch_encode_sat(bf16_bits_to_f32(key[t]) / ks[:, None])
         vq = torch_encode_sat(bf16_bits_to_f32(value[t]) / vs[:, None])
         np.testing.assert_array_equal(kc.reshape(NB * BS, Hkv, D)[s], kq)
-        np.testing.assert_array_equal(vc.reshape(NB * BS, Hkv, D)[s], vq)
+        np.testing.assert_array_equal(vnat[s].reshape(Hkv, D), vq)
     np.testing.assert_array_equal(kc.reshape(NB * BS, -1)[~written], kc0.reshape(NB * BS, -1)[~written])
-    np.testing.assert_array_equal(vc.reshape(NB * BS, -1)[~written], vc0.reshape(NB * BS, -1)[~written])
+    np.testing.assert_array_equal(vnat[~written], vnat0[~written])
 
 
 # --------------------------------------------------------------- metadata
@@ -157,13 +168,13 @@ def test_fp8_incremental_meta_equals_rebuild(oracle_lib):
     """One new token per sequence per step, quantised into the cache and
     folded into the metadata: the running metadata equals the rebuild."""
     rng = np.random.default_rng(5)
-    B, Hkv, D, BS, steps = 3, 2, 16, 4, 11
-    ctx = np.array([1, 4, 6])
+    B, Hkv, D, BS, steps = 3, 2, 16, 16, 11
+    ctx = np.array([1, 13, 30])
     MBS = (int(ctx.max()) + steps + BS - 1) // BS
     NB = B * MBS
     bt = rng.permutation(NB).astype(np.int32).reshape(B, MBS)
     kc = _random_fp8_cache(rng, NB, BS, Hkv, D)
-    vc = kc.copy()
+    vc = np.ascontiguousarray(kc.transpose(0, 2, 3, 1))
     ks = np.array([0.013, 0.021], dtype=np.float32)
     kmin, kmax = oracle_lib.quest_rebuild_meta_fp8(kc, bt, ctx.astype(np.int32))
     for _ in range(steps):
@@ -181,12 +192,12 @@ def test_fp8_incremental_meta_equals_rebuild(oracle_lib):
 # -------------------------------------------------------------- attention
 
 
-def _case(rng, B=3, Hq=6, Hkv=2, D=32, BS=4, MBS=4):
+def _case(rng, B=3, Hq=6, Hkv=2, D=32, BS=16, MBS=3):
     NB = B * MBS + 2
-    ctx = np.array([MBS * BS, 7, 1][:B], dtype=np.int32)
+    ctx = np.array([MBS * BS, 21, 1][:B], dtype=np.int32)
     bt = rng.permutation(NB)[: B * MBS].astype(np.int32).reshape(B, MBS)
     kc = _random_fp8_cache(rng, NB, BS, Hkv, D)
-    vc = _random_fp8_cache(rng, NB, BS, Hkv, D)
+    vc = np.ascontiguousarray(_random_fp8_cache(rng, NB, BS, Hkv, D).transpose(0, 2, 3, 1))
     q = bf16(rng.standard_normal((B, Hq, D)))
     return q, kc, vc, bt, ctx
 
@@ -200,13 +211,13 @@ def test_fp8_attention_equals_bf16_attention_on_exact_values(oracle_lib):
     ks = np.array([2.0 ** -5, 2.0 ** -3], dtype=np.float32)
     vs = np.array([2.0 ** -4, 2.0 ** 1], dtype=np.float32)
     kb = bf16(torch_decode(kc) * ks[None, None, :, None])
-    vb = bf16(torch_decode(vc) * vs[None, None, :, None])
+    vb = bf16(torch_decode(v_token_major(vc)) * vs[None, None, :, None])
     np.testing.assert_array_equal(bf16_bits_to_f32(kb), torch_decode(kc) * ks[None, None, :, None])
     scale = 1 / math.sqrt(32)
     a = oracle_lib.attention_fp8(q, kc, vc, ks, vs, bt, ctx, scale)
     b = oracle_lib.paged_attention(q, kb, vb, bt, ctx, scale)
     np.testing.assert_array_equal(a, b)
-    sel = np.array([[[2, 0], [1, -1]], [[0, 1], [1, 3]], [[0, -1], [-1, -1]]], dtype=np.int32)
+    sel = np.array([[[2, 0], [1, -1]], [[0, 1], [1, 2]], [[0, -1], [-1, -1]]], dtype=np.int32)
     a = oracle_lib.attention_fp8(q, kc, vc, ks, vs, bt, ctx, scale, selected=sel)
     b = oracle_lib.sparse_attention(q, kb, vb, bt, ctx, sel, scale)
     np.testing.assert_array_equal(a, b)
@@ -223,7 +234,7 @@ def test_fp8_attention_brute_force_any_scale(oracle_lib):
     got = oracle_lib.attention_fp8(q, kc, vc, ks, vs, bt, ctx, scale)
     B, Hq, D = q.shape
     BS, Hkv, G = kc.shape[1], kc.shape[2], Hq // kc.shape[2]
-    kd, vd = torch_decode(kc), torch_decode(vc)
+    kd, vd = torch_decode(kc), torch_decode(v_token_major(vc))
     for b in range(B):
         for h in range(Hq):
             kvh = h // G
