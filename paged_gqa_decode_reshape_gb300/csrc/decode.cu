@@ -264,10 +264,13 @@ __global__ void __launch_bounds__(DecodeCfg<D, F8>::THREADS, 1)
         int issued = 0;  // items [0, issued) have been armed
         int fail_step = 0;
         unsigned fail_armed = 0;  // after a failure: leader lanes whose item was armed
-        // 8 items per step: lane = 4 * item + part, part = which tile copy
-        const int it = lane >> 2, part = lane & 3;
+        // IPS items per step, LPI lanes per item: lane = LPI * item + part,
+        // part = which tile copy (bf16: K and V in two 64-dim halves each;
+        // E4M3: one K and one V copy, so twice the items per step)
+        constexpr int LPI = F8 ? 2 : 4, IPS = 32 / LPI;
+        const int it = lane / LPI, part = lane % LPI;
         constexpr int PARTS = F8 ? 2 : 2 * (D / 64);  // K and V (bf16: 64-dim halves)
-        for (int k0 = 0; k0 < n_items; k0 += 8) {
+        for (int k0 = 0; k0 < n_items; k0 += IPS) {
             if (k0 >= wbase + 32) {
                 wa = wb;
                 wb = wc;
@@ -298,7 +301,7 @@ __global__ void __launch_bounds__(DecodeCfg<D, F8>::THREADS, 1)
                     else mbar_arrive(fb);
                 }
             }
-            ok = __shfl_sync(0xffffffffu, ok, lane & ~3);
+            ok = __shfl_sync(0xffffffffu, ok, lane - part);
             __syncwarp();
             if (live && ok && nv > 0 && part < PARTS) {
                 if constexpr (F8) {
@@ -330,15 +333,15 @@ __global__ void __launch_bounds__(DecodeCfg<D, F8>::THREADS, 1)
                 fail_armed = __ballot_sync(0xffffffffu, live && part == 0 && ok);
                 break;
             }
-            issued = min(n_items, k0 + 8);
+            issued = min(n_items, k0 + IPS);
         }
         // keep the CTA alive until every copy issued has landed (consumers that
         // gave up do not wait for them)
         if (lane == 0) {
             for (int k = max(0, issued - S); k < issued; ++k)
                 mbar_wait_bounded(full_bar + (k % S) * 8, (k / S) & 1, kWaitLimitNs);
-            for (int i = 0; i < 8; ++i)
-                if (fail_armed & (1u << (4 * i))) {
+            for (int i = 0; i < IPS; ++i)
+                if (fail_armed & (1u << (LPI * i))) {
                     const int k = fail_step + i;
                     mbar_wait_bounded(full_bar + (k % S) * 8, (k / S) & 1, kWaitLimitNs);
                 }
