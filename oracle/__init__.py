@@ -88,6 +88,9 @@ def lib():
             L.oracle_attention_fp8.restype = i32
             L.oracle_quest_scores_fp8.argtypes = [vp, vp, vp, vp, vp, i32, vp, i32, i32, i32, i32, i32, i64]
             L.oracle_quest_scores_fp8.restype = i32
+            L.oracle_paged_attention_multi.argtypes = [vp, vp, vp, vp, vp, i32, vp, vp, i32, i32, i32,
+                                                       i32, i32, i32, i64, f64, vp, i64]
+            L.oracle_paged_attention_multi.restype = i32
             _lib = L
     return _lib
 
@@ -381,3 +384,30 @@ def quest_select_fp8(q, kmin, kmax, block_tables, context_lens, BS: int, topk: i
     """Scores on E4M3 metadata then top-K."""
     return quest_topk(quest_scores_fp8(q, kmin, kmax, block_tables, context_lens, BS),
                       context_lens, BS, topk)
+
+
+# ------------------------------------------------------ multi-token rows
+
+
+def paged_attention_multi(q, key_cache, value_cache, block_tables, cu_seqlens_q, context_lens, scale,
+                          rows=None):
+    """Dense attention of multi-token query rows with right-aligned causal masks.
+
+    q: [total_q, Hq, D] bf16 bits; cu_seqlens_q: [B+1]. Returns [total_q, Hq, D]
+    float64 (or [len(rows), D] for the listed (row, head) pairs)."""
+    q = _c(q, np.uint16)
+    kc = _c(key_cache, np.uint16)
+    vc = _c(value_cache, np.uint16)
+    bt = _c(block_tables, np.int32)
+    cu = _c(cu_seqlens_q, np.int32)
+    ctx = _c(context_lens, np.int32)
+    total_q, Hq, D = q.shape
+    NB, BS, Hkv, D2 = kc.shape
+    B = ctx.shape[0]
+    assert D == D2 and vc.shape == kc.shape and bt.shape[0] == B and cu.shape == (B + 1,)
+    r, nr = _rows_arg(rows)
+    out = np.zeros((nr, D) if r is not None else (total_q, Hq, D), dtype=np.float64)
+    rc = lib().oracle_paged_attention_multi(_p(out), _p(q), _p(kc), _p(vc), _p(bt), bt.shape[1], _p(cu),
+                                            _p(ctx), B, total_q, Hq, Hkv, D, BS, NB, float(scale), _p(r), nr)
+    _check(rc, "paged_attention_multi")
+    return out

@@ -783,6 +783,63 @@ int oracle_attention_fp8(double *out, const uint16_t *q,
                           nrows, 0, 0);
 }
 
+/* Multi-token query rows (chunked prefill or speculative tokens mixed into a
+ * decode batch): sequence b owns query rows cu_seqlens_q[b] ..
+ * cu_seqlens_q[b+1]-1, the newest q_len_b = cu[b+1] - cu[b] tokens of the
+ * sequence, at positions ctx_b - q_len_b .. ctx_b - 1 (context_lens includes
+ * them; the causal mask is right-aligned). Row i of sequence b attends to
+ * positions t < ctx_b - q_len_b + i + 1, i.e. to itself and everything
+ * before it; a row whose limit is <= 0 gets a zero output. q and out are
+ * [total_q][Hq][D]; the attention per row is the two-pass softmax above.
+ * rows (if not NULL) lists (row, head) pairs to compute; out is then
+ * [nrows][D]. Returns 0, -1 on a table entry outside the pool, -2 on bad
+ * sizes or a malformed cu_seqlens_q. */
+int oracle_paged_attention_multi(double *out, const uint16_t *q,
+                                 const uint16_t *key_cache, const uint16_t *value_cache,
+                                 const int32_t *block_tables, int MBS,
+                                 const int32_t *cu_seqlens_q, const int32_t *context_lens,
+                                 int B, int total_q, int Hq, int Hkv, int D, int BS, int64_t NB,
+                                 double scale, const int32_t *rows, int64_t nrows)
+{
+    if (B <= 0 || total_q < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || D <= 0 || BS <= 0)
+        return -2;
+    if (cu_seqlens_q[0] != 0 || cu_seqlens_q[B] != total_q)
+        return -2;
+    for (int b = 0; b < B; ++b)
+        if (cu_seqlens_q[b + 1] < cu_seqlens_q[b])
+            return -2;
+    const int G = Hq / Hkv;
+    const kvsrc K = {key_cache, NULL, NULL, 0, 0, 0, 0}, V = {value_cache, NULL, NULL, 0, 0, 0, 0};
+    const int64_t max_tokens = (int64_t)MBS * BS;
+    int64_t *pos = (int64_t *)malloc(sizeof(int64_t) * (size_t)(max_tokens + 1));
+    double *s = (double *)malloc(sizeof(double) * (size_t)(max_tokens + 1));
+    int rc = 0;
+    const int64_t total = rows ? nrows : (int64_t)total_q * Hq;
+    for (int64_t r = 0; r < total && rc == 0; ++r) {
+        const int64_t row = rows ? rows[2 * r] : r / Hq;
+        const int64_t h = rows ? rows[2 * r + 1] : r % Hq;
+        int b = 0;
+        while (cu_seqlens_q[b + 1] <= row)
+            ++b;
+        int64_t ctx = context_lens[b];
+        if (ctx > max_tokens)
+            ctx = max_tokens;
+        if (ctx < 0)
+            ctx = 0;
+        const int64_t q_len = cu_seqlens_q[b + 1] - cu_seqlens_q[b];
+        int64_t lim = ctx - q_len + (row - cu_seqlens_q[b]) + 1;
+        if (lim < 0)
+            lim = 0;
+        const int64_t n = token_list(pos, lim, BS, NULL, 0);
+        rc = attend_two_pass(out + r * (int64_t)D, q + (row * Hq + h) * (int64_t)D, &K, &V,
+                             block_tables + (int64_t)b * MBS, pos, n, (int)(h / G), Hkv, D, BS, NB,
+                             scale, s);
+    }
+    free(pos);
+    free(s);
+    return rc;
+}
+
 /* ------------------------------------------------------------ Quest score */
 
 /* Quest block score, evaluated in fp32 in one fixed order that the GPU
