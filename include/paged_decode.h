@@ -233,6 +233,29 @@ PA_API int pa_check_metadata(int32_t *counts, const int64_t *slot_mapping, int64
                       const int32_t *context_lens, int batch, int block_size,
                       int64_t num_blocks, void *stream);
 
+/* Multi-token query rows ([P2] 2.7 "continuous batching and varlen": a
+ * chunked-prefill chunk or speculative tokens mixed into a decode batch;
+ * [P2] 3.3: flat query rows with cu_seqlens_q, causal mask aligned on the
+ * right). Sequence b owns query rows cu_seqlens_q[b] .. cu_seqlens_q[b+1]-1
+ * of query / out [total_q][Hq][D]: its q_len = cu[b+1] - cu[b] newest tokens,
+ * at positions context_lens[b] - q_len .. context_lens[b] - 1 (context_lens
+ * includes them, and ReshapeAndCache has written their K/V). Row i of
+ * sequence b attends, as pa_decode, to the positions
+ *     t < context_lens[b] - q_len + i + 1
+ * (itself and everything before it); a row whose limit is <= 0 gets a zero
+ * output. cu_seqlens_q is [batch + 1] int32 on the device, 0 = cu[0] <= ... <=
+ * cu[batch] = total_q (not checked on the host; a malformed array gives
+ * undefined rows, never a fault). block_tables and context_lens are per
+ * sequence. Workspace: pa_decode_workspace_size(total_q, ...), same zero-fill
+ * rule. Supported: batch, total_q <= 2048; other limits as pa_decode. */
+PA_API int pa_decode_multi(pa_bf16 *out, const pa_bf16 *query,
+                    const pa_bf16 *key_cache, const pa_bf16 *value_cache,
+                    const int32_t *block_tables, int max_blocks_per_seq,
+                    const int32_t *cu_seqlens_q, const int32_t *context_lens,
+                    int batch, int total_q, int num_q_heads, int num_kv_heads,
+                    int head_dim, int block_size, int64_t num_blocks, float scale,
+                    void *workspace, size_t workspace_bytes, void *stream);
+
 /* ---------------------------------------------------- 8-bit KV cache ----
  * The same path over a KV cache stored in 8 bits per element, which halves
  * the bytes decode attention reads ([P2] 2.5 and 3.1: long-context serving is

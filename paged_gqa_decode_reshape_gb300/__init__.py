@@ -88,6 +88,9 @@ def load_library(path: Optional[str] = None):
         L.pa_workspace_status.restype = i32
         L.pa_check_metadata.argtypes = [vp, vp, i64, vp, i32, vp, i32, i32, i64, vp]
         L.pa_check_metadata.restype = i32
+        L.pa_decode_multi.argtypes = [vp, vp, vp, vp, vp, i32, vp, vp, i32, i32, i32, i32, i32, i32,
+                                      i64, f32, vp, sz, vp]
+        L.pa_decode_multi.restype = i32
         L.pa_reshape_and_cache_fp8.argtypes = [vp, vp, vp, vp, vp, i64, vp, vp, i32, i32, i32, i64, vp]
         L.pa_reshape_and_cache_fp8.restype = i32
         L.quest_update_meta_fp8.argtypes = [vp, vp, vp, vp, i64, vp, i32, i32, i32, i64, vp]
@@ -559,4 +562,39 @@ def quest_sparse_decode_fp8(out: torch.Tensor, query: torch.Tensor, key_cache: t
                                      _ptr(context_lens), _ptr(selected), topk, B, Hq, Hkv, D, BS, NB,
                                      float(scale), _ptr(ws), ws.numel() * ws.element_size(),
                                      _stream(dev)))
+    return out
+
+
+# ------------------------------------------------------ multi-token rows
+
+
+def pa_decode_multi(out: torch.Tensor, query: torch.Tensor, key_cache: torch.Tensor,
+                    value_cache: torch.Tensor, block_tables: torch.Tensor, cu_seqlens_q: torch.Tensor,
+                    context_lens: torch.Tensor, scale: float,
+                    workspace: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """Decode attention of multi-token query rows [total_q, Hq, D] with right-aligned
+    causal masks; cu_seqlens_q [B+1] int32 gives each sequence's rows."""
+    L = load_library()
+    _need(key_cache, "key_cache", torch.bfloat16, 4)
+    dev = key_cache.device
+    _need(value_cache, "value_cache", torch.bfloat16, 4, dev)
+    _need(query, "query", torch.bfloat16, 3, dev)
+    _need(out, "out", torch.bfloat16, 3, dev)
+    _need(block_tables, "block_tables", torch.int32, 2, dev)
+    _need(cu_seqlens_q, "cu_seqlens_q", torch.int32, 1, dev)
+    _need(context_lens, "context_lens", torch.int32, 1, dev)
+    total_q, Hq, D = query.shape
+    NB, BS, Hkv, D2 = key_cache.shape
+    B = context_lens.shape[0]
+    if D != D2 or value_cache.shape != key_cache.shape or out.shape != query.shape:
+        raise ValueError("shape mismatch between query/out and the caches")
+    if block_tables.shape[0] != B or cu_seqlens_q.shape[0] != B + 1:
+        raise ValueError("block_tables / cu_seqlens_q / context_lens batch mismatch")
+    need = pa_decode_workspace_size(max(total_q, 1), Hq, Hkv, D)
+    ws = workspace if workspace is not None else _default_ws.get(dev, need)
+    _check("pa_decode_multi",
+           L.pa_decode_multi(_ptr(out), _ptr(query), _ptr(key_cache), _ptr(value_cache),
+                             _ptr(block_tables), block_tables.shape[1], _ptr(cu_seqlens_q),
+                             _ptr(context_lens), B, total_q, Hq, Hkv, D, BS, NB, float(scale), _ptr(ws),
+                             ws.numel() * ws.element_size(), _stream(dev)))
     return out

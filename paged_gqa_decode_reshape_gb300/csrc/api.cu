@@ -108,7 +108,8 @@ int run_decode(pa_bf16 *out, const pa_bf16 *query, const void *key_cache, const 
                const int32_t *block_tables, int MBS, const int32_t *context_lens,
                const int32_t *selected, int topk, int B, int Hq, int Hkv, int D, int BS, int64_t NB,
                float scale, void *workspace, size_t workspace_bytes, void *stream, bool sparse,
-               const float *k_scale = nullptr, const float *v_scale = nullptr, bool fp8 = false) {
+               const float *k_scale = nullptr, const float *v_scale = nullptr, bool fp8 = false,
+               const int32_t *cu_q = nullptr, int nseq = 0) {
     int rc = check_attention_args(out, query, key_cache, value_cache, block_tables, MBS,
                                   context_lens, B, Hq, Hkv, D, BS, NB, scale, workspace);
     if (rc != PA_OK) return rc;
@@ -133,6 +134,8 @@ int run_decode(pa_bf16 *out, const pa_bf16 *query, const void *key_cache, const 
     a.k_scale = k_scale;
     a.v_scale = v_scale;
     a.v8 = fp8 ? static_cast<const uint8_t *>(value_cache) : nullptr;
+    a.cu_q = cu_q;
+    a.nseq = cu_q ? nseq : B;
     a.out = out;
     a.part = w.part;
     a.counters = w.counters;
@@ -460,6 +463,24 @@ int quest_sparse_decode_fp8(pa_bf16 *out, const pa_bf16 *query, const pa_e4m3 *k
                       context_lens, selected, topk, batch, num_q_heads, num_kv_heads, head_dim,
                       block_size, num_blocks, scale, workspace, workspace_bytes, stream, true, k_scale,
                       v_scale, true);
+}
+
+}  // extern "C"
+
+extern "C" {
+
+int pa_decode_multi(pa_bf16 *out, const pa_bf16 *query, const pa_bf16 *key_cache,
+                    const pa_bf16 *value_cache, const int32_t *block_tables, int max_blocks_per_seq,
+                    const int32_t *cu_seqlens_q, const int32_t *context_lens, int batch, int total_q,
+                    int num_q_heads, int num_kv_heads, int head_dim, int block_size, int64_t num_blocks,
+                    float scale, void *workspace, size_t workspace_bytes, void *stream) {
+    if (batch <= 0 || total_q < 0 || !cu_seqlens_q) return PA_ERR_INVALID_ARG;
+    if (batch > kMaxMultiRows || total_q > kMaxMultiRows) return PA_ERR_UNSUPPORTED;
+    if (total_q == 0) return PA_OK;
+    return run_decode(out, query, key_cache, value_cache, block_tables, max_blocks_per_seq, context_lens,
+                      nullptr, 0, total_q, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks,
+                      scale, workspace, workspace_bytes, stream, false, nullptr, nullptr, false,
+                      cu_seqlens_q, batch);
 }
 
 }  // extern "C"

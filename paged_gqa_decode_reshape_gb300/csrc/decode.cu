@@ -110,7 +110,11 @@ struct DecodeCfg {
     static constexpr size_t off_scr = off_info + size_t(S) * 8;
     static constexpr size_t off_flags = off_scr + size_t(NC) * SCR * 4;
     static constexpr size_t off_pre = off_flags + 64;
-    static constexpr size_t smem_bytes(int B) { return 1024 + off_pre + size_t(B + 1) * 4; }
+    // per-row item prefix, then (multi-token rows) each row's sequence
+    static constexpr size_t seq_off(int B) { return off_pre + (size_t(B + 1) * 4 + 15) / 16 * 16; }
+    static constexpr size_t smem_bytes(int B, bool multi = false) {
+        return 1024 + seq_off(B) + (multi ? (size_t(B) * 2 + 15) / 16 * 16 : 0);
+    }
 };
 
 template <int D, bool SPARSE, bool F8>
@@ -130,6 +134,7 @@ __global__ void __launch_bounds__(DecodeCfg<D, F8>::THREADS, 1)
     float *scr = reinterpret_cast<float *>(bp + C::off_scr);
     volatile int *flags = reinterpret_cast<volatile int *>(bp + C::off_flags);
     int32_t *pre = reinterpret_cast<int32_t *>(bp + C::off_pre);
+    uint16_t *seq_of = reinterpret_cast<uint16_t *>(bp + C::seq_off(a.B));  // multi-token rows only
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int B = a.B, Hkv = a.Hkv, G = a.G;
@@ -147,8 +152,9 @@ __global__ void __launch_bounds__(DecodeCfg<D, F8>::THREADS, 1)
         // context lengths, block table and selection into L2 (hints only).
         const int64_t nthr = int64_t(gridDim.x) * C::THREADS;
         const int64_t gt = int64_t(blockIdx.x) * C::THREADS + tid;
-        for (int64_t off = gt * 32; off < int64_t(B); off += nthr * 32) prefetch_l2(a.ctx + off);
-        const int64_t bt_n = int64_t(B) * a.MBS;
+        const int nseq = a.cu_q ? a.nseq : B;  // ctx and block tables are per sequence
+        for (int64_t off = gt * 32; off < int64_t(nseq); off += nthr * 32) prefetch_l2(a.ctx + off);
+        const int64_t bt_n = int64_t(nseq) * a.MBS;
         for (int64_t off = gt * 32; off < bt_n; off += nthr * 32) prefetch_l2(a.bt + off);
         if (SPARSE) {
             const int64_t sel_n = int64_t(B) * Hkv * a.topk;
@@ -156,8 +162,28 @@ __global__ void __launch_bounds__(DecodeCfg<D, F8>::THREADS, 1)
         }
     }
     pdl_wait();  // inputs may come from the previous kernel in the stream
+    // Multi-token rows ("18 e2e inference serving", sections 2.7 and 3.3):
+    // row r belongs to the sequence s with cu_q[s] <= r < cu_q[s+1] and sees
+    // the positions before ctx_s - q_len_s + (r - cu_q[s]) + 1 (causal mask
+    // aligned on the right).
+    auto row_ctx = [&](int r, int s) -> int {
+        const int c0 = min(max(__ldg(a.ctx + s), 0), max_tok);
+        const int c1 = __ldg(a.cu_q + s), ql = __ldg(a.cu_q + s + 1) - c1;
+        return min(max(c0 - ql + (r - c1) + 1, 0), c0);
+    };
     for (int b = tid; b < B; b += C::THREADS) {
-        const int c = min(max(__ldg(a.ctx + b), 0), max_tok);
+        int c;
+        if (a.cu_q) {
+            int lo = 0, hi = a.nseq;  // the last sequence whose first row is <= b
+            while (hi - lo > 1) {
+                const int mid = (lo + hi) >> 1;
+                if (__ldg(a.cu_q + mid) <= b) lo = mid; else hi = mid;
+            }
+            seq_of[b] = uint16_t(lo);
+            c = row_ctx(b, lo);
+        } else {
+            c = min(max(__ldg(a.ctx + b), 0), max_tok);
+        }
         const int nblk = (c + BS - 1) / BS;
         pre[b + 1] = SPARSE ? (nblk > 0 ? a.topk : 0) : nblk;
     }
@@ -246,14 +272,15 @@ __global__ void __launch_bounds__(DecodeCfg<D, F8>::THREADS, 1)
             const int kvh = int(r / n);
             const int i = int(r - int64_t(kvh) * n);
             it.seg = b * Hkv + kvh;
-            it.ctxv = __ldg(a.ctx + b);
+            it.ctxv = a.cu_q ? row_ctx(b, seq_of[b]) : __ldg(a.ctx + b);
             it.j = SPARSE ? __ldg(a.sel + (int64_t(b) * Hkv + kvh) * a.topk + i) : i;
             return it;
         };
         auto stage_b = [&](Win &it) {
             if (it.seg < 0) return;
             const int b = it.seg / Hkv;
-            it.phys = (it.j >= 0 && it.j < a.MBS) ? __ldg(a.bt + int64_t(b) * a.MBS + it.j) : -1;
+            const int s = a.cu_q ? int(seq_of[b]) : b;  // the row's sequence
+            it.phys = (it.j >= 0 && it.j < a.MBS) ? __ldg(a.bt + int64_t(s) * a.MBS + it.j) : -1;
         };
         const uint64_t policy = l2_policy_evict_first();
         Win wa = stage_c(0), wb = stage_c(32);
@@ -891,9 +918,10 @@ cudaError_t launch_t(const CUtensorMap &tm_k, const CUtensorMap &tm_v, const Dec
     DecodeGeometry geo;
     cudaError_t e = decode_geometry(D, &geo, F8);
     if (e != cudaSuccess) return e;
-    if (C::smem_bytes(a.B) > geo.smem) return cudaErrorInvalidConfiguration;  // batch too large
-    return launch_pdl(decode_kernel<D, SPARSE, F8>, dim3(geo.grid), dim3(C::THREADS),
-                      C::smem_bytes(a.B), stream, tm_k, tm_v, a);
+    const size_t smem = C::smem_bytes(a.B, a.cu_q != nullptr);
+    if (smem > geo.smem) return cudaErrorInvalidConfiguration;  // batch too large
+    return launch_pdl(decode_kernel<D, SPARSE, F8>, dim3(geo.grid), dim3(C::THREADS), smem, stream, tm_k,
+                      tm_v, a);
 }
 
 constexpr int kMaxDevices = 64;

@@ -10,6 +10,7 @@ namespace pa {
 constexpr int kBlockSize = 16;       // tokens per KV block
 constexpr int kMaxBatch = 4096;      // sequences per call
 constexpr int kMaxGroup = 8;         // query heads per KV head (one mma n-tile)
+constexpr int kMaxMultiRows = 2048;  // query rows of a multi-token decode call
 
 // Arguments of the split-KV decode kernel (dense and Quest-sparse).
 struct DecodeArgs {
@@ -20,6 +21,9 @@ struct DecodeArgs {
     const float *k_scale;       // [Hkv] per-KV-head scales of an E4M3 cache (else null)
     const float *v_scale;
     const uint8_t *v8;          // E4M3 V cache [NB][Hkv][D][16] (else null): tiles are contiguous
+    const int32_t *cu_q;        // multi-token rows: [nseq + 1] row offsets per sequence (else null;
+                                // B then counts query rows, ctx / bt are per sequence)
+    int nseq;
     uint16_t *out;              // [B][Hq][D] bf16
     float *part;                // [B*Hkv + W][D*8 + 8] partial outputs and lse (log2 domain)
     int32_t *counters;          // [B*Hkv] arrival counters (zero between calls)
