@@ -48,6 +48,9 @@ def parse():
                    choices=["tiny", "dense_b32", "quest_8k", "long_40k", "mixed_b128"])
     p.add_argument("--kv", choices=["bf16", "fp8"], default="bf16",
                    help="KV-cache element type: bf16, or 8-bit E4M3 codes with per-KV-head scales")
+    p.add_argument("--qlen", type=int, default=1,
+                   help="query rows per sequence of the dense call (> 1: pa_decode_multi, right-aligned "
+                        "causal masks, for speculative / chunked-prefill rows)")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-budget", type=float, default=12.0,
                    help="seconds of oracle work for the CPU baseline sample")
@@ -154,11 +157,20 @@ def gpu_id_for(torch, dev) -> str:
 class Step:
     """Device buffers of one workload and the five C-ABI calls of a step."""
 
-    def __init__(self, w, dev, kv: str = "bf16"):
+    def __init__(self, w, dev, kv: str = "bf16", qlen: int = 1):
         import torch
         import paged_gqa_decode_reshape_gb300 as pg
         import workloads
-        self.pg, self.torch, self.w, self.dev, self.kv = pg, torch, w, dev, kv
+        self.pg, self.torch, self.w, self.dev, self.kv, self.qlen = pg, torch, w, dev, kv, qlen
+        if qlen > 1:
+            # qlen query rows per sequence (seeded N(0, 1), bf16) for pa_decode_multi
+            rng = np.random.default_rng(1234)
+            qm = workloads.f32_to_bf16_bits(rng.standard_normal((w.B * qlen, w.Hq, w.D)).astype(np.float32))
+            self.q_multi = torch.from_numpy(qm.view(np.int16)).to(dev).view(torch.bfloat16)
+            self.out_multi = torch.empty_like(self.q_multi)
+            self.cu_q = torch.arange(0, w.B * qlen + 1, qlen, dtype=torch.int32, device=dev)
+            self.ws_multi = torch.zeros(pg.pa_decode_multi_workspace_size(w.B * qlen, w.Hq, w.Hkv, w.D),
+                                        dtype=torch.uint8, device=dev)
 
         def d16(a):
             return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)
@@ -221,11 +233,16 @@ class Step:
                                                    self.k_scale, self.v_scale, self.bt, self.ctx,
                                                    self.sel, w.scale, workspace=self.ws),
             ]
+        if self.qlen > 1:
+            dense = lambda: pg.pa_decode_multi(self.out_multi, self.q_multi, self.kc, self.vc, self.bt,
+                                               self.cu_q, self.ctx, w.scale, workspace=self.ws_multi)
+        else:
+            dense = lambda: pg.pa_decode(self.out, self.q, self.kc, self.vc, self.bt, self.ctx, w.scale,
+                                         workspace=self.ws)
         return [
             lambda: pg.quest_reshape_and_cache(self.key, self.value, self.kc, self.vc, self.kmin,
                                                self.kmax, self.slots),
-            lambda: pg.pa_decode(self.out, self.q, self.kc, self.vc, self.bt, self.ctx, w.scale,
-                                 workspace=self.ws),
+            dense,
             lambda: pg.quest_select_topk(self.sel, self.q, self.kmin, self.kmax, self.bt, self.ctx,
                                          w.BS, workspace=self.sel_ws),
             lambda: pg.quest_sparse_decode(self.out_sparse, self.q, self.kc, self.vc, self.bt,
@@ -240,7 +257,7 @@ LAUNCHES_PER_CALL = [1, 1, 2, 1]
 # -------------------------------------------------------------- CPU oracle
 
 
-def oracle_sample(w, budget_s: float, kv: str = "bf16"):
+def oracle_sample(w, budget_s: float, kv: str = "bf16", qlen: int = 1):
     """The oracle on a bounded sample of the step: the write path for every
     token, then whole sequences (dense attention for all heads, Quest scores
     and top-K for all KV heads, sparse attention for all heads) until the
@@ -262,11 +279,21 @@ def oracle_sample(w, budget_s: float, kv: str = "bf16"):
     nbytes = ledger.step_bytes(w.context_lens, w.slot_mapping, w.Hq, w.Hkv, w.D, w.BS, w.topk)
     done_bytes = nbytes.reshape + nbytes.meta
     seqs = 0
+    if qlen > 1:  # the same query rows the GPU step attends with (Step: seed 1234)
+        import workloads
+        rng = np.random.default_rng(1234)
+        qm = workloads.f32_to_bf16_bits(rng.standard_normal((w.B * qlen, w.Hq, w.D)).astype(np.float32))
+        cu = np.arange(0, w.B * qlen + 1, qlen, dtype=np.int32)
     for b in range(w.B):
         if time.perf_counter() - t0 - t_setup > budget_s and seqs > 0:
             break
         rows = np.array([(b, h) for h in range(w.Hq)], dtype=np.int32)
-        oracle.paged_attention(w.q, kc, vc, w.block_tables, w.context_lens, w.scale, rows=rows)
+        if qlen > 1:
+            mrows = np.array([(r, h) for r in range(b * qlen, (b + 1) * qlen) for h in range(w.Hq)],
+                             dtype=np.int32)
+            oracle.paged_attention_multi(qm, kc, vc, w.block_tables, cu, w.context_lens, w.scale, rows=mrows)
+        else:
+            oracle.paged_attention(w.q, kc, vc, w.block_tables, w.context_lens, w.scale, rows=rows)
         sc = oracle.quest_scores(w.q[b:b + 1], kmin, kmax, w.block_tables[b:b + 1],
                                  w.context_lens[b:b + 1], w.BS)
         sel = oracle.quest_topk(sc, w.context_lens[b:b + 1], w.BS, w.topk)
@@ -275,7 +302,7 @@ def oracle_sample(w, budget_s: float, kv: str = "bf16"):
         oracle.sparse_attention(w.q, kc, vc, w.block_tables, w.context_lens, full_sel, w.scale,
                                 rows=rows)
         one = ledger.step_bytes(w.context_lens[b:b + 1], np.zeros(0, np.int64), w.Hq, w.Hkv, w.D,
-                                w.BS, w.topk, selected=sel)
+                                w.BS, w.topk, selected=sel, q_rows=qlen)
         done_bytes += one.dense + one.select + one.sparse
         seqs += 1
     elapsed = time.perf_counter() - t0 - t_setup
@@ -367,7 +394,7 @@ def run_reference(args, world, rank, pgroup):
     times, nbytes = [], []
     for i in range(args.warmup + args.steps):
         # the oracle's writes are idempotent, so every step reuses the same inputs
-        b, s, seqs = oracle_sample(w0, args.cpu_budget / max(1, args.steps + args.warmup), args.kv)
+        b, s, seqs = oracle_sample(w0, args.cpu_budget / max(1, args.steps + args.warmup), args.kv, args.qlen)
         if i >= args.warmup:
             times.append(s)
             nbytes.append(b)
@@ -407,7 +434,9 @@ def main():
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     w = workloads.make(args.workload, poison=False)
-    step = Step(w, dev, args.kv)
+    if args.qlen > 1 and (args.kv != "bf16" or w.B * args.qlen > 2048):
+        raise SystemExit("--qlen > 1: bf16 cache and at most 2048 query rows")
+    step = Step(w, dev, args.kv, args.qlen)
     calls = step.calls()
     stream = torch.cuda.current_stream(dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
@@ -420,7 +449,7 @@ def main():
     sel_host = step.sel.cpu().numpy()
     fp8 = args.kv == "fp8"
     nb = ledger.step_bytes(w.context_lens, w.slot_mapping, w.Hq, w.Hkv, w.D, w.BS, w.topk,
-                           selected=sel_host, elem_bytes=1 if fp8 else 2)
+                           selected=sel_host, elem_bytes=1 if fp8 else 2, q_rows=args.qlen)
 
     # Pass A (the timed region): whole steps, one event pair per step, L2
     # flushed before each step outside the events. Kernels launch with
@@ -541,6 +570,7 @@ def main():
         "config": {
             "workload": args.workload, "batch": w.B, "num_q_heads": w.Hq, "num_kv_heads": w.Hkv,
             "head_dim": w.D, "block_size": w.BS, "topk_blocks": w.topk, "kv_cache": args.kv,
+            "query_rows_per_sequence": args.qlen,
             "context_lens_mean": round(float(w.context_lens.mean()), 1),
             "context_lens_max": int(w.context_lens.max()), "pool_blocks": w.NB,
             "kv_pool_bytes": int(2 * w.key_cache.nbytes // (2 if fp8 else 1)),
@@ -554,10 +584,12 @@ def main():
         },
         "roofline": {
             "bound": "hbm",
-            "kernel": ("pa_decode_fp8" if fp8 else "pa_decode") + " (split-KV decode + fused combine, 1 launch)",
+            "kernel": ("pa_decode_fp8" if fp8 else "pa_decode_multi" if args.qlen > 1 else "pa_decode")
+                      + " (split-KV decode + fused combine, 1 launch)",
             "achieved": round(dense_gbs, 1), "peak": peak, "unit": "GB/s",
             "frac": round(dense_gbs / peak, 4), "peak_kind": peak_kind,
-            "traffic": recorded_traffic("pa_decode_fp8" if fp8 else "pa_decode", args.workload),
+            "traffic": (recorded_traffic("pa_decode_fp8" if fp8 else "pa_decode", args.workload)
+                        if args.qlen == 1 else None),
             "algorithmic_bytes_per_launch": int(nb.dense),
         },
         "breakdown": breakdown,
@@ -579,7 +611,7 @@ def main():
     }
     if world == 1 and not args.no_cpu_baseline:
         wc = workloads.make(args.workload, poison=False)
-        b, s, seqs = oracle_sample(wc, args.cpu_budget, args.kv)
+        b, s, seqs = oracle_sample(wc, args.cpu_budget, args.kv, args.qlen)
         line["cpu_baseline"] = {
             "value": round(b / s / 1e9, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
             "sample": f"write path for all {w.T} tokens + {seqs} of {w.B} sequences "

@@ -246,8 +246,12 @@ PA_API int pa_check_metadata(int32_t *counts, const int64_t *slot_mapping, int64
  * output. cu_seqlens_q is [batch + 1] int32 on the device, 0 = cu[0] <= ... <=
  * cu[batch] = total_q (not checked on the host; a malformed array gives
  * undefined rows, never a fault). block_tables and context_lens are per
- * sequence. Workspace: pa_decode_workspace_size(total_q, ...), same zero-fill
- * rule. Supported: batch, total_q <= 2048; other limits as pa_decode. */
+ * sequence. Up to 4 query rows of a sequence share one pass over its KV.
+ * Workspace: pa_decode_multi_workspace_size(total_q, ...) bytes, zero-filled
+ * once like pa_decode's. Supported: batch, total_q <= 2048; other limits as
+ * pa_decode. */
+PA_API size_t pa_decode_multi_workspace_size(int total_q, int num_q_heads, int num_kv_heads, int head_dim);
+
 PA_API int pa_decode_multi(pa_bf16 *out, const pa_bf16 *query,
                     const pa_bf16 *key_cache, const pa_bf16 *value_cache,
                     const int32_t *block_tables, int max_blocks_per_seq,

@@ -88,6 +88,8 @@ def load_library(path: Optional[str] = None):
         L.pa_workspace_status.restype = i32
         L.pa_check_metadata.argtypes = [vp, vp, i64, vp, i32, vp, i32, i32, i64, vp]
         L.pa_check_metadata.restype = i32
+        L.pa_decode_multi_workspace_size.argtypes = [i32, i32, i32, i32]
+        L.pa_decode_multi_workspace_size.restype = sz
         L.pa_decode_multi.argtypes = [vp, vp, vp, vp, vp, i32, vp, vp, i32, i32, i32, i32, i32, i32,
                                       i64, f32, vp, sz, vp]
         L.pa_decode_multi.restype = i32
@@ -568,6 +570,10 @@ def quest_sparse_decode_fp8(out: torch.Tensor, query: torch.Tensor, key_cache: t
 # ------------------------------------------------------ multi-token rows
 
 
+def pa_decode_multi_workspace_size(total_q: int, num_q_heads: int, num_kv_heads: int, head_dim: int) -> int:
+    return int(load_library().pa_decode_multi_workspace_size(total_q, num_q_heads, num_kv_heads, head_dim))
+
+
 def pa_decode_multi(out: torch.Tensor, query: torch.Tensor, key_cache: torch.Tensor,
                     value_cache: torch.Tensor, block_tables: torch.Tensor, cu_seqlens_q: torch.Tensor,
                     context_lens: torch.Tensor, scale: float,
@@ -590,7 +596,7 @@ def pa_decode_multi(out: torch.Tensor, query: torch.Tensor, key_cache: torch.Ten
         raise ValueError("shape mismatch between query/out and the caches")
     if block_tables.shape[0] != B or cu_seqlens_q.shape[0] != B + 1:
         raise ValueError("block_tables / cu_seqlens_q / context_lens batch mismatch")
-    need = pa_decode_workspace_size(max(total_q, 1), Hq, Hkv, D)
+    need = pa_decode_multi_workspace_size(max(total_q, 1), Hq, Hkv, D)
     ws = workspace if workspace is not None else _default_ws.get(dev, need)
     _check("pa_decode_multi",
            L.pa_decode_multi(_ptr(out), _ptr(query), _ptr(key_cache), _ptr(value_cache),

@@ -77,10 +77,10 @@ struct DecodeWorkspace {
     float *part;
 };
 
-DecodeWorkspace carve_decode_ws(void *ws, int B, int Hkv) {
+DecodeWorkspace carve_decode_ws(void *ws, int B, int Hkv, int per_seg = 1) {
     uint8_t *p = static_cast<uint8_t *>(ws);
     const size_t segs = size_t(B) * Hkv;
-    const size_t counters = (segs * 4 + 255) / 256 * 256;
+    const size_t counters = (segs * per_seg * 4 + 255) / 256 * 256;
     DecodeWorkspace d;
     d.status = reinterpret_cast<int32_t *>(p);
     d.counters = reinterpret_cast<int32_t *>(p + 256);
@@ -119,13 +119,15 @@ int run_decode(pa_bf16 *out, const pa_bf16 *query, const void *key_cache, const 
     DecodeGeometry geo;
     cudaError_t e = decode_geometry(D, &geo, fp8);
     if (e != cudaSuccess) return cuda_fail(e);
-    if (workspace_bytes < decode_workspace_bytes(B, Hkv, D, geo.workers)) return PA_ERR_WORKSPACE;
+    const size_t need = cu_q ? decode_multi_workspace_bytes(B, Hkv, D, geo.workers)
+                             : decode_workspace_bytes(B, Hkv, D, geo.workers);
+    if (workspace_bytes < need) return PA_ERR_WORKSPACE;
     CUtensorMap tk, tv;
     if ((rc = make_cache_map(&tk, key_cache, Hkv, D, BS, NB, fp8)) != PA_OK) return rc;
     // an E4M3 V cache is read with plain bulk copies (its tiles are contiguous)
     if (fp8) std::memset(&tv, 0, sizeof tv);
     else if ((rc = make_cache_map(&tv, value_cache, Hkv, D, BS, NB)) != PA_OK) return rc;
-    const DecodeWorkspace w = carve_decode_ws(workspace, B, Hkv);
+    const DecodeWorkspace w = carve_decode_ws(workspace, B, Hkv, cu_q ? kMultiRowGroup : 1);
     DecodeArgs a;
     a.q = query;
     a.bt = block_tables;
@@ -468,6 +470,14 @@ int quest_sparse_decode_fp8(pa_bf16 *out, const pa_bf16 *query, const pa_e4m3 *k
 }  // extern "C"
 
 extern "C" {
+
+size_t pa_decode_multi_workspace_size(int total_q, int num_q_heads, int num_kv_heads, int head_dim) {
+    if (total_q <= 0 || num_q_heads <= 0 || num_kv_heads <= 0 || num_q_heads % num_kv_heads != 0) return 0;
+    if (total_q > kMaxMultiRows || !shape_supported(head_dim, kBlockSize)) return 0;
+    DecodeGeometry geo;
+    if (decode_geometry(head_dim, &geo) != cudaSuccess) return 0;
+    return decode_multi_workspace_bytes(total_q, num_kv_heads, head_dim, geo.workers);
+}
 
 int pa_decode_multi(pa_bf16 *out, const pa_bf16 *query, const pa_bf16 *key_cache,
                     const pa_bf16 *value_cache, const int32_t *block_tables, int max_blocks_per_seq,

@@ -104,6 +104,12 @@ __device__ __forceinline__ uint64_t l2_policy_evict_first() {
     return p;
 }
 
+__device__ __forceinline__ uint64_t l2_policy_evict_last() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
 // Hint: bring one 128-byte line into L2 (no value is returned, nothing is
 // cached closer to the SM, so a later write by another kernel is still seen).
 __device__ __forceinline__ void prefetch_l2(const void *p) {

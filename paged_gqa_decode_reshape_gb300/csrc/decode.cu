@@ -110,14 +110,14 @@ struct DecodeCfg {
     static constexpr size_t off_scr = off_info + size_t(S) * 8;
     static constexpr size_t off_flags = off_scr + size_t(NC) * SCR * 4;
     static constexpr size_t off_pre = off_flags + 64;
-    // per-row item prefix, then (multi-token rows) each row's sequence
-    static constexpr size_t seq_off(int B) { return off_pre + (size_t(B + 1) * 4 + 15) / 16 * 16; }
-    static constexpr size_t smem_bytes(int B, bool multi = false) {
-        return 1024 + seq_off(B) + (multi ? (size_t(B) * 2 + 15) / 16 * 16 : 0);
-    }
+    // per-row item prefix (PB + 1 entries); multi-token rows then add each
+    // row group's sequence and first query row (R entries each)
+    static constexpr size_t seq_off(int PB) { return off_pre + (size_t(PB + 1) * 4 + 15) / 16 * 16; }
+    static constexpr size_t row0_off(int PB, int R) { return seq_off(PB) + (size_t(R) * 2 + 15) / 16 * 16; }
+    static constexpr size_t smem_bytes(int PB, int R = 0) { return 1024 + row0_off(PB, R) + (size_t(R) * 2 + 15) / 16 * 16; }
 };
 
-template <int D, bool SPARSE, bool F8>
+template <int D, bool SPARSE, bool F8, bool MULTI>
 __global__ void __launch_bounds__(DecodeCfg<D, F8>::THREADS, 1)
     decode_kernel(const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const DecodeArgs a) {
@@ -134,7 +134,13 @@ __global__ void __launch_bounds__(DecodeCfg<D, F8>::THREADS, 1)
     float *scr = reinterpret_cast<float *>(bp + C::off_scr);
     volatile int *flags = reinterpret_cast<volatile int *>(bp + C::off_flags);
     int32_t *pre = reinterpret_cast<int32_t *>(bp + C::off_pre);
-    uint16_t *seq_of = reinterpret_cast<uint16_t *>(bp + C::seq_off(a.B));  // multi-token rows only
+    // multi-token rows: a work-list row is a group of up to RG query rows of
+    // one sequence; seq_of / row0_of give its sequence and first query row
+    constexpr int RG = C::NC;
+    static_assert(!MULTI || RG == kMultiRowGroup, "multi-token rows: one query row per consumer warp");
+    const int PB = MULTI ? max(a.B, a.nseq) : a.B;
+    uint16_t *seq_of = reinterpret_cast<uint16_t *>(bp + C::seq_off(PB));
+    uint16_t *row0_of = reinterpret_cast<uint16_t *>(bp + C::row0_off(PB, a.B));
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int B = a.B, Hkv = a.Hkv, G = a.G;
@@ -152,7 +158,7 @@ __global__ void __launch_bounds__(DecodeCfg<D, F8>::THREADS, 1)
         // context lengths, block table and selection into L2 (hints only).
         const int64_t nthr = int64_t(gridDim.x) * C::THREADS;
         const int64_t gt = int64_t(blockIdx.x) * C::THREADS + tid;
-        const int nseq = a.cu_q ? a.nseq : B;  // ctx and block tables are per sequence
+        const int nseq = MULTI ? a.nseq : B;  // ctx and block tables are per sequence
         for (int64_t off = gt * 32; off < int64_t(nseq); off += nthr * 32) prefetch_l2(a.ctx + off);
         const int64_t bt_n = int64_t(nseq) * a.MBS;
         for (int64_t off = gt * 32; off < bt_n; off += nthr * 32) prefetch_l2(a.bt + off);
@@ -163,30 +169,42 @@ __global__ void __launch_bounds__(DecodeCfg<D, F8>::THREADS, 1)
     }
     pdl_wait();  // inputs may come from the previous kernel in the stream
     // Multi-token rows ("18 e2e inference serving", sections 2.7 and 3.3):
-    // row r belongs to the sequence s with cu_q[s] <= r < cu_q[s+1] and sees
-    // the positions before ctx_s - q_len_s + (r - cu_q[s]) + 1 (causal mask
+    // query row r of sequence s (cu_q[s] <= r < cu_q[s+1]) sees the
+    // positions before ctx_s - q_len_s + (r - cu_q[s]) + 1 (causal mask
     // aligned on the right).
     auto row_ctx = [&](int r, int s) -> int {
         const int c0 = min(max(__ldg(a.ctx + s), 0), max_tok);
         const int c1 = __ldg(a.cu_q + s), ql = __ldg(a.cu_q + s + 1) - c1;
         return min(max(c0 - ql + (r - c1) + 1, 0), c0);
     };
-    for (int b = tid; b < B; b += C::THREADS) {
+    // block count of work-list row v (MULTI: the blocks its last query row sees)
+    auto row_items = [&](int v) -> int {
         int c;
-        if (a.cu_q) {
-            int lo = 0, hi = a.nseq;  // the last sequence whose first row is <= b
-            while (hi - lo > 1) {
-                const int mid = (lo + hi) >> 1;
-                if (__ldg(a.cu_q + mid) <= b) lo = mid; else hi = mid;
-            }
-            seq_of[b] = uint16_t(lo);
-            c = row_ctx(b, lo);
+        if constexpr (MULTI) {
+            const int sq = seq_of[v];
+            c = row_ctx(min(int(row0_of[v]) + RG, __ldg(a.cu_q + sq + 1)) - 1, sq);
         } else {
-            c = min(max(__ldg(a.ctx + b), 0), max_tok);
+            c = min(max(__ldg(a.ctx + v), 0), max_tok);
         }
         const int nblk = (c + BS - 1) / BS;
-        pre[b + 1] = SPARSE ? (nblk > 0 ? a.topk : 0) : nblk;
-    }
+        return SPARSE ? (nblk > 0 ? a.topk : 0) : nblk;
+    };
+    auto scan_pre = [&](int n) {  // pre[1..n] -> inclusive prefix sums (warp 0)
+        if (warp == 0) {
+            int carry = 0;
+            for (int b0 = 0; b0 < n; b0 += 32) {
+                const int b = b0 + lane;
+                int v = (b < n) ? pre[b + 1] : 0;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const int u = __shfl_up_sync(0xffffffffu, v, o);
+                    if (lane >= o) v += u;
+                }
+                if (b < n) pre[b + 1] = carry + v;
+                carry += __shfl_sync(0xffffffffu, v, 31);
+            }
+        }
+    };
     if (tid == 0) {
         pre[0] = 0;
         flags[0] = 0;  // abort
@@ -194,38 +212,58 @@ __global__ void __launch_bounds__(DecodeCfg<D, F8>::THREADS, 1)
         flags[2] = 0;  // segment ends whose states have been merged
         for (int s = 0; s < S; ++s) {
             mbar_init(full_bar + s * 8, 1);
-            mbar_init(empty_bar + s * 8, 1);
+            mbar_init(empty_bar + s * 8, MULTI ? NC : 1);  // MULTI: every consumer reads every stage
         }
         fence_barrier_init();
     }
-    __syncthreads();
-    if (warp == 0) {
-        int carry = 0;
-        for (int b0 = 0; b0 < B; b0 += 32) {
-            const int b = b0 + lane;
-            int v = (b < B) ? pre[b + 1] : 0;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const int u = __shfl_up_sync(0xffffffffu, v, o);
-                if (lane >= o) v += u;
+    int NR = B;  // work-list rows
+    if constexpr (MULTI) {
+        // row groups: ceil(q_len / RG) per sequence, then each group's sequence and first row
+        for (int sq = tid; sq < a.nseq; sq += C::THREADS) {
+            const int ql = max(__ldg(a.cu_q + sq + 1) - __ldg(a.cu_q + sq), 0);
+            pre[sq + 1] = (ql + RG - 1) / RG;
+        }
+        __syncthreads();
+        scan_pre(a.nseq);
+        __syncthreads();
+        NR = min(pre[a.nseq], B);
+        for (int sq = tid; sq < a.nseq; sq += C::THREADS) {
+            const int g0 = pre[sq], r0 = __ldg(a.cu_q + sq);
+            for (int gi = g0; gi < min(pre[sq + 1], NR); ++gi) {
+                seq_of[gi] = uint16_t(sq);
+                row0_of[gi] = uint16_t(min(r0 + (gi - g0) * RG, 0xffff));
             }
-            if (b < B) pre[b + 1] = carry + v;
-            carry += __shfl_sync(0xffffffffu, v, 31);
         }
+        __syncthreads();
     }
+    for (int v = tid; v < NR; v += C::THREADS) pre[v + 1] = row_items(v);
+    __syncthreads();
+    scan_pre(NR);
     __syncthreads();
 
-    // sequences with nothing to attend to get a zero output
-    for (int idx = blockIdx.x * C::THREADS + tid; idx < B * a.Hq; idx += gridDim.x * C::THREADS) {
-        const int b = idx / a.Hq;
-        if (pre[b + 1] == pre[b]) {
-            uint4 *o = reinterpret_cast<uint4 *>(a.out + int64_t(idx) * D);
+    // sequences (MULTI: query rows of groups) with nothing to attend to get a zero output
+    if constexpr (MULTI) {
+        for (int idx = blockIdx.x * C::THREADS + tid; idx < NR * RG * a.Hq; idx += gridDim.x * C::THREADS) {
+            const int v = idx / (RG * a.Hq), r = (idx / a.Hq) % RG, h = idx % a.Hq;
+            const int row = row0_of[v] + r;
+            if (pre[v + 1] == pre[v] && row < __ldg(a.cu_q + seq_of[v] + 1) && row < B) {
+                uint4 *o = reinterpret_cast<uint4 *>(a.out + (int64_t(row) * a.Hq + h) * D);
 #pragma unroll
-            for (int i = 0; i < D / 8; ++i) o[i] = make_uint4(0, 0, 0, 0);
+                for (int i = 0; i < D / 8; ++i) o[i] = make_uint4(0, 0, 0, 0);
+            }
+        }
+    } else {
+        for (int idx = blockIdx.x * C::THREADS + tid; idx < B * a.Hq; idx += gridDim.x * C::THREADS) {
+            const int b = idx / a.Hq;
+            if (pre[b + 1] == pre[b]) {
+                uint4 *o = reinterpret_cast<uint4 *>(a.out + int64_t(idx) * D);
+#pragma unroll
+                for (int i = 0; i < D / 8; ++i) o[i] = make_uint4(0, 0, 0, 0);
+            }
         }
     }
 
-    const int64_t total = int64_t(Hkv) * pre[B];
+    const int64_t total = int64_t(Hkv) * pre[NR];
     const int64_t L = (total + gridDim.x - 1) / gridDim.x;
     const int64_t pos0 = int64_t(blockIdx.x) * L;
     const int64_t pos1 = min(total, pos0 + L);
@@ -243,7 +281,7 @@ __global__ void __launch_bounds__(DecodeCfg<D, F8>::THREADS, 1)
 
     // sequence holding global item position p
     auto find_seq = [&](int64_t p) -> int {
-        int lo = 0, hi = B;
+        int lo = 0, hi = NR;
         while (hi - lo > 1) {
             const int mid = (lo + hi) >> 1;
             if (int64_t(Hkv) * pre[mid] <= p) lo = mid; else hi = mid;
@@ -272,14 +310,19 @@ __global__ void __launch_bounds__(DecodeCfg<D, F8>::THREADS, 1)
             const int kvh = int(r / n);
             const int i = int(r - int64_t(kvh) * n);
             it.seg = b * Hkv + kvh;
-            it.ctxv = a.cu_q ? row_ctx(b, seq_of[b]) : __ldg(a.ctx + b);
+            if constexpr (MULTI) {
+                const int sq = seq_of[b];
+                it.ctxv = row_ctx(min(int(row0_of[b]) + RG, __ldg(a.cu_q + sq + 1)) - 1, sq);
+            } else {
+                it.ctxv = __ldg(a.ctx + b);
+            }
             it.j = SPARSE ? __ldg(a.sel + (int64_t(b) * Hkv + kvh) * a.topk + i) : i;
             return it;
         };
         auto stage_b = [&](Win &it) {
             if (it.seg < 0) return;
             const int b = it.seg / Hkv;
-            const int s = a.cu_q ? int(seq_of[b]) : b;  // the row's sequence
+            const int s = MULTI ? int(seq_of[b]) : b;  // the row's sequence
             it.phys = (it.j >= 0 && it.j < a.MBS) ? __ldg(a.bt + int64_t(s) * a.MBS + it.j) : -1;
         };
         const uint64_t policy = l2_policy_evict_first();
@@ -323,7 +366,7 @@ __global__ void __launch_bounds__(DecodeCfg<D, F8>::THREADS, 1)
                 if (k >= S && !mbar_wait_bounded(empty_bar + st * 8, ((k / S) & 1) ^ 1, kWaitLimitNs)) {
                     ok = 0;
                 } else {
-                    info[st] = make_int2(seg, nv);
+                    info[st] = make_int2(MULTI ? j : seg, nv);  // MULTI: consumers mask per query row
                     if (nv > 0) mbar_arrive_expect_tx(fb, C::STAGE);
                     else mbar_arrive(fb);
                 }
@@ -386,9 +429,12 @@ __global__ void __launch_bounds__(DecodeCfg<D, F8>::THREADS, 1)
     float m0, m1, l0, l1;
     bool traced_first = false;
 
-    auto load_q = [&](int seg) {
-        const int b = seg / Hkv, kvh = seg % Hkv;
-        const bool hv = g < G;
+    // reset the running state and load query row qr's group of heads for
+    // segment seg's KV head (qr < 0: zero queries)
+    auto load_q = [&](int seg, int qr) {
+        const int kvh = seg % Hkv;
+        const int b = qr < 0 ? 0 : qr;
+        const bool hv = g < G && qr >= 0;
         const uint32_t *qrow = reinterpret_cast<const uint32_t *>(
             a.q + (int64_t(b) * a.Hq + kvh * G + (hv ? g : 0)) * D);
         if constexpr (F8) {
@@ -522,6 +568,12 @@ __global__ void __launch_bounds__(DecodeCfg<D, F8>::THREADS, 1)
         }
         return info[k % S].y;
     };
+    // MULTI: the item's logical block too (each consumer masks its own row)
+    auto wait_full_j = [&](int k, int &j) -> int {
+        const int nv = wait_full(k);
+        j = info[k % S].x;
+        return nv;
+    };
     // one online-softmax step over up to two staged blocks (nv == 0: no block)
     auto step = [&](int ka, int nva, int kb_, int nvb) {
         const uint32_t s0a = base + (ka % S) * C::STAGE;
@@ -595,10 +647,11 @@ __global__ void __launch_bounds__(DecodeCfg<D, F8>::THREADS, 1)
     // to arrive), pieces in order with a running max per head; piece `own`
     // (or none: -1) comes from registers (log2-sum-exp ol, normalised ox)
     // instead of the workspace
-    auto combine = [&](int seg, int64_t s0, int64_t e0, int own, const float (&ol)[4],
-                       const float4 (&ox)[NSL]) {
+    // pieces in slots (slot0 + i) * pst (i < pieces), output rows at ob
+    auto combine = [&](int64_t slot0, int64_t pst, uint16_t *ob, int64_t s0, int64_t e0, int own,
+                       const float (&ol)[4], const float4 (&ox)[NSL]) {
         const int w0 = int(s0 / L), np = int((e0 - 1) / L) - w0 + 1;
-        const float *pb = a.part + int64_t(seg + w0) * C::PART;
+        (void)w0;
         float M[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
         float W[4] = {0.f, 0.f, 0.f, 0.f};
         float O[NSL][4];
@@ -617,7 +670,7 @@ __global__ void __launch_bounds__(DecodeCfg<D, F8>::THREADS, 1)
                     for (int r = 0; r < NSL; ++r) xv[u][r] = ox[r];
                     continue;
                 }
-                const float *ps = pb + int64_t(min(i0 + u, np - 1)) * C::PART;
+                const float *ps = a.part + (slot0 + int64_t(min(i0 + u, np - 1)) * pst) * C::PART;
                 lx[u] = __ldcg(reinterpret_cast<const float4 *>(ps + D * 8 + h4));
 #pragma unroll
                 for (int r = 0; r < NSL; ++r)
@@ -647,8 +700,6 @@ __global__ void __launch_bounds__(DecodeCfg<D, F8>::THREADS, 1)
                 }
             }
         }
-        const int b = seg / Hkv, kvh = seg % Hkv;
-        uint16_t *ob = a.out + (int64_t(b) * a.Hq + kvh * G) * D;
 #pragma unroll
         for (int r = 0; r < NSL; ++r) {
             const int d = (lane >> 1) + 16 * r;
@@ -798,7 +849,8 @@ __global__ void __launch_bounds__(DecodeCfg<D, F8>::THREADS, 1)
             // fence makes the counted pieces' partials visible to the loads.
             __threadfence();
             if (last_seg) PA_TRACE_LANE(6);
-            combine(seg, s0, e0, int(blockIdx.x) - w0, lse, ox);
+            combine(int64_t(seg) + w0, 1, a.out + (int64_t(seg / Hkv) * a.Hq + (seg % Hkv) * G) * D, s0, e0,
+                    int(blockIdx.x) - w0, lse, ox);
             if (lane == 0) a.counters[seg] = 0;
             if (last_seg) {
                 PA_TRACE_LANE(7);
@@ -827,12 +879,119 @@ __global__ void __launch_bounds__(DecodeCfg<D, F8>::THREADS, 1)
         if (last_seg) PA_TRACE_LANE(6);
         if (last) {
             const float nol[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-            combine(seg, s0, e0, -1, nol, ox);
+            combine(int64_t(seg) + w0, 1, a.out + (int64_t(seg / Hkv) * a.Hq + (seg % Hkv) * G) * D, s0, e0,
+                    -1, nol, ox);
             if (lane == 0) a.counters[seg] = 0;
             if (last_seg) PA_TRACE_LANE(7);
         }
         if (last_seg) PA_TRACE_LANE(4);
     };
+
+    // MULTI: end of a piece [s0, e0) of work-list segment seg for this
+    // consumer's own query row `row` (slot index (segment + CTA) * RG + c_id;
+    // counter segment * RG + c_id): the whole segment writes the row's bf16
+    // output from the registers, otherwise a normalised partial and its lse,
+    // and the piece that completes the count combines.
+    auto finish_row = [&](int seg, int row, int64_t s0, int64_t e0, bool whole) {
+        l0 += __shfl_xor_sync(0xffffffffu, l0, 4);
+        l0 += __shfl_xor_sync(0xffffffffu, l0, 8);
+        l0 += __shfl_xor_sync(0xffffffffu, l0, 16);
+        l1 += __shfl_xor_sync(0xffffffffu, l1, 4);
+        l1 += __shfl_xor_sync(0xffffffffu, l1, 8);
+        l1 += __shfl_xor_sync(0xffffffffu, l1, 16);
+        const int kvh = seg % Hkv, h0 = 2 * q4;
+        const float inv0 = l0 > 0.f ? 1.f / l0 : 0.f, inv1 = l1 > 0.f ? 1.f / l1 : 0.f;
+        uint16_t *ob = a.out + (int64_t(row) * a.Hq + kvh * G) * D;
+        if (whole) {
+#pragma unroll
+            for (int mt = 0; mt < NKK; ++mt) {
+                const int d = 16 * mt + g;
+                if (h0 < G) {
+                    ob[h0 * D + d] = __bfloat16_as_ushort(__float2bfloat16_rn(acc[mt][0] * inv0));
+                    ob[h0 * D + d + 8] = __bfloat16_as_ushort(__float2bfloat16_rn(acc[mt][2] * inv0));
+                }
+                if (h0 + 1 < G) {
+                    ob[(h0 + 1) * D + d] = __bfloat16_as_ushort(__float2bfloat16_rn(acc[mt][1] * inv1));
+                    ob[(h0 + 1) * D + d + 8] = __bfloat16_as_ushort(__float2bfloat16_rn(acc[mt][3] * inv1));
+                }
+            }
+            return;
+        }
+        const int w0 = int(s0 / L);
+        const int npieces = int((e0 - 1) / L) - w0 + 1;
+        float *ps = a.part + ((int64_t(seg) + blockIdx.x) * RG + c_id) * C::PART;
+#pragma unroll
+        for (int mt = 0; mt < NKK; ++mt) {
+            const int d = 16 * mt + g;
+            __stcg(reinterpret_cast<float2 *>(ps + d * 8 + h0), make_float2(acc[mt][0] * inv0, acc[mt][1] * inv1));
+            __stcg(reinterpret_cast<float2 *>(ps + (d + 8) * 8 + h0),
+                   make_float2(acc[mt][2] * inv0, acc[mt][3] * inv1));
+        }
+        if (g == 0)
+            __stcg(reinterpret_cast<float2 *>(ps + D * 8 + h0),
+                   make_float2(l0 > 0.f ? m0 + log2f(l0) : -INFINITY, l1 > 0.f ? m1 + log2f(l1) : -INFINITY));
+        __syncwarp();
+        int last = 0;
+        if (lane == 0) {
+            __threadfence_block();
+            last = (atomic_add_acq_rel_gpu(a.counters + int64_t(seg) * RG + c_id, 1) == npieces - 1);
+        }
+        last = __shfl_sync(0xffffffffu, last, 0);
+        __syncwarp();
+        if (last) {
+            const float nol[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+            float4 dummy[NSL];
+#pragma unroll
+            for (int r = 0; r < NSL; ++r) dummy[r] = make_float4(0.f, 0.f, 0.f, 0.f);
+            combine((int64_t(seg) + w0) * RG + c_id, RG, ob, s0, e0, -1, nol, dummy);
+            if (lane == 0) a.counters[int64_t(seg) * RG + c_id] = 0;
+        }
+    };
+
+    if constexpr (MULTI) {
+        // every consumer streams every item of the segment for its own query row
+        int64_t p = pos0;
+        int b = find_seq(p);
+        int kvh = int((p - int64_t(Hkv) * pre[b]) / (pre[b + 1] - pre[b]));
+        while (p < pos1) {
+            const int n = pre[b + 1] - pre[b];
+            const int seg = b * Hkv + kvh;
+            const int64_t s0 = int64_t(Hkv) * pre[b] + int64_t(kvh) * n;
+            const int64_t e0 = s0 + n;
+            const int ks0 = int(p - pos0), ks1 = int(min(e0, pos1) - pos0);
+            const int sq = seq_of[b], row = row0_of[b] + c_id;
+            const bool act = row < __ldg(a.cu_q + sq + 1) && row < B;
+            const int lim = act ? row_ctx(row, sq) : 0;
+            load_q(seg, act ? row : -1);
+            for (int ka = ks0; ka < ks1; ka += 2) {
+                const int kb = min(ka + 1, ks1 - 1);
+                int ja = 0, jb = 0;
+                int nva = wait_full_j(ka, ja);
+                int nvb = (kb > ka) ? wait_full_j(kb, jb) : 0;
+                nva = act ? min(nva, max(lim - ja * BS, 0)) : 0;
+                nvb = act ? min(nvb, max(lim - jb * BS, 0)) : 0;
+                if (!traced_first) {
+                    traced_first = true;
+                    if (c_id == 0) PA_TRACE(2);
+                }
+                if (nva > 0 || nvb > 0) step(ka, nva, kb, nvb);
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(empty_bar + (ka % S) * 8);
+                    if (kb > ka) mbar_arrive(empty_bar + (kb % S) * 8);
+                }
+            }
+            if (act) finish_row(seg, row, s0, e0, (s0 >= pos0) && (e0 <= pos1));
+            p = min(e0, pos1);
+            if (++kvh == Hkv) {
+                kvh = 0;
+                do {
+                    ++b;
+                } while (b < NR && pre[b + 1] == pre[b]);
+            }
+        }
+        return;
+    }
 
     // walk the segments of this CTA's range in order; every consumer warp
     // takes part in every segment's merge
@@ -846,7 +1005,7 @@ __global__ void __launch_bounds__(DecodeCfg<D, F8>::THREADS, 1)
         const int64_t s0 = int64_t(Hkv) * pre[b] + int64_t(kvh) * n;
         const int64_t e0 = s0 + n;
         const int ks0 = int(p - pos0), ks1 = int(min(e0, pos1) - pos0);
-        load_q(seg);
+        load_q(seg, b);
         // item pairs (2q, 2q+1) of this segment owned by this warp: q % NC == c_id
         int q = ks0 >> 1;
         q += (c_id - q % NC + NC) % NC;
@@ -874,7 +1033,7 @@ __global__ void __launch_bounds__(DecodeCfg<D, F8>::THREADS, 1)
             kvh = 0;
             do {
                 ++b;
-            } while (b < B && pre[b + 1] == pre[b]);
+            } while (b < NR && pre[b + 1] == pre[b]);
         }
     }
 }
@@ -892,16 +1051,16 @@ cudaError_t geometry_t(DecodeGeometry *g) {
     // per-sequence prefix grows with the batch)
     const size_t smem = C::smem_bytes(kMaxBatch) < size_t(optin) ? C::smem_bytes(kMaxBatch) : size_t(optin);
     if (smem < C::smem_bytes(1)) return cudaErrorInvalidConfiguration;
-    e = cudaFuncSetAttribute(decode_kernel<D, false, F8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             int(smem));
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(decode_kernel<D, true, F8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             int(smem));
-    if (e != cudaSuccess) return e;
-    // same L1/shared split as the library's other kernels: no reconfiguration between them
-    cudaFuncSetAttribute(decode_kernel<D, false, F8>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
-    cudaFuncSetAttribute(decode_kernel<D, true, F8>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_kernel<D, false, F8>, C::THREADS, smem);
+    void (*kernels[3])(CUtensorMap, CUtensorMap, DecodeArgs) = {
+        decode_kernel<D, false, F8, false>, decode_kernel<D, true, F8, false>, decode_kernel<D, false, F8, !F8>};
+    for (auto *kfn : kernels) {
+        e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+        if (e != cudaSuccess) return e;
+        // same L1/shared split as the library's other kernels: no reconfiguration between them
+        cudaFuncSetAttribute(kfn, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+    }
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_kernel<D, false, F8, false>, C::THREADS,
+                                                      smem);
     if (e != cudaSuccess) return e;
     if (per_sm < 1) return cudaErrorInvalidConfiguration;
     g->grid = sms * per_sm;
@@ -911,17 +1070,17 @@ cudaError_t geometry_t(DecodeGeometry *g) {
     return cudaSuccess;
 }
 
-template <int D, bool SPARSE, bool F8>
+template <int D, bool SPARSE, bool F8, bool MULTI = false>
 cudaError_t launch_t(const CUtensorMap &tm_k, const CUtensorMap &tm_v, const DecodeArgs &a,
                      cudaStream_t stream) {
     using C = DecodeCfg<D, F8>;
     DecodeGeometry geo;
     cudaError_t e = decode_geometry(D, &geo, F8);
     if (e != cudaSuccess) return e;
-    const size_t smem = C::smem_bytes(a.B, a.cu_q != nullptr);
+    const size_t smem = MULTI ? C::smem_bytes(a.B > a.nseq ? a.B : a.nseq, a.B) : C::smem_bytes(a.B);
     if (smem > geo.smem) return cudaErrorInvalidConfiguration;  // batch too large
-    return launch_pdl(decode_kernel<D, SPARSE, F8>, dim3(geo.grid), dim3(C::THREADS), smem, stream, tm_k,
-                      tm_v, a);
+    return launch_pdl(decode_kernel<D, SPARSE, F8, MULTI>, dim3(geo.grid), dim3(C::THREADS), smem, stream,
+                      tm_k, tm_v, a);
 }
 
 constexpr int kMaxDevices = 64;
@@ -957,6 +1116,18 @@ size_t decode_trace_offset(int B, int Hkv, int head_dim, int workers) {
     return head + counters + part;
 }
 
+// multi-token rows: one counter and one partial slot per (segment, query row of its group)
+size_t decode_multi_workspace_bytes(int total_q, int Hkv, int head_dim, int workers) {
+    const int RG = kMultiRowGroup;
+    const size_t segs = size_t(total_q) * Hkv;
+    const size_t counters = (segs * RG * 4 + 255) / 256 * 256;
+    size_t bytes = 256 + counters + (segs + size_t(workers)) * RG * size_t(head_dim * 8 + 8) * 4;
+#ifdef PA_DECODE_TRACE
+    bytes += size_t(workers) * 16 * sizeof(uint64_t);
+#endif
+    return bytes;
+}
+
 size_t decode_workspace_bytes(int B, int Hkv, int head_dim, int workers) {
     size_t bytes = decode_trace_offset(B, Hkv, head_dim, workers);
 #ifdef PA_DECODE_TRACE
@@ -967,6 +1138,11 @@ size_t decode_workspace_bytes(int B, int Hkv, int head_dim, int workers) {
 
 cudaError_t launch_decode(const CUtensorMap &tm_k, const CUtensorMap &tm_v, const DecodeArgs &a,
                           int head_dim, bool sparse, cudaStream_t stream, bool fp8) {
+    if (a.cu_q) {  // multi-token query rows (bf16 cache, dense)
+        if (fp8 || sparse) return cudaErrorInvalidValue;
+        return head_dim == 128 ? launch_t<128, false, false, true>(tm_k, tm_v, a, stream)
+                               : launch_t<64, false, false, true>(tm_k, tm_v, a, stream);
+    }
     if (fp8) {
         if (head_dim != 128) return cudaErrorInvalidValue;
         return sparse ? launch_t<128, true, true>(tm_k, tm_v, a, stream)

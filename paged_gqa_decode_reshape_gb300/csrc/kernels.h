@@ -11,6 +11,7 @@ constexpr int kBlockSize = 16;       // tokens per KV block
 constexpr int kMaxBatch = 4096;      // sequences per call
 constexpr int kMaxGroup = 8;         // query heads per KV head (one mma n-tile)
 constexpr int kMaxMultiRows = 2048;  // query rows of a multi-token decode call
+constexpr int kMultiRowGroup = 4;    // query rows sharing one pass over the KV (one per consumer warp)
 
 // Arguments of the split-KV decode kernel (dense and Quest-sparse).
 struct DecodeArgs {
@@ -44,6 +45,7 @@ struct DecodeGeometry {
 
 cudaError_t decode_geometry(int head_dim, DecodeGeometry *g, bool fp8 = false);
 size_t decode_workspace_bytes(int B, int Hkv, int head_dim, int workers);
+size_t decode_multi_workspace_bytes(int total_q, int Hkv, int head_dim, int workers);
 size_t decode_trace_offset(int B, int Hkv, int head_dim, int workers);
 cudaError_t launch_decode(const CUtensorMap &tm_k, const CUtensorMap &tm_v, const DecodeArgs &a,
                           int head_dim, bool sparse, cudaStream_t stream, bool fp8 = false);

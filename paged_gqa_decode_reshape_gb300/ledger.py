@@ -56,7 +56,7 @@ class StepBytes:
 
 def step_bytes(context_lens: np.ndarray, slot_mapping: np.ndarray, Hq: int, Hkv: int, D: int,
                BS: int, topk: int, selected: Optional[np.ndarray] = None,
-               elem_bytes: int = BF16, io_elem_bytes: int = BF16) -> StepBytes:
+               elem_bytes: int = BF16, io_elem_bytes: int = BF16, q_rows: int = 1) -> StepBytes:
     """Algorithmic bytes of one step's five calls.
 
     reshape: new K and V rows read and written, plus the slots;
@@ -70,7 +70,9 @@ def step_bytes(context_lens: np.ndarray, slot_mapping: np.ndarray, Hq: int, Hkv:
 
     elem_bytes is the size of one cache / metadata element (2 for bf16, 1
     for an 8-bit cache); io_elem_bytes that of q, out and the new K/V rows
-    (bf16 in both cases).
+    (bf16 in both cases). q_rows is the number of query rows per sequence of
+    the dense call (multi-token rows: each sequence's KV is still read once,
+    the query and output bytes scale with the rows).
     """
     ctx = np.clip(np.asarray(context_lens, dtype=np.int64), 0, None)
     slots = np.asarray(slot_mapping, dtype=np.int64)
@@ -84,7 +86,7 @@ def step_bytes(context_lens: np.ndarray, slot_mapping: np.ndarray, Hq: int, Hkv:
     q_bytes = B * Hq * D * io_elem_bytes
     reshape = 2 * t_valid * (row_io + row) + 8 * slots.shape[0]
     meta = t_valid * row_io + touched * row * 2 * 2 + 8 * slots.shape[0]
-    dense = int(ctx.sum()) * 2 * row + 2 * q_bytes + int(nb.sum()) * 4 + 4 * B
+    dense = int(ctx.sum()) * 2 * row + 2 * q_bytes * q_rows + int(nb.sum()) * 4 + 4 * B
     select = int(nb.sum()) * 2 * row + q_bytes + int(nb.sum()) * 4 + 4 * B + B * Hkv * topk * 4
     if selected is None:
         sparse = 0
