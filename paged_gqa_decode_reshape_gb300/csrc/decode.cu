@@ -70,6 +70,11 @@ constexpr uint64_t kWaitLimitNs = 500ull * 1000ull * 1000ull;  // 0.5 s per mbar
 #define PA_DECODE_PAIRS_F8 3
 #endif
 
+// Sparse decode of small selections (fewer than kSparseLargeItems items per
+// SM): the grid follows the segments, pieces of at least kSparseMinItems items.
+constexpr int kSparseLargeItems = 96;
+constexpr int kSparseMinItems = 24;
+
 // Optional CTA timeline (%globaltimer) for tuning builds: compile with
 // -DPA_DECODE_TRACE and the kernel writes 16 words per CTA (timestamps, SM id,
 // item count) after the partials in the workspace.
@@ -1079,7 +1084,27 @@ cudaError_t launch_t(const CUtensorMap &tm_k, const CUtensorMap &tm_v, const Dec
     if (e != cudaSuccess) return e;
     const size_t smem = MULTI ? C::smem_bytes(a.B > a.nseq ? a.B : a.nseq, a.B) : C::smem_bytes(a.B);
     if (smem > geo.smem) return cudaErrorInvalidConfiguration;  // batch too large
-    return launch_pdl(decode_kernel<D, SPARSE, F8, MULTI>, dim3(geo.grid), dim3(C::THREADS), smem, stream,
+    int grid = geo.grid;
+    if (SPARSE) {
+        // Every non-empty (sequence, KV head) segment has exactly topk items,
+        // known here. For small selections a CTA holding a few items spends
+        // most of its time on fixed costs (start-up, publishing partials, the
+        // cross-CTA combine), and a range boundary inside a segment costs a
+        // combine: cut each segment into c equal pieces (c a power of two, at
+        // least kSparseMinItems items each) or give each CTA whole segments.
+        const int64_t segs = int64_t(a.B) * a.Hkv;
+        if (segs * a.topk < int64_t(grid) * kSparseLargeItems) {
+            int64_t c = 1;
+            while (a.topk % (2 * c) == 0 && a.topk / (2 * c) >= kSparseMinItems && segs * 2 * c <= grid) c *= 2;
+            if (segs * c <= grid) {
+                grid = int(segs * c);
+            } else {
+                const int64_t m = (segs + grid - 1) / grid;  // segments per CTA
+                grid = int((segs + m - 1) / m);
+            }
+        }
+    }
+    return launch_pdl(decode_kernel<D, SPARSE, F8, MULTI>, dim3(grid), dim3(C::THREADS), smem, stream,
                       tm_k, tm_v, a);
 }
 
