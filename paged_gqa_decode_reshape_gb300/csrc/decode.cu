@@ -122,11 +122,17 @@ struct DecodeCfg {
     static constexpr size_t smem_bytes(int PB, int R = 0) { return 1024 + row0_off(PB, R) + (size_t(R) * 2 + 15) / 16 * 16; }
 };
 
-template <int D, bool SPARSE, bool F8, bool MULTI>
+// One binary serves the dense call and the sparse one (topk > 0: the items
+// are the selected blocks), so either call runs code the other has just
+// brought into the SMs' instruction caches; code that runs once per CTA (the
+// prologue, the merge and the combine) is otherwise fetched cold, several
+// microseconds per launch.
+template <int D, bool F8, bool MULTI>
 __global__ void __launch_bounds__(DecodeCfg<D, F8>::THREADS, 1)
     decode_kernel(const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const DecodeArgs a) {
     using C = DecodeCfg<D, F8>;
+    const bool SPARSE = !MULTI && a.topk > 0;
     constexpr int BS = C::BS, NC = C::NC, S = C::S, NKK = C::NKK;
 
     extern __shared__ uint8_t smem_raw[];
@@ -1056,15 +1062,15 @@ cudaError_t geometry_t(DecodeGeometry *g) {
     // per-sequence prefix grows with the batch)
     const size_t smem = C::smem_bytes(kMaxBatch) < size_t(optin) ? C::smem_bytes(kMaxBatch) : size_t(optin);
     if (smem < C::smem_bytes(1)) return cudaErrorInvalidConfiguration;
-    void (*kernels[3])(CUtensorMap, CUtensorMap, DecodeArgs) = {
-        decode_kernel<D, false, F8, false>, decode_kernel<D, true, F8, false>, decode_kernel<D, false, F8, !F8>};
+    void (*kernels[2])(CUtensorMap, CUtensorMap, DecodeArgs) = {decode_kernel<D, F8, false>,
+                                                                decode_kernel<D, F8, !F8>};
     for (auto *kfn : kernels) {
         e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
         if (e != cudaSuccess) return e;
         // same L1/shared split as the library's other kernels: no reconfiguration between them
         cudaFuncSetAttribute(kfn, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
     }
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_kernel<D, false, F8, false>, C::THREADS,
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_kernel<D, F8, false>, C::THREADS,
                                                       smem);
     if (e != cudaSuccess) return e;
     if (per_sm < 1) return cudaErrorInvalidConfiguration;
@@ -1104,7 +1110,7 @@ cudaError_t launch_t(const CUtensorMap &tm_k, const CUtensorMap &tm_v, const Dec
             }
         }
     }
-    return launch_pdl(decode_kernel<D, SPARSE, F8, MULTI>, dim3(grid), dim3(C::THREADS), smem, stream,
+    return launch_pdl(decode_kernel<D, F8, MULTI>, dim3(grid), dim3(C::THREADS), smem, stream,
                       tm_k, tm_v, a);
 }
 
