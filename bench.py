@@ -155,6 +155,20 @@ def gpu_id_for(torch, dev) -> str:
 # --------------------------------------------------------------- the step
 
 
+def arena(torch, dev, specs):
+    """One device buffer holding several tensors (each 256-byte aligned), so a
+    step's inputs (or outputs) move between host and device in one copy.
+    specs: [(name, shape, torch dtype)]. Returns (buffer, {name: view})."""
+    offs, off = {}, 0
+    for name, shape, dt in specs:
+        n = int(np.prod(shape)) * torch.empty((), dtype=dt).element_size()
+        offs[name] = (off, n)
+        off += (n + 255) // 256 * 256
+    buf = torch.empty(max(off, 256), dtype=torch.uint8, device=dev)
+    views = {name: buf[o: o + n].view(dt).view(shape) for (name, shape, dt), (o, n) in zip(specs, offs.values())}
+    return buf, views
+
+
 class Step:
     """Device buffers of one workload and the five C-ABI calls of a step."""
 
@@ -163,32 +177,42 @@ class Step:
         import paged_gqa_decode_reshape_gb300 as pg
         import workloads
         self.pg, self.torch, self.w, self.dev, self.kv, self.qlen = pg, torch, w, dev, kv, qlen
+        def d16(a):
+            return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)
+
+        # the step's inputs in one device buffer and its results in another
+        # (one host<->device copy each way per step end to end)
+        bf, i32, i64 = torch.bfloat16, torch.int32, torch.int64
+        ins = [("q", w.q.shape, bf), ("key", w.key.shape, bf), ("value", w.value.shape, bf),
+               ("slots", w.slot_mapping.shape, i64), ("bt", w.block_tables.shape, i32),
+               ("ctx", w.context_lens.shape, i32)]
+        outs = [("out", (w.B, w.Hq, w.D), bf), ("out_sparse", (w.B, w.Hq, w.D), bf),
+                ("sel", (w.B, w.Hkv, w.topk), i32)]
+        if qlen > 1:
+            ins.append(("q_multi", (w.B * qlen, w.Hq, w.D), bf))
+            outs.append(("out_multi", (w.B * qlen, w.Hq, w.D), bf))
+        self.in_buf, iv = arena(torch, dev, ins)
+        self.out_buf, ov = arena(torch, dev, outs)
+        for name, t in list(iv.items()) + list(ov.items()):
+            setattr(self, name, t)
+        self.q.copy_(d16(w.q))
+        self.key.copy_(d16(w.key))
+        self.value.copy_(d16(w.value))
+        self.slots.copy_(torch.from_numpy(w.slot_mapping))
+        self.bt.copy_(torch.from_numpy(w.block_tables))
+        self.ctx.copy_(torch.from_numpy(w.context_lens))
         if qlen > 1:
             # qlen query rows per sequence (seeded N(0, 1), bf16) for pa_decode_multi
             rng = np.random.default_rng(1234)
             qm = workloads.f32_to_bf16_bits(rng.standard_normal((w.B * qlen, w.Hq, w.D)).astype(np.float32))
-            self.q_multi = torch.from_numpy(qm.view(np.int16)).to(dev).view(torch.bfloat16)
-            self.out_multi = torch.empty_like(self.q_multi)
+            self.q_multi.copy_(torch.from_numpy(qm.view(np.int16)).view(torch.bfloat16))
             self.cu_q = torch.arange(0, w.B * qlen + 1, qlen, dtype=torch.int32, device=dev)
             self.ws_multi = torch.zeros(pg.pa_decode_multi_workspace_size(w.B * qlen, w.Hq, w.Hkv, w.D),
                                         dtype=torch.uint8, device=dev)
-
-        def d16(a):
-            return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)
-
-        self.q = d16(w.q)
         self.kc = d16(w.key_cache)
         self.vc = d16(w.value_cache)
-        self.key = d16(w.key)
-        self.value = d16(w.value)
-        self.slots = torch.from_numpy(w.slot_mapping).to(dev)
-        self.bt = torch.from_numpy(w.block_tables).to(dev)
-        self.ctx = torch.from_numpy(w.context_lens).to(dev)
-        self.out = torch.empty((w.B, w.Hq, w.D), dtype=torch.bfloat16, device=dev)
-        self.out_sparse = torch.empty_like(self.out)
         self.kmin = torch.zeros((w.NB, w.Hkv, w.D), dtype=torch.bfloat16, device=dev)
         self.kmax = torch.zeros_like(self.kmin)
-        self.sel = torch.empty((w.B, w.Hkv, w.topk), dtype=torch.int32, device=dev)
         self.ws = torch.zeros(pg.pa_decode_workspace_size(w.B, w.Hq, w.Hkv, w.D), dtype=torch.uint8,
                               device=dev)
         self.sel_ws = torch.zeros(pg.quest_select_workspace_size(w.B, w.Hkv, w.MBS),
@@ -517,30 +541,22 @@ def main():
     graph_ms = float(np.mean([e0.elapsed_time(e1) for e0, e1 in evc]))
 
     # end to end through the C ABI with host buffers: H2D of the step's inputs
-    # from pinned memory, the five calls, D2H of the outputs, every step
-    h_in = {n: t.cpu().pin_memory() for n, t in
-            dict(q=step.q, key=step.key, value=step.value, slots=step.slots, bt=step.bt,
-                 ctx=step.ctx).items()}
-    h_out = {n: torch.empty_like(t, device="cpu").pin_memory() for n, t in
-             dict(out=step.out, out_sparse=step.out_sparse, sel=step.sel).items()}
-    h2d = sum(t.numel() * t.element_size() for t in h_in.values())
-    d2h = sum(t.numel() * t.element_size() for t in h_out.values())
+    # (q, new K/V rows, slots, block tables, context lengths: one pinned
+    # buffer) and D2H of its results (dense and sparse outputs, selection),
+    # every step
+    h_in = step.in_buf.cpu().pin_memory()
+    h_out = torch.empty_like(step.out_buf, device="cpu").pin_memory()
+    h2d = h_in.numel()
+    d2h = h_out.numel()
     e2e_ms = []
     for i in range(K):
         flush.fill_(i & 0xFF)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
-        step.q.copy_(h_in["q"], non_blocking=True)
-        step.key.copy_(h_in["key"], non_blocking=True)
-        step.value.copy_(h_in["value"], non_blocking=True)
-        step.slots.copy_(h_in["slots"], non_blocking=True)
-        step.bt.copy_(h_in["bt"], non_blocking=True)
-        step.ctx.copy_(h_in["ctx"], non_blocking=True)
+        step.in_buf.copy_(h_in, non_blocking=True)
         for c in calls:
             c()
-        h_out["out"].copy_(step.out, non_blocking=True)
-        h_out["out_sparse"].copy_(step.out_sparse, non_blocking=True)
-        h_out["sel"].copy_(step.sel, non_blocking=True)
+        h_out.copy_(step.out_buf, non_blocking=True)
         e1.record(stream)
         e1.synchronize()
         e2e_ms.append(e0.elapsed_time(e1))
