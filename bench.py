@@ -52,6 +52,9 @@ def parse():
     p.add_argument("--qlen", type=int, default=1,
                    help="query rows per sequence of the dense call (> 1: pa_decode_multi, right-aligned "
                         "causal masks, for speculative / chunked-prefill rows)")
+    p.add_argument("--serial", action="store_true",
+                   help="run the step's calls one after another on one stream (default: the Quest "
+                        "selection on a second stream, alongside the dense decode)")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-budget", type=float, default=12.0,
                    help="seconds of oracle work for the CPU baseline sample")
@@ -398,6 +401,38 @@ def max_over_ranks(values, pgroup):
     return [float(v) for v in t]
 
 
+def step_runner(torch, logical, serial: bool):
+    """One step's calls (logical order: write, dense, select, sparse). Unless
+    serial, the Quest selection runs on a second stream, forked after the
+    write path and joined before the sparse decode, so it overlaps the dense
+    decode: neither reads the other's output, and the selection's CTAs fit on
+    the SMs beside the dense decode's (registers, threads and shared memory).
+    The step's first and last work stay on the calling stream."""
+    write, dense, select, sparse = logical
+    if serial:
+        order = [logical[k] for k in STEP_ORDER]
+
+        def run():
+            for c in order:
+                c()
+        return run
+    side = torch.cuda.Stream()
+    ev_write, ev_select = torch.cuda.Event(), torch.cuda.Event()
+
+    def run():
+        main = torch.cuda.current_stream()
+        write()
+        ev_write.record(main)
+        dense()  # first, so that its persistent grid takes one CTA slot per SM
+        side.wait_event(ev_write)
+        with torch.cuda.stream(side):
+            select()
+        ev_select.record(side)
+        main.wait_event(ev_select)
+        sparse()
+    return run
+
+
 def job_throughput(world: int, bytes_per_replica_step: int, ms_per_step: float) -> float:
     """Whole-job GB/s: every replica moves its step's bytes in the max-over-ranks time."""
     return world * bytes_per_replica_step / (ms_per_step * 1e-3) / 1e9
@@ -469,12 +504,12 @@ def main():
     step = Step(w, dev, args.kv, args.qlen)
     calls = [step.calls()[k] for k in STEP_ORDER]  # launch order
     stream = torch.cuda.current_stream(dev)
+    run_step = step_runner(torch, step.calls(), args.serial)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
 
     # warm-up (untimed)
     for _ in range(max(3, args.warmup)):
-        for c in calls:
-            c()
+        run_step()
     torch.cuda.synchronize(dev)
     sel_host = step.sel.cpu().numpy()
     fp8 = args.kv == "fp8"
@@ -484,7 +519,8 @@ def main():
     # Pass A (the timed region): whole steps, one event pair per step, L2
     # flushed before each step outside the events. Kernels launch with
     # programmatic stream serialization, so consecutive launches overlap their
-    # start-up with the previous kernel's tail.
+    # start-up with the previous kernel's tail; the selection runs beside the
+    # dense decode on a second stream (step_runner).
     K = args.steps
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
     sampler = ClockSampler(gpu_id_for(torch, dev))
@@ -497,8 +533,7 @@ def main():
     for i in range(K):
         flush.fill_(i & 0xFF)
         ev[i][0].record(stream)
-        for c in calls:
-            c()
+        run_step()
         ev[i][1].record(stream)
     torch.cuda.synchronize(dev)
     wall = time.perf_counter() - wall0
@@ -506,9 +541,9 @@ def main():
     step_ms = np.array([e0.elapsed_time(e1) for e0, e1 in ev])
     local_ms = float(step_ms.mean())
 
-    # Pass B: the same steps with an event between consecutive calls, for the
-    # per-call breakdown and the decode kernel's roofline (the extra events
-    # keep each call's launch gap inside its own interval).
+    # Pass B: the same steps on one stream with an event between consecutive
+    # calls, for the per-call breakdown and the decode kernel's roofline (the
+    # extra events keep each call's launch gap inside its own interval).
     evb = [[torch.cuda.Event(enable_timing=True) for _ in range(len(calls) + 1)] for _ in range(K)]
     for i in range(K):
         flush.fill_(i & 0xFF)
@@ -526,8 +561,7 @@ def main():
     # beside the eager numbers above.
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph):
-        for c in calls:
-            c()
+        run_step()
     torch.cuda.synchronize(dev)
     for _ in range(3):
         graph.replay()
@@ -554,8 +588,7 @@ def main():
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
         step.in_buf.copy_(h_in, non_blocking=True)
-        for c in calls:
-            c()
+        run_step()
         h_out.copy_(step.out_buf, non_blocking=True)
         e1.record(stream)
         e1.synchronize()
@@ -600,8 +633,10 @@ def main():
             "step": ("quest_reshape_and_cache{0} (ReshapeAndCache + metadata update, one launch) + "
                      "quest_select_topk{0} + pa_decode{0} + quest_sparse_decode{0}, in that order").format(
                          "_fp8" if fp8 else ""),
-            "timing": "value/ms_per_step: one event pair per step; breakdown/roofline: a second "
-                      "pass of the same steps with an event between calls",
+            "timing": ("value/ms_per_step: one event pair per step" +
+                       ("" if args.serial else ", the selection on a second stream beside the dense decode") +
+                       "; breakdown/roofline: a second pass of the same steps on one stream with an event "
+                       "between calls"),
             "l2": f"flushed before every step ({L2_FLUSH_BYTES >> 20} MiB write), outside the timed events",
             "parallelism": f"replicas x{world}",
         },

@@ -212,7 +212,10 @@ __device__ __forceinline__ int block_rank(bool flag, int *warp_cnt, int &total) 
     return before + in_warp;
 }
 
-constexpr int kTopkSmemKeys = 8192;  // keys cached in shared memory (32 KiB)
+// Keys cached in shared memory (12 KiB; longer rows are re-read from L2 on
+// every pass). Small enough that a top-K CTA fits on an SM beside a decode
+// CTA, so the selection can run alongside the dense decode.
+constexpr int kTopkSmemKeys = 3072;
 
 __global__ void __launch_bounds__(kTopkThreads) quest_topk_kernel(
     int32_t *__restrict__ sel, const float *__restrict__ scores, int MBS,

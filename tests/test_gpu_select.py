@@ -1,6 +1,6 @@
 """Quest selection (scores + top-K) on the GPU against the CPU oracle: a
-sequence long enough that its keys do not fit the top-K kernel's
-shared-memory cache (more than 8192 blocks), and every score of a segment
+sequence whose keys do not fit the top-K kernel's shared-memory cache
+(8199 blocks; the cache holds 3072 keys), and every score of a segment
 tied (the lower block index wins). Scores and selections must be
 bit-exact."""
 
