@@ -217,7 +217,9 @@ __device__ __forceinline__ int block_rank(bool flag, int *warp_cnt, int &total) 
 // CTA, so the selection can run alongside the dense decode.
 constexpr int kTopkSmemKeys = 3072;
 
-__global__ void __launch_bounds__(kTopkThreads) quest_topk_kernel(
+// At most 32 registers (8 CTAs per SM): a top-K CTA and a score CTA then fit
+// together on an SM beside a decode CTA.
+__global__ void __launch_bounds__(kTopkThreads, 8) quest_topk_kernel(
     int32_t *__restrict__ sel, const float *__restrict__ scores, int MBS,
     const int32_t *__restrict__ ctx, int Hkv, int BS, int topk) {
     __shared__ int hist[256];
