@@ -1,14 +1,15 @@
 """Benchmark of the paged decode hot path on GB300.
 
-One step = one pass of the whole path over one batch of synthetic input:
-ReshapeAndCache + Quest metadata update (one launch) -> Quest scoring + top-K
--> dense GQA paged decode (split-KV + combine) -> Quest sparse decode, every
-call through the C ABI (the two decode calls back to back: one kernel
-binary, so the second finds its code in the instruction caches). Inputs are resident in HBM before timing; the L2
-is flushed (a 512 MiB write) before every step, outside the timed events.
-The step time comes from one event pair per step; a second pass of the same
-steps with an event between calls gives the per-call breakdown and the
-roofline of the dominant kernel (the dense decode).
+One step = one pass of the whole path over one batch of synthetic input, every
+call through the C ABI: ReshapeAndCache + Quest metadata update (one launch),
+then the dense GQA paged decode (split-KV + combine) on the calling stream
+and, beside it on a second stream, Quest scoring + top-K followed by the
+Quest sparse decode (step_runner; --serial runs them one after another).
+Inputs are resident in HBM before timing; the L2 is flushed (a 512 MiB write)
+before every step, outside the timed events. The step time comes from one
+event pair per step; a second pass of the same steps, on one stream with an
+event between calls, gives the per-call breakdown and the roofline of the
+dominant kernel (the dense decode).
 
 Prints ONE JSON line (rank 0). With --impl reference it times the CPU oracle
 instead (a bounded sample of the same workload per step).
@@ -54,7 +55,7 @@ def parse():
                         "causal masks, for speculative / chunked-prefill rows)")
     p.add_argument("--serial", action="store_true",
                    help="run the step's calls one after another on one stream (default: the Quest "
-                        "selection on a second stream, alongside the dense decode)")
+                        "selection and sparse decode on a second stream, alongside the dense decode)")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-budget", type=float, default=12.0,
                    help="seconds of oracle work for the CPU baseline sample")
@@ -218,6 +219,8 @@ class Step:
         self.kmax = torch.zeros_like(self.kmin)
         self.ws = torch.zeros(pg.pa_decode_workspace_size(w.B, w.Hq, w.Hkv, w.D), dtype=torch.uint8,
                               device=dev)
+        # the sparse decode's own workspace: it may run at the same time as the dense one
+        self.ws_sparse = torch.zeros_like(self.ws)
         self.sel_ws = torch.zeros(pg.quest_select_workspace_size(w.B, w.Hkv, w.MBS),
                                   dtype=torch.uint8, device=dev)
         if kv == "fp8":
@@ -259,7 +262,7 @@ class Step:
                                                  self.ctx, w.BS, workspace=self.sel_ws),
                 lambda: pg.quest_sparse_decode_fp8(self.out_sparse, self.q, self.kc, self.vc,
                                                    self.k_scale, self.v_scale, self.bt, self.ctx,
-                                                   self.sel, w.scale, workspace=self.ws),
+                                                   self.sel, w.scale, workspace=self.ws_sparse),
             ]
         if self.qlen > 1:
             dense = lambda: pg.pa_decode_multi(self.out_multi, self.q_multi, self.kc, self.vc, self.bt,
@@ -274,16 +277,17 @@ class Step:
             lambda: pg.quest_select_topk(self.sel, self.q, self.kmin, self.kmax, self.bt, self.ctx,
                                          w.BS, workspace=self.sel_ws),
             lambda: pg.quest_sparse_decode(self.out_sparse, self.q, self.kc, self.vc, self.bt,
-                                           self.ctx, self.sel, w.scale, workspace=self.ws),
+                                           self.ctx, self.sel, w.scale, workspace=self.ws_sparse),
         ]
 
 
 CALL_NAMES = ["write", "dense", "select", "sparse"]
 LAUNCHES_PER_CALL = [1, 1, 2, 1]
-# Launch order of the calls within a step: the Quest selection first, then the
-# two decode calls back to back. Dense and sparse decode are one kernel binary,
-# so the second runs with the code the first left in the SMs' instruction
-# caches (the selection has no data dependence on the dense call).
+# Launch order of the calls in a one-stream step (--serial, and the per-call
+# pass): the Quest selection first, then the two decode calls back to back.
+# Dense and sparse decode are one kernel binary, so the second runs with the
+# code the first left in the SMs' instruction caches (the selection has no
+# data dependence on the dense call).
 STEP_ORDER = [0, 2, 1, 3]
 
 
@@ -403,11 +407,12 @@ def max_over_ranks(values, pgroup):
 
 def step_runner(torch, logical, serial: bool):
     """One step's calls (logical order: write, dense, select, sparse). Unless
-    serial, the Quest selection runs on a second stream, forked after the
-    write path and joined before the sparse decode, so it overlaps the dense
-    decode: neither reads the other's output, and the selection's CTAs fit on
-    the SMs beside the dense decode's (registers, threads and shared memory).
-    The step's first and last work stay on the calling stream."""
+    serial, the Quest path (selection, then sparse decode) runs on a second
+    stream forked after the write path and joined at the end of the step, so
+    it overlaps the dense decode. Neither path reads the other's output, the
+    two decode calls have their own workspaces, the selection's CTAs fit on
+    the SMs beside the dense decode's (registers, threads and shared memory),
+    and the sparse decode's CTAs take SMs as the dense decode's finish."""
     write, dense, select, sparse = logical
     if serial:
         order = [logical[k] for k in STEP_ORDER]
@@ -417,7 +422,7 @@ def step_runner(torch, logical, serial: bool):
                 c()
         return run
     side = torch.cuda.Stream()
-    ev_write, ev_select = torch.cuda.Event(), torch.cuda.Event()
+    ev_write, ev_quest = torch.cuda.Event(), torch.cuda.Event()
 
     def run():
         main = torch.cuda.current_stream()
@@ -427,9 +432,9 @@ def step_runner(torch, logical, serial: bool):
         side.wait_event(ev_write)
         with torch.cuda.stream(side):
             select()
-        ev_select.record(side)
-        main.wait_event(ev_select)
-        sparse()
+            sparse()
+        ev_quest.record(side)
+        main.wait_event(ev_quest)
     return run
 
 
@@ -519,8 +524,8 @@ def main():
     # Pass A (the timed region): whole steps, one event pair per step, L2
     # flushed before each step outside the events. Kernels launch with
     # programmatic stream serialization, so consecutive launches overlap their
-    # start-up with the previous kernel's tail; the selection runs beside the
-    # dense decode on a second stream (step_runner).
+    # start-up with the previous kernel's tail; the Quest selection and sparse
+    # decode run beside the dense decode on a second stream (step_runner).
     K = args.steps
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
     sampler = ClockSampler(gpu_id_for(torch, dev))
@@ -634,7 +639,8 @@ def main():
                      "quest_select_topk{0} + pa_decode{0} + quest_sparse_decode{0}, in that order").format(
                          "_fp8" if fp8 else ""),
             "timing": ("value/ms_per_step: one event pair per step" +
-                       ("" if args.serial else ", the selection on a second stream beside the dense decode") +
+                       ("" if args.serial else ", the Quest selection and sparse decode on a second stream "
+                        "beside the dense decode") +
                        "; breakdown/roofline: a second pass of the same steps on one stream with an event "
                        "between calls"),
             "l2": f"flushed before every step ({L2_FLUSH_BYTES >> 20} MiB write), outside the timed events",
