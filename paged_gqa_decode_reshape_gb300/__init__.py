@@ -8,8 +8,11 @@ library's CUDA kernels; there is no fallback. PyTorch provides device memory
 and streams only.
 
 Names follow the C ABI: ``pa_reshape_and_cache``, ``pa_decode``,
-``quest_update_meta``, ``quest_rebuild_meta``, ``quest_select_topk``,
-``quest_sparse_decode`` (plus workspace-size queries and checks).
+``quest_update_meta``, ``quest_reshape_and_cache`` (both write steps in one
+launch), ``quest_rebuild_meta``, ``quest_select_topk``,
+``quest_sparse_decode``; ``pa_decode_multi`` for several query rows per
+sequence; the ``*_fp8`` variants for an 8-bit (E4M3) cache; plus the
+workspace-size queries and checks.
 """
 
 from __future__ import annotations
@@ -33,6 +36,9 @@ __all__ = [
     "pa_decode_workspace_size", "pa_decode", "quest_update_meta", "quest_reshape_and_cache",
     "quest_rebuild_meta",
     "quest_select_workspace_size", "quest_select_topk", "quest_sparse_decode",
+    "pa_decode_multi_workspace_size", "pa_decode_multi",
+    "pa_reshape_and_cache_fp8", "quest_update_meta_fp8", "quest_reshape_and_cache_fp8",
+    "quest_rebuild_meta_fp8", "quest_select_topk_fp8", "pa_decode_fp8", "quest_sparse_decode_fp8",
     "pa_workspace_status", "pa_check_metadata", "Workspace",
 ]
 

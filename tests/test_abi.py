@@ -41,6 +41,16 @@ def test_library_exports_every_declared_symbol(lib):
         assert hasattr(lib, n), f"{n} declared in paged_decode.h but not exported"
 
 
+def test_binding_wraps_every_entry_point():
+    """Every C entry point has a same-named Python wrapper in the binding (argument
+    marshalling only). pa_last_cuda_error feeds the binding's error messages, and
+    pa_decode_no_alloc is for C callers that must not allocate."""
+    for n in declared_functions():
+        if n in ("pa_last_cuda_error", "pa_decode_no_alloc"):
+            continue
+        assert n in pg.__all__ and callable(getattr(pg, n, None)), f"{n} has no Python wrapper"
+
+
 def test_status_strings(lib):
     assert pg.pa_status_string(0) == "PA_OK"
     assert pg.pa_status_string(-1) == "PA_ERR_INVALID_ARG"
