@@ -408,11 +408,13 @@ def max_over_ranks(values, pgroup):
 def step_runner(torch, logical, serial: bool):
     """One step's calls (logical order: write, dense, select, sparse). Unless
     serial, the Quest path (selection, then sparse decode) runs on a second
-    stream forked after the write path and joined at the end of the step, so
-    it overlaps the dense decode. Neither path reads the other's output, the
-    two decode calls have their own workspaces, the selection's CTAs fit on
-    the SMs beside the dense decode's (registers, threads and shared memory),
-    and the sparse decode's CTAs take SMs as the dense decode's finish."""
+    stream forked after the write path and joined at the end of the step.
+    Neither path reads the other's output, and the two decode calls have
+    their own workspaces. The Quest path's CTAs take SMs as the dense
+    decode's CTAs finish (its last ~13 us), instead of waiting for the whole
+    dense grid. Nothing runs on an SM beside a dense-decode CTA itself: its
+    five 248-register warps fill one of the SM's four register-file
+    partitions."""
     write, dense, select, sparse = logical
     if serial:
         order = [logical[k] for k in STEP_ORDER]

@@ -213,12 +213,10 @@ __device__ __forceinline__ int block_rank(bool flag, int *warp_cnt, int &total) 
 }
 
 // Keys cached in shared memory (12 KiB; longer rows are re-read from L2 on
-// every pass). Small enough that a top-K CTA fits on an SM beside a decode
-// CTA, so the selection can run alongside the dense decode.
+// every pass): small, so that many top-K CTAs fit on an SM.
 constexpr int kTopkSmemKeys = 3072;
 
-// At most 32 registers (8 CTAs per SM): a top-K CTA and a score CTA then fit
-// together on an SM beside a decode CTA.
+// At most 32 registers (8 CTAs per SM).
 __global__ void __launch_bounds__(kTopkThreads, 8) quest_topk_kernel(
     int32_t *__restrict__ sel, const float *__restrict__ scores, int MBS,
     const int32_t *__restrict__ ctx, int Hkv, int BS, int topk) {
