@@ -410,11 +410,10 @@ def step_runner(torch, logical, serial: bool):
     serial, the Quest path (selection, then sparse decode) runs on a second
     stream forked after the write path and joined at the end of the step.
     Neither path reads the other's output, and the two decode calls have
-    their own workspaces. The Quest path's CTAs take SMs as the dense
-    decode's CTAs finish (its last ~13 us), instead of waiting for the whole
-    dense grid. Nothing runs on an SM beside a dense-decode CTA itself: its
-    five 248-register warps fill one of the SM's four register-file
-    partitions."""
+    their own workspaces. The selection's CTAs run on the SMs beside the
+    dense decode's (a decode CTA's four warps leave room in each of the SM's
+    register-file partitions); the sparse decode's CTAs, which need a whole
+    SM's shared memory, take SMs as the dense decode's CTAs finish."""
     write, dense, select, sparse = logical
     if serial:
         order = [logical[k] for k in STEP_ORDER]

@@ -55,11 +55,19 @@ constexpr uint64_t kWaitLimitNs = 500ull * 1000ull * 1000ull;  // 0.5 s per mbar
 // stage s always belongs to consumer (s / 2) % consumers: every consumer waits
 // on its own stages in order and an mbarrier parity wait can never be
 // answered by an older phase.
+// Three consumers (four warps per CTA) keep one decode warp in each of the
+// SM's four register-file partitions, leaving room for the selection's CTAs
+// to run beside a decode CTA; four warps at 248 registers each already carry
+// the HBM rate. The multi-token kernel keeps one consumer per query row of a
+// group (kMultiRowGroup).
 #ifndef PA_DECODE_CONSUMERS
-#define PA_DECODE_CONSUMERS 4
+#define PA_DECODE_CONSUMERS 3
 #endif
 #ifndef PA_DECODE_PAIRS
-#define PA_DECODE_PAIRS 3
+#define PA_DECODE_PAIRS 4
+#endif
+#ifndef PA_DECODE_PAIRS_MULTI
+#define PA_DECODE_PAIRS_MULTI 3
 #endif
 // E4M3 cache: consumer warps and pairs in flight (its items are half the
 // bytes, so twice the consumers keep the same bytes in flight)
@@ -96,7 +104,7 @@ constexpr int kSparseMinItems = 24;
     } while (0)
 #endif
 
-template <int D, bool F8 = false>
+template <int D, bool F8 = false, bool MULTI = false>
 struct DecodeCfg {
     static_assert(!F8 || D == 128, "the E4M3 cache path is for head_dim 128");
     static constexpr int BS = kBlockSize;
@@ -105,9 +113,10 @@ struct DecodeCfg {
     static constexpr int NKK = D / 16;          // QK k-steps == PV m-tiles
     static constexpr int HALF = BS * 128;       // bytes of one 64-dim half tile
     static constexpr int PART = D * 8 + 8;      // floats per partial slot: O[D][8], lse[8]
-    static constexpr int NC = F8 ? PA_DECODE_CONSUMERS_F8 : PA_DECODE_CONSUMERS;
+    static constexpr int NC = F8 ? PA_DECODE_CONSUMERS_F8 : (MULTI ? kMultiRowGroup : PA_DECODE_CONSUMERS);
     static constexpr int THREADS = (NC + 1) * 32;
-    static constexpr int R = F8 ? PA_DECODE_PAIRS_F8 : (D == 128 ? PA_DECODE_PAIRS : 2 * PA_DECODE_PAIRS);
+    static constexpr int PAIRS = MULTI ? PA_DECODE_PAIRS_MULTI : PA_DECODE_PAIRS;
+    static constexpr int R = F8 ? PA_DECODE_PAIRS_F8 : (D == 128 ? PAIRS : 2 * PAIRS);
     static constexpr int S = 2 * NC * R;        // ring stages
     static constexpr int SCR = D * 8 + 16;      // floats per consumer merge slot: acc[D][8], m[8], l[8]
     static constexpr size_t off_bars = size_t(S) * STAGE;
@@ -128,10 +137,10 @@ struct DecodeCfg {
 // prologue, the merge and the combine) is otherwise fetched cold, several
 // microseconds per launch.
 template <int D, bool F8, bool MULTI>
-__global__ void __launch_bounds__(DecodeCfg<D, F8>::THREADS, 1)
+__global__ void __launch_bounds__(DecodeCfg<D, F8, MULTI>::THREADS, 1)
     decode_kernel(const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const DecodeArgs a) {
-    using C = DecodeCfg<D, F8>;
+    using C = DecodeCfg<D, F8, MULTI>;
     const bool SPARSE = !MULTI && a.topk > 0;
     constexpr int BS = C::BS, NC = C::NC, S = C::S, NKK = C::NKK;
 
@@ -1052,6 +1061,7 @@ __global__ void __launch_bounds__(DecodeCfg<D, F8>::THREADS, 1)
 template <int D, bool F8>
 cudaError_t geometry_t(DecodeGeometry *g) {
     using C = DecodeCfg<D, F8>;
+    using CM = DecodeCfg<D, F8, true>;
     cudaError_t e;
     int dev = 0, sms = 0, per_sm = 0, optin = 0;
     if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
@@ -1061,14 +1071,16 @@ cudaError_t geometry_t(DecodeGeometry *g) {
     // shared memory for the largest batch that fits (the ring is fixed; the
     // per-sequence prefix grows with the batch)
     const size_t smem = C::smem_bytes(kMaxBatch) < size_t(optin) ? C::smem_bytes(kMaxBatch) : size_t(optin);
+    const size_t smem_m = CM::smem_bytes(kMaxBatch) < size_t(optin) ? CM::smem_bytes(kMaxBatch) : size_t(optin);
     if (smem < C::smem_bytes(1)) return cudaErrorInvalidConfiguration;
     void (*kernels[2])(CUtensorMap, CUtensorMap, DecodeArgs) = {decode_kernel<D, F8, false>,
                                                                 decode_kernel<D, F8, !F8>};
-    for (auto *kfn : kernels) {
-        e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+    const size_t limits[2] = {smem, F8 ? smem : smem_m};
+    for (int i = 0; i < 2; ++i) {
+        e = cudaFuncSetAttribute(kernels[i], cudaFuncAttributeMaxDynamicSharedMemorySize, int(limits[i]));
         if (e != cudaSuccess) return e;
         // same L1/shared split as the library's other kernels: no reconfiguration between them
-        cudaFuncSetAttribute(kfn, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+        cudaFuncSetAttribute(kernels[i], cudaFuncAttributePreferredSharedMemoryCarveout, 100);
     }
     e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_kernel<D, F8, false>, C::THREADS,
                                                       smem);
@@ -1078,18 +1090,19 @@ cudaError_t geometry_t(DecodeGeometry *g) {
     g->warps = C::NC + 1;
     g->workers = g->grid;
     g->smem = smem;
+    g->smem_multi = smem_m;
     return cudaSuccess;
 }
 
 template <int D, bool SPARSE, bool F8, bool MULTI = false>
 cudaError_t launch_t(const CUtensorMap &tm_k, const CUtensorMap &tm_v, const DecodeArgs &a,
                      cudaStream_t stream) {
-    using C = DecodeCfg<D, F8>;
+    using C = DecodeCfg<D, F8, MULTI>;
     DecodeGeometry geo;
     cudaError_t e = decode_geometry(D, &geo, F8);
     if (e != cudaSuccess) return e;
     const size_t smem = MULTI ? C::smem_bytes(a.B > a.nseq ? a.B : a.nseq, a.B) : C::smem_bytes(a.B);
-    if (smem > geo.smem) return cudaErrorInvalidConfiguration;  // batch too large
+    if (smem > (MULTI ? geo.smem_multi : geo.smem)) return cudaErrorInvalidConfiguration;  // batch too large
     int grid = geo.grid;
     if (SPARSE) {
         // Every non-empty (sequence, KV head) segment has exactly topk items,

@@ -40,7 +40,8 @@ struct DecodeGeometry {
     int grid;          // CTAs (persistent)
     int warps;         // warps per CTA
     int workers;       // grid * warps
-    size_t smem;       // dynamic shared memory limit set on the kernel
+    size_t smem;       // dynamic shared memory limit set on the kernel (one query row per sequence)
+    size_t smem_multi; // the same for the multi-token kernel
 };
 
 cudaError_t decode_geometry(int head_dim, DecodeGeometry *g, bool fp8 = false);
