@@ -12,6 +12,10 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <mutex>
+#include <utility>
+#include <vector>
+
 namespace pa {
 
 constexpr int kStatusTimeout = 1;  // bit in a workspace status word: a wait gave up
@@ -240,18 +244,26 @@ __device__ __forceinline__ uint32_t f32_order_key(float f) {
     return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
+// Host side: ask once per (device, kernel) for the largest shared-memory
+// carveout, the split the decode kernel needs, so that consecutive kernels of
+// the library never make the SMs reconfigure between them.
+inline void carveout_once(const void *kernel) {
+    static std::mutex mu;
+    static std::vector<std::pair<int, const void *>> done;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return;
+    std::lock_guard<std::mutex> lock(mu);
+    for (const auto &d : done)
+        if (d.first == dev && d.second == kernel) return;
+    cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+    done.emplace_back(dev, kernel);
+}
+
 // Host side: launch a kernel with programmatic stream serialization allowed.
-// The first launch of each kernel also asks for the largest shared-memory
-// carveout, the split the decode kernel needs, so consecutive kernels of the
-// library never make the SMs reconfigure between them.
 template <typename... KArgs, typename... Args>
 inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
                               cudaStream_t stream, Args... args) {
-    static const bool carveout_set = [kernel] {
-        cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
-        return true;
-    }();
-    (void)carveout_set;
+    carveout_once(reinterpret_cast<const void *>(kernel));
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
     cfg.blockDim = block;

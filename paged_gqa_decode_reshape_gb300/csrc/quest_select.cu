@@ -308,18 +308,19 @@ template <int D, bool F8>
 cudaError_t launch_score(float *scores, const uint16_t *q, const void *kmin, const void *kmax,
                          const int32_t *bt, int MBS, const int32_t *ctx, int B, int Hq, int Hkv,
                          int BS, int64_t NB, cudaStream_t stream) {
-    static int grid = 0;  // persistent grid: every SM full
-    const size_t smem = size_t(B + 1) * 4;
-    if (!grid) {
+    // persistent grid, every SM full (computed once, thread-safe; the same on
+    // every GPU of a node)
+    static const int grid = [] {
         int dev = 0, sms = 0, per_sm = 0;
-        cudaError_t e;
-        if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
-        if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, quest_score_kernel<D, F8>, kScoreThreads,
-                                                          size_t(kMaxBatch + 1) * 4);
-        if (e != cudaSuccess) return e;
-        grid = sms * (per_sm < 1 ? 1 : per_sm);
-    }
+        if (cudaGetDevice(&dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, quest_score_kernel<D, F8>, kScoreThreads,
+                                                          size_t(kMaxBatch + 1) * 4) != cudaSuccess)
+            return 0;
+        return sms * (per_sm < 1 ? 1 : per_sm);
+    }();
+    if (grid == 0) return cudaErrorInvalidConfiguration;
+    const size_t smem = size_t(B + 1) * 4;
     return launch_pdl(quest_score_kernel<D, F8>, dim3(grid), dim3(kScoreThreads), smem, stream, scores, q,
                       kmin, kmax, bt, MBS, ctx, B, Hq, Hkv, BS, NB);
 }
