@@ -30,68 +30,77 @@ _lib = None
 CFLAGS = ["-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math", "-fPIC", "-shared"]
 
 
+def compile_source(src: str, out: str) -> str:
+    """Compile a C oracle source into the shared library ``out`` (gcc, no FMA contraction)."""
+    tmp = out + f".{os.getpid()}.tmp"
+    subprocess.check_call(["gcc", *CFLAGS, src, "-o", tmp, "-lm"])
+    os.replace(tmp, out)
+    return out
+
+
 def build(force: bool = False) -> str:
-    """Compile oracle.c into oracle/_build/liboracle.so (gcc, no FMA contraction)."""
+    """Compile oracle.c into oracle/_build/liboracle.so."""
     os.makedirs(_BUILD_DIR, exist_ok=True)
     if (not force and os.path.exists(_LIB_PATH)
             and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
         return _LIB_PATH
-    tmp = _LIB_PATH + f".{os.getpid()}.tmp"
-    subprocess.check_call(["gcc", *CFLAGS, _SRC, "-o", tmp, "-lm"])
-    os.replace(tmp, _LIB_PATH)
-    return _LIB_PATH
+    return compile_source(_SRC, _LIB_PATH)
 
 
 def _p(a: Optional[np.ndarray]):
     return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
 
 
+def load(path: str):
+    """Load a compiled oracle library and declare the signatures of its entry points."""
+    L = ctypes.CDLL(path)
+    vp, i32, i64, f64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_double
+    L.oracle_reshape_and_cache.argtypes = [vp, vp, vp, vp, vp, i64, i32, i32, i32, i64]
+    L.oracle_reshape_and_cache.restype = i64
+    L.oracle_quest_update_meta.argtypes = [vp, vp, vp, vp, i64, i32, i32, i32, i64]
+    L.oracle_quest_update_meta.restype = i64
+    L.oracle_quest_rebuild_meta.argtypes = [vp, vp, vp, vp, i32, vp, i32, i32, i32, i32, i64]
+    L.oracle_quest_rebuild_meta.restype = i32
+    att = [vp, vp, vp, vp, vp, i32, vp, i32, i32, i32, i32, i32, i64, f64]
+    L.oracle_paged_attention.argtypes = att + [vp, i64]
+    L.oracle_paged_attention.restype = i32
+    L.oracle_paged_attention_online.argtypes = att + [i64]
+    L.oracle_paged_attention_online.restype = i32
+    L.oracle_paged_attention_split.argtypes = att + [i32]
+    L.oracle_paged_attention_split.restype = i32
+    L.oracle_sparse_attention.argtypes = [vp, vp, vp, vp, vp, i32, vp, vp, i32,
+                                          i32, i32, i32, i32, i32, i64, f64, vp, i64]
+    L.oracle_sparse_attention.restype = i32
+    L.oracle_quest_scores.argtypes = [vp, vp, vp, vp, vp, i32, vp, i32, i32, i32, i32, i32, i64]
+    L.oracle_quest_scores.restype = i32
+    L.oracle_quest_topk.argtypes = [vp, vp, i32, vp, i32, i32, i32, i32]
+    L.oracle_quest_topk.restype = i32
+    L.oracle_e4m3_encode_array.argtypes = [vp, vp, i64]
+    L.oracle_e4m3_encode_array.restype = None
+    L.oracle_e4m3_decode_array.argtypes = [vp, vp, i64]
+    L.oracle_e4m3_decode_array.restype = None
+    L.oracle_reshape_and_cache_fp8.argtypes = [vp, vp, vp, vp, vp, i64, vp, vp, i32, i32, i32, i64]
+    L.oracle_reshape_and_cache_fp8.restype = i64
+    L.oracle_quest_update_meta_fp8.argtypes = [vp, vp, vp, vp, i64, vp, i32, i32, i32, i64]
+    L.oracle_quest_update_meta_fp8.restype = i64
+    L.oracle_quest_rebuild_meta_fp8.argtypes = [vp, vp, vp, vp, i32, vp, i32, i32, i32, i32, i64]
+    L.oracle_quest_rebuild_meta_fp8.restype = i32
+    L.oracle_attention_fp8.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, vp, vp, i32,
+                                       i32, i32, i32, i32, i32, i64, f64, vp, i64]
+    L.oracle_attention_fp8.restype = i32
+    L.oracle_quest_scores_fp8.argtypes = [vp, vp, vp, vp, vp, i32, vp, i32, i32, i32, i32, i32, i64]
+    L.oracle_quest_scores_fp8.restype = i32
+    L.oracle_paged_attention_multi.argtypes = [vp, vp, vp, vp, vp, i32, vp, vp, i32, i32, i32,
+                                               i32, i32, i32, i64, f64, vp, i64]
+    L.oracle_paged_attention_multi.restype = i32
+    return L
+
+
 def lib():
     global _lib
     with _lock:
         if _lib is None:
-            path = build()
-            L = ctypes.CDLL(path)
-            vp, i32, i64, f64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_double
-            L.oracle_reshape_and_cache.argtypes = [vp, vp, vp, vp, vp, i64, i32, i32, i32, i64]
-            L.oracle_reshape_and_cache.restype = i64
-            L.oracle_quest_update_meta.argtypes = [vp, vp, vp, vp, i64, i32, i32, i32, i64]
-            L.oracle_quest_update_meta.restype = i64
-            L.oracle_quest_rebuild_meta.argtypes = [vp, vp, vp, vp, i32, vp, i32, i32, i32, i32, i64]
-            L.oracle_quest_rebuild_meta.restype = i32
-            att = [vp, vp, vp, vp, vp, i32, vp, i32, i32, i32, i32, i32, i64, f64]
-            L.oracle_paged_attention.argtypes = att + [vp, i64]
-            L.oracle_paged_attention.restype = i32
-            L.oracle_paged_attention_online.argtypes = att + [i64]
-            L.oracle_paged_attention_online.restype = i32
-            L.oracle_paged_attention_split.argtypes = att + [i32]
-            L.oracle_paged_attention_split.restype = i32
-            L.oracle_sparse_attention.argtypes = [vp, vp, vp, vp, vp, i32, vp, vp, i32,
-                                                  i32, i32, i32, i32, i32, i64, f64, vp, i64]
-            L.oracle_sparse_attention.restype = i32
-            L.oracle_quest_scores.argtypes = [vp, vp, vp, vp, vp, i32, vp, i32, i32, i32, i32, i32, i64]
-            L.oracle_quest_scores.restype = i32
-            L.oracle_quest_topk.argtypes = [vp, vp, i32, vp, i32, i32, i32, i32]
-            L.oracle_quest_topk.restype = i32
-            L.oracle_e4m3_encode_array.argtypes = [vp, vp, i64]
-            L.oracle_e4m3_encode_array.restype = None
-            L.oracle_e4m3_decode_array.argtypes = [vp, vp, i64]
-            L.oracle_e4m3_decode_array.restype = None
-            L.oracle_reshape_and_cache_fp8.argtypes = [vp, vp, vp, vp, vp, i64, vp, vp, i32, i32, i32, i64]
-            L.oracle_reshape_and_cache_fp8.restype = i64
-            L.oracle_quest_update_meta_fp8.argtypes = [vp, vp, vp, vp, i64, vp, i32, i32, i32, i64]
-            L.oracle_quest_update_meta_fp8.restype = i64
-            L.oracle_quest_rebuild_meta_fp8.argtypes = [vp, vp, vp, vp, i32, vp, i32, i32, i32, i32, i64]
-            L.oracle_quest_rebuild_meta_fp8.restype = i32
-            L.oracle_attention_fp8.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, vp, vp, i32,
-                                               i32, i32, i32, i32, i32, i64, f64, vp, i64]
-            L.oracle_attention_fp8.restype = i32
-            L.oracle_quest_scores_fp8.argtypes = [vp, vp, vp, vp, vp, i32, vp, i32, i32, i32, i32, i32, i64]
-            L.oracle_quest_scores_fp8.restype = i32
-            L.oracle_paged_attention_multi.argtypes = [vp, vp, vp, vp, vp, i32, vp, vp, i32, i32, i32,
-                                                       i32, i32, i32, i64, f64, vp, i64]
-            L.oracle_paged_attention_multi.restype = i32
-            _lib = L
+            _lib = load(build())
     return _lib
 
 
