@@ -144,11 +144,19 @@ __global__ void __launch_bounds__(256) write_quest_kernel(
     const int lane = threadIdx.x & 31;
     if (t >= T) return;
     const int64_t s = __ldg(slots + t);
+    // the token's K and V rows do not depend on its slot: load the first two
+    // vectors per lane while the slot is in flight
+    const int64_t src = t * row_vecs;
+    const uint4 zero = make_uint4(0, 0, 0, 0);
+    const uint4 k0 = lane < row_vecs ? __ldg(key + src + lane) : zero;
+    const uint4 v0 = lane < row_vecs ? __ldg(value + src + lane) : zero;
+    const uint4 k1 = lane + 32 < row_vecs ? __ldg(key + src + lane + 32) : zero;
+    const uint4 v1 = lane + 32 < row_vecs ? __ldg(value + src + lane + 32) : zero;
     if (s < 0 || s >= NB * BS) return;  // padding token, or outside the pool
     const int64_t dst = s * row_vecs;   // (block * BS + offset) rows of Hkv*D
     for (int e = lane; e < row_vecs; e += 32) {
-        kc[dst + e] = __ldg(key + t * row_vecs + e);
-        vc[dst + e] = __ldg(value + t * row_vecs + e);
+        kc[dst + e] = e < 32 ? k0 : (e < 64 ? k1 : __ldg(key + src + e));
+        vc[dst + e] = e < 32 ? v0 : (e < 64 ? v1 : __ldg(value + src + e));
     }
     meta_update_warp(kmin, kmax, key, slots, T, t, s, row_vecs, BS, NB, lane);
 }

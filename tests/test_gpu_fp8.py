@@ -183,3 +183,47 @@ def test_fp8_zero_length_sequences():
     got = to_host_f64(c.out)
     assert (got[1] == 0).all() and (got[3] == 0).all()
     assert_close_attention(got, want, "fp8 dense with empty sequences")
+
+
+@pytest.mark.parametrize("with_meta", [True, False])
+def test_fp8_write_shuffled_tokens_sharing_blocks(with_meta):
+    """One call whose tokens land in the same blocks in shuffled order, with
+    padding slots, blocks that start fresh and blocks merged with their old
+    metadata, over more than one 32-token chunk of the call. Caches and
+    metadata byte for byte against the oracle (so the bytes of untouched
+    slots are unchanged)."""
+    import paged_gqa_decode_reshape_gb300 as pg
+    rng = np.random.default_rng(21)
+    NB, BS, Hkv, D, T = 12, 16, 2, 128, 70
+    d = torch.device("cuda:0")
+    slots = rng.choice(NB * BS, size=T, replace=False).astype(np.int64)
+    slots[rng.choice(T, size=6, replace=False)] = -1
+    key = workloads.f32_to_bf16_bits((rng.standard_normal((T, Hkv, D)) * 2).astype(np.float32))
+    value = workloads.f32_to_bf16_bits((rng.standard_normal((T, Hkv, D)) * 2).astype(np.float32))
+    finite = np.array([c for c in range(256) if (c & 0x7F) != 0x7F], dtype=np.uint8)
+    kc0 = rng.choice(finite, size=(NB, BS, Hkv, D)).astype(np.uint8)
+    vc0 = rng.choice(finite, size=(NB, Hkv, D, BS)).astype(np.uint8)
+    kmin0 = rng.choice(finite, size=(NB, Hkv, D)).astype(np.uint8)
+    kmax0 = rng.choice(finite, size=(NB, Hkv, D)).astype(np.uint8)
+    ks, vs = workloads.fp8_scales(Hkv)
+
+    def d16(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(d).view(torch.bfloat16)
+
+    kc, vc = torch.from_numpy(kc0.copy()).to(d), torch.from_numpy(vc0.copy()).to(d)
+    kmin, kmax = torch.from_numpy(kmin0.copy()).to(d), torch.from_numpy(kmax0.copy()).to(d)
+    ksd, vsd = torch.from_numpy(ks).to(d), torch.from_numpy(vs).to(d)
+    slots_d = torch.from_numpy(slots).to(d)
+    if with_meta:
+        pg.quest_reshape_and_cache_fp8(d16(key), d16(value), kc, vc, kmin, kmax, slots_d, ksd, vsd)
+    else:
+        pg.pa_reshape_and_cache_fp8(d16(key), d16(value), kc, vc, slots_d, ksd, vsd)
+    okc, ovc = kc0.copy(), vc0.copy()
+    oracle.reshape_and_cache_fp8(key, value, okc, ovc, slots, ks, vs)
+    np.testing.assert_array_equal(u8(kc), okc)
+    np.testing.assert_array_equal(u8(vc), ovc)
+    okmin, okmax = kmin0.copy(), kmax0.copy()
+    if with_meta:
+        oracle.quest_update_meta_fp8(okmin, okmax, key, slots, ks, BS)
+    np.testing.assert_array_equal(u8(kmin), okmin)
+    np.testing.assert_array_equal(u8(kmax), okmax)
