@@ -71,10 +71,17 @@ def load(path: str):
     L.oracle_sparse_attention.argtypes = [vp, vp, vp, vp, vp, i32, vp, vp, i32,
                                           i32, i32, i32, i32, i32, i64, f64, vp, i64]
     L.oracle_sparse_attention.restype = i32
-    L.oracle_quest_scores.argtypes = [vp, vp, vp, vp, vp, i32, vp, i32, i32, i32, i32, i32, i64]
-    L.oracle_quest_scores.restype = i32
+    score = [vp, vp, vp, vp, vp, i32, vp, i32, i32, i32, i32, i32, i64]
+    L.oracle_quest_scores_kernel_order.argtypes = score
+    L.oracle_quest_scores_kernel_order.restype = i32
+    L.oracle_quest_scores_plain.argtypes = [vp] + score
+    L.oracle_quest_scores_plain.restype = i32
+    L.oracle_quest_scores_plain_fp8.argtypes = [vp] + score
+    L.oracle_quest_scores_plain_fp8.restype = i32
     L.oracle_quest_topk.argtypes = [vp, vp, i32, vp, i32, i32, i32, i32]
     L.oracle_quest_topk.restype = i32
+    L.oracle_quest_topk_f64.argtypes = [vp, vp, i32, vp, i32, i32, i32, i32]
+    L.oracle_quest_topk_f64.restype = i32
     L.oracle_e4m3_encode_array.argtypes = [vp, vp, i64]
     L.oracle_e4m3_encode_array.restype = None
     L.oracle_e4m3_decode_array.argtypes = [vp, vp, i64]
@@ -88,8 +95,8 @@ def load(path: str):
     L.oracle_attention_fp8.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, vp, vp, i32,
                                        i32, i32, i32, i32, i32, i64, f64, vp, i64]
     L.oracle_attention_fp8.restype = i32
-    L.oracle_quest_scores_fp8.argtypes = [vp, vp, vp, vp, vp, i32, vp, i32, i32, i32, i32, i32, i64]
-    L.oracle_quest_scores_fp8.restype = i32
+    L.oracle_quest_scores_kernel_order_fp8.argtypes = score
+    L.oracle_quest_scores_kernel_order_fp8.restype = i32
     L.oracle_paged_attention_multi.argtypes = [vp, vp, vp, vp, vp, i32, vp, vp, i32, i32, i32,
                                                i32, i32, i32, i64, f64, vp, i64]
     L.oracle_paged_attention_multi.restype = i32
@@ -241,38 +248,74 @@ def sparse_attention(q, key_cache, value_cache, block_tables, context_lens, sele
 # ----------------------------------------------------------------- Quest
 
 
-def quest_scores(q, kmin, kmax, block_tables, context_lens, BS: int):
-    """Quest block scores [B, Hkv, MBS] float32 (-inf past each sequence's blocks)."""
+def _score_args(q, kmin, kmax, block_tables, context_lens, meta_dtype):
     q = _c(q, np.uint16)
-    kmin = _c(kmin, np.uint16)
-    kmax = _c(kmax, np.uint16)
+    kmin = _c(kmin, meta_dtype)
+    kmax = _c(kmax, meta_dtype)
     bt = _c(block_tables, np.int32)
     ctx = _c(context_lens, np.int32)
     B, Hq, D = q.shape
     NB, Hkv, D2 = kmin.shape
-    assert D == D2
-    MBS = bt.shape[1]
-    out = np.empty((B, Hkv, MBS), dtype=np.float32)
-    rc = lib().oracle_quest_scores(_p(out), _p(q), _p(kmin), _p(kmax), _p(bt), MBS, _p(ctx),
-                                   B, Hq, Hkv, D, BS, NB)
+    assert D == D2 and kmax.shape == kmin.shape
+    return q, kmin, kmax, bt, ctx, (B, Hq, Hkv, D, NB, bt.shape[1])
+
+
+def _scores_plain(fn, q, kmin, kmax, block_tables, context_lens, BS, meta_dtype, with_abs):
+    q, kmin, kmax, bt, ctx, (B, Hq, Hkv, D, NB, MBS) = _score_args(q, kmin, kmax, block_tables,
+                                                                   context_lens, meta_dtype)
+    out = np.empty((B, Hkv, MBS), dtype=np.float64)
+    absum = np.empty((B, Hkv, MBS), dtype=np.float64)
+    rc = fn(_p(out), _p(absum), _p(q), _p(kmin), _p(kmax), _p(bt), MBS, _p(ctx), B, Hq, Hkv, D, BS, NB)
     _check(rc, "quest_scores")
+    return (out, absum) if with_abs else out
+
+
+def quest_scores(q, kmin, kmax, block_tables, context_lens, BS: int, with_abs: bool = False):
+    """Quest block scores as the method defines them, [B, Hkv, MBS] float64:
+    sum over the GQA group of sum_d max(q*min, q*max), written out term by
+    term in fp64 (-inf past each sequence's blocks). with_abs: also return
+    A = sum_h sum_d |q| * max(|min|, |max|) per block (scales any
+    floating-point evaluation's rounding error)."""
+    return _scores_plain(lib().oracle_quest_scores_plain, q, kmin, kmax, block_tables, context_lens, BS,
+                         np.uint16, with_abs)
+
+
+def quest_scores_kernel_order(q, kmin, kmax, block_tables, context_lens, BS: int):
+    """The same block scores evaluated in fp32 in the CUDA kernel's fixed
+    order (a bit-exact reproduction of the kernel's arithmetic), [B, Hkv, MBS]
+    float32."""
+    q, kmin, kmax, bt, ctx, (B, Hq, Hkv, D, NB, MBS) = _score_args(q, kmin, kmax, block_tables,
+                                                                   context_lens, np.uint16)
+    out = np.empty((B, Hkv, MBS), dtype=np.float32)
+    rc = lib().oracle_quest_scores_kernel_order(_p(out), _p(q), _p(kmin), _p(kmax), _p(bt), MBS, _p(ctx),
+                                                B, Hq, Hkv, D, BS, NB)
+    _check(rc, "quest_scores_kernel_order")
     return out
 
 
 def quest_topk(scores, context_lens, BS: int, topk: int):
-    """Top-K logical blocks per (b, kvh): [B, Hkv, topk] int32, ascending, -1 padded."""
-    s = _c(scores, np.float32)
+    """Top-K logical blocks per (b, kvh): [B, Hkv, topk] int32, ascending, -1
+    padded; ties to the lower block index. Scores float32 or float64."""
+    f64 = np.asarray(scores).dtype == np.float64
+    s = _c(scores, np.float64 if f64 else np.float32)
     ctx = _c(context_lens, np.int32)
     B, Hkv, MBS = s.shape
     out = np.empty((B, Hkv, topk), dtype=np.int32)
-    rc = lib().oracle_quest_topk(_p(out), _p(s), MBS, _p(ctx), B, Hkv, BS, int(topk))
+    fn = lib().oracle_quest_topk_f64 if f64 else lib().oracle_quest_topk
+    rc = fn(_p(out), _p(s), MBS, _p(ctx), B, Hkv, BS, int(topk))
     _check(rc, "quest_topk")
     return out
 
 
 def quest_select(q, kmin, kmax, block_tables, context_lens, BS: int, topk: int):
-    """Scores then top-K: the selection the Quest path attends over."""
+    """The selection the method defines: top-K of the plain fp64 scores."""
     return quest_topk(quest_scores(q, kmin, kmax, block_tables, context_lens, BS),
+                      context_lens, BS, topk)
+
+
+def quest_select_kernel_order(q, kmin, kmax, block_tables, context_lens, BS: int, topk: int):
+    """Top-K of the fp32 kernel-order scores (the CUDA path's exact set)."""
+    return quest_topk(quest_scores_kernel_order(q, kmin, kmax, block_tables, context_lens, BS),
                       context_lens, BS, topk)
 
 
@@ -371,31 +414,34 @@ def attention_fp8(q, key_cache, value_cache, k_scale, v_scale, block_tables, con
     return out
 
 
-def quest_scores_fp8(q, kmin, kmax, block_tables, context_lens, BS: int):
-    """Quest block scores [B, Hkv, MBS] float32 on E4M3 metadata."""
-    q = _c(q, np.uint16)
-    kmin = _c(kmin, np.uint8)
-    kmax = _c(kmax, np.uint8)
-    bt = _c(block_tables, np.int32)
-    ctx = _c(context_lens, np.int32)
-    B, Hq, D = q.shape
-    NB, Hkv, D2 = kmin.shape
-    assert D == D2
-    MBS = bt.shape[1]
+def quest_scores_fp8(q, kmin, kmax, block_tables, context_lens, BS: int, with_abs: bool = False):
+    """Plain fp64 Quest scores over E4M3 metadata (min/max = decoded codes;
+    the per-KV-head K scale, a positive factor of a whole row, is left out)."""
+    return _scores_plain(lib().oracle_quest_scores_plain_fp8, q, kmin, kmax, block_tables, context_lens,
+                         BS, np.uint8, with_abs)
+
+
+def quest_scores_kernel_order_fp8(q, kmin, kmax, block_tables, context_lens, BS: int):
+    """fp32 kernel-order scores over E4M3 metadata, [B, Hkv, MBS] float32."""
+    q, kmin, kmax, bt, ctx, (B, Hq, Hkv, D, NB, MBS) = _score_args(q, kmin, kmax, block_tables,
+                                                                   context_lens, np.uint8)
     out = np.empty((B, Hkv, MBS), dtype=np.float32)
-    rc = lib().oracle_quest_scores_fp8(_p(out), _p(q), _p(kmin), _p(kmax), _p(bt), MBS, _p(ctx),
-                                       B, Hq, Hkv, D, BS, NB)
-    _check(rc, "quest_scores_fp8")
+    rc = lib().oracle_quest_scores_kernel_order_fp8(_p(out), _p(q), _p(kmin), _p(kmax), _p(bt), MBS,
+                                                    _p(ctx), B, Hq, Hkv, D, BS, NB)
+    _check(rc, "quest_scores_kernel_order_fp8")
     return out
 
 
 def quest_select_fp8(q, kmin, kmax, block_tables, context_lens, BS: int, topk: int):
-    """Scores on E4M3 metadata then top-K."""
+    """Top-K of the plain fp64 scores over E4M3 metadata."""
     return quest_topk(quest_scores_fp8(q, kmin, kmax, block_tables, context_lens, BS),
                       context_lens, BS, topk)
 
 
-# ------------------------------------------------------ multi-token rows
+def quest_select_kernel_order_fp8(q, kmin, kmax, block_tables, context_lens, BS: int, topk: int):
+    """Top-K of the fp32 kernel-order scores over E4M3 metadata."""
+    return quest_topk(quest_scores_kernel_order_fp8(q, kmin, kmax, block_tables, context_lens, BS),
+                      context_lens, BS, topk)
 
 
 def paged_attention_multi(q, key_cache, value_cache, block_tables, cu_seqlens_q, context_lens, scale,

@@ -27,8 +27,15 @@
  *   "GQA Paged Attention" says only that several query heads share one KV head).
  *   Attention arithmetic is fp64 (at least the fp32 the method asks for).
  *
+ * The Quest block score exists twice: oracle_quest_scores_plain is the
+ * method's sum written out term by term in fp64 (the definition the selected
+ * sets are checked against); oracle_quest_scores_kernel_order evaluates the
+ * same sum in fp32 in the CUDA kernel's fixed order, a bit-exact reproduction
+ * of the kernel's arithmetic that the tests hold to a stated error bound
+ * around the plain form.
+ *
  * Build: gcc -O2 -std=c11 -ffp-contract=off -fPIC -shared oracle.c -lm
- * (no fused multiply-add contraction: the Quest score below is defined as a
+ * (no fused multiply-add contraction: the kernel-order score is defined as a
  * sequence of individually rounded fp32 operations).
  */
 #include <math.h>
@@ -67,6 +74,14 @@ static uint32_t f32_order_key(float f)
     uint32_t u;
     memcpy(&u, &f, sizeof u);
     return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+/* totalOrder key of an fp64 value (same idea, 64 bits). */
+static uint64_t f64_order_key(double f)
+{
+    uint64_t u;
+    memcpy(&u, &f, sizeof u);
+    return (u >> 63) ? ~u : (u | (1ull << 63));
 }
 
 /* ------------------------------------------------- 8-bit float (E4M3) */
@@ -840,11 +855,110 @@ int oracle_paged_attention_multi(double *out, const uint16_t *q,
     return rc;
 }
 
-/* ------------------------------------------------------------ Quest score */
+/* ------------------------------------------------ Quest score, plain form */
 
-/* Quest block score, evaluated in fp32 in one fixed order that the GPU
- * kernel reproduces bit for bit (the score decides an integer, the top-K
- * set, so both sides take that decision in the same precision and order).
+/* metadata element as fp32: bf16, or an E4M3 code (decoded exactly) */
+static float meta_f32(const uint16_t *m16, const uint8_t *m8, int64_t idx)
+{
+    return m16 ? bf16_f32(m16[idx]) : (float)oracle_e4m3_decode(m8[idx]);
+}
+
+/* Quest block score as the method states it ([P1] "Quest Sparse Attention":
+ * a cheap upper-bound score per logical block; the bound itself is fixed by
+ * the statement of the method), written out term by term:
+ *
+ *   score(b, kvh, j) = sum_{h in group(kvh)} sum_{d < D}
+ *                      max(q[b,h,d] * min[p,kvh,d], q[b,h,d] * max[p,kvh,d])
+ *
+ * with p = block_tables[b][j] and group(kvh) = {kvh*G, ..., kvh*G + G-1}.
+ * Arithmetic is fp64: every product of two bf16 (or E4M3) values is exact in
+ * fp64, and the G*D additions are done in the order written (h ascending,
+ * then d ascending), each rounded once at 2^-53 relative.
+ *
+ * abs_sum (if not NULL) receives A = sum_h sum_d |q[b,h,d]| *
+ * max(|min_d|, |max_d|): every term of the sum above is at most its share of
+ * A in magnitude, so A scales the rounding error of any floating-point
+ * evaluation of the score.
+ *
+ * Logical blocks j >= ceil(ctx/BS) and table entries outside the pool score
+ * -inf (abs_sum 0). scores, abs_sum: [B][Hkv][MBS] fp64. */
+static int quest_scores_plain_impl(double *scores, double *abs_sum, const uint16_t *q,
+                                   const uint16_t *kmin, const uint16_t *kmax,
+                                   const uint8_t *kmin8, const uint8_t *kmax8,
+                                   const int32_t *block_tables, int MBS,
+                                   const int32_t *context_lens, int B, int Hq, int Hkv,
+                                   int D, int BS, int64_t NB)
+{
+    if (Hq % Hkv != 0)
+        return -2;
+    const int G = Hq / Hkv;
+    for (int b = 0; b < B; ++b) {
+        const int64_t ctx = context_lens[b] > 0 ? context_lens[b] : 0;
+        const int64_t nblk = (ctx + BS - 1) / BS;
+        for (int kvh = 0; kvh < Hkv; ++kvh) {
+            for (int64_t j = 0; j < MBS; ++j) {
+                const int64_t o = ((int64_t)b * Hkv + kvh) * MBS + j;
+                const int64_t p = j < nblk ? block_tables[(int64_t)b * MBS + j] : -1;
+                if (p < 0 || p >= NB) {
+                    scores[o] = -INFINITY;
+                    if (abs_sum)
+                        abs_sum[o] = 0.0;
+                    continue;
+                }
+                const int64_t base = (p * Hkv + kvh) * (int64_t)D;
+                double s = 0.0, a = 0.0;
+                for (int g = 0; g < G; ++g) {
+                    const int64_t h = (int64_t)kvh * G + g;
+                    const uint16_t *qrow = q + ((int64_t)b * Hq + h) * D;
+                    for (int d = 0; d < D; ++d) {
+                        const double qv = bf16_val(qrow[d]);
+                        const double lo = (double)meta_f32(kmin, kmin8, base + d);
+                        const double hi = (double)meta_f32(kmax, kmax8, base + d);
+                        const double x = qv * lo, y = qv * hi;
+                        s += x > y ? x : y;
+                        const double m = fabs(lo) > fabs(hi) ? fabs(lo) : fabs(hi);
+                        a += fabs(qv) * m;
+                    }
+                }
+                scores[o] = s;
+                if (abs_sum)
+                    abs_sum[o] = a;
+            }
+        }
+    }
+    return 0;
+}
+
+int oracle_quest_scores_plain(double *scores, double *abs_sum, const uint16_t *q,
+                              const uint16_t *kmin, const uint16_t *kmax,
+                              const int32_t *block_tables, int MBS,
+                              const int32_t *context_lens, int B, int Hq, int Hkv,
+                              int D, int BS, int64_t NB)
+{
+    return quest_scores_plain_impl(scores, abs_sum, q, kmin, kmax, NULL, NULL, block_tables, MBS,
+                                   context_lens, B, Hq, Hkv, D, BS, NB);
+}
+
+/* The same plain score over E4M3 metadata (min_d, max_d = the decoded codes;
+ * the cache's per-KV-head K scale is a positive factor of a whole row and is
+ * left out, as it cannot change that row's top-K). */
+int oracle_quest_scores_plain_fp8(double *scores, double *abs_sum, const uint16_t *q,
+                                  const uint8_t *kmin, const uint8_t *kmax,
+                                  const int32_t *block_tables, int MBS,
+                                  const int32_t *context_lens, int B, int Hq, int Hkv,
+                                  int D, int BS, int64_t NB)
+{
+    return quest_scores_plain_impl(scores, abs_sum, q, NULL, NULL, kmin, kmax, block_tables, MBS,
+                                   context_lens, B, Hq, Hkv, D, BS, NB);
+}
+
+/* --------------------------------- Quest score, fp32 kernel-order reproduction */
+
+/* The same block score evaluated in fp32 in the one fixed order the GPU
+ * kernel uses. It serves as a bit-exact check of the kernel's arithmetic;
+ * agreement with the method's definition is checked against the plain form
+ * above (the selected sets must match it except where the fp32 rounding
+ * error bound covers the score gap at the K-th place).
  *
  * Definition: score(b, kvh, j) = sum_{h in group(kvh)} sum_d
  *                                max(q[b,h,d]*min_d, q[b,h,d]*max_d)
@@ -863,12 +977,6 @@ int oracle_paged_attention_multi(double *out, const uint16_t *q,
  * Logical blocks j >= ceil(ctx/BS) are excluded (score -inf). A table entry
  * outside the pool also scores -inf.
  * scores: [B][Hkv][MBS] fp32. Requires D % 32 == 0. */
-/* metadata element as fp32: bf16, or an E4M3 code (decoded exactly) */
-static float meta_f32(const uint16_t *m16, const uint8_t *m8, int64_t idx)
-{
-    return m16 ? bf16_f32(m16[idx]) : (float)oracle_e4m3_decode(m8[idx]);
-}
-
 static int quest_scores_impl(float *scores, const uint16_t *q,
                              const uint16_t *kmin, const uint16_t *kmax,
                              const uint8_t *kmin8, const uint8_t *kmax8,
@@ -934,7 +1042,7 @@ static int quest_scores_impl(float *scores, const uint16_t *q,
     return 0;
 }
 
-int oracle_quest_scores(float *scores, const uint16_t *q,
+int oracle_quest_scores_kernel_order(float *scores, const uint16_t *q,
                         const uint16_t *kmin, const uint16_t *kmax,
                         const int32_t *block_tables, int MBS,
                         const int32_t *context_lens, int B, int Hq, int Hkv,
@@ -948,7 +1056,7 @@ int oracle_quest_scores(float *scores, const uint16_t *q,
  * (exact in fp32), every other step as above. The cache's per-KV-head scale
  * is left out: it multiplies every score of a (sequence, KV head) row by the
  * same positive factor and cannot change that row's top-K. */
-int oracle_quest_scores_fp8(float *scores, const uint16_t *q,
+int oracle_quest_scores_kernel_order_fp8(float *scores, const uint16_t *q,
                             const uint8_t *kmin, const uint8_t *kmax,
                             const int32_t *block_tables, int MBS,
                             const int32_t *context_lens, int B, int Hq, int Hkv,
@@ -961,7 +1069,7 @@ int oracle_quest_scores_fp8(float *scores, const uint16_t *q,
 /* ------------------------------------------------------------ Quest top-K */
 
 typedef struct {
-    uint32_t key;
+    uint64_t key; /* totalOrder key of the score (fp32 keys zero-extended) */
     int32_t j;
 } ranked_block;
 
@@ -984,9 +1092,10 @@ static int index_cmp(const void *a, const void *b)
  * logical blocks j < ceil(ctx/BS); they are fully sorted by (score desc,
  * j asc) with scores ranked by IEEE totalOrder; the first min(topk, nblk) are
  * returned in ascending block order and the row is padded with -1.
+ * Scores are fp32 (s32) or fp64 (s64), whichever is not NULL.
  * selected: [B][Hkv][topk] int32. */
-int oracle_quest_topk(int32_t *selected, const float *scores, int MBS,
-                      const int32_t *context_lens, int B, int Hkv, int BS, int topk)
+static int quest_topk_impl(int32_t *selected, const float *s32, const double *s64, int MBS,
+                           const int32_t *context_lens, int B, int Hkv, int BS, int topk)
 {
     if (topk <= 0)
         return -2;
@@ -997,9 +1106,9 @@ int oracle_quest_topk(int32_t *selected, const float *scores, int MBS,
         if (nblk > MBS)
             nblk = MBS;
         for (int kvh = 0; kvh < Hkv; ++kvh) {
-            const float *srow = scores + ((int64_t)b * Hkv + kvh) * MBS;
+            const int64_t row = ((int64_t)b * Hkv + kvh) * MBS;
             for (int64_t j = 0; j < nblk; ++j) {
-                items[j].key = f32_order_key(srow[j]);
+                items[j].key = s32 ? (uint64_t)f32_order_key(s32[row + j]) : f64_order_key(s64[row + j]);
                 items[j].j = (int32_t)j;
             }
             qsort(items, (size_t)nblk, sizeof(ranked_block), rank_cmp);
@@ -1014,4 +1123,17 @@ int oracle_quest_topk(int32_t *selected, const float *scores, int MBS,
     }
     free(items);
     return 0;
+}
+
+int oracle_quest_topk(int32_t *selected, const float *scores, int MBS,
+                      const int32_t *context_lens, int B, int Hkv, int BS, int topk)
+{
+    return quest_topk_impl(selected, scores, NULL, MBS, context_lens, B, Hkv, BS, topk);
+}
+
+/* The same selection over fp64 scores (the plain form of the score). */
+int oracle_quest_topk_f64(int32_t *selected, const double *scores, int MBS,
+                          const int32_t *context_lens, int B, int Hkv, int BS, int topk)
+{
+    return quest_topk_impl(selected, NULL, scores, MBS, context_lens, B, Hkv, BS, topk);
 }

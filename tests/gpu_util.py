@@ -11,6 +11,7 @@ import torch
 
 import oracle
 import paged_gqa_decode_reshape_gb300 as pg
+from tests.selection_check import check_selection
 from workloads import bf16_bits_to_f32
 
 MAX_ABS_TOL = 1e-2
@@ -101,12 +102,24 @@ class OracleStep:
                                       rows=rows)
 
     def scores(self, kmin, kmax):
+        """fp32 scores in the kernel's evaluation order (bit-exact reproduction)."""
         w = self.w
-        return oracle.quest_scores(w.q, kmin, kmax, w.block_tables, w.context_lens, w.BS)
+        return oracle.quest_scores_kernel_order(w.q, kmin, kmax, w.block_tables, w.context_lens, w.BS)
 
     def select(self, kmin, kmax):
+        """Top-K of the kernel-order scores: the CUDA path's exact set."""
         w = self.w
         return oracle.quest_topk(self.scores(kmin, kmax), w.context_lens, w.BS, w.topk)
+
+    def check_plain(self, sel, kmin, kmax, fp8: bool = False, what: str = "selection") -> int:
+        """The selected sets against the top-K of the plain fp64 scores (the
+        method's definition), exact up to the fp32 score error bound; returns
+        the number of exempt rows."""
+        w = self.w
+        fn = oracle.quest_scores_fp8 if fp8 else oracle.quest_scores
+        plain, absum = fn(w.q, kmin, kmax, w.block_tables, w.context_lens, w.BS, with_abs=True)
+        return check_selection(np.asarray(sel), plain, absum, w.context_lens, w.BS, w.topk,
+                               w.Hq // w.Hkv, w.D, what)
 
     def sparse(self, sel, rows=None):
         w = self.w

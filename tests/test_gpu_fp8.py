@@ -13,6 +13,7 @@ import torch
 import oracle
 import workloads
 from tests.gpu_util import assert_close_attention, gather_rows, sample_rows, to_host_f64
+from tests.selection_check import check_selection
 
 pytestmark = pytest.mark.gpu
 
@@ -112,13 +113,19 @@ def run_fp8_compare(w, sample=None, seed=0):
     pg.quest_select_topk_fp8(c.sel, c.q, c.kmin, c.kmax, c.bt, c.ctx, w.BS, workspace=c.sel_ws)
     n = w.B * w.Hkv * w.MBS
     got_scores = c.sel_ws[: n * 4].view(torch.float32).cpu().numpy().reshape(w.B, w.Hkv, w.MBS)
-    want_scores = oracle.quest_scores_fp8(w.q, kmin, kmax, w.block_tables, w.context_lens, w.BS)
+    want_scores = oracle.quest_scores_kernel_order_fp8(w.q, kmin, kmax, w.block_tables, w.context_lens,
+                                                       w.BS)
     nb = (np.minimum(w.context_lens, w.MBS * w.BS) + w.BS - 1) // w.BS
     for b in range(w.B):
         np.testing.assert_array_equal(got_scores[b, :, : nb[b]].view(np.uint32),
                                       want_scores[b, :, : nb[b]].view(np.uint32))
     sel = oracle.quest_topk(want_scores, w.context_lens, w.BS, w.topk)
     np.testing.assert_array_equal(c.sel.cpu().numpy(), sel)
+    # and against the method's definition: top-K of the plain fp64 scores
+    plain, absum = oracle.quest_scores_fp8(w.q, kmin, kmax, w.block_tables, w.context_lens, w.BS,
+                                           with_abs=True)
+    check_selection(c.sel.cpu().numpy(), plain, absum, w.context_lens, w.BS, w.topk, w.Hq // w.Hkv, w.D,
+                    f"{w.name} fp8 selection vs plain scores")
     # attention
     rows = None if sample is None else sample_rows(w, sample, seed)
     pg.pa_decode_fp8(c.out, c.q, c.kc, c.vc, c.ks, c.vs, c.bt, c.ctx, w.scale, workspace=c.ws)

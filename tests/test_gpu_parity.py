@@ -70,6 +70,8 @@ def run_full_compare(w, sample=None, seed=0):
         np.testing.assert_array_equal(ds[b, :, : nb[b]], os_[b, :, : nb[b]])
     osel = ora.select(kmin, kmax)
     np.testing.assert_array_equal(dsel.cpu().numpy(), osel)
+    # and against the method's definition: top-K of the plain fp64 scores
+    ora.check_plain(dsel.cpu().numpy(), kmin, kmax, what=f"{w.name} selection vs plain scores")
     # a7 sparse decode on the oracle's selection
     got = to_host_f64(dev.sparse(torch.from_numpy(osel).to(dev.dev)))
     want = ora.sparse(osel, rows)

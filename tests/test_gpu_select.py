@@ -48,6 +48,7 @@ def test_select_ties_across_parts():
     dsel = dev.select().cpu().numpy()
     osel = ora.select(kmin, kmax)
     np.testing.assert_array_equal(dsel, osel)
+    assert ora.check_plain(dsel, kmin, kmax, what="all-tied selection vs plain scores") == 0
     nb = w.num_blocks()
     for b in range(w.B):
         want = np.arange(w.topk) if nb[b] > w.topk else np.r_[np.arange(nb[b]), -np.ones(w.topk - nb[b])]

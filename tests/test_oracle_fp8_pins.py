@@ -256,6 +256,9 @@ def test_fp8_scores_equal_bf16_scores_on_decoded_meta(oracle_lib):
     q, kc, vc, bt, ctx = _case(rng)
     kmin, kmax = oracle_lib.quest_rebuild_meta_fp8(kc, bt, ctx)
     bmin, bmax = bf16(torch_decode(kmin)), bf16(torch_decode(kmax))
+    a = oracle_lib.quest_scores_kernel_order_fp8(q, kmin, kmax, bt, ctx, kc.shape[1])
+    b = oracle_lib.quest_scores_kernel_order(q, bmin, bmax, bt, ctx, kc.shape[1])
+    np.testing.assert_array_equal(a, b)
     a = oracle_lib.quest_scores_fp8(q, kmin, kmax, bt, ctx, kc.shape[1])
     b = oracle_lib.quest_scores(q, bmin, bmax, bt, ctx, kc.shape[1])
     np.testing.assert_array_equal(a, b)
@@ -269,6 +272,7 @@ def test_fp8_score_bounds_every_token(oracle_lib):
     ks = np.array([0.02, 0.007], dtype=np.float32)
     kmin, kmax = oracle_lib.quest_rebuild_meta_fp8(kc, bt, ctx)
     sc = oracle_lib.quest_scores_fp8(q, kmin, kmax, bt, ctx, kc.shape[1])
+    sk = oracle_lib.quest_scores_kernel_order_fp8(q, kmin, kmax, bt, ctx, kc.shape[1])
     B, Hq, D = q.shape
     BS, Hkv = kc.shape[1], kc.shape[2]
     G = Hq // Hkv
@@ -281,4 +285,6 @@ def test_fp8_score_bounds_every_token(oracle_lib):
                 n = min(BS, ctx[b] - j * BS)
                 logits = kd[bt[b, j], :n, kvh] @ qs * ks[kvh]
                 bound = float(sc[b, kvh, j]) * float(ks[kvh])
+                assert bound >= logits.max() - 1e-9 * (abs(bound) + 1.0)
+                bound = float(sk[b, kvh, j]) * float(ks[kvh])
                 assert bound >= logits.max() - 1e-5 * (abs(bound) + 1.0)

@@ -22,8 +22,8 @@ import test_oracle_multi_pins as M
 import test_oracle_pins as P
 
 
-def _pin(mod, name, **kw):
-    return (mod, name, kw)
+def _pin(mod, test_name, **kw):
+    return (mod, test_name, kw)
 
 
 SDPA_G3 = _pin(P, "test_dense_matches_library_sdpa", B=2, Hq=6, Hkv=2, D=8, BS=4, ctx=[3, 13],
@@ -92,10 +92,29 @@ MUTANTS = [
      [_pin(P, "test_quest_score_exact_on_integers"), _pin(P, "test_quest_bound_dominates_true_max")]),
     ("score_last_reduction_step_dropped", "for (int off = 16; off >= 1; off >>= 1)",
      "for (int off = 16; off > 1; off >>= 1)", 1,
-     [_pin(P, "test_quest_score_exact_on_integers"), _pin(P, "test_quest_score_close_to_definition")]),
+     [_pin(P, "test_quest_score_exact_on_integers"),
+      _pin(P, "test_quest_score_kernel_order_within_fp32_bound", name="tiny")]),
     ("score_block_past_context_kept", "if (j >= nblk) {", "if (j > nblk) {", 1,
      [_pin(P, "test_quest_score_exact_on_integers")]),
+    # Quest block score, plain fp64 form
+    ("plain_score_max_uses_min", "const double x = qv * lo, y = qv * hi;",
+     "const double x = qv * lo, y = qv * lo;", 1,
+     [_pin(P, "test_quest_score_exact_on_integers"), _pin(P, "test_quest_score_sign_closed_forms")]),
+    ("plain_score_min_of_products", "s += x > y ? x : y;", "s += x < y ? x : y;", 1,
+     [_pin(P, "test_quest_score_exact_on_integers"), _pin(P, "test_quest_bound_dominates_true_max")]),
+    ("plain_score_group_interleaved", "const int64_t h = (int64_t)kvh * G + g;",
+     "const int64_t h = (int64_t)g * Hkv + kvh;", 1,
+     [_pin(P, "test_quest_score_group_mapping"), _pin(P, "test_quest_score_identical_tokens_is_group_dot_product")]),
+    ("plain_score_block_past_context_kept",
+     "const int64_t p = j < nblk ? block_tables[(int64_t)b * MBS + j] : -1;",
+     "const int64_t p = j <= nblk ? block_tables[(int64_t)b * MBS + j] : -1;", 1,
+     [_pin(P, "test_quest_score_exact_on_integers")]),
+    ("plain_abs_sum_min_side_only", "const double m = fabs(lo) > fabs(hi) ? fabs(lo) : fabs(hi);",
+     "const double m = fabs(lo);", 1,
+     [_pin(P, "test_quest_score_abs_sum")]),
     # Quest top-K
+    ("topk_f64_raw_bits_order", "return (u >> 63) ? ~u : (u | (1ull << 63));", "return u;", 1,
+     [_pin(P, "test_topk_f64_brute_force_with_ties_and_signs")]),
     ("topk_lowest_first", "return x->key > y->key ? -1 : 1;", "return x->key < y->key ? -1 : 1;", 1,
      [_pin(P, "test_topk_brute_force_with_ties"), _pin(P, "test_topk_tie_goes_to_lower_index")]),
     ("topk_tie_to_higher_index", "return x->j < y->j ? -1 : (x->j > y->j);",

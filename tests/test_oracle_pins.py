@@ -398,31 +398,22 @@ def test_incremental_decode_meta_equals_rebuild(oracle_lib):
 
 
 # ------------------------------------------------------------- Quest score
+#
+# Two oracle functions compute the block score: quest_scores (the method's
+# sum written out term by term in fp64) and quest_scores_kernel_order (fp32 in
+# the CUDA kernel's evaluation order, for bit-exact comparison). Each is
+# pinned to closed forms and brute force; the kernel-order one is also held
+# to the stated fp32 error bound around the plain one.
 
 
-def _score_fp64(q, kmin, kmax, bt, ctx, BS):
-    B, Hq, D = q.shape
-    NB, Hkv, _ = kmin.shape
-    G = Hq // Hkv
-    qf = bf16_bits_to_f32(q).astype(np.float64)
-    mn = bf16_bits_to_f32(kmin).astype(np.float64)
-    mx = bf16_bits_to_f32(kmax).astype(np.float64)
-    out = np.full((B, Hkv, bt.shape[1]), -np.inf)
-    for b in range(B):
-        for j in range((int(ctx[b]) + BS - 1) // BS):
-            p = bt[b, j]
-            for kvh in range(Hkv):
-                s = 0.0
-                for g in range(G):
-                    qq = qf[b, kvh * G + g]
-                    s += np.maximum(qq * mn[p, kvh], qq * mx[p, kvh]).sum()
-                out[b, kvh, j] = s
-    return out
+def _both(oracle_lib, q, kmin, kmax, bt, ctx, BS):
+    return (oracle_lib.quest_scores(q, kmin, kmax, bt, ctx, BS),
+            oracle_lib.quest_scores_kernel_order(q, kmin, kmax, bt, ctx, BS).astype(np.float64))
 
 
 def test_quest_score_exact_on_integers(oracle_lib):
-    """Small-integer inputs make every fp32 step exact: the score must equal the
-    integer value of sum_h sum_d max(q*min, q*max) computed directly."""
+    """Small-integer inputs make every fp32 and fp64 step exact: both score
+    functions must equal the integer value of sum_h sum_d max(q*min, q*max)."""
     rng = np.random.default_rng(11)
     B, Hq, Hkv, D, BS = 2, 6, 2, 64, 4
     NB = 8
@@ -432,24 +423,123 @@ def test_quest_score_exact_on_integers(oracle_lib):
     kmin, kmax = bf16(lo.astype(np.float32)), bf16(hi.astype(np.float32))
     bt = rng.permutation(NB).astype(np.int32).reshape(B, 4)
     ctx = np.array([13, 5], dtype=np.int32)
-    got = oracle_lib.quest_scores(q, kmin, kmax, bt, ctx, BS)
-    want = _score_fp64(q, kmin, kmax, bt, ctx, BS)
-    np.testing.assert_array_equal(got.astype(np.float64), want)
-    assert np.isneginf(got[1, :, 2:]).all()          # blocks past ctx excluded
+    qi = bf16_bits_to_f32(q).astype(np.int64)
+    want = np.full((B, Hkv, 4), -np.inf)
+    G = Hq // Hkv
+    for b in range(B):
+        for j in range((int(ctx[b]) + BS - 1) // BS):
+            p = bt[b, j]
+            for kvh in range(Hkv):
+                qq = qi[b, kvh * G:(kvh + 1) * G]                  # [G, D]
+                want[b, kvh, j] = np.maximum(qq * lo[p, kvh], qq * hi[p, kvh]).sum()
+    for got in _both(oracle_lib, q, kmin, kmax, bt, ctx, BS):
+        np.testing.assert_array_equal(got, want)
+        assert np.isneginf(got[1, :, 2:]).all()          # blocks past ctx excluded
 
 
-def test_quest_score_close_to_definition(oracle_lib):
-    w = workloads.make("tiny")
-    oracle_lib.reshape_and_cache(w.key, w.value, w.key_cache, w.value_cache, w.slot_mapping)
+def test_quest_score_identical_tokens_is_group_dot_product(oracle_lib):
+    """A block whose tokens all hold the same key k has min = max = k, and the
+    bound collapses to the group-summed logit sum_h q_h . k: a library dot
+    product (numpy, fp64)."""
+    rng = np.random.default_rng(21)
+    B, Hq, Hkv, D, BS, NB = 3, 28, 4, 128, 16, 9
+    q = rand_bf16(rng, (B, Hq, D))
+    k = rand_bf16(rng, (NB, Hkv, D))
+    bt = rng.permutation(NB).astype(np.int32).reshape(B, 3)
+    ctx = np.array([40, 33, 17], dtype=np.int32)
+    plain, korder = _both(oracle_lib, q, k, k, bt, ctx, BS)
+    qf = bf16_bits_to_f32(q).astype(np.float64)
+    kf = bf16_bits_to_f32(k).astype(np.float64)
+    G = Hq // Hkv
+    for b in range(B):
+        for j in range((int(ctx[b]) + BS - 1) // BS):
+            for kvh in range(Hkv):
+                want = np.dot(qf[b, kvh * G:(kvh + 1) * G].sum(axis=0), kf[bt[b, j], kvh])
+                assert abs(plain[b, kvh, j] - want) <= 1e-12 * (1 + abs(want))
+                assert abs(korder[b, kvh, j] - want) <= 1e-4 * (1 + abs(want))
+
+
+def test_quest_score_sign_closed_forms(oracle_lib):
+    """With every query element >= 0 the bound takes the max side everywhere:
+    score = (sum_h q_h) . max; with every element <= 0 it takes the min side:
+    score = (sum_h q_h) . min (library dot products)."""
+    rng = np.random.default_rng(22)
+    B, Hq, Hkv, D, BS, NB = 2, 8, 2, 64, 16, 6
+    lo = rng.standard_normal((NB, Hkv, D)).astype(np.float32)
+    kmin = bf16(lo)
+    kmax = bf16(lo + np.abs(rng.standard_normal((NB, Hkv, D))).astype(np.float32) + 0.25)
+    bt = rng.permutation(NB).astype(np.int32).reshape(B, 3)
+    ctx = np.array([48, 20], dtype=np.int32)
+    mn = bf16_bits_to_f32(kmin).astype(np.float64)
+    mx = bf16_bits_to_f32(kmax).astype(np.float64)
+    G = Hq // Hkv
+    for sign, side in ((1.0, mx), (-1.0, mn)):
+        q = bf16(sign * np.abs(rng.standard_normal((B, Hq, D))).astype(np.float32))
+        qf = bf16_bits_to_f32(q).astype(np.float64)
+        plain, korder = _both(oracle_lib, q, kmin, kmax, bt, ctx, BS)
+        for b in range(B):
+            for j in range((int(ctx[b]) + BS - 1) // BS):
+                for kvh in range(Hkv):
+                    want = np.dot(qf[b, kvh * G:(kvh + 1) * G].sum(axis=0), side[bt[b, j], kvh])
+                    assert abs(plain[b, kvh, j] - want) <= 1e-12 * (1 + abs(want))
+                    assert abs(korder[b, kvh, j] - want) <= 1e-4 * (1 + abs(want))
+
+
+def test_quest_score_group_mapping(oracle_lib):
+    """Query head h belongs to KV head h // G: with one non-zero query head,
+    only its KV head's score row is non-zero."""
+    rng = np.random.default_rng(23)
+    B, Hq, Hkv, D, BS, NB = 1, 12, 3, 64, 16, 4
+    kmin = rand_bf16(rng, (NB, Hkv, D))
+    kmax = bf16(bf16_bits_to_f32(kmin) + 1.0)
+    bt = np.arange(NB, dtype=np.int32).reshape(1, NB)
+    ctx = np.array([NB * BS], dtype=np.int32)
+    G = Hq // Hkv
+    for h0 in (0, 5, 11):
+        q = np.zeros((B, Hq, D), dtype=np.uint16)
+        q[0, h0] = rand_bf16(rng, (D,))
+        for sc in _both(oracle_lib, q, kmin, kmax, bt, ctx, BS):
+            nz = np.abs(sc[0]).sum(axis=1) > 0
+            np.testing.assert_array_equal(nz, np.arange(Hkv) == h0 // G)
+
+
+def test_quest_score_abs_sum(oracle_lib):
+    """A = sum_h sum_d |q| max(|min|, |max|) bounds |score|, and equals the
+    score when q and the metadata are all non-negative."""
+    rng = np.random.default_rng(24)
+    B, Hq, Hkv, D, BS, NB = 2, 8, 2, 64, 16, 6
+    bt = rng.permutation(NB).astype(np.int32).reshape(B, 3)
+    ctx = np.array([48, 20], dtype=np.int32)
+    q = rand_bf16(rng, (B, Hq, D))
+    lo = rng.standard_normal((NB, Hkv, D)).astype(np.float32)
+    kmin, kmax = bf16(lo), bf16(lo + 0.5)
+    s, a = oracle_lib.quest_scores(q, kmin, kmax, bt, ctx, BS, with_abs=True)
+    fin = np.isfinite(s)
+    assert (a[fin] >= np.abs(s[fin])).all() and (a[~fin] == 0).all()
+    q = bf16(np.abs(bf16_bits_to_f32(q)))
+    kmin = bf16(np.abs(lo))
+    kmax = bf16(np.abs(lo) + 0.5)
+    s, a = oracle_lib.quest_scores(q, kmin, kmax, bt, ctx, BS, with_abs=True)
+    np.testing.assert_array_equal(a[fin], s[fin])
+
+
+@pytest.mark.parametrize("name", ["tiny", "quest_8k"])
+def test_quest_score_kernel_order_within_fp32_bound(oracle_lib, name):
+    """The fp32 kernel-order score stays within the stated rounding bound
+    E = (gamma_{G+D/32+5}(2^-24) + gamma_{G*D}(2^-53)) * A of the plain fp64
+    score, on every block of the workload (the bound the selection check
+    relies on)."""
+    from tests.selection_check import score_error_bound
+    kw = {} if name == "tiny" else dict(batch=4, ctx_scale=0.25, topk=16)
+    w = workloads.make(name, poison=False, **kw)
     kmin, kmax = oracle_lib.quest_rebuild_meta(w.key_cache, w.block_tables, w.context_lens)
-    got = oracle_lib.quest_scores(w.q, kmin, kmax, w.block_tables, w.context_lens, w.BS)
-    want = _score_fp64(w.q, kmin, kmax, w.block_tables, w.context_lens, w.BS)
-    finite = np.isfinite(want)
-    assert (np.isfinite(got) == finite).all()
-    # fp32 evaluation error bound: (G + D/32 + 7) ulps of the absolute term sum
-    G = w.Hq // w.Hkv
-    bound = (G + w.D // 32 + 7) * 2.0 ** -24 * np.abs(want[finite]).max() * 4 + 1e-6
-    assert np.abs(got[finite] - want[finite]).max() <= bound
+    plain, a = oracle_lib.quest_scores(w.q, kmin, kmax, w.block_tables, w.context_lens, w.BS, with_abs=True)
+    korder = oracle_lib.quest_scores_kernel_order(w.q, kmin, kmax, w.block_tables, w.context_lens, w.BS)
+    fin = np.isfinite(plain)
+    assert (np.isfinite(korder) == fin).all()
+    E = score_error_bound(a, w.Hq // w.Hkv, w.D)
+    err = np.abs(korder[fin].astype(np.float64) - plain[fin])
+    assert (err <= E[fin]).all(), float((err / E[fin]).max())
 
 
 def test_quest_bound_dominates_true_max(oracle_lib):
@@ -461,7 +551,7 @@ def test_quest_bound_dominates_true_max(oracle_lib):
     qf = bf16_bits_to_f32(w.q).astype(np.float64)
     mn = bf16_bits_to_f32(kmin).astype(np.float64)
     mx = bf16_bits_to_f32(kmax).astype(np.float64)
-    scores = oracle_lib.quest_scores(w.q, kmin, kmax, w.block_tables, w.context_lens, w.BS)
+    plain, korder = _both(oracle_lib, w.q, kmin, kmax, w.block_tables, w.context_lens, w.BS)
     G = w.Hq // w.Hkv
     for b in range(w.B):
         for j in range(w.num_blocks()[b]):
@@ -476,7 +566,8 @@ def test_quest_bound_dominates_true_max(oracle_lib):
                     logits = K[:, kvh] @ qq
                     assert bound_h >= logits.max() - 1e-9
                     group_logits += logits
-                assert scores[b, kvh, j] >= group_logits.max() - 1e-3
+                assert plain[b, kvh, j] >= group_logits.max() - 1e-9
+                assert korder[b, kvh, j] >= group_logits.max() - 1e-3
 
 
 # -------------------------------------------------------------- Quest top-K
@@ -493,6 +584,27 @@ def test_topk_brute_force_with_ties(oracle_lib):
         for kvh in range(Hkv):
             s = scores[b, kvh, :nb]
             order = np.lexsort((np.arange(nb), -s))      # score desc, index asc
+            want = np.sort(order[: min(K, nb)])
+            row = sel[b, kvh]
+            np.testing.assert_array_equal(row[: len(want)], want)
+            assert (row[len(want):] == -1).all()
+
+
+def test_topk_f64_brute_force_with_ties_and_signs(oracle_lib):
+    """The top-K over fp64 scores (the plain score's type): negative and
+    positive scores, -0 ranked below +0, planted ties, against a lexsort."""
+    rng = np.random.default_rng(13)
+    B, Hkv, MBS, BS, K = 3, 2, 50, 16, 9
+    scores = rng.integers(-4, 4, (B, Hkv, MBS)).astype(np.float64) * 0.375
+    scores[0, 0, :6] = [0.0, -0.0, 0.0, -0.0, 1e300, -1e300]
+    ctx = np.array([50 * 16, 6 * 16 - 1, 20 * 16], dtype=np.int32)
+    sel = oracle_lib.quest_topk(scores, ctx, BS, K)
+    for b in range(B):
+        nb = (int(ctx[b]) + BS - 1) // BS
+        for kvh in range(Hkv):
+            s = scores[b, kvh, :nb]
+            signbit = np.signbit(s).astype(np.int8)            # -0 ranks below +0
+            order = np.lexsort((np.arange(nb), signbit * (s == 0), -s))
             want = np.sort(order[: min(K, nb)])
             row = sel[b, kvh]
             np.testing.assert_array_equal(row[: len(want)], want)
