@@ -134,13 +134,23 @@ PA_API int pa_decode(pa_bf16 *out, const pa_bf16 *query,
  * `stream` and then runs pa_decode's kernel; all calls share the one buffer,
  * so calls that overlap on the GPU race. Returns PA_ERR_WORKSPACE when the
  * batch and head shape need more scratch than the buffer holds (about
- * B * Hkv + number_of_SMs partial slots of (8 * head_dim + 8) floats). */
+ * B * Hkv + number_of_SMs partial slots of (8 * head_dim + 8) floats).
+ * A kernel that gave up on a bounded wait (the output is then undefined) is
+ * reported by pa_decode_no_alloc_status, which must be read before the next
+ * pa_decode_no_alloc call on that device clears the status word. */
 PA_API int pa_decode_no_alloc(pa_bf16 *out, const pa_bf16 *query,
                               const pa_bf16 *key_cache, const pa_bf16 *value_cache,
                               const int32_t *block_tables, int max_blocks_per_seq,
                               const int32_t *context_lens, int batch, int num_q_heads,
                               int num_kv_heads, int head_dim, int block_size, int64_t num_blocks,
                               float scale, void *stream);
+
+/* Device-side status of the last pa_decode_no_alloc call on the current
+ * device: waits for `stream`, then reads the fixed buffer's status word.
+ * PA_OK, PA_ERR_DEVICE if that call's kernel gave up on a bounded wait, or
+ * PA_ERR_INVALID_ARG if pa_decode_no_alloc has not run on this device yet.
+ * Allocates nothing. */
+PA_API int pa_decode_no_alloc_status(void *stream);
 
 /* Quest metadata update for the tokens of one ReshapeAndCache call. For each
  * physical block touched by a valid slot: if one of the call's tokens lands

@@ -70,3 +70,16 @@ extern "C" int pa_decode_no_alloc(pa_bf16 *out, const pa_bf16 *query, const pa_b
                      context_lens, batch, num_q_heads, num_kv_heads, head_dim, block_size,
                      num_blocks, scale, scratch, kNoAllocScratchBytes, stream);
 }
+
+extern "C" int pa_decode_no_alloc_status(void *stream) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return PA_ERR_CUDA;
+    if (dev < 0 || dev >= kMaxDevices) return PA_ERR_UNSUPPORTED;
+    void *scratch = nullptr;
+    {
+        std::lock_guard<std::mutex> lock(g_scratch_mu);
+        scratch = g_scratch_ptr[dev];
+    }
+    if (!scratch) return PA_ERR_INVALID_ARG;  // no call on this device yet
+    return pa_workspace_status(scratch, stream);
+}

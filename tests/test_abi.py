@@ -44,9 +44,10 @@ def test_library_exports_every_declared_symbol(lib):
 def test_binding_wraps_every_entry_point():
     """Every C entry point has a same-named Python wrapper in the binding (argument
     marshalling only). pa_last_cuda_error feeds the binding's error messages, and
-    pa_decode_no_alloc is for C callers that must not allocate."""
+    pa_decode_no_alloc (with its status query) is for C callers that must not
+    allocate."""
     for n in declared_functions():
-        if n in ("pa_last_cuda_error", "pa_decode_no_alloc"):
+        if n in ("pa_last_cuda_error", "pa_decode_no_alloc", "pa_decode_no_alloc_status"):
             continue
         assert n in pg.__all__ and callable(getattr(pg, n, None)), f"{n} has no Python wrapper"
 
