@@ -1,6 +1,8 @@
 // api.cu -- the C ABI (include/paged_decode.h): argument checks on the host,
 // TMA descriptors, workspace carving, and the kernel launches. Nothing here
 // allocates device memory.
+#include <atomic>
+#include <climits>
 #include <cstring>
 
 #include "../../include/paged_decode.h"
@@ -11,6 +13,14 @@ using namespace pa;
 namespace {
 
 thread_local int g_last_cuda_error = 0;
+
+// Limit of every bounded wait inside the decode kernel, and the item at which
+// its producer stops issuing copies. Fixed at 0.5 s and "never" in the
+// library; the failure-test build (PA_FAULT_TEST) lets a test change both, so
+// that a wait runs out on purpose and the timeout path can be checked.
+constexpr uint64_t kDefaultWaitNs = 500ull * 1000ull * 1000ull;
+std::atomic<uint64_t> g_wait_ns{kDefaultWaitNs};
+std::atomic<int> g_stop_item{INT_MAX};
 
 int cuda_fail(cudaError_t e) {
     g_last_cuda_error = int(e);
@@ -140,12 +150,8 @@ int run_decode(pa_bf16 *out, const pa_bf16 *query, const void *key_cache, const 
     a.part = w.part;
     a.counters = w.counters;
     a.status = w.status;
-#ifdef PA_DECODE_TRACE
-    a.trace = reinterpret_cast<uint64_t *>(static_cast<uint8_t *>(workspace) +
-                                           decode_trace_offset(B, Hkv, D, geo.workers));
-#else
-    a.trace = nullptr;
-#endif
+    a.wait_ns = g_wait_ns.load(std::memory_order_relaxed);
+    a.stop_item = g_stop_item.load(std::memory_order_relaxed);
     a.NB = NB;
     a.MBS = MBS;
     a.topk = sparse ? topk : 0;
@@ -492,3 +498,14 @@ int pa_decode_multi(pa_bf16 *out, const pa_bf16 *query, const pa_bf16 *key_cache
 }
 
 }  // extern "C"
+
+#ifdef PA_FAULT_TEST
+// Failure-test build only: every later decode launch gives up a bounded wait
+// after wait_ns (0: the default 0.5 s) and its producer stops issuing at item
+// stop_item of each CTA's range (negative: never), so the consumers' waits
+// for the stages that are never armed run out.
+extern "C" PA_API void pa_fault_test_configure(int stop_item, uint64_t wait_ns) {
+    g_wait_ns.store(wait_ns ? wait_ns : kDefaultWaitNs, std::memory_order_relaxed);
+    g_stop_item.store(stop_item < 0 ? INT_MAX : stop_item, std::memory_order_relaxed);
+}
+#endif

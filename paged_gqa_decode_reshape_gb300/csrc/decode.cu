@@ -48,8 +48,6 @@ namespace pa {
 
 namespace {
 
-constexpr uint64_t kWaitLimitNs = 500ull * 1000ull * 1000ull;  // 0.5 s per mbarrier wait
-
 // Launch geometry (tuning knobs): consumer warps, and block pairs each
 // consumer has in flight. The ring has S = 2 * consumers * pairs stages, so
 // stage s always belongs to consumer (s / 2) % consumers: every consumer waits
@@ -82,27 +80,6 @@ constexpr uint64_t kWaitLimitNs = 500ull * 1000ull * 1000ull;  // 0.5 s per mbar
 // SM): the grid follows the segments, pieces of at least kSparseMinItems items.
 constexpr int kSparseLargeItems = 96;
 constexpr int kSparseMinItems = 24;
-
-// Optional CTA timeline (%globaltimer) for tuning builds: compile with
-// -DPA_DECODE_TRACE and the kernel writes 16 words per CTA (timestamps, SM id,
-// item count) after the partials in the workspace.
-#ifdef PA_DECODE_TRACE
-#define PA_TRACE(k)                                                                      \
-    do {                                                                                 \
-        if (tid == 0 && a.trace) a.trace[int64_t(blockIdx.x) * 16 + (k)] = global_timer_ns(); \
-    } while (0)
-#define PA_TRACE_LANE(k)                                                                  \
-    do {                                                                                  \
-        if (lane == 0 && a.trace) a.trace[int64_t(blockIdx.x) * 16 + (k)] = global_timer_ns(); \
-    } while (0)
-#else
-#define PA_TRACE(k) \
-    do {            \
-    } while (0)
-#define PA_TRACE_LANE(k) \
-    do {                 \
-    } while (0)
-#endif
 
 template <int D, bool F8 = false, bool MULTI = false>
 struct DecodeCfg {
@@ -165,7 +142,6 @@ __global__ void __launch_bounds__(DecodeCfg<D, F8, MULTI>::THREADS, 1)
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int B = a.B, Hkv = a.Hkv, G = a.G;
     const int max_tok = a.MBS * BS;
-    PA_TRACE(0);
 
     // ---- prologue: items per KV head of every sequence and their prefix sum
     pdl_trigger();
@@ -289,15 +265,6 @@ __global__ void __launch_bounds__(DecodeCfg<D, F8, MULTI>::THREADS, 1)
     const int64_t pos1 = min(total, pos0 + L);
     if (pos0 >= pos1) return;  // whole CTA: nothing to do
     const int n_items = int(pos1 - pos0);
-    PA_TRACE(1);
-#ifdef PA_DECODE_TRACE
-    if (tid == 0 && a.trace) {
-        uint32_t smid;
-        asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
-        a.trace[int64_t(blockIdx.x) * 16 + 8] = smid;
-        a.trace[int64_t(blockIdx.x) * 16 + 9] = uint64_t(n_items);
-    }
-#endif
 
     // sequence holding global item position p
     auto find_seq = [&](int64_t p) -> int {
@@ -361,6 +328,7 @@ __global__ void __launch_bounds__(DecodeCfg<D, F8, MULTI>::THREADS, 1)
         const int it = lane / LPI, part = lane % LPI;
         constexpr int PARTS = F8 ? 2 : 2 * (D / 64);  // K and V (bf16: 64-dim halves)
         for (int k0 = 0; k0 < n_items; k0 += IPS) {
+            if (k0 >= a.stop_item) break;  // failure tests: the stages from here on are never armed
             if (k0 >= wbase + 32) {
                 wa = wb;
                 wb = wc;
@@ -383,7 +351,7 @@ __global__ void __launch_bounds__(DecodeCfg<D, F8, MULTI>::THREADS, 1)
             // the item's leader lane waits for its stage to be released, then arms it
             int ok = 1;
             if (live && part == 0) {
-                if (k >= S && !mbar_wait_bounded(empty_bar + st * 8, ((k / S) & 1) ^ 1, kWaitLimitNs)) {
+                if (k >= S && !mbar_wait_bounded(empty_bar + st * 8, ((k / S) & 1) ^ 1, a.wait_ns)) {
                     ok = 0;
                 } else {
                     info[st] = make_int2(MULTI ? j : seg, nv);  // MULTI: consumers mask per query row
@@ -429,11 +397,11 @@ __global__ void __launch_bounds__(DecodeCfg<D, F8, MULTI>::THREADS, 1)
         // gave up do not wait for them)
         if (lane == 0) {
             for (int k = max(0, issued - S); k < issued; ++k)
-                mbar_wait_bounded(full_bar + (k % S) * 8, (k / S) & 1, kWaitLimitNs);
+                mbar_wait_bounded(full_bar + (k % S) * 8, (k / S) & 1, a.wait_ns);
             for (int i = 0; i < IPS; ++i)
                 if (fail_armed & (1u << (LPI * i))) {
                     const int k = fail_step + i;
-                    mbar_wait_bounded(full_bar + (k % S) * 8, (k / S) & 1, kWaitLimitNs);
+                    mbar_wait_bounded(full_bar + (k % S) * 8, (k / S) & 1, a.wait_ns);
                 }
         }
         return;
@@ -447,7 +415,6 @@ __global__ void __launch_bounds__(DecodeCfg<D, F8, MULTI>::THREADS, 1)
     uint32_t qb[NKK][2];
     float acc[NKK][4];
     float m0, m1, l0, l1;
-    bool traced_first = false;
 
     // reset the running state and load query row qr's group of heads for
     // segment seg's KV head (qr < 0: zero queries)
@@ -579,7 +546,7 @@ __global__ void __launch_bounds__(DecodeCfg<D, F8, MULTI>::THREADS, 1)
     // the item's valid token count
     auto wait_full = [&](int k) -> int {
         if (flags[0]) return 0;
-        if (!mbar_wait_bounded(full_bar + (k % S) * 8, (k / S) & 1, kWaitLimitNs)) {
+        if (!mbar_wait_bounded(full_bar + (k % S) * 8, (k / S) & 1, a.wait_ns)) {
             if (lane == 0) {
                 flags[0] = 1;
                 atomicOr(a.status, kStatusTimeout);
@@ -738,7 +705,7 @@ __global__ void __launch_bounds__(DecodeCfg<D, F8, MULTI>::THREADS, 1)
     // combine); the other warps go straight on to the next segment.
     volatile int *arrive_cnt = flags + 1;  // warps that deposited the current instance
     volatile int *read_done = flags + 2;   // instances whose states the merger has read
-    auto merge = [&](int seg, int64_t s0, int64_t e0, bool whole, int inst, bool last_seg) {
+    auto merge = [&](int seg, int64_t s0, int64_t e0, bool whole, int inst) {
         l0 += __shfl_xor_sync(0xffffffffu, l0, 4);
         l0 += __shfl_xor_sync(0xffffffffu, l0, 8);
         l0 += __shfl_xor_sync(0xffffffffu, l0, 16);
@@ -749,7 +716,7 @@ __global__ void __launch_bounds__(DecodeCfg<D, F8, MULTI>::THREADS, 1)
         if (lane == 0 && *read_done < inst) {
             const uint64_t t0 = global_timer_ns();
             while (*read_done < inst) {
-                if (global_timer_ns() - t0 > kWaitLimitNs) {
+                if (global_timer_ns() - t0 > a.wait_ns) {
                     flags[0] = 1;
                     atomicOr(a.status, kStatusTimeout);
                     break;
@@ -791,7 +758,6 @@ __global__ void __launch_bounds__(DecodeCfg<D, F8, MULTI>::THREADS, 1)
         if (!merger) return;
 
         // ---- this warp merges the NC states
-        if (last_seg) PA_TRACE_LANE(5);
         // pieces of a split segment already counted (read while merging)
         int seen = 0;
         if (!whole && lane == 0) seen = ld_relaxed_s32(a.counters + seg);
@@ -846,7 +812,6 @@ __global__ void __launch_bounds__(DecodeCfg<D, F8, MULTI>::THREADS, 1)
                         ob[(h4 + e) * D + d] =
                             __bfloat16_as_ushort(__float2bfloat16_rn(Ls[e] > 0.f ? O[r][e] / Ls[e] : 0.f));
             }
-            if (last_seg) PA_TRACE_LANE(4);
             return;
         }
         // this CTA's piece, normalised, and its log2-sum-exp
@@ -868,14 +833,9 @@ __global__ void __launch_bounds__(DecodeCfg<D, F8, MULTI>::THREADS, 1)
             // segment: combine from registers, without publishing it. The
             // fence makes the counted pieces' partials visible to the loads.
             __threadfence();
-            if (last_seg) PA_TRACE_LANE(6);
             combine(int64_t(seg) + w0, 1, a.out + (int64_t(seg / Hkv) * a.Hq + (seg % Hkv) * G) * D, s0, e0,
                     int(blockIdx.x) - w0, lse, ox);
             if (lane == 0) a.counters[seg] = 0;
-            if (last_seg) {
-                PA_TRACE_LANE(7);
-                PA_TRACE_LANE(4);
-            }
             return;
         }
         float *ps = a.part + int64_t(seg + blockIdx.x) * C::PART;
@@ -896,15 +856,12 @@ __global__ void __launch_bounds__(DecodeCfg<D, F8, MULTI>::THREADS, 1)
         }
         last = __shfl_sync(0xffffffffu, last, 0);
         __syncwarp();  // every lane's reads of the pieces follow lane 0's acquire
-        if (last_seg) PA_TRACE_LANE(6);
         if (last) {
             const float nol[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
             combine(int64_t(seg) + w0, 1, a.out + (int64_t(seg / Hkv) * a.Hq + (seg % Hkv) * G) * D, s0, e0,
                     -1, nol, ox);
             if (lane == 0) a.counters[seg] = 0;
-            if (last_seg) PA_TRACE_LANE(7);
         }
-        if (last_seg) PA_TRACE_LANE(4);
     };
 
     // MULTI: end of a piece [s0, e0) of work-list segment seg for this
@@ -990,10 +947,6 @@ __global__ void __launch_bounds__(DecodeCfg<D, F8, MULTI>::THREADS, 1)
                 int nvb = (kb > ka) ? wait_full_j(kb, jb) : 0;
                 nva = act ? min(nva, max(lim - ja * BS, 0)) : 0;
                 nvb = act ? min(nvb, max(lim - jb * BS, 0)) : 0;
-                if (!traced_first) {
-                    traced_first = true;
-                    if (c_id == 0) PA_TRACE(2);
-                }
                 if (nva > 0 || nvb > 0) step(ka, nva, kb, nvb);
                 __syncwarp();
                 if (lane == 0) {
@@ -1034,10 +987,6 @@ __global__ void __launch_bounds__(DecodeCfg<D, F8, MULTI>::THREADS, 1)
             const int kb = min(2 * q + 1, ks1 - 1);
             const int nva = wait_full(ka);
             const int nvb = (kb > ka) ? wait_full(kb) : 0;
-            if (!traced_first) {
-                traced_first = true;
-                if (c_id == 0) PA_TRACE(2);
-            }
             if (nva > 0 || nvb > 0) step(ka, nva, kb, nvb);
             __syncwarp();
             if (lane == 0) {
@@ -1046,8 +995,7 @@ __global__ void __launch_bounds__(DecodeCfg<D, F8, MULTI>::THREADS, 1)
             }
         }
         const bool whole = (s0 >= pos0) && (e0 <= pos1);
-        if (e0 >= pos1) PA_TRACE(3);
-        merge(seg, s0, e0, whole, inst++, e0 >= pos1);
+        merge(seg, s0, e0, whole, inst++);
         p = min(e0, pos1);
         if (++kvh == Hkv) {
             kvh = 0;
@@ -1157,7 +1105,7 @@ cudaError_t decode_geometry(int head_dim, DecodeGeometry *g, bool fp8) {
     return cudaSuccess;
 }
 
-size_t decode_trace_offset(int B, int Hkv, int head_dim, int workers) {
+size_t decode_workspace_bytes(int B, int Hkv, int head_dim, int workers) {
     const size_t segs = size_t(B) * Hkv;
     const size_t head = 256;                                        // status word + padding
     const size_t counters = (segs * 4 + 255) / 256 * 256;
@@ -1170,19 +1118,7 @@ size_t decode_multi_workspace_bytes(int total_q, int Hkv, int head_dim, int work
     const int RG = kMultiRowGroup;
     const size_t segs = size_t(total_q) * Hkv;
     const size_t counters = (segs * RG * 4 + 255) / 256 * 256;
-    size_t bytes = 256 + counters + (segs + size_t(workers)) * RG * size_t(head_dim * 8 + 8) * 4;
-#ifdef PA_DECODE_TRACE
-    bytes += size_t(workers) * 16 * sizeof(uint64_t);
-#endif
-    return bytes;
-}
-
-size_t decode_workspace_bytes(int B, int Hkv, int head_dim, int workers) {
-    size_t bytes = decode_trace_offset(B, Hkv, head_dim, workers);
-#ifdef PA_DECODE_TRACE
-    bytes += size_t(workers) * 16 * sizeof(uint64_t);
-#endif
-    return bytes;
+    return 256 + counters + (segs + size_t(workers)) * RG * size_t(head_dim * 8 + 8) * 4;
 }
 
 cudaError_t launch_decode(const CUtensorMap &tm_k, const CUtensorMap &tm_v, const DecodeArgs &a,

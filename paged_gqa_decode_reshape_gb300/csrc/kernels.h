@@ -29,7 +29,9 @@ struct DecodeArgs {
     float *part;                // [B*Hkv + W][D*8 + 8] partial outputs and lse (log2 domain)
     int32_t *counters;          // [B*Hkv] arrival counters (zero between calls)
     int32_t *status;            // workspace status word
-    uint64_t *trace;            // per-warp timeline (tuning builds only), or null
+    uint64_t wait_ns;           // limit of every bounded wait inside the kernel (ns)
+    int stop_item;              // the producer stops issuing at this item of its CTA's range
+                                // (failure tests only; INT_MAX otherwise)
     int64_t NB;
     int MBS, topk, B, Hq, Hkv, G;
     float scale_log2;           // softmax scale * log2(e)
@@ -47,7 +49,6 @@ struct DecodeGeometry {
 cudaError_t decode_geometry(int head_dim, DecodeGeometry *g, bool fp8 = false);
 size_t decode_workspace_bytes(int B, int Hkv, int head_dim, int workers);
 size_t decode_multi_workspace_bytes(int total_q, int Hkv, int head_dim, int workers);
-size_t decode_trace_offset(int B, int Hkv, int head_dim, int workers);
 cudaError_t launch_decode(const CUtensorMap &tm_k, const CUtensorMap &tm_v, const DecodeArgs &a,
                           int head_dim, bool sparse, cudaStream_t stream, bool fp8 = false);
 
