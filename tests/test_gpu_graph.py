@@ -2,14 +2,15 @@
 and Quest sparse decode -- captured in one CUDA graph. Replaying the graph
 must give the same bytes as calling the entry points one by one: caches,
 metadata, both attention outputs and the selection. The step launches with
-programmatic dependent launch, so the capture also records those edges."""
+programmatic dependent launch, so the capture also records those edges. The
+replayed results are also checked against the CPU oracle."""
 
 import numpy as np
 import pytest
 import torch
 
 import workloads
-from tests.gpu_util import DeviceStep
+from tests.gpu_util import DeviceStep, OracleStep, assert_close_attention, to_host_f64, to_host_u16
 
 pytestmark = pytest.mark.gpu
 
@@ -64,6 +65,28 @@ def _reset(dev, s0):
     dev.sel.fill_(-7)
 
 
+def _check_against_oracle(dev, w):
+    """The replayed step's results against the CPU oracle run on the same
+    pre-step state: caches and metadata byte for byte, the selection bit for
+    bit (and against the plain score's top-K), both attention outputs within
+    the tolerances."""
+    import oracle
+    ora = OracleStep(w)
+    pre_ctx = (w.context_lens - 1).clip(0).astype(np.int32)
+    kmin, kmax = oracle.quest_rebuild_meta(ora.kc, w.block_tables, pre_ctx)
+    ora.reshape()
+    oracle.quest_update_meta(kmin, kmax, w.key, w.slot_mapping, w.BS)
+    np.testing.assert_array_equal(to_host_u16(dev.kc), ora.kc)
+    np.testing.assert_array_equal(to_host_u16(dev.vc), ora.vc)
+    np.testing.assert_array_equal(to_host_u16(dev.kmin), kmin)
+    np.testing.assert_array_equal(to_host_u16(dev.kmax), kmax)
+    sel = dev.sel.cpu().numpy()
+    np.testing.assert_array_equal(sel, ora.select(kmin, kmax))
+    ora.check_plain(sel, kmin, kmax, what=f"{w.name} replayed selection vs plain scores")
+    assert_close_attention(to_host_f64(dev.out), ora.dense(), f"{w.name} replayed dense")
+    assert_close_attention(to_host_f64(dev.out_sparse), ora.sparse(sel), f"{w.name} replayed sparse")
+
+
 @pytest.mark.parametrize("case", list(CASES))
 def test_graph_replay_is_bit_identical_to_eager(case):
     from paged_gqa_decode_reshape_gb300 import pa_workspace_status, quest_rebuild_meta
@@ -98,6 +121,7 @@ def test_graph_replay_is_bit_identical_to_eager(case):
         for n, t, e in zip(names, _outputs(dev), eager):
             assert torch.equal(_bits(t), e), f"replay {rep}: {n} differs from the eager step"
     assert pa_workspace_status(dev.ws) == 0
+    _check_against_oracle(dev, w)
     # the workspaces are left as the next call expects them: eager after replay
     _reset(dev, s0)
     for c in calls:

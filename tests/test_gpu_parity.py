@@ -105,8 +105,10 @@ def test_sparse_on_fixed_selection(case):
 
 @pytest.mark.parametrize("name", ["dense_b32", "quest_8k", "long_40k", "mixed_b128"])
 def test_full_size(name):
+    """Full sizes, in the benchmark's launch configuration: every cache and
+    metadata byte, every score and selection, every attention row."""
     w = workloads.make(name)
-    run_full_compare(w, sample=48, seed=11)
+    run_full_compare(w)
 
 
 def test_update_meta_incremental_bit_exact():
@@ -251,10 +253,14 @@ def test_fused_write_path_equals_separate_calls(name, kw):
     from paged_gqa_decode_reshape_gb300 import quest_rebuild_meta, quest_reshape_and_cache
     w = workloads.make(name, **kw)
     dev, ora = DeviceStep(w), OracleStep(w)
-    pre_ctx = torch.from_numpy((w.context_lens - 1).astype(np.int32)).to(dev.dev)
-    quest_rebuild_meta(dev.kmin, dev.kmax, dev.kc, dev.bt, pre_ctx)
-    kmin = to_host_u16(dev.kmin).copy()
-    kmax = to_host_u16(dev.kmax).copy()
+    # metadata of the cache as it stood before the step's tokens, on both sides
+    # from the same cache (the oracle's own rebuild seeds the oracle's update)
+    pre_ctx_h = (w.context_lens - 1).clip(0).astype(np.int32)
+    quest_rebuild_meta(dev.kmin, dev.kmax, dev.kc, dev.bt, torch.from_numpy(pre_ctx_h).to(dev.dev))
+    kmin, kmax = oracle.quest_rebuild_meta(ora.kc, w.block_tables, pre_ctx_h)
+    # (blocks outside every sequence's context stay zero on both sides)
+    np.testing.assert_array_equal(to_host_u16(dev.kmin), kmin)
+    np.testing.assert_array_equal(to_host_u16(dev.kmax), kmax)
     quest_reshape_and_cache(dev.key, dev.value, dev.kc, dev.vc, dev.kmin, dev.kmax, dev.slots)
     ora.reshape()
     oracle.quest_update_meta(kmin, kmax, w.key, w.slot_mapping, w.BS)

@@ -3,13 +3,16 @@ calls on one stream. On two streams the Quest selection and sparse decode
 run beside the dense decode, and each decode call has its own workspace.
 Every kernel's output is a deterministic function of its inputs (the split-KV
 combine merges the pieces in a fixed order), so running calls at the same
-time may change timing but never a bit of the results."""
+time may change timing but never a bit of the results. The results are
+also checked against the CPU oracle (bf16 cache)."""
 
+import numpy as np
 import pytest
 import torch
 
 import bench
 import workloads
+from tests.gpu_util import OracleStep, assert_close_attention, to_host_f64
 
 pytestmark = pytest.mark.gpu
 
@@ -20,6 +23,20 @@ def _cuda():
         pytest.skip("needs a CUDA GPU")
     import paged_gqa_decode_reshape_gb300.build as b
     b.build()
+
+
+def _check_against_oracle(st, w):
+    """The step's results (the last, two-stream run) against the CPU oracle:
+    the selection bit for bit and against the plain score's top-K, both
+    attention outputs within the tolerances."""
+    ora = OracleStep(w)
+    ora.reshape()
+    kmin, kmax = ora.rebuild_meta()
+    sel = st.sel.cpu().numpy()
+    np.testing.assert_array_equal(sel, ora.select(kmin, kmax))
+    ora.check_plain(sel, kmin, kmax, what=f"{w.name} two-stream selection vs plain scores")
+    assert_close_attention(to_host_f64(st.out), ora.dense(), f"{w.name} two-stream dense")
+    assert_close_attention(to_host_f64(st.out_sparse), ora.sparse(sel), f"{w.name} two-stream sparse")
 
 
 @pytest.mark.parametrize("name,kw,kv", [
@@ -40,6 +57,8 @@ def test_two_stream_step_matches_one_stream(name, kw, kv):
         results.append(st.out_buf.clone())
     for r in results[1:]:
         assert torch.equal(r, results[0])
+    if kv == "bf16":
+        _check_against_oracle(st, w)
     # the workspaces are left clean after both orders
     assert int(st.ws[:4].view(torch.int32)[0]) == 0
     assert int(st.ws_sparse[:4].view(torch.int32)[0]) == 0
