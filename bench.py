@@ -38,12 +38,13 @@ if HERE not in sys.path:
 METRIC = "decode-attn KV GB/s & % HBM roofline; µs/step dense vs Quest at 8K/40K ctx"
 UNIT = "GB/s"
 L2_FLUSH_BYTES = 512 << 20
+NOMINAL_HBM_GBS = 8000.0  # the GB300's ~8 TB/s HBM3e peak (nominal)
 
 
 def parse():
     p = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=50)
+    p.add_argument("--steps", type=int, default=200)
     p.add_argument("--warmup", type=int, default=10)
     p.add_argument("--impl", choices=["native", "reference"], default="native")
     p.add_argument("--workload", default="quest_8k",
@@ -57,6 +58,8 @@ def parse():
                    help="run the step's calls one after another on one stream (default: the Quest "
                         "selection and sparse decode on a second stream, alongside the dense decode)")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-long-point", action="store_true",
+                   help="skip the 40K-context point (long_40k) that the default quest_8k line also reports")
     p.add_argument("--cpu-budget", type=float, default=12.0,
                    help="seconds of oracle work for the CPU baseline sample")
     return p.parse_args()
@@ -294,100 +297,89 @@ STEP_ORDER = [0, 2, 1, 3]
 # -------------------------------------------------------------- CPU oracle
 
 
-def oracle_sample(w, budget_s: float, kv: str = "bf16", qlen: int = 1):
-    """The oracle on a bounded sample of the step: the write path for every
-    token, then whole sequences (dense attention for all heads, Quest scores
-    and top-K for all KV heads, sparse attention for all heads) until the
-    time budget is spent. Returns (algorithmic bytes, seconds, sequences)."""
-    import oracle
-    from paged_gqa_decode_reshape_gb300 import ledger
-    if kv == "fp8":
-        return oracle_sample_fp8(w, budget_s)
-    kc, vc = w.key_cache, w.value_cache       # the oracle writes in place: state after the step
-    t0 = time.perf_counter()
-    oracle.reshape_and_cache(w.key, w.value, kc, vc, w.slot_mapping)
-    kmin = np.zeros((w.NB, w.Hkv, w.D), dtype=np.uint16)
-    kmax = np.zeros_like(kmin)
-    # the metadata of the pre-existing cache is setup on both sides (not timed)
-    t_setup0 = time.perf_counter()
-    oracle.quest_rebuild_meta(kc, w.block_tables, w.context_lens, kmin, kmax)
-    t_setup = time.perf_counter() - t_setup0
-    oracle.quest_update_meta(kmin, kmax, w.key, w.slot_mapping, w.BS)
-    nbytes = ledger.step_bytes(w.context_lens, w.slot_mapping, w.Hq, w.Hkv, w.D, w.BS, w.topk)
-    done_bytes = nbytes.reshape + nbytes.meta
-    seqs = 0
-    if qlen > 1:  # the same query rows the GPU step attends with (Step: seed 1234)
+class OracleSampler:
+    """The oracle on bounded samples of the step. Set-up (not timed): the
+    8-bit pool quantised once for --kv fp8, and the Quest metadata of the
+    cache as it stands. A sample: the write path for every token (the writes
+    and the metadata update are idempotent, so every sample starts from the
+    same state), then whole sequences -- dense attention for all heads, Quest
+    scores and top-K for all KV heads, sparse attention for all heads -- from
+    a rotating cursor until the time budget is spent (at least one)."""
+
+    def __init__(self, w, kv: str = "bf16", qlen: int = 1):
+        import oracle
         import workloads
-        rng = np.random.default_rng(1234)
-        qm = workloads.f32_to_bf16_bits(rng.standard_normal((w.B * qlen, w.Hq, w.D)).astype(np.float32))
-        cu = np.arange(0, w.B * qlen + 1, qlen, dtype=np.int32)
-    for b in range(w.B):
-        if time.perf_counter() - t0 - t_setup > budget_s and seqs > 0:
-            break
-        rows = np.array([(b, h) for h in range(w.Hq)], dtype=np.int32)
-        if qlen > 1:
-            mrows = np.array([(r, h) for r in range(b * qlen, (b + 1) * qlen) for h in range(w.Hq)],
-                             dtype=np.int32)
-            oracle.paged_attention_multi(qm, kc, vc, w.block_tables, cu, w.context_lens, w.scale, rows=mrows)
+        self.oracle, self.w, self.kv, self.qlen = oracle, w, kv, qlen
+        self.cursor = 0
+        self.fp8 = kv == "fp8"
+        if self.fp8:
+            self.ks, self.vs = workloads.fp8_scales(w.Hkv)
+            NB, BS = w.NB, w.BS
+            self.kc = np.zeros((NB, BS, w.Hkv, w.D), dtype=np.uint8)
+            self.vc = np.zeros((NB, w.Hkv, w.D, BS), dtype=np.uint8)
+            oracle.reshape_and_cache_fp8(w.key_cache.reshape(NB * BS, w.Hkv, w.D),
+                                         w.value_cache.reshape(NB * BS, w.Hkv, w.D), self.kc, self.vc,
+                                         np.arange(NB * BS, dtype=np.int64), self.ks, self.vs)
+            self.kmin, self.kmax = oracle.quest_rebuild_meta_fp8(self.kc, w.block_tables, w.context_lens)
         else:
-            oracle.paged_attention(w.q, kc, vc, w.block_tables, w.context_lens, w.scale, rows=rows)
-        sc = oracle.quest_scores(w.q[b:b + 1], kmin, kmax, w.block_tables[b:b + 1],
-                                 w.context_lens[b:b + 1], w.BS)
-        sel = oracle.quest_topk(sc, w.context_lens[b:b + 1], w.BS, w.topk)
-        full_sel = np.full((w.B, w.Hkv, w.topk), -1, dtype=np.int32)
-        full_sel[b] = sel[0]
-        oracle.sparse_attention(w.q, kc, vc, w.block_tables, w.context_lens, full_sel, w.scale,
-                                rows=rows)
-        one = ledger.step_bytes(w.context_lens[b:b + 1], np.zeros(0, np.int64), w.Hq, w.Hkv, w.D,
-                                w.BS, w.topk, selected=sel, q_rows=qlen)
-        done_bytes += one.dense + one.select + one.sparse
-        seqs += 1
-    elapsed = time.perf_counter() - t0 - t_setup
-    return done_bytes, elapsed, seqs
+            self.kc, self.vc = w.key_cache, w.value_cache   # written in place: the state after the step
+            self.kmin, self.kmax = oracle.quest_rebuild_meta(self.kc, w.block_tables, w.context_lens)
+        if qlen > 1:  # the same query rows the GPU step attends with (Step: seed 1234)
+            rng = np.random.default_rng(1234)
+            self.qm = workloads.f32_to_bf16_bits(
+                rng.standard_normal((w.B * qlen, w.Hq, w.D)).astype(np.float32))
+            self.cu = np.arange(0, w.B * qlen + 1, qlen, dtype=np.int32)
 
-
-def oracle_sample_fp8(w, budget_s: float):
-    """oracle_sample over an 8-bit cache: the pool quantised once (setup, not
-    timed), then the 8-bit write path for every token and whole sequences of
-    8-bit dense attention, Quest selection and sparse attention."""
-    import oracle
-    import workloads
-    from paged_gqa_decode_reshape_gb300 import ledger
-    ks, vs = workloads.fp8_scales(w.Hkv)
-    NB, BS = w.NB, w.BS
-    t_setup0 = time.perf_counter()
-    kc = np.zeros((NB, BS, w.Hkv, w.D), dtype=np.uint8)
-    vc = np.zeros((NB, w.Hkv, w.D, BS), dtype=np.uint8)
-    oracle.reshape_and_cache_fp8(w.key_cache.reshape(NB * BS, w.Hkv, w.D),
-                                 w.value_cache.reshape(NB * BS, w.Hkv, w.D), kc, vc,
-                                 np.arange(NB * BS, dtype=np.int64), ks, vs)
-    kmin, kmax = oracle.quest_rebuild_meta_fp8(kc, w.block_tables, w.context_lens)
-    t_setup = time.perf_counter() - t_setup0
-    t0 = time.perf_counter()
-    oracle.reshape_and_cache_fp8(w.key, w.value, kc, vc, w.slot_mapping, ks, vs)
-    oracle.quest_update_meta_fp8(kmin, kmax, w.key, w.slot_mapping, ks, w.BS)
-    nbytes = ledger.step_bytes(w.context_lens, w.slot_mapping, w.Hq, w.Hkv, w.D, w.BS, w.topk,
-                               elem_bytes=1)
-    done_bytes = nbytes.reshape + nbytes.meta
-    seqs = 0
-    for b in range(w.B):
-        if time.perf_counter() - t0 > budget_s and seqs > 0:
-            break
-        rows = np.array([(b, h) for h in range(w.Hq)], dtype=np.int32)
-        oracle.attention_fp8(w.q, kc, vc, ks, vs, w.block_tables, w.context_lens, w.scale, rows=rows)
-        sc = oracle.quest_scores_fp8(w.q[b:b + 1], kmin, kmax, w.block_tables[b:b + 1],
-                                     w.context_lens[b:b + 1], w.BS)
-        sel = oracle.quest_topk(sc, w.context_lens[b:b + 1], w.BS, w.topk)
-        full_sel = np.full((w.B, w.Hkv, w.topk), -1, dtype=np.int32)
-        full_sel[b] = sel[0]
-        oracle.attention_fp8(w.q, kc, vc, ks, vs, w.block_tables, w.context_lens, w.scale,
-                             selected=full_sel, rows=rows)
-        one = ledger.step_bytes(w.context_lens[b:b + 1], np.zeros(0, np.int64), w.Hq, w.Hkv, w.D,
-                                w.BS, w.topk, selected=sel, elem_bytes=1)
-        done_bytes += one.dense + one.select + one.sparse
-        seqs += 1
-    del t_setup
-    return done_bytes, time.perf_counter() - t0, seqs
+    def sample(self, budget_s: float):
+        """Returns (algorithmic bytes, seconds, sequences) of one sample."""
+        from paged_gqa_decode_reshape_gb300 import ledger
+        o, w, eb = self.oracle, self.w, 1 if self.fp8 else 2
+        t0 = time.perf_counter()
+        if self.fp8:
+            o.reshape_and_cache_fp8(w.key, w.value, self.kc, self.vc, w.slot_mapping, self.ks, self.vs)
+            o.quest_update_meta_fp8(self.kmin, self.kmax, w.key, w.slot_mapping, self.ks, w.BS)
+        else:
+            o.reshape_and_cache(w.key, w.value, self.kc, self.vc, w.slot_mapping)
+            o.quest_update_meta(self.kmin, self.kmax, w.key, w.slot_mapping, w.BS)
+        nbytes = ledger.step_bytes(w.context_lens, w.slot_mapping, w.Hq, w.Hkv, w.D, w.BS, w.topk,
+                                   elem_bytes=eb)
+        done_bytes = nbytes.reshape + nbytes.meta
+        seqs = 0
+        while seqs < w.B and (seqs == 0 or time.perf_counter() - t0 <= budget_s):
+            b = self.cursor
+            self.cursor = (self.cursor + 1) % w.B
+            rows = np.array([(b, h) for h in range(w.Hq)], dtype=np.int32)
+            sl = slice(b, b + 1)
+            if self.fp8:
+                o.attention_fp8(w.q, self.kc, self.vc, self.ks, self.vs, w.block_tables, w.context_lens,
+                                w.scale, rows=rows)
+                sc = o.quest_scores_fp8(w.q[sl], self.kmin, self.kmax, w.block_tables[sl],
+                                        w.context_lens[sl], w.BS)
+            else:
+                if self.qlen > 1:
+                    mrows = np.array([(r, h) for r in range(b * self.qlen, (b + 1) * self.qlen)
+                                      for h in range(w.Hq)], dtype=np.int32)
+                    o.paged_attention_multi(self.qm, self.kc, self.vc, w.block_tables, self.cu,
+                                            w.context_lens, w.scale, rows=mrows)
+                else:
+                    o.paged_attention(w.q, self.kc, self.vc, w.block_tables, w.context_lens, w.scale,
+                                      rows=rows)
+                sc = o.quest_scores(w.q[sl], self.kmin, self.kmax, w.block_tables[sl], w.context_lens[sl],
+                                    w.BS)
+            sel = o.quest_topk(sc, w.context_lens[sl], w.BS, w.topk)
+            full_sel = np.full((w.B, w.Hkv, w.topk), -1, dtype=np.int32)
+            full_sel[b] = sel[0]
+            if self.fp8:
+                o.attention_fp8(w.q, self.kc, self.vc, self.ks, self.vs, w.block_tables, w.context_lens,
+                                w.scale, selected=full_sel, rows=rows)
+            else:
+                o.sparse_attention(w.q, self.kc, self.vc, w.block_tables, w.context_lens, full_sel, w.scale,
+                                   rows=rows)
+            one = ledger.step_bytes(w.context_lens[sl], np.zeros(0, np.int64), w.Hq, w.Hkv, w.D, w.BS,
+                                    w.topk, selected=sel, q_rows=self.qlen, elem_bytes=eb)
+            done_bytes += one.dense + one.select + one.sparse
+            seqs += 1
+        return done_bytes, time.perf_counter() - t0, seqs
 
 
 # -------------------------------------------------------------------- main
@@ -462,58 +454,70 @@ def run_reference(args, world, rank, pgroup):
         return 0
     w0 = workloads.make(args.workload, poison=False)
     cores = 1
-    times, nbytes = [], []
+    times, nbytes, seq_counts = [], [], []
+    sampler = OracleSampler(w0, args.kv, args.qlen)
     for i in range(args.warmup + args.steps):
         # the oracle's writes are idempotent, so every step reuses the same inputs
-        b, s, seqs = oracle_sample(w0, args.cpu_budget / max(1, args.steps + args.warmup), args.kv, args.qlen)
+        b, s, seqs = sampler.sample(args.cpu_budget / max(1, args.steps + args.warmup))
         if i >= args.warmup:
             times.append(s)
             nbytes.append(b)
+            seq_counts.append(seqs)
     value = sum(nbytes) / sum(times) / 1e9
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": 1e3 * sum(times) / len(times),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "impl": "reference",
-        "config": {"workload": args.workload, "kv_cache": args.kv,
-                   "sample": "per step: the write path for every token, "
-                   "then whole sequences in order until the step's time share is spent"},
+        "config": config_of(w0, args, world),
+        "timing": "per step: the oracle on a bounded sample of the step (the write path for every "
+                  "token, then whole sequences from a rotating cursor until the step's time share is "
+                  "spent); value = sampled algorithmic bytes / sampled CPU seconds",
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
-                         "sample": f"{args.steps} steps of a bounded sample of {args.workload}"},
+                         "sample": f"{args.steps} steps of a bounded sample of {args.workload}: "
+                                   f"{sum(seq_counts)} sequences of {w0.B} in all, "
+                                   f"{sum(times):.1f} s of CPU time"},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line))
     return 0
 
 
-def main():
-    args = parse()
-    world, rank, local, pgroup = dist_setup(args)
-    if args.impl == "reference":
-        return run_reference(args, world, rank, pgroup)
+def config_of(w, args, world: int) -> dict:
+    """The workload a line measures (the same for the native and the reference arm)."""
+    fp8 = args.kv == "fp8"
+    return {
+        "workload": args.workload, "batch": w.B, "num_q_heads": w.Hq, "num_kv_heads": w.Hkv,
+        "head_dim": w.D, "block_size": w.BS, "topk_blocks": w.topk, "kv_cache": args.kv,
+        "query_rows_per_sequence": args.qlen,
+        "context_lens_mean": round(float(w.context_lens.mean()), 1),
+        "context_lens_max": int(w.context_lens.max()), "pool_blocks": w.NB,
+        "kv_pool_bytes": int(2 * w.key_cache.nbytes // (2 if fp8 else 1)),
+        "step": ("quest_reshape_and_cache{0} (ReshapeAndCache + metadata update) + "
+                 "quest_select_topk{0} + pa_decode{0} + quest_sparse_decode{0}").format("_fp8" if fp8 else ""),
+        "l2": "inputs resident; L2 flushed before every timed sample",
+        "parallelism": f"replicas x{world}",
+    }
 
-    import torch
-    import paged_gqa_decode_reshape_gb300 as pg
-    import paged_gqa_decode_reshape_gb300.build as pgb
-    import workloads
+
+def stats_ms(samples) -> dict:
+    a = np.asarray(samples, dtype=np.float64)
+    return {"median": round(float(np.median(a)), 5), "min": round(float(a.min()), 5),
+            "mean": round(float(a.mean()), 5), "samples": int(a.size)}
+
+
+def measure(torch, pg, w, dev, args, flush, pgroup):
+    """Time one workload: pass A (whole steps, one event pair each), pass B
+    (one stream, an event between calls), pass C (graph replay) and the end
+    to end pass. Every timed sample is preceded by an L2 flush outside its
+    events. Returns the raw per-sample times (ms) and the step's byte ledger."""
     from paged_gqa_decode_reshape_gb300 import ledger
-
-    if not torch.cuda.is_available():
-        raise SystemExit("bench.py needs a CUDA GPU (the native path has no CPU fallback)")
-    pgb.build()
-    pg.load_library()
-    dev = torch.device("cuda", local)
-    torch.cuda.set_device(dev)
-    w = workloads.make(args.workload, poison=False)
-    if args.qlen > 1 and (args.kv != "bf16" or w.B * args.qlen > 2048):
-        raise SystemExit("--qlen > 1: bf16 cache and at most 2048 query rows")
     step = Step(w, dev, args.kv, args.qlen)
     calls = [step.calls()[k] for k in STEP_ORDER]  # launch order
     stream = torch.cuda.current_stream(dev)
     run_step = step_runner(torch, step.calls(), args.serial)
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    K = args.steps
 
-    # warm-up (untimed)
     for _ in range(max(3, args.warmup)):
         run_step()
     torch.cuda.synchronize(dev)
@@ -522,12 +526,11 @@ def main():
     nb = ledger.step_bytes(w.context_lens, w.slot_mapping, w.Hq, w.Hkv, w.D, w.BS, w.topk,
                            selected=sel_host, elem_bytes=1 if fp8 else 2, q_rows=args.qlen)
 
-    # Pass A (the timed region): whole steps, one event pair per step, L2
-    # flushed before each step outside the events. Kernels launch with
-    # programmatic stream serialization, so consecutive launches overlap their
-    # start-up with the previous kernel's tail; the Quest selection and sparse
-    # decode run beside the dense decode on a second stream (step_runner).
-    K = args.steps
+    # Pass A (the timed region): whole steps, one event pair per step.
+    # Kernels launch with programmatic stream serialization, so consecutive
+    # launches overlap their start-up with the previous kernel's tail; the
+    # Quest selection and sparse decode run beside the dense decode on a
+    # second stream (step_runner).
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
     sampler = ClockSampler(gpu_id_for(torch, dev))
     if pgroup:
@@ -544,12 +547,11 @@ def main():
     torch.cuda.synchronize(dev)
     wall = time.perf_counter() - wall0
     clocks = sampler.stop()
-    step_ms = np.array([e0.elapsed_time(e1) for e0, e1 in ev])
-    local_ms = float(step_ms.mean())
+    step_ms = [e0.elapsed_time(e1) for e0, e1 in ev]
 
     # Pass B: the same steps on one stream with an event between consecutive
-    # calls, for the per-call breakdown and the decode kernel's roofline (the
-    # extra events keep each call's launch gap inside its own interval).
+    # calls, for the per-call breakdown and the decode kernels' rooflines
+    # (the extra events keep each call's launch gap inside its own interval).
     evb = [[torch.cuda.Event(enable_timing=True) for _ in range(len(calls) + 1)] for _ in range(K)]
     for i in range(K):
         flush.fill_(i & 0xFF)
@@ -562,9 +564,7 @@ def main():
                          for i in range(K)])              # ms, launch order
     per_call = per_call[:, np.argsort(STEP_ORDER)]       # ms, in CALL_NAMES order
 
-    # Pass C: the same step captured once in a CUDA graph and replayed (L2
-    # flushed before each replay, outside the events); reported on its own
-    # beside the eager numbers above.
+    # Pass C: the step captured once in a CUDA graph and replayed.
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph):
         run_step()
@@ -578,7 +578,7 @@ def main():
         graph.replay()
         evc[i][1].record(stream)
     torch.cuda.synchronize(dev)
-    graph_ms = float(np.mean([e0.elapsed_time(e1) for e0, e1 in evc]))
+    graph_ms = [e0.elapsed_time(e1) for e0, e1 in evc]
 
     # end to end through the C ABI with host buffers: H2D of the step's inputs
     # (q, new K/V rows, slots, block tables, context lengths: one pinned
@@ -586,8 +586,6 @@ def main():
     # every step
     h_in = step.in_buf.cpu().pin_memory()
     h_out = torch.empty_like(step.out_buf, device="cpu").pin_memory()
-    h2d = h_in.numel()
-    d2h = h_out.numel()
     e2e_ms = []
     for i in range(K):
         flush.fill_(i & 0xFF)
@@ -599,23 +597,84 @@ def main():
         e1.record(stream)
         e1.synchronize()
         e2e_ms.append(e0.elapsed_time(e1))
-    e2e_local = float(np.mean(e2e_ms))
+    del graph, step
+    torch.cuda.synchronize(dev)
+    return dict(nb=nb, step_ms=step_ms, per_call=per_call, graph_ms=graph_ms, e2e_ms=e2e_ms,
+                h2d=int(h_in.numel()), d2h=int(h_out.numel()), clocks=clocks, wall=wall)
 
-    ms, e2e_ms_max, graph_ms_max = max_over_ranks([local_ms, e2e_local, graph_ms], pgroup)
 
+def call_summary(m, peak: float) -> dict:
+    """Per-call medians of pass B, their GB/s on the algorithmic bytes, and
+    the fraction of the measured copy peak and of the nominal ~8 TB/s."""
+    nb = m["nb"]
+    call_bytes = [nb.reshape + nb.meta, nb.dense, nb.select, nb.sparse]
+    med = np.median(m["per_call"], axis=0)
+    out = {}
+    for n, ms, b in zip(CALL_NAMES, med, call_bytes):
+        gbs = b / (ms * 1e-3) / 1e9
+        out[n] = {"us": round(float(ms) * 1e3, 2), "us_min": round(float(m["per_call"][:, CALL_NAMES.index(n)].min())
+                                                                  * 1e3, 2),
+                  "GBps": round(gbs, 1), "frac_of_measured_peak": round(gbs / peak, 3),
+                  "frac_of_nominal_8tbs": round(gbs / NOMINAL_HBM_GBS, 3), "bytes": int(b)}
+    return out
+
+
+def point_summary(m, peak: float, world: int) -> dict:
+    """The metric's "µs/step dense vs Quest" at one context length: per-call
+    medians (pass B), the dense step (write + dense decode) and the Quest step
+    (write + selection + sparse decode), and the whole step of pass A."""
+    calls = call_summary(m, peak)
+    dense_us = calls["write"]["us"] + calls["dense"]["us"]
+    quest_us = calls["write"]["us"] + calls["select"]["us"] + calls["sparse"]["us"]
+    return {
+        "dense_step_us": round(dense_us, 2), "quest_step_us": round(quest_us, 2),
+        "dense_decode": calls["dense"], "sparse_decode": calls["sparse"], "select": calls["select"],
+        "write": calls["write"],
+        "whole_step_us": stats_ms(np.asarray(m["step_ms"]) * 1e3),
+        "whole_step_GBps": round(job_throughput(world, m["nb"].total, float(np.median(m["step_ms"]))), 1),
+    }
+
+
+def main():
+    args = parse()
+    world, rank, local, pgroup = dist_setup(args)
+    if args.impl == "reference":
+        return run_reference(args, world, rank, pgroup)
+
+    import torch
+    import paged_gqa_decode_reshape_gb300 as pg
+    import paged_gqa_decode_reshape_gb300.build as pgb
+    import workloads
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU (the native path has no CPU fallback)")
+    pgb.build()
+    pg.load_library()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    w = workloads.make(args.workload, poison=False)
+    if args.qlen > 1 and (args.kv != "bf16" or w.B * args.qlen > 2048):
+        raise SystemExit("--qlen > 1: bf16 cache and at most 2048 query rows")
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    K = args.steps
+    fp8 = args.kv == "fp8"
+    peak, peak_kind = measured_peaks()
+
+    m = measure(torch, pg, w, dev, args, flush, pgroup)
+    # the metric's second context length, from the same run (one replica)
+    m40 = None
+    if args.workload == "quest_8k" and args.qlen == 1 and not args.no_long_point:
+        m40 = measure(torch, pg, workloads.make("long_40k", poison=False), dev, args, flush, pgroup)
+
+    mine = [float(np.median(m["step_ms"])), float(np.median(m["e2e_ms"])), float(np.median(m["graph_ms"]))]
+    ms, e2e_ms_max, graph_ms_max = max_over_ranks(mine, pgroup)
     if rank != 0:
         return 0
 
-    call_ms = per_call.mean(axis=0)
-    call_bytes = [nb.reshape + nb.meta, nb.dense, nb.select, nb.sparse]
+    nb = m["nb"]
     value = job_throughput(world, nb.total, ms)
-    peak, peak_kind = measured_peaks()
-    dense_gbs = nb.dense / (call_ms[1] * 1e-3) / 1e9
-    breakdown = {n: {"us": round(float(m) * 1e3, 2), "GBps": round(b / (m * 1e-3) / 1e9, 1),
-                     "frac_of_peak": round(b / (m * 1e-3) / 1e9 / peak, 3), "bytes": int(b)}
-                 for n, m, b in zip(CALL_NAMES, call_ms, call_bytes)}
-    dense_us = float(call_ms[0] + call_ms[1]) * 1e3
-    quest_us = float(call_ms[0] + call_ms[2] + call_ms[3]) * 1e3
+    point = point_summary(m, peak, world)
+    dense = point["dense_decode"]
     line = {
         "metric": METRIC,
         "value": round(value, 2),
@@ -629,54 +688,59 @@ def main():
         "vs_baseline": None,
         "dtype": "e4m3 KV cache, bf16 q/out" if fp8 else "bf16",
         "data": "synthetic",
-        "config": {
-            "workload": args.workload, "batch": w.B, "num_q_heads": w.Hq, "num_kv_heads": w.Hkv,
-            "head_dim": w.D, "block_size": w.BS, "topk_blocks": w.topk, "kv_cache": args.kv,
-            "query_rows_per_sequence": args.qlen,
-            "context_lens_mean": round(float(w.context_lens.mean()), 1),
-            "context_lens_max": int(w.context_lens.max()), "pool_blocks": w.NB,
-            "kv_pool_bytes": int(2 * w.key_cache.nbytes // (2 if fp8 else 1)),
-            "step": ("quest_reshape_and_cache{0} (ReshapeAndCache + metadata update, one launch) + "
-                     "quest_select_topk{0} + pa_decode{0} + quest_sparse_decode{0}, in that order").format(
-                         "_fp8" if fp8 else ""),
-            "timing": ("value/ms_per_step: one event pair per step" +
-                       ("" if args.serial else ", the Quest selection and sparse decode on a second stream "
-                        "beside the dense decode") +
-                       "; breakdown/roofline: a second pass of the same steps on one stream with an event "
-                       "between calls"),
-            "l2": f"flushed before every step ({L2_FLUSH_BYTES >> 20} MiB write), outside the timed events",
-            "parallelism": f"replicas x{world}",
-        },
+        "config": config_of(w, args, world),
+        "timing": ("value/ms_per_step: median over the timed steps of one event pair per step" +
+                   ("" if args.serial else ", the Quest selection and sparse decode on a second stream "
+                    "beside the dense decode") +
+                   "; breakdown/roofline: medians of a second pass of the same steps on one stream with "
+                   "an event between calls; L2 flushed before every timed sample "
+                   f"({L2_FLUSH_BYTES >> 20} MiB write), outside the events"),
+        "step_ms_stats": stats_ms(m["step_ms"]),
         "roofline": {
             "bound": "hbm",
             "kernel": ("pa_decode_fp8" if fp8 else "pa_decode_multi" if args.qlen > 1 else "pa_decode")
                       + " (split-KV decode + fused combine, 1 launch)",
-            "achieved": round(dense_gbs, 1), "peak": peak, "unit": "GB/s",
-            "frac": round(dense_gbs / peak, 4), "peak_kind": peak_kind,
+            "achieved": dense["GBps"], "peak": peak, "unit": "GB/s",
+            "frac": round(dense["GBps"] / peak, 4), "peak_kind": peak_kind,
+            "frac_of_nominal_8tbs": round(dense["GBps"] / NOMINAL_HBM_GBS, 4),
             "traffic": (recorded_traffic("pa_decode_fp8" if fp8 else "pa_decode", args.workload)
                         if args.qlen == 1 else None),
             "algorithmic_bytes_per_launch": int(nb.dense),
+            "launch_us": {"median": dense["us"], "min": dense["us_min"]},
         },
-        "breakdown": breakdown,
+        "roofline_sparse": {
+            "bound": "hbm", "kernel": "quest_sparse_decode" + ("_fp8" if fp8 else ""),
+            "achieved": point["sparse_decode"]["GBps"], "peak": peak, "unit": "GB/s",
+            "frac": point["sparse_decode"]["frac_of_measured_peak"],
+            "frac_of_nominal_8tbs": point["sparse_decode"]["frac_of_nominal_8tbs"],
+            "algorithmic_bytes_per_launch": point["sparse_decode"]["bytes"],
+        },
+        "breakdown": {n: point[k] for n, k in (("write", "write"), ("dense", "dense_decode"),
+                                               ("select", "select"), ("sparse", "sparse_decode"))},
         "breakdown_steps": K,
-        "dense_us_per_step": round(dense_us, 2),
-        "quest_us_per_step": round(quest_us, 2),
+        "dense_us_per_step": point["dense_step_us"],
+        "quest_us_per_step": point["quest_step_us"],
         "dense_step": "write + pa_decode", "quest_step": "write + quest_select_topk + quest_sparse_decode",
-        "tokens_per_s": {"dense": round(world * w.B / (dense_us * 1e-6), 1),
-                         "quest": round(world * w.B / (quest_us * 1e-6), 1)},
+        "tokens_per_s": {"dense": round(world * w.B / (point["dense_step_us"] * 1e-6), 1),
+                         "quest": round(world * w.B / (point["quest_step_us"] * 1e-6), 1)},
         "e2e": {"value": round(job_throughput(world, nb.total, e2e_ms_max), 2), "unit": UNIT,
-                "ms_per_step": round(e2e_ms_max, 5), "h2d_bytes_per_step": int(h2d),
-                "d2h_bytes_per_step": int(d2h)},
+                "ms_per_step": round(e2e_ms_max, 5), "h2d_bytes_per_step": m["h2d"],
+                "d2h_bytes_per_step": m["d2h"], "ms_stats": stats_ms(m["e2e_ms"])},
         "graph": {"value": round(job_throughput(world, nb.total, graph_ms_max), 2), "unit": UNIT,
-                  "ms_per_step": round(graph_ms_max, 5),
+                  "ms_per_step": round(graph_ms_max, 5), "ms_stats": stats_ms(m["graph_ms"]),
                   "how": "the step's calls captured once in a CUDA graph, replayed K times"},
         "gpu_launches": int(K * sum(LAUNCHES_PER_CALL)),
-        "wall_s_timed_region": round(wall, 4),
-        "clocks": clocks,
+        "wall_s_timed_region": round(m["wall"], 4),
+        "clocks": m["clocks"],
     }
+    if m40 is not None:
+        line["context_points"] = {
+            "8K": dict(workload=args.workload, **point),
+            "40K": dict(workload="long_40k", **point_summary(m40, peak, world), clocks=m40["clocks"]),
+        }
     if world == 1 and not args.no_cpu_baseline:
-        wc = workloads.make(args.workload, poison=False)
-        b, s, seqs = oracle_sample(wc, args.cpu_budget, args.kv, args.qlen)
+        b, s, seqs = OracleSampler(workloads.make(args.workload, poison=False), args.kv,
+                                   args.qlen).sample(args.cpu_budget)
         line["cpu_baseline"] = {
             "value": round(b / s / 1e9, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
             "sample": f"write path for all {w.T} tokens + {seqs} of {w.B} sequences "
