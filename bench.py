@@ -38,6 +38,10 @@ if HERE not in sys.path:
 METRIC = "decode-attn KV GB/s & % HBM roofline; µs/step dense vs Quest at 8K/40K ctx"
 UNIT = "GB/s"
 L2_FLUSH_BYTES = 512 << 20
+# Before each device-timed sample a short spin kernel (outside the events)
+# lets the host enqueue the whole step before the GPU reaches it, so a
+# device-timed interval never waits on Python's launch overhead.
+HEAD_START_CYCLES = 400_000
 NOMINAL_HBM_GBS = 8000.0  # the GB300's ~8 TB/s HBM3e peak (nominal)
 
 
@@ -58,6 +62,8 @@ def parse():
                    help="run the step's calls one after another on one stream (default: the Quest "
                         "selection and sparse decode on a second stream, alongside the dense decode)")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-head-start", action="store_true",
+                   help="no spin kernel before each device-timed sample (the host may then lag the GPU)")
     p.add_argument("--no-long-point", action="store_true",
                    help="skip the 40K-context point (long_40k) that the default quest_8k line also reports")
     p.add_argument("--cpu-budget", type=float, default=12.0,
@@ -518,6 +524,10 @@ def measure(torch, pg, w, dev, args, flush, pgroup):
     run_step = step_runner(torch, step.calls(), args.serial)
     K = args.steps
 
+    def head_start():
+        if not args.no_head_start:
+            torch.cuda._sleep(HEAD_START_CYCLES)
+
     for _ in range(max(3, args.warmup)):
         run_step()
     torch.cuda.synchronize(dev)
@@ -541,6 +551,7 @@ def measure(torch, pg, w, dev, args, flush, pgroup):
     wall0 = time.perf_counter()
     for i in range(K):
         flush.fill_(i & 0xFF)
+        head_start()
         ev[i][0].record(stream)
         run_step()
         ev[i][1].record(stream)
@@ -555,6 +566,7 @@ def measure(torch, pg, w, dev, args, flush, pgroup):
     evb = [[torch.cuda.Event(enable_timing=True) for _ in range(len(calls) + 1)] for _ in range(K)]
     for i in range(K):
         flush.fill_(i & 0xFF)
+        head_start()
         evb[i][0].record(stream)
         for j, c in enumerate(calls):
             c()
@@ -574,6 +586,7 @@ def measure(torch, pg, w, dev, args, flush, pgroup):
     evc = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
     for i in range(K):
         flush.fill_(i & 0xFF)
+        head_start()
         evc[i][0].record(stream)
         graph.replay()
         evc[i][1].record(stream)
@@ -694,7 +707,10 @@ def main():
                     "beside the dense decode") +
                    "; breakdown/roofline: medians of a second pass of the same steps on one stream with "
                    "an event between calls; L2 flushed before every timed sample "
-                   f"({L2_FLUSH_BYTES >> 20} MiB write), outside the events"),
+                   f"({L2_FLUSH_BYTES >> 20} MiB write), outside the events" +
+                   ("" if args.no_head_start else
+                    f", then a {HEAD_START_CYCLES}-cycle spin kernel so the host has enqueued the step "
+                    "before the GPU reaches it (device-timed passes; the e2e pass has none)")),
         "step_ms_stats": stats_ms(m["step_ms"]),
         "roofline": {
             "bound": "hbm",
