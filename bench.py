@@ -3,8 +3,9 @@
 One step = one pass of the whole path over one batch of synthetic input, every
 call through the C ABI: ReshapeAndCache + Quest metadata update (one launch),
 then the dense GQA paged decode (split-KV + combine) on the calling stream
-and, beside it on a second stream, Quest scoring + top-K followed by the
-Quest sparse decode (step_runner; --serial runs them one after another).
+and, beside it on a second stream, the Quest path: block scores, then top-K
+and sparse decode in one launch (quest_decode; step_runner; --serial runs
+them one after another).
 Inputs are resident in HBM before timing; the L2 is flushed (a 512 MiB write)
 before every step, outside the timed events. The step time comes from one
 event pair per step; a second pass of the same steps, on one stream with an
@@ -190,6 +191,7 @@ class Step:
         import paged_gqa_decode_reshape_gb300 as pg
         import workloads
         self.pg, self.torch, self.w, self.dev, self.kv, self.qlen = pg, torch, w, dev, kv, qlen
+        self.sms = torch.cuda.get_device_properties(dev).multi_processor_count
         def d16(a):
             return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)
 
@@ -232,6 +234,8 @@ class Step:
         self.ws_sparse = torch.zeros_like(self.ws)
         self.sel_ws = torch.zeros(pg.quest_select_workspace_size(w.B, w.Hkv, w.MBS),
                                   dtype=torch.uint8, device=dev)
+        self.ws_quest = torch.zeros(pg.quest_decode_workspace_size(w.B, w.Hq, w.Hkv, w.D, w.MBS),
+                                    dtype=torch.uint8, device=dev)
         if kv == "fp8":
             # the 8-bit pool: every slot of the bf16 pool quantised once (setup)
             ks, vs = workloads.fp8_scales(w.Hkv)
@@ -256,10 +260,49 @@ class Step:
         pg.quest_rebuild_meta(self.kmin, self.kmax, self.kc, self.bt, self.ctx)
         torch.cuda.synchronize(dev)
 
+    def quest(self, max_ctas: int = 0):
+        """The Quest path after the write: quest_decode (block scores, then
+        one launch that selects each segment's top-K and attends over it),
+        on at most max_ctas CTAs (0: one per SM)."""
+        pg, w = self.pg, self.w
+        if self.kv == "fp8":
+            return lambda: pg.quest_decode_fp8(self.out_sparse, self.sel, self.q, self.kmin, self.kmax, self.kc,
+                                               self.vc, self.k_scale, self.v_scale, self.bt, self.ctx, w.topk,
+                                               w.scale, max_ctas=max_ctas, workspace=self.ws_quest)
+        return lambda: pg.quest_decode(self.out_sparse, self.sel, self.q, self.kmin, self.kmax, self.kc, self.vc,
+                                       self.bt, self.ctx, w.topk, w.scale, max_ctas=max_ctas,
+                                       workspace=self.ws_quest)
+
+    def quest_beside(self):
+        """The Quest path as the two-stream step runs it, beside the dense
+        decode: quest_select_topk, whose CTAs fit on the SMs beside the dense
+        decode's, then the sparse decode on at most half the SMs (its CTAs
+        need a whole SM's shared memory, start as the dense CTAs finish and
+        need not wait for the last of them). quest_decode would put its top-K
+        after the dense decode instead of beside it."""
+        pg, w, budget = self.pg, self.w, self.sms // 2
+        select = self.calls()[CALL_NAMES.index("select")]
+        if self.kv == "fp8":
+            sparse = lambda: pg.quest_sparse_decode_fp8_budget(self.out_sparse, self.q, self.kc, self.vc,
+                                                               self.k_scale, self.v_scale, self.bt, self.ctx,
+                                                               self.sel, w.scale, budget,
+                                                               workspace=self.ws_sparse)
+        else:
+            sparse = lambda: pg.quest_sparse_decode_budget(self.out_sparse, self.q, self.kc, self.vc, self.bt,
+                                                           self.ctx, self.sel, w.scale, budget,
+                                                           workspace=self.ws_sparse)
+
+        def run():
+            select()
+            sparse()
+        return run
+
     def calls(self):
-        """The step's C-ABI calls in order: the write path (ReshapeAndCache and
-        the metadata update in one launch), dense decode, Quest selection
-        (score + top-K launches), Quest sparse decode."""
+        """The step's C-ABI calls: the write path (ReshapeAndCache and the
+        metadata update in one launch), dense decode, Quest selection (score +
+        top-K launches), Quest sparse decode on that selection, and the fused
+        Quest path (quest_decode: score launch, then top-K + sparse decode in
+        one launch), which the step uses."""
         pg, w = self.pg, self.w
         if self.kv == "fp8":
             return [
@@ -272,6 +315,7 @@ class Step:
                 lambda: pg.quest_sparse_decode_fp8(self.out_sparse, self.q, self.kc, self.vc,
                                                    self.k_scale, self.v_scale, self.bt, self.ctx,
                                                    self.sel, w.scale, workspace=self.ws_sparse),
+                self.quest(),
             ]
         if self.qlen > 1:
             dense = lambda: pg.pa_decode_multi(self.out_multi, self.q_multi, self.kc, self.vc, self.bt,
@@ -287,17 +331,20 @@ class Step:
                                          w.BS, workspace=self.sel_ws),
             lambda: pg.quest_sparse_decode(self.out_sparse, self.q, self.kc, self.vc, self.bt,
                                            self.ctx, self.sel, w.scale, workspace=self.ws_sparse),
+            self.quest(),
         ]
 
 
-CALL_NAMES = ["write", "dense", "select", "sparse"]
-LAUNCHES_PER_CALL = [1, 1, 2, 1]
-# Launch order of the calls in a one-stream step (--serial, and the per-call
-# pass): the Quest selection first, then the two decode calls back to back.
-# Dense and sparse decode are one kernel binary, so the second runs with the
-# code the first left in the SMs' instruction caches (the selection has no
-# data dependence on the dense call).
-STEP_ORDER = [0, 2, 1, 3]
+CALL_NAMES = ["write", "dense", "select", "sparse", "quest"]
+# Order of the per-call pass: the separate selection and sparse decode (for
+# reference), then the fused Quest path and the dense decode back to back
+# (the decode launches are one kernel binary, so the second runs on code the
+# first left in the SMs' instruction caches).
+PASS_B_ORDER = [0, 2, 3, 4, 1]
+# The step: write, Quest path (selection 2 launches + sparse decode 1 beside
+# the dense decode; quest_decode's 2 with --serial), dense decode
+STEP_LAUNCHES = 5
+STEP_LAUNCHES_SERIAL = 4
 
 
 # -------------------------------------------------------------- CPU oracle
@@ -403,23 +450,28 @@ def max_over_ranks(values, pgroup):
     return [float(v) for v in t]
 
 
-def step_runner(torch, logical, serial: bool):
-    """One step's calls (logical order: write, dense, select, sparse). Unless
-    serial, the Quest path (selection, then sparse decode) runs on a second
-    stream forked after the write path and joined at the end of the step.
-    Neither path reads the other's output, and the two decode calls have
-    their own workspaces. The selection's CTAs run on the SMs beside the
-    dense decode's (a decode CTA's four warps leave room in each of the SM's
-    register-file partitions); the sparse decode's CTAs, which need a whole
-    SM's shared memory, take SMs as the dense decode's CTAs finish."""
-    write, dense, select, sparse = logical
+def step_runner(torch, step, serial: bool, quest=None):
+    """One step: the write path, the Quest path and the dense decode. Serial:
+    write, quest_decode, dense decode on one stream. Else the Quest path runs
+    on a second stream forked after the write path and joined at the end of
+    the step (step.quest_beside(): the selection's CTAs run on the SMs beside
+    the dense decode's, since a decode CTA's four warps leave room in each of
+    the SM's register-file partitions; the sparse decode's CTAs, which need a
+    whole SM's shared memory, take SMs as the dense decode's CTAs finish, on
+    at most half the SMs). Neither path reads the other's output, and the two
+    decode calls have their own workspaces. `quest` overrides the Quest-path
+    call in either mode."""
+    c = dict(zip(CALL_NAMES, step.calls()))
+    write, dense = c["write"], c["dense"]
     if serial:
-        order = [logical[k] for k in STEP_ORDER]
+        q = quest or c["quest"]
 
         def run():
-            for c in order:
-                c()
+            write()
+            q()
+            dense()
         return run
+    q = quest or step.quest_beside()
     side = torch.cuda.Stream()
     ev_write, ev_quest = torch.cuda.Event(), torch.cuda.Event()
 
@@ -430,8 +482,7 @@ def step_runner(torch, logical, serial: bool):
         dense()  # first, so that its persistent grid takes one CTA slot per SM
         side.wait_event(ev_write)
         with torch.cuda.stream(side):
-            select()
-            sparse()
+            q()
         ev_quest.record(side)
         main.wait_event(ev_quest)
     return run
@@ -500,7 +551,8 @@ def config_of(w, args, world: int) -> dict:
         "context_lens_max": int(w.context_lens.max()), "pool_blocks": w.NB,
         "kv_pool_bytes": int(2 * w.key_cache.nbytes // (2 if fp8 else 1)),
         "step": ("quest_reshape_and_cache{0} (ReshapeAndCache + metadata update) + "
-                 "quest_select_topk{0} + pa_decode{0} + quest_sparse_decode{0}").format("_fp8" if fp8 else ""),
+                 "quest_select_topk{0} + quest_sparse_decode{0}_budget (half the SMs) on a second stream "
+                 "beside pa_decode{0}; --serial: quest_decode{0} then pa_decode{0}").format("_fp8" if fp8 else ""),
         "l2": "inputs resident; L2 flushed before every timed sample",
         "parallelism": f"replicas x{world}",
     }
@@ -519,9 +571,9 @@ def measure(torch, pg, w, dev, args, flush, pgroup):
     events. Returns the raw per-sample times (ms) and the step's byte ledger."""
     from paged_gqa_decode_reshape_gb300 import ledger
     step = Step(w, dev, args.kv, args.qlen)
-    calls = [step.calls()[k] for k in STEP_ORDER]  # launch order
+    calls = [step.calls()[k] for k in PASS_B_ORDER]  # launch order of the per-call pass
     stream = torch.cuda.current_stream(dev)
-    run_step = step_runner(torch, step.calls(), args.serial)
+    run_step = step_runner(torch, step, args.serial)
     K = args.steps
 
     def head_start():
@@ -574,7 +626,7 @@ def measure(torch, pg, w, dev, args, flush, pgroup):
     torch.cuda.synchronize(dev)
     per_call = np.array([[evb[i][j].elapsed_time(evb[i][j + 1]) for j in range(len(calls))]
                          for i in range(K)])              # ms, launch order
-    per_call = per_call[:, np.argsort(STEP_ORDER)]       # ms, in CALL_NAMES order
+    per_call = per_call[:, np.argsort(PASS_B_ORDER)]     # ms, in CALL_NAMES order
 
     # Pass C: the step captured once in a CUDA graph and replayed.
     graph = torch.cuda.CUDAGraph()
@@ -620,7 +672,7 @@ def call_summary(m, peak: float) -> dict:
     """Per-call medians of pass B, their GB/s on the algorithmic bytes, and
     the fraction of the measured copy peak and of the nominal ~8 TB/s."""
     nb = m["nb"]
-    call_bytes = [nb.reshape + nb.meta, nb.dense, nb.select, nb.sparse]
+    call_bytes = [nb.reshape + nb.meta, nb.dense, nb.select, nb.sparse, nb.select + nb.sparse]
     med = np.median(m["per_call"], axis=0)
     out = {}
     for n, ms, b in zip(CALL_NAMES, med, call_bytes):
@@ -635,14 +687,16 @@ def call_summary(m, peak: float) -> dict:
 def point_summary(m, peak: float, world: int) -> dict:
     """The metric's "µs/step dense vs Quest" at one context length: per-call
     medians (pass B), the dense step (write + dense decode) and the Quest step
-    (write + selection + sparse decode), and the whole step of pass A."""
+    (write + quest_decode; and write + selection + sparse decode, unfused),
+    and the whole step of pass A."""
     calls = call_summary(m, peak)
     dense_us = calls["write"]["us"] + calls["dense"]["us"]
-    quest_us = calls["write"]["us"] + calls["select"]["us"] + calls["sparse"]["us"]
+    quest_us = calls["write"]["us"] + calls["quest"]["us"]
     return {
         "dense_step_us": round(dense_us, 2), "quest_step_us": round(quest_us, 2),
-        "dense_decode": calls["dense"], "sparse_decode": calls["sparse"], "select": calls["select"],
-        "write": calls["write"],
+        "quest_step_unfused_us": round(calls["write"]["us"] + calls["select"]["us"] + calls["sparse"]["us"], 2),
+        "dense_decode": calls["dense"], "quest_decode": calls["quest"], "sparse_decode": calls["sparse"],
+        "select": calls["select"], "write": calls["write"],
         "whole_step_us": stats_ms(np.asarray(m["step_ms"]) * 1e3),
         "whole_step_GBps": round(job_throughput(world, m["nb"].total, float(np.median(m["step_ms"]))), 1),
     }
@@ -732,11 +786,15 @@ def main():
             "algorithmic_bytes_per_launch": point["sparse_decode"]["bytes"],
         },
         "breakdown": {n: point[k] for n, k in (("write", "write"), ("dense", "dense_decode"),
-                                               ("select", "select"), ("sparse", "sparse_decode"))},
+                                               ("select", "select"), ("sparse", "sparse_decode"),
+                                               ("quest", "quest_decode"))},
         "breakdown_steps": K,
         "dense_us_per_step": point["dense_step_us"],
         "quest_us_per_step": point["quest_step_us"],
-        "dense_step": "write + pa_decode", "quest_step": "write + quest_select_topk + quest_sparse_decode",
+        "quest_us_per_step_unfused": point["quest_step_unfused_us"],
+        "dense_step": "write + pa_decode",
+        "quest_step": "write + quest_decode (scores; then top-K and sparse decode in one launch)",
+        "quest_step_unfused": "write + quest_select_topk + quest_sparse_decode",
         "tokens_per_s": {"dense": round(world * w.B / (point["dense_step_us"] * 1e-6), 1),
                          "quest": round(world * w.B / (point["quest_step_us"] * 1e-6), 1)},
         "e2e": {"value": round(job_throughput(world, nb.total, e2e_ms_max), 2), "unit": UNIT,
@@ -745,7 +803,7 @@ def main():
         "graph": {"value": round(job_throughput(world, nb.total, graph_ms_max), 2), "unit": UNIT,
                   "ms_per_step": round(graph_ms_max, 5), "ms_stats": stats_ms(m["graph_ms"]),
                   "how": "the step's calls captured once in a CUDA graph, replayed K times"},
-        "gpu_launches": int(K * sum(LAUNCHES_PER_CALL)),
+        "gpu_launches": int(K * (STEP_LAUNCHES_SERIAL if args.serial else STEP_LAUNCHES)),
         "wall_s_timed_region": round(m["wall"], 4),
         "clocks": m["clocks"],
     }

@@ -225,6 +225,51 @@ PA_API int quest_sparse_decode(pa_bf16 *out, const pa_bf16 *query,
                         int block_size, int64_t num_blocks, float scale,
                         void *workspace, size_t workspace_bytes, void *stream);
 
+/* quest_sparse_decode with a cap on the CTAs it launches (max_ctas 0: one
+ * per SM, as quest_sparse_decode; max_ctas < 0 is PA_ERR_INVALID_ARG). For a
+ * step that runs the sparse decode on its own stream beside a dense
+ * pa_decode: each sparse CTA needs a whole SM's shared memory, so they start
+ * as the dense call's CTAs finish, and a smaller grid lets the sparse call
+ * complete without waiting for the last of them. The split-KV pieces, and so
+ * the rounding of the result, depend on max_ctas; for a given max_ctas the
+ * result is deterministic. */
+PA_API int quest_sparse_decode_budget(pa_bf16 *out, const pa_bf16 *query,
+                               const pa_bf16 *key_cache, const pa_bf16 *value_cache,
+                               const int32_t *block_tables, int max_blocks_per_seq,
+                               const int32_t *context_lens, const int32_t *selected, int topk,
+                               int batch, int num_q_heads, int num_kv_heads, int head_dim,
+                               int block_size, int64_t num_blocks, float scale, int max_ctas,
+                               void *workspace, size_t workspace_bytes, void *stream);
+
+/* Bytes of workspace quest_decode / quest_decode_fp8 need (0 for an invalid
+ * or unsupported shape): the pa_decode workspace, then the block scores. */
+PA_API size_t quest_decode_workspace_size(int batch, int num_q_heads, int num_kv_heads, int head_dim,
+                                          int max_blocks_per_seq);
+
+/* The Quest path after the write ([P1] "Quest Sparse Attention": score the
+ * blocks, keep the top-K, attend over those only) in two launches:
+ * quest_select_topk's block scores, then one sparse-decode launch whose CTAs
+ * each select the top-K blocks of their own (sequence, KV head) segments
+ * from those scores and attend over them. Results: `selected` [B][Hkv][topk]
+ * exactly as quest_select_topk writes it, and `out` as quest_sparse_decode
+ * on that selection (with the same max_ctas, bit for bit). It saves the
+ * top-K launch and the selection's round trip through global memory. For a
+ * large selection (batch * num_kv_heads * topk at least 96 items per SM),
+ * where every sparse CTA would hold several whole segments and select for
+ * each in turn, it runs quest_select_topk and quest_sparse_decode_budget
+ * instead (three launches, the same results).
+ * max_ctas: as quest_sparse_decode_budget (0: one CTA per SM). Workspace:
+ * quest_decode_workspace_size bytes, zero-filled once, as pa_decode's (the
+ * scores follow the decode part). Errors as quest_select_topk and
+ * quest_sparse_decode. */
+PA_API int quest_decode(pa_bf16 *out, int32_t *selected, const pa_bf16 *query,
+                 const pa_bf16 *kmin, const pa_bf16 *kmax,
+                 const pa_bf16 *key_cache, const pa_bf16 *value_cache,
+                 const int32_t *block_tables, int max_blocks_per_seq,
+                 const int32_t *context_lens, int batch, int num_q_heads, int num_kv_heads,
+                 int head_dim, int block_size, int64_t num_blocks, int topk, float scale,
+                 int max_ctas, void *workspace, size_t workspace_bytes, void *stream);
+
 /* Reads the status word a pa_decode / quest_sparse_decode workspace carries
  * (synchronises `stream`): PA_OK, or PA_ERR_DEVICE if a kernel gave up on a
  * wait (its output is then undefined and the workspace must be zero-filled
@@ -364,6 +409,28 @@ PA_API int quest_sparse_decode_fp8(pa_bf16 *out, const pa_bf16 *query,
                             int batch, int num_q_heads, int num_kv_heads, int head_dim,
                             int block_size, int64_t num_blocks, float scale,
                             void *workspace, size_t workspace_bytes, void *stream);
+
+/* quest_sparse_decode_fp8 with a cap on the CTAs it launches, as
+ * quest_sparse_decode_budget. */
+PA_API int quest_sparse_decode_fp8_budget(pa_bf16 *out, const pa_bf16 *query,
+                                   const pa_e4m3 *key_cache, const pa_e4m3 *value_cache,
+                                   const float *k_scale, const float *v_scale,
+                                   const int32_t *block_tables, int max_blocks_per_seq,
+                                   const int32_t *context_lens, const int32_t *selected, int topk,
+                                   int batch, int num_q_heads, int num_kv_heads, int head_dim,
+                                   int block_size, int64_t num_blocks, float scale, int max_ctas,
+                                   void *workspace, size_t workspace_bytes, void *stream);
+
+/* quest_decode over an 8-bit cache: quest_select_topk_fp8's scores, then the
+ * fused selection and quest_sparse_decode_fp8. */
+PA_API int quest_decode_fp8(pa_bf16 *out, int32_t *selected, const pa_bf16 *query,
+                     const pa_e4m3 *kmin, const pa_e4m3 *kmax,
+                     const pa_e4m3 *key_cache, const pa_e4m3 *value_cache,
+                     const float *k_scale, const float *v_scale,
+                     const int32_t *block_tables, int max_blocks_per_seq,
+                     const int32_t *context_lens, int batch, int num_q_heads, int num_kv_heads,
+                     int head_dim, int block_size, int64_t num_blocks, int topk, float scale,
+                     int max_ctas, void *workspace, size_t workspace_bytes, void *stream);
 
 #ifdef __cplusplus
 }

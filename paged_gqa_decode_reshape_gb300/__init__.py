@@ -35,10 +35,12 @@ __all__ = [
     "PagedDecodeError", "load_library", "pa_status_string", "pa_reshape_and_cache",
     "pa_decode_workspace_size", "pa_decode", "quest_update_meta", "quest_reshape_and_cache",
     "quest_rebuild_meta",
-    "quest_select_workspace_size", "quest_select_topk", "quest_sparse_decode",
+    "quest_select_workspace_size", "quest_select_topk", "quest_sparse_decode", "quest_sparse_decode_budget",
+    "quest_decode_workspace_size", "quest_decode", "quest_decode_fp8",
     "pa_decode_multi_workspace_size", "pa_decode_multi",
     "pa_reshape_and_cache_fp8", "quest_update_meta_fp8", "quest_reshape_and_cache_fp8",
     "quest_rebuild_meta_fp8", "quest_select_topk_fp8", "pa_decode_fp8", "quest_sparse_decode_fp8",
+    "quest_sparse_decode_fp8_budget",
     "pa_workspace_status", "pa_check_metadata", "Workspace",
 ]
 
@@ -90,6 +92,17 @@ def load_library(path: Optional[str] = None):
         L.quest_sparse_decode.argtypes = [vp, vp, vp, vp, vp, i32, vp, vp, i32, i32, i32, i32, i32,
                                           i32, i64, f32, vp, sz, vp]
         L.quest_sparse_decode.restype = i32
+        L.quest_sparse_decode_budget.argtypes = [vp, vp, vp, vp, vp, i32, vp, vp, i32, i32, i32, i32, i32,
+                                                 i32, i64, f32, i32, vp, sz, vp]
+        L.quest_sparse_decode_budget.restype = i32
+        L.quest_decode_workspace_size.argtypes = [i32, i32, i32, i32, i32]
+        L.quest_decode_workspace_size.restype = sz
+        L.quest_decode.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i32, vp, i32, i32, i32, i32, i32, i64,
+                                   i32, f32, i32, vp, sz, vp]
+        L.quest_decode.restype = i32
+        L.quest_decode_fp8.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, vp, i32, i32, i32, i32,
+                                       i32, i64, i32, f32, i32, vp, sz, vp]
+        L.quest_decode_fp8.restype = i32
         L.pa_workspace_status.argtypes = [vp, vp]
         L.pa_workspace_status.restype = i32
         L.pa_check_metadata.argtypes = [vp, vp, i64, vp, i32, vp, i32, i32, i64, vp]
@@ -117,6 +130,9 @@ def load_library(path: Optional[str] = None):
         L.quest_sparse_decode_fp8.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, vp, vp, i32, i32, i32,
                                               i32, i32, i32, i64, f32, vp, sz, vp]
         L.quest_sparse_decode_fp8.restype = i32
+        L.quest_sparse_decode_fp8_budget.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, vp, vp, i32, i32, i32,
+                                                     i32, i32, i32, i64, f32, i32, vp, sz, vp]
+        L.quest_sparse_decode_fp8_budget.restype = i32
         _lib = L
         return _lib
 
@@ -261,6 +277,28 @@ def quest_sparse_decode(out: torch.Tensor, query: torch.Tensor, key_cache: torch
                                  _ptr(block_tables), MBS, _ptr(context_lens), _ptr(selected), topk,
                                  B, Hq, Hkv, D, BS, NB, float(scale), _ptr(ws),
                                  ws.numel() * ws.element_size(), _stream(dev)))
+    return out
+
+
+def quest_sparse_decode_budget(out: torch.Tensor, query: torch.Tensor, key_cache: torch.Tensor,
+                               value_cache: torch.Tensor, block_tables: torch.Tensor,
+                               context_lens: torch.Tensor, selected: torch.Tensor, scale: float,
+                               max_ctas: int, workspace: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """quest_sparse_decode launching at most max_ctas CTAs (0: one per SM)."""
+    L = load_library()
+    dev, B, Hq, Hkv, D, BS, NB, MBS = _attention_checks(out, query, key_cache, value_cache,
+                                                        block_tables, context_lens)
+    _need(selected, "selected", torch.int32, 3, dev)
+    if selected.shape[:2] != (B, Hkv):
+        raise ValueError("selected must be [B, Hkv, topk]")
+    topk = selected.shape[2]
+    need = pa_decode_workspace_size(B, Hq, Hkv, D)
+    ws = workspace if workspace is not None else _default_ws.get(dev, need)
+    _check("quest_sparse_decode_budget",
+           L.quest_sparse_decode_budget(_ptr(out), _ptr(query), _ptr(key_cache), _ptr(value_cache),
+                                        _ptr(block_tables), MBS, _ptr(context_lens), _ptr(selected), topk,
+                                        B, Hq, Hkv, D, BS, NB, float(scale), int(max_ctas), _ptr(ws),
+                                        ws.numel() * ws.element_size(), _stream(dev)))
     return out
 
 
@@ -573,6 +611,30 @@ def quest_sparse_decode_fp8(out: torch.Tensor, query: torch.Tensor, key_cache: t
     return out
 
 
+def quest_sparse_decode_fp8_budget(out: torch.Tensor, query: torch.Tensor, key_cache: torch.Tensor,
+                                   value_cache: torch.Tensor, k_scale: torch.Tensor, v_scale: torch.Tensor,
+                                   block_tables: torch.Tensor, context_lens: torch.Tensor,
+                                   selected: torch.Tensor, scale: float, max_ctas: int,
+                                   workspace: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """quest_sparse_decode_fp8 launching at most max_ctas CTAs (0: one per SM)."""
+    L = load_library()
+    dev, B, Hq, Hkv, D, BS, NB, MBS = _attention_checks_fp8(out, query, key_cache, value_cache,
+                                                            block_tables, context_lens, k_scale, v_scale)
+    _need(selected, "selected", torch.int32, 3, dev)
+    if selected.shape[:2] != (B, Hkv):
+        raise ValueError("selected must be [B, Hkv, topk]")
+    topk = selected.shape[2]
+    need = pa_decode_workspace_size(B, Hq, Hkv, D)
+    ws = workspace if workspace is not None else _default_ws.get(dev, need)
+    _check("quest_sparse_decode_fp8_budget",
+           L.quest_sparse_decode_fp8_budget(_ptr(out), _ptr(query), _ptr(key_cache), _ptr(value_cache),
+                                            _ptr(k_scale), _ptr(v_scale), _ptr(block_tables), MBS,
+                                            _ptr(context_lens), _ptr(selected), topk, B, Hq, Hkv, D, BS, NB,
+                                            float(scale), int(max_ctas), _ptr(ws), ws.numel() * ws.element_size(),
+                                            _stream(dev)))
+    return out
+
+
 # ------------------------------------------------------ multi-token rows
 
 
@@ -610,3 +672,57 @@ def pa_decode_multi(out: torch.Tensor, query: torch.Tensor, key_cache: torch.Ten
                              _ptr(context_lens), B, total_q, Hq, Hkv, D, BS, NB, float(scale), _ptr(ws),
                              ws.numel() * ws.element_size(), _stream(dev)))
     return out
+
+
+def quest_decode_workspace_size(batch: int, num_q_heads: int, num_kv_heads: int, head_dim: int,
+                                max_blocks_per_seq: int) -> int:
+    return int(load_library().quest_decode_workspace_size(batch, num_q_heads, num_kv_heads, head_dim,
+                                                          max_blocks_per_seq))
+
+
+def _quest_decode(fn, what, out, selected, query, kmin, kmax, key_cache, value_cache, block_tables,
+                  context_lens, topk, scale, max_ctas, workspace, scales, checks):
+    dev, B, Hq, Hkv, D, BS, NB, MBS = checks
+    _need(selected, "selected", torch.int32, 3, dev)
+    if tuple(selected.shape) != (B, Hkv, int(topk)):
+        raise ValueError("selected must be [B, Hkv, topk]")
+    if tuple(kmin.shape) != (NB, Hkv, D) or tuple(kmax.shape) != (NB, Hkv, D):
+        raise ValueError("kmin / kmax must be [NB, Hkv, D]")
+    need = quest_decode_workspace_size(B, Hq, Hkv, D, MBS)
+    if need == 0:
+        raise PagedDecodeError(f"{what}: unsupported shape")
+    ws = workspace if workspace is not None else _default_ws.get(dev, need)
+    _check(what, fn(_ptr(out), _ptr(selected), _ptr(query), _ptr(kmin), _ptr(kmax), _ptr(key_cache),
+                    _ptr(value_cache), *scales, _ptr(block_tables), MBS, _ptr(context_lens), B, Hq, Hkv, D, BS,
+                    NB, int(topk), float(scale), int(max_ctas), _ptr(ws), ws.numel() * ws.element_size(),
+                    _stream(dev)))
+    return out
+
+
+def quest_decode(out: torch.Tensor, selected: torch.Tensor, query: torch.Tensor, kmin: torch.Tensor,
+                 kmax: torch.Tensor, key_cache: torch.Tensor, value_cache: torch.Tensor,
+                 block_tables: torch.Tensor, context_lens: torch.Tensor, topk: int, scale: float,
+                 max_ctas: int = 0, workspace: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """Quest scores, then top-K and sparse attention in one launch; writes selected and out."""
+    L = load_library()
+    checks = _attention_checks(out, query, key_cache, value_cache, block_tables, context_lens)
+    _need(kmin, "kmin", torch.bfloat16, 3, checks[0])
+    _need(kmax, "kmax", torch.bfloat16, 3, checks[0])
+    return _quest_decode(L.quest_decode, "quest_decode", out, selected, query, kmin, kmax, key_cache,
+                         value_cache, block_tables, context_lens, topk, scale, max_ctas, workspace, (), checks)
+
+
+def quest_decode_fp8(out: torch.Tensor, selected: torch.Tensor, query: torch.Tensor, kmin: torch.Tensor,
+                     kmax: torch.Tensor, key_cache: torch.Tensor, value_cache: torch.Tensor,
+                     k_scale: torch.Tensor, v_scale: torch.Tensor, block_tables: torch.Tensor,
+                     context_lens: torch.Tensor, topk: int, scale: float, max_ctas: int = 0,
+                     workspace: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """quest_decode over 8-bit caches (E4M3 metadata, K and V codes with per-KV-head scales)."""
+    L = load_library()
+    checks = _attention_checks_fp8(out, query, key_cache, value_cache, block_tables, context_lens, k_scale,
+                                   v_scale)
+    _need(kmin, "kmin", torch.uint8, 3, checks[0])
+    _need(kmax, "kmax", torch.uint8, 3, checks[0])
+    return _quest_decode(L.quest_decode_fp8, "quest_decode_fp8", out, selected, query, kmin, kmax, key_cache,
+                         value_cache, block_tables, context_lens, topk, scale, max_ctas, workspace,
+                         (_ptr(k_scale), _ptr(v_scale)), checks)

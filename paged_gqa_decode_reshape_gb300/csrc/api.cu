@@ -117,11 +117,12 @@ int run_decode(pa_bf16 *out, const pa_bf16 *query, const void *key_cache, const 
                const int32_t *selected, int topk, int B, int Hq, int Hkv, int D, int BS, int64_t NB,
                float scale, void *workspace, size_t workspace_bytes, void *stream, bool sparse,
                const float *k_scale = nullptr, const float *v_scale = nullptr, bool fp8 = false,
-               const int32_t *cu_q = nullptr, int nseq = 0) {
+               const int32_t *cu_q = nullptr, int nseq = 0, int max_ctas = 0,
+               const float *scores = nullptr, int32_t *sel_out = nullptr) {
     int rc = check_attention_args(out, query, key_cache, value_cache, block_tables, MBS,
                                   context_lens, B, Hq, Hkv, D, BS, NB, scale, workspace);
     if (rc != PA_OK) return rc;
-    if (sparse && (!selected || topk <= 0)) return PA_ERR_INVALID_ARG;
+    if (sparse && ((!selected && !scores) || topk <= 0)) return PA_ERR_INVALID_ARG;
     if (fp8 && (!k_scale || !v_scale)) return PA_ERR_INVALID_ARG;
     if (fp8 && D != 128) return PA_ERR_UNSUPPORTED;
     DecodeGeometry geo;
@@ -150,6 +151,9 @@ int run_decode(pa_bf16 *out, const pa_bf16 *query, const void *key_cache, const 
     a.part = w.part;
     a.counters = w.counters;
     a.status = w.status;
+    a.scores = scores;
+    a.sel_out = sel_out;
+    a.nsel_cap = 0;
     a.wait_ns = g_wait_ns.load(std::memory_order_relaxed);
     a.stop_item = g_stop_item.load(std::memory_order_relaxed);
     a.NB = NB;
@@ -160,7 +164,7 @@ int run_decode(pa_bf16 *out, const pa_bf16 *query, const void *key_cache, const 
     a.Hkv = Hkv;
     a.G = Hq / Hkv;
     a.scale_log2 = scale * 1.4426950408889634f;
-    e = launch_decode(tk, tv, a, D, sparse, static_cast<cudaStream_t>(stream), fp8);
+    e = launch_decode(tk, tv, a, D, sparse, static_cast<cudaStream_t>(stream), fp8, max_ctas);
     if (e != cudaSuccess) return cuda_fail(e);
     return PA_OK;
 }
@@ -229,6 +233,20 @@ int quest_sparse_decode(pa_bf16 *out, const pa_bf16 *query, const pa_bf16 *key_c
     return run_decode(out, query, key_cache, value_cache, block_tables, max_blocks_per_seq,
                       context_lens, selected, topk, batch, num_q_heads, num_kv_heads, head_dim,
                       block_size, num_blocks, scale, workspace, workspace_bytes, stream, true);
+}
+
+int quest_sparse_decode_budget(pa_bf16 *out, const pa_bf16 *query, const pa_bf16 *key_cache,
+                               const pa_bf16 *value_cache, const int32_t *block_tables,
+                               int max_blocks_per_seq, const int32_t *context_lens,
+                               const int32_t *selected, int topk, int batch, int num_q_heads,
+                               int num_kv_heads, int head_dim, int block_size, int64_t num_blocks,
+                               float scale, int max_ctas, void *workspace, size_t workspace_bytes,
+                               void *stream) {
+    if (max_ctas < 0) return PA_ERR_INVALID_ARG;
+    return run_decode(out, query, key_cache, value_cache, block_tables, max_blocks_per_seq,
+                      context_lens, selected, topk, batch, num_q_heads, num_kv_heads, head_dim,
+                      block_size, num_blocks, scale, workspace, workspace_bytes, stream, true, nullptr,
+                      nullptr, false, nullptr, 0, max_ctas);
 }
 
 int quest_update_meta(pa_bf16 *kmin, pa_bf16 *kmax, const pa_bf16 *key,
@@ -311,6 +329,82 @@ int quest_select_topk(int32_t *selected, const pa_bf16 *query, const pa_bf16 *km
         max_blocks_per_seq, context_lens, batch, num_q_heads, num_kv_heads, head_dim, block_size,
         num_blocks, topk, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? PA_OK : cuda_fail(e);
+}
+
+size_t quest_decode_workspace_size(int batch, int num_q_heads, int num_kv_heads, int head_dim,
+                                   int max_blocks_per_seq) {
+    const size_t dec = pa_decode_workspace_size(batch, num_q_heads, num_kv_heads, head_dim);
+    const size_t sc = quest_select_workspace_size(batch, num_kv_heads, max_blocks_per_seq);
+    if (dec == 0 || sc == 0) return 0;
+    return (dec + 255) / 256 * 256 + sc;
+}
+
+namespace {
+// score launch + fused top-K / sparse decode launch (bf16 or E4M3 cache)
+int run_quest_decode(pa_bf16 *out, int32_t *selected, const pa_bf16 *query, const void *kmin,
+                     const void *kmax, const void *key_cache, const void *value_cache,
+                     const float *k_scale, const float *v_scale, const int32_t *block_tables, int MBS,
+                     const int32_t *context_lens, int B, int Hq, int Hkv, int D, int BS, int64_t NB,
+                     int topk, float scale, int max_ctas, void *workspace, size_t workspace_bytes,
+                     void *stream, bool fp8) {
+    if (!selected || !kmin || !kmax || !workspace || max_ctas < 0) return PA_ERR_INVALID_ARG;
+    int rc = check_attention_args(out, query, key_cache, value_cache, block_tables, MBS, context_lens, B, Hq,
+                                  Hkv, D, BS, NB, scale, workspace);
+    if (rc != PA_OK) return rc;
+    if (topk <= 0) return PA_ERR_INVALID_ARG;
+    if (fp8 && D != 128) return PA_ERR_UNSUPPORTED;
+    if (!aligned16(kmin) || !aligned16(kmax)) return PA_ERR_INVALID_ARG;
+    const size_t dec = pa_decode_workspace_size(B, Hq, Hkv, D);
+    const size_t need = quest_decode_workspace_size(B, Hq, Hkv, D, MBS);
+    if (dec == 0 || need == 0) return PA_ERR_UNSUPPORTED;
+    if (workspace_bytes < need) return PA_ERR_WORKSPACE;
+    float *scores = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) + (dec + 255) / 256 * 256);
+    DecodeGeometry geo;
+    cudaError_t e = decode_geometry(D, &geo, fp8);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (int64_t(B) * Hkv * topk >= int64_t(geo.grid) * kSparseLargeItems) {
+        // A large selection: every CTA holds several whole segments, and their
+        // top-Ks would run one after another inside it; the top-K kernel
+        // (one CTA per segment) runs them all at once instead.
+        e = launch_quest_select(selected, scores, query, kmin, kmax, block_tables, MBS, context_lens, B, Hq, Hkv,
+                                D, BS, NB, topk, static_cast<cudaStream_t>(stream), fp8);
+        if (e != cudaSuccess) return cuda_fail(e);
+        return run_decode(out, query, key_cache, value_cache, block_tables, MBS, context_lens, selected, topk, B,
+                          Hq, Hkv, D, BS, NB, scale, workspace, dec, stream, true, k_scale, v_scale, fp8, nullptr,
+                          0, max_ctas);
+    }
+    e = launch_quest_scores(scores, query, kmin, kmax, block_tables, MBS, context_lens, B, Hq, Hkv, D, BS, NB,
+                            static_cast<cudaStream_t>(stream), fp8);
+    if (e != cudaSuccess) return cuda_fail(e);
+    return run_decode(out, query, key_cache, value_cache, block_tables, MBS, context_lens, nullptr, topk, B,
+                      Hq, Hkv, D, BS, NB, scale, workspace, dec, stream, true, k_scale, v_scale, fp8, nullptr, 0,
+                      max_ctas, scores, selected);
+}
+}  // namespace
+
+int quest_decode(pa_bf16 *out, int32_t *selected, const pa_bf16 *query, const pa_bf16 *kmin,
+                 const pa_bf16 *kmax, const pa_bf16 *key_cache, const pa_bf16 *value_cache,
+                 const int32_t *block_tables, int max_blocks_per_seq, const int32_t *context_lens,
+                 int batch, int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                 int64_t num_blocks, int topk, float scale, int max_ctas, void *workspace,
+                 size_t workspace_bytes, void *stream) {
+    return run_quest_decode(out, selected, query, kmin, kmax, key_cache, value_cache, nullptr, nullptr,
+                            block_tables, max_blocks_per_seq, context_lens, batch, num_q_heads, num_kv_heads,
+                            head_dim, block_size, num_blocks, topk, scale, max_ctas, workspace, workspace_bytes,
+                            stream, false);
+}
+
+int quest_decode_fp8(pa_bf16 *out, int32_t *selected, const pa_bf16 *query, const pa_e4m3 *kmin,
+                     const pa_e4m3 *kmax, const pa_e4m3 *key_cache, const pa_e4m3 *value_cache,
+                     const float *k_scale, const float *v_scale, const int32_t *block_tables,
+                     int max_blocks_per_seq, const int32_t *context_lens, int batch, int num_q_heads,
+                     int num_kv_heads, int head_dim, int block_size, int64_t num_blocks, int topk,
+                     float scale, int max_ctas, void *workspace, size_t workspace_bytes, void *stream) {
+    if (!k_scale || !v_scale) return PA_ERR_INVALID_ARG;
+    return run_quest_decode(out, selected, query, kmin, kmax, key_cache, value_cache, k_scale, v_scale,
+                            block_tables, max_blocks_per_seq, context_lens, batch, num_q_heads, num_kv_heads,
+                            head_dim, block_size, num_blocks, topk, scale, max_ctas, workspace, workspace_bytes,
+                            stream, true);
 }
 
 int pa_workspace_status(const void *workspace, void *stream) {
@@ -444,6 +538,20 @@ int quest_select_topk_fp8(int32_t *selected, const pa_bf16 *query, const pa_e4m3
         context_lens, batch, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, topk,
         static_cast<cudaStream_t>(stream), true);
     return e == cudaSuccess ? PA_OK : cuda_fail(e);
+}
+
+int quest_sparse_decode_fp8_budget(pa_bf16 *out, const pa_bf16 *query, const pa_e4m3 *key_cache,
+                                   const pa_e4m3 *value_cache, const float *k_scale, const float *v_scale,
+                                   const int32_t *block_tables, int max_blocks_per_seq,
+                                   const int32_t *context_lens, const int32_t *selected, int topk,
+                                   int batch, int num_q_heads, int num_kv_heads, int head_dim,
+                                   int block_size, int64_t num_blocks, float scale, int max_ctas,
+                                   void *workspace, size_t workspace_bytes, void *stream) {
+    if (max_ctas < 0) return PA_ERR_INVALID_ARG;
+    return run_decode(out, query, key_cache, value_cache, block_tables, max_blocks_per_seq,
+                      context_lens, selected, topk, batch, num_q_heads, num_kv_heads, head_dim,
+                      block_size, num_blocks, scale, workspace, workspace_bytes, stream, true, k_scale,
+                      v_scale, true, nullptr, 0, max_ctas);
 }
 
 int pa_decode_fp8(pa_bf16 *out, const pa_bf16 *query, const pa_e4m3 *key_cache,

@@ -30,6 +30,12 @@ __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
 }
 
+// Order this thread's earlier shared-memory accesses before later accesses
+// of the async (TMA) proxy to the same memory.
+__device__ __forceinline__ void fence_proxy_async() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 // Make barrier initialisation visible to the async (TMA) proxy.
 __device__ __forceinline__ void fence_barrier_init() {
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -242,6 +248,166 @@ __device__ __forceinline__ uint32_t bf16_order_key(uint32_t h) {
 __device__ __forceinline__ uint32_t f32_order_key(float f) {
     const uint32_t u = __float_as_uint(f);
     return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// keys[j] = totalOrder key of row[j] for j < n, by all THREADS threads of a
+// CTA: each thread issues U independent loads before storing any, so a row
+// costs a few L2 round trips rather than one per element a thread holds.
+template <int THREADS, int U = 16>
+__device__ __forceinline__ void cta_load_keys(uint32_t *keys, const float *row, int n) {
+    for (int j0 = threadIdx.x; j0 < n; j0 += THREADS * U) {
+        float v[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int j = j0 + u * THREADS;
+            v[u] = j < n ? __ldcg(row + j) : 0.f;
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int j = j0 + u * THREADS;
+            if (j < n) keys[j] = f32_order_key(v[u]);
+        }
+    }
+}
+
+// ---- Top-K of a row of totalOrder keys, by all THREADS threads of a CTA
+// (the Quest block selection: the topk largest scores, ties to the lower
+// block index). key_of(j) gives key j < n (n > topk).
+//
+// Threshold: the topk-th largest key `thr`, and `keq`, how many keys equal
+// to it are taken (the keq lowest-index ones; every key above thr is taken).
+// Radix select from the top in digits of up to 8 bits, starting at the
+// highest bit where the row's smallest and largest keys differ (the scores of
+// a row share their sign, exponent and often more, so a fixed first digit
+// would put every key into one bin and serialise its atomic adds).
+// hist: 256 ints of shared memory; red: at least 2 * THREADS / 32 + 2 ints.
+template <int THREADS, typename KeyOf>
+__device__ __forceinline__ void cta_topk_threshold(KeyOf key_of, int n, int topk, int *hist, int *red,
+                                                   uint32_t &thr, int &keq) {
+    constexpr int NW = THREADS / 32;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    uint32_t lo = 0xffffffffu, hi = 0u;
+    for (int j = tid; j < n; j += THREADS) {
+        const uint32_t u = key_of(j);
+        lo = min(lo, u);
+        hi = max(hi, u);
+    }
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) {
+        lo = min(lo, __shfl_xor_sync(0xffffffffu, lo, o));
+        hi = max(hi, __shfl_xor_sync(0xffffffffu, hi, o));
+    }
+    if (lane == 0) {
+        red[warp] = int(lo);
+        red[NW + warp] = int(hi);
+    }
+    __syncthreads();
+    lo = 0xffffffffu;
+    hi = 0u;
+#pragma unroll
+    for (int w = 0; w < NW; ++w) {
+        lo = min(lo, uint32_t(red[w]));
+        hi = max(hi, uint32_t(red[NW + w]));
+    }
+    int k = topk;
+    if (lo == hi) {  // every key equal: the topk lowest indices
+        thr = hi;
+        keq = k;
+        __syncthreads();  // red may be reused by the caller
+        return;
+    }
+    const int top = 31 - __clz(lo ^ hi);  // the keys agree on every bit above this one
+    uint32_t mask = top == 31 ? 0u : ~((2u << top) - 1u);
+    uint32_t prefix = hi & mask;
+    for (int h = top; h >= 0;) {
+        const int l = h >= 7 ? h - 7 : 0;
+        const uint32_t dm = (2u << (h - l)) - 1u;  // digit of bits l..h
+        for (int i = tid; i < 256; i += THREADS) hist[i] = 0;
+        __syncthreads();
+        for (int j = tid; j < n; j += THREADS) {
+            const uint32_t u = key_of(j);
+            if ((u & mask) == prefix) atomicAdd(&hist[(u >> l) & dm], 1);
+        }
+        __syncthreads();
+        if (warp == 0) {
+            // lane t holds digits 255-8t .. 248-8t (descending)
+            int cnt[8], sum = 0;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                cnt[i] = hist[255 - 8 * lane - i];
+                sum += cnt[i];
+            }
+            int incl = sum;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int v = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += v;
+            }
+            int before = incl - sum;
+            if (before < k && k <= incl) {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    if (before + cnt[i] >= k) {
+                        red[2 * NW] = 255 - 8 * lane - i;
+                        red[2 * NW + 1] = before;
+                        break;
+                    }
+                    before += cnt[i];
+                }
+            }
+        }
+        __syncthreads();
+        prefix |= uint32_t(red[2 * NW]) << l;
+        mask |= dm << l;
+        k -= red[2 * NW + 1];
+        h = l - 1;
+    }
+    thr = prefix;
+    keq = k;
+    __syncthreads();  // red may be reused by the caller
+}
+
+// The selection for a threshold: every key above thr and the keq lowest-index
+// keys equal to it, emitted as emit(r, j) with r the rank of block j among
+// the selected (ascending j). Each warp counts, then emits, one contiguous
+// range of keys; red: at least 2 * THREADS / 32 ints.
+template <int THREADS, typename KeyOf, typename Emit>
+__device__ __forceinline__ void cta_topk_emit(KeyOf key_of, int n, uint32_t thr, int keq, int *red, Emit emit) {
+    constexpr int NW = THREADS / 32;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const unsigned lt = (1u << lane) - 1u;
+    const int per = ((n + NW * 32 - 1) / (NW * 32)) * 32;
+    const int jb = warp * per, je = min(n, jb + per);
+    int cgt = 0, ceq = 0;
+    for (int j0 = jb; j0 < je; j0 += 32) {
+        const int j = j0 + lane;
+        const uint32_t u = j < je ? key_of(j) : 0u;
+        cgt += __popc(__ballot_sync(0xffffffffu, j < je && u > thr));
+        ceq += __popc(__ballot_sync(0xffffffffu, j < je && u == thr));
+    }
+    if (lane == 0) {
+        red[warp] = cgt;
+        red[NW + warp] = ceq;
+    }
+    __syncthreads();
+    int run_eq = 0, run_pos = 0;
+    for (int w = 0; w < warp; ++w) {
+        const int e = red[NW + w];
+        run_pos += red[w] + min(max(keq - run_eq, 0), e);
+        run_eq += e;
+    }
+    for (int j0 = jb; j0 < je; j0 += 32) {
+        const int j = j0 + lane;
+        const uint32_t u = j < je ? key_of(j) : 0u;
+        const bool gt = j < je && u > thr, eq = j < je && u == thr;
+        const unsigned beq = __ballot_sync(0xffffffffu, eq);
+        const bool take = gt || (eq && run_eq + __popc(beq & lt) < keq);
+        const unsigned btk = __ballot_sync(0xffffffffu, take);
+        if (take) emit(run_pos + __popc(btk & lt), j);
+        run_eq += __popc(beq);
+        run_pos += __popc(btk);
+    }
+    __syncthreads();  // red may be reused by the caller
 }
 
 // Host side: ask once per (device, kernel) for the largest shared-memory

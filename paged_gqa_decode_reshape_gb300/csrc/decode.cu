@@ -78,8 +78,7 @@ namespace {
 
 // Sparse decode of small selections (fewer than kSparseLargeItems items per
 // SM): the grid follows the segments, pieces of at least kSparseMinItems items.
-constexpr int kSparseLargeItems = 96;
-constexpr int kSparseMinItems = 24;
+constexpr int kSparseMinItems = 16;
 
 template <int D, bool F8 = false, bool MULTI = false>
 struct DecodeCfg {
@@ -106,6 +105,14 @@ struct DecodeCfg {
     static constexpr size_t seq_off(int PB) { return off_pre + (size_t(PB + 1) * 4 + 15) / 16 * 16; }
     static constexpr size_t row0_off(int PB, int R) { return seq_off(PB) + (size_t(R) * 2 + 15) / 16 * 16; }
     static constexpr size_t smem_bytes(int PB, int R = 0) { return 1024 + row0_off(PB, R) + (size_t(R) * 2 + 15) / 16 * 16; }
+    // fused Quest decode (one query row per sequence): the CTA's selection
+    // entries [nsel] after the per-row prefix
+    static constexpr size_t sel_off(int PB) { return row0_off(PB, 0); }
+    static constexpr size_t smem_bytes_sel(int PB, int nsel) { return 1024 + sel_off(PB) + size_t(nsel) * 4; }
+    // top-K scratch of the fused Quest decode, in the ring (free until the
+    // first copy): the keys, then 256 histogram bins and per-warp counts
+    static constexpr int KEYS_CAP = int((size_t(S) * STAGE - 4096) / 4);
+    static constexpr size_t off_topk_hist = size_t(S) * STAGE - 4096;
 };
 
 // One binary serves the dense call and the sparse one (topk > 0: the items
@@ -158,7 +165,7 @@ __global__ void __launch_bounds__(DecodeCfg<D, F8, MULTI>::THREADS, 1)
         for (int64_t off = gt * 32; off < int64_t(nseq); off += nthr * 32) prefetch_l2(a.ctx + off);
         const int64_t bt_n = int64_t(nseq) * a.MBS;
         for (int64_t off = gt * 32; off < bt_n; off += nthr * 32) prefetch_l2(a.bt + off);
-        if (SPARSE) {
+        if (SPARSE && !a.scores) {
             const int64_t sel_n = int64_t(B) * Hkv * a.topk;
             for (int64_t off = gt * 32; off < sel_n; off += nthr * 32) prefetch_l2(a.sel + off);
         }
@@ -232,7 +239,27 @@ __global__ void __launch_bounds__(DecodeCfg<D, F8, MULTI>::THREADS, 1)
         }
         __syncthreads();
     }
-    for (int v = tid; v < NR; v += C::THREADS) pre[v + 1] = row_items(v);
+    if constexpr (MULTI) {
+        for (int v = tid; v < NR; v += C::THREADS) pre[v + 1] = row_items(v);
+    } else {
+        // eight independent context-length loads per thread in flight
+        for (int v0 = tid; v0 < NR; v0 += 8 * C::THREADS) {
+            int c8[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int v = v0 + u * C::THREADS;
+                c8[u] = v < NR ? __ldg(a.ctx + v) : 0;
+            }
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int v = v0 + u * C::THREADS;
+                if (v < NR) {
+                    const int nblk = (min(max(c8[u], 0), max_tok) + BS - 1) / BS;
+                    pre[v + 1] = SPARSE ? (nblk > 0 ? a.topk : 0) : nblk;
+                }
+            }
+        }
+    }
     __syncthreads();
     scan_pre(NR);
     __syncthreads();
@@ -257,6 +284,12 @@ __global__ void __launch_bounds__(DecodeCfg<D, F8, MULTI>::THREADS, 1)
                 for (int i = 0; i < D / 8; ++i) o[i] = make_uint4(0, 0, 0, 0);
             }
         }
+        if (SPARSE && a.scores)  // fused Quest decode: sequences with no blocks select nothing
+            for (int64_t idx = int64_t(blockIdx.x) * C::THREADS + tid; idx < int64_t(B) * Hkv * a.topk;
+                 idx += int64_t(gridDim.x) * C::THREADS) {
+                const int b = int(idx / (int64_t(Hkv) * a.topk));
+                if (pre[b + 1] == pre[b]) a.sel_out[idx] = -1;
+            }
     }
 
     const int64_t total = int64_t(Hkv) * pre[NR];
@@ -275,6 +308,61 @@ __global__ void __launch_bounds__(DecodeCfg<D, F8, MULTI>::THREADS, 1)
         }
         return lo;
     };
+
+    // ---- fused Quest decode: this CTA selects, for every segment it holds a
+    // piece of, the top-K blocks of that (sequence, KV head) from the scores
+    // ([P1] "Quest Sparse Attention": ties to the lower block index), keeps
+    // its piece of the selection in shared memory, and the CTA holding the
+    // segment's first entry writes the selection row out. The same rule as
+    // quest_select_topk (cta_topk_threshold / cta_topk_emit).
+    int32_t *sel_s = reinterpret_cast<int32_t *>(bp + C::sel_off(PB));
+    if (SPARSE && a.scores) {
+        uint32_t *keys = reinterpret_cast<uint32_t *>(bp);  // the ring: no copy has been issued yet
+        int *hist = reinterpret_cast<int *>(bp + C::off_topk_hist);
+        int *wcnt = hist + 256;  // scratch of the top-K helpers
+        int64_t p = pos0;
+        int b = find_seq(p);
+        int kvh = int((p - int64_t(Hkv) * pre[b]) / (pre[b + 1] - pre[b]));
+        while (p < pos1) {
+            const int nseg = pre[b + 1] - pre[b];
+            const int seg = b * Hkv + kvh;
+            const int64_t s0 = int64_t(Hkv) * pre[b] + int64_t(kvh) * nseg;
+            const int64_t e0 = s0 + nseg;
+            const int i0 = int(p - s0), i1 = int(min(e0, pos1) - s0);  // this CTA's entries
+            int32_t *mine = sel_s + (p - pos0) - i0;                   // entry r -> mine[r], r in [i0, i1)
+            const bool writer = s0 >= pos0;                            // holds entry 0: writes the row
+            int32_t *orow = a.sel_out + int64_t(seg) * a.topk;
+            const float *srow = a.scores + int64_t(seg) * a.MBS;
+            const int n = (min(max(__ldg(a.ctx + b), 0), max_tok) + BS - 1) / BS;
+            const int topk = a.topk;
+            if (n <= topk) {
+                for (int i = tid; i < topk; i += C::THREADS) {
+                    const int v = i < n ? i : -1;
+                    if (writer) orow[i] = v;
+                    if (i >= i0 && i < i1) mine[i] = v;
+                }
+            } else {
+                const bool cached = n <= C::KEYS_CAP;
+                if (cached) cta_load_keys<C::THREADS>(keys, srow, n);
+                auto key_of = [&](int j) -> uint32_t { return cached ? keys[j] : f32_order_key(__ldcg(srow + j)); };
+                uint32_t thr;
+                int keq;
+                cta_topk_threshold<C::THREADS>(key_of, n, topk, hist, wcnt, thr, keq);
+                cta_topk_emit<C::THREADS>(key_of, n, thr, keq, wcnt, [&](int r, int j) {
+                    if (writer) orow[r] = j;
+                    if (r >= i0 && r < i1) mine[r] = j;
+                });
+            }
+            __syncthreads();  // keys and counts are reused by the next segment
+            p = min(e0, pos1);
+            if (++kvh == Hkv) {
+                kvh = 0;
+                do {
+                    ++b;
+                } while (b < NR && pre[b + 1] == pre[b]);
+            }
+        }
+    }
 
     if (warp == NC) {
         // ================================================================ producer
@@ -303,7 +391,7 @@ __global__ void __launch_bounds__(DecodeCfg<D, F8, MULTI>::THREADS, 1)
             } else {
                 it.ctxv = __ldg(a.ctx + b);
             }
-            it.j = SPARSE ? __ldg(a.sel + (int64_t(b) * Hkv + kvh) * a.topk + i) : i;
+            it.j = !SPARSE ? i : a.scores ? sel_s[k] : __ldg(a.sel + (int64_t(b) * Hkv + kvh) * a.topk + i);
             return it;
         };
         auto stage_b = [&](Win &it) {
@@ -313,6 +401,7 @@ __global__ void __launch_bounds__(DecodeCfg<D, F8, MULTI>::THREADS, 1)
             it.phys = (it.j >= 0 && it.j < a.MBS) ? __ldg(a.bt + int64_t(s) * a.MBS + it.j) : -1;
         };
         const uint64_t policy = l2_policy_evict_first();
+        if (SPARSE && a.scores) fence_proxy_async();  // the ring held the top-K scratch
         Win wa = stage_c(0), wb = stage_c(32);
         stage_b(wa);
         stage_b(wb);
@@ -1044,7 +1133,7 @@ cudaError_t geometry_t(DecodeGeometry *g) {
 
 template <int D, bool SPARSE, bool F8, bool MULTI = false>
 cudaError_t launch_t(const CUtensorMap &tm_k, const CUtensorMap &tm_v, const DecodeArgs &a,
-                     cudaStream_t stream) {
+                     cudaStream_t stream, int max_ctas = 0) {
     using C = DecodeCfg<D, F8, MULTI>;
     DecodeGeometry geo;
     cudaError_t e = decode_geometry(D, &geo, F8);
@@ -1058,23 +1147,39 @@ cudaError_t launch_t(const CUtensorMap &tm_k, const CUtensorMap &tm_v, const Dec
         // most of its time on fixed costs (start-up, publishing partials, the
         // cross-CTA combine), and a range boundary inside a segment costs a
         // combine: cut each segment into c equal pieces (c a power of two, at
-        // least kSparseMinItems items each, at most half the SMs in all) or
-        // give each CTA whole segments. Half the SMs: in a step the sparse
-        // decode runs beside the dense one and starts on the SMs its CTAs
-        // free; it need not wait for the last of them (quest_8k step 83.6 ->
-        // 77.3 us with 64 CTAs of 64 items instead of 128 of 32).
+        // least kSparseMinItems items each, at most `budget` CTAs in all) or
+        // give each CTA whole segments. The budget is one CTA per SM unless
+        // the caller sets a smaller one: in a step that runs the sparse
+        // decode beside the dense one, half the SMs let it start on the SMs
+        // the dense CTAs free without waiting for the last of them (quest_8k
+        // step 83.6 -> 77.3 us with 64 CTAs of 64 items instead of 128 of 32).
+        const int budget = (max_ctas > 0 && max_ctas < grid) ? max_ctas : grid;
         const int64_t segs = int64_t(a.B) * a.Hkv;
         if (segs * a.topk < int64_t(grid) * kSparseLargeItems) {
             int64_t c = 1;
-            while (a.topk % (2 * c) == 0 && a.topk / (2 * c) >= kSparseMinItems && segs * 2 * c <= grid / 2)
+            while (a.topk % (2 * c) == 0 && a.topk / (2 * c) >= kSparseMinItems && segs * 2 * c <= budget)
                 c *= 2;
-            if (segs * c <= grid) {
+            if (segs * c <= budget) {
                 grid = int(segs * c);
             } else {
-                const int64_t m = (segs + grid - 1) / grid;  // segments per CTA
+                const int64_t m = (segs + budget - 1) / budget;  // segments per CTA
                 grid = int((segs + m - 1) / m);
             }
+        } else {
+            grid = budget;
         }
+    }
+    if (SPARSE && a.scores) {
+        // fused Quest decode: room for the CTA's selection entries (at most
+        // ceil(items / CTAs), items <= segments * topk)
+        DecodeArgs f = a;
+        const int64_t items = int64_t(a.B) * a.Hkv * a.topk;
+        const int64_t cap = (items + grid - 1) / grid;
+        const size_t fsmem = C::smem_bytes_sel(a.B, int(cap));
+        if (cap > (int64_t(1) << 20) || fsmem > geo.smem) return cudaErrorInvalidConfiguration;
+        f.nsel_cap = int(cap);
+        return launch_pdl(decode_kernel<D, F8, MULTI>, dim3(grid), dim3(C::THREADS), fsmem, stream, tm_k, tm_v,
+                          f);
     }
     return launch_pdl(decode_kernel<D, F8, MULTI>, dim3(grid), dim3(C::THREADS), smem, stream,
                       tm_k, tm_v, a);
@@ -1122,7 +1227,7 @@ size_t decode_multi_workspace_bytes(int total_q, int Hkv, int head_dim, int work
 }
 
 cudaError_t launch_decode(const CUtensorMap &tm_k, const CUtensorMap &tm_v, const DecodeArgs &a,
-                          int head_dim, bool sparse, cudaStream_t stream, bool fp8) {
+                          int head_dim, bool sparse, cudaStream_t stream, bool fp8, int max_ctas) {
     if (a.cu_q) {  // multi-token query rows (bf16 cache, dense)
         if (fp8 || sparse) return cudaErrorInvalidValue;
         return head_dim == 128 ? launch_t<128, false, false, true>(tm_k, tm_v, a, stream)
@@ -1130,13 +1235,13 @@ cudaError_t launch_decode(const CUtensorMap &tm_k, const CUtensorMap &tm_v, cons
     }
     if (fp8) {
         if (head_dim != 128) return cudaErrorInvalidValue;
-        return sparse ? launch_t<128, true, true>(tm_k, tm_v, a, stream)
+        return sparse ? launch_t<128, true, true>(tm_k, tm_v, a, stream, max_ctas)
                       : launch_t<128, false, true>(tm_k, tm_v, a, stream);
     }
     if (head_dim == 128)
-        return sparse ? launch_t<128, true, false>(tm_k, tm_v, a, stream)
+        return sparse ? launch_t<128, true, false>(tm_k, tm_v, a, stream, max_ctas)
                       : launch_t<128, false, false>(tm_k, tm_v, a, stream);
-    return sparse ? launch_t<64, true, false>(tm_k, tm_v, a, stream)
+    return sparse ? launch_t<64, true, false>(tm_k, tm_v, a, stream, max_ctas)
                   : launch_t<64, false, false>(tm_k, tm_v, a, stream);
 }
 

@@ -12,6 +12,9 @@ constexpr int kMaxBatch = 4096;      // sequences per call
 constexpr int kMaxGroup = 8;         // query heads per KV head (one mma n-tile)
 constexpr int kMaxMultiRows = 2048;  // query rows of a multi-token decode call
 constexpr int kMultiRowGroup = 4;    // query rows sharing one pass over the KV (one per consumer warp)
+// Sparse decode of small selections (fewer than kSparseLargeItems items per
+// SM): the grid follows the segments instead of cutting one work list evenly
+constexpr int kSparseLargeItems = 96;
 
 // Arguments of the split-KV decode kernel (dense and Quest-sparse).
 struct DecodeArgs {
@@ -29,6 +32,10 @@ struct DecodeArgs {
     float *part;                // [B*Hkv + W][D*8 + 8] partial outputs and lse (log2 domain)
     int32_t *counters;          // [B*Hkv] arrival counters (zero between calls)
     int32_t *status;            // workspace status word
+    const float *scores;        // fused Quest decode: block scores [B][Hkv][MBS]; each CTA selects
+                                // the top-K of its segments itself (else null: selection in sel)
+    int32_t *sel_out;           // fused Quest decode: [B][Hkv][topk] selection written out
+    int nsel_cap;               // fused Quest decode: capacity of the CTA's selection array
     uint64_t wait_ns;           // limit of every bounded wait inside the kernel (ns)
     int stop_item;              // the producer stops issuing at this item of its CTA's range
                                 // (failure tests only; INT_MAX otherwise)
@@ -49,8 +56,10 @@ struct DecodeGeometry {
 cudaError_t decode_geometry(int head_dim, DecodeGeometry *g, bool fp8 = false);
 size_t decode_workspace_bytes(int B, int Hkv, int head_dim, int workers);
 size_t decode_multi_workspace_bytes(int total_q, int Hkv, int head_dim, int workers);
+// max_ctas (sparse only): at most this many CTAs (<= 0: one per SM)
 cudaError_t launch_decode(const CUtensorMap &tm_k, const CUtensorMap &tm_v, const DecodeArgs &a,
-                          int head_dim, bool sparse, cudaStream_t stream, bool fp8 = false);
+                          int head_dim, bool sparse, cudaStream_t stream, bool fp8 = false,
+                          int max_ctas = 0);
 
 cudaError_t launch_reshape_and_cache(const uint16_t *key, const uint16_t *value, uint16_t *kc,
                                      uint16_t *vc, const int64_t *slots, int64_t T, int Hkv, int D,
@@ -79,6 +88,10 @@ cudaError_t launch_rebuild_meta_fp8(uint8_t *kmin, uint8_t *kmax, const uint8_t 
                                     int MBS, const int32_t *ctx, int B, int Hkv, int D, int BS, int64_t NB,
                                     cudaStream_t stream);
 
+// block scores only (the first launch of the fused Quest decode)
+cudaError_t launch_quest_scores(float *scores, const uint16_t *q, const void *kmin, const void *kmax,
+                                const int32_t *bt, int MBS, const int32_t *ctx, int B, int Hq, int Hkv, int D,
+                                int BS, int64_t NB, cudaStream_t stream, bool fp8 = false);
 // kmin / kmax: bf16 metadata, or E4M3 codes when fp8 (head_dim 128)
 cudaError_t launch_quest_select(int32_t *sel, float *scores, const uint16_t *q, const void *kmin,
                                 const void *kmax, const int32_t *bt, int MBS, const int32_t *ctx,

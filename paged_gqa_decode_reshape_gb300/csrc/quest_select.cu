@@ -20,10 +20,11 @@
 // block's two metadata rows with one 8-byte (D=128) load per lane, i.e. 256
 // contiguous bytes per row per warp, a whole chunk in flight.
 //
-// Top-K: one CTA per (sequence, KV head): a 4-pass, 8-bit radix select over
-// the totalOrder keys of the scores finds the K-th largest key; blocks above
-// it, then the lowest-index blocks equal to it, are written in ascending
-// block order.
+// Top-K: one CTA per (sequence, KV head): a radix select over the
+// totalOrder keys of the scores (digits of up to 8 bits, from the highest bit
+// where the row's keys differ) finds the K-th largest key; blocks above it,
+// then the lowest-index blocks equal to it, are written in ascending block
+// order (cta_topk_threshold, cta_topk_emit).
 #include "common.cuh"
 #include "kernels.h"
 
@@ -193,42 +194,21 @@ __global__ void __launch_bounds__(kScoreThreads, 4) quest_score_kernel(
     }
 }
 
-// block-wide exclusive scan of a 0/1 flag (kTopkThreads threads)
-__device__ __forceinline__ int block_rank(bool flag, int *warp_cnt, int &total) {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const unsigned bal = __ballot_sync(0xffffffffu, flag);
-    const int in_warp = __popc(bal & ((1u << lane) - 1u));
-    __syncthreads();
-    if (lane == 0) warp_cnt[warp] = __popc(bal);
-    __syncthreads();
-    int before = 0;
-    total = 0;
-#pragma unroll
-    for (int w = 0; w < kTopkThreads / 32; ++w) {
-        const int c = warp_cnt[w];
-        before += (w < warp) ? c : 0;
-        total += c;
-    }
-    return before + in_warp;
-}
-
 // Keys cached in shared memory (12 KiB; longer rows are re-read from L2 on
-// every pass): small, so that many top-K CTAs fit on an SM.
+// every pass): small, so that a top-K CTA fits on an SM beside a decode CTA.
 constexpr int kTopkSmemKeys = 3072;
 
-// At most 32 registers (8 CTAs per SM).
-__global__ void __launch_bounds__(kTopkThreads, 8) quest_topk_kernel(
+__global__ void __launch_bounds__(kTopkThreads, 4) quest_topk_kernel(
     int32_t *__restrict__ sel, const float *__restrict__ scores, int MBS,
     const int32_t *__restrict__ ctx, int Hkv, int BS, int topk) {
     __shared__ int hist[256];
-    __shared__ int warp_cnt[kTopkThreads / 32];
-    __shared__ int sh_digit, sh_above;
+    __shared__ int red[2 * kTopkThreads / 32 + 2];
     __shared__ uint32_t keys[kTopkSmemKeys];
     pdl_trigger();
     pdl_wait();
     const int seg = blockIdx.x;
     const int b = seg / Hkv;
-    const int tid = threadIdx.x, lane = tid & 31;
+    const int tid = threadIdx.x;
     const int c = min(max(__ldg(ctx + b), 0), MBS * BS);
     const int n = (c + BS - 1) / BS;
     const float *srow = scores + int64_t(seg) * MBS;
@@ -239,69 +219,13 @@ __global__ void __launch_bounds__(kTopkThreads, 8) quest_topk_kernel(
     }
     // totalOrder keys of the segment's scores: in shared memory when they fit
     const bool cached = n <= kTopkSmemKeys;
-    if (cached)
-        for (int j = tid; j < n; j += kTopkThreads) keys[j] = f32_order_key(__ldcg(srow + j));
+    if (cached) cta_load_keys<kTopkThreads>(keys, srow, n);
+    __syncthreads();
     auto key_of = [&](int j) -> uint32_t { return cached ? keys[j] : f32_order_key(__ldcg(srow + j)); };
-    uint32_t prefix = 0, mask = 0;
-    int k = topk;
-    for (int shift = 24; shift >= 0; shift -= 8) {
-        hist[tid] = 0;  // kTopkThreads == 256 bins
-        __syncthreads();
-        for (int j = tid; j < n; j += kTopkThreads) {
-            const uint32_t u = key_of(j);
-            if ((u & mask) == prefix) atomicAdd(&hist[(u >> shift) & 255u], 1);
-        }
-        __syncthreads();
-        if (tid < 32) {
-            // lane l holds digits 255-8l .. 248-8l (descending)
-            int cnt[8], s = 0;
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                cnt[i] = hist[255 - 8 * lane - i];
-                s += cnt[i];
-            }
-            int incl = s;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const int v = __shfl_up_sync(0xffffffffu, incl, o);
-                if (lane >= o) incl += v;
-            }
-            int before = incl - s;
-            if (before < k && k <= incl) {
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    if (before + cnt[i] >= k) {
-                        sh_digit = 255 - 8 * lane - i;
-                        sh_above = before;
-                        break;
-                    }
-                    before += cnt[i];
-                }
-            }
-        }
-        __syncthreads();
-        prefix |= uint32_t(sh_digit) << shift;
-        mask |= 0xffu << shift;
-        k -= sh_above;
-        __syncthreads();
-    }
-    // prefix is the K-th largest key; take every key above it and the k
-    // lowest-index keys equal to it, in ascending block order
-    int carry_eq = 0, carry_pos = 0;
-    for (int j0 = 0; j0 < n; j0 += kTopkThreads) {
-        const int j = j0 + tid;
-        const uint32_t u = j < n ? key_of(j) : 0u;
-        const bool gt = j < n && u > prefix;
-        const bool eq = j < n && u == prefix;
-        int tot_eq;
-        const int r_eq = block_rank(eq, warp_cnt, tot_eq) + carry_eq;
-        const bool take = gt || (eq && r_eq < k);
-        int tot_take;
-        const int r_take = block_rank(take, warp_cnt, tot_take) + carry_pos;
-        if (take) out[r_take] = j;
-        carry_eq += tot_eq;
-        carry_pos += tot_take;
-    }
+    uint32_t thr;
+    int keq;
+    cta_topk_threshold<kTopkThreads>(key_of, n, topk, hist, red, thr, keq);
+    cta_topk_emit<kTopkThreads>(key_of, n, thr, keq, red, [&](int r, int j) { out[r] = j; });
 }
 
 template <int D, bool F8>
@@ -326,6 +250,17 @@ cudaError_t launch_score(float *scores, const uint16_t *q, const void *kmin, con
 }
 
 }  // namespace
+
+cudaError_t launch_quest_scores(float *scores, const uint16_t *q, const void *kmin, const void *kmax,
+                                const int32_t *bt, int MBS, const int32_t *ctx, int B, int Hq, int Hkv, int D,
+                                int BS, int64_t NB, cudaStream_t stream, bool fp8) {
+    if (fp8) {
+        if (D != 128) return cudaErrorInvalidValue;
+        return launch_score<128, true>(scores, q, kmin, kmax, bt, MBS, ctx, B, Hq, Hkv, BS, NB, stream);
+    }
+    return D == 128 ? launch_score<128, false>(scores, q, kmin, kmax, bt, MBS, ctx, B, Hq, Hkv, BS, NB, stream)
+                    : launch_score<64, false>(scores, q, kmin, kmax, bt, MBS, ctx, B, Hq, Hkv, BS, NB, stream);
+}
 
 cudaError_t launch_quest_select(int32_t *sel, float *scores, const uint16_t *q, const void *kmin,
                                 const void *kmax, const int32_t *bt, int MBS, const int32_t *ctx,

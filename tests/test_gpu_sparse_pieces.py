@@ -1,6 +1,6 @@
 """Sparse decode of small selections: the grid follows the (sequence, KV
-head) segments, each cut into 2, 4 or 8 equal pieces (one CTA each) that
-are merged with the split-KV combine. Parity against the CPU oracle (bf16
+head) segments, each cut into equal pieces (one CTA each, their number set
+by the CTA budget) that are merged with the split-KV combine. Parity against the CPU oracle (bf16
 and 8-bit caches), with an empty sequence and a sequence shorter than the
 selection (-1 padding, so some pieces hold invalid entries) in the batch."""
 
@@ -17,8 +17,9 @@ from tests.test_gpu_parity import run_full_compare
 
 pytestmark = pytest.mark.gpu
 
-# name: (B, Hq, Hkv, topk, context lengths); with at least 24 items per piece
-# the segments split into 2, 4, 4 and 8 pieces
+# name: (B, Hq, Hkv, topk, context lengths); with one CTA per SM allowed and
+# at least 16 items per piece the segments split into 4, 8, 8 and 8 pieces
+# (fewer under a smaller CTA budget)
 CASES = {
     "pieces2": (4, 28, 4, 64, [0, 700, 1500, 2200]),
     "pieces4": (4, 28, 4, 128, [2500, 0, 1000, 3000]),
@@ -81,3 +82,28 @@ def test_segment_pieces_fixed_selection(name):
 @pytest.mark.parametrize("name", ["pieces2", "pieces8"])
 def test_segment_pieces_fp8(name):
     run_fp8_compare(make_case(name))
+
+
+@pytest.mark.parametrize("max_ctas", [1, 3, 16, 64, 0])
+@pytest.mark.parametrize("name", ["pieces4", "pieces8"])
+def test_segment_pieces_under_a_cta_budget(name, max_ctas):
+    """quest_sparse_decode_budget: one CTA for everything, a few CTAs holding
+    several segments each, and segments cut into fewer pieces than the whole
+    GPU allows; each result within tolerance of the oracle and the same on a
+    second call."""
+    import paged_gqa_decode_reshape_gb300 as pg
+    w = make_case(name)
+    dev, ora = DeviceStep(w), OracleStep(w)
+    dev.reshape()
+    ora.reshape()
+    sel_h = workloads.random_selection(w, seed=4)
+    sel = torch.from_numpy(sel_h).to(dev.dev)
+    outs = []
+    for _ in range(2):
+        out = torch.full_like(dev.out, float("nan"))
+        pg.quest_sparse_decode_budget(out, dev.q, dev.kc, dev.vc, dev.bt, dev.ctx, sel, w.scale, max_ctas,
+                                      workspace=dev.ws)
+        outs.append(out)
+    assert torch.equal(outs[0].view(torch.int16), outs[1].view(torch.int16))
+    assert_close_attention(to_host_f64(outs[0]), ora.sparse(sel_h), f"{name} budget {max_ctas}")
+    assert pg.pa_workspace_status(dev.ws) == 0

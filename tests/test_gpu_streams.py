@@ -1,6 +1,6 @@
 """The step's calls on two streams give results bit-identical to the same
-calls on one stream. On two streams the Quest selection and sparse decode
-run beside the dense decode, and each decode call has its own workspace.
+calls on one stream. On two streams the Quest path (quest_decode) runs
+beside the dense decode, and each decode call has its own workspace.
 Every kernel's output is a deterministic function of its inputs (the split-KV
 combine merges the pieces in a fixed order), so running calls at the same
 time may change timing but never a bit of the results. The results are
@@ -49,7 +49,7 @@ def test_two_stream_step_matches_one_stream(name, kw, kv):
     st = bench.Step(w, torch.device("cuda:0"), kv)
     results = []
     for serial in (True, False, True, False):
-        run = bench.step_runner(torch, st.calls(), serial)
+        run = bench.step_runner(torch, st, serial, quest=st.quest_beside())  # the same grids in both orders
         for _ in range(2):  # the write path is idempotent: the same tokens into the same slots
             st.out_buf.zero_()
             run()
