@@ -97,6 +97,16 @@ def load(path: str):
     L.oracle_attention_fp8.restype = i32
     L.oracle_quest_scores_kernel_order_fp8.argtypes = score
     L.oracle_quest_scores_kernel_order_fp8.restype = i32
+    L.oracle_reshape_and_cache_fp8_block.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i64, i32, i32, i32,
+                                                     i64]
+    L.oracle_reshape_and_cache_fp8_block.restype = i64
+    L.oracle_attention_fp8_block.argtypes = L.oracle_attention_fp8.argtypes
+    L.oracle_attention_fp8_block.restype = i32
+    bscore = [vp, vp, vp, vp, vp, vp, i32, vp, i32, i32, i32, i32, i32, i64]
+    L.oracle_quest_scores_kernel_order_fp8_block.argtypes = bscore
+    L.oracle_quest_scores_kernel_order_fp8_block.restype = i32
+    L.oracle_quest_scores_plain_fp8_block.argtypes = [vp] + bscore
+    L.oracle_quest_scores_plain_fp8_block.restype = i32
     L.oracle_paged_attention_multi.argtypes = [vp, vp, vp, vp, vp, i32, vp, vp, i32, i32, i32,
                                                i32, i32, i32, i64, f64, vp, i64]
     L.oracle_paged_attention_multi.restype = i32
@@ -358,6 +368,29 @@ def reshape_and_cache_fp8(key, value, key_cache, value_cache, slot_mapping, k_sc
                                                   NB))
 
 
+def reshape_and_cache_fp8_block(key, value, key_cache, value_cache, slot_mapping, k_bscale, v_bscale,
+                                kmin=None, kmax=None) -> int:
+    """Quantise and scatter new K/V rows into uint8 E4M3 caches with per-block
+    power-of-two scales, IN PLACE (caches, k_bscale / v_bscale [NB, Hkv]
+    float32, and the E4M3 metadata kmin / kmax [NB, Hkv, D] when given);
+    returns #out-of-pool slots. A scale of 0 marks a block that holds nothing."""
+    for a in (key_cache, value_cache):
+        assert a.dtype == np.uint8 and a.flags.c_contiguous
+    NB, BS, Hkv, D = key_cache.shape
+    assert value_cache.shape == (NB, Hkv, D, BS) and BS == 16
+    for a in (k_bscale, v_bscale):
+        assert a.dtype == np.float32 and a.flags.c_contiguous and a.shape == (NB, Hkv)
+    if kmin is not None:
+        for a in (kmin, kmax):
+            assert a.dtype == np.uint8 and a.flags.c_contiguous and a.shape == (NB, Hkv, D)
+    key = _c(key, np.uint16)
+    value = _c(value, np.uint16)
+    slots = _c(slot_mapping, np.int64)
+    return int(lib().oracle_reshape_and_cache_fp8_block(_p(key), _p(value), _p(key_cache), _p(value_cache),
+                                                        _p(kmin), _p(kmax), _p(k_bscale), _p(v_bscale),
+                                                        _p(slots), slots.shape[0], Hkv, D, BS, NB))
+
+
 def quest_update_meta_fp8(kmin, kmax, key, slot_mapping, k_scale, BS: int) -> int:
     """Incremental Quest metadata (E4M3 codes) update IN PLACE; returns #out-of-pool slots."""
     assert kmin.dtype == np.uint8 and kmin.flags.c_contiguous
@@ -389,7 +422,8 @@ def quest_rebuild_meta_fp8(key_cache, block_tables, context_lens, kmin=None, kma
 def attention_fp8(q, key_cache, value_cache, k_scale, v_scale, block_tables, context_lens, scale,
                   selected=None, rows=None):
     """Dense (selected None) or Quest sparse attention over E4M3 caches, fp64
-    (value_cache in the [NB, Hkv, D, 16] layout of reshape_and_cache_fp8)."""
+    (value_cache in the [NB, Hkv, D, 16] layout of reshape_and_cache_fp8).
+    k_scale / v_scale: [Hkv] per-KV-head scales, or [NB, Hkv] per-block scales."""
     q = _c(q, np.uint16)
     kc = _c(key_cache, np.uint8)
     vc = _c(value_cache, np.uint8)
@@ -399,7 +433,9 @@ def attention_fp8(q, key_cache, value_cache, k_scale, v_scale, block_tables, con
     ctx = _c(context_lens, np.int32)
     B, Hq, D = q.shape
     NB, BS, Hkv, D2 = kc.shape
-    assert D == D2 and vc.shape == (NB, Hkv, D, BS) and ks.shape == (Hkv,) and vs.shape == (Hkv,)
+    per_block = ks.ndim == 2
+    want = (NB, Hkv) if per_block else (Hkv,)
+    assert D == D2 and vc.shape == (NB, Hkv, D, BS) and ks.shape == want and vs.shape == want
     sel, topk = None, 0
     if selected is not None:
         sel = _c(selected, np.int32)
@@ -407,40 +443,69 @@ def attention_fp8(q, key_cache, value_cache, k_scale, v_scale, block_tables, con
         topk = sel.shape[2]
     r, nr = _rows_arg(rows)
     out = np.zeros((nr, D) if r is not None else (B, Hq, D), dtype=np.float64)
-    rc = lib().oracle_attention_fp8(_p(out), _p(q), _p(kc), _p(vc), _p(ks), _p(vs), _p(bt),
-                                    bt.shape[1], _p(ctx), _p(sel), topk, B, Hq, Hkv, D, BS, NB,
-                                    float(scale), _p(r), nr)
+    fn = lib().oracle_attention_fp8_block if per_block else lib().oracle_attention_fp8
+    rc = fn(_p(out), _p(q), _p(kc), _p(vc), _p(ks), _p(vs), _p(bt), bt.shape[1], _p(ctx), _p(sel), topk,
+            B, Hq, Hkv, D, BS, NB, float(scale), _p(r), nr)
     _check(rc, "attention_fp8")
     return out
 
 
-def quest_scores_fp8(q, kmin, kmax, block_tables, context_lens, BS: int, with_abs: bool = False):
-    """Plain fp64 Quest scores over E4M3 metadata (min/max = decoded codes;
-    the per-KV-head K scale, a positive factor of a whole row, is left out)."""
-    return _scores_plain(lib().oracle_quest_scores_plain_fp8, q, kmin, kmax, block_tables, context_lens,
-                         BS, np.uint8, with_abs)
+def _bscale_arg(k_bscale, NB, Hkv):
+    if k_bscale is None:
+        return None
+    ks = _c(k_bscale, np.float32)
+    assert ks.shape == (NB, Hkv)
+    return ks
 
 
-def quest_scores_kernel_order_fp8(q, kmin, kmax, block_tables, context_lens, BS: int):
-    """fp32 kernel-order scores over E4M3 metadata, [B, Hkv, MBS] float32."""
+def quest_scores_fp8(q, kmin, kmax, block_tables, context_lens, BS: int, with_abs: bool = False,
+                     k_bscale=None):
+    """Plain fp64 Quest scores over E4M3 metadata (min/max = decoded codes).
+    With per-KV-head scales (k_bscale None) the K scale, a positive factor of
+    a whole row, is left out; with per-block scales k_bscale [NB, Hkv] each
+    block's score carries its own K scale."""
+    if k_bscale is None:
+        return _scores_plain(lib().oracle_quest_scores_plain_fp8, q, kmin, kmax, block_tables,
+                             context_lens, BS, np.uint8, with_abs)
+    q, kmin, kmax, bt, ctx, (B, Hq, Hkv, D, NB, MBS) = _score_args(q, kmin, kmax, block_tables,
+                                                                   context_lens, np.uint8)
+    ks = _bscale_arg(k_bscale, NB, Hkv)
+    out = np.empty((B, Hkv, MBS), dtype=np.float64)
+    absum = np.empty((B, Hkv, MBS), dtype=np.float64)
+    rc = lib().oracle_quest_scores_plain_fp8_block(_p(out), _p(absum), _p(q), _p(kmin), _p(kmax), _p(ks),
+                                                   _p(bt), MBS, _p(ctx), B, Hq, Hkv, D, BS, NB)
+    _check(rc, "quest_scores_fp8 (per-block scales)")
+    return (out, absum) if with_abs else out
+
+
+def quest_scores_kernel_order_fp8(q, kmin, kmax, block_tables, context_lens, BS: int, k_bscale=None):
+    """fp32 kernel-order scores over E4M3 metadata, [B, Hkv, MBS] float32
+    (times the block's K scale when per-block scales k_bscale are given)."""
     q, kmin, kmax, bt, ctx, (B, Hq, Hkv, D, NB, MBS) = _score_args(q, kmin, kmax, block_tables,
                                                                    context_lens, np.uint8)
     out = np.empty((B, Hkv, MBS), dtype=np.float32)
-    rc = lib().oracle_quest_scores_kernel_order_fp8(_p(out), _p(q), _p(kmin), _p(kmax), _p(bt), MBS,
-                                                    _p(ctx), B, Hq, Hkv, D, BS, NB)
+    if k_bscale is None:
+        rc = lib().oracle_quest_scores_kernel_order_fp8(_p(out), _p(q), _p(kmin), _p(kmax), _p(bt), MBS,
+                                                        _p(ctx), B, Hq, Hkv, D, BS, NB)
+    else:
+        ks = _bscale_arg(k_bscale, NB, Hkv)
+        rc = lib().oracle_quest_scores_kernel_order_fp8_block(_p(out), _p(q), _p(kmin), _p(kmax), _p(ks),
+                                                              _p(bt), MBS, _p(ctx), B, Hq, Hkv, D, BS, NB)
     _check(rc, "quest_scores_kernel_order_fp8")
     return out
 
 
-def quest_select_fp8(q, kmin, kmax, block_tables, context_lens, BS: int, topk: int):
+def quest_select_fp8(q, kmin, kmax, block_tables, context_lens, BS: int, topk: int, k_bscale=None):
     """Top-K of the plain fp64 scores over E4M3 metadata."""
-    return quest_topk(quest_scores_fp8(q, kmin, kmax, block_tables, context_lens, BS),
+    return quest_topk(quest_scores_fp8(q, kmin, kmax, block_tables, context_lens, BS, k_bscale=k_bscale),
                       context_lens, BS, topk)
 
 
-def quest_select_kernel_order_fp8(q, kmin, kmax, block_tables, context_lens, BS: int, topk: int):
+def quest_select_kernel_order_fp8(q, kmin, kmax, block_tables, context_lens, BS: int, topk: int,
+                                  k_bscale=None):
     """Top-K of the fp32 kernel-order scores over E4M3 metadata."""
-    return quest_topk(quest_scores_kernel_order_fp8(q, kmin, kmax, block_tables, context_lens, BS),
+    return quest_topk(quest_scores_kernel_order_fp8(q, kmin, kmax, block_tables, context_lens, BS,
+                                                    k_bscale=k_bscale),
                       context_lens, BS, topk)
 
 

@@ -460,6 +460,172 @@ int oracle_quest_rebuild_meta_fp8(uint8_t *kmin, uint8_t *kmax, const uint8_t *k
     return 0;
 }
 
+/* ------------------- fp8 KV cache with per-block power-of-two scales */
+
+/* The 8-bit cache with a scale per physical block instead of per KV head
+ * (the pages name "fp8 K/V with a per-block scale" as the quantised form of
+ * the cache without fixing how the scale is chosen; this is the plainest
+ * reading that works for a cache filled one token at a time). Every
+ * (physical block p, KV head h) has a K scale k_bscale[p*Hkv + h] and a V
+ * scale v_bscale[p*Hkv + h], each a power of two, or 0 while the block holds
+ * nothing. One call's write to block p, for K (V alike, without metadata):
+ *   1. members: the call's tokens whose slot lands in p; the block restarts
+ *      (reset) if a member lands at offset 0;
+ *   2. a = the largest finite |x| over the members' elements of head h;
+ *   3. e_call = the smallest integer e >= -126 with a <= 448 * 2^e;
+ *   4. e_old = log2 of the stored scale, unless the block restarts or the
+ *      stored scale is 0 (then there is no e_old);
+ *   5. e = max(e_old, e_call); the stored scale becomes 2^e;
+ *   6. if e > e_old, every stored code of (p, h) at an offset no member
+ *      writes is re-encoded: c <- e4m3(decode(c) * 2^(e_old - e));
+ *   7. each member's element is stored as e4m3(fl32(x / 2^e)) (the division
+ *      by a power of two is exact);
+ *   8. metadata (K): on a restart the min / max of the members' codes; else
+ *      the stored min / max, re-encoded as in 6 when e grew, merged with the
+ *      members' codes.
+ * Because 2^(e_old - e) is a power of two, step 6 changes no value that
+ * stays in the E4M3 normal range; only codes that fall below 2^-6 round.
+ * Step 8 equals the min / max of the re-encoded codes, as rounding to
+ * nearest is monotone. Returns the number of out-of-pool slots skipped, -2
+ * for block_size != 16. */
+static int block_fit_exponent(double a)
+{
+    int e = -126;
+    while (a > ldexp(448.0, e))
+        ++e;
+    return e;
+}
+
+static void block_scale_step(float *scale_slot, int reset, double amax, int *e_old, int *e_new)
+{
+    const float s = *scale_slot;
+    int have_old = 0, eo = 0;
+    if (!reset && s > 0.0f) {
+        int E = 0;
+        (void)frexp((double)s, &E); /* s = 0.5 * 2^E for a power of two */
+        eo = E - 1;
+        have_old = 1;
+    }
+    const int ec = block_fit_exponent(amax);
+    const int en = have_old && eo > ec ? eo : ec;
+    *e_old = have_old ? eo : en; /* no rescale without an old scale */
+    *e_new = en;
+    *scale_slot = (float)ldexp(1.0, en);
+}
+
+static uint8_t rescale_code(uint8_t c, int shift) /* shift = e_old - e_new <= 0 */
+{
+    if (shift == 0)
+        return c;
+    return oracle_e4m3_encode((float)(oracle_e4m3_decode(c) * ldexp(1.0, shift)));
+}
+
+int64_t oracle_reshape_and_cache_fp8_block(const uint16_t *key, const uint16_t *value,
+                                           uint8_t *key_cache, uint8_t *value_cache,
+                                           uint8_t *kmin, uint8_t *kmax,
+                                           float *k_bscale, float *v_bscale,
+                                           const int64_t *slot_mapping, int64_t T,
+                                           int Hkv, int D, int BS, int64_t NB)
+{
+    if (BS != 16)
+        return -2;
+    const int64_t row = (int64_t)Hkv * D;
+    int64_t out_of_range = 0;
+    unsigned char *done = (unsigned char *)calloc((size_t)T + 1, 1);
+    for (int64_t t = 0; t < T; ++t) {
+        const int64_t s = slot_mapping[t];
+        if (s < 0 || done[t])
+            continue;
+        const int64_t p = s / BS;
+        if (p >= NB) {
+            ++out_of_range;
+            done[t] = 1;
+            continue;
+        }
+        /* step 1: members (t and the later tokens of the call in block p) */
+        int reset = 0;
+        unsigned written = 0; /* offsets the call writes */
+        for (int64_t u = t; u < T; ++u) {
+            const int64_t su = slot_mapping[u];
+            if (su < 0 || su / BS != p)
+                continue;
+            written |= 1u << (su % BS);
+            if (su % BS == 0)
+                reset = 1;
+        }
+        for (int h = 0; h < Hkv; ++h) {
+            /* step 2 */
+            double ak = 0.0, av = 0.0;
+            for (int64_t u = t; u < T; ++u) {
+                const int64_t su = slot_mapping[u];
+                if (su < 0 || su / BS != p)
+                    continue;
+                for (int d = 0; d < D; ++d) {
+                    const double xk = fabs(bf16_val(key[u * row + (int64_t)h * D + d]));
+                    const double xv = fabs(bf16_val(value[u * row + (int64_t)h * D + d]));
+                    if (isfinite(xk) && xk > ak)
+                        ak = xk;
+                    if (isfinite(xv) && xv > av)
+                        av = xv;
+                }
+            }
+            /* steps 3-5 */
+            int eko, ekn, evo, evn;
+            block_scale_step(&k_bscale[p * Hkv + h], reset, ak, &eko, &ekn);
+            block_scale_step(&v_bscale[p * Hkv + h], reset, av, &evo, &evn);
+            /* step 6: the block's other offsets, and step 8's stored min / max */
+            for (int o = 0; o < BS; ++o) {
+                if (written & (1u << o))
+                    continue;
+                for (int d = 0; d < D; ++d) {
+                    uint8_t *kc = &key_cache[(p * BS + o) * row + (int64_t)h * D + d];
+                    *kc = rescale_code(*kc, eko - ekn);
+                    uint8_t *vc = &value_cache[vt_index(p, o, h, d, Hkv, D)];
+                    *vc = rescale_code(*vc, evo - evn);
+                }
+            }
+            const float ks = (float)ldexp(1.0, ekn), vs = (float)ldexp(1.0, evn);
+            int have = 0;
+            if (kmin && !reset) {
+                for (int d = 0; d < D; ++d) {
+                    const int64_t m = (p * Hkv + h) * (int64_t)D + d;
+                    kmin[m] = rescale_code(kmin[m], eko - ekn);
+                    kmax[m] = rescale_code(kmax[m], eko - ekn);
+                }
+                have = 1;
+            }
+            /* step 7, and step 8's merge */
+            for (int64_t u = t; u < T; ++u) {
+                const int64_t su = slot_mapping[u];
+                if (su < 0 || su / BS != p)
+                    continue;
+                const int64_t o = su % BS;
+                for (int d = 0; d < D; ++d) {
+                    const int64_t e = (int64_t)h * D + d;
+                    const uint8_t c = quantize(key[u * row + e], ks);
+                    key_cache[(p * BS + o) * row + e] = c;
+                    value_cache[vt_index(p, o, h, d, Hkv, D)] = quantize(value[u * row + e], vs);
+                    if (kmin) {
+                        const int64_t m = (p * Hkv + h) * (int64_t)D + d;
+                        if (!have || e4m3_order_key(c) < e4m3_order_key(kmin[m]))
+                            kmin[m] = c;
+                        if (!have || e4m3_order_key(c) > e4m3_order_key(kmax[m]))
+                            kmax[m] = c;
+                    }
+                }
+                have = 1;
+            }
+        }
+        for (int64_t u = t; u < T; ++u) {
+            const int64_t su = slot_mapping[u];
+            if (su >= 0 && su / BS == p)
+                done[u] = 1;
+        }
+    }
+    free(done);
+    return out_of_range;
+}
+
 /* ------------------------------------------------------------ attention */
 
 /* The tokens one (sequence, KV head) attends to, in order.
@@ -490,13 +656,14 @@ static int64_t token_list(int64_t *pos, int64_t ctx, int BS,
 }
 
 /* A K or V cache as the attention reads it: bf16 elements, or E4M3 codes
- * with one fp32 scale per KV head (element value = decode(code) * scale,
- * exact in fp64). */
+ * with one fp32 scale per KV head, or per (physical block, KV head) when
+ * per_block is set (element value = decode(code) * scale, exact in fp64). */
 typedef struct {
     const uint16_t *bf16;
     const uint8_t *e4m3;
     const float *scale;
     int vt, Hkv, D, BS; /* vt: E4M3 codes in the V layout (vt_index) */
+    int per_block;      /* scale[p * Hkv + kvh] instead of scale[kvh] */
 } kvsrc;
 
 /* element idx of the [NB][BS][Hkv][D] index space */
@@ -504,12 +671,13 @@ static double kv_val(const kvsrc *c, int64_t idx, int kvh)
 {
     if (c->bf16)
         return bf16_val(c->bf16[idx]);
+    const int64_t p = idx / ((int64_t)c->D * c->Hkv * c->BS);
+    const double sc = (double)c->scale[c->per_block ? p * c->Hkv + kvh : kvh];
     if (c->vt) {
         const int64_t d = idx % c->D, o = (idx / ((int64_t)c->D * c->Hkv)) % c->BS;
-        const int64_t p = idx / ((int64_t)c->D * c->Hkv * c->BS);
         idx = vt_index(p, o, kvh, d, c->Hkv, c->D);
     }
-    return oracle_e4m3_decode(c->e4m3[idx]) * (double)c->scale[kvh];
+    return oracle_e4m3_decode(c->e4m3[idx]) * sc;
 }
 
 /* Element index of K (or V) of sequence position t for one KV head through
@@ -726,7 +894,7 @@ int oracle_paged_attention(double *out, const uint16_t *q,
                            int D, int BS, int64_t NB, double scale,
                            const int32_t *rows, int64_t nrows)
 {
-    const kvsrc K = {key_cache, NULL, NULL, 0, 0, 0, 0}, V = {value_cache, NULL, NULL, 0, 0, 0, 0};
+    const kvsrc K = {key_cache, NULL, NULL, 0, 0, 0, 0, 0}, V = {value_cache, NULL, NULL, 0, 0, 0, 0, 0};
     return attention_rows(out, q, &K, &V, block_tables, MBS, context_lens,
                           NULL, 0, B, Hq, Hkv, D, BS, NB, scale, rows, nrows, 0, 0);
 }
@@ -741,7 +909,7 @@ int oracle_paged_attention_online(double *out, const uint16_t *q,
 {
     if (chunk <= 0)
         return -2;
-    const kvsrc K = {key_cache, NULL, NULL, 0, 0, 0, 0}, V = {value_cache, NULL, NULL, 0, 0, 0, 0};
+    const kvsrc K = {key_cache, NULL, NULL, 0, 0, 0, 0, 0}, V = {value_cache, NULL, NULL, 0, 0, 0, 0, 0};
     return attention_rows(out, q, &K, &V, block_tables, MBS, context_lens,
                           NULL, 0, B, Hq, Hkv, D, BS, NB, scale, NULL, 0, 1, chunk);
 }
@@ -755,7 +923,7 @@ int oracle_paged_attention_split(double *out, const uint16_t *q,
 {
     if (num_splits <= 0)
         return -2;
-    const kvsrc K = {key_cache, NULL, NULL, 0, 0, 0, 0}, V = {value_cache, NULL, NULL, 0, 0, 0, 0};
+    const kvsrc K = {key_cache, NULL, NULL, 0, 0, 0, 0, 0}, V = {value_cache, NULL, NULL, 0, 0, 0, 0, 0};
     return attention_rows(out, q, &K, &V, block_tables, MBS, context_lens,
                           NULL, 0, B, Hq, Hkv, D, BS, NB, scale, NULL, 0, 2, num_splits);
 }
@@ -773,7 +941,7 @@ int oracle_sparse_attention(double *out, const uint16_t *q,
 {
     if (topk <= 0)
         return -2;
-    const kvsrc K = {key_cache, NULL, NULL, 0, 0, 0, 0}, V = {value_cache, NULL, NULL, 0, 0, 0, 0};
+    const kvsrc K = {key_cache, NULL, NULL, 0, 0, 0, 0, 0}, V = {value_cache, NULL, NULL, 0, 0, 0, 0, 0};
     return attention_rows(out, q, &K, &V, block_tables, MBS, context_lens,
                           selected, topk, B, Hq, Hkv, D, BS, NB, scale, rows, nrows, 0, 0);
 }
@@ -791,8 +959,28 @@ int oracle_attention_fp8(double *out, const uint16_t *q,
 {
     if ((selected && topk <= 0) || BS != 16)
         return -2;
-    const kvsrc K = {NULL, key_cache, k_scale, 0, Hkv, D, BS};
-    const kvsrc V = {NULL, value_cache, v_scale, 1, Hkv, D, BS};
+    const kvsrc K = {NULL, key_cache, k_scale, 0, Hkv, D, BS, 0};
+    const kvsrc V = {NULL, value_cache, v_scale, 1, Hkv, D, BS, 0};
+    return attention_rows(out, q, &K, &V, block_tables, MBS, context_lens,
+                          selected, selected ? topk : 0, B, Hq, Hkv, D, BS, NB, scale, rows,
+                          nrows, 0, 0);
+}
+
+/* The same attention over an E4M3 cache with per-block scales: element value
+ * decode(code) * k_bscale[p * Hkv + kvh] (V alike), p the token's physical
+ * block. */
+int oracle_attention_fp8_block(double *out, const uint16_t *q,
+                               const uint8_t *key_cache, const uint8_t *value_cache,
+                               const float *k_bscale, const float *v_bscale,
+                               const int32_t *block_tables, int MBS,
+                               const int32_t *context_lens, const int32_t *selected, int topk,
+                               int B, int Hq, int Hkv, int D, int BS, int64_t NB, double scale,
+                               const int32_t *rows, int64_t nrows)
+{
+    if ((selected && topk <= 0) || BS != 16)
+        return -2;
+    const kvsrc K = {NULL, key_cache, k_bscale, 0, Hkv, D, BS, 1};
+    const kvsrc V = {NULL, value_cache, v_bscale, 1, Hkv, D, BS, 1};
     return attention_rows(out, q, &K, &V, block_tables, MBS, context_lens,
                           selected, selected ? topk : 0, B, Hq, Hkv, D, BS, NB, scale, rows,
                           nrows, 0, 0);
@@ -824,7 +1012,7 @@ int oracle_paged_attention_multi(double *out, const uint16_t *q,
         if (cu_seqlens_q[b + 1] < cu_seqlens_q[b])
             return -2;
     const int G = Hq / Hkv;
-    const kvsrc K = {key_cache, NULL, NULL, 0, 0, 0, 0}, V = {value_cache, NULL, NULL, 0, 0, 0, 0};
+    const kvsrc K = {key_cache, NULL, NULL, 0, 0, 0, 0, 0}, V = {value_cache, NULL, NULL, 0, 0, 0, 0, 0};
     const int64_t max_tokens = (int64_t)MBS * BS;
     int64_t *pos = (int64_t *)malloc(sizeof(int64_t) * (size_t)(max_tokens + 1));
     double *s = (double *)malloc(sizeof(double) * (size_t)(max_tokens + 1));
@@ -885,6 +1073,7 @@ static float meta_f32(const uint16_t *m16, const uint8_t *m8, int64_t idx)
 static int quest_scores_plain_impl(double *scores, double *abs_sum, const uint16_t *q,
                                    const uint16_t *kmin, const uint16_t *kmax,
                                    const uint8_t *kmin8, const uint8_t *kmax8,
+                                   const float *k_bscale,
                                    const int32_t *block_tables, int MBS,
                                    const int32_t *context_lens, int B, int Hq, int Hkv,
                                    int D, int BS, int64_t NB)
@@ -920,6 +1109,10 @@ static int quest_scores_plain_impl(double *scores, double *abs_sum, const uint16
                         a += fabs(qv) * m;
                     }
                 }
+                if (k_bscale) { /* per-block K scale: min, max and the score scale with it */
+                    s *= (double)k_bscale[p * Hkv + kvh];
+                    a *= (double)k_bscale[p * Hkv + kvh];
+                }
                 scores[o] = s;
                 if (abs_sum)
                     abs_sum[o] = a;
@@ -935,7 +1128,7 @@ int oracle_quest_scores_plain(double *scores, double *abs_sum, const uint16_t *q
                               const int32_t *context_lens, int B, int Hq, int Hkv,
                               int D, int BS, int64_t NB)
 {
-    return quest_scores_plain_impl(scores, abs_sum, q, kmin, kmax, NULL, NULL, block_tables, MBS,
+    return quest_scores_plain_impl(scores, abs_sum, q, kmin, kmax, NULL, NULL, NULL, block_tables, MBS,
                                    context_lens, B, Hq, Hkv, D, BS, NB);
 }
 
@@ -948,8 +1141,23 @@ int oracle_quest_scores_plain_fp8(double *scores, double *abs_sum, const uint16_
                                   const int32_t *context_lens, int B, int Hq, int Hkv,
                                   int D, int BS, int64_t NB)
 {
-    return quest_scores_plain_impl(scores, abs_sum, q, NULL, NULL, kmin, kmax, block_tables, MBS,
+    return quest_scores_plain_impl(scores, abs_sum, q, NULL, NULL, kmin, kmax, NULL, block_tables, MBS,
                                    context_lens, B, Hq, Hkv, D, BS, NB);
+}
+
+/* The plain score over E4M3 metadata of a cache with per-block scales: the
+ * block's metadata stand for decode(code) * k_bscale[p * Hkv + kvh], so the
+ * block's score (and abs_sum) carry that factor, which differs from block to
+ * block. */
+int oracle_quest_scores_plain_fp8_block(double *scores, double *abs_sum, const uint16_t *q,
+                                        const uint8_t *kmin, const uint8_t *kmax,
+                                        const float *k_bscale,
+                                        const int32_t *block_tables, int MBS,
+                                        const int32_t *context_lens, int B, int Hq, int Hkv,
+                                        int D, int BS, int64_t NB)
+{
+    return quest_scores_plain_impl(scores, abs_sum, q, NULL, NULL, kmin, kmax, k_bscale, block_tables,
+                                   MBS, context_lens, B, Hq, Hkv, D, BS, NB);
 }
 
 /* --------------------------------- Quest score, fp32 kernel-order reproduction */
@@ -973,13 +1181,15 @@ int oracle_quest_scores_plain_fp8(double *scores, double *abs_sum, const uint16_
  *   3. D is cut into 32 equal chunks of C = D/32 consecutive d; chunk sum
  *      c_l = (((t_{lC} + t_{lC+1}) + ...) + t_{lC+C-1}), left to right;
  *   4. the 32 chunk sums are combined pairwise: for off = 16, 8, 4, 2, 1:
- *      c_l <- c_l + c_{l xor off}; the score is c_0.
+ *      c_l <- c_l + c_{l xor off}; the score is c_0;
+ *   5. (E4M3 cache with per-block scales only) fl(c_0 * k_bscale[p, kvh]).
  * Logical blocks j >= ceil(ctx/BS) are excluded (score -inf). A table entry
  * outside the pool also scores -inf.
  * scores: [B][Hkv][MBS] fp32. Requires D % 32 == 0. */
 static int quest_scores_impl(float *scores, const uint16_t *q,
                              const uint16_t *kmin, const uint16_t *kmax,
                              const uint8_t *kmin8, const uint8_t *kmax8,
+                             const float *k_bscale,
                              const int32_t *block_tables, int MBS,
                              const int32_t *context_lens, int B, int Hq, int Hkv,
                              int D, int BS, int64_t NB)
@@ -1033,7 +1243,9 @@ static int quest_scores_impl(float *scores, const uint16_t *q,
                         nc[l] = c[l] + c[l ^ off];
                     memcpy(c, nc, sizeof c);
                 }
-                srow[j] = c[0];
+                /* 5. per-block K scale (E4M3 cache with block scales): one
+                 * fp32 product, exact for a power of two */
+                srow[j] = k_bscale ? c[0] * k_bscale[p * Hkv + kvh] : c[0];
             }
         }
     }
@@ -1048,7 +1260,7 @@ int oracle_quest_scores_kernel_order(float *scores, const uint16_t *q,
                         const int32_t *context_lens, int B, int Hq, int Hkv,
                         int D, int BS, int64_t NB)
 {
-    return quest_scores_impl(scores, q, kmin, kmax, NULL, NULL, block_tables, MBS,
+    return quest_scores_impl(scores, q, kmin, kmax, NULL, NULL, NULL, block_tables, MBS,
                              context_lens, B, Hq, Hkv, D, BS, NB);
 }
 
@@ -1062,7 +1274,20 @@ int oracle_quest_scores_kernel_order_fp8(float *scores, const uint16_t *q,
                             const int32_t *context_lens, int B, int Hq, int Hkv,
                             int D, int BS, int64_t NB)
 {
-    return quest_scores_impl(scores, q, NULL, NULL, kmin, kmax, block_tables, MBS,
+    return quest_scores_impl(scores, q, NULL, NULL, kmin, kmax, NULL, block_tables, MBS,
+                             context_lens, B, Hq, Hkv, D, BS, NB);
+}
+
+/* The kernel-order score of a cache with per-block scales: the sum above,
+ * then one fp32 product with the block's K scale (step 5). */
+int oracle_quest_scores_kernel_order_fp8_block(float *scores, const uint16_t *q,
+                                               const uint8_t *kmin, const uint8_t *kmax,
+                                               const float *k_bscale,
+                                               const int32_t *block_tables, int MBS,
+                                               const int32_t *context_lens, int B, int Hq,
+                                               int Hkv, int D, int BS, int64_t NB)
+{
+    return quest_scores_impl(scores, q, NULL, NULL, kmin, kmax, k_bscale, block_tables, MBS,
                              context_lens, B, Hq, Hkv, D, BS, NB);
 }
 

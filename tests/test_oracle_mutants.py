@@ -17,6 +17,7 @@ import os
 import pytest
 
 import oracle
+import test_oracle_fp8_block_pins as FB
 import test_oracle_fp8_pins as F
 import test_oracle_multi_pins as M
 import test_oracle_pins as P
@@ -132,11 +133,29 @@ MUTANTS = [
      [_pin(F, "test_e4m3_encode_saturates_and_keeps_nan")]),
     ("fp8_quantise_multiplies", "const float y = bf16_f32(x) / scale;", "const float y = bf16_f32(x) * scale;", 1,
      [_pin(F, "test_fp8_write_quantises_each_element")]),
-    ("fp8_dequantise_without_scale", "return oracle_e4m3_decode(c->e4m3[idx]) * (double)c->scale[kvh];",
+    ("fp8_dequantise_without_scale", "return oracle_e4m3_decode(c->e4m3[idx]) * sc;",
      "return oracle_e4m3_decode(c->e4m3[idx]);", 1,
      [_pin(F, "test_fp8_attention_brute_force_any_scale")]),
     ("fp8_v_layout_natural_order", "return 4 * ((o & 7) >> 1) + 2 * (o >> 3) + (o & 1);", "return o;", 1,
      [_pin(F, "test_fp8_write_quantises_each_element")]),
+    # the 8-bit cache with per-block power-of-two scales
+    ("block_fit_pow2_max", "while (a > ldexp(448.0, e))", "while (a > ldexp(256.0, e))", 1,
+     [_pin(FB, "test_hand_worked_example"), _pin(FB, "test_first_write_scale_and_codes")]),
+    ("block_old_rows_not_rescaled", "*kc = rescale_code(*kc, eko - ekn);", "*kc = rescale_code(*kc, 0);", 1,
+     [_pin(FB, "test_hand_worked_example"), _pin(FB, "test_incremental_equals_from_scratch")]),
+    ("block_v_rows_use_k_shift", "*vc = rescale_code(*vc, evo - evn);", "*vc = rescale_code(*vc, eko - ekn);",
+     1, [_pin(FB, "test_incremental_equals_from_scratch")]),
+    ("block_meta_not_rescaled", "kmin[m] = rescale_code(kmin[m], eko - ekn);", "kmin[m] = kmin[m];", 1,
+     [_pin(FB, "test_incremental_equals_from_scratch")]),
+    ("block_restart_keeps_scale", "if (!reset && s > 0.0f) {", "if (s > 0.0f) {", 1,
+     [_pin(FB, "test_restart_resets_scale_and_keeps_other_rows")]),
+    ("block_kernel_order_score_unscaled", "srow[j] = k_bscale ? c[0] * k_bscale[p * Hkv + kvh] : c[0];",
+     "srow[j] = c[0];", 1, [_pin(FB, "test_block_scores_equal_bf16_scores_on_scaled_meta")]),
+    ("block_plain_score_unscaled", "s *= (double)k_bscale[p * Hkv + kvh];", "s *= 1.0;", 1,
+     [_pin(FB, "test_block_scores_equal_bf16_scores_on_scaled_meta"),
+      _pin(FB, "test_block_score_bounds_every_token")]),
+    ("block_attention_head_scale", "c->scale[c->per_block ? p * c->Hkv + kvh : kvh]", "c->scale[kvh]", 1,
+     [_pin(FB, "test_block_attention_equals_bf16_attention_on_exact_values")]),
     # multi-row queries: right-aligned causal mask and head mapping
     ("multi_mask_excludes_self", "int64_t lim = ctx - q_len + (row - cu_seqlens_q[b]) + 1;",
      "int64_t lim = ctx - q_len + (row - cu_seqlens_q[b]);", 1,
