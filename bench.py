@@ -54,7 +54,7 @@ def parse():
     p.add_argument("--impl", choices=["native", "reference"], default="native")
     p.add_argument("--workload", default="quest_8k",
                    choices=["tiny", "dense_b32", "quest_8k", "long_40k", "mixed_b128"])
-    p.add_argument("--kv", choices=["bf16", "fp8"], default="bf16",
+    p.add_argument("--kv", choices=["bf16", "fp8", "fp8_block"], default="bf16",
                    help="KV-cache element type: bf16, or 8-bit E4M3 codes with per-KV-head scales")
     p.add_argument("--qlen", type=int, default=1,
                    help="query rows per sequence of the dense call (> 1: pa_decode_multi, right-aligned "
@@ -236,22 +236,26 @@ class Step:
                                   dtype=torch.uint8, device=dev)
         self.ws_quest = torch.zeros(pg.quest_decode_workspace_size(w.B, w.Hq, w.Hkv, w.D, w.MBS),
                                     dtype=torch.uint8, device=dev)
-        if kv == "fp8":
-            # the 8-bit pool: every slot of the bf16 pool quantised once (setup)
-            ks, vs = workloads.fp8_scales(w.Hkv)
-            self.k_scale, self.v_scale = torch.from_numpy(ks).to(dev), torch.from_numpy(vs).to(dev)
+        if kv in ("fp8", "fp8_block"):
+            # the 8-bit pool: every slot of the bf16 pool quantised once (setup),
+            # with fixed per-KV-head scales or with per-block scales
             NB, BS = w.NB, w.BS
+            if kv == "fp8":
+                ks, vs = workloads.fp8_scales(w.Hkv)
+                self.k_scale, self.v_scale = torch.from_numpy(ks).to(dev), torch.from_numpy(vs).to(dev)
+            else:
+                self.k_scale = torch.zeros((NB, w.Hkv), dtype=torch.float32, device=dev)
+                self.v_scale = torch.zeros_like(self.k_scale)
             kc8 = torch.empty((NB, BS, w.Hkv, w.D), dtype=torch.uint8, device=dev)
             vc8 = torch.empty((NB, w.Hkv, w.D, BS), dtype=torch.uint8, device=dev)
-            pg.pa_reshape_and_cache_fp8(self.kc.view(NB * BS, w.Hkv, w.D), self.vc.view(NB * BS, w.Hkv, w.D),
-                                        kc8, vc8, torch.arange(NB * BS, dtype=torch.int64, device=dev),
-                                        self.k_scale, self.v_scale)
+            write = pg.pa_reshape_and_cache_fp8 if kv == "fp8" else pg.pa_reshape_and_cache_fp8_block
+            write(self.kc.view(NB * BS, w.Hkv, w.D), self.vc.view(NB * BS, w.Hkv, w.D), kc8, vc8,
+                  torch.arange(NB * BS, dtype=torch.int64, device=dev), self.k_scale, self.v_scale)
             torch.cuda.synchronize(dev)
             self.kc, self.vc = kc8, vc8
             self.kmin = torch.zeros((w.NB, w.Hkv, w.D), dtype=torch.uint8, device=dev)
             self.kmax = torch.zeros_like(self.kmin)
-            pg.quest_reshape_and_cache_fp8(self.key, self.value, self.kc, self.vc, self.kmin, self.kmax,
-                                           self.slots, self.k_scale, self.v_scale)
+            self.calls()[0]()  # the step's write path once, then the metadata as they stand
             pg.quest_rebuild_meta_fp8(self.kmin, self.kmax, self.kc, self.bt, self.ctx)
             torch.cuda.synchronize(dev)
             return
@@ -265,10 +269,11 @@ class Step:
         one launch that selects each segment's top-K and attends over it),
         on at most max_ctas CTAs (0: one per SM)."""
         pg, w = self.pg, self.w
-        if self.kv == "fp8":
-            return lambda: pg.quest_decode_fp8(self.out_sparse, self.sel, self.q, self.kmin, self.kmax, self.kc,
-                                               self.vc, self.k_scale, self.v_scale, self.bt, self.ctx, w.topk,
-                                               w.scale, max_ctas=max_ctas, workspace=self.ws_quest)
+        if self.kv != "bf16":
+            fn = pg.quest_decode_fp8 if self.kv == "fp8" else pg.quest_decode_fp8_block
+            return lambda: fn(self.out_sparse, self.sel, self.q, self.kmin, self.kmax, self.kc, self.vc,
+                              self.k_scale, self.v_scale, self.bt, self.ctx, w.topk, w.scale, max_ctas=max_ctas,
+                              workspace=self.ws_quest)
         return lambda: pg.quest_decode(self.out_sparse, self.sel, self.q, self.kmin, self.kmax, self.kc, self.vc,
                                        self.bt, self.ctx, w.topk, w.scale, max_ctas=max_ctas,
                                        workspace=self.ws_quest)
@@ -282,11 +287,10 @@ class Step:
         after the dense decode instead of beside it."""
         pg, w, budget = self.pg, self.w, self.sms // 2
         select = self.calls()[CALL_NAMES.index("select")]
-        if self.kv == "fp8":
-            sparse = lambda: pg.quest_sparse_decode_fp8_budget(self.out_sparse, self.q, self.kc, self.vc,
-                                                               self.k_scale, self.v_scale, self.bt, self.ctx,
-                                                               self.sel, w.scale, budget,
-                                                               workspace=self.ws_sparse)
+        if self.kv != "bf16":
+            fn = pg.quest_sparse_decode_fp8_budget if self.kv == "fp8" else pg.quest_sparse_decode_fp8_block
+            sparse = lambda: fn(self.out_sparse, self.q, self.kc, self.vc, self.k_scale, self.v_scale, self.bt,
+                                self.ctx, self.sel, w.scale, budget, workspace=self.ws_sparse)
         else:
             sparse = lambda: pg.quest_sparse_decode_budget(self.out_sparse, self.q, self.kc, self.vc, self.bt,
                                                            self.ctx, self.sel, w.scale, budget,
@@ -315,6 +319,19 @@ class Step:
                 lambda: pg.quest_sparse_decode_fp8(self.out_sparse, self.q, self.kc, self.vc,
                                                    self.k_scale, self.v_scale, self.bt, self.ctx,
                                                    self.sel, w.scale, workspace=self.ws_sparse),
+                self.quest(),
+            ]
+        if self.kv == "fp8_block":
+            return [
+                lambda: pg.quest_reshape_and_cache_fp8_block(self.key, self.value, self.kc, self.vc, self.kmin,
+                                                             self.kmax, self.slots, self.k_scale, self.v_scale),
+                lambda: pg.pa_decode_fp8_block(self.out, self.q, self.kc, self.vc, self.k_scale, self.v_scale,
+                                               self.bt, self.ctx, w.scale, workspace=self.ws),
+                lambda: pg.quest_select_topk_fp8_block(self.sel, self.q, self.kmin, self.kmax, self.k_scale,
+                                                       self.bt, self.ctx, w.BS, workspace=self.sel_ws),
+                lambda: pg.quest_sparse_decode_fp8_block(self.out_sparse, self.q, self.kc, self.vc,
+                                                         self.k_scale, self.v_scale, self.bt, self.ctx,
+                                                         self.sel, w.scale, workspace=self.ws_sparse),
                 self.quest(),
             ]
         if self.qlen > 1:
@@ -364,15 +381,21 @@ class OracleSampler:
         import workloads
         self.oracle, self.w, self.kv, self.qlen = oracle, w, kv, qlen
         self.cursor = 0
-        self.fp8 = kv == "fp8"
+        self.fp8 = kv != "bf16"
+        self.block = kv == "fp8_block"
         if self.fp8:
-            self.ks, self.vs = workloads.fp8_scales(w.Hkv)
             NB, BS = w.NB, w.BS
             self.kc = np.zeros((NB, BS, w.Hkv, w.D), dtype=np.uint8)
             self.vc = np.zeros((NB, w.Hkv, w.D, BS), dtype=np.uint8)
-            oracle.reshape_and_cache_fp8(w.key_cache.reshape(NB * BS, w.Hkv, w.D),
-                                         w.value_cache.reshape(NB * BS, w.Hkv, w.D), self.kc, self.vc,
-                                         np.arange(NB * BS, dtype=np.int64), self.ks, self.vs)
+            pool = (w.key_cache.reshape(NB * BS, w.Hkv, w.D), w.value_cache.reshape(NB * BS, w.Hkv, w.D),
+                    self.kc, self.vc, np.arange(NB * BS, dtype=np.int64))
+            if self.block:
+                self.ks = np.zeros((NB, w.Hkv), dtype=np.float32)
+                self.vs = np.zeros_like(self.ks)
+                oracle.reshape_and_cache_fp8_block(*pool, self.ks, self.vs)
+            else:
+                self.ks, self.vs = workloads.fp8_scales(w.Hkv)
+                oracle.reshape_and_cache_fp8(*pool, self.ks, self.vs)
             self.kmin, self.kmax = oracle.quest_rebuild_meta_fp8(self.kc, w.block_tables, w.context_lens)
         else:
             self.kc, self.vc = w.key_cache, w.value_cache   # written in place: the state after the step
@@ -388,14 +411,17 @@ class OracleSampler:
         from paged_gqa_decode_reshape_gb300 import ledger
         o, w, eb = self.oracle, self.w, 1 if self.fp8 else 2
         t0 = time.perf_counter()
-        if self.fp8:
+        if self.block:
+            o.reshape_and_cache_fp8_block(w.key, w.value, self.kc, self.vc, w.slot_mapping, self.ks, self.vs,
+                                          self.kmin, self.kmax)
+        elif self.fp8:
             o.reshape_and_cache_fp8(w.key, w.value, self.kc, self.vc, w.slot_mapping, self.ks, self.vs)
             o.quest_update_meta_fp8(self.kmin, self.kmax, w.key, w.slot_mapping, self.ks, w.BS)
         else:
             o.reshape_and_cache(w.key, w.value, self.kc, self.vc, w.slot_mapping)
             o.quest_update_meta(self.kmin, self.kmax, w.key, w.slot_mapping, w.BS)
         nbytes = ledger.step_bytes(w.context_lens, w.slot_mapping, w.Hq, w.Hkv, w.D, w.BS, w.topk,
-                                   elem_bytes=eb)
+                                   elem_bytes=eb, block_scales=self.block)
         done_bytes = nbytes.reshape + nbytes.meta
         seqs = 0
         while seqs < w.B and (seqs == 0 or time.perf_counter() - t0 <= budget_s):
@@ -407,7 +433,7 @@ class OracleSampler:
                 o.attention_fp8(w.q, self.kc, self.vc, self.ks, self.vs, w.block_tables, w.context_lens,
                                 w.scale, rows=rows)
                 sc = o.quest_scores_fp8(w.q[sl], self.kmin, self.kmax, w.block_tables[sl],
-                                        w.context_lens[sl], w.BS)
+                                        w.context_lens[sl], w.BS, k_bscale=self.ks if self.block else None)
             else:
                 if self.qlen > 1:
                     mrows = np.array([(r, h) for r in range(b * self.qlen, (b + 1) * self.qlen)
@@ -429,7 +455,8 @@ class OracleSampler:
                 o.sparse_attention(w.q, self.kc, self.vc, w.block_tables, w.context_lens, full_sel, w.scale,
                                    rows=rows)
             one = ledger.step_bytes(w.context_lens[sl], np.zeros(0, np.int64), w.Hq, w.Hkv, w.D, w.BS,
-                                    w.topk, selected=sel, q_rows=self.qlen, elem_bytes=eb)
+                                    w.topk, selected=sel, q_rows=self.qlen, elem_bytes=eb,
+                                    block_scales=self.block)
             done_bytes += one.dense + one.select + one.sparse
             seqs += 1
         return done_bytes, time.perf_counter() - t0, seqs
@@ -542,7 +569,7 @@ def run_reference(args, world, rank, pgroup):
 
 def config_of(w, args, world: int) -> dict:
     """The workload a line measures (the same for the native and the reference arm)."""
-    fp8 = args.kv == "fp8"
+    fp8 = args.kv != "bf16"
     return {
         "workload": args.workload, "batch": w.B, "num_q_heads": w.Hq, "num_kv_heads": w.Hkv,
         "head_dim": w.D, "block_size": w.BS, "topk_blocks": w.topk, "kv_cache": args.kv,
@@ -552,7 +579,8 @@ def config_of(w, args, world: int) -> dict:
         "kv_pool_bytes": int(2 * w.key_cache.nbytes // (2 if fp8 else 1)),
         "step": ("quest_reshape_and_cache{0} (ReshapeAndCache + metadata update) + "
                  "quest_select_topk{0} + quest_sparse_decode{0}_budget (half the SMs) on a second stream "
-                 "beside pa_decode{0}; --serial: quest_decode{0} then pa_decode{0}").format("_fp8" if fp8 else ""),
+                 "beside pa_decode{0}; --serial: quest_decode{0} then pa_decode{0}").format(
+                     "" if args.kv == "bf16" else "_" + args.kv),
         "l2": "inputs resident; L2 flushed before every timed sample",
         "parallelism": f"replicas x{world}",
     }
@@ -584,9 +612,10 @@ def measure(torch, pg, w, dev, args, flush, pgroup):
         run_step()
     torch.cuda.synchronize(dev)
     sel_host = step.sel.cpu().numpy()
-    fp8 = args.kv == "fp8"
+    fp8 = args.kv != "bf16"
     nb = ledger.step_bytes(w.context_lens, w.slot_mapping, w.Hq, w.Hkv, w.D, w.BS, w.topk,
-                           selected=sel_host, elem_bytes=1 if fp8 else 2, q_rows=args.qlen)
+                           selected=sel_host, elem_bytes=1 if fp8 else 2, q_rows=args.qlen,
+                           block_scales=args.kv == "fp8_block")
 
     # Pass A (the timed region): whole steps, one event pair per step.
     # Kernels launch with programmatic stream serialization, so consecutive
@@ -724,7 +753,8 @@ def main():
         raise SystemExit("--qlen > 1: bf16 cache and at most 2048 query rows")
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     K = args.steps
-    fp8 = args.kv == "fp8"
+    fp8 = args.kv != "bf16"
+    sfx = "" if args.kv == "bf16" else "_" + args.kv
     peak, peak_kind = measured_peaks()
 
     m = measure(torch, pg, w, dev, args, flush, pgroup)
@@ -753,7 +783,8 @@ def main():
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "e4m3 KV cache, bf16 q/out" if fp8 else "bf16",
+        "dtype": ("e4m3 KV cache (per-block scales), bf16 q/out" if args.kv == "fp8_block" else
+                  "e4m3 KV cache, bf16 q/out" if fp8 else "bf16"),
         "data": "synthetic",
         "config": config_of(w, args, world),
         "timing": ("value/ms_per_step: median over the timed steps of one event pair per step" +
@@ -768,18 +799,17 @@ def main():
         "step_ms_stats": stats_ms(m["step_ms"]),
         "roofline": {
             "bound": "hbm",
-            "kernel": ("pa_decode_fp8" if fp8 else "pa_decode_multi" if args.qlen > 1 else "pa_decode")
+            "kernel": ("pa_decode" + sfx if fp8 else "pa_decode_multi" if args.qlen > 1 else "pa_decode")
                       + " (split-KV decode + fused combine, 1 launch)",
             "achieved": dense["GBps"], "peak": peak, "unit": "GB/s",
             "frac": round(dense["GBps"] / peak, 4), "peak_kind": peak_kind,
             "frac_of_nominal_8tbs": round(dense["GBps"] / NOMINAL_HBM_GBS, 4),
-            "traffic": (recorded_traffic("pa_decode_fp8" if fp8 else "pa_decode", args.workload)
-                        if args.qlen == 1 else None),
+            "traffic": (recorded_traffic("pa_decode" + sfx, args.workload) if args.qlen == 1 else None),
             "algorithmic_bytes_per_launch": int(nb.dense),
             "launch_us": {"median": dense["us"], "min": dense["us_min"]},
         },
         "roofline_sparse": {
-            "bound": "hbm", "kernel": "quest_sparse_decode" + ("_fp8" if fp8 else ""),
+            "bound": "hbm", "kernel": "quest_sparse_decode" + sfx,
             "achieved": point["sparse_decode"]["GBps"], "peak": peak, "unit": "GB/s",
             "frac": point["sparse_decode"]["frac_of_measured_peak"],
             "frac_of_nominal_8tbs": point["sparse_decode"]["frac_of_nominal_8tbs"],

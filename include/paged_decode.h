@@ -432,6 +432,106 @@ PA_API int quest_decode_fp8(pa_bf16 *out, int32_t *selected, const pa_bf16 *quer
                      int head_dim, int block_size, int64_t num_blocks, int topk, float scale,
                      int max_ctas, void *workspace, size_t workspace_bytes, void *stream);
 
+/* ------------------------- 8-bit KV cache with per-block scales ----
+ * The 8-bit cache with one K scale and one V scale per (physical block, KV
+ * head) instead of per KV head ([P2] 2.5 and 3.1 name KV quantisation as the
+ * long-context lever; a per-block scale is the form that needs no
+ * calibration and follows each block's range). Same E4M3 code format and
+ * cache / metadata layouts as above; the scales are k_bscale and v_bscale,
+ * [NB][Hkv] fp32 device arrays, read and written by the library: each entry
+ * is a power of two 2^e (-126 <= e <= 127), or 0 for a block that holds
+ * nothing yet (a new pool starts all zeros). A stored element stands for
+ * decode(code) * scale[p][h] of its block p.
+ *
+ * Writing (pa_reshape_and_cache_fp8_block): for every physical block p a
+ * call writes into, per KV head and for K and V separately,
+ *   a      = the largest finite |x| over the call's tokens in p;
+ *   e_call = the smallest integer e >= -126 with a <= 448 * 2^e;
+ *   if a token of the call lands at offset 0 (the block restarts) or the
+ *   stored scale is 0: e = e_call; else e = max(e_old, e_call) with
+ *   2^e_old the stored scale;
+ *   when e > e_old, every code of the block at an offset the call does not
+ *   write is re-encoded as e4m3(decode(code) * 2^(e_old - e)): exact while
+ *   the value stays in the E4M3 normal range (>= 2^-6), rounded to nearest
+ *   (ties to even) below it;
+ *   the call's elements are stored as e4m3(x / 2^e) (nearest, ties to even;
+ *   infinities saturate to +-448, NaN becomes 0x7F) and the scale becomes 2^e.
+ * The Quest metadata (quest_reshape_and_cache_fp8_block) follow the same
+ * rule as quest_update_meta_fp8 on the re-encoded codes: on a restart the
+ * min / max of the call's codes, else the stored min / max, re-encoded like
+ * the codes when e grew, merged with the call's codes. The slots of one call
+ * must be distinct. quest_rebuild_meta_fp8 works unchanged on this cache.
+ *
+ * Reading: the attention dequantises each block's K and V with its own
+ * scales; the Quest score of a block is the score of its stored metadata
+ * times the block's K scale (one fp32 product: the blocks' scales differ,
+ * so it can change the top-K). */
+
+/* ReshapeAndCache into an 8-bit cache with per-block scales (k_bscale,
+ * v_bscale updated in place), one launch. Same argument rules as
+ * pa_reshape_and_cache_fp8. */
+PA_API int pa_reshape_and_cache_fp8_block(const pa_bf16 *key, const pa_bf16 *value,
+                                          pa_e4m3 *key_cache, pa_e4m3 *value_cache,
+                                          const int64_t *slot_mapping, int64_t num_tokens,
+                                          float *k_bscale, float *v_bscale, int num_kv_heads,
+                                          int head_dim, int block_size, int64_t num_blocks,
+                                          void *stream);
+
+/* pa_reshape_and_cache_fp8_block and the Quest metadata update, one launch. */
+PA_API int quest_reshape_and_cache_fp8_block(const pa_bf16 *key, const pa_bf16 *value,
+                                             pa_e4m3 *key_cache, pa_e4m3 *value_cache,
+                                             pa_e4m3 *kmin, pa_e4m3 *kmax,
+                                             const int64_t *slot_mapping, int64_t num_tokens,
+                                             float *k_bscale, float *v_bscale, int num_kv_heads,
+                                             int head_dim, int block_size, int64_t num_blocks,
+                                             void *stream);
+
+/* quest_select_topk_fp8 on a cache with per-block scales: every block's
+ * score is the metadata score times k_bscale[p][kvh] (p its physical block),
+ * then the same top-K rule and workspace. */
+PA_API int quest_select_topk_fp8_block(int32_t *selected, const pa_bf16 *query,
+                                       const pa_e4m3 *kmin, const pa_e4m3 *kmax,
+                                       const float *k_bscale, const int32_t *block_tables,
+                                       int max_blocks_per_seq, const int32_t *context_lens,
+                                       int batch, int num_q_heads, int num_kv_heads, int head_dim,
+                                       int block_size, int64_t num_blocks, int topk,
+                                       void *workspace, size_t workspace_bytes, void *stream);
+
+/* pa_decode_fp8 on a cache with per-block scales: K and V of physical block
+ * p read as decode(code) * k_bscale[p][kvh] (v_bscale alike). */
+PA_API int pa_decode_fp8_block(pa_bf16 *out, const pa_bf16 *query,
+                               const pa_e4m3 *key_cache, const pa_e4m3 *value_cache,
+                               const float *k_bscale, const float *v_bscale,
+                               const int32_t *block_tables, int max_blocks_per_seq,
+                               const int32_t *context_lens, int batch, int num_q_heads,
+                               int num_kv_heads, int head_dim, int block_size, int64_t num_blocks,
+                               float scale, void *workspace, size_t workspace_bytes, void *stream);
+
+/* quest_sparse_decode_fp8_budget on a cache with per-block scales
+ * (max_ctas 0: one CTA per SM at most). */
+PA_API int quest_sparse_decode_fp8_block(pa_bf16 *out, const pa_bf16 *query,
+                                         const pa_e4m3 *key_cache, const pa_e4m3 *value_cache,
+                                         const float *k_bscale, const float *v_bscale,
+                                         const int32_t *block_tables, int max_blocks_per_seq,
+                                         const int32_t *context_lens, const int32_t *selected,
+                                         int topk, int batch, int num_q_heads, int num_kv_heads,
+                                         int head_dim, int block_size, int64_t num_blocks,
+                                         float scale, int max_ctas, void *workspace,
+                                         size_t workspace_bytes, void *stream);
+
+/* quest_decode_fp8 on a cache with per-block scales: the block-scaled scores,
+ * then the fused selection and sparse decode (or, for a large selection,
+ * quest_select_topk_fp8_block and quest_sparse_decode_fp8_block). */
+PA_API int quest_decode_fp8_block(pa_bf16 *out, int32_t *selected, const pa_bf16 *query,
+                                  const pa_e4m3 *kmin, const pa_e4m3 *kmax,
+                                  const pa_e4m3 *key_cache, const pa_e4m3 *value_cache,
+                                  const float *k_bscale, const float *v_bscale,
+                                  const int32_t *block_tables, int max_blocks_per_seq,
+                                  const int32_t *context_lens, int batch, int num_q_heads,
+                                  int num_kv_heads, int head_dim, int block_size, int64_t num_blocks,
+                                  int topk, float scale, int max_ctas, void *workspace,
+                                  size_t workspace_bytes, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

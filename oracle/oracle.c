@@ -532,6 +532,7 @@ int64_t oracle_reshape_and_cache_fp8_block(const uint16_t *key, const uint16_t *
     const int64_t row = (int64_t)Hkv * D;
     int64_t out_of_range = 0;
     unsigned char *done = (unsigned char *)calloc((size_t)T + 1, 1);
+    int64_t *members = (int64_t *)malloc(sizeof(int64_t) * (size_t)(T + 1));
     for (int64_t t = 0; t < T; ++t) {
         const int64_t s = slot_mapping[t];
         if (s < 0 || done[t])
@@ -542,13 +543,16 @@ int64_t oracle_reshape_and_cache_fp8_block(const uint16_t *key, const uint16_t *
             done[t] = 1;
             continue;
         }
-        /* step 1: members (t and the later tokens of the call in block p) */
+        /* step 1: members (t and the later tokens of the call in block p, in order) */
         int reset = 0;
         unsigned written = 0; /* offsets the call writes */
+        int64_t nm = 0;
         for (int64_t u = t; u < T; ++u) {
             const int64_t su = slot_mapping[u];
             if (su < 0 || su / BS != p)
                 continue;
+            members[nm++] = u;
+            done[u] = 1;
             written |= 1u << (su % BS);
             if (su % BS == 0)
                 reset = 1;
@@ -556,10 +560,8 @@ int64_t oracle_reshape_and_cache_fp8_block(const uint16_t *key, const uint16_t *
         for (int h = 0; h < Hkv; ++h) {
             /* step 2 */
             double ak = 0.0, av = 0.0;
-            for (int64_t u = t; u < T; ++u) {
-                const int64_t su = slot_mapping[u];
-                if (su < 0 || su / BS != p)
-                    continue;
+            for (int64_t i = 0; i < nm; ++i) {
+                const int64_t u = members[i];
                 for (int d = 0; d < D; ++d) {
                     const double xk = fabs(bf16_val(key[u * row + (int64_t)h * D + d]));
                     const double xv = fabs(bf16_val(value[u * row + (int64_t)h * D + d]));
@@ -595,11 +597,9 @@ int64_t oracle_reshape_and_cache_fp8_block(const uint16_t *key, const uint16_t *
                 have = 1;
             }
             /* step 7, and step 8's merge */
-            for (int64_t u = t; u < T; ++u) {
-                const int64_t su = slot_mapping[u];
-                if (su < 0 || su / BS != p)
-                    continue;
-                const int64_t o = su % BS;
+            for (int64_t i = 0; i < nm; ++i) {
+                const int64_t u = members[i];
+                const int64_t o = slot_mapping[u] % BS;
                 for (int d = 0; d < D; ++d) {
                     const int64_t e = (int64_t)h * D + d;
                     const uint8_t c = quantize(key[u * row + e], ks);
@@ -616,13 +616,9 @@ int64_t oracle_reshape_and_cache_fp8_block(const uint16_t *key, const uint16_t *
                 have = 1;
             }
         }
-        for (int64_t u = t; u < T; ++u) {
-            const int64_t su = slot_mapping[u];
-            if (su >= 0 && su / BS == p)
-                done[u] = 1;
-        }
     }
     free(done);
+    free(members);
     return out_of_range;
 }
 

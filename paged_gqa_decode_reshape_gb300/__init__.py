@@ -41,6 +41,8 @@ __all__ = [
     "pa_reshape_and_cache_fp8", "quest_update_meta_fp8", "quest_reshape_and_cache_fp8",
     "quest_rebuild_meta_fp8", "quest_select_topk_fp8", "pa_decode_fp8", "quest_sparse_decode_fp8",
     "quest_sparse_decode_fp8_budget",
+    "pa_reshape_and_cache_fp8_block", "quest_reshape_and_cache_fp8_block", "quest_select_topk_fp8_block",
+    "pa_decode_fp8_block", "quest_sparse_decode_fp8_block", "quest_decode_fp8_block",
     "pa_workspace_status", "pa_check_metadata", "Workspace",
 ]
 
@@ -133,6 +135,20 @@ def load_library(path: Optional[str] = None):
         L.quest_sparse_decode_fp8_budget.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, vp, vp, i32, i32, i32,
                                                      i32, i32, i32, i64, f32, i32, vp, sz, vp]
         L.quest_sparse_decode_fp8_budget.restype = i32
+        L.pa_reshape_and_cache_fp8_block.argtypes = [vp, vp, vp, vp, vp, i64, vp, vp, i32, i32, i32, i64, vp]
+        L.pa_reshape_and_cache_fp8_block.restype = i32
+        L.quest_reshape_and_cache_fp8_block.argtypes = [vp, vp, vp, vp, vp, vp, vp, i64, vp, vp, i32, i32,
+                                                        i32, i64, vp]
+        L.quest_reshape_and_cache_fp8_block.restype = i32
+        L.quest_select_topk_fp8_block.argtypes = [vp, vp, vp, vp, vp, vp, i32, vp, i32, i32, i32, i32, i32,
+                                                  i64, i32, vp, sz, vp]
+        L.quest_select_topk_fp8_block.restype = i32
+        L.pa_decode_fp8_block.argtypes = L.pa_decode_fp8.argtypes
+        L.pa_decode_fp8_block.restype = i32
+        L.quest_sparse_decode_fp8_block.argtypes = L.quest_sparse_decode_fp8_budget.argtypes
+        L.quest_sparse_decode_fp8_block.restype = i32
+        L.quest_decode_fp8_block.argtypes = L.quest_decode_fp8.argtypes
+        L.quest_decode_fp8_block.restype = i32
         _lib = L
         return _lib
 
@@ -551,7 +567,7 @@ def quest_select_topk_fp8(selected: torch.Tensor, query: torch.Tensor, kmin: tor
 
 
 def _attention_checks_fp8(out, query, key_cache, value_cache, block_tables, context_lens,
-                          k_scale, v_scale):
+                          k_scale, v_scale, per_block=False):
     _need(key_cache, "key_cache", torch.uint8, 4)
     dev = key_cache.device
     _need(value_cache, "value_cache", torch.uint8, 4, dev)
@@ -565,7 +581,10 @@ def _attention_checks_fp8(out, query, key_cache, value_cache, block_tables, cont
         raise ValueError("shape mismatch between query/out and the caches")
     if block_tables.shape[0] != B or context_lens.shape[0] != B:
         raise ValueError("block_tables / context_lens batch mismatch")
-    _scales(k_scale, v_scale, Hkv, dev)
+    if per_block:
+        _block_scales(k_scale, v_scale, NB, Hkv, dev)
+    else:
+        _scales(k_scale, v_scale, Hkv, dev)
     return dev, B, Hq, Hkv, D, BS, NB, block_tables.shape[1]
 
 
@@ -726,3 +745,145 @@ def quest_decode_fp8(out: torch.Tensor, selected: torch.Tensor, query: torch.Ten
     return _quest_decode(L.quest_decode_fp8, "quest_decode_fp8", out, selected, query, kmin, kmax, key_cache,
                          value_cache, block_tables, context_lens, topk, scale, max_ctas, workspace,
                          (_ptr(k_scale), _ptr(v_scale)), checks)
+
+
+# ------------------------------------- 8-bit cache with per-block scales
+
+
+def _block_scales(k_bscale, v_bscale, NB, Hkv, dev):
+    _need(k_bscale, "k_bscale", torch.float32, 2, dev)
+    if v_bscale is not None:
+        _need(v_bscale, "v_bscale", torch.float32, 2, dev)
+    if tuple(k_bscale.shape) != (NB, Hkv) or (v_bscale is not None and tuple(v_bscale.shape) != (NB, Hkv)):
+        raise ValueError("per-block scales must be [num_blocks, num_kv_heads]")
+
+
+def _write_fp8_block(fn, what, key, value, key_cache, value_cache, slot_mapping, k_bscale, v_bscale,
+                     meta=None):
+    _need(key_cache, "key_cache", torch.uint8, 4)
+    dev = key_cache.device
+    _need(value_cache, "value_cache", torch.uint8, 4, dev)
+    _need(key, "key", torch.bfloat16, 3, dev)
+    _need(value, "value", torch.bfloat16, 3, dev)
+    _need(slot_mapping, "slot_mapping", torch.int64, 1, dev)
+    NB, BS, Hkv, D = key_cache.shape
+    T = slot_mapping.shape[0]
+    if value_cache.shape != (NB, Hkv, D, BS) or key.shape != (T, Hkv, D) or value.shape != key.shape:
+        raise ValueError("shape mismatch between key/value and the caches")
+    _block_scales(k_bscale, v_bscale, NB, Hkv, dev)
+    m = ()
+    if meta is not None:
+        for t, n in zip(meta, ("kmin", "kmax")):
+            _need(t, n, torch.uint8, 3, dev)
+            if tuple(t.shape) != (NB, Hkv, D):
+                raise ValueError("metadata must be [NB, Hkv, D]")
+        m = (_ptr(meta[0]), _ptr(meta[1]))
+    _check(what, fn(_ptr(key), _ptr(value), _ptr(key_cache), _ptr(value_cache), *m, _ptr(slot_mapping), T,
+                    _ptr(k_bscale), _ptr(v_bscale), Hkv, D, BS, NB, _stream(dev)))
+
+
+def pa_reshape_and_cache_fp8_block(key: torch.Tensor, value: torch.Tensor, key_cache: torch.Tensor,
+                                   value_cache: torch.Tensor, slot_mapping: torch.Tensor,
+                                   k_bscale: torch.Tensor, v_bscale: torch.Tensor) -> None:
+    """Quantise this step's K/V rows into 8-bit caches with per-block power-of-two scales
+    k_bscale / v_bscale [NB, Hkv] (fp32, updated in place; 0 marks an empty block)."""
+    L = load_library()
+    _write_fp8_block(L.pa_reshape_and_cache_fp8_block, "pa_reshape_and_cache_fp8_block", key, value,
+                     key_cache, value_cache, slot_mapping, k_bscale, v_bscale)
+
+
+def quest_reshape_and_cache_fp8_block(key: torch.Tensor, value: torch.Tensor, key_cache: torch.Tensor,
+                                      value_cache: torch.Tensor, kmin: torch.Tensor, kmax: torch.Tensor,
+                                      slot_mapping: torch.Tensor, k_bscale: torch.Tensor,
+                                      v_bscale: torch.Tensor) -> None:
+    """pa_reshape_and_cache_fp8_block and the Quest metadata update in one launch."""
+    L = load_library()
+    _write_fp8_block(L.quest_reshape_and_cache_fp8_block, "quest_reshape_and_cache_fp8_block", key, value,
+                     key_cache, value_cache, slot_mapping, k_bscale, v_bscale, meta=(kmin, kmax))
+
+
+def quest_select_topk_fp8_block(selected: torch.Tensor, query: torch.Tensor, kmin: torch.Tensor,
+                                kmax: torch.Tensor, k_bscale: torch.Tensor, block_tables: torch.Tensor,
+                                context_lens: torch.Tensor, block_size: int,
+                                workspace: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """Quest selection on 8-bit metadata of a cache with per-block scales."""
+    L = load_library()
+    _need(kmin, "kmin", torch.uint8, 3)
+    dev = kmin.device
+    _need(kmax, "kmax", torch.uint8, 3, dev)
+    _need(query, "query", torch.bfloat16, 3, dev)
+    _need(selected, "selected", torch.int32, 3, dev)
+    _need(block_tables, "block_tables", torch.int32, 2, dev)
+    _need(context_lens, "context_lens", torch.int32, 1, dev)
+    B, Hq, D = query.shape
+    NB, Hkv, D2 = kmin.shape
+    MBS = block_tables.shape[1]
+    if D != D2 or selected.shape[:2] != (B, Hkv):
+        raise ValueError("shape mismatch in quest_select_topk_fp8_block")
+    _block_scales(k_bscale, None, NB, Hkv, dev)
+    topk = selected.shape[2]
+    need = quest_select_workspace_size(B, Hkv, MBS)
+    ws = workspace if workspace is not None else _default_sel_ws.get(dev, need)
+    _check("quest_select_topk_fp8_block",
+           L.quest_select_topk_fp8_block(_ptr(selected), _ptr(query), _ptr(kmin), _ptr(kmax), _ptr(k_bscale),
+                                         _ptr(block_tables), MBS, _ptr(context_lens), B, Hq, Hkv, D,
+                                         int(block_size), NB, topk, _ptr(ws), ws.numel() * ws.element_size(),
+                                         _stream(dev)))
+    return selected
+
+
+def pa_decode_fp8_block(out: torch.Tensor, query: torch.Tensor, key_cache: torch.Tensor,
+                        value_cache: torch.Tensor, k_bscale: torch.Tensor, v_bscale: torch.Tensor,
+                        block_tables: torch.Tensor, context_lens: torch.Tensor, scale: float,
+                        workspace: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """Dense GQA paged decode over 8-bit caches with per-block scales [NB, Hkv]."""
+    L = load_library()
+    dev, B, Hq, Hkv, D, BS, NB, MBS = _attention_checks_fp8(out, query, key_cache, value_cache, block_tables,
+                                                            context_lens, k_bscale, v_bscale, per_block=True)
+    need = pa_decode_workspace_size(B, Hq, Hkv, D)
+    ws = workspace if workspace is not None else _default_ws.get(dev, need)
+    _check("pa_decode_fp8_block",
+           L.pa_decode_fp8_block(_ptr(out), _ptr(query), _ptr(key_cache), _ptr(value_cache), _ptr(k_bscale),
+                                 _ptr(v_bscale), _ptr(block_tables), MBS, _ptr(context_lens), B, Hq, Hkv, D,
+                                 BS, NB, float(scale), _ptr(ws), ws.numel() * ws.element_size(), _stream(dev)))
+    return out
+
+
+def quest_sparse_decode_fp8_block(out: torch.Tensor, query: torch.Tensor, key_cache: torch.Tensor,
+                                  value_cache: torch.Tensor, k_bscale: torch.Tensor, v_bscale: torch.Tensor,
+                                  block_tables: torch.Tensor, context_lens: torch.Tensor,
+                                  selected: torch.Tensor, scale: float, max_ctas: int = 0,
+                                  workspace: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """Quest sparse attention over 8-bit caches with per-block scales (max_ctas 0: one CTA per SM at most)."""
+    L = load_library()
+    dev, B, Hq, Hkv, D, BS, NB, MBS = _attention_checks_fp8(out, query, key_cache, value_cache, block_tables,
+                                                            context_lens, k_bscale, v_bscale, per_block=True)
+    _need(selected, "selected", torch.int32, 3, dev)
+    if selected.shape[:2] != (B, Hkv):
+        raise ValueError("selected must be [B, Hkv, topk]")
+    topk = selected.shape[2]
+    need = pa_decode_workspace_size(B, Hq, Hkv, D)
+    ws = workspace if workspace is not None else _default_ws.get(dev, need)
+    _check("quest_sparse_decode_fp8_block",
+           L.quest_sparse_decode_fp8_block(_ptr(out), _ptr(query), _ptr(key_cache), _ptr(value_cache),
+                                           _ptr(k_bscale), _ptr(v_bscale), _ptr(block_tables), MBS,
+                                           _ptr(context_lens), _ptr(selected), topk, B, Hq, Hkv, D, BS, NB,
+                                           float(scale), int(max_ctas), _ptr(ws), ws.numel() * ws.element_size(),
+                                           _stream(dev)))
+    return out
+
+
+def quest_decode_fp8_block(out: torch.Tensor, selected: torch.Tensor, query: torch.Tensor, kmin: torch.Tensor,
+                           kmax: torch.Tensor, key_cache: torch.Tensor, value_cache: torch.Tensor,
+                           k_bscale: torch.Tensor, v_bscale: torch.Tensor, block_tables: torch.Tensor,
+                           context_lens: torch.Tensor, topk: int, scale: float, max_ctas: int = 0,
+                           workspace: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """quest_decode over 8-bit caches with per-block scales."""
+    L = load_library()
+    checks = _attention_checks_fp8(out, query, key_cache, value_cache, block_tables, context_lens, k_bscale,
+                                   v_bscale, per_block=True)
+    _need(kmin, "kmin", torch.uint8, 3, checks[0])
+    _need(kmax, "kmax", torch.uint8, 3, checks[0])
+    return _quest_decode(L.quest_decode_fp8_block, "quest_decode_fp8_block", out, selected, query, kmin, kmax,
+                         key_cache, value_cache, block_tables, context_lens, topk, scale, max_ctas, workspace,
+                         (_ptr(k_bscale), _ptr(v_bscale)), checks)

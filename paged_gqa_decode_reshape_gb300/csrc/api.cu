@@ -118,7 +118,7 @@ int run_decode(pa_bf16 *out, const pa_bf16 *query, const void *key_cache, const 
                float scale, void *workspace, size_t workspace_bytes, void *stream, bool sparse,
                const float *k_scale = nullptr, const float *v_scale = nullptr, bool fp8 = false,
                const int32_t *cu_q = nullptr, int nseq = 0, int max_ctas = 0,
-               const float *scores = nullptr, int32_t *sel_out = nullptr) {
+               const float *scores = nullptr, int32_t *sel_out = nullptr, bool bscale = false) {
     int rc = check_attention_args(out, query, key_cache, value_cache, block_tables, MBS,
                                   context_lens, B, Hq, Hkv, D, BS, NB, scale, workspace);
     if (rc != PA_OK) return rc;
@@ -144,6 +144,7 @@ int run_decode(pa_bf16 *out, const pa_bf16 *query, const void *key_cache, const 
     a.sel = selected;
     a.k_scale = k_scale;
     a.v_scale = v_scale;
+    a.scale_per_block = bscale ? 1 : 0;
     a.v8 = fp8 ? static_cast<const uint8_t *>(value_cache) : nullptr;
     a.cu_q = cu_q;
     a.nseq = cu_q ? nseq : B;
@@ -346,7 +347,7 @@ int run_quest_decode(pa_bf16 *out, int32_t *selected, const pa_bf16 *query, cons
                      const float *k_scale, const float *v_scale, const int32_t *block_tables, int MBS,
                      const int32_t *context_lens, int B, int Hq, int Hkv, int D, int BS, int64_t NB,
                      int topk, float scale, int max_ctas, void *workspace, size_t workspace_bytes,
-                     void *stream, bool fp8) {
+                     void *stream, bool fp8, bool bscale = false) {
     if (!selected || !kmin || !kmax || !workspace || max_ctas < 0) return PA_ERR_INVALID_ARG;
     int rc = check_attention_args(out, query, key_cache, value_cache, block_tables, MBS, context_lens, B, Hq,
                                   Hkv, D, BS, NB, scale, workspace);
@@ -367,18 +368,18 @@ int run_quest_decode(pa_bf16 *out, int32_t *selected, const pa_bf16 *query, cons
         // top-Ks would run one after another inside it; the top-K kernel
         // (one CTA per segment) runs them all at once instead.
         e = launch_quest_select(selected, scores, query, kmin, kmax, block_tables, MBS, context_lens, B, Hq, Hkv,
-                                D, BS, NB, topk, static_cast<cudaStream_t>(stream), fp8);
+                                D, BS, NB, topk, static_cast<cudaStream_t>(stream), fp8, bscale ? k_scale : nullptr);
         if (e != cudaSuccess) return cuda_fail(e);
         return run_decode(out, query, key_cache, value_cache, block_tables, MBS, context_lens, selected, topk, B,
                           Hq, Hkv, D, BS, NB, scale, workspace, dec, stream, true, k_scale, v_scale, fp8, nullptr,
-                          0, max_ctas);
+                          0, max_ctas, nullptr, nullptr, bscale);
     }
     e = launch_quest_scores(scores, query, kmin, kmax, block_tables, MBS, context_lens, B, Hq, Hkv, D, BS, NB,
-                            static_cast<cudaStream_t>(stream), fp8);
+                            static_cast<cudaStream_t>(stream), fp8, bscale ? k_scale : nullptr);
     if (e != cudaSuccess) return cuda_fail(e);
     return run_decode(out, query, key_cache, value_cache, block_tables, MBS, context_lens, nullptr, topk, B,
                       Hq, Hkv, D, BS, NB, scale, workspace, dec, stream, true, k_scale, v_scale, fp8, nullptr, 0,
-                      max_ctas, scores, selected);
+                      max_ctas, scores, selected, bscale);
 }
 }  // namespace
 
@@ -516,11 +517,14 @@ int quest_rebuild_meta_fp8(pa_e4m3 *kmin, pa_e4m3 *kmax, const pa_e4m3 *key_cach
     return e == cudaSuccess ? PA_OK : cuda_fail(e);
 }
 
-int quest_select_topk_fp8(int32_t *selected, const pa_bf16 *query, const pa_e4m3 *kmin,
-                          const pa_e4m3 *kmax, const int32_t *block_tables, int max_blocks_per_seq,
-                          const int32_t *context_lens, int batch, int num_q_heads, int num_kv_heads,
-                          int head_dim, int block_size, int64_t num_blocks, int topk, void *workspace,
-                          size_t workspace_bytes, void *stream) {
+}  // extern "C"
+
+namespace {
+int run_select_fp8(int32_t *selected, const pa_bf16 *query, const pa_e4m3 *kmin, const pa_e4m3 *kmax,
+                   const float *k_bscale, const int32_t *block_tables, int max_blocks_per_seq,
+                   const int32_t *context_lens, int batch, int num_q_heads, int num_kv_heads, int head_dim,
+                   int block_size, int64_t num_blocks, int topk, void *workspace, size_t workspace_bytes,
+                   void *stream) {
     if (!selected || !query || !kmin || !kmax || !block_tables || !context_lens || !workspace)
         return PA_ERR_INVALID_ARG;
     if (batch <= 0 || num_q_heads <= 0 || num_kv_heads <= 0 || max_blocks_per_seq <= 0 ||
@@ -536,8 +540,111 @@ int quest_select_topk_fp8(int32_t *selected, const pa_bf16 *query, const pa_e4m3
     const cudaError_t e = launch_quest_select(
         selected, static_cast<float *>(workspace), query, kmin, kmax, block_tables, max_blocks_per_seq,
         context_lens, batch, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, topk,
-        static_cast<cudaStream_t>(stream), true);
+        static_cast<cudaStream_t>(stream), true, k_bscale);
     return e == cudaSuccess ? PA_OK : cuda_fail(e);
+}
+}  // namespace
+
+extern "C" {
+
+int quest_select_topk_fp8(int32_t *selected, const pa_bf16 *query, const pa_e4m3 *kmin,
+                          const pa_e4m3 *kmax, const int32_t *block_tables, int max_blocks_per_seq,
+                          const int32_t *context_lens, int batch, int num_q_heads, int num_kv_heads,
+                          int head_dim, int block_size, int64_t num_blocks, int topk, void *workspace,
+                          size_t workspace_bytes, void *stream) {
+    return run_select_fp8(selected, query, kmin, kmax, nullptr, block_tables, max_blocks_per_seq, context_lens,
+                          batch, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, topk, workspace,
+                          workspace_bytes, stream);
+}
+
+/* ------------------------------------ E4M3 cache with per-block scales */
+
+int pa_reshape_and_cache_fp8_block(const pa_bf16 *key, const pa_bf16 *value, pa_e4m3 *key_cache,
+                                   pa_e4m3 *value_cache, const int64_t *slot_mapping, int64_t num_tokens,
+                                   float *k_bscale, float *v_bscale, int num_kv_heads, int head_dim,
+                                   int block_size, int64_t num_blocks, void *stream) {
+    int rc = check_fp8_write(num_tokens, num_kv_heads, head_dim, block_size, num_blocks);
+    if (rc != PA_OK) return rc;
+    if (num_tokens == 0) return PA_OK;
+    if (!key || !value || !key_cache || !value_cache || !slot_mapping || !k_bscale || !v_bscale)
+        return PA_ERR_INVALID_ARG;
+    if (!aligned16(key) || !aligned16(value) || !aligned16(key_cache) || !aligned16(value_cache))
+        return PA_ERR_INVALID_ARG;
+    const cudaError_t e = launch_write_fp8_block(key_cache, value_cache, nullptr, nullptr, k_bscale, v_bscale,
+                                                 key, value, slot_mapping, num_tokens, num_kv_heads, head_dim,
+                                                 block_size, num_blocks, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? PA_OK : cuda_fail(e);
+}
+
+int quest_reshape_and_cache_fp8_block(const pa_bf16 *key, const pa_bf16 *value, pa_e4m3 *key_cache,
+                                      pa_e4m3 *value_cache, pa_e4m3 *kmin, pa_e4m3 *kmax,
+                                      const int64_t *slot_mapping, int64_t num_tokens, float *k_bscale,
+                                      float *v_bscale, int num_kv_heads, int head_dim, int block_size,
+                                      int64_t num_blocks, void *stream) {
+    int rc = check_fp8_write(num_tokens, num_kv_heads, head_dim, block_size, num_blocks);
+    if (rc != PA_OK) return rc;
+    if (num_tokens == 0) return PA_OK;
+    if (!key || !value || !key_cache || !value_cache || !kmin || !kmax || !slot_mapping || !k_bscale ||
+        !v_bscale)
+        return PA_ERR_INVALID_ARG;
+    if (!aligned16(key) || !aligned16(value) || !aligned16(key_cache) || !aligned16(value_cache) ||
+        !aligned16(kmin) || !aligned16(kmax))
+        return PA_ERR_INVALID_ARG;
+    const cudaError_t e = launch_write_fp8_block(key_cache, value_cache, kmin, kmax, k_bscale, v_bscale, key,
+                                                 value, slot_mapping, num_tokens, num_kv_heads, head_dim,
+                                                 block_size, num_blocks, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? PA_OK : cuda_fail(e);
+}
+
+int quest_select_topk_fp8_block(int32_t *selected, const pa_bf16 *query, const pa_e4m3 *kmin,
+                                const pa_e4m3 *kmax, const float *k_bscale, const int32_t *block_tables,
+                                int max_blocks_per_seq, const int32_t *context_lens, int batch,
+                                int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                                int64_t num_blocks, int topk, void *workspace, size_t workspace_bytes,
+                                void *stream) {
+    if (!k_bscale) return PA_ERR_INVALID_ARG;
+    return run_select_fp8(selected, query, kmin, kmax, k_bscale, block_tables, max_blocks_per_seq, context_lens,
+                          batch, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, topk, workspace,
+                          workspace_bytes, stream);
+}
+
+int pa_decode_fp8_block(pa_bf16 *out, const pa_bf16 *query, const pa_e4m3 *key_cache,
+                        const pa_e4m3 *value_cache, const float *k_bscale, const float *v_bscale,
+                        const int32_t *block_tables, int max_blocks_per_seq, const int32_t *context_lens,
+                        int batch, int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                        int64_t num_blocks, float scale, void *workspace, size_t workspace_bytes,
+                        void *stream) {
+    return run_decode(out, query, key_cache, value_cache, block_tables, max_blocks_per_seq, context_lens,
+                      nullptr, 0, batch, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, scale,
+                      workspace, workspace_bytes, stream, false, k_bscale, v_bscale, true, nullptr, 0, 0,
+                      nullptr, nullptr, true);
+}
+
+int quest_sparse_decode_fp8_block(pa_bf16 *out, const pa_bf16 *query, const pa_e4m3 *key_cache,
+                                  const pa_e4m3 *value_cache, const float *k_bscale, const float *v_bscale,
+                                  const int32_t *block_tables, int max_blocks_per_seq,
+                                  const int32_t *context_lens, const int32_t *selected, int topk, int batch,
+                                  int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                                  int64_t num_blocks, float scale, int max_ctas, void *workspace,
+                                  size_t workspace_bytes, void *stream) {
+    if (max_ctas < 0) return PA_ERR_INVALID_ARG;
+    return run_decode(out, query, key_cache, value_cache, block_tables, max_blocks_per_seq, context_lens,
+                      selected, topk, batch, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, scale,
+                      workspace, workspace_bytes, stream, true, k_bscale, v_bscale, true, nullptr, 0, max_ctas,
+                      nullptr, nullptr, true);
+}
+
+int quest_decode_fp8_block(pa_bf16 *out, int32_t *selected, const pa_bf16 *query, const pa_e4m3 *kmin,
+                           const pa_e4m3 *kmax, const pa_e4m3 *key_cache, const pa_e4m3 *value_cache,
+                           const float *k_bscale, const float *v_bscale, const int32_t *block_tables,
+                           int max_blocks_per_seq, const int32_t *context_lens, int batch, int num_q_heads,
+                           int num_kv_heads, int head_dim, int block_size, int64_t num_blocks, int topk,
+                           float scale, int max_ctas, void *workspace, size_t workspace_bytes, void *stream) {
+    if (!k_bscale || !v_bscale) return PA_ERR_INVALID_ARG;
+    return run_quest_decode(out, selected, query, kmin, kmax, key_cache, value_cache, k_bscale, v_bscale,
+                            block_tables, max_blocks_per_seq, context_lens, batch, num_q_heads, num_kv_heads,
+                            head_dim, block_size, num_blocks, topk, scale, max_ctas, workspace, workspace_bytes,
+                            stream, true, true);
 }
 
 int quest_sparse_decode_fp8_budget(pa_bf16 *out, const pa_bf16 *query, const pa_e4m3 *key_cache,

@@ -220,6 +220,12 @@ __device__ __forceinline__ float f16_hi(uint32_t v) {
     return __half2float(__ushort_as_half(static_cast<unsigned short>(v >> 16)));
 }
 
+// An f16 pair times r (rounded to f16), each product rounded to nearest.
+__device__ __forceinline__ uint32_t scale_f16x2(uint32_t v, float r) {
+    const __half2 m = __hmul2(*reinterpret_cast<const __half2 *>(&v), __float2half2_rn(r));
+    return *reinterpret_cast<const uint32_t *>(&m);
+}
+
 // Two E4M3 codes (low byte first) to an f16 pair (low half first); exact.
 __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_codes) {
     const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(

@@ -97,7 +97,9 @@ struct DecodeCfg {
     static constexpr int SCR = D * 8 + 16;      // floats per consumer merge slot: acc[D][8], m[8], l[8]
     static constexpr size_t off_bars = size_t(S) * STAGE;
     static constexpr size_t off_info = off_bars + size_t(S) * 16;
-    static constexpr size_t off_scr = off_info + size_t(S) * 8;
+    // E4M3 cache: each stage's K and V scale (float2) after the item info
+    static constexpr size_t off_iscale = off_info + size_t(S) * 8;
+    static constexpr size_t off_scr = off_iscale + (F8 ? size_t(S) * 8 : 0);
     static constexpr size_t off_flags = off_scr + size_t(NC) * SCR * 4;
     static constexpr size_t off_pre = off_flags + 64;
     // per-row item prefix (PB + 1 entries); multi-token rows then add each
@@ -135,6 +137,7 @@ __global__ void __launch_bounds__(DecodeCfg<D, F8, MULTI>::THREADS, 1)
     const uint32_t full_bar = base + uint32_t(C::off_bars);
     const uint32_t empty_bar = full_bar + S * 8;
     int2 *info = reinterpret_cast<int2 *>(bp + C::off_info);
+    float2 *iscale = reinterpret_cast<float2 *>(bp + C::off_iscale);  // E4M3 cache only
     float *scr = reinterpret_cast<float *>(bp + C::off_scr);
     volatile int *flags = reinterpret_cast<volatile int *>(bp + C::off_flags);
     int32_t *pre = reinterpret_cast<int32_t *>(bp + C::off_pre);
@@ -373,9 +376,10 @@ __global__ void __launch_bounds__(DecodeCfg<D, F8, MULTI>::THREADS, 1)
         // window after that the items are issued.
         struct Win {
             int seg, j, phys, ctxv;
+            float sk, sv;  // E4M3 cache: the item's K and V scale
         };
         auto stage_c = [&](int k0) -> Win {
-            Win it{-1, -1, -1, 0};
+            Win it{-1, -1, -1, 0, 0.f, 0.f};
             const int k = k0 + lane;
             if (k >= n_items) return it;
             const int64_t p = pos0 + k;
@@ -400,12 +404,38 @@ __global__ void __launch_bounds__(DecodeCfg<D, F8, MULTI>::THREADS, 1)
             const int s = MULTI ? int(seq_of[b]) : b;  // the row's sequence
             it.phys = (it.j >= 0 && it.j < a.MBS) ? __ldg(a.bt + int64_t(s) * a.MBS + it.j) : -1;
         };
+        // E4M3 cache: the item's scales, per KV head or per (physical block,
+        // KV head); with per-block scales this load depends on the block-table
+        // entry, so it runs one window after stage B
+        auto stage_s = [&](Win &it) {
+            if constexpr (F8) {
+                if (it.seg < 0) return;
+                const int kvh = it.seg % Hkv;
+                if (!a.scale_per_block) {
+                    it.sk = __ldg(a.k_scale + kvh);
+                    it.sv = __ldg(a.v_scale + kvh);
+                } else if (it.phys >= 0 && int64_t(it.phys) < a.NB) {
+                    it.sk = __ldg(a.k_scale + int64_t(it.phys) * Hkv + kvh);
+                    it.sv = __ldg(a.v_scale + int64_t(it.phys) * Hkv + kvh);
+                }
+            }
+        };
         const uint64_t policy = l2_policy_evict_first();
         if (SPARSE && a.scores) fence_proxy_async();  // the ring held the top-K scratch
         Win wa = stage_c(0), wb = stage_c(32);
         stage_b(wa);
         stage_b(wb);
         Win wc = stage_c(64);
+        // E4M3 cache: a fourth window, so the scale loads (stage S) have a
+        // window to land in: wa issued, wb scales, wc block-table entries,
+        // wd context and selection
+        Win wd{-1, -1, -1, 0, 0.f, 0.f};
+        if constexpr (F8) {
+            stage_b(wc);
+            wd = stage_c(96);
+            stage_s(wa);
+            stage_s(wb);
+        }
         int wbase = 0;
         int issued = 0;  // items [0, issued) have been armed
         int fail_step = 0;
@@ -421,15 +451,28 @@ __global__ void __launch_bounds__(DecodeCfg<D, F8, MULTI>::THREADS, 1)
             if (k0 >= wbase + 32) {
                 wa = wb;
                 wb = wc;
-                stage_b(wb);
-                wbase += 32;
-                wc = stage_c(wbase + 64);
+                if constexpr (F8) {
+                    wc = wd;
+                    stage_s(wb);
+                    stage_b(wc);
+                    wbase += 32;
+                    wd = stage_c(wbase + 96);
+                } else {
+                    stage_b(wb);
+                    wbase += 32;
+                    wc = stage_c(wbase + 64);
+                }
             }
             const int k = k0 + it;
             const int seg = __shfl_sync(0xffffffffu, wa.seg, k & 31);
             const int j = __shfl_sync(0xffffffffu, wa.j, k & 31);
             const int ph = __shfl_sync(0xffffffffu, wa.phys, k & 31);
             const int cv = __shfl_sync(0xffffffffu, wa.ctxv, k & 31);
+            float sk = 0.f, sv = 0.f;
+            if constexpr (F8) {
+                sk = __shfl_sync(0xffffffffu, wa.sk, k & 31);
+                sv = __shfl_sync(0xffffffffu, wa.sv, k & 31);
+            }
             const bool live = k < n_items;
             const int c = min(max(cv, 0), max_tok);
             const int nblk = (c + BS - 1) / BS;
@@ -444,6 +487,7 @@ __global__ void __launch_bounds__(DecodeCfg<D, F8, MULTI>::THREADS, 1)
                     ok = 0;
                 } else {
                     info[st] = make_int2(MULTI ? j : seg, nv);  // MULTI: consumers mask per query row
+                    if constexpr (F8) iscale[st] = make_float2(sk, sv);
                     if (nv > 0) mbar_arrive_expect_tx(fb, C::STAGE);
                     else mbar_arrive(fb);
                 }
@@ -499,8 +543,10 @@ __global__ void __launch_bounds__(DecodeCfg<D, F8, MULTI>::THREADS, 1)
     // ==================================================================== consumers
     const int c_id = warp;  // 0 .. NC-1
     const int g = lane >> 2, q4 = lane & 3;
-    float scale_log2 = a.scale_log2;  // E4M3 cache: times the segment's K scale
-    float v_scale = 1.f;               // E4M3 cache: the segment's V scale
+    const float scale_log2 = a.scale_log2;
+    // E4M3 cache: acc holds O / vref, vref the largest V scale of the
+    // segment's blocks seen so far (0 before the first)
+    float vref = 0.f;
     uint32_t qb[NKK][2];
     float acc[NKK][4];
     float m0, m1, l0, l1;
@@ -523,8 +569,7 @@ __global__ void __launch_bounds__(DecodeCfg<D, F8, MULTI>::THREADS, 1)
                 qb[kk][0] = pack_f16x2(bf16_lo(v.x), bf16_hi(v.x));
                 qb[kk][1] = pack_f16x2(bf16_lo(v.y), bf16_hi(v.y));
             }
-            scale_log2 = a.scale_log2 * __ldg(a.k_scale + kvh);
-            v_scale = __ldg(a.v_scale + kvh);
+            vref = 0.f;
         } else {
 #pragma unroll
             for (int kk = 0; kk < NKK; ++kk) {
@@ -655,21 +700,41 @@ __global__ void __launch_bounds__(DecodeCfg<D, F8, MULTI>::THREADS, 1)
         const uint32_t s0a = base + (ka % S) * C::STAGE;
         const uint32_t s1a = base + (kb_ % S) * C::STAGE;
         float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
+        float sla = scale_log2, slb = scale_log2;  // times the blocks' K scales (E4M3)
+        float ra = 1.f, rb = 1.f, vr = 1.f;        // V scale ratios (E4M3), warp-uniform
         if constexpr (F8) {
             if (nva > 0) qk8(s0a, s0);
             if (nvb > 0) qk8(s1a, s1);
+            // Each block's V codes stand for decode(code) * sv. acc is kept in
+            // units of vref = the largest sv so far: a block with a larger sv
+            // rescales acc by vref / sv first; a block's P enters the PV
+            // product times sv / vref (1 for per-KV-head scales; a power of
+            // two for per-block ones, so the f16 product is exact down to
+            // the f16 subnormal range).
+            const float2 ca = iscale[ka % S], cb = iscale[kb_ % S];
+            sla = scale_log2 * ca.x;
+            slb = scale_log2 * cb.x;
+            float vnew = vref;
+            if (nva > 0) vnew = fmaxf(vnew, ca.y);
+            if (nvb > 0) vnew = fmaxf(vnew, cb.y);
+            if (vnew != vref) {
+                vr = __fdiv_rn(vref, vnew);
+                vref = vnew;
+            }
+            if (nva > 0 && ca.y != vnew) ra = __fdiv_rn(ca.y, vnew);
+            if (nvb > 0 && cb.y != vnew) rb = __fdiv_rn(cb.y, vnew);
         } else {
             if (nva > 0) qk(s0a, s0);
             if (nvb > 0) qk(s1a, s1);
         }
-        const float x0 = (g < nva) ? s0[0] * scale_log2 : -INFINITY;
-        const float x1 = (g < nva) ? s0[1] * scale_log2 : -INFINITY;
-        const float x2 = (g + 8 < nva) ? s0[2] * scale_log2 : -INFINITY;
-        const float x3 = (g + 8 < nva) ? s0[3] * scale_log2 : -INFINITY;
-        const float y0 = (g < nvb) ? s1[0] * scale_log2 : -INFINITY;
-        const float y1 = (g < nvb) ? s1[1] * scale_log2 : -INFINITY;
-        const float y2 = (g + 8 < nvb) ? s1[2] * scale_log2 : -INFINITY;
-        const float y3 = (g + 8 < nvb) ? s1[3] * scale_log2 : -INFINITY;
+        const float x0 = (g < nva) ? s0[0] * sla : -INFINITY;
+        const float x1 = (g < nva) ? s0[1] * sla : -INFINITY;
+        const float x2 = (g + 8 < nva) ? s0[2] * sla : -INFINITY;
+        const float x3 = (g + 8 < nva) ? s0[3] * sla : -INFINITY;
+        const float y0 = (g < nvb) ? s1[0] * slb : -INFINITY;
+        const float y1 = (g < nvb) ? s1[1] * slb : -INFINITY;
+        const float y2 = (g + 8 < nvb) ? s1[2] * slb : -INFINITY;
+        const float y3 = (g + 8 < nvb) ? s1[3] * slb : -INFINITY;
         float bm0 = fmaxf(fmaxf(x0, x2), fmaxf(y0, y2));
         float bm1 = fmaxf(fmaxf(x1, x3), fmaxf(y1, y3));
 #pragma unroll
@@ -681,7 +746,7 @@ __global__ void __launch_bounds__(DecodeCfg<D, F8, MULTI>::THREADS, 1)
         const float r0 = (mn0 == -INFINITY) ? 0.f : mn0;
         const float r1 = (mn1 == -INFINITY) ? 0.f : mn1;
         const bool grow = (mn0 != m0) || (mn1 != m1);
-        const float al0 = fast_exp2(m0 - r0), al1 = fast_exp2(m1 - r1);
+        float al0 = fast_exp2(m0 - r0), al1 = fast_exp2(m1 - r1);
         // P rounded to the mma input type (bf16, or f16 for an E4M3 cache);
         // the normaliser sums the rounded values
         auto pk = [](float lo, float hi) { return F8 ? pack_f16x2(lo, hi) : pack_bf16x2(lo, hi); };
@@ -695,7 +760,15 @@ __global__ void __launch_bounds__(DecodeCfg<D, F8, MULTI>::THREADS, 1)
         l1 = l1 * al1 + ((phi(p01) + phi(p23)) + (phi(q01) + phi(q23)));
         m0 = mn0;
         m1 = mn1;
-        if (__any_sync(0xffffffffu, grow)) {
+        bool rescale = __any_sync(0xffffffffu, grow);
+        if constexpr (F8) {
+            if (vr != 1.f) {  // acc into the units of the new vref (l keeps its own)
+                al0 *= vr;
+                al1 *= vr;
+                rescale = true;
+            }
+        }
+        if (rescale) {
 #pragma unroll
             for (int mt = 0; mt < NKK; ++mt) {
                 acc[mt][0] *= al0;
@@ -705,8 +778,14 @@ __global__ void __launch_bounds__(DecodeCfg<D, F8, MULTI>::THREADS, 1)
             }
         }
         if constexpr (F8) {
-            if (nva > 0) pv8(s0a + C::KT, p01, p23, nva);
-            if (nvb > 0) pv8(s1a + C::KT, q01, q23, nvb);
+            if (nva > 0) {
+                if (ra != 1.f) pv8(s0a + C::KT, scale_f16x2(p01, ra), scale_f16x2(p23, ra), nva);
+                else pv8(s0a + C::KT, p01, p23, nva);
+            }
+            if (nvb > 0) {
+                if (rb != 1.f) pv8(s1a + C::KT, scale_f16x2(q01, rb), scale_f16x2(q23, rb), nvb);
+                else pv8(s1a + C::KT, q01, q23, nvb);
+            }
         } else {
             if (nva > 0) pv(s0a + C::KT, p01, p23, nva);
             if (nvb > 0) pv(s1a + C::KT, q01, q23, nvb);
@@ -817,12 +896,12 @@ __global__ void __launch_bounds__(DecodeCfg<D, F8, MULTI>::THREADS, 1)
         const int hh = 2 * q4;
 #pragma unroll
         for (int mt = 0; mt < NKK; ++mt) {
-            if constexpr (F8) {  // the V scale of the segment's KV head
+            if constexpr (F8) {  // acc is in units of vref
                 const int d = 16 * mt + g;
                 *reinterpret_cast<float2 *>(my + d * 8 + hh) =
-                    make_float2(acc[mt][0] * v_scale, acc[mt][1] * v_scale);
+                    make_float2(acc[mt][0] * vref, acc[mt][1] * vref);
                 *reinterpret_cast<float2 *>(my + (d + 8) * 8 + hh) =
-                    make_float2(acc[mt][2] * v_scale, acc[mt][3] * v_scale);
+                    make_float2(acc[mt][2] * vref, acc[mt][3] * vref);
             } else {
                 const int d = 16 * mt + g;
                 *reinterpret_cast<float2 *>(my + d * 8 + hh) = make_float2(acc[mt][0], acc[mt][1]);

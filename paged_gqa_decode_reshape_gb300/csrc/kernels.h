@@ -22,8 +22,9 @@ struct DecodeArgs {
     const int32_t *bt;          // [B][MBS]
     const int32_t *ctx;         // [B]
     const int32_t *sel;         // [B][Hkv][topk] (sparse only)
-    const float *k_scale;       // [Hkv] per-KV-head scales of an E4M3 cache (else null)
-    const float *v_scale;
+    const float *k_scale;       // scales of an E4M3 cache (else null): [Hkv] per KV head,
+    const float *v_scale;       // or [NB][Hkv] per physical block when scale_per_block
+    int scale_per_block;
     const uint8_t *v8;          // E4M3 V cache [NB][Hkv][D][16] (else null): tiles are contiguous
     const int32_t *cu_q;        // multi-token rows: [nseq + 1] row offsets per sequence (else null;
                                 // B then counts query rows, ctx / bt are per sequence)
@@ -88,14 +89,24 @@ cudaError_t launch_rebuild_meta_fp8(uint8_t *kmin, uint8_t *kmax, const uint8_t 
                                     int MBS, const int32_t *ctx, int B, int Hkv, int D, int BS, int64_t NB,
                                     cudaStream_t stream);
 
+// E4M3 cache with per-block scales: ReshapeAndCache (and the metadata when
+// kmin is not null) with the scales k_bscale / v_bscale [NB][Hkv] kept up to
+// date (powers of two; 0 for an empty block)
+cudaError_t launch_write_fp8_block(uint8_t *kc, uint8_t *vc, uint8_t *kmin, uint8_t *kmax, float *k_bscale,
+                                   float *v_bscale, const uint16_t *key, const uint16_t *value,
+                                   const int64_t *slots, int64_t T, int Hkv, int D, int BS, int64_t NB,
+                                   cudaStream_t stream);
+
 // block scores only (the first launch of the fused Quest decode)
+// k_bscale: per-block K scales [NB][Hkv] of an E4M3 cache (else null)
 cudaError_t launch_quest_scores(float *scores, const uint16_t *q, const void *kmin, const void *kmax,
                                 const int32_t *bt, int MBS, const int32_t *ctx, int B, int Hq, int Hkv, int D,
-                                int BS, int64_t NB, cudaStream_t stream, bool fp8 = false);
+                                int BS, int64_t NB, cudaStream_t stream, bool fp8 = false,
+                                const float *k_bscale = nullptr);
 // kmin / kmax: bf16 metadata, or E4M3 codes when fp8 (head_dim 128)
 cudaError_t launch_quest_select(int32_t *sel, float *scores, const uint16_t *q, const void *kmin,
                                 const void *kmax, const int32_t *bt, int MBS, const int32_t *ctx,
                                 int B, int Hq, int Hkv, int D, int BS, int64_t NB, int topk,
-                                cudaStream_t stream, bool fp8 = false);
+                                cudaStream_t stream, bool fp8 = false, const float *k_bscale = nullptr);
 
 }  // namespace pa

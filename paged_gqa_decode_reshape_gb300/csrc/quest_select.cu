@@ -43,12 +43,14 @@ constexpr int kChunk = 8;
 constexpr int kScoreThreads = 256;
 
 // F8: the metadata are E4M3 codes (one byte per element, decoded exactly);
-// the score is the same fp32 expression of the decoded values.
+// the score is the same fp32 expression of the decoded values. With
+// per-block scales (kbs [NB][Hkv], else null) the block's score is then
+// multiplied by its K scale (one fp32 product, exact for a power of two).
 template <int D, bool F8>
 __global__ void __launch_bounds__(kScoreThreads, 4) quest_score_kernel(
     float *__restrict__ scores, const uint16_t *__restrict__ q, const void *__restrict__ kmin_v,
-    const void *__restrict__ kmax_v, const int32_t *__restrict__ bt, int MBS,
-    const int32_t *__restrict__ ctx, int B, int Hq, int Hkv, int BS, int64_t NB) {
+    const void *__restrict__ kmax_v, const float *__restrict__ kbs, const int32_t *__restrict__ bt,
+    int MBS, const int32_t *__restrict__ ctx, int B, int Hq, int Hkv, int BS, int64_t NB) {
     static_assert(!F8 || D == 128, "E4M3 metadata: head_dim 128");
     const uint16_t *__restrict__ kmin = static_cast<const uint16_t *>(kmin_v);
     const uint16_t *__restrict__ kmax = static_cast<const uint16_t *>(kmax_v);
@@ -154,6 +156,10 @@ __global__ void __launch_bounds__(kScoreThreads, 4) quest_score_kernel(
                 mxv[u][0] = __ldg(reinterpret_cast<const uint32_t *>(kmax + off));
             }
         }
+        // per-block K scale of block j0 + lane (E4M3 cache with block scales)
+        const float bsc = (F8 && kbs && lane < cnt && ph_l >= 0 && int64_t(ph_l) < NB)
+                              ? __ldg(kbs + int64_t(ph_l) * Hkv + kvh)
+                              : 1.f;
         float mine = -INFINITY;  // lane u keeps block j0 + u's score
 #pragma unroll
         for (int u = 0; u < kChunk; ++u) {
@@ -178,6 +184,7 @@ __global__ void __launch_bounds__(kScoreThreads, 4) quest_score_kernel(
             for (int o = 16; o >= 1; o >>= 1) acc = __fadd_rn(acc, __shfl_xor_sync(0xffffffffu, acc, o));
             if (lane == u) mine = ok[u] ? acc : -INFINITY;
         }
+        if (F8 && kbs && lane < cnt && mine != -INFINITY) mine = __fmul_rn(mine, bsc);
         if (lane < cnt) scores[(int64_t(b) * Hkv + kvh) * MBS + j0 + lane] = mine;
         // next chunk
         if (++ch == nch) {
@@ -230,8 +237,8 @@ __global__ void __launch_bounds__(kTopkThreads, 4) quest_topk_kernel(
 
 template <int D, bool F8>
 cudaError_t launch_score(float *scores, const uint16_t *q, const void *kmin, const void *kmax,
-                         const int32_t *bt, int MBS, const int32_t *ctx, int B, int Hq, int Hkv,
-                         int BS, int64_t NB, cudaStream_t stream) {
+                         const float *kbs, const int32_t *bt, int MBS, const int32_t *ctx, int B, int Hq,
+                         int Hkv, int BS, int64_t NB, cudaStream_t stream) {
     // persistent grid, every SM full (computed once, thread-safe; the same on
     // every GPU of a node)
     static const int grid = [] {
@@ -246,34 +253,30 @@ cudaError_t launch_score(float *scores, const uint16_t *q, const void *kmin, con
     if (grid == 0) return cudaErrorInvalidConfiguration;
     const size_t smem = size_t(B + 1) * 4;
     return launch_pdl(quest_score_kernel<D, F8>, dim3(grid), dim3(kScoreThreads), smem, stream, scores, q,
-                      kmin, kmax, bt, MBS, ctx, B, Hq, Hkv, BS, NB);
+                      kmin, kmax, kbs, bt, MBS, ctx, B, Hq, Hkv, BS, NB);
 }
 
 }  // namespace
 
 cudaError_t launch_quest_scores(float *scores, const uint16_t *q, const void *kmin, const void *kmax,
                                 const int32_t *bt, int MBS, const int32_t *ctx, int B, int Hq, int Hkv, int D,
-                                int BS, int64_t NB, cudaStream_t stream, bool fp8) {
+                                int BS, int64_t NB, cudaStream_t stream, bool fp8, const float *k_bscale) {
     if (fp8) {
         if (D != 128) return cudaErrorInvalidValue;
-        return launch_score<128, true>(scores, q, kmin, kmax, bt, MBS, ctx, B, Hq, Hkv, BS, NB, stream);
+        return launch_score<128, true>(scores, q, kmin, kmax, k_bscale, bt, MBS, ctx, B, Hq, Hkv, BS, NB,
+                                       stream);
     }
-    return D == 128 ? launch_score<128, false>(scores, q, kmin, kmax, bt, MBS, ctx, B, Hq, Hkv, BS, NB, stream)
-                    : launch_score<64, false>(scores, q, kmin, kmax, bt, MBS, ctx, B, Hq, Hkv, BS, NB, stream);
+    return D == 128
+               ? launch_score<128, false>(scores, q, kmin, kmax, nullptr, bt, MBS, ctx, B, Hq, Hkv, BS, NB, stream)
+               : launch_score<64, false>(scores, q, kmin, kmax, nullptr, bt, MBS, ctx, B, Hq, Hkv, BS, NB, stream);
 }
 
 cudaError_t launch_quest_select(int32_t *sel, float *scores, const uint16_t *q, const void *kmin,
                                 const void *kmax, const int32_t *bt, int MBS, const int32_t *ctx,
                                 int B, int Hq, int Hkv, int D, int BS, int64_t NB, int topk,
-                                cudaStream_t stream, bool fp8) {
-    cudaError_t e;
-    if (fp8) {
-        if (D != 128) return cudaErrorInvalidValue;
-        e = launch_score<128, true>(scores, q, kmin, kmax, bt, MBS, ctx, B, Hq, Hkv, BS, NB, stream);
-    } else {
-        e = D == 128 ? launch_score<128, false>(scores, q, kmin, kmax, bt, MBS, ctx, B, Hq, Hkv, BS, NB, stream)
-                     : launch_score<64, false>(scores, q, kmin, kmax, bt, MBS, ctx, B, Hq, Hkv, BS, NB, stream);
-    }
+                                cudaStream_t stream, bool fp8, const float *k_bscale) {
+    const cudaError_t e =
+        launch_quest_scores(scores, q, kmin, kmax, bt, MBS, ctx, B, Hq, Hkv, D, BS, NB, stream, fp8, k_bscale);
     if (e != cudaSuccess) return e;
     return launch_pdl(quest_topk_kernel, dim3(unsigned(B) * unsigned(Hkv)), dim3(kTopkThreads), 0, stream,
                       sel, static_cast<const float *>(scores), MBS, ctx, Hkv, BS, topk);

@@ -56,7 +56,8 @@ class StepBytes:
 
 def step_bytes(context_lens: np.ndarray, slot_mapping: np.ndarray, Hq: int, Hkv: int, D: int,
                BS: int, topk: int, selected: Optional[np.ndarray] = None,
-               elem_bytes: int = BF16, io_elem_bytes: int = BF16, q_rows: int = 1) -> StepBytes:
+               elem_bytes: int = BF16, io_elem_bytes: int = BF16, q_rows: int = 1,
+               block_scales: bool = False) -> StepBytes:
     """Algorithmic bytes of one step's five calls.
 
     reshape: new K and V rows read and written, plus the slots;
@@ -72,7 +73,10 @@ def step_bytes(context_lens: np.ndarray, slot_mapping: np.ndarray, Hq: int, Hkv:
     for an 8-bit cache); io_elem_bytes that of q, out and the new K/V rows
     (bf16 in both cases). q_rows is the number of query rows per sequence of
     the dense call (multi-token rows: each sequence's KV is still read once,
-    the query and output bytes scale with the rows).
+    the query and output bytes scale with the rows). block_scales: an 8-bit
+    cache with per-block scales, whose fp32 K and V scale per (block, KV
+    head) are read with each block (K only for the selection) and read and
+    written by the write path for each touched block.
     """
     ctx = np.clip(np.asarray(context_lens, dtype=np.int64), 0, None)
     slots = np.asarray(slot_mapping, dtype=np.int64)
@@ -101,5 +105,11 @@ def step_bytes(context_lens: np.ndarray, slot_mapping: np.ndarray, Hq: int, Hkv:
                 nsel += js.shape[0]
                 tokens += int(np.minimum(BS, ctx[b] - js * BS).sum())
         sparse = tokens * 2 * D * elem_bytes + 2 * q_bytes + B * Hkv * topk * 4 + nsel * 4 + 4 * B
+    if block_scales:
+        reshape += touched * Hkv * 2 * 4 * 2
+        dense += int(nb.sum()) * Hkv * 2 * 4
+        select += int(nb.sum()) * Hkv * 4
+        if selected is not None:
+            sparse += nsel * 2 * 4
     return StepBytes(reshape=int(reshape), meta=int(meta), dense=int(dense), select=int(select),
                      sparse=int(sparse))
