@@ -286,17 +286,30 @@ __device__ __forceinline__ void cta_load_keys(uint32_t *keys, const float *row, 
 // highest bit where the row's smallest and largest keys differ (the scores of
 // a row share their sign, exponent and often more, so a fixed first digit
 // would put every key into one bin and serialise its atomic adds).
-// hist: 256 ints of shared memory; red: at least 2 * THREADS / 32 + 2 ints.
-template <int THREADS, typename KeyOf>
+// hist: HC * 256 ints of shared memory, HC histogram copies (warp w adds to
+// copy w % HC: the keys of a row crowd into few bins, and copies spread the
+// atomic adds of different warps over different addresses); red: at least
+// 2 * THREADS / 32 + 2 ints.
+template <int THREADS, int HC = 1, typename KeyOf>
 __device__ __forceinline__ void cta_topk_threshold(KeyOf key_of, int n, int topk, int *hist, int *red,
                                                    uint32_t &thr, int &keq) {
-    constexpr int NW = THREADS / 32;
+    static_assert(HC >= 1 && HC <= THREADS / 32, "one histogram copy per warp at most");
+    constexpr int NW = THREADS / 32, U = 4;  // U keys per thread in flight
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     uint32_t lo = 0xffffffffu, hi = 0u;
-    for (int j = tid; j < n; j += THREADS) {
-        const uint32_t u = key_of(j);
-        lo = min(lo, u);
-        hi = max(hi, u);
+    for (int j0 = tid; j0 < n; j0 += U * THREADS) {
+        uint32_t u[U];
+#pragma unroll
+        for (int i = 0; i < U; ++i) {
+            const int j = j0 + i * THREADS;
+            u[i] = j < n ? key_of(j) : 0u;
+        }
+#pragma unroll
+        for (int i = 0; i < U; ++i)
+            if (j0 + i * THREADS < n) {
+                lo = min(lo, u[i]);
+                hi = max(hi, u[i]);
+            }
     }
 #pragma unroll
     for (int o = 16; o >= 1; o >>= 1) {
@@ -328,11 +341,19 @@ __device__ __forceinline__ void cta_topk_threshold(KeyOf key_of, int n, int topk
     for (int h = top; h >= 0;) {
         const int l = h >= 7 ? h - 7 : 0;
         const uint32_t dm = (2u << (h - l)) - 1u;  // digit of bits l..h
-        for (int i = tid; i < 256; i += THREADS) hist[i] = 0;
+        for (int i = tid; i < HC * 256; i += THREADS) hist[i] = 0;
         __syncthreads();
-        for (int j = tid; j < n; j += THREADS) {
-            const uint32_t u = key_of(j);
-            if ((u & mask) == prefix) atomicAdd(&hist[(u >> l) & dm], 1);
+        int *my_hist = hist + (warp % HC) * 256;
+        for (int j0 = tid; j0 < n; j0 += U * THREADS) {
+            uint32_t u[U];
+#pragma unroll
+            for (int i = 0; i < U; ++i) {
+                const int j = j0 + i * THREADS;
+                u[i] = j < n ? key_of(j) : 0u;
+            }
+#pragma unroll
+            for (int i = 0; i < U; ++i)
+                if (j0 + i * THREADS < n && (u[i] & mask) == prefix) atomicAdd(&my_hist[(u[i] >> l) & dm], 1);
         }
         __syncthreads();
         if (warp == 0) {
@@ -340,7 +361,9 @@ __device__ __forceinline__ void cta_topk_threshold(KeyOf key_of, int n, int topk
             int cnt[8], sum = 0;
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
-                cnt[i] = hist[255 - 8 * lane - i];
+                cnt[i] = 0;
+#pragma unroll
+                for (int c = 0; c < HC; ++c) cnt[i] += hist[c * 256 + 255 - 8 * lane - i];
                 sum += cnt[i];
             }
             int incl = sum;
@@ -375,43 +398,52 @@ __device__ __forceinline__ void cta_topk_threshold(KeyOf key_of, int n, int topk
 
 // The selection for a threshold: every key above thr and the keq lowest-index
 // keys equal to it, emitted as emit(r, j) with r the rank of block j among
-// the selected (ascending j). Each warp counts, then emits, one contiguous
-// range of keys; red: at least 2 * THREADS / 32 ints.
+// the selected (ascending j). The row is cut into one contiguous range per
+// thread (ranges ascending with the thread index): each thread counts its
+// keys above and equal to thr, an exclusive scan over the CTA gives every
+// thread its first rank and the equal keys before it, then each thread emits
+// its own range in order. red: at least 2 * THREADS / 32 ints.
 template <int THREADS, typename KeyOf, typename Emit>
 __device__ __forceinline__ void cta_topk_emit(KeyOf key_of, int n, uint32_t thr, int keq, int *red, Emit emit) {
     constexpr int NW = THREADS / 32;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const unsigned lt = (1u << lane) - 1u;
-    const int per = ((n + NW * 32 - 1) / (NW * 32)) * 32;
-    const int jb = warp * per, je = min(n, jb + per);
+    const int per = (n + THREADS - 1) / THREADS;  // keys per thread
+    const int j0 = min(n, tid * per), j1 = min(n, j0 + per);
     int cgt = 0, ceq = 0;
-    for (int j0 = jb; j0 < je; j0 += 32) {
-        const int j = j0 + lane;
-        const uint32_t u = j < je ? key_of(j) : 0u;
-        cgt += __popc(__ballot_sync(0xffffffffu, j < je && u > thr));
-        ceq += __popc(__ballot_sync(0xffffffffu, j < je && u == thr));
+    for (int j = j0; j < j1; ++j) {
+        const uint32_t u = key_of(j);
+        cgt += u > thr;
+        ceq += u == thr;
     }
-    if (lane == 0) {
-        red[warp] = cgt;
-        red[NW + warp] = ceq;
+    // exclusive scans of the two counts over the warp, then over the warps
+    int xgt = cgt, xeq = ceq;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int a = __shfl_up_sync(0xffffffffu, xgt, o), b = __shfl_up_sync(0xffffffffu, xeq, o);
+        if (lane >= o) {
+            xgt += a;
+            xeq += b;
+        }
     }
+    if (lane == 31) {
+        red[warp] = xgt;
+        red[NW + warp] = xeq;
+    }
+    xgt -= cgt;
+    xeq -= ceq;
     __syncthreads();
-    int run_eq = 0, run_pos = 0;
     for (int w = 0; w < warp; ++w) {
-        const int e = red[NW + w];
-        run_pos += red[w] + min(max(keq - run_eq, 0), e);
-        run_eq += e;
+        xgt += red[w];
+        xeq += red[NW + w];
     }
-    for (int j0 = jb; j0 < je; j0 += 32) {
-        const int j = j0 + lane;
-        const uint32_t u = j < je ? key_of(j) : 0u;
-        const bool gt = j < je && u > thr, eq = j < je && u == thr;
-        const unsigned beq = __ballot_sync(0xffffffffu, eq);
-        const bool take = gt || (eq && run_eq + __popc(beq & lt) < keq);
-        const unsigned btk = __ballot_sync(0xffffffffu, take);
-        if (take) emit(run_pos + __popc(btk & lt), j);
-        run_eq += __popc(beq);
-        run_pos += __popc(btk);
+    // rank of the thread's first selected key: the keys above thr before it,
+    // plus the equal keys before it that are taken
+    int pos = xgt + min(max(keq, 0), xeq), seen_eq = xeq;
+    for (int j = j0; j < j1; ++j) {
+        const uint32_t u = key_of(j);
+        const bool take = u > thr || (u == thr && seen_eq < keq);
+        seen_eq += u == thr;
+        if (take) emit(pos++, j);
     }
     __syncthreads();  // red may be reused by the caller
 }

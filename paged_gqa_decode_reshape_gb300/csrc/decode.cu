@@ -112,9 +112,12 @@ struct DecodeCfg {
     static constexpr size_t sel_off(int PB) { return row0_off(PB, 0); }
     static constexpr size_t smem_bytes_sel(int PB, int nsel) { return 1024 + sel_off(PB) + size_t(nsel) * 4; }
     // top-K scratch of the fused Quest decode, in the ring (free until the
-    // first copy): the keys, then 256 histogram bins and per-warp counts
-    static constexpr int KEYS_CAP = int((size_t(S) * STAGE - 4096) / 4);
-    static constexpr size_t off_topk_hist = size_t(S) * STAGE - 4096;
+    // first copy): the keys, then one 256-bin histogram per warp and the
+    // per-warp counts
+    static constexpr int TOPK_HC = THREADS / 32;
+    static constexpr size_t TOPK_SCRATCH = size_t(TOPK_HC) * 1024 + 256;
+    static constexpr int KEYS_CAP = int((size_t(S) * STAGE - TOPK_SCRATCH) / 4);
+    static constexpr size_t off_topk_hist = size_t(S) * STAGE - TOPK_SCRATCH;
 };
 
 // One binary serves the dense call and the sparse one (topk > 0: the items
@@ -122,11 +125,15 @@ struct DecodeCfg {
 // brought into the SMs' instruction caches; code that runs once per CTA (the
 // prologue, the merge and the combine) is otherwise fetched cold, several
 // microseconds per launch.
-template <int D, bool F8, bool MULTI>
+// BSC (E4M3 cache only): per-block scales, read per item, instead of one K
+// and V scale per KV head.
+template <int D, bool F8, bool MULTI, bool BSC = false>
 __global__ void __launch_bounds__(DecodeCfg<D, F8, MULTI>::THREADS, 1)
     decode_kernel(const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const DecodeArgs a) {
     using C = DecodeCfg<D, F8, MULTI>;
+    static_assert(!BSC || (F8 && !MULTI), "per-block scales: the E4M3 cache, one query row");
+    constexpr bool PSC = F8 && BSC;  // per-item scales
     const bool SPARSE = !MULTI && a.topk > 0;
     constexpr int BS = C::BS, NC = C::NC, S = C::S, NKK = C::NKK;
 
@@ -322,7 +329,7 @@ __global__ void __launch_bounds__(DecodeCfg<D, F8, MULTI>::THREADS, 1)
     if (SPARSE && a.scores) {
         uint32_t *keys = reinterpret_cast<uint32_t *>(bp);  // the ring: no copy has been issued yet
         int *hist = reinterpret_cast<int *>(bp + C::off_topk_hist);
-        int *wcnt = hist + 256;  // scratch of the top-K helpers
+        int *wcnt = hist + C::TOPK_HC * 256;  // scratch of the top-K helpers
         int64_t p = pos0;
         int b = find_seq(p);
         int kvh = int((p - int64_t(Hkv) * pre[b]) / (pre[b + 1] - pre[b]));
@@ -350,7 +357,7 @@ __global__ void __launch_bounds__(DecodeCfg<D, F8, MULTI>::THREADS, 1)
                 auto key_of = [&](int j) -> uint32_t { return cached ? keys[j] : f32_order_key(__ldcg(srow + j)); };
                 uint32_t thr;
                 int keq;
-                cta_topk_threshold<C::THREADS>(key_of, n, topk, hist, wcnt, thr, keq);
+                cta_topk_threshold<C::THREADS, C::TOPK_HC>(key_of, n, topk, hist, wcnt, thr, keq);
                 cta_topk_emit<C::THREADS>(key_of, n, thr, keq, wcnt, [&](int r, int j) {
                     if (writer) orow[r] = j;
                     if (r >= i0 && r < i1) mine[r] = j;
@@ -404,20 +411,15 @@ __global__ void __launch_bounds__(DecodeCfg<D, F8, MULTI>::THREADS, 1)
             const int s = MULTI ? int(seq_of[b]) : b;  // the row's sequence
             it.phys = (it.j >= 0 && it.j < a.MBS) ? __ldg(a.bt + int64_t(s) * a.MBS + it.j) : -1;
         };
-        // E4M3 cache: the item's scales, per KV head or per (physical block,
-        // KV head); with per-block scales this load depends on the block-table
-        // entry, so it runs one window after stage B
+        // per-block scales: the item's K and V scale of its (physical block,
+        // KV head); the load depends on the block-table entry, so it runs one
+        // window after stage B
         auto stage_s = [&](Win &it) {
-            if constexpr (F8) {
-                if (it.seg < 0) return;
-                const int kvh = it.seg % Hkv;
-                if (!a.scale_per_block) {
-                    it.sk = __ldg(a.k_scale + kvh);
-                    it.sv = __ldg(a.v_scale + kvh);
-                } else if (it.phys >= 0 && int64_t(it.phys) < a.NB) {
-                    it.sk = __ldg(a.k_scale + int64_t(it.phys) * Hkv + kvh);
-                    it.sv = __ldg(a.v_scale + int64_t(it.phys) * Hkv + kvh);
-                }
+            if constexpr (PSC) {
+                if (it.seg < 0 || it.phys < 0 || int64_t(it.phys) >= a.NB) return;
+                const int64_t si = int64_t(it.phys) * Hkv + it.seg % Hkv;
+                it.sk = __ldg(a.k_scale + si);
+                it.sv = __ldg(a.v_scale + si);
             }
         };
         const uint64_t policy = l2_policy_evict_first();
@@ -426,11 +428,11 @@ __global__ void __launch_bounds__(DecodeCfg<D, F8, MULTI>::THREADS, 1)
         stage_b(wa);
         stage_b(wb);
         Win wc = stage_c(64);
-        // E4M3 cache: a fourth window, so the scale loads (stage S) have a
-        // window to land in: wa issued, wb scales, wc block-table entries,
+        // per-block scales: a fourth window, so the scale loads (stage S) have
+        // a window to land in: wa issued, wb scales, wc block-table entries,
         // wd context and selection
         Win wd{-1, -1, -1, 0, 0.f, 0.f};
-        if constexpr (F8) {
+        if constexpr (PSC) {
             stage_b(wc);
             wd = stage_c(96);
             stage_s(wa);
@@ -451,7 +453,7 @@ __global__ void __launch_bounds__(DecodeCfg<D, F8, MULTI>::THREADS, 1)
             if (k0 >= wbase + 32) {
                 wa = wb;
                 wb = wc;
-                if constexpr (F8) {
+                if constexpr (PSC) {
                     wc = wd;
                     stage_s(wb);
                     stage_b(wc);
@@ -469,7 +471,7 @@ __global__ void __launch_bounds__(DecodeCfg<D, F8, MULTI>::THREADS, 1)
             const int ph = __shfl_sync(0xffffffffu, wa.phys, k & 31);
             const int cv = __shfl_sync(0xffffffffu, wa.ctxv, k & 31);
             float sk = 0.f, sv = 0.f;
-            if constexpr (F8) {
+            if constexpr (PSC) {
                 sk = __shfl_sync(0xffffffffu, wa.sk, k & 31);
                 sv = __shfl_sync(0xffffffffu, wa.sv, k & 31);
             }
@@ -487,7 +489,7 @@ __global__ void __launch_bounds__(DecodeCfg<D, F8, MULTI>::THREADS, 1)
                     ok = 0;
                 } else {
                     info[st] = make_int2(MULTI ? j : seg, nv);  // MULTI: consumers mask per query row
-                    if constexpr (F8) iscale[st] = make_float2(sk, sv);
+                    if constexpr (PSC) iscale[st] = make_float2(sk, sv);
                     if (nv > 0) mbar_arrive_expect_tx(fb, C::STAGE);
                     else mbar_arrive(fb);
                 }
@@ -543,9 +545,11 @@ __global__ void __launch_bounds__(DecodeCfg<D, F8, MULTI>::THREADS, 1)
     // ==================================================================== consumers
     const int c_id = warp;  // 0 .. NC-1
     const int g = lane >> 2, q4 = lane & 3;
-    const float scale_log2 = a.scale_log2;
-    // E4M3 cache: acc holds O / vref, vref the largest V scale of the
-    // segment's blocks seen so far (0 before the first)
+    // E4M3 cache: times the segment's K scale (per-KV-head scales)
+    float scale_log2 = a.scale_log2;
+    // E4M3 cache: acc holds O / vref. Per-KV-head scales: vref is the
+    // segment's V scale; per-block scales: the largest V scale of the
+    // segment's blocks seen so far (0 before the first).
     float vref = 0.f;
     uint32_t qb[NKK][2];
     float acc[NKK][4];
@@ -569,7 +573,12 @@ __global__ void __launch_bounds__(DecodeCfg<D, F8, MULTI>::THREADS, 1)
                 qb[kk][0] = pack_f16x2(bf16_lo(v.x), bf16_hi(v.x));
                 qb[kk][1] = pack_f16x2(bf16_lo(v.y), bf16_hi(v.y));
             }
-            vref = 0.f;
+            if constexpr (BSC) {
+                vref = 0.f;
+            } else {
+                scale_log2 = a.scale_log2 * __ldg(a.k_scale + kvh);
+                vref = __ldg(a.v_scale + kvh);
+            }
         } else {
 #pragma unroll
             for (int kk = 0; kk < NKK; ++kk) {
@@ -700,17 +709,21 @@ __global__ void __launch_bounds__(DecodeCfg<D, F8, MULTI>::THREADS, 1)
         const uint32_t s0a = base + (ka % S) * C::STAGE;
         const uint32_t s1a = base + (kb_ % S) * C::STAGE;
         float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
-        float sla = scale_log2, slb = scale_log2;  // times the blocks' K scales (E4M3)
-        float ra = 1.f, rb = 1.f, vr = 1.f;        // V scale ratios (E4M3), warp-uniform
+        float sla = scale_log2, slb = scale_log2;  // per-block scales: times the blocks' K scales
+        float ra = 1.f, rb = 1.f, vr = 1.f;        // per-block scales: V scale ratios, warp-uniform
         if constexpr (F8) {
             if (nva > 0) qk8(s0a, s0);
             if (nvb > 0) qk8(s1a, s1);
+        } else {
+            if (nva > 0) qk(s0a, s0);
+            if (nvb > 0) qk(s1a, s1);
+        }
+        if constexpr (PSC) {
             // Each block's V codes stand for decode(code) * sv. acc is kept in
             // units of vref = the largest sv so far: a block with a larger sv
             // rescales acc by vref / sv first; a block's P enters the PV
-            // product times sv / vref (1 for per-KV-head scales; a power of
-            // two for per-block ones, so the f16 product is exact down to
-            // the f16 subnormal range).
+            // product times sv / vref (a power of two, so the f16 product is
+            // exact down to the f16 subnormal range).
             const float2 ca = iscale[ka % S], cb = iscale[kb_ % S];
             sla = scale_log2 * ca.x;
             slb = scale_log2 * cb.x;
@@ -723,9 +736,6 @@ __global__ void __launch_bounds__(DecodeCfg<D, F8, MULTI>::THREADS, 1)
             }
             if (nva > 0 && ca.y != vnew) ra = __fdiv_rn(ca.y, vnew);
             if (nvb > 0 && cb.y != vnew) rb = __fdiv_rn(cb.y, vnew);
-        } else {
-            if (nva > 0) qk(s0a, s0);
-            if (nvb > 0) qk(s1a, s1);
         }
         const float x0 = (g < nva) ? s0[0] * sla : -INFINITY;
         const float x1 = (g < nva) ? s0[1] * sla : -INFINITY;
@@ -761,7 +771,7 @@ __global__ void __launch_bounds__(DecodeCfg<D, F8, MULTI>::THREADS, 1)
         m0 = mn0;
         m1 = mn1;
         bool rescale = __any_sync(0xffffffffu, grow);
-        if constexpr (F8) {
+        if constexpr (PSC) {
             if (vr != 1.f) {  // acc into the units of the new vref (l keeps its own)
                 al0 *= vr;
                 al1 *= vr;
@@ -777,7 +787,7 @@ __global__ void __launch_bounds__(DecodeCfg<D, F8, MULTI>::THREADS, 1)
                 acc[mt][3] *= al1;
             }
         }
-        if constexpr (F8) {
+        if constexpr (PSC) {
             if (nva > 0) {
                 if (ra != 1.f) pv8(s0a + C::KT, scale_f16x2(p01, ra), scale_f16x2(p23, ra), nva);
                 else pv8(s0a + C::KT, p01, p23, nva);
@@ -786,6 +796,9 @@ __global__ void __launch_bounds__(DecodeCfg<D, F8, MULTI>::THREADS, 1)
                 if (rb != 1.f) pv8(s1a + C::KT, scale_f16x2(q01, rb), scale_f16x2(q23, rb), nvb);
                 else pv8(s1a + C::KT, q01, q23, nvb);
             }
+        } else if constexpr (F8) {
+            if (nva > 0) pv8(s0a + C::KT, p01, p23, nva);
+            if (nvb > 0) pv8(s1a + C::KT, q01, q23, nvb);
         } else {
             if (nva > 0) pv(s0a + C::KT, p01, p23, nva);
             if (nvb > 0) pv(s1a + C::KT, q01, q23, nvb);
@@ -1189,8 +1202,9 @@ cudaError_t geometry_t(DecodeGeometry *g) {
     const size_t smem = C::smem_bytes(kMaxBatch) < size_t(optin) ? C::smem_bytes(kMaxBatch) : size_t(optin);
     const size_t smem_m = CM::smem_bytes(kMaxBatch) < size_t(optin) ? CM::smem_bytes(kMaxBatch) : size_t(optin);
     if (smem < C::smem_bytes(1)) return cudaErrorInvalidConfiguration;
+    // the second kernel: multi-token rows (bf16), or per-block scales (E4M3)
     void (*kernels[2])(CUtensorMap, CUtensorMap, DecodeArgs) = {decode_kernel<D, F8, false>,
-                                                                decode_kernel<D, F8, !F8>};
+                                                                decode_kernel<D, F8, !F8, F8>};
     const size_t limits[2] = {smem, F8 ? smem : smem_m};
     for (int i = 0; i < 2; ++i) {
         e = cudaFuncSetAttribute(kernels[i], cudaFuncAttributeMaxDynamicSharedMemorySize, int(limits[i]));
@@ -1210,7 +1224,7 @@ cudaError_t geometry_t(DecodeGeometry *g) {
     return cudaSuccess;
 }
 
-template <int D, bool SPARSE, bool F8, bool MULTI = false>
+template <int D, bool SPARSE, bool F8, bool MULTI = false, bool BSC = false>
 cudaError_t launch_t(const CUtensorMap &tm_k, const CUtensorMap &tm_v, const DecodeArgs &a,
                      cudaStream_t stream, int max_ctas = 0) {
     using C = DecodeCfg<D, F8, MULTI>;
@@ -1257,10 +1271,10 @@ cudaError_t launch_t(const CUtensorMap &tm_k, const CUtensorMap &tm_v, const Dec
         const size_t fsmem = C::smem_bytes_sel(a.B, int(cap));
         if (cap > (int64_t(1) << 20) || fsmem > geo.smem) return cudaErrorInvalidConfiguration;
         f.nsel_cap = int(cap);
-        return launch_pdl(decode_kernel<D, F8, MULTI>, dim3(grid), dim3(C::THREADS), fsmem, stream, tm_k, tm_v,
+        return launch_pdl(decode_kernel<D, F8, MULTI, BSC>, dim3(grid), dim3(C::THREADS), fsmem, stream, tm_k, tm_v,
                           f);
     }
-    return launch_pdl(decode_kernel<D, F8, MULTI>, dim3(grid), dim3(C::THREADS), smem, stream,
+    return launch_pdl(decode_kernel<D, F8, MULTI, BSC>, dim3(grid), dim3(C::THREADS), smem, stream,
                       tm_k, tm_v, a);
 }
 
@@ -1314,6 +1328,9 @@ cudaError_t launch_decode(const CUtensorMap &tm_k, const CUtensorMap &tm_v, cons
     }
     if (fp8) {
         if (head_dim != 128) return cudaErrorInvalidValue;
+        if (a.scale_per_block)
+            return sparse ? launch_t<128, true, true, false, true>(tm_k, tm_v, a, stream, max_ctas)
+                          : launch_t<128, false, true, false, true>(tm_k, tm_v, a, stream);
         return sparse ? launch_t<128, true, true>(tm_k, tm_v, a, stream, max_ctas)
                       : launch_t<128, false, true>(tm_k, tm_v, a, stream);
     }

@@ -116,21 +116,31 @@ __global__ void __launch_bounds__(kScoreThreads, 4) quest_score_kernel(
                 P[cc] = 0.f;
                 N[cc] = 0.f;
             }
-            for (int gg = 0; gg < G; ++gg) {
-                const uint16_t *qr = q + (int64_t(b) * Hq + int64_t(kvh) * G + gg) * D + lane * C;
-                uint32_t qw[CW];
-                if (C == 4) {
-                    const uint2 v2 = __ldg(reinterpret_cast<const uint2 *>(qr));
-                    qw[0] = v2.x;
-                    qw[CW - 1] = v2.y;
-                } else {
-                    qw[0] = __ldg(reinterpret_cast<const uint32_t *>(qr));
+            // the group's query rows, QB loads in flight before their sums
+            constexpr int QB = 4;
+            for (int g0 = 0; g0 < G; g0 += QB) {
+                uint32_t qw[QB][CW];
+#pragma unroll
+                for (int i = 0; i < QB; ++i) {
+                    if (g0 + i >= G) break;
+                    const uint16_t *qr = q + (int64_t(b) * Hq + int64_t(kvh) * G + g0 + i) * D + lane * C;
+                    if (C == 4) {
+                        const uint2 v2 = __ldg(reinterpret_cast<const uint2 *>(qr));
+                        qw[i][0] = v2.x;
+                        qw[i][CW - 1] = v2.y;
+                    } else {
+                        qw[i][0] = __ldg(reinterpret_cast<const uint32_t *>(qr));
+                    }
                 }
 #pragma unroll
-                for (int cc = 0; cc < C; ++cc) {
-                    const float v = (cc & 1) ? bf16_hi(qw[cc >> 1]) : bf16_lo(qw[cc >> 1]);
-                    P[cc] = __fadd_rn(P[cc], v > 0.f ? v : 0.f);
-                    N[cc] = __fadd_rn(N[cc], v < 0.f ? v : 0.f);
+                for (int i = 0; i < QB; ++i) {
+                    if (g0 + i >= G) break;
+#pragma unroll
+                    for (int cc = 0; cc < C; ++cc) {
+                        const float v = (cc & 1) ? bf16_hi(qw[i][cc >> 1]) : bf16_lo(qw[i][cc >> 1]);
+                        P[cc] = __fadd_rn(P[cc], v > 0.f ? v : 0.f);
+                        N[cc] = __fadd_rn(N[cc], v < 0.f ? v : 0.f);
+                    }
                 }
             }
         }
