@@ -320,6 +320,8 @@ class Step:
                                                    self.k_scale, self.v_scale, self.bt, self.ctx,
                                                    self.sel, w.scale, workspace=self.ws_sparse),
                 self.quest(),
+                None,
+                None,
             ]
         if self.kv == "fp8_block":
             return [
@@ -333,13 +335,24 @@ class Step:
                                                          self.k_scale, self.v_scale, self.bt, self.ctx,
                                                          self.sel, w.scale, workspace=self.ws_sparse),
                 self.quest(),
+                None,
+                None,
             ]
         if self.qlen > 1:
             dense = lambda: pg.pa_decode_multi(self.out_multi, self.q_multi, self.kc, self.vc, self.bt,
                                                self.cu_q, self.ctx, w.scale, workspace=self.ws_multi)
+            dense_w = quest_w = None
         else:
             dense = lambda: pg.pa_decode(self.out, self.q, self.kc, self.vc, self.bt, self.ctx, w.scale,
                                          workspace=self.ws)
+            # the step's write folded into the first launch (the same results)
+            dense_w = lambda: pg.pa_reshape_and_decode(self.out, self.q, self.key, self.value, self.slots, self.kc,
+                                                       self.vc, self.bt, self.ctx, w.scale, kmin=self.kmin,
+                                                       kmax=self.kmax, workspace=self.ws)
+            quest_w = lambda: pg.quest_reshape_and_decode(self.out_sparse, self.sel, self.q, self.key, self.value,
+                                                          self.slots, self.kmin, self.kmax, self.kc, self.vc,
+                                                          self.bt, self.ctx, w.topk, w.scale,
+                                                          workspace=self.ws_quest)
         return [
             lambda: pg.quest_reshape_and_cache(self.key, self.value, self.kc, self.vc, self.kmin,
                                                self.kmax, self.slots),
@@ -349,15 +362,20 @@ class Step:
             lambda: pg.quest_sparse_decode(self.out_sparse, self.q, self.kc, self.vc, self.bt,
                                            self.ctx, self.sel, w.scale, workspace=self.ws_sparse),
             self.quest(),
+            dense_w,
+            quest_w,
         ]
 
 
-CALL_NAMES = ["write", "dense", "select", "sparse", "quest"]
+# dense_w / quest_w: the dense and the Quest step with the write folded into
+# the first launch (pa_reshape_and_decode, quest_reshape_and_decode; bf16
+# cache, one query row); None where that form does not exist
+CALL_NAMES = ["write", "dense", "select", "sparse", "quest", "dense_w", "quest_w"]
 # Order of the per-call pass: the separate selection and sparse decode (for
 # reference), then the fused Quest path and the dense decode back to back
 # (the decode launches are one kernel binary, so the second runs on code the
 # first left in the SMs' instruction caches).
-PASS_B_ORDER = [0, 2, 3, 4, 1]
+PASS_B_ORDER = [0, 2, 3, 4, 1, 6, 5]
 # The step: write, Quest path (selection 2 launches + sparse decode 1 beside
 # the dense decode; quest_decode's 2 with --serial), dense decode
 STEP_LAUNCHES = 5
@@ -600,6 +618,7 @@ def measure(torch, pg, w, dev, args, flush, pgroup):
     from paged_gqa_decode_reshape_gb300 import ledger
     step = Step(w, dev, args.kv, args.qlen)
     calls = [step.calls()[k] for k in PASS_B_ORDER]  # launch order of the per-call pass
+    present = [c is not None for c in step.calls()]  # in CALL_NAMES order
     stream = torch.cuda.current_stream(dev)
     run_step = step_runner(torch, step, args.serial)
     K = args.steps
@@ -650,7 +669,8 @@ def measure(torch, pg, w, dev, args, flush, pgroup):
         head_start()
         evb[i][0].record(stream)
         for j, c in enumerate(calls):
-            c()
+            if c is not None:
+                c()
             evb[i][j + 1].record(stream)
     torch.cuda.synchronize(dev)
     per_call = np.array([[evb[i][j].elapsed_time(evb[i][j + 1]) for j in range(len(calls))]
@@ -693,7 +713,7 @@ def measure(torch, pg, w, dev, args, flush, pgroup):
         e2e_ms.append(e0.elapsed_time(e1))
     del graph, step
     torch.cuda.synchronize(dev)
-    return dict(nb=nb, step_ms=step_ms, per_call=per_call, graph_ms=graph_ms, e2e_ms=e2e_ms,
+    return dict(nb=nb, step_ms=step_ms, per_call=per_call, present=present, graph_ms=graph_ms, e2e_ms=e2e_ms,
                 h2d=int(h_in.numel()), d2h=int(h_out.numel()), clocks=clocks, wall=wall)
 
 
@@ -701,10 +721,14 @@ def call_summary(m, peak: float) -> dict:
     """Per-call medians of pass B, their GB/s on the algorithmic bytes, and
     the fraction of the measured copy peak and of the nominal ~8 TB/s."""
     nb = m["nb"]
-    call_bytes = [nb.reshape + nb.meta, nb.dense, nb.select, nb.sparse, nb.select + nb.sparse]
+    wb = nb.reshape + nb.meta
+    call_bytes = [wb, nb.dense, nb.select, nb.sparse, nb.select + nb.sparse, wb + nb.dense,
+                  wb + nb.select + nb.sparse]
     med = np.median(m["per_call"], axis=0)
     out = {}
-    for n, ms, b in zip(CALL_NAMES, med, call_bytes):
+    for n, ms, b, here in zip(CALL_NAMES, med, call_bytes, m["present"]):
+        if not here:
+            continue
         gbs = b / (ms * 1e-3) / 1e9
         out[n] = {"us": round(float(ms) * 1e3, 2), "us_min": round(float(m["per_call"][:, CALL_NAMES.index(n)].min())
                                                                   * 1e3, 2),
@@ -719,12 +743,16 @@ def point_summary(m, peak: float, world: int) -> dict:
     (write + quest_decode; and write + selection + sparse decode, unfused),
     and the whole step of pass A."""
     calls = call_summary(m, peak)
-    dense_us = calls["write"]["us"] + calls["dense"]["us"]
-    quest_us = calls["write"]["us"] + calls["quest"]["us"]
+    dense_sep = calls["write"]["us"] + calls["dense"]["us"]
+    quest_sep = calls["write"]["us"] + calls["quest"]["us"]
+    dense_us = calls["dense_w"]["us"] if "dense_w" in calls else dense_sep
+    quest_us = calls["quest_w"]["us"] if "quest_w" in calls else quest_sep
     return {
         "dense_step_us": round(dense_us, 2), "quest_step_us": round(quest_us, 2),
+        "dense_step_separate_write_us": round(dense_sep, 2), "quest_step_separate_write_us": round(quest_sep, 2),
         "quest_step_unfused_us": round(calls["write"]["us"] + calls["select"]["us"] + calls["sparse"]["us"], 2),
         "dense_decode": calls["dense"], "quest_decode": calls["quest"], "sparse_decode": calls["sparse"],
+        **{k: calls[k] for k in ("dense_w", "quest_w") if k in calls},
         "select": calls["select"], "write": calls["write"],
         "whole_step_us": stats_ms(np.asarray(m["step_ms"]) * 1e3),
         "whole_step_GBps": round(job_throughput(world, m["nb"].total, float(np.median(m["step_ms"]))), 1),
@@ -817,13 +845,19 @@ def main():
         },
         "breakdown": {n: point[k] for n, k in (("write", "write"), ("dense", "dense_decode"),
                                                ("select", "select"), ("sparse", "sparse_decode"),
-                                               ("quest", "quest_decode"))},
+                                               ("quest", "quest_decode"), ("dense_w", "dense_w"),
+                                               ("quest_w", "quest_w")) if k in point},
         "breakdown_steps": K,
         "dense_us_per_step": point["dense_step_us"],
         "quest_us_per_step": point["quest_step_us"],
         "quest_us_per_step_unfused": point["quest_step_unfused_us"],
-        "dense_step": "write + pa_decode",
-        "quest_step": "write + quest_decode (scores; then top-K and sparse decode in one launch)",
+        "dense_step": ("pa_reshape_and_decode (write folded into the decode launch, 1 launch)"
+                       if "dense_w" in point else "write + pa_decode"),
+        "quest_step": ("quest_reshape_and_decode (write folded into the score launch; then top-K and "
+                       "sparse decode in one launch: 2 launches)" if "quest_w" in point else
+                       "write + quest_decode (scores; then top-K and sparse decode in one launch)"),
+        "dense_step_separate_write_us": point["dense_step_separate_write_us"],
+        "quest_step_separate_write_us": point["quest_step_separate_write_us"],
         "quest_step_unfused": "write + quest_select_topk + quest_sparse_decode",
         "tokens_per_s": {"dense": round(world * w.B / (point["dense_step_us"] * 1e-6), 1),
                          "quest": round(world * w.B / (point["quest_step_us"] * 1e-6), 1)},

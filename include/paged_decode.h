@@ -315,6 +315,53 @@ PA_API int pa_decode_multi(pa_bf16 *out, const pa_bf16 *query,
                     int head_dim, int block_size, int64_t num_blocks, float scale,
                     void *workspace, size_t workspace_bytes, void *stream);
 
+/* ------------------------------- the step's write folded into decode ----
+ * A decode step writes each sequence's new token into the cache ([P1]
+ * "ReshapeAndCache", and the Quest metadata update) and then attends over
+ * the cache including it. These two calls fold that write into the step's
+ * first launch, for the decode case: one new token per sequence, at its
+ * position ctx_b - 1.
+ *
+ * key, value: [batch][Hkv][D] bf16, the new token of each sequence;
+ * slot_mapping: [batch] int64. Token b is written at slot_mapping[b] when
+ * that is the slot of position ctx_b - 1 of sequence b, i.e.
+ *     block_tables[b][(ctx_b - 1) / BS] * BS + (ctx_b - 1) % BS
+ * with that table entry inside the pool. Any other slot (negative, past the
+ * pool, or another position) is not written. pa_reshape_and_cache writes any
+ * in-pool slot instead. The slots of one call must be distinct, and no other
+ * kernel may touch the written blocks while the call runs. With those slots,
+ * the results are byte for byte those of the separate calls (the write, then
+ * pa_decode or quest_decode): caches, metadata, selection and outputs.
+ * bf16 cache only; 16-byte aligned key and value. Workspaces and errors as
+ * pa_decode / quest_decode. */
+
+/* ReshapeAndCache of the step's tokens, then pa_decode, in one launch: the
+ * CTA that reads a sequence's last block writes the new token's slice of
+ * its KV head into it first. kmin / kmax: both null, or the Quest metadata,
+ * updated as quest_update_meta does (reset when the token lands at offset 0
+ * of its block, else merged). */
+PA_API int pa_reshape_and_decode(pa_bf16 *out, const pa_bf16 *query, const pa_bf16 *key,
+                                 const pa_bf16 *value, const int64_t *slot_mapping,
+                                 pa_bf16 *key_cache, pa_bf16 *value_cache, pa_bf16 *kmin,
+                                 pa_bf16 *kmax, const int32_t *block_tables, int max_blocks_per_seq,
+                                 const int32_t *context_lens, int batch, int num_q_heads,
+                                 int num_kv_heads, int head_dim, int block_size, int64_t num_blocks,
+                                 float scale, void *workspace, size_t workspace_bytes, void *stream);
+
+/* quest_reshape_and_cache of the step's tokens, then quest_decode, in two
+ * launches: the score launch's warp that scores a sequence's last block
+ * writes the new token's slice of its KV head and updates the block's
+ * metadata before scoring it; then the fused top-K and sparse decode. */
+PA_API int quest_reshape_and_decode(pa_bf16 *out, int32_t *selected, const pa_bf16 *query,
+                                    const pa_bf16 *key, const pa_bf16 *value,
+                                    const int64_t *slot_mapping, pa_bf16 *kmin, pa_bf16 *kmax,
+                                    pa_bf16 *key_cache, pa_bf16 *value_cache,
+                                    const int32_t *block_tables, int max_blocks_per_seq,
+                                    const int32_t *context_lens, int batch, int num_q_heads,
+                                    int num_kv_heads, int head_dim, int block_size,
+                                    int64_t num_blocks, int topk, float scale, int max_ctas,
+                                    void *workspace, size_t workspace_bytes, void *stream);
+
 /* ---------------------------------------------------- 8-bit KV cache ----
  * The same path over a KV cache stored in 8 bits per element, which halves
  * the bytes decode attention reads ([P2] 2.5 and 3.1: long-context serving is

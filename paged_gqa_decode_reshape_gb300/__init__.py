@@ -43,6 +43,7 @@ __all__ = [
     "quest_sparse_decode_fp8_budget",
     "pa_reshape_and_cache_fp8_block", "quest_reshape_and_cache_fp8_block", "quest_select_topk_fp8_block",
     "pa_decode_fp8_block", "quest_sparse_decode_fp8_block", "quest_decode_fp8_block",
+    "pa_reshape_and_decode", "quest_reshape_and_decode",
     "pa_workspace_status", "pa_check_metadata", "Workspace",
 ]
 
@@ -135,6 +136,12 @@ def load_library(path: Optional[str] = None):
         L.quest_sparse_decode_fp8_budget.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, vp, vp, i32, i32, i32,
                                                      i32, i32, i32, i64, f32, i32, vp, sz, vp]
         L.quest_sparse_decode_fp8_budget.restype = i32
+        L.pa_reshape_and_decode.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, vp, i32, i32, i32, i32,
+                                            i32, i64, f32, vp, sz, vp]
+        L.pa_reshape_and_decode.restype = i32
+        L.quest_reshape_and_decode.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, vp, i32, i32, i32,
+                                               i32, i32, i64, i32, f32, i32, vp, sz, vp]
+        L.quest_reshape_and_decode.restype = i32
         L.pa_reshape_and_cache_fp8_block.argtypes = [vp, vp, vp, vp, vp, i64, vp, vp, i32, i32, i32, i64, vp]
         L.pa_reshape_and_cache_fp8_block.restype = i32
         L.quest_reshape_and_cache_fp8_block.argtypes = [vp, vp, vp, vp, vp, vp, vp, i64, vp, vp, i32, i32,
@@ -887,3 +894,61 @@ def quest_decode_fp8_block(out: torch.Tensor, selected: torch.Tensor, query: tor
     return _quest_decode(L.quest_decode_fp8_block, "quest_decode_fp8_block", out, selected, query, kmin, kmax,
                          key_cache, value_cache, block_tables, context_lens, topk, scale, max_ctas, workspace,
                          (_ptr(k_bscale), _ptr(v_bscale)), checks)
+
+
+# ------------------------------------- the step's write folded into decode
+
+
+def _step_tokens(key, value, slot_mapping, B, Hkv, D, dev):
+    _need(key, "key", torch.bfloat16, 3, dev)
+    _need(value, "value", torch.bfloat16, 3, dev)
+    _need(slot_mapping, "slot_mapping", torch.int64, 1, dev)
+    if tuple(key.shape) != (B, Hkv, D) or value.shape != key.shape or slot_mapping.shape[0] != B:
+        raise ValueError("key / value must be [B, Hkv, D] and slot_mapping [B]: one new token per sequence")
+
+
+def pa_reshape_and_decode(out: torch.Tensor, query: torch.Tensor, key: torch.Tensor, value: torch.Tensor,
+                          slot_mapping: torch.Tensor, key_cache: torch.Tensor, value_cache: torch.Tensor,
+                          block_tables: torch.Tensor, context_lens: torch.Tensor, scale: float,
+                          kmin: Optional[torch.Tensor] = None, kmax: Optional[torch.Tensor] = None,
+                          workspace: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """Each sequence's new token written at position ctx_b - 1 (when slot_mapping[b] is that
+    slot; also into kmin / kmax when given), then dense decode, in one launch."""
+    L = load_library()
+    dev, B, Hq, Hkv, D, BS, NB, MBS = _attention_checks(out, query, key_cache, value_cache, block_tables,
+                                                        context_lens)
+    _step_tokens(key, value, slot_mapping, B, Hkv, D, dev)
+    if (kmin is None) != (kmax is None):
+        raise ValueError("kmin and kmax go together")
+    if kmin is not None:
+        for t, n in ((kmin, "kmin"), (kmax, "kmax")):
+            _need(t, n, torch.bfloat16, 3, dev)
+            if tuple(t.shape) != (NB, Hkv, D):
+                raise ValueError("kmin / kmax must be [NB, Hkv, D]")
+    need = pa_decode_workspace_size(B, Hq, Hkv, D)
+    ws = workspace if workspace is not None else _default_ws.get(dev, need)
+    _check("pa_reshape_and_decode",
+           L.pa_reshape_and_decode(_ptr(out), _ptr(query), _ptr(key), _ptr(value), _ptr(slot_mapping),
+                                   _ptr(key_cache), _ptr(value_cache), _ptr(kmin), _ptr(kmax), _ptr(block_tables),
+                                   MBS, _ptr(context_lens), B, Hq, Hkv, D, BS, NB, float(scale), _ptr(ws),
+                                   ws.numel() * ws.element_size(), _stream(dev)))
+    return out
+
+
+def quest_reshape_and_decode(out: torch.Tensor, selected: torch.Tensor, query: torch.Tensor, key: torch.Tensor,
+                             value: torch.Tensor, slot_mapping: torch.Tensor, kmin: torch.Tensor,
+                             kmax: torch.Tensor, key_cache: torch.Tensor, value_cache: torch.Tensor,
+                             block_tables: torch.Tensor, context_lens: torch.Tensor, topk: int, scale: float,
+                             max_ctas: int = 0, workspace: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """The step's write and metadata update folded into the score launch, then the
+    fused top-K and sparse decode: quest_reshape_and_cache + quest_decode in two launches."""
+    L = load_library()
+    checks = _attention_checks(out, query, key_cache, value_cache, block_tables, context_lens)
+    dev, B, Hq, Hkv, D = checks[:5]
+    _step_tokens(key, value, slot_mapping, B, Hkv, D, dev)
+    _need(kmin, "kmin", torch.bfloat16, 3, dev)
+    _need(kmax, "kmax", torch.bfloat16, 3, dev)
+    fn = lambda *a: L.quest_reshape_and_decode(a[0], a[1], a[2], _ptr(key), _ptr(value), _ptr(slot_mapping),
+                                               *a[3:])
+    return _quest_decode(fn, "quest_reshape_and_decode", out, selected, query, kmin, kmax, key_cache,
+                         value_cache, block_tables, context_lens, topk, scale, max_ctas, workspace, (), checks)

@@ -118,7 +118,8 @@ int run_decode(pa_bf16 *out, const pa_bf16 *query, const void *key_cache, const 
                float scale, void *workspace, size_t workspace_bytes, void *stream, bool sparse,
                const float *k_scale = nullptr, const float *v_scale = nullptr, bool fp8 = false,
                const int32_t *cu_q = nullptr, int nseq = 0, int max_ctas = 0,
-               const float *scores = nullptr, int32_t *sel_out = nullptr, bool bscale = false) {
+               const float *scores = nullptr, int32_t *sel_out = nullptr, bool bscale = false,
+               const ScoreWrite *sw = nullptr) {
     int rc = check_attention_args(out, query, key_cache, value_cache, block_tables, MBS,
                                   context_lens, B, Hq, Hkv, D, BS, NB, scale, workspace);
     if (rc != PA_OK) return rc;
@@ -154,6 +155,13 @@ int run_decode(pa_bf16 *out, const pa_bf16 *query, const void *key_cache, const 
     a.status = w.status;
     a.scores = scores;
     a.sel_out = sel_out;
+    a.new_k = sw ? sw->key : nullptr;  // dense decode with the step's write
+    a.new_v = sw ? sw->value : nullptr;
+    a.new_slots = sw ? sw->slots : nullptr;
+    a.kc_w = sw ? sw->kc : nullptr;
+    a.vc_w = sw ? sw->vc : nullptr;
+    a.kmin_w = sw ? sw->kmin : nullptr;
+    a.kmax_w = sw ? sw->kmax : nullptr;
     a.nsel_cap = 0;
     a.wait_ns = g_wait_ns.load(std::memory_order_relaxed);
     a.stop_item = g_stop_item.load(std::memory_order_relaxed);
@@ -347,7 +355,7 @@ int run_quest_decode(pa_bf16 *out, int32_t *selected, const pa_bf16 *query, cons
                      const float *k_scale, const float *v_scale, const int32_t *block_tables, int MBS,
                      const int32_t *context_lens, int B, int Hq, int Hkv, int D, int BS, int64_t NB,
                      int topk, float scale, int max_ctas, void *workspace, size_t workspace_bytes,
-                     void *stream, bool fp8, bool bscale = false) {
+                     void *stream, bool fp8, bool bscale = false, const ScoreWrite *sw = nullptr) {
     if (!selected || !kmin || !kmax || !workspace || max_ctas < 0) return PA_ERR_INVALID_ARG;
     int rc = check_attention_args(out, query, key_cache, value_cache, block_tables, MBS, context_lens, B, Hq,
                                   Hkv, D, BS, NB, scale, workspace);
@@ -368,14 +376,15 @@ int run_quest_decode(pa_bf16 *out, int32_t *selected, const pa_bf16 *query, cons
         // top-Ks would run one after another inside it; the top-K kernel
         // (one CTA per segment) runs them all at once instead.
         e = launch_quest_select(selected, scores, query, kmin, kmax, block_tables, MBS, context_lens, B, Hq, Hkv,
-                                D, BS, NB, topk, static_cast<cudaStream_t>(stream), fp8, bscale ? k_scale : nullptr);
+                                D, BS, NB, topk, static_cast<cudaStream_t>(stream), fp8, bscale ? k_scale : nullptr,
+                                sw);
         if (e != cudaSuccess) return cuda_fail(e);
         return run_decode(out, query, key_cache, value_cache, block_tables, MBS, context_lens, selected, topk, B,
                           Hq, Hkv, D, BS, NB, scale, workspace, dec, stream, true, k_scale, v_scale, fp8, nullptr,
                           0, max_ctas, nullptr, nullptr, bscale);
     }
     e = launch_quest_scores(scores, query, kmin, kmax, block_tables, MBS, context_lens, B, Hq, Hkv, D, BS, NB,
-                            static_cast<cudaStream_t>(stream), fp8, bscale ? k_scale : nullptr);
+                            static_cast<cudaStream_t>(stream), fp8, bscale ? k_scale : nullptr, sw);
     if (e != cudaSuccess) return cuda_fail(e);
     return run_decode(out, query, key_cache, value_cache, block_tables, MBS, context_lens, nullptr, topk, B,
                       Hq, Hkv, D, BS, NB, scale, workspace, dec, stream, true, k_scale, v_scale, fp8, nullptr, 0,
@@ -406,6 +415,48 @@ int quest_decode_fp8(pa_bf16 *out, int32_t *selected, const pa_bf16 *query, cons
                             block_tables, max_blocks_per_seq, context_lens, batch, num_q_heads, num_kv_heads,
                             head_dim, block_size, num_blocks, topk, scale, max_ctas, workspace, workspace_bytes,
                             stream, true);
+}
+
+/* ----------------------------------- the step's write folded into decode */
+
+namespace {
+int check_step_write(const pa_bf16 *key, const pa_bf16 *value, const int64_t *slot_mapping, int batch) {
+    if (!key || !value || !slot_mapping || batch <= 0) return PA_ERR_INVALID_ARG;
+    if (!aligned16(key) || !aligned16(value)) return PA_ERR_INVALID_ARG;
+    return PA_OK;
+}
+}  // namespace
+
+int pa_reshape_and_decode(pa_bf16 *out, const pa_bf16 *query, const pa_bf16 *key, const pa_bf16 *value,
+                          const int64_t *slot_mapping, pa_bf16 *key_cache, pa_bf16 *value_cache, pa_bf16 *kmin,
+                          pa_bf16 *kmax, const int32_t *block_tables, int max_blocks_per_seq,
+                          const int32_t *context_lens, int batch, int num_q_heads, int num_kv_heads, int head_dim,
+                          int block_size, int64_t num_blocks, float scale, void *workspace,
+                          size_t workspace_bytes, void *stream) {
+    int rc = check_step_write(key, value, slot_mapping, batch);
+    if (rc != PA_OK) return rc;
+    if ((kmin == nullptr) != (kmax == nullptr)) return PA_ERR_INVALID_ARG;
+    if (kmin && (!aligned16(kmin) || !aligned16(kmax))) return PA_ERR_INVALID_ARG;
+    const ScoreWrite sw{key, value, slot_mapping, key_cache, value_cache, kmin, kmax};
+    return run_decode(out, query, key_cache, value_cache, block_tables, max_blocks_per_seq, context_lens, nullptr,
+                      0, batch, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, scale, workspace,
+                      workspace_bytes, stream, false, nullptr, nullptr, false, nullptr, 0, 0, nullptr, nullptr,
+                      false, &sw);
+}
+
+int quest_reshape_and_decode(pa_bf16 *out, int32_t *selected, const pa_bf16 *query, const pa_bf16 *key,
+                             const pa_bf16 *value, const int64_t *slot_mapping, pa_bf16 *kmin, pa_bf16 *kmax,
+                             pa_bf16 *key_cache, pa_bf16 *value_cache, const int32_t *block_tables,
+                             int max_blocks_per_seq, const int32_t *context_lens, int batch, int num_q_heads,
+                             int num_kv_heads, int head_dim, int block_size, int64_t num_blocks, int topk,
+                             float scale, int max_ctas, void *workspace, size_t workspace_bytes, void *stream) {
+    int rc = check_step_write(key, value, slot_mapping, batch);
+    if (rc != PA_OK) return rc;
+    const ScoreWrite sw{key, value, slot_mapping, key_cache, value_cache, kmin, kmax};
+    return run_quest_decode(out, selected, query, kmin, kmax, key_cache, value_cache, nullptr, nullptr,
+                            block_tables, max_blocks_per_seq, context_lens, batch, num_q_heads, num_kv_heads,
+                            head_dim, block_size, num_blocks, topk, scale, max_ctas, workspace, workspace_bytes,
+                            stream, false, false, &sw);
 }
 
 int pa_workspace_status(const void *workspace, void *stream) {

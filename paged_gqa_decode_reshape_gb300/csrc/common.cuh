@@ -36,6 +36,13 @@ __device__ __forceinline__ void fence_proxy_async() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// Order this thread's earlier global-memory writes before later accesses of
+// the async (TMA) proxy to the same memory (a kernel that writes cache rows
+// and then loads them with TMA).
+__device__ __forceinline__ void fence_proxy_async_global() {
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
 // Make barrier initialisation visible to the async (TMA) proxy.
 __device__ __forceinline__ void fence_barrier_init() {
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -248,6 +255,20 @@ __device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v 
 // IEEE totalOrder key of a bf16 bit pattern (numeric order, -0 < +0).
 __device__ __forceinline__ uint32_t bf16_order_key(uint32_t h) {
     return (h & 0x8000u) ? (~h & 0xFFFFu) : (h | 0x8000u);
+}
+
+// Elementwise min / max (totalOrder) of two packed bf16 values with x.
+__device__ __forceinline__ void minmax_bf16x2(uint32_t &lo, uint32_t &hi, uint32_t x) {
+    uint32_t l = 0, h = 0;
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        const uint32_t xv = (x >> (16 * i)) & 0xffffu;
+        const uint32_t lv = (lo >> (16 * i)) & 0xffffu, hv = (hi >> (16 * i)) & 0xffffu;
+        l |= (bf16_order_key(xv) < bf16_order_key(lv) ? xv : lv) << (16 * i);
+        h |= (bf16_order_key(xv) > bf16_order_key(hv) ? xv : hv) << (16 * i);
+    }
+    lo = l;
+    hi = h;
 }
 
 // IEEE totalOrder key of an fp32 value.

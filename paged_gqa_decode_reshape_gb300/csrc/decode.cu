@@ -422,6 +422,39 @@ __global__ void __launch_bounds__(DecodeCfg<D, F8, MULTI>::THREADS, 1)
                 it.sv = __ldg(a.v_scale + si);
             }
         };
+        // dense decode with the step's write: sequence seg / Hkv's new token,
+        // KV head seg % Hkv, into physical block ph_w at offset (c_w - 1) % BS
+        // (when the token's slot is that one), by the whole warp: lanes
+        // [0, D/8) copy 16 bytes of K each and merge the metadata, lanes
+        // [D/8, D/4) copy V
+        auto write_new_token = [&](int seg_w, int ph_w, int c_w) {
+            if constexpr (!F8 && !MULTI) {
+                const int b = seg_w / Hkv, kvh = seg_w % Hkv, o = (c_w - 1) % BS;
+                if (__ldg(a.new_slots + b) != int64_t(ph_w) * BS + o) return;
+                constexpr int VPR = D / 8;  // 16-byte vectors per KV-head row
+                const int half = lane / VPR, e = lane % VPR;
+                if (half >= 2) return;
+                const int64_t src = (int64_t(b) * Hkv + kvh) * D;
+                const int64_t dst = ((int64_t(ph_w) * BS + o) * Hkv + kvh) * D;
+                const uint4 x = __ldg(reinterpret_cast<const uint4 *>((half ? a.new_v : a.new_k) + src) + e);
+                reinterpret_cast<uint4 *>((half ? a.vc_w : a.kc_w) + dst)[e] = x;
+                if (half == 0 && a.kmin_w) {  // reset at offset 0, else merge
+                    uint4 *mn = reinterpret_cast<uint4 *>(a.kmin_w + (int64_t(ph_w) * Hkv + kvh) * D) + e;
+                    uint4 *mx = reinterpret_cast<uint4 *>(a.kmax_w + (int64_t(ph_w) * Hkv + kvh) * D) + e;
+                    uint4 lo = x, hi = x;
+                    if (o != 0) {
+                        lo = *mn;
+                        hi = *mx;
+                        minmax_bf16x2(lo.x, hi.x, x.x);
+                        minmax_bf16x2(lo.y, hi.y, x.y);
+                        minmax_bf16x2(lo.z, hi.z, x.z);
+                        minmax_bf16x2(lo.w, hi.w, x.w);
+                    }
+                    *mn = lo;
+                    *mx = hi;
+                }
+            }
+        };
         const uint64_t policy = l2_policy_evict_first();
         if (SPARSE && a.scores) fence_proxy_async();  // the ring held the top-K scratch
         Win wa = stage_c(0), wb = stage_c(32);
@@ -496,6 +529,24 @@ __global__ void __launch_bounds__(DecodeCfg<D, F8, MULTI>::THREADS, 1)
             }
             ok = __shfl_sync(0xffffffffu, ok, lane - part);
             __syncwarp();
+            if constexpr (!F8 && !MULTI) {
+                // with the step's write: a segment's last block gets the
+                // sequence's new token before its copy is issued (this CTA is
+                // the only reader of that block in the call)
+                if (!SPARSE && a.new_k) {
+                    unsigned wm = __ballot_sync(0xffffffffu, part == 0 && live && ok && nv > 0 && j == nblk - 1);
+                    if (wm) {
+                        while (wm) {
+                            const int src = __ffs(wm) - 1;
+                            wm &= wm - 1;
+                            write_new_token(__shfl_sync(0xffffffffu, seg, src), __shfl_sync(0xffffffffu, ph, src),
+                                            __shfl_sync(0xffffffffu, c, src));
+                        }
+                        fence_proxy_async_global();  // the copies below read what was written
+                        __syncwarp();
+                    }
+                }
+            }
             if (live && ok && nv > 0 && part < PARTS) {
                 if constexpr (F8) {
                     // K: one [16 tokens x 128 dims] byte box (tensor map); V:

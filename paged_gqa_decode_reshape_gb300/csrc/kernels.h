@@ -37,6 +37,13 @@ struct DecodeArgs {
                                 // the top-K of its segments itself (else null: selection in sel)
     int32_t *sel_out;           // fused Quest decode: [B][Hkv][topk] selection written out
     int nsel_cap;               // fused Quest decode: capacity of the CTA's selection array
+    // dense decode with the step's write (bf16 cache, one query row): token b's
+    // K and V rows ([B][Hkv][D]) go to slot new_slots[b] when that is the
+    // slot of position ctx_b - 1 of sequence b; the CTA that reads the block
+    // writes its KV head's slice first (and the metadata when kmin_w is set)
+    const uint16_t *new_k, *new_v;
+    const int64_t *new_slots;
+    uint16_t *kc_w, *vc_w, *kmin_w, *kmax_w;
     uint64_t wait_ns;           // limit of every bounded wait inside the kernel (ns)
     int stop_item;              // the producer stops issuing at this item of its CTA's range
                                 // (failure tests only; INT_MAX otherwise)
@@ -97,16 +104,28 @@ cudaError_t launch_write_fp8_block(uint8_t *kc, uint8_t *vc, uint8_t *kmin, uint
                                    const int64_t *slots, int64_t T, int Hkv, int D, int BS, int64_t NB,
                                    cudaStream_t stream);
 
+// The step's write folded into the score launch (bf16 cache): the warp that
+// scores the chunk holding sequence b's block of position ctx_b - 1 writes
+// token b's KV-head slice there (when slots[b] is that slot) and updates the
+// block's metadata before scoring it.
+struct ScoreWrite {
+    const uint16_t *key, *value;  // [B][Hkv][D] bf16
+    const int64_t *slots;         // [B]
+    uint16_t *kc, *vc;            // the caches
+    uint16_t *kmin, *kmax;        // the metadata (the score kernel's kmin / kmax)
+};
+
 // block scores only (the first launch of the fused Quest decode)
 // k_bscale: per-block K scales [NB][Hkv] of an E4M3 cache (else null)
 cudaError_t launch_quest_scores(float *scores, const uint16_t *q, const void *kmin, const void *kmax,
                                 const int32_t *bt, int MBS, const int32_t *ctx, int B, int Hq, int Hkv, int D,
                                 int BS, int64_t NB, cudaStream_t stream, bool fp8 = false,
-                                const float *k_bscale = nullptr);
+                                const float *k_bscale = nullptr, const ScoreWrite *write = nullptr);
 // kmin / kmax: bf16 metadata, or E4M3 codes when fp8 (head_dim 128)
 cudaError_t launch_quest_select(int32_t *sel, float *scores, const uint16_t *q, const void *kmin,
                                 const void *kmax, const int32_t *bt, int MBS, const int32_t *ctx,
                                 int B, int Hq, int Hkv, int D, int BS, int64_t NB, int topk,
-                                cudaStream_t stream, bool fp8 = false, const float *k_bscale = nullptr);
+                                cudaStream_t stream, bool fp8 = false, const float *k_bscale = nullptr,
+                                const ScoreWrite *write = nullptr);
 
 }  // namespace pa

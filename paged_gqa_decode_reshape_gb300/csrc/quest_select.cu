@@ -46,14 +46,21 @@ constexpr int kScoreThreads = 256;
 // the score is the same fp32 expression of the decoded values. With
 // per-block scales (kbs [NB][Hkv], else null) the block's score is then
 // multiplied by its K scale (one fp32 product, exact for a power of two).
+//
+// With the step's write (bf16, wr.key not null): the warp whose chunk holds
+// block (ctx_b - 1) / BS of sequence b writes token b's KV-head slice into
+// the cache when wr.slots[b] is the slot of position ctx_b - 1, and updates
+// that block's metadata (reset at offset 0, else merged), before it loads
+// the chunk's metadata; the loads then see the update (same lane, same
+// address, no read-only cache path).
 template <int D, bool F8>
 __global__ void __launch_bounds__(kScoreThreads, 4) quest_score_kernel(
-    float *__restrict__ scores, const uint16_t *__restrict__ q, const void *__restrict__ kmin_v,
-    const void *__restrict__ kmax_v, const float *__restrict__ kbs, const int32_t *__restrict__ bt,
-    int MBS, const int32_t *__restrict__ ctx, int B, int Hq, int Hkv, int BS, int64_t NB) {
+    float *__restrict__ scores, const uint16_t *__restrict__ q, const void *kmin_v,
+    const void *kmax_v, const float *__restrict__ kbs, const int32_t *__restrict__ bt,
+    int MBS, const int32_t *__restrict__ ctx, int B, int Hq, int Hkv, int BS, int64_t NB, ScoreWrite wr) {
     static_assert(!F8 || D == 128, "E4M3 metadata: head_dim 128");
-    const uint16_t *__restrict__ kmin = static_cast<const uint16_t *>(kmin_v);
-    const uint16_t *__restrict__ kmax = static_cast<const uint16_t *>(kmax_v);
+    const uint16_t *kmin = static_cast<const uint16_t *>(kmin_v);
+    const uint16_t *kmax = static_cast<const uint16_t *>(kmax_v);
     constexpr int C = D / 32;  // dims per lane
     constexpr int CW = C / 2;  // 32-bit words per lane per row
     extern __shared__ int32_t pre[];  // [B+1] chunk prefix per KV head
@@ -144,6 +151,38 @@ __global__ void __launch_bounds__(kScoreThreads, 4) quest_score_kernel(
                 }
             }
         }
+        if constexpr (!F8) {
+            const int jl = nblk - 1;  // the block holding the new token
+            if (wr.key && jl >= j0 && jl < j0 + cnt) {
+                const int ph = __shfl_sync(0xffffffffu, ph_l, jl - j0);
+                const int o = (c - 1) % BS;
+                if (ph >= 0 && int64_t(ph) < NB && __ldg(wr.slots + b) == int64_t(ph) * BS + o) {
+                    const int64_t src = (int64_t(b) * Hkv + kvh) * D + lane * C;
+                    const int64_t dst = ((int64_t(ph) * BS + o) * Hkv + kvh) * D + lane * C;
+                    const int64_t m = (int64_t(ph) * Hkv + kvh) * D + lane * C;
+                    uint32_t kx[CW], vx[CW], lo[CW], hi[CW];
+#pragma unroll
+                    for (int i = 0; i < CW; ++i) {
+                        kx[i] = __ldg(reinterpret_cast<const uint32_t *>(wr.key + src) + i);
+                        vx[i] = __ldg(reinterpret_cast<const uint32_t *>(wr.value + src) + i);
+                        lo[i] = kx[i];
+                        hi[i] = kx[i];
+                        if (o != 0) {
+                            lo[i] = __ldcg(reinterpret_cast<const uint32_t *>(wr.kmin + m) + i);
+                            hi[i] = __ldcg(reinterpret_cast<const uint32_t *>(wr.kmax + m) + i);
+                            minmax_bf16x2(lo[i], hi[i], kx[i]);
+                        }
+                    }
+#pragma unroll
+                    for (int i = 0; i < CW; ++i) {
+                        reinterpret_cast<uint32_t *>(wr.kc + dst)[i] = kx[i];
+                        reinterpret_cast<uint32_t *>(wr.vc + dst)[i] = vx[i];
+                        reinterpret_cast<uint32_t *>(wr.kmin + m)[i] = lo[i];
+                        reinterpret_cast<uint32_t *>(wr.kmax + m)[i] = hi[i];
+                    }
+                }
+            }
+        }
         uint32_t mnv[kChunk][CW], mxv[kChunk][CW];
         bool ok[kChunk];
 #pragma unroll
@@ -155,15 +194,15 @@ __global__ void __launch_bounds__(kScoreThreads, 4) quest_score_kernel(
                 mnv[u][0] = __ldg(reinterpret_cast<const uint32_t *>(static_cast<const uint8_t *>(kmin_v) + off));
                 mxv[u][0] = __ldg(reinterpret_cast<const uint32_t *>(static_cast<const uint8_t *>(kmax_v) + off));
             } else if (C == 4) {
-                const uint2 a2 = __ldg(reinterpret_cast<const uint2 *>(kmin + off));
-                const uint2 b2 = __ldg(reinterpret_cast<const uint2 *>(kmax + off));
+                const uint2 a2 = __ldcg(reinterpret_cast<const uint2 *>(kmin + off));
+                const uint2 b2 = __ldcg(reinterpret_cast<const uint2 *>(kmax + off));
                 mnv[u][0] = a2.x;
                 mnv[u][CW - 1] = a2.y;
                 mxv[u][0] = b2.x;
                 mxv[u][CW - 1] = b2.y;
             } else {
-                mnv[u][0] = __ldg(reinterpret_cast<const uint32_t *>(kmin + off));
-                mxv[u][0] = __ldg(reinterpret_cast<const uint32_t *>(kmax + off));
+                mnv[u][0] = __ldcg(reinterpret_cast<const uint32_t *>(kmin + off));
+                mxv[u][0] = __ldcg(reinterpret_cast<const uint32_t *>(kmax + off));
             }
         }
         // per-block K scale of block j0 + lane (E4M3 cache with block scales)
@@ -248,7 +287,7 @@ __global__ void __launch_bounds__(kTopkThreads, 4) quest_topk_kernel(
 template <int D, bool F8>
 cudaError_t launch_score(float *scores, const uint16_t *q, const void *kmin, const void *kmax,
                          const float *kbs, const int32_t *bt, int MBS, const int32_t *ctx, int B, int Hq,
-                         int Hkv, int BS, int64_t NB, cudaStream_t stream) {
+                         int Hkv, int BS, int64_t NB, cudaStream_t stream, const ScoreWrite *write) {
     // persistent grid, every SM full (computed once, thread-safe; the same on
     // every GPU of a node)
     static const int grid = [] {
@@ -262,31 +301,35 @@ cudaError_t launch_score(float *scores, const uint16_t *q, const void *kmin, con
     }();
     if (grid == 0) return cudaErrorInvalidConfiguration;
     const size_t smem = size_t(B + 1) * 4;
+    ScoreWrite wr{};
+    if (write) wr = *write;
     return launch_pdl(quest_score_kernel<D, F8>, dim3(grid), dim3(kScoreThreads), smem, stream, scores, q,
-                      kmin, kmax, kbs, bt, MBS, ctx, B, Hq, Hkv, BS, NB);
+                      kmin, kmax, kbs, bt, MBS, ctx, B, Hq, Hkv, BS, NB, wr);
 }
 
 }  // namespace
 
 cudaError_t launch_quest_scores(float *scores, const uint16_t *q, const void *kmin, const void *kmax,
                                 const int32_t *bt, int MBS, const int32_t *ctx, int B, int Hq, int Hkv, int D,
-                                int BS, int64_t NB, cudaStream_t stream, bool fp8, const float *k_bscale) {
+                                int BS, int64_t NB, cudaStream_t stream, bool fp8, const float *k_bscale,
+                                const ScoreWrite *write) {
     if (fp8) {
-        if (D != 128) return cudaErrorInvalidValue;
+        if (D != 128 || write) return cudaErrorInvalidValue;
         return launch_score<128, true>(scores, q, kmin, kmax, k_bscale, bt, MBS, ctx, B, Hq, Hkv, BS, NB,
-                                       stream);
+                                       stream, nullptr);
     }
-    return D == 128
-               ? launch_score<128, false>(scores, q, kmin, kmax, nullptr, bt, MBS, ctx, B, Hq, Hkv, BS, NB, stream)
-               : launch_score<64, false>(scores, q, kmin, kmax, nullptr, bt, MBS, ctx, B, Hq, Hkv, BS, NB, stream);
+    return D == 128 ? launch_score<128, false>(scores, q, kmin, kmax, nullptr, bt, MBS, ctx, B, Hq, Hkv, BS, NB,
+                                               stream, write)
+                    : launch_score<64, false>(scores, q, kmin, kmax, nullptr, bt, MBS, ctx, B, Hq, Hkv, BS, NB,
+                                              stream, write);
 }
 
 cudaError_t launch_quest_select(int32_t *sel, float *scores, const uint16_t *q, const void *kmin,
                                 const void *kmax, const int32_t *bt, int MBS, const int32_t *ctx,
                                 int B, int Hq, int Hkv, int D, int BS, int64_t NB, int topk,
-                                cudaStream_t stream, bool fp8, const float *k_bscale) {
-    const cudaError_t e =
-        launch_quest_scores(scores, q, kmin, kmax, bt, MBS, ctx, B, Hq, Hkv, D, BS, NB, stream, fp8, k_bscale);
+                                cudaStream_t stream, bool fp8, const float *k_bscale, const ScoreWrite *write) {
+    const cudaError_t e = launch_quest_scores(scores, q, kmin, kmax, bt, MBS, ctx, B, Hq, Hkv, D, BS, NB, stream,
+                                              fp8, k_bscale, write);
     if (e != cudaSuccess) return e;
     return launch_pdl(quest_topk_kernel, dim3(unsigned(B) * unsigned(Hkv)), dim3(kTopkThreads), 0, stream,
                       sel, static_cast<const float *>(scores), MBS, ctx, Hkv, BS, topk);
