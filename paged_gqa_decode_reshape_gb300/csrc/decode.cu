@@ -430,25 +430,34 @@ __global__ void __launch_bounds__(DecodeCfg<D, F8, MULTI>::THREADS, 1)
         auto write_new_token = [&](int seg_w, int ph_w, int c_w) {
             if constexpr (!F8 && !MULTI) {
                 const int b = seg_w / Hkv, kvh = seg_w % Hkv, o = (c_w - 1) % BS;
-                if (__ldg(a.new_slots + b) != int64_t(ph_w) * BS + o) return;
                 constexpr int VPR = D / 8;  // 16-byte vectors per KV-head row
                 const int half = lane / VPR, e = lane % VPR;
-                if (half >= 2) return;
-                const int64_t src = (int64_t(b) * Hkv + kvh) * D;
-                const int64_t dst = ((int64_t(ph_w) * BS + o) * Hkv + kvh) * D;
-                const uint4 x = __ldg(reinterpret_cast<const uint4 *>((half ? a.new_v : a.new_k) + src) + e);
-                reinterpret_cast<uint4 *>((half ? a.vc_w : a.kc_w) + dst)[e] = x;
+                const bool meta = half == 0 && a.kmin_w && o != 0;
+                const int64_t mrow = (int64_t(ph_w) * Hkv + kvh) * D;
+                uint4 *mn = a.kmin_w ? reinterpret_cast<uint4 *>(a.kmin_w + mrow) + e : nullptr;
+                uint4 *mx = a.kmin_w ? reinterpret_cast<uint4 *>(a.kmax_w + mrow) + e : nullptr;
+                // every load in flight before the first use: the slot, the
+                // token's 16 bytes, the block's metadata
+                const int64_t slot = __ldg(a.new_slots + b);
+                uint4 x = make_uint4(0u, 0u, 0u, 0u), lo = x, hi = x;
+                if (half < 2)
+                    x = __ldg(reinterpret_cast<const uint4 *>((half ? a.new_v : a.new_k) + (int64_t(b) * Hkv + kvh) * D) +
+                              e);
+                if (meta) {
+                    lo = *mn;
+                    hi = *mx;
+                }
+                if (slot != int64_t(ph_w) * BS + o || half >= 2) return;
+                reinterpret_cast<uint4 *>((half ? a.vc_w : a.kc_w) + ((int64_t(ph_w) * BS + o) * Hkv + kvh) * D)[e] = x;
                 if (half == 0 && a.kmin_w) {  // reset at offset 0, else merge
-                    uint4 *mn = reinterpret_cast<uint4 *>(a.kmin_w + (int64_t(ph_w) * Hkv + kvh) * D) + e;
-                    uint4 *mx = reinterpret_cast<uint4 *>(a.kmax_w + (int64_t(ph_w) * Hkv + kvh) * D) + e;
-                    uint4 lo = x, hi = x;
-                    if (o != 0) {
-                        lo = *mn;
-                        hi = *mx;
+                    if (meta) {
                         minmax_bf16x2(lo.x, hi.x, x.x);
                         minmax_bf16x2(lo.y, hi.y, x.y);
                         minmax_bf16x2(lo.z, hi.z, x.z);
                         minmax_bf16x2(lo.w, hi.w, x.w);
+                    } else {
+                        lo = x;
+                        hi = x;
                     }
                     *mn = lo;
                     *mx = hi;
