@@ -225,8 +225,10 @@ PA_API int quest_sparse_decode(pa_bf16 *out, const pa_bf16 *query,
                         int block_size, int64_t num_blocks, float scale,
                         void *workspace, size_t workspace_bytes, void *stream);
 
-/* quest_sparse_decode with a cap on the CTAs it launches (max_ctas 0: one
- * per SM, as quest_sparse_decode; max_ctas < 0 is PA_ERR_INVALID_ARG). For a
+/* quest_sparse_decode with a cap on the CTAs it launches (max_ctas 0: the
+ * default of quest_sparse_decode, half the SMs when the batch's (sequence,
+ * KV head) segments fit in them, else one CTA per SM; max_ctas < 0 is
+ * PA_ERR_INVALID_ARG). For a
  * step that runs the sparse decode on its own stream beside a dense
  * pa_decode: each sparse CTA needs a whole SM's shared memory, so they start
  * as the dense call's CTAs finish, and a smaller grid lets the sparse call
@@ -258,7 +260,7 @@ PA_API size_t quest_decode_workspace_size(int batch, int num_q_heads, int num_kv
  * where every sparse CTA would hold several whole segments and select for
  * each in turn, it runs quest_select_topk and quest_sparse_decode_budget
  * instead (three launches, the same results).
- * max_ctas: as quest_sparse_decode_budget (0: one CTA per SM). Workspace:
+ * max_ctas: as quest_sparse_decode_budget (0: the default). Workspace:
  * quest_decode_workspace_size bytes, zero-filled once, as pa_decode's (the
  * scores follow the decode part). Errors as quest_select_topk and
  * quest_sparse_decode. */
@@ -555,7 +557,7 @@ PA_API int pa_decode_fp8_block(pa_bf16 *out, const pa_bf16 *query,
                                float scale, void *workspace, size_t workspace_bytes, void *stream);
 
 /* quest_sparse_decode_fp8_budget on a cache with per-block scales
- * (max_ctas 0: one CTA per SM at most). */
+ * (max_ctas 0: the default). */
 PA_API int quest_sparse_decode_fp8_block(pa_bf16 *out, const pa_bf16 *query,
                                          const pa_e4m3 *key_cache, const pa_e4m3 *value_cache,
                                          const float *k_bscale, const float *v_bscale,

@@ -307,7 +307,7 @@ def quest_sparse_decode_budget(out: torch.Tensor, query: torch.Tensor, key_cache
                                value_cache: torch.Tensor, block_tables: torch.Tensor,
                                context_lens: torch.Tensor, selected: torch.Tensor, scale: float,
                                max_ctas: int, workspace: Optional[torch.Tensor] = None) -> torch.Tensor:
-    """quest_sparse_decode launching at most max_ctas CTAs (0: one per SM)."""
+    """quest_sparse_decode launching at most max_ctas CTAs (0: the default)."""
     L = load_library()
     dev, B, Hq, Hkv, D, BS, NB, MBS = _attention_checks(out, query, key_cache, value_cache,
                                                         block_tables, context_lens)
@@ -642,7 +642,7 @@ def quest_sparse_decode_fp8_budget(out: torch.Tensor, query: torch.Tensor, key_c
                                    block_tables: torch.Tensor, context_lens: torch.Tensor,
                                    selected: torch.Tensor, scale: float, max_ctas: int,
                                    workspace: Optional[torch.Tensor] = None) -> torch.Tensor:
-    """quest_sparse_decode_fp8 launching at most max_ctas CTAs (0: one per SM)."""
+    """quest_sparse_decode_fp8 launching at most max_ctas CTAs (0: the default)."""
     L = load_library()
     dev, B, Hq, Hkv, D, BS, NB, MBS = _attention_checks_fp8(out, query, key_cache, value_cache,
                                                             block_tables, context_lens, k_scale, v_scale)
@@ -861,7 +861,7 @@ def quest_sparse_decode_fp8_block(out: torch.Tensor, query: torch.Tensor, key_ca
                                   block_tables: torch.Tensor, context_lens: torch.Tensor,
                                   selected: torch.Tensor, scale: float, max_ctas: int = 0,
                                   workspace: Optional[torch.Tensor] = None) -> torch.Tensor:
-    """Quest sparse attention over 8-bit caches with per-block scales (max_ctas 0: one CTA per SM at most)."""
+    """Quest sparse attention over 8-bit caches with per-block scales (max_ctas 0: the default)."""
     L = load_library()
     dev, B, Hq, Hkv, D, BS, NB, MBS = _attention_checks_fp8(out, query, key_cache, value_cache, block_tables,
                                                             context_lens, k_bscale, v_bscale, per_block=True)

@@ -1301,13 +1301,18 @@ cudaError_t launch_t(const CUtensorMap &tm_k, const CUtensorMap &tm_v, const Dec
         // cross-CTA combine), and a range boundary inside a segment costs a
         // combine: cut each segment into c equal pieces (c a power of two, at
         // least kSparseMinItems items each, at most `budget` CTAs in all) or
-        // give each CTA whole segments. The budget is one CTA per SM unless
-        // the caller sets a smaller one: in a step that runs the sparse
-        // decode beside the dense one, half the SMs let it start on the SMs
-        // the dense CTAs free without waiting for the last of them (quest_8k
-        // step 83.6 -> 77.3 us with 64 CTAs of 64 items instead of 128 of 32).
-        const int budget = (max_ctas > 0 && max_ctas < grid) ? max_ctas : grid;
+        // give each CTA whole segments. The budget is the caller's max_ctas;
+        // by default half the SMs when the segments fit in it, else one CTA
+        // per SM. A piece boundary costs a partial and a combine, and in the
+        // fused Quest decode every piece repeats its segment's top-K: on
+        // quest_8k (64 segments of 64 blocks) 64 CTAs took 41.0 us against
+        // 45.1 us for 128 (quest_decode), with the sparse decode alone equal;
+        // dense_b32's 128 segments need 128 CTAs (43.0 against 57.3 us).
+        // In a step that runs the sparse decode beside the dense one, half
+        // the SMs also let it start on the SMs the dense CTAs free without
+        // waiting for the last of them (quest_8k step 83.6 -> 77.3 us).
         const int64_t segs = int64_t(a.B) * a.Hkv;
+        const int budget = (max_ctas > 0 && max_ctas < grid) ? max_ctas : (segs <= grid / 2 ? grid / 2 : grid);
         if (segs * a.topk < int64_t(grid) * kSparseLargeItems) {
             int64_t c = 1;
             while (a.topk % (2 * c) == 0 && a.topk / (2 * c) >= kSparseMinItems && segs * 2 * c <= budget)

@@ -17,9 +17,9 @@ from tests.test_gpu_parity import run_full_compare
 
 pytestmark = pytest.mark.gpu
 
-# name: (B, Hq, Hkv, topk, context lengths); with one CTA per SM allowed and
-# at least 16 items per piece the segments split into 4, 8, 8 and 8 pieces
-# (fewer under a smaller CTA budget)
+# name: (B, Hq, Hkv, topk, context lengths); with the default CTA budget (half
+# the SMs, as these segments fit in it) and at least 16 items per piece the
+# segments split into 4, 4, 8 and 8 pieces (fewer under a smaller budget)
 CASES = {
     "pieces2": (4, 28, 4, 64, [0, 700, 1500, 2200]),
     "pieces4": (4, 28, 4, 128, [2500, 0, 1000, 3000]),
