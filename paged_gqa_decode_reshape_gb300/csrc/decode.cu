@@ -488,6 +488,9 @@ __global__ void __launch_bounds__(DecodeCfg<D, F8, MULTI>::THREADS, 1)
         // part = which tile copy (bf16: K and V in two 64-dim halves each;
         // E4M3: one K and one V copy, so twice the items per step)
         constexpr int LPI = F8 ? 2 : 4, IPS = 32 / LPI;
+        // a step's items take distinct stages, and each waits only for items
+        // of earlier steps to leave its stage (no two items of a step alias)
+        static_assert(IPS < S, "items per producer step must stay below the ring depth");
         const int it = lane / LPI, part = lane % LPI;
         constexpr int PARTS = F8 ? 2 : 2 * (D / 64);  // K and V (bf16: 64-dim halves)
         for (int k0 = 0; k0 < n_items; k0 += IPS) {
