@@ -180,7 +180,14 @@ __global__ void __launch_bounds__(DecodeCfg<D, F8, MULTI>::THREADS, 1)
             for (int64_t off = gt * 32; off < sel_n; off += nthr * 32) prefetch_l2(a.sel + off);
         }
     }
-    pdl_wait();  // inputs may come from the previous kernel in the stream
+    // The bf16 dense call reads only the context lengths and block-table
+    // entries before its first copy: the caller's inputs, which no kernel of
+    // this library writes. So its producer resolves its first items while the
+    // previous kernel in the stream finishes, and waits for that kernel just
+    // before issuing copies; its consumers wait before they touch q, the
+    // outputs or the workspace. Every other call waits here.
+    const bool early = !MULTI && !F8 && !SPARSE;
+    if (!early) pdl_wait();  // inputs may come from the previous kernel in the stream
     // Multi-token rows ("18 e2e inference serving", sections 2.7 and 3.3):
     // query row r of sequence s (cu_q[s] <= r < cu_q[s+1]) sees the
     // positions before ctx_s - q_len_s + (r - cu_q[s]) + 1 (causal mask
@@ -285,8 +292,10 @@ __global__ void __launch_bounds__(DecodeCfg<D, F8, MULTI>::THREADS, 1)
                 for (int i = 0; i < D / 8; ++i) o[i] = make_uint4(0, 0, 0, 0);
             }
         }
-    } else {
-        for (int idx = blockIdx.x * C::THREADS + tid; idx < B * a.Hq; idx += gridDim.x * C::THREADS) {
+    } else if (!early || warp < NC) {  // early: the consumers, after their wait
+        if (early) pdl_wait();
+        const int nt = early ? NC * 32 : C::THREADS;
+        for (int idx = blockIdx.x * nt + tid; idx < B * a.Hq; idx += gridDim.x * nt) {
             const int b = idx / a.Hq;
             if (pre[b + 1] == pre[b]) {
                 uint4 *o = reinterpret_cast<uint4 *>(a.out + int64_t(idx) * D);
@@ -480,6 +489,7 @@ __global__ void __launch_bounds__(DecodeCfg<D, F8, MULTI>::THREADS, 1)
             stage_s(wa);
             stage_s(wb);
         }
+        if (early) pdl_wait();  // the first items are resolved: now the previous kernel
         int wbase = 0;
         int issued = 0;  // items [0, issued) have been armed
         int fail_step = 0;
