@@ -500,10 +500,11 @@ def step_runner(torch, step, serial: bool, quest=None):
     write, quest_decode, dense decode on one stream. Else the Quest path runs
     on a second stream forked after the write path and joined at the end of
     the step (step.quest_beside(): the selection's CTAs run on the SMs beside
-    the dense decode's, since a decode CTA's four warps leave room in each of
-    the SM's register-file partitions; the sparse decode's CTAs, which need a
-    whole SM's shared memory, take SMs as the dense decode's CTAs finish, on
-    at most half the SMs). Neither path reads the other's output, and the two
+    the dense decode's, since a decode CTA's warps (at most 184 registers
+    each) leave room in each of the SM's register-file partitions; the
+    sparse decode's CTAs, which need a whole SM's shared memory, take SMs as
+    the dense decode's CTAs finish, on at most half the SMs). Neither path
+    reads the other's output, and the two
     decode calls have their own workspaces. `quest` overrides the Quest-path
     call in either mode."""
     c = dict(zip(CALL_NAMES, step.calls()))

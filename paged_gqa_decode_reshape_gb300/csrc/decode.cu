@@ -36,11 +36,13 @@
 //  * Masking. Tokens past ctx get score -inf and their V fragment lanes are
 //    zeroed, so NaN/Inf garbage in unused slots never reaches the output.
 //  * Combine. At the end of each segment every consumer warp deposits its
-//    state in shared memory and moves on; the last one to arrive merges the
-//    states. A CTA holding a whole segment writes bf16 output; otherwise the
-//    merging warp writes a normalised partial and its log2-sum-exp, and in
-//    the last CTA to arrive (atomic counter per segment, reset to zero
-//    afterwards) merges the pieces with weights exp2(lse_s - max lse).
+//    state in shared memory and moves on; a merge warp (one query row per
+//    sequence) merges the states, so a merge never holds a consumer's ring
+//    stages and stalls the in-order producer. A CTA holding a whole segment
+//    writes bf16 output; otherwise the merge warp writes a normalised
+//    partial and its log2-sum-exp, and in the last CTA to arrive (atomic
+//    counter per segment, reset to zero afterwards) merges the pieces with
+//    weights exp2(lse_s - max lse).
 #include "common.cuh"
 #include "kernels.h"
 
@@ -53,11 +55,10 @@ namespace {
 // stage s always belongs to consumer (s / 2) % consumers: every consumer waits
 // on its own stages in order and an mbarrier parity wait can never be
 // answered by an older phase.
-// Three consumers (four warps per CTA) keep one decode warp in each of the
-// SM's four register-file partitions, leaving room for the selection's CTAs
-// to run beside a decode CTA; four warps at 248 registers each already carry
-// the HBM rate. The multi-token kernel keeps one consumer per query row of a
-// group (kMultiRowGroup).
+// Three consumers, the producer and the merge warp: five warps at 248
+// registers each carry the HBM rate and leave room for the selection's CTAs
+// beside a decode CTA. The multi-token kernel keeps one consumer per query
+// row of a group (kMultiRowGroup) and no merge warp.
 #ifndef PA_DECODE_CONSUMERS
 #define PA_DECODE_CONSUMERS 3
 #endif
@@ -68,12 +69,24 @@ namespace {
 #define PA_DECODE_PAIRS_MULTI 3
 #endif
 // E4M3 cache: consumer warps and pairs in flight (its items are half the
-// bytes, so twice the consumers keep the same bytes in flight)
+// bytes, so more consumers keep the bytes in flight). Six consumers, the
+// producer and the merge warp are eight warps: two per register-file
+// partition, which holds the kernel's 255 registers per thread without spills
+// (a ninth warp would cap it at 168 and spill).
 #ifndef PA_DECODE_CONSUMERS_F8
-#define PA_DECODE_CONSUMERS_F8 7
+#define PA_DECODE_CONSUMERS_F8 6
 #endif
 #ifndef PA_DECODE_PAIRS_F8
 #define PA_DECODE_PAIRS_F8 3
+#endif
+// Registers per thread. With five warps, one register-file partition holds
+// two decode warps; at 184 registers each (11,776 of the partition's 16,384)
+// two warps of a selection kernel (64 registers each) still fit beside them,
+// so the Quest path's scoring can run on the SMs the dense decode occupies.
+// The kernel needs no spills at this cap (the combine loads two pieces per
+// round).
+#ifndef PA_DECODE_MAXNREG
+#define PA_DECODE_MAXNREG 184
 #endif
 
 // Sparse decode of small selections (fewer than kSparseLargeItems items per
@@ -90,7 +103,10 @@ struct DecodeCfg {
     static constexpr int HALF = BS * 128;       // bytes of one 64-dim half tile
     static constexpr int PART = D * 8 + 8;      // floats per partial slot: O[D][8], lse[8]
     static constexpr int NC = F8 ? PA_DECODE_CONSUMERS_F8 : (MULTI ? kMultiRowGroup : PA_DECODE_CONSUMERS);
-    static constexpr int THREADS = (NC + 1) * 32;
+    // one query row per sequence: a merge warp after the producer takes the
+    // segment-end merges off the consumers
+    static constexpr int MW = MULTI ? 0 : 1;
+    static constexpr int THREADS = (NC + 1 + MW) * 32;
     static constexpr int PAIRS = MULTI ? PA_DECODE_PAIRS_MULTI : PA_DECODE_PAIRS;
     static constexpr int R = F8 ? PA_DECODE_PAIRS_F8 : (D == 128 ? PAIRS : 2 * PAIRS);
     static constexpr int S = 2 * NC * R;        // ring stages
@@ -128,7 +144,7 @@ struct DecodeCfg {
 // BSC (E4M3 cache only): per-block scales, read per item, instead of one K
 // and V scale per KV head.
 template <int D, bool F8, bool MULTI, bool BSC = false>
-__global__ void __launch_bounds__(DecodeCfg<D, F8, MULTI>::THREADS, 1)
+__global__ void __maxnreg__(PA_DECODE_MAXNREG)
     decode_kernel(const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const DecodeArgs a) {
     using C = DecodeCfg<D, F8, MULTI>;
@@ -147,6 +163,7 @@ __global__ void __launch_bounds__(DecodeCfg<D, F8, MULTI>::THREADS, 1)
     float2 *iscale = reinterpret_cast<float2 *>(bp + C::off_iscale);  // E4M3 cache only
     float *scr = reinterpret_cast<float *>(bp + C::off_scr);
     volatile int *flags = reinterpret_cast<volatile int *>(bp + C::off_flags);
+    const uint32_t merge_bar = base + uint32_t(C::off_flags) + 16;  // consumers' deposits (count NC)
     int32_t *pre = reinterpret_cast<int32_t *>(bp + C::off_pre);
     // multi-token rows: a work-list row is a group of up to RG query rows of
     // one sequence; seq_of / row0_of give its sequence and first query row
@@ -228,12 +245,12 @@ __global__ void __launch_bounds__(DecodeCfg<D, F8, MULTI>::THREADS, 1)
     if (tid == 0) {
         pre[0] = 0;
         flags[0] = 0;  // abort
-        flags[1] = 0;  // consumers arrived at the current segment end
-        flags[2] = 0;  // segment ends whose states have been merged
+        flags[2] = 0;  // segment ends whose states the merge warp has read
         for (int s = 0; s < S; ++s) {
             mbar_init(full_bar + s * 8, 1);
             mbar_init(empty_bar + s * 8, MULTI ? NC : 1);  // MULTI: every consumer reads every stage
         }
+        if (!MULTI) mbar_init(merge_bar, NC);
         fence_barrier_init();
     }
     int NR = B;  // work-list rows
@@ -900,7 +917,7 @@ __global__ void __launch_bounds__(DecodeCfg<D, F8, MULTI>::THREADS, 1)
         for (int r = 0; r < NSL; ++r)
 #pragma unroll
             for (int e = 0; e < 4; ++e) O[r][e] = 0.f;
-        constexpr int U = 4;  // pieces in flight per round
+        constexpr int U = 2;  // pieces in flight per round
         for (int i0 = 0; i0 < np; i0 += U) {
             float4 lx[U], xv[U][NSL];
 #pragma unroll
@@ -952,21 +969,21 @@ __global__ void __launch_bounds__(DecodeCfg<D, F8, MULTI>::THREADS, 1)
         }
     };
 
-    // End of a segment for this warp. Every consumer deposits its state in
-    // its shared-memory slot and counts itself in; the last warp to arrive
-    // merges the NC states and writes the CTA's piece (final output, or a
-    // partial followed by the cross-CTA arrival and, for the last CTA, the
-    // combine); the other warps go straight on to the next segment.
-    volatile int *arrive_cnt = flags + 1;  // warps that deposited the current instance
-    volatile int *read_done = flags + 2;   // instances whose states the merger has read
-    auto merge = [&](int seg, int64_t s0, int64_t e0, bool whole, int inst) {
+    // End of a segment for a consumer warp: it deposits its state in its
+    // shared-memory slot and arrives on merge_bar, then goes straight on to
+    // the next segment. The merge warp merges the NC states and writes the
+    // CTA's piece (final output, or a partial followed by the cross-CTA
+    // arrival and, for the last CTA, the combine), so no consumer holds its
+    // ring stages while a merge runs.
+    volatile int *read_done = flags + 2;  // instances whose states the merge warp has read
+    auto deposit = [&](int inst) {
         l0 += __shfl_xor_sync(0xffffffffu, l0, 4);
         l0 += __shfl_xor_sync(0xffffffffu, l0, 8);
         l0 += __shfl_xor_sync(0xffffffffu, l0, 16);
         l1 += __shfl_xor_sync(0xffffffffu, l1, 4);
         l1 += __shfl_xor_sync(0xffffffffu, l1, 8);
         l1 += __shfl_xor_sync(0xffffffffu, l1, 16);
-        // the slot is free once the previous instance's merger has read it
+        // the slot is free once the merge warp has read the previous instance
         if (lane == 0 && *read_done < inst) {
             const uint64_t t0 = global_timer_ns();
             while (*read_done < inst) {
@@ -982,14 +999,12 @@ __global__ void __launch_bounds__(DecodeCfg<D, F8, MULTI>::THREADS, 1)
         const int hh = 2 * q4;
 #pragma unroll
         for (int mt = 0; mt < NKK; ++mt) {
+            const int d = 16 * mt + g;
             if constexpr (F8) {  // acc is in units of vref
-                const int d = 16 * mt + g;
-                *reinterpret_cast<float2 *>(my + d * 8 + hh) =
-                    make_float2(acc[mt][0] * vref, acc[mt][1] * vref);
+                *reinterpret_cast<float2 *>(my + d * 8 + hh) = make_float2(acc[mt][0] * vref, acc[mt][1] * vref);
                 *reinterpret_cast<float2 *>(my + (d + 8) * 8 + hh) =
                     make_float2(acc[mt][2] * vref, acc[mt][3] * vref);
             } else {
-                const int d = 16 * mt + g;
                 *reinterpret_cast<float2 *>(my + d * 8 + hh) = make_float2(acc[mt][0], acc[mt][1]);
                 *reinterpret_cast<float2 *>(my + (d + 8) * 8 + hh) = make_float2(acc[mt][2], acc[mt][3]);
             }
@@ -999,19 +1014,19 @@ __global__ void __launch_bounds__(DecodeCfg<D, F8, MULTI>::THREADS, 1)
             *reinterpret_cast<float2 *>(my + D * 8 + 8 + hh) = make_float2(l0, l1);
         }
         __syncwarp();
-        int merger = 0;
-        if (lane == 0) {
-            __threadfence_block();
-            merger = (atomicAdd(const_cast<int *>(arrive_cnt), 1) == NC - 1);
-            if (merger) {
-                *arrive_cnt = 0;
-                __threadfence_block();
-            }
-        }
-        merger = __shfl_sync(0xffffffffu, merger, 0);
-        if (!merger) return;
+        if (lane == 0) mbar_arrive(merge_bar);  // release: the slot's writes precede the arrival
+    };
 
-        // ---- this warp merges the NC states
+    // the merge warp's part of segment seg's end: the NC deposited states
+    // (instance inst) merged into the CTA's piece
+    auto merge_states = [&](int seg, int64_t s0, int64_t e0, bool whole, int inst) {
+        if (!mbar_wait_bounded(merge_bar, uint32_t(inst & 1), a.wait_ns)) {
+            if (lane == 0) {
+                flags[0] = 1;
+                atomicOr(a.status, kStatusTimeout);
+            }
+            return false;
+        }
         // pieces of a split segment already counted (read while merging)
         int seen = 0;
         if (!whole && lane == 0) seen = ld_relaxed_s32(a.counters + seg);
@@ -1066,7 +1081,7 @@ __global__ void __launch_bounds__(DecodeCfg<D, F8, MULTI>::THREADS, 1)
                         ob[(h4 + e) * D + d] =
                             __bfloat16_as_ushort(__float2bfloat16_rn(Ls[e] > 0.f ? O[r][e] / Ls[e] : 0.f));
             }
-            return;
+            return true;
         }
         // this CTA's piece, normalised, and its log2-sum-exp
         float inv[4], lse[4];
@@ -1090,7 +1105,7 @@ __global__ void __launch_bounds__(DecodeCfg<D, F8, MULTI>::THREADS, 1)
             combine(int64_t(seg) + w0, 1, a.out + (int64_t(seg / Hkv) * a.Hq + (seg % Hkv) * G) * D, s0, e0,
                     int(blockIdx.x) - w0, lse, ox);
             if (lane == 0) a.counters[seg] = 0;
-            return;
+            return true;
         }
         float *ps = a.part + int64_t(seg + blockIdx.x) * C::PART;
 #pragma unroll
@@ -1116,6 +1131,7 @@ __global__ void __launch_bounds__(DecodeCfg<D, F8, MULTI>::THREADS, 1)
                     -1, nol, ox);
             if (lane == 0) a.counters[seg] = 0;
         }
+        return true;
     };
 
     // MULTI: end of a piece [s0, e0) of work-list segment seg for this
@@ -1220,10 +1236,14 @@ __global__ void __launch_bounds__(DecodeCfg<D, F8, MULTI>::THREADS, 1)
         return;
     }
 
-    // walk the segments of this CTA's range in order; every consumer warp
-    // takes part in every segment's merge
+    // walk the segments of this CTA's range in order: the consumers stream
+    // each segment's items and deposit their states, the merge warp merges
+    // them (instance inst = segments finished so far, the same count in
+    // every warp)
+    const bool merge_warp = warp == NC + 1;
+    if (merge_warp && early) pdl_wait();  // before its first write
     int64_t p = pos0;
-    int inst = 0;  // segments finished so far (the same count in every consumer)
+    int inst = 0;
     int b = find_seq(p);
     int kvh = int((p - int64_t(Hkv) * pre[b]) / (pre[b + 1] - pre[b]));
     while (p < pos1) {
@@ -1232,6 +1252,18 @@ __global__ void __launch_bounds__(DecodeCfg<D, F8, MULTI>::THREADS, 1)
         const int64_t s0 = int64_t(Hkv) * pre[b] + int64_t(kvh) * n;
         const int64_t e0 = s0 + n;
         const int ks0 = int(p - pos0), ks1 = int(min(e0, pos1) - pos0);
+        const bool whole = (s0 >= pos0) && (e0 <= pos1);
+        if (merge_warp) {
+            if (!merge_states(seg, s0, e0, whole, inst++)) return;
+            p = min(e0, pos1);
+            if (++kvh == Hkv) {
+                kvh = 0;
+                do {
+                    ++b;
+                } while (b < NR && pre[b + 1] == pre[b]);
+            }
+            continue;
+        }
         load_q(seg, b);
         // item pairs (2q, 2q+1) of this segment owned by this warp: q % NC == c_id
         int q = ks0 >> 1;
@@ -1248,8 +1280,7 @@ __global__ void __launch_bounds__(DecodeCfg<D, F8, MULTI>::THREADS, 1)
                 if (kb > ka) mbar_arrive(empty_bar + (kb % S) * 8);
             }
         }
-        const bool whole = (s0 >= pos0) && (e0 <= pos1);
-        merge(seg, s0, e0, whole, inst++);
+        deposit(inst++);
         p = min(e0, pos1);
         if (++kvh == Hkv) {
             kvh = 0;
