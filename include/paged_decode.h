@@ -126,6 +126,22 @@ PA_API int pa_decode(pa_bf16 *out, const pa_bf16 *query,
               int num_kv_heads, int head_dim, int block_size, int64_t num_blocks,
               float scale, void *workspace, size_t workspace_bytes, void *stream);
 
+/* pa_decode on at most max_ctas CTAs (max_ctas 0, or at least one per SM:
+ * one CTA per SM, as pa_decode; max_ctas < 0 is PA_ERR_INVALID_ARG). For a
+ * step that runs other work on its own stream beside the dense decode: a
+ * decode CTA takes a whole SM's shared memory, and its persistent grid cuts
+ * the batch's KV blocks into max_ctas equal ranges, so the SMs beyond
+ * max_ctas stay free for the other stream. The split-KV pieces, and so the
+ * rounding of the result, depend on max_ctas; for a given max_ctas the result
+ * is deterministic. Workspace: as pa_decode. */
+PA_API int pa_decode_budget(pa_bf16 *out, const pa_bf16 *query,
+                     const pa_bf16 *key_cache, const pa_bf16 *value_cache,
+                     const int32_t *block_tables, int max_blocks_per_seq,
+                     const int32_t *context_lens, int batch, int num_q_heads,
+                     int num_kv_heads, int head_dim, int block_size, int64_t num_blocks,
+                     float scale, int max_ctas, void *workspace, size_t workspace_bytes,
+                     void *stream);
+
 /* Size of the fixed scratch buffer behind pa_decode_no_alloc (8 MiB). */
 #define PA_NO_ALLOC_SCRATCH_BYTES (8u << 20)
 

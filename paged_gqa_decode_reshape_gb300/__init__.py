@@ -33,7 +33,7 @@ _lock = threading.Lock()
 
 __all__ = [
     "PagedDecodeError", "load_library", "pa_status_string", "pa_reshape_and_cache",
-    "pa_decode_workspace_size", "pa_decode", "quest_update_meta", "quest_reshape_and_cache",
+    "pa_decode_workspace_size", "pa_decode", "pa_decode_budget", "quest_update_meta", "quest_reshape_and_cache",
     "quest_rebuild_meta",
     "quest_select_workspace_size", "quest_select_topk", "quest_sparse_decode", "quest_sparse_decode_budget",
     "quest_decode_workspace_size", "quest_decode", "quest_decode_fp8",
@@ -81,6 +81,9 @@ def load_library(path: Optional[str] = None):
         L.pa_decode.argtypes = [vp, vp, vp, vp, vp, i32, vp, i32, i32, i32, i32, i32, i64, f32,
                                 vp, sz, vp]
         L.pa_decode.restype = i32
+        L.pa_decode_budget.argtypes = [vp, vp, vp, vp, vp, i32, vp, i32, i32, i32, i32, i32, i64, f32,
+                                       i32, vp, sz, vp]
+        L.pa_decode_budget.restype = i32
         L.quest_update_meta.argtypes = [vp, vp, vp, vp, i64, i32, i32, i32, i64, vp]
         L.quest_update_meta.restype = i32
         L.quest_reshape_and_cache.argtypes = [vp, vp, vp, vp, vp, vp, vp, i64, i32, i32, i32, i64, vp]
@@ -278,6 +281,24 @@ def pa_decode(out: torch.Tensor, query: torch.Tensor, key_cache: torch.Tensor,
            L.pa_decode(_ptr(out), _ptr(query), _ptr(key_cache), _ptr(value_cache),
                        _ptr(block_tables), MBS, _ptr(context_lens), B, Hq, Hkv, D, BS, NB,
                        float(scale), _ptr(ws), ws.numel() * ws.element_size(), _stream(dev)))
+    return out
+
+
+def pa_decode_budget(out: torch.Tensor, query: torch.Tensor, key_cache: torch.Tensor,
+                     value_cache: torch.Tensor, block_tables: torch.Tensor, context_lens: torch.Tensor,
+                     scale: float, max_ctas: int, workspace: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """pa_decode on at most max_ctas CTAs (0: one per SM), leaving the other
+    SMs to work on another stream."""
+    L = load_library()
+    dev, B, Hq, Hkv, D, BS, NB, MBS = _attention_checks(out, query, key_cache, value_cache,
+                                                        block_tables, context_lens)
+    need = pa_decode_workspace_size(B, Hq, Hkv, D)
+    ws = workspace if workspace is not None else _default_ws.get(dev, need)
+    _check("pa_decode_budget",
+           L.pa_decode_budget(_ptr(out), _ptr(query), _ptr(key_cache), _ptr(value_cache),
+                              _ptr(block_tables), MBS, _ptr(context_lens), B, Hq, Hkv, D, BS, NB,
+                              float(scale), int(max_ctas), _ptr(ws), ws.numel() * ws.element_size(),
+                              _stream(dev)))
     return out
 
 

@@ -233,6 +233,18 @@ int pa_decode(pa_bf16 *out, const pa_bf16 *query, const pa_bf16 *key_cache,
                       block_size, num_blocks, scale, workspace, workspace_bytes, stream, false);
 }
 
+int pa_decode_budget(pa_bf16 *out, const pa_bf16 *query, const pa_bf16 *key_cache,
+                     const pa_bf16 *value_cache, const int32_t *block_tables, int max_blocks_per_seq,
+                     const int32_t *context_lens, int batch, int num_q_heads, int num_kv_heads,
+                     int head_dim, int block_size, int64_t num_blocks, float scale, int max_ctas,
+                     void *workspace, size_t workspace_bytes, void *stream) {
+    if (max_ctas < 0) return PA_ERR_INVALID_ARG;
+    return run_decode(out, query, key_cache, value_cache, block_tables, max_blocks_per_seq,
+                      context_lens, nullptr, 0, batch, num_q_heads, num_kv_heads, head_dim,
+                      block_size, num_blocks, scale, workspace, workspace_bytes, stream, false, nullptr,
+                      nullptr, false, nullptr, 0, max_ctas);
+}
+
 int quest_sparse_decode(pa_bf16 *out, const pa_bf16 *query, const pa_bf16 *key_cache,
                         const pa_bf16 *value_cache, const int32_t *block_tables,
                         int max_blocks_per_seq, const int32_t *context_lens,

@@ -1370,6 +1370,10 @@ cudaError_t launch_t(const CUtensorMap &tm_k, const CUtensorMap &tm_v, const Dec
         } else {
             grid = budget;
         }
+    } else if (max_ctas > 0 && max_ctas < grid) {
+        // dense: the caller's CTA budget, so that other work can run on the
+        // remaining SMs (the work list is cut into max_ctas equal ranges)
+        grid = max_ctas;
     }
     if (SPARSE && a.scores) {
         // fused Quest decode: room for the CTA's selection entries (at most
@@ -1432,22 +1436,22 @@ cudaError_t launch_decode(const CUtensorMap &tm_k, const CUtensorMap &tm_v, cons
                           int head_dim, bool sparse, cudaStream_t stream, bool fp8, int max_ctas) {
     if (a.cu_q) {  // multi-token query rows (bf16 cache, dense)
         if (fp8 || sparse) return cudaErrorInvalidValue;
-        return head_dim == 128 ? launch_t<128, false, false, true>(tm_k, tm_v, a, stream)
-                               : launch_t<64, false, false, true>(tm_k, tm_v, a, stream);
+        return head_dim == 128 ? launch_t<128, false, false, true>(tm_k, tm_v, a, stream, max_ctas)
+                               : launch_t<64, false, false, true>(tm_k, tm_v, a, stream, max_ctas);
     }
     if (fp8) {
         if (head_dim != 128) return cudaErrorInvalidValue;
         if (a.scale_per_block)
             return sparse ? launch_t<128, true, true, false, true>(tm_k, tm_v, a, stream, max_ctas)
-                          : launch_t<128, false, true, false, true>(tm_k, tm_v, a, stream);
+                          : launch_t<128, false, true, false, true>(tm_k, tm_v, a, stream, max_ctas);
         return sparse ? launch_t<128, true, true>(tm_k, tm_v, a, stream, max_ctas)
-                      : launch_t<128, false, true>(tm_k, tm_v, a, stream);
+                      : launch_t<128, false, true>(tm_k, tm_v, a, stream, max_ctas);
     }
     if (head_dim == 128)
         return sparse ? launch_t<128, true, false>(tm_k, tm_v, a, stream, max_ctas)
-                      : launch_t<128, false, false>(tm_k, tm_v, a, stream);
+                      : launch_t<128, false, false>(tm_k, tm_v, a, stream, max_ctas);
     return sparse ? launch_t<64, true, false>(tm_k, tm_v, a, stream, max_ctas)
-                  : launch_t<64, false, false>(tm_k, tm_v, a, stream);
+                  : launch_t<64, false, false>(tm_k, tm_v, a, stream, max_ctas);
 }
 
 }  // namespace pa

@@ -64,8 +64,8 @@ struct DecodeGeometry {
 cudaError_t decode_geometry(int head_dim, DecodeGeometry *g, bool fp8 = false);
 size_t decode_workspace_bytes(int B, int Hkv, int head_dim, int workers);
 size_t decode_multi_workspace_bytes(int total_q, int Hkv, int head_dim, int workers);
-// max_ctas (sparse only): at most this many CTAs (<= 0: half the SMs when the
-// segments fit in them, else one per SM)
+// max_ctas: at most this many CTAs. Sparse: <= 0 gives half the SMs when the
+// segments fit in them, else one per SM. Dense: <= 0 gives one per SM.
 cudaError_t launch_decode(const CUtensorMap &tm_k, const CUtensorMap &tm_v, const DecodeArgs &a,
                           int head_dim, bool sparse, cudaStream_t stream, bool fp8 = false,
                           int max_ctas = 0);

@@ -105,6 +105,13 @@ def test_select_workspace_size_and_checks(lib):
     assert rc == -1
 
 
+def test_dense_budget_rejects_a_negative_budget(lib):
+    fake = ctypes.c_void_p(1 << 20)
+    rc = lib.pa_decode_budget(fake, fake, fake, fake, fake, 4, fake, 2, 28, 4, 128, 16, 64, 0.088, -1,
+                              fake, 1 << 30, None)
+    assert rc == -1
+
+
 def test_sparse_requires_selection(lib):
     fake = ctypes.c_void_p(1 << 20)
     rc = lib.quest_sparse_decode(fake, fake, fake, fake, fake, 4, fake, None, 4, 2, 28, 4, 128, 16,
