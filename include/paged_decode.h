@@ -38,13 +38,14 @@
  *     are detected on the host before anything is launched.
  *   - Kernels launch with programmatic stream serialization: a kernel may
  *     start while the previous kernel in the stream finishes, and waits for
- *     it before reading anything that kernel may write. One exception: the
- *     bf16 dense decode (pa_decode, pa_reshape_and_decode) reads
- *     context_lens and block_tables before that wait. No kernel of this
- *     library writes them. A caller kernel that writes them and lets
- *     dependent launches start early must not run just before such a call.
- *     A kernel that never triggers early starts its dependents only when it
- *     completes, so the usual case is safe.
+ *     it before reading anything that kernel may write. The exceptions are
+ *     context_lens (read before that wait by every decode and selection
+ *     call, and cu_seqlens_q by pa_decode_multi) and block_tables (read
+ *     before it by the bf16 dense decode and by the selection's score
+ *     kernel). No kernel of this library writes them. A caller kernel that
+ *     writes them and lets dependent launches start early must not run just
+ *     before such a call. A kernel that never triggers early starts its
+ *     dependents only when it completes, so the usual case is safe.
  *   - Supported shapes: head_dim D in {64, 128}; block_size BS = 16;
  *     group size Hq / Hkv in 1..8; B <= 4096.
  *   - Device data is never trusted to the point of a fault: negative or

@@ -197,14 +197,15 @@ __global__ void __maxnreg__(PA_DECODE_MAXNREG)
             for (int64_t off = gt * 32; off < sel_n; off += nthr * 32) prefetch_l2(a.sel + off);
         }
     }
-    // The bf16 dense call reads only the context lengths and block-table
-    // entries before its first copy: the caller's inputs, which no kernel of
-    // this library writes. So its producer resolves its first items while the
-    // previous kernel in the stream finishes, and waits for that kernel just
-    // before issuing copies; its consumers wait before they touch q, the
-    // outputs or the workspace. Every other call waits here.
+    // Every call builds its per-sequence prefix from the context lengths (and
+    // the query-row offsets of multi-token rows) while the previous kernel in
+    // the stream finishes: the caller's inputs, which no kernel of this
+    // library writes. The bf16 dense call also reads only block-table entries
+    // before its first copy, so its producer resolves its first items too and
+    // waits for that kernel just before issuing copies; its consumers wait
+    // before they touch q, the outputs or the workspace. Every other call
+    // waits once the prefix is built.
     const bool early = !MULTI && !F8 && !SPARSE;
-    if (!early) pdl_wait();  // inputs may come from the previous kernel in the stream
     // Multi-token rows ("18 e2e inference serving", sections 2.7 and 3.3):
     // query row r of sequence s (cu_q[s] <= r < cu_q[s+1]) sees the
     // positions before ctx_s - q_len_s + (r - cu_q[s]) + 1 (causal mask
@@ -297,6 +298,7 @@ __global__ void __maxnreg__(PA_DECODE_MAXNREG)
     __syncthreads();
     scan_pre(NR);
     __syncthreads();
+    if (!early) pdl_wait();  // the rest may read what the previous kernel wrote
 
     // sequences (MULTI: query rows of groups) with nothing to attend to get a zero output
     if constexpr (MULTI) {

@@ -65,7 +65,10 @@ __global__ void __launch_bounds__(kScoreThreads, 4) quest_score_kernel(
     constexpr int CW = C / 2;  // 32-bit words per lane per row
     extern __shared__ int32_t pre[];  // [B+1] chunk prefix per KV head
     pdl_trigger();
-    pdl_wait();
+    // The context lengths and the first chunk's block-table entries are the
+    // caller's inputs, which no kernel of this library writes: they are read
+    // while the previous kernel in the stream finishes. Everything else (q,
+    // the metadata, the scores, the step's write) waits for it.
     const int tid = threadIdx.x, lane = tid & 31;
     const int G = Hq / Hkv;
     const int max_tok = MBS * BS;
@@ -96,7 +99,10 @@ __global__ void __launch_bounds__(kScoreThreads, 4) quest_score_kernel(
     const int64_t R = (total + W - 1) / W;
     int64_t id = w * R;
     const int64_t id1 = min(total, id + R);
-    if (id >= id1) return;
+    if (id >= id1) {
+        pdl_wait();
+        return;
+    }
     // locate the first chunk
     int lo = 0, hi = B;
     while (hi - lo > 1) {
@@ -107,6 +113,15 @@ __global__ void __launch_bounds__(kScoreThreads, 4) quest_score_kernel(
     int nch = pre[b + 1] - pre[b];
     int kvh = int((id - int64_t(Hkv) * pre[b]) / nch);
     int ch = int(id - int64_t(Hkv) * pre[b] - int64_t(kvh) * nch);
+    // block-table entries of chunk (b, ch), one per lane
+    auto chunk_phys = [&](int bb, int cc) -> int {
+        const int nb = (min(max(__ldg(ctx + bb), 0), max_tok) + BS - 1) / BS;
+        const int j = cc * kChunk + lane;
+        return (lane < kChunk && j < nb) ? __ldg(bt + int64_t(bb) * MBS + j) : -1;
+    };
+    int ph_first = chunk_phys(b, ch);
+    bool first = true;
+    pdl_wait();
     int pn_seg = -1;
     float P[C], N[C];
     for (; id < id1; ++id) {
@@ -114,7 +129,8 @@ __global__ void __launch_bounds__(kScoreThreads, 4) quest_score_kernel(
         const int nblk = (c + BS - 1) / BS;
         const int j0 = ch * kChunk;
         const int cnt = min(kChunk, nblk - j0);
-        const int ph_l = lane < cnt ? __ldg(bt + int64_t(b) * MBS + j0 + lane) : -1;
+        const int ph_l = first ? ph_first : chunk_phys(b, ch);
+        first = false;
         if (b * Hkv + kvh != pn_seg) {
             // P_d = sum_h max(q, 0), N_d = sum_h min(q, 0), h ascending from +0
             pn_seg = b * Hkv + kvh;
