@@ -79,10 +79,12 @@ __device__ __forceinline__ int atomic_add_acq_rel_gpu(int *p, int v) {
     return old;
 }
 
-// Relaxed load at GPU scope (a counter other CTAs update atomically).
-__device__ __forceinline__ int ld_relaxed_s32(const int *p) {
+// Acquire load at GPU scope (a counter other CTAs update with release
+// semantics): what those CTAs published before their update is visible to
+// this thread's later reads.
+__device__ __forceinline__ int ld_acquire_s32(const int *p) {
     int v;
-    asm volatile("ld.relaxed.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
     return v;
 }
 

@@ -960,14 +960,15 @@ __global__ void __maxnreg__(PA_DECODE_MAXNREG)
                 }
             }
         }
+        float iw[4];  // one reciprocal per head (32 divisions per lane took about 5 us)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) iw[e] = W[e] > 0.f ? 1.f / W[e] : 0.f;
 #pragma unroll
         for (int r = 0; r < NSL; ++r) {
             const int d = (lane >> 1) + 16 * r;
 #pragma unroll
             for (int e = 0; e < 4; ++e)
-                if (h4 + e < G)
-                    ob[(h4 + e) * D + d] =
-                        __bfloat16_as_ushort(__float2bfloat16_rn(W[e] > 0.f ? O[r][e] / W[e] : 0.f));
+                if (h4 + e < G) ob[(h4 + e) * D + d] = __bfloat16_as_ushort(__float2bfloat16_rn(O[r][e] * iw[e]));
         }
     };
 
@@ -1031,7 +1032,7 @@ __global__ void __maxnreg__(PA_DECODE_MAXNREG)
         }
         // pieces of a split segment already counted (read while merging)
         int seen = 0;
-        if (!whole && lane == 0) seen = ld_relaxed_s32(a.counters + seg);
+        if (!whole && lane == 0) seen = ld_acquire_s32(a.counters + seg);
         float M[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
         float mc[NC][4], lc[NC][4];
 #pragma unroll
@@ -1072,6 +1073,11 @@ __global__ void __maxnreg__(PA_DECODE_MAXNREG)
             *read_done = inst + 1;  // the slots may be written again
         }
         const int b = seg / Hkv, kvh = seg % Hkv;
+        // one reciprocal per head, then products: 32 divisions per lane here
+        // held a merge for about 5 us
+        float inv[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) inv[e] = Ls[e] > 0.f ? 1.f / Ls[e] : 0.f;
         if (whole) {
             uint16_t *ob = a.out + (int64_t(b) * a.Hq + kvh * G) * D;
 #pragma unroll
@@ -1079,19 +1085,14 @@ __global__ void __maxnreg__(PA_DECODE_MAXNREG)
                 const int d = (lane >> 1) + 16 * r;
 #pragma unroll
                 for (int e = 0; e < 4; ++e)
-                    if (h4 + e < G)
-                        ob[(h4 + e) * D + d] =
-                            __bfloat16_as_ushort(__float2bfloat16_rn(Ls[e] > 0.f ? O[r][e] / Ls[e] : 0.f));
+                    if (h4 + e < G) ob[(h4 + e) * D + d] = __bfloat16_as_ushort(__float2bfloat16_rn(O[r][e] * inv[e]));
             }
             return true;
         }
         // this CTA's piece, normalised, and its log2-sum-exp
-        float inv[4], lse[4];
+        float lse[4];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            inv[e] = Ls[e] > 0.f ? 1.f / Ls[e] : 0.f;
-            lse[e] = Ls[e] > 0.f ? M[e] + log2f(Ls[e]) : -INFINITY;
-        }
+        for (int e = 0; e < 4; ++e) lse[e] = Ls[e] > 0.f ? M[e] + log2f(Ls[e]) : -INFINITY;
         float4 ox[NSL];
 #pragma unroll
         for (int r = 0; r < NSL; ++r)
@@ -1101,9 +1102,11 @@ __global__ void __maxnreg__(PA_DECODE_MAXNREG)
         seen = __shfl_sync(0xffffffffu, seen, 0);
         if (seen == npieces - 1) {
             // Every other piece has been counted, so this one completes the
-            // segment: combine from registers, without publishing it. The
-            // fence makes the counted pieces' partials visible to the loads.
-            __threadfence();
+            // segment: combine from registers, without publishing it. Lane 0
+            // read the count with acquire semantics, and the warp barrier
+            // orders every lane's loads of the counted pieces after it (a
+            // full GPU fence here held the merge warp for 5-9 us).
+            __syncwarp();
             combine(int64_t(seg) + w0, 1, a.out + (int64_t(seg / Hkv) * a.Hq + (seg % Hkv) * G) * D, s0, e0,
                     int(blockIdx.x) - w0, lse, ox);
             if (lane == 0) a.counters[seg] = 0;
