@@ -79,6 +79,10 @@ __device__ __forceinline__ int atomic_add_acq_rel_gpu(int *p, int v) {
     return old;
 }
 
+// 1 / x for x a normal power of two 2^k with k <= 126 (the result 2^-k is
+// normal too), exact: the exponent field is negated around the bias.
+__device__ __forceinline__ float rcp_pow2(float x) { return __int_as_float(0x7f000000 - __float_as_int(x)); }
+
 // Acquire load at GPU scope (a counter other CTAs update with release
 // semantics): what those CTAs published before their update is visible to
 // this thread's later reads.

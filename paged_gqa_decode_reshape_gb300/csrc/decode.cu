@@ -822,12 +822,16 @@ __global__ void __maxnreg__(PA_DECODE_MAXNREG)
             float vnew = vref;
             if (nva > 0) vnew = fmaxf(vnew, ca.y);
             if (nvb > 0) vnew = fmaxf(vnew, cb.y);
+            // the ratios are exact: the scales are powers of two between
+            // 2^-126 and 2^120 (the largest bf16 value over 448), so dividing
+            // by vnew is a product with its exact reciprocal
+            const float rv = rcp_pow2(vnew);
             if (vnew != vref) {
-                vr = __fdiv_rn(vref, vnew);
+                vr = vref * rv;
                 vref = vnew;
             }
-            if (nva > 0 && ca.y != vnew) ra = __fdiv_rn(ca.y, vnew);
-            if (nvb > 0 && cb.y != vnew) rb = __fdiv_rn(cb.y, vnew);
+            if (nva > 0 && ca.y != vnew) ra = ca.y * rv;
+            if (nvb > 0 && cb.y != vnew) rb = cb.y * rv;
         }
         const float x0 = (g < nva) ? s0[0] * sla : -INFINITY;
         const float x1 = (g < nva) ? s0[1] * sla : -INFINITY;
