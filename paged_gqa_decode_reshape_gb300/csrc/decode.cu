@@ -11,7 +11,8 @@
 // How (GB300 design):
 //  * Work list. Each (sequence, KV head) is a segment of items, one item per
 //    16-token KV block (dense: logical blocks 0..ceil(ctx/16)-1; sparse: the
-//    topk selection entries). The segments are concatenated and cut into
+//    topk selection entries); the E4M3 cache takes two consecutive blocks
+//    (or entries) per item, so that its items carry the bytes of a bf16 one. The segments are concatenated and cut into
 //    equal contiguous ranges, one per CTA of a persistent grid (one CTA per
 //    SM), so every SM streams the same number of KV bytes whatever the
 //    length mix.
@@ -24,9 +25,9 @@
 //    coordinate.
 //    The producer's lanes work on 8 items at a time (one lane per tile copy),
 //    so one warp instruction issues up to 32 TMA copies.
-//  * Math. Consumer warps take the ring's items in pairs, round-robin; the
-//    ring has 2 * consumers * pairs-in-flight stages so that every stage
-//    belongs to one consumer.
+//  * Math. Consumer warps take the ring's items in pairs (E4M3: one
+//    two-block item), round-robin; the ring's depth is a multiple of that
+//    round so that every stage belongs to one consumer.
 //    The GQA group's queries stay in registers as mma B fragments; S^T = K Q^T
 //    and O^T += V^T P^T run on bf16 mma.sync (m16n8k16) with the tokens as M
 //    and the (up to 8) heads of the group as N, so every K/V byte serves the
@@ -50,11 +51,12 @@ namespace pa {
 
 namespace {
 
-// Launch geometry (tuning knobs): consumer warps, and block pairs each
-// consumer has in flight. The ring has S = 2 * consumers * pairs stages, so
-// stage s always belongs to consumer (s / 2) % consumers: every consumer waits
-// on its own stages in order and an mbarrier parity wait can never be
-// answered by an older phase.
+// Launch geometry (tuning knobs): consumer warps, and item pairs (E4M3:
+// two-block items) each consumer has in flight. The ring has S = 2 *
+// consumers * pairs stages (E4M3: consumers * items), so stage s always
+// belongs to consumer (s / 2) % consumers (E4M3: s % consumers): every
+// consumer waits on its own stages in order and an mbarrier parity wait can
+// never be answered by an older phase.
 // Three consumers, the producer and the merge warp: five warps at 248
 // registers each carry the HBM rate and leave room for the selection's CTAs
 // beside a decode CTA. The multi-token kernel keeps one consumer per query
@@ -68,11 +70,10 @@ namespace {
 #ifndef PA_DECODE_PAIRS_MULTI
 #define PA_DECODE_PAIRS_MULTI 3
 #endif
-// E4M3 cache: consumer warps and pairs in flight (its items are half the
-// bytes, so more consumers keep the bytes in flight). Six consumers, the
-// producer and the merge warp are eight warps: two per register-file
-// partition, which holds the kernel's 255 registers per thread without spills
-// (a ninth warp would cap it at 168 and spill).
+// E4M3 cache: consumer warps and two-block items in flight per consumer. Six
+// consumers, the producer and the merge warp are eight warps: two per
+// register-file partition (a ninth warp would cap registers at 168 and
+// spill).
 #ifndef PA_DECODE_CONSUMERS_F8
 #define PA_DECODE_CONSUMERS_F8 6
 #endif
@@ -98,7 +99,11 @@ struct DecodeCfg {
     static_assert(!F8 || D == 128, "the E4M3 cache path is for head_dim 128");
     static constexpr int BS = kBlockSize;
     static constexpr int KT = BS * D * (F8 ? 1 : 2);  // bytes of one K (or V) tile
-    static constexpr int STAGE = 2 * KT;        // K + V
+    // KV blocks per item: the E4M3 cache takes two consecutive blocks of a
+    // segment per item, so that an item moves as many bytes as a bf16 one
+    // (the loop is bound per item at small items)
+    static constexpr int BPI = F8 ? 2 : 1;
+    static constexpr int STAGE = 2 * KT * BPI;  // K + V of the item's blocks
     static constexpr int NKK = D / 16;          // QK k-steps == PV m-tiles
     static constexpr int HALF = BS * 128;       // bytes of one 64-dim half tile
     static constexpr int PART = D * 8 + 8;      // floats per partial slot: O[D][8], lse[8]
@@ -109,13 +114,15 @@ struct DecodeCfg {
     static constexpr int THREADS = (NC + 1 + MW) * 32;
     static constexpr int PAIRS = MULTI ? PA_DECODE_PAIRS_MULTI : PA_DECODE_PAIRS;
     static constexpr int R = F8 ? PA_DECODE_PAIRS_F8 : (D == 128 ? PAIRS : 2 * PAIRS);
-    static constexpr int S = 2 * NC * R;        // ring stages
+    // stages per consumer step: bf16 takes items in pairs, E4M3 one (two-block) item
+    static constexpr int SPS = F8 ? 1 : 2;
+    static constexpr int S = SPS * NC * R;      // ring stages
     static constexpr int SCR = D * 8 + 16;      // floats per consumer merge slot: acc[D][8], m[8], l[8]
     static constexpr size_t off_bars = size_t(S) * STAGE;
     static constexpr size_t off_info = off_bars + size_t(S) * 16;
-    // E4M3 cache: each stage's K and V scale (float2) after the item info
+    // E4M3 cache: each stage's K and V scales (float4: the two blocks) after the item info
     static constexpr size_t off_iscale = off_info + size_t(S) * 8;
-    static constexpr size_t off_scr = off_iscale + (F8 ? size_t(S) * 8 : 0);
+    static constexpr size_t off_scr = off_iscale + (F8 ? size_t(S) * 16 : 0);
     static constexpr size_t off_flags = off_scr + size_t(NC) * SCR * 4;
     static constexpr size_t off_pre = off_flags + 64;
     // per-row item prefix (PB + 1 entries); multi-token rows then add each
@@ -151,7 +158,7 @@ __global__ void __maxnreg__(PA_DECODE_MAXNREG)
     static_assert(!BSC || (F8 && !MULTI), "per-block scales: the E4M3 cache, one query row");
     constexpr bool PSC = F8 && BSC;  // per-item scales
     const bool SPARSE = !MULTI && a.topk > 0;
-    constexpr int BS = C::BS, NC = C::NC, S = C::S, NKK = C::NKK;
+    constexpr int BS = C::BS, NC = C::NC, S = C::S, NKK = C::NKK, BPI = C::BPI;
 
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
@@ -160,7 +167,7 @@ __global__ void __maxnreg__(PA_DECODE_MAXNREG)
     const uint32_t full_bar = base + uint32_t(C::off_bars);
     const uint32_t empty_bar = full_bar + S * 8;
     int2 *info = reinterpret_cast<int2 *>(bp + C::off_info);
-    float2 *iscale = reinterpret_cast<float2 *>(bp + C::off_iscale);  // E4M3 cache only
+    float4 *iscale = reinterpret_cast<float4 *>(bp + C::off_iscale);  // E4M3 cache only
     float *scr = reinterpret_cast<float *>(bp + C::off_scr);
     volatile int *flags = reinterpret_cast<volatile int *>(bp + C::off_flags);
     const uint32_t merge_bar = base + uint32_t(C::off_flags) + 16;  // consumers' deposits (count NC)
@@ -225,7 +232,7 @@ __global__ void __maxnreg__(PA_DECODE_MAXNREG)
             c = min(max(__ldg(a.ctx + v), 0), max_tok);
         }
         const int nblk = (c + BS - 1) / BS;
-        return SPARSE ? (nblk > 0 ? a.topk : 0) : nblk;
+        return SPARSE ? (nblk > 0 ? (a.topk + BPI - 1) / BPI : 0) : (nblk + BPI - 1) / BPI;
     };
     auto scan_pre = [&](int n) {  // pre[1..n] -> inclusive prefix sums (warp 0)
         if (warp == 0) {
@@ -290,7 +297,7 @@ __global__ void __maxnreg__(PA_DECODE_MAXNREG)
                 const int v = v0 + u * C::THREADS;
                 if (v < NR) {
                     const int nblk = (min(max(c8[u], 0), max_tok) + BS - 1) / BS;
-                    pre[v + 1] = SPARSE ? (nblk > 0 ? a.topk : 0) : nblk;
+                    pre[v + 1] = SPARSE ? (nblk > 0 ? (a.topk + BPI - 1) / BPI : 0) : (nblk + BPI - 1) / BPI;
                 }
             }
         }
@@ -366,8 +373,9 @@ __global__ void __maxnreg__(PA_DECODE_MAXNREG)
             const int seg = b * Hkv + kvh;
             const int64_t s0 = int64_t(Hkv) * pre[b] + int64_t(kvh) * nseg;
             const int64_t e0 = s0 + nseg;
-            const int i0 = int(p - s0), i1 = int(min(e0, pos1) - s0);  // this CTA's entries
-            int32_t *mine = sel_s + (p - pos0) - i0;                   // entry r -> mine[r], r in [i0, i1)
+            // this CTA's entries [i0, i1) (BPI per item): entry r -> mine[r]
+            const int i0 = BPI * int(p - s0), i1 = BPI * int(min(e0, pos1) - s0);
+            int32_t *mine = sel_s + BPI * (p - pos0) - i0;
             const bool writer = s0 >= pos0;                            // holds entry 0: writes the row
             int32_t *orow = a.sel_out + int64_t(seg) * a.topk;
             const float *srow = a.scores + int64_t(seg) * a.MBS;
@@ -409,12 +417,17 @@ __global__ void __maxnreg__(PA_DECODE_MAXNREG)
         // item and starts loading ctx (and the selection entry for sparse);
         // one window later stage B starts loading the block-table entry; one
         // window after that the items are issued.
+        // an item's logical blocks j, j1 (j1: the second block of an E4M3
+        // item, -1 if none), their physical blocks and their K and V scales
         struct Win {
             int seg, j, phys, ctxv;
             float sk, sv;  // E4M3 cache: the item's K and V scale
+            int j1, phys1;
+            float sk1, sv1;
         };
+        const Win none{-1, -1, -1, 0, 0.f, 0.f, -1, -1, 0.f, 0.f};
         auto stage_c = [&](int k0) -> Win {
-            Win it{-1, -1, -1, 0, 0.f, 0.f};
+            Win it = none;
             const int k = k0 + lane;
             if (k >= n_items) return it;
             const int64_t p = pos0 + k;
@@ -430,7 +443,22 @@ __global__ void __maxnreg__(PA_DECODE_MAXNREG)
             } else {
                 it.ctxv = __ldg(a.ctx + b);
             }
-            it.j = !SPARSE ? i : a.scores ? sel_s[k] : __ldg(a.sel + (int64_t(b) * Hkv + kvh) * a.topk + i);
+            if constexpr (BPI == 1) {
+                it.j = !SPARSE ? i : a.scores ? sel_s[k] : __ldg(a.sel + (int64_t(b) * Hkv + kvh) * a.topk + i);
+            } else {  // entries e, e + 1 of the segment (blocks for dense, selection entries for sparse)
+                const int e = BPI * i;
+                const int32_t *srow = a.sel + (int64_t(b) * Hkv + kvh) * a.topk;
+                if (!SPARSE) {
+                    it.j = e;
+                    it.j1 = e + 1;
+                } else if (a.scores) {
+                    it.j = sel_s[BPI * k];
+                    it.j1 = e + 1 < a.topk ? sel_s[BPI * k + 1] : -1;
+                } else {
+                    it.j = __ldg(srow + e);
+                    it.j1 = e + 1 < a.topk ? __ldg(srow + e + 1) : -1;
+                }
+            }
             return it;
         };
         auto stage_b = [&](Win &it) {
@@ -438,13 +466,20 @@ __global__ void __maxnreg__(PA_DECODE_MAXNREG)
             const int b = it.seg / Hkv;
             const int s = MULTI ? int(seq_of[b]) : b;  // the row's sequence
             it.phys = (it.j >= 0 && it.j < a.MBS) ? __ldg(a.bt + int64_t(s) * a.MBS + it.j) : -1;
+            if (BPI > 1) it.phys1 = (it.j1 >= 0 && it.j1 < a.MBS) ? __ldg(a.bt + int64_t(s) * a.MBS + it.j1) : -1;
         };
         // per-block scales: the item's K and V scale of its (physical block,
         // KV head); the load depends on the block-table entry, so it runs one
         // window after stage B
         auto stage_s = [&](Win &it) {
             if constexpr (PSC) {
-                if (it.seg < 0 || it.phys < 0 || int64_t(it.phys) >= a.NB) return;
+                if (it.seg < 0) return;
+                if (it.phys1 >= 0 && int64_t(it.phys1) < a.NB) {
+                    const int64_t si = int64_t(it.phys1) * Hkv + it.seg % Hkv;
+                    it.sk1 = __ldg(a.k_scale + si);
+                    it.sv1 = __ldg(a.v_scale + si);
+                }
+                if (it.phys < 0 || int64_t(it.phys) >= a.NB) return;
                 const int64_t si = int64_t(it.phys) * Hkv + it.seg % Hkv;
                 it.sk = __ldg(a.k_scale + si);
                 it.sv = __ldg(a.v_scale + si);
@@ -501,7 +536,7 @@ __global__ void __maxnreg__(PA_DECODE_MAXNREG)
         // per-block scales: a fourth window, so the scale loads (stage S) have
         // a window to land in: wa issued, wb scales, wc block-table entries,
         // wd context and selection
-        Win wd{-1, -1, -1, 0, 0.f, 0.f};
+        Win wd = none;
         if constexpr (PSC) {
             stage_b(wc);
             wd = stage_c(96);
@@ -515,13 +550,13 @@ __global__ void __maxnreg__(PA_DECODE_MAXNREG)
         unsigned fail_armed = 0;  // after a failure: leader lanes whose item was armed
         // IPS items per step, LPI lanes per item: lane = LPI * item + part,
         // part = which tile copy (bf16: K and V in two 64-dim halves each;
-        // E4M3: one K and one V copy, so twice the items per step)
-        constexpr int LPI = F8 ? 2 : 4, IPS = 32 / LPI;
+        // E4M3: K and V of each of the item's two blocks)
+        constexpr int LPI = 4, IPS = 32 / LPI;
         // a step's items take distinct stages, and each waits only for items
         // of earlier steps to leave its stage (no two items of a step alias)
         static_assert(IPS < S, "items per producer step must stay below the ring depth");
         const int it = lane / LPI, part = lane % LPI;
-        constexpr int PARTS = F8 ? 2 : 2 * (D / 64);  // K and V (bf16: 64-dim halves)
+        constexpr int PARTS = F8 ? 2 * BPI : 2 * (D / 64);  // K and V (bf16: 64-dim halves)
         for (int k0 = 0; k0 < n_items; k0 += IPS) {
             if (k0 >= a.stop_item) break;  // failure tests: the stages from here on are never armed
             if (k0 >= wbase + 32) {
@@ -544,16 +579,26 @@ __global__ void __maxnreg__(PA_DECODE_MAXNREG)
             const int j = __shfl_sync(0xffffffffu, wa.j, k & 31);
             const int ph = __shfl_sync(0xffffffffu, wa.phys, k & 31);
             const int cv = __shfl_sync(0xffffffffu, wa.ctxv, k & 31);
-            float sk = 0.f, sv = 0.f;
+            float sk = 0.f, sv = 0.f, sk1 = 0.f, sv1 = 0.f;
             if constexpr (PSC) {
                 sk = __shfl_sync(0xffffffffu, wa.sk, k & 31);
                 sv = __shfl_sync(0xffffffffu, wa.sv, k & 31);
+                sk1 = __shfl_sync(0xffffffffu, wa.sk1, k & 31);
+                sv1 = __shfl_sync(0xffffffffu, wa.sv1, k & 31);
             }
             const bool live = k < n_items;
             const int c = min(max(cv, 0), max_tok);
             const int nblk = (c + BS - 1) / BS;
             const bool valid = live && j >= 0 && j < nblk && ph >= 0 && int64_t(ph) < a.NB;
             const int nv = valid ? min(BS, c - j * BS) : 0;
+            // E4M3: the item's second block (valid tokens nv1; info packs nv + nv1 * 256)
+            int ph1 = -1, nv1 = 0;
+            if constexpr (BPI > 1) {
+                const int j1 = __shfl_sync(0xffffffffu, wa.j1, k & 31);
+                ph1 = __shfl_sync(0xffffffffu, wa.phys1, k & 31);
+                const bool valid1 = live && j1 >= 0 && j1 < nblk && ph1 >= 0 && int64_t(ph1) < a.NB;
+                nv1 = valid1 ? min(BS, c - j1 * BS) : 0;
+            }
             const int st = k % S;
             const uint32_t fb = full_bar + st * 8;
             // the item's leader lane waits for its stage to be released, then arms it
@@ -562,9 +607,11 @@ __global__ void __maxnreg__(PA_DECODE_MAXNREG)
                 if (k >= S && !mbar_wait_bounded(empty_bar + st * 8, ((k / S) & 1) ^ 1, a.wait_ns)) {
                     ok = 0;
                 } else {
-                    info[st] = make_int2(MULTI ? j : seg, nv);  // MULTI: consumers mask per query row
-                    if constexpr (PSC) iscale[st] = make_float2(sk, sv);
-                    if (nv > 0) mbar_arrive_expect_tx(fb, C::STAGE);
+                    info[st] = make_int2(MULTI ? j : seg, nv + (nv1 << 8));  // MULTI: consumers mask per query row
+                    if constexpr (PSC) iscale[st] = make_float4(sk, sv, sk1, sv1);
+                    const uint32_t bytes = BPI > 1 ? (nv > 0 ? 2u * C::KT : 0u) + (nv1 > 0 ? 2u * C::KT : 0u)
+                                                   : (nv > 0 ? uint32_t(C::STAGE) : 0u);
+                    if (bytes > 0) mbar_arrive_expect_tx(fb, bytes);
                     else mbar_arrive(fb);
                 }
             }
@@ -588,23 +635,27 @@ __global__ void __maxnreg__(PA_DECODE_MAXNREG)
                     }
                 }
             }
-            if (live && ok && nv > 0 && part < PARTS) {
-                if constexpr (F8) {
-                    // K: one [16 tokens x 128 dims] byte box (tensor map); V:
-                    // the block's [128 dims x 16 tokens] byte matrix of this KV head
+            if constexpr (F8) {
+                // parts: K and V of block 0, then of block 1. K: one [16 tokens
+                // x 128 dims] byte box (tensor map); V: the block's [128 dims x
+                // 16 tokens] byte matrix of this KV head, 2 KB of contiguous
+                // bytes: one plain bulk copy
+                const int blk = part >> 1;
+                const int phb = blk ? ph1 : ph;
+                if (live && ok && part < PARTS && (blk ? nv1 : nv) > 0) {
                     const uint32_t dst = base + st * C::STAGE + part * C::KT;
-                    if (part == 0) {
-                        tma_load_4d(dst, &tm_k, fb, 0, seg % Hkv, 0, ph, policy);
-                    } else {  // the V tile is 2 KB of contiguous bytes: one plain bulk copy
-                        const uint8_t *src = a.v8 + (int64_t(ph) * Hkv + seg % Hkv) * int64_t(C::KT);
+                    if ((part & 1) == 0) {
+                        tma_load_4d(dst, &tm_k, fb, 0, seg % Hkv, 0, phb, policy);
+                    } else {
+                        const uint8_t *src = a.v8 + (int64_t(phb) * Hkv + seg % Hkv) * int64_t(C::KT);
                         bulk_load_1d(dst, src, uint32_t(C::KT), fb, policy);
                     }
-                } else {
-                    constexpr int HV = D / 64;             // 64-dim halves per tile
-                    const int tsel = part / HV, hf = part % HV;  // 0: K, 1: V
-                    const uint32_t dst = base + st * C::STAGE + tsel * C::KT + hf * C::HALF;
-                    tma_load_4d(dst, tsel ? &tm_v : &tm_k, fb, hf * 64, seg % Hkv, 0, ph, policy);
                 }
+            } else if (live && ok && nv > 0 && part < PARTS) {
+                constexpr int HV = D / 64;                   // 64-dim halves per tile
+                const int tsel = part / HV, hf = part % HV;  // 0: K, 1: V
+                const uint32_t dst = base + st * C::STAGE + tsel * C::KT + hf * C::HALF;
+                tma_load_4d(dst, tsel ? &tm_v : &tm_k, fb, hf * 64, seg % Hkv, 0, ph, policy);
             }
             if (!__all_sync(0xffffffffu, ok)) {
                 // a stage was never released: give up (consumers skip their
@@ -796,10 +847,10 @@ __global__ void __maxnreg__(PA_DECODE_MAXNREG)
         j = info[k % S].x;
         return nv;
     };
-    // one online-softmax step over up to two staged blocks (nv == 0: no block)
-    auto step = [&](int ka, int nva, int kb_, int nvb) {
-        const uint32_t s0a = base + (ka % S) * C::STAGE;
-        const uint32_t s1a = base + (kb_ % S) * C::STAGE;
+    // one online-softmax step over up to two staged blocks at shared-memory
+    // addresses s0a, s1a (K tile, then V tile; nv == 0: no block), with their
+    // K and V scales ca, cb (per-block scales only)
+    auto step = [&](uint32_t s0a, int nva, float2 ca, uint32_t s1a, int nvb, float2 cb) {
         float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
         float sla = scale_log2, slb = scale_log2;  // per-block scales: times the blocks' K scales
         float ra = 1.f, rb = 1.f, vr = 1.f;        // per-block scales: V scale ratios, warp-uniform
@@ -816,7 +867,6 @@ __global__ void __maxnreg__(PA_DECODE_MAXNREG)
             // rescales acc by vref / sv first; a block's P enters the PV
             // product times sv / vref (a power of two, so the f16 product is
             // exact down to the f16 subnormal range).
-            const float2 ca = iscale[ka % S], cb = iscale[kb_ % S];
             sla = scale_log2 * ca.x;
             slb = scale_log2 * cb.x;
             float vnew = vref;
@@ -1226,7 +1276,8 @@ __global__ void __maxnreg__(PA_DECODE_MAXNREG)
                 int nvb = (kb > ka) ? wait_full_j(kb, jb) : 0;
                 nva = act ? min(nva, max(lim - ja * BS, 0)) : 0;
                 nvb = act ? min(nvb, max(lim - jb * BS, 0)) : 0;
-                if (nva > 0 || nvb > 0) step(ka, nva, kb, nvb);
+                if (nva > 0 || nvb > 0)
+                    step(base + (ka % S) * C::STAGE, nva, float2{}, base + (kb % S) * C::STAGE, nvb, float2{});
                 __syncwarp();
                 if (lane == 0) {
                     mbar_arrive(empty_bar + (ka % S) * 8);
@@ -1274,19 +1325,35 @@ __global__ void __maxnreg__(PA_DECODE_MAXNREG)
             continue;
         }
         load_q(seg, b);
-        // item pairs (2q, 2q+1) of this segment owned by this warp: q % NC == c_id
-        int q = ks0 >> 1;
-        q += (c_id - q % NC + NC) % NC;
-        for (; 2 * q < ks1; q += NC) {
-            const int ka = max(2 * q, ks0);
-            const int kb = min(2 * q + 1, ks1 - 1);
-            const int nva = wait_full(ka);
-            const int nvb = (kb > ka) ? wait_full(kb) : 0;
-            if (nva > 0 || nvb > 0) step(ka, nva, kb, nvb);
-            __syncwarp();
-            if (lane == 0) {
-                mbar_arrive(empty_bar + (ka % S) * 8);
-                if (kb > ka) mbar_arrive(empty_bar + (kb % S) * 8);
+        if constexpr (F8) {
+            // two-block items of this segment owned by this warp: k % NC == c_id
+            for (int k = ks0 + (c_id - ks0 % NC + NC) % NC; k < ks1; k += NC) {
+                const int nvp = wait_full(k);
+                const int nva = nvp & 255, nvb = nvp >> 8;
+                const uint32_t sa = base + (k % S) * C::STAGE;
+                float4 sc4 = make_float4(0.f, 0.f, 0.f, 0.f);
+                if constexpr (PSC) sc4 = iscale[k % S];
+                if (nva > 0 || nvb > 0)
+                    step(sa, nva, make_float2(sc4.x, sc4.y), sa + 2 * C::KT, nvb, make_float2(sc4.z, sc4.w));
+                __syncwarp();
+                if (lane == 0) mbar_arrive(empty_bar + (k % S) * 8);
+            }
+        } else {
+            // item pairs (2q, 2q+1) of this segment owned by this warp: q % NC == c_id
+            int q = ks0 >> 1;
+            q += (c_id - q % NC + NC) % NC;
+            for (; 2 * q < ks1; q += NC) {
+                const int ka = max(2 * q, ks0);
+                const int kb = min(2 * q + 1, ks1 - 1);
+                const int nva = wait_full(ka);
+                const int nvb = (kb > ka) ? wait_full(kb) : 0;
+                if (nva > 0 || nvb > 0)
+                    step(base + (ka % S) * C::STAGE, nva, float2{}, base + (kb % S) * C::STAGE, nvb, float2{});
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(empty_bar + (ka % S) * 8);
+                    if (kb > ka) mbar_arrive(empty_bar + (kb % S) * 8);
+                }
             }
         }
         deposit(inst++);
@@ -1366,9 +1433,10 @@ cudaError_t launch_t(const CUtensorMap &tm_k, const CUtensorMap &tm_v, const Dec
         // waiting for the last of them (quest_8k step 83.6 -> 77.3 us).
         const int64_t segs = int64_t(a.B) * a.Hkv;
         const int budget = (max_ctas > 0 && max_ctas < grid) ? max_ctas : (segs <= grid / 2 ? grid / 2 : grid);
+        const int tk = (a.topk + C::BPI - 1) / C::BPI;  // items per segment
         if (segs * a.topk < int64_t(grid) * kSparseLargeItems) {
             int64_t c = 1;
-            while (a.topk % (2 * c) == 0 && a.topk / (2 * c) >= kSparseMinItems && segs * 2 * c <= budget)
+            while (tk % (2 * c) == 0 && a.topk / (2 * c) >= kSparseMinItems && segs * 2 * c <= budget)
                 c *= 2;
             if (segs * c <= budget) {
                 grid = int(segs * c);
@@ -1386,10 +1454,10 @@ cudaError_t launch_t(const CUtensorMap &tm_k, const CUtensorMap &tm_v, const Dec
     }
     if (SPARSE && a.scores) {
         // fused Quest decode: room for the CTA's selection entries (at most
-        // ceil(items / CTAs), items <= segments * topk)
+        // BPI * ceil(items / CTAs), items <= segments * ceil(topk / BPI))
         DecodeArgs f = a;
-        const int64_t items = int64_t(a.B) * a.Hkv * a.topk;
-        const int64_t cap = (items + grid - 1) / grid;
+        const int64_t items = int64_t(a.B) * a.Hkv * ((a.topk + C::BPI - 1) / C::BPI);
+        const int64_t cap = C::BPI * ((items + grid - 1) / grid);
         const size_t fsmem = C::smem_bytes_sel(a.B, int(cap));
         if (cap > (int64_t(1) << 20) || fsmem > geo.smem) return cudaErrorInvalidConfiguration;
         f.nsel_cap = int(cap);
