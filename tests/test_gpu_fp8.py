@@ -22,6 +22,9 @@ SMALL = {
     "mixed_small": ("mixed_b128", dict(batch=16, ctx_scale=0.02, topk=8)),
     "long_small": ("long_40k", dict(batch=2, ctx_scale=0.02, topk=16)),
     "dense_small": ("dense_b32", dict(batch=6, ctx_scale=0.05, topk=8)),
+    # odd topk: a segment's last two-block item of the 8-bit decode holds one entry
+    "odd_topk": ("quest_8k", dict(batch=4, ctx_scale=0.05, topk=7)),
+    "odd_topk_long": ("long_40k", dict(batch=2, ctx_scale=0.02, topk=15)),
 }
 
 

@@ -114,10 +114,14 @@ def test_rows_longer_than_the_key_cache():
     run_compare(w, budgets=(0,))
 
 
-def test_fp8_cache():
+@pytest.mark.parametrize("topk,max_ctas", [(24, 0), (23, 0), (23, 5)])
+def test_fp8_cache(topk, max_ctas):
+    """The 8-bit cache (two blocks per ring item): an odd topk leaves a
+    segment's last item one entry, and a small CTA budget puts several
+    segments, and ranges that start mid-segment, in one CTA."""
     import paged_gqa_decode_reshape_gb300 as pg
     from tests.test_gpu_fp8 import Fp8Case
-    w = workloads.make("quest_8k", batch=4, ctx_scale=0.25, topk=24)
+    w = workloads.make("quest_8k", batch=4, ctx_scale=0.25, topk=topk)
     c = Fp8Case(w)
     kmin, kmax = c.write_step()
     want_sel = oracle.quest_select_kernel_order_fp8(w.q, kmin, kmax, w.block_tables, w.context_lens, w.BS,
@@ -129,7 +133,7 @@ def test_fp8_cache():
     sel = torch.empty((w.B, w.Hkv, w.topk), dtype=torch.int32, device=c.q.device)
     out = torch.empty_like(c.out)
     pg.quest_decode_fp8(out, sel, c.q, c.kmin, c.kmax, c.kc, c.vc, c.ks, c.vs, c.bt, c.ctx, w.topk, w.scale,
-                        workspace=ws)
+                        max_ctas=max_ctas, workspace=ws)
     np.testing.assert_array_equal(sel.cpu().numpy(), want_sel)
     assert_close_attention(to_host_f64(out), want, "fp8 quest_decode")
     assert pg.pa_workspace_status(ws) == 0
