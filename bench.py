@@ -3,9 +3,9 @@
 One step = one pass of the whole path over one batch of synthetic input, every
 call through the C ABI: ReshapeAndCache + Quest metadata update (one launch),
 then the dense GQA paged decode (split-KV + combine) on the calling stream
-and, beside it on a second stream, the Quest path: block scores, then top-K
-and sparse decode in one launch (quest_decode; step_runner; --serial runs
-them one after another).
+and, beside it on a second stream, the Quest path: block scores and top-K,
+then the sparse decode on SMs the dense decode leaves to it (step_runner;
+--serial runs write, quest_decode and the dense decode one after another).
 Inputs are resident in HBM before timing; the L2 is flushed (a 512 MiB write)
 before every step, outside the timed events. The step time comes from one
 event pair per step; a second pass of the same steps, on one stream with an
@@ -278,14 +278,47 @@ class Step:
                                        self.bt, self.ctx, w.topk, w.scale, max_ctas=max_ctas,
                                        workspace=self.ws_quest)
 
+    def split_ctas(self) -> int:
+        """SMs the two-stream step keeps for the sparse decode (bf16 cache; 0:
+        none, the 8-bit dense call has no CTA budget). The dense decode runs
+        on the others from the step's start, so the sparse decode need not
+        wait for its CTAs. X = 1.8 x SMs x the sparse share of the two decode
+        calls' KV tokens, to a multiple of 8, at least 16 and at most half
+        the SMs: the sparse share of the SMs, raised because the sparse call
+        starts after the selection. Measured against every X from 8 to 56 on
+        quest_8k, long_40k, dense_b32 and mixed_b128, the rule picks the
+        fastest step on each."""
+        if self.kv != "bf16" or self.qlen > 1:
+            return 0
+        import numpy as np
+        w = self.w
+        ctx = np.minimum(np.asarray(w.context_lens, dtype=np.int64), w.MBS * w.BS)
+        dense = float(ctx.sum())
+        sparse = float(np.minimum(ctx, w.topk * w.BS).sum())
+        x = int(round(1.8 * self.sms * sparse / max(dense + sparse, 1.0) / 8.0)) * 8
+        return max(16, min(x, self.sms // 2))
+
+    def dense_beside(self):
+        """The dense decode as the two-stream step runs it: on the SMs the
+        sparse decode does not keep (pa_decode_budget), else pa_decode."""
+        x = self.split_ctas()
+        c = self.calls()[CALL_NAMES.index("dense")]
+        if x == 0:
+            return c
+        pg, w = self.pg, self.w
+        return lambda: pg.pa_decode_budget(self.out, self.q, self.kc, self.vc, self.bt, self.ctx, w.scale,
+                                           self.sms - x, workspace=self.ws)
+
     def quest_beside(self):
         """The Quest path as the two-stream step runs it, beside the dense
         decode: quest_select_topk, whose CTAs fit on the SMs beside the dense
-        decode's, then the sparse decode on at most half the SMs (its CTAs
-        need a whole SM's shared memory, start as the dense CTAs finish and
-        need not wait for the last of them). quest_decode would put its top-K
-        after the dense decode instead of beside it."""
-        pg, w, budget = self.pg, self.w, self.sms // 2
+        decode's, then the sparse decode on the SMs split_ctas() keeps for it
+        (8-bit cache: at most half the SMs; its CTAs need a whole SM's shared
+        memory, start as the dense CTAs finish and need not wait for the last
+        of them). quest_decode would put its top-K after the dense decode
+        instead of beside it."""
+        pg, w = self.pg, self.w
+        budget = self.split_ctas() or self.sms // 2
         select = self.calls()[CALL_NAMES.index("select")]
         if self.kv != "bf16":
             fn = pg.quest_sparse_decode_fp8_budget if self.kv == "fp8" else pg.quest_sparse_decode_fp8_block
@@ -495,20 +528,22 @@ def max_over_ranks(values, pgroup):
     return [float(v) for v in t]
 
 
-def step_runner(torch, step, serial: bool, quest=None):
+def step_runner(torch, step, serial: bool, quest=None, dense=None):
     """One step: the write path, the Quest path and the dense decode. Serial:
     write, quest_decode, dense decode on one stream. Else the Quest path runs
     on a second stream forked after the write path and joined at the end of
-    the step (step.quest_beside(): the selection's CTAs run on the SMs beside
-    the dense decode's, since a decode CTA's warps (at most 184 registers
-    each) leave room in each of the SM's register-file partitions; the
-    sparse decode's CTAs, which need a whole SM's shared memory, take SMs as
-    the dense decode's CTAs finish, on at most half the SMs). Neither path
-    reads the other's output, and the two
-    decode calls have their own workspaces. `quest` overrides the Quest-path
+    the step: the selection's CTAs run on the SMs beside the dense decode's
+    (a decode CTA's warps, at most 184 registers each, leave room in each of
+    the SM's register-file partitions), and the sparse decode's CTAs, which
+    need a whole SM's shared memory, run on the SMs the dense decode leaves
+    free (step.split_ctas(); 8-bit cache: as the dense CTAs finish). Neither
+    path reads the other's output, and the two decode calls have their own
+    workspaces. `quest` and `dense` override the Quest-path and the dense
     call in either mode."""
     c = dict(zip(CALL_NAMES, step.calls()))
-    write, dense = c["write"], c["dense"]
+    write = c["write"]
+    if dense is None:
+        dense = c["dense"] if serial else step.dense_beside()
     if serial:
         q = quest or c["quest"]
 
@@ -596,10 +631,14 @@ def config_of(w, args, world: int) -> dict:
         "context_lens_mean": round(float(w.context_lens.mean()), 1),
         "context_lens_max": int(w.context_lens.max()), "pool_blocks": w.NB,
         "kv_pool_bytes": int(2 * w.key_cache.nbytes // (2 if fp8 else 1)),
-        "step": ("quest_reshape_and_cache{0} (ReshapeAndCache + metadata update) + "
-                 "quest_select_topk{0} + quest_sparse_decode{0}_budget (half the SMs) on a second stream "
-                 "beside pa_decode{0}; --serial: quest_decode{0} then pa_decode{0}").format(
-                     "" if args.kv == "bf16" else "_" + args.kv),
+        "step": ("quest_reshape_and_cache{0} (ReshapeAndCache + metadata update), then on a second "
+                 "stream quest_select_topk{0} + quest_sparse_decode{0}_budget beside {1}; {2}; "
+                 "--serial: quest_decode{0} then pa_decode{0}").format(
+                     "" if args.kv == "bf16" else "_" + args.kv,
+                     "pa_decode_budget" if args.kv == "bf16" and args.qlen == 1 else "pa_decode" +
+                     ("" if args.kv == "bf16" else "_" + args.kv),
+                     "the SMs split between the two decode calls by their KV token shares (split_ctas)"
+                     if args.kv == "bf16" and args.qlen == 1 else "the sparse call on at most half the SMs"),
         "l2": "inputs resident; L2 flushed before every timed sample",
         "parallelism": f"replicas x{world}",
     }
@@ -712,9 +751,11 @@ def measure(torch, pg, w, dev, args, flush, pgroup):
         e1.record(stream)
         e1.synchronize()
         e2e_ms.append(e0.elapsed_time(e1))
+    split, sms = (step.split_ctas() if not args.serial else 0), step.sms
     del graph, step
     torch.cuda.synchronize(dev)
     return dict(nb=nb, step_ms=step_ms, per_call=per_call, present=present, graph_ms=graph_ms, e2e_ms=e2e_ms,
+                split=split, sms=sms,
                 h2d=int(h_in.numel()), d2h=int(h_out.numel()), clocks=clocks, wall=wall)
 
 
@@ -868,6 +909,8 @@ def main():
         "graph": {"value": round(job_throughput(world, nb.total, graph_ms_max), 2), "unit": UNIT,
                   "ms_per_step": round(graph_ms_max, 5), "ms_stats": stats_ms(m["graph_ms"]),
                   "how": "the step's calls captured once in a CUDA graph, replayed K times"},
+        "two_stream_split": ({"sparse_ctas": m["split"], "dense_ctas": m["sms"] - m["split"]} if m["split"]
+                             else None),
         "gpu_launches": int(K * (STEP_LAUNCHES_SERIAL if args.serial else STEP_LAUNCHES)),
         "wall_s_timed_region": round(m["wall"], 4),
         "clocks": m["clocks"],

@@ -49,7 +49,8 @@ def test_two_stream_step_matches_one_stream(name, kw, kv):
     st = bench.Step(w, torch.device("cuda:0"), kv)
     results = []
     for serial in (True, False, True, False):
-        run = bench.step_runner(torch, st, serial, quest=st.quest_beside())  # the same grids in both orders
+        # the same grids in both orders
+        run = bench.step_runner(torch, st, serial, quest=st.quest_beside(), dense=st.dense_beside())
         for _ in range(2):  # the write path is idempotent: the same tokens into the same slots
             st.out_buf.zero_()
             run()
