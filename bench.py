@@ -279,8 +279,8 @@ class Step:
                                        workspace=self.ws_quest)
 
     def split_ctas(self) -> int:
-        """SMs the two-stream step keeps for the sparse decode (bf16 cache; 0:
-        none, the 8-bit dense call has no CTA budget). The dense decode runs
+        """SMs the two-stream step keeps for the sparse decode (0: none, for
+        multi-token rows). The dense decode runs
         on the others from the step's start, so the sparse decode need not
         wait for its CTAs. X = 1.8 x SMs x the sparse share of the two decode
         calls' KV tokens, to a multiple of 8, at least 16 and at most half
@@ -288,7 +288,7 @@ class Step:
         starts after the selection. Measured against every X from 8 to 56 on
         quest_8k, long_40k, dense_b32 and mixed_b128, the rule picks the
         fastest step on each."""
-        if self.kv != "bf16" or self.qlen > 1:
+        if self.qlen > 1:
             return 0
         import numpy as np
         w = self.w
@@ -305,18 +305,20 @@ class Step:
         c = self.calls()[CALL_NAMES.index("dense")]
         if x == 0:
             return c
-        pg, w = self.pg, self.w
-        return lambda: pg.pa_decode_budget(self.out, self.q, self.kc, self.vc, self.bt, self.ctx, w.scale,
-                                           self.sms - x, workspace=self.ws)
+        pg, w, n = self.pg, self.w, self.sms - x
+        if self.kv != "bf16":
+            fn = pg.pa_decode_fp8_budget if self.kv == "fp8" else pg.pa_decode_fp8_block_budget
+            return lambda: fn(self.out, self.q, self.kc, self.vc, self.k_scale, self.v_scale, self.bt, self.ctx,
+                              w.scale, n, workspace=self.ws)
+        return lambda: pg.pa_decode_budget(self.out, self.q, self.kc, self.vc, self.bt, self.ctx, w.scale, n,
+                                           workspace=self.ws)
 
     def quest_beside(self):
         """The Quest path as the two-stream step runs it, beside the dense
         decode: quest_select_topk, whose CTAs fit on the SMs beside the dense
         decode's, then the sparse decode on the SMs split_ctas() keeps for it
-        (8-bit cache: at most half the SMs; its CTAs need a whole SM's shared
-        memory, start as the dense CTAs finish and need not wait for the last
-        of them). quest_decode would put its top-K after the dense decode
-        instead of beside it."""
+        (its CTAs need a whole SM's shared memory). quest_decode would put its
+        top-K after the dense decode instead of beside it."""
         pg, w = self.pg, self.w
         budget = self.split_ctas() or self.sms // 2
         select = self.calls()[CALL_NAMES.index("select")]
@@ -536,7 +538,7 @@ def step_runner(torch, step, serial: bool, quest=None, dense=None):
     (a decode CTA's warps, at most 184 registers each, leave room in each of
     the SM's register-file partitions), and the sparse decode's CTAs, which
     need a whole SM's shared memory, run on the SMs the dense decode leaves
-    free (step.split_ctas(); 8-bit cache: as the dense CTAs finish). Neither
+    free (step.split_ctas()). Neither
     path reads the other's output, and the two decode calls have their own
     workspaces. `quest` and `dense` override the Quest-path and the dense
     call in either mode."""
@@ -632,13 +634,12 @@ def config_of(w, args, world: int) -> dict:
         "context_lens_max": int(w.context_lens.max()), "pool_blocks": w.NB,
         "kv_pool_bytes": int(2 * w.key_cache.nbytes // (2 if fp8 else 1)),
         "step": ("quest_reshape_and_cache{0} (ReshapeAndCache + metadata update), then on a second "
-                 "stream quest_select_topk{0} + quest_sparse_decode{0}_budget beside {1}; {2}; "
+                 "stream quest_select_topk{0} + quest_sparse_decode{0}_budget beside pa_decode{0}{1}; {2}; "
                  "--serial: quest_decode{0} then pa_decode{0}").format(
                      "" if args.kv == "bf16" else "_" + args.kv,
-                     "pa_decode_budget" if args.kv == "bf16" and args.qlen == 1 else "pa_decode" +
-                     ("" if args.kv == "bf16" else "_" + args.kv),
+                     "_budget" if args.qlen == 1 else "",
                      "the SMs split between the two decode calls by their KV token shares (split_ctas)"
-                     if args.kv == "bf16" and args.qlen == 1 else "the sparse call on at most half the SMs"),
+                     if args.qlen == 1 else "the sparse call on at most half the SMs"),
         "l2": "inputs resident; L2 flushed before every timed sample",
         "parallelism": f"replicas x{world}",
     }

@@ -474,6 +474,15 @@ PA_API int pa_decode_fp8(pa_bf16 *out, const pa_bf16 *query,
                   int head_dim, int block_size, int64_t num_blocks, float scale,
                   void *workspace, size_t workspace_bytes, void *stream);
 
+/* pa_decode_fp8 on at most max_ctas CTAs (as pa_decode_budget). */
+PA_API int pa_decode_fp8_budget(pa_bf16 *out, const pa_bf16 *query,
+                         const pa_e4m3 *key_cache, const pa_e4m3 *value_cache,
+                         const float *k_scale, const float *v_scale,
+                         const int32_t *block_tables, int max_blocks_per_seq,
+                         const int32_t *context_lens, int batch, int num_q_heads, int num_kv_heads,
+                         int head_dim, int block_size, int64_t num_blocks, float scale, int max_ctas,
+                         void *workspace, size_t workspace_bytes, void *stream);
+
 /* Quest sparse attention ([P1] "Quest Sparse Attention") over an 8-bit
  * cache: quest_sparse_decode with K and V decoded as in pa_decode_fp8. */
 PA_API int quest_sparse_decode_fp8(pa_bf16 *out, const pa_bf16 *query,
@@ -581,6 +590,16 @@ PA_API int pa_decode_fp8_block(pa_bf16 *out, const pa_bf16 *query,
                                const int32_t *context_lens, int batch, int num_q_heads,
                                int num_kv_heads, int head_dim, int block_size, int64_t num_blocks,
                                float scale, void *workspace, size_t workspace_bytes, void *stream);
+
+/* pa_decode_fp8_block on at most max_ctas CTAs (as pa_decode_budget). */
+PA_API int pa_decode_fp8_block_budget(pa_bf16 *out, const pa_bf16 *query,
+                               const pa_e4m3 *key_cache, const pa_e4m3 *value_cache,
+                               const float *k_bscale, const float *v_bscale,
+                               const int32_t *block_tables, int max_blocks_per_seq,
+                               const int32_t *context_lens, int batch, int num_q_heads,
+                               int num_kv_heads, int head_dim, int block_size, int64_t num_blocks,
+                               float scale, int max_ctas, void *workspace, size_t workspace_bytes,
+                               void *stream);
 
 /* quest_sparse_decode_fp8_budget on a cache with per-block scales
  * (max_ctas 0: the default). */

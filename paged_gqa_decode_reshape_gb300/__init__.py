@@ -39,10 +39,11 @@ __all__ = [
     "quest_decode_workspace_size", "quest_decode", "quest_decode_fp8",
     "pa_decode_multi_workspace_size", "pa_decode_multi",
     "pa_reshape_and_cache_fp8", "quest_update_meta_fp8", "quest_reshape_and_cache_fp8",
-    "quest_rebuild_meta_fp8", "quest_select_topk_fp8", "pa_decode_fp8", "quest_sparse_decode_fp8",
+    "quest_rebuild_meta_fp8", "quest_select_topk_fp8", "pa_decode_fp8", "pa_decode_fp8_budget",
+    "quest_sparse_decode_fp8",
     "quest_sparse_decode_fp8_budget",
     "pa_reshape_and_cache_fp8_block", "quest_reshape_and_cache_fp8_block", "quest_select_topk_fp8_block",
-    "pa_decode_fp8_block", "quest_sparse_decode_fp8_block", "quest_decode_fp8_block",
+    "pa_decode_fp8_block", "pa_decode_fp8_block_budget", "quest_sparse_decode_fp8_block", "quest_decode_fp8_block",
     "pa_reshape_and_decode", "quest_reshape_and_decode",
     "pa_workspace_status", "pa_check_metadata", "Workspace",
 ]
@@ -155,6 +156,11 @@ def load_library(path: Optional[str] = None):
         L.quest_select_topk_fp8_block.restype = i32
         L.pa_decode_fp8_block.argtypes = L.pa_decode_fp8.argtypes
         L.pa_decode_fp8_block.restype = i32
+        L.pa_decode_fp8_budget.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, vp, i32, i32, i32, i32, i32,
+                                           i64, f32, i32, vp, sz, vp]
+        L.pa_decode_fp8_budget.restype = i32
+        L.pa_decode_fp8_block_budget.argtypes = L.pa_decode_fp8_budget.argtypes
+        L.pa_decode_fp8_block_budget.restype = i32
         L.quest_sparse_decode_fp8_block.argtypes = L.quest_sparse_decode_fp8_budget.argtypes
         L.quest_sparse_decode_fp8_block.restype = i32
         L.quest_decode_fp8_block.argtypes = L.quest_decode_fp8.argtypes
@@ -634,6 +640,24 @@ def pa_decode_fp8(out: torch.Tensor, query: torch.Tensor, key_cache: torch.Tenso
     return out
 
 
+def pa_decode_fp8_budget(out: torch.Tensor, query: torch.Tensor, key_cache: torch.Tensor,
+                         value_cache: torch.Tensor, k_scale: torch.Tensor, v_scale: torch.Tensor,
+                         block_tables: torch.Tensor, context_lens: torch.Tensor, scale: float, max_ctas: int,
+                         workspace: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """pa_decode_fp8 on at most max_ctas CTAs (0: one per SM)."""
+    L = load_library()
+    dev, B, Hq, Hkv, D, BS, NB, MBS = _attention_checks_fp8(out, query, key_cache, value_cache,
+                                                            block_tables, context_lens, k_scale, v_scale)
+    need = pa_decode_workspace_size(B, Hq, Hkv, D)
+    ws = workspace if workspace is not None else _default_ws.get(dev, need)
+    _check("pa_decode_fp8_budget",
+           L.pa_decode_fp8_budget(_ptr(out), _ptr(query), _ptr(key_cache), _ptr(value_cache), _ptr(k_scale),
+                                  _ptr(v_scale), _ptr(block_tables), MBS, _ptr(context_lens), B, Hq, Hkv, D,
+                                  BS, NB, float(scale), int(max_ctas), _ptr(ws), ws.numel() * ws.element_size(),
+                                  _stream(dev)))
+    return out
+
+
 def quest_sparse_decode_fp8(out: torch.Tensor, query: torch.Tensor, key_cache: torch.Tensor,
                             value_cache: torch.Tensor, k_scale: torch.Tensor, v_scale: torch.Tensor,
                             block_tables: torch.Tensor, context_lens: torch.Tensor,
@@ -874,6 +898,24 @@ def pa_decode_fp8_block(out: torch.Tensor, query: torch.Tensor, key_cache: torch
            L.pa_decode_fp8_block(_ptr(out), _ptr(query), _ptr(key_cache), _ptr(value_cache), _ptr(k_bscale),
                                  _ptr(v_bscale), _ptr(block_tables), MBS, _ptr(context_lens), B, Hq, Hkv, D,
                                  BS, NB, float(scale), _ptr(ws), ws.numel() * ws.element_size(), _stream(dev)))
+    return out
+
+
+def pa_decode_fp8_block_budget(out: torch.Tensor, query: torch.Tensor, key_cache: torch.Tensor,
+                               value_cache: torch.Tensor, k_bscale: torch.Tensor, v_bscale: torch.Tensor,
+                               block_tables: torch.Tensor, context_lens: torch.Tensor, scale: float,
+                               max_ctas: int, workspace: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """pa_decode_fp8_block on at most max_ctas CTAs (0: one per SM)."""
+    L = load_library()
+    dev, B, Hq, Hkv, D, BS, NB, MBS = _attention_checks_fp8(out, query, key_cache, value_cache, block_tables,
+                                                            context_lens, k_bscale, v_bscale, per_block=True)
+    need = pa_decode_workspace_size(B, Hq, Hkv, D)
+    ws = workspace if workspace is not None else _default_ws.get(dev, need)
+    _check("pa_decode_fp8_block_budget",
+           L.pa_decode_fp8_block_budget(_ptr(out), _ptr(query), _ptr(key_cache), _ptr(value_cache),
+                                        _ptr(k_bscale), _ptr(v_bscale), _ptr(block_tables), MBS,
+                                        _ptr(context_lens), B, Hq, Hkv, D, BS, NB, float(scale), int(max_ctas),
+                                        _ptr(ws), ws.numel() * ws.element_size(), _stream(dev)))
     return out
 
 

@@ -683,6 +683,19 @@ int pa_decode_fp8_block(pa_bf16 *out, const pa_bf16 *query, const pa_e4m3 *key_c
                       nullptr, nullptr, true);
 }
 
+int pa_decode_fp8_block_budget(pa_bf16 *out, const pa_bf16 *query, const pa_e4m3 *key_cache,
+                               const pa_e4m3 *value_cache, const float *k_bscale, const float *v_bscale,
+                               const int32_t *block_tables, int max_blocks_per_seq,
+                               const int32_t *context_lens, int batch, int num_q_heads, int num_kv_heads,
+                               int head_dim, int block_size, int64_t num_blocks, float scale, int max_ctas,
+                               void *workspace, size_t workspace_bytes, void *stream) {
+    if (max_ctas < 0) return PA_ERR_INVALID_ARG;
+    return run_decode(out, query, key_cache, value_cache, block_tables, max_blocks_per_seq, context_lens,
+                      nullptr, 0, batch, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, scale,
+                      workspace, workspace_bytes, stream, false, k_bscale, v_bscale, true, nullptr, 0, max_ctas,
+                      nullptr, nullptr, true);
+}
+
 int quest_sparse_decode_fp8_block(pa_bf16 *out, const pa_bf16 *query, const pa_e4m3 *key_cache,
                                   const pa_e4m3 *value_cache, const float *k_bscale, const float *v_bscale,
                                   const int32_t *block_tables, int max_blocks_per_seq,
@@ -734,6 +747,19 @@ int pa_decode_fp8(pa_bf16 *out, const pa_bf16 *query, const pa_e4m3 *key_cache,
                       context_lens, nullptr, 0, batch, num_q_heads, num_kv_heads, head_dim,
                       block_size, num_blocks, scale, workspace, workspace_bytes, stream, false, k_scale,
                       v_scale, true);
+}
+
+int pa_decode_fp8_budget(pa_bf16 *out, const pa_bf16 *query, const pa_e4m3 *key_cache,
+                         const pa_e4m3 *value_cache, const float *k_scale, const float *v_scale,
+                         const int32_t *block_tables, int max_blocks_per_seq, const int32_t *context_lens,
+                         int batch, int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                         int64_t num_blocks, float scale, int max_ctas, void *workspace,
+                         size_t workspace_bytes, void *stream) {
+    if (max_ctas < 0) return PA_ERR_INVALID_ARG;
+    return run_decode(out, query, key_cache, value_cache, block_tables, max_blocks_per_seq,
+                      context_lens, nullptr, 0, batch, num_q_heads, num_kv_heads, head_dim,
+                      block_size, num_blocks, scale, workspace, workspace_bytes, stream, false, k_scale,
+                      v_scale, true, nullptr, 0, max_ctas);
 }
 
 int quest_sparse_decode_fp8(pa_bf16 *out, const pa_bf16 *query, const pa_e4m3 *key_cache,

@@ -64,3 +64,33 @@ def test_a_budget_of_every_sm_is_pa_decode(case):
         out = torch.full_like(dev.out, float("nan"))
         pg.pa_decode_budget(out, dev.q, dev.kc, dev.vc, dev.bt, dev.ctx, w.scale, budget, workspace=dev.ws)
         assert torch.equal(out.view(torch.int16), ref.view(torch.int16)), f"budget {budget}"
+
+
+@pytest.mark.parametrize("max_ctas", [1, 37, 0])
+def test_fp8_dense_budget_matches_the_oracle(max_ctas):
+    """pa_decode_fp8_budget and pa_decode_fp8_block_budget (two-block ring
+    items) against the oracle, and equal to the calls without a budget when
+    the budget is 0."""
+    import paged_gqa_decode_reshape_gb300 as pg
+    import oracle
+    from tests.test_gpu_fp8 import Fp8Case
+    from tests.test_gpu_fp8_block import BlockCase
+    w = workloads.make("quest_8k", batch=4, ctx_scale=0.05, topk=6)
+    c = Fp8Case(w)
+    c.write_step()  # the step's tokens (their slots hold poison until written)
+    out = torch.full_like(c.out, float("nan"))
+    pg.pa_decode_fp8_budget(out, c.q, c.kc, c.vc, c.ks, c.vs, c.bt, c.ctx, w.scale, max_ctas, workspace=c.ws)
+    want = oracle.attention_fp8(w.q, c.okc, c.ovc, c.ks_h, c.vs_h, w.block_tables, w.context_lens, w.scale)
+    assert_close_attention(to_host_f64(out), want, f"fp8 budget {max_ctas}")
+    if max_ctas == 0:
+        ref = torch.full_like(c.out, float("nan"))
+        pg.pa_decode_fp8(ref, c.q, c.kc, c.vc, c.ks, c.vs, c.bt, c.ctx, w.scale, workspace=c.ws)
+        assert torch.equal(out.view(torch.int16), ref.view(torch.int16))
+    b = BlockCase(w)
+    b.write_step()
+    outb = torch.full_like(b.out, float("nan"))
+    pg.pa_decode_fp8_block_budget(outb, b.q, b.kc, b.vc, b.ks, b.vs, b.bt, b.ctx, w.scale, max_ctas,
+                                  workspace=b.ws)
+    wantb = oracle.attention_fp8(w.q, b.okc, b.ovc, b.oks, b.ovs, w.block_tables, w.context_lens, w.scale)
+    assert_close_attention(to_host_f64(outb), wantb, f"fp8 block budget {max_ctas}")
+    assert pg.pa_workspace_status(c.ws) == 0 and pg.pa_workspace_status(b.ws) == 0
