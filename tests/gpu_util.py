@@ -2,7 +2,10 @@
 CUDA path through the C ABI binding, run the oracle on the same inputs, and
 compare with the tolerances of the method's statement (attention outputs
 within max-abs 1e-2 and mean-abs 1e-3 of the oracle; caches, metadata and
-selections bit-exact)."""
+selections bit-exact). The output is bf16, so the mean-abs bound counts on
+top of the error that rounding the exact result to bf16 already carries:
+about 1e-5 on the benchmark workloads, about 1e-3 on a batch whose rows each
+attend to one token (each output row is then one V row, of magnitude ~1)."""
 
 from __future__ import annotations
 
@@ -12,7 +15,7 @@ import torch
 import oracle
 import paged_gqa_decode_reshape_gb300 as pg
 from tests.selection_check import check_selection
-from workloads import bf16_bits_to_f32
+from workloads import bf16_bits_to_f32, f32_to_bf16_bits
 
 MAX_ABS_TOL = 1e-2
 MEAN_ABS_TOL = 1e-3
@@ -132,10 +135,13 @@ def assert_close_attention(got: np.ndarray, want: np.ndarray, what: str):
     assert np.isfinite(got).all(), f"{what}: non-finite outputs"
     err = np.abs(got - want)
     max_abs, mean_abs = float(err.max()), float(err.mean())
-    print(f"{what}: max_abs={max_abs:.3e} mean_abs={mean_abs:.3e} "
-          f"{'PASS' if max_abs <= MAX_ABS_TOL and mean_abs <= MEAN_ABS_TOL else 'FAIL'}")
+    # the mean-abs error of the exact result rounded to the bf16 output
+    floor = float(np.abs(bf16_bits_to_f32(f32_to_bf16_bits(want.astype(np.float32))) - want).mean())
+    mean_tol = MEAN_ABS_TOL + floor
+    print(f"{what}: max_abs={max_abs:.3e} mean_abs={mean_abs:.3e} (bf16 rounding floor {floor:.1e}) "
+          f"{'PASS' if max_abs <= MAX_ABS_TOL and mean_abs <= mean_tol else 'FAIL'}")
     assert max_abs <= MAX_ABS_TOL, f"{what}: max-abs error {max_abs:.3e} > {MAX_ABS_TOL}"
-    assert mean_abs <= MEAN_ABS_TOL, f"{what}: mean-abs error {mean_abs:.3e} > {MEAN_ABS_TOL}"
+    assert mean_abs <= mean_tol, f"{what}: mean-abs error {mean_abs:.3e} > {MEAN_ABS_TOL} + {floor:.1e}"
 
 
 def sample_rows(w, n: int, seed: int):
