@@ -316,7 +316,10 @@ __device__ __forceinline__ void cta_load_keys(uint32_t *keys, const float *row, 
 // hist: HC * 256 ints of shared memory, HC histogram copies (warp w adds to
 // copy w % HC: the keys of a row crowd into few bins, and copies spread the
 // atomic adds of different warps over different addresses); red: at least
-// 2 * THREADS / 32 + 2 ints.
+// 2 * THREADS / 32 + 3 ints. When the bin holding the topk-th key ends
+// exactly at the topk-th key, the selection is every key from that bin's
+// lowest value up: the passes stop there, with thr one below that value and
+// keq = 0 (the same selection as the full descent).
 template <int THREADS, int HC = 1, typename KeyOf>
 __device__ __forceinline__ void cta_topk_threshold(KeyOf key_of, int n, int topk, int *hist, int *red,
                                                    uint32_t &thr, int &keq) {
@@ -406,6 +409,7 @@ __device__ __forceinline__ void cta_topk_threshold(KeyOf key_of, int n, int topk
                     if (before + cnt[i] >= k) {
                         red[2 * NW] = 255 - 8 * lane - i;
                         red[2 * NW + 1] = before;
+                        red[2 * NW + 2] = before + cnt[i] == k;
                         break;
                     }
                     before += cnt[i];
@@ -417,6 +421,13 @@ __device__ __forceinline__ void cta_topk_threshold(KeyOf key_of, int n, int topk
         mask |= dm << l;
         k -= red[2 * NW + 1];
         h = l - 1;
+        if (red[2 * NW + 2] && prefix != 0u && h >= 0) {
+            // every key of the bin is taken: all keys >= prefix (low bits 0)
+            thr = prefix - 1u;
+            keq = 0;
+            __syncthreads();  // red may be reused by the caller
+            return;
+        }
     }
     thr = prefix;
     keq = k;

@@ -274,15 +274,16 @@ __global__ void __launch_bounds__(kTopkThreads, 4) quest_topk_kernel(
     int32_t *__restrict__ sel, const float *__restrict__ scores, int MBS,
     const int32_t *__restrict__ ctx, int Hkv, int BS, int topk) {
     __shared__ int hist[256];
-    __shared__ int red[2 * kTopkThreads / 32 + 2];
+    __shared__ int red[2 * kTopkThreads / 32 + 3];
     __shared__ uint32_t keys[kTopkSmemKeys];
     pdl_trigger();
-    pdl_wait();
     const int seg = blockIdx.x;
     const int b = seg / Hkv;
     const int tid = threadIdx.x;
+    // the context length is the caller's input: read while the score kernel finishes
     const int c = min(max(__ldg(ctx + b), 0), MBS * BS);
     const int n = (c + BS - 1) / BS;
+    pdl_wait();
     const float *srow = scores + int64_t(seg) * MBS;
     int32_t *out = sel + int64_t(seg) * topk;
     if (n <= topk) {
