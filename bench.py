@@ -86,8 +86,9 @@ def measured_peaks():
 
 def recorded_traffic(kernel: str, workload: str):
     """DRAM bytes per launch from an ncu capture, if it was taken on the
-    current source of the kernel (else None)."""
-    import hashlib
+    current sources of the kernel (else None). `source` names the files the
+    kernel is compiled from, joined by '+'; `source_sha` is the first 16 hex
+    digits of the SHA-256 of their contents in that order."""
     path = os.path.join(HERE, "profiles", "dram_traffic.json")
     if not os.path.exists(path):
         return None
@@ -96,13 +97,23 @@ def recorded_traffic(kernel: str, workload: str):
     ent = rec.get(kernel, {}).get(workload)
     if not ent:
         return None
-    src = os.path.join(HERE, "paged_gqa_decode_reshape_gb300", "csrc", ent["source"])
-    if not os.path.exists(src):
-        return None
-    sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
-    if sha != ent.get("source_sha"):
+    sha = sources_sha(ent["source"])
+    if sha is None or sha != ent.get("source_sha"):
         return None
     return int(ent["dram_bytes_per_launch"])
+
+
+def sources_sha(source: str):
+    """First 16 hex digits of the SHA-256 of the '+'-joined csrc files, in order."""
+    import hashlib
+    h = hashlib.sha256()
+    for name in source.split("+"):
+        src = os.path.join(HERE, "paged_gqa_decode_reshape_gb300", "csrc", name)
+        if not os.path.exists(src):
+            return None
+        with open(src, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
 
 
 class ClockSampler:
