@@ -72,6 +72,15 @@ __global__ void __launch_bounds__(kScoreThreads, 4) quest_score_kernel(
     const int tid = threadIdx.x, lane = tid & 31;
     const int G = Hq / Hkv;
     const int max_tok = MBS * BS;
+    {
+        // L2 prefetch hints (no registers held): the block table and the
+        // queries, a 128-byte line per thread of the grid. L2 is coherent
+        // with the previous kernel's writes, so hints may precede the wait.
+        const int64_t nthr = int64_t(gridDim.x) * kScoreThreads;
+        const int64_t gt = int64_t(blockIdx.x) * kScoreThreads + tid;
+        for (int64_t off = gt * 32; off < int64_t(B) * MBS; off += nthr * 32) prefetch_l2(bt + off);
+        for (int64_t off = gt * 64; off < int64_t(B) * Hq * D; off += nthr * 64) prefetch_l2(q + off);
+    }
     for (int b = tid; b < B; b += kScoreThreads) {
         const int c = min(max(__ldg(ctx + b), 0), max_tok);
         pre[b + 1] = ((c + BS - 1) / BS + kChunk - 1) / kChunk;
@@ -120,6 +129,17 @@ __global__ void __launch_bounds__(kScoreThreads, 4) quest_score_kernel(
         return (lane < kChunk && j < nb) ? __ldg(bt + int64_t(bb) * MBS + j) : -1;
     };
     int ph_first = chunk_phys(b, ch);
+    if (ph_first >= 0 && int64_t(ph_first) < NB) {
+        // the first chunk's metadata rows into L2 while the previous kernel
+        // finishes (lane u: block u's two rows)
+        constexpr int EB = F8 ? 1 : 2;  // bytes per element
+        const int64_t off = (int64_t(ph_first) * Hkv + kvh) * D * EB;
+#pragma unroll
+        for (int x = 0; x < D * EB; x += 128) {
+            prefetch_l2(static_cast<const uint8_t *>(kmin_v) + off + x);
+            prefetch_l2(static_cast<const uint8_t *>(kmax_v) + off + x);
+        }
+    }
     bool first = true;
     pdl_wait();
     int pn_seg = -1;
