@@ -68,3 +68,28 @@ def test_native_arm_without_gpu_fails_loudly():
     assert r.returncode != 0
     assert "needs a CUDA GPU" in r.stderr
     assert _json_lines(r.stdout) == []
+
+
+def test_recorded_traffic_holds_only_for_the_captured_sources(tmp_path, monkeypatch):
+    """The DRAM traffic bench.py reports comes from the record only while the
+    hash of every source file of the kernel matches the capture's."""
+    rec = json.load(open(os.path.join(bench.HERE, "profiles", "dram_traffic.json")))
+    ent = rec["pa_decode"]["quest_8k"]
+    assert ent["source"] == "decode.cu+common.cuh+kernels.h"
+    # the committed record was taken on the committed sources
+    assert bench.recorded_traffic("pa_decode", "quest_8k") == ent["dram_bytes_per_launch"]
+    assert ent["dram_bytes_per_launch"] == ent["dram_bytes_read"] + ent["dram_bytes_write"]
+    # a copy of the tree with one source byte changed: no traffic
+    csrc = tmp_path / "paged_gqa_decode_reshape_gb300" / "csrc"
+    csrc.mkdir(parents=True)
+    (tmp_path / "profiles").mkdir()
+    (tmp_path / "profiles" / "dram_traffic.json").write_text(json.dumps(rec))
+    for name in ent["source"].split("+"):
+        src = os.path.join(bench.HERE, "paged_gqa_decode_reshape_gb300", "csrc", name)
+        (csrc / name).write_bytes(open(src, "rb").read())
+    monkeypatch.setattr(bench, "HERE", str(tmp_path))
+    assert bench.recorded_traffic("pa_decode", "quest_8k") == ent["dram_bytes_per_launch"]
+    with open(csrc / "common.cuh", "ab") as f:
+        f.write(b"\n")
+    assert bench.recorded_traffic("pa_decode", "quest_8k") is None
+    assert bench.recorded_traffic("pa_decode", "no_such_workload") is None
